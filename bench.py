@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""RankMixer block forward + backward throughput on GB300.
+
+One step = rmx_forward + rmx_backward of the whole block over one batch
+(B=1024, T=64, D=1280, H=2560, bf16 storage by default), inputs resident in
+HBM.  Prints one JSON line (rank 0).  Timing follows the page's protocol
+("Subgraph-fusion-based Mega-kernel Generation", section "Exact timing
+behavior"): warm-up, an L2 flush and a barrier before every measured step
+(outside the timed region), CUDA events around the complete forward+backward.
+
+Multi-GPU (--gpus N under torchrun): N independent replicas, one per GPU, each
+on its own batch (the block needs no exchange at EP=1); value = all rows
+processed / the slowest rank's time.
+
+--impl reference times the float64 CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RankMixer fwd+bwd rows/s (B*T) at B1024/T64/D1280/H2560; % of roofline"
+WORKLOAD_NAMES = {
+    "c3": "RankMixer production block B=1024 T=64 D=1280 H=2560 bf16",
+    "c4": "RankMixer ragged block B=1000 T=40 D=1200 H=3600 fp16",
+    "c2": "RankMixer mid block B=256 T=32 D=512 H=1536 bf16",
+    "c1": "RankMixer small block B=64 T=16 D=256 H=512 fp32",
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--samples", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--reps", type=int, default=1, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- accounting
+
+def flops_per_step(s) -> float:
+    """18 * B*T*D*H: the four forward contractions (2 x 2*B*T*D*2H ... ) and
+    the eight backward ones (dgrad + wgrad of each)."""
+    return 18.0 * s.B * s.T * s.D * s.H
+
+
+def min_bytes_per_step(s) -> float:
+    """Bytes the API forces: x, dy read; y, dx written; parameters read in the
+    forward and the backward; parameter gradients written once."""
+    e = 4 if s.dtype == "f32" else 2
+    act = 4 * s.B * s.T * s.D * e
+    params = (3 * s.T * s.D * s.H + s.T * 2 * s.H + s.T * s.D + 6 * s.D + 4 * s.H) * e
+    return act + 3 * params
+
+
+def gemm_flops_per_launch(s) -> dict:
+    BTDH = s.B * s.T * s.D * s.H
+    return {
+        "gemm1_fwd": 4.0 * BTDH, "gemm2_fwd": 2.0 * BTDH,
+        "gemm2_dgrad": 2.0 * BTDH, "gemm2_wgrad": 2.0 * BTDH,
+        "gemm1_dgrad": 4.0 * BTDH, "gemm1_wgrad": 4.0 * BTDH,
+    }
+
+
+def row_bytes_per_launch(s) -> dict:
+    """Algorithmic HBM bytes of each row pass (reads + writes of full tensors)."""
+    e = 4 if s.dtype == "f32" else 2
+    N = s.B * s.T
+    BTD, BTH = N * s.D * e, N * s.H * e
+    return {
+        "ln0_mix_ln1_fwd": 2 * BTD,                 # x in, out1 out
+        "gate_fwd": 2 * BTH + BTH,                  # Z in, hidden out
+        "ln2_fwd": 2 * BTD,                         # s2 in, y out
+        "ln2_bwd": 3 * BTD,                         # dy, s2 in, ds2 out
+        "gate_bwd": BTH + 2 * BTH + 2 * BTH,        # dh, Z in, dZ out
+        "ln1_mix_ln0_bwd": 3 * BTD,                 # x, dout1 in, dx out
+    }
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("ffn_block_gb300/csrc/gemm_tc.cu", "ffn_block_gb300/csrc/common.cuh",
+                "ffn_block_gb300/csrc/rows.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+def gpu_selector(dev: int) -> str:
+    """nvidia-smi -i argument for torch device `dev` (by UUID when known)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        if u:
+            return u if u.startswith("GPU-") else f"GPU-{u}"
+    except Exception:
+        pass
+    return str(dev)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+
+def oracle_worker(args) -> None:
+    """Times the float64 oracle on `--samples` samples of the workload (one
+    forward + backward per repetition) and prints a JSON line."""
+    import numpy as np
+    from ffn_block_gb300 import inputs as I
+    from oracle import rmx_oracle as O
+
+    shape = I.shape_of(args.config)
+    sub = I.Shape(B=args.samples, T=shape.T, D=shape.D, H=shape.H, dtype=shape.dtype)
+    arrays = I.to_float64(I.make_inputs(sub))
+    p = {k: arrays[k] for k in I.PARAM_NAMES}
+    times = []
+    for _ in range(args.reps):
+        t0 = time.perf_counter()
+        O.forward_backward(arrays["x"], arrays["dy"], p)
+        times.append(time.perf_counter() - t0)
+    print(json.dumps({"samples": args.samples, "rows": args.samples * shape.T, "times": times,
+                      "numpy": np.__version__}))
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_oracle(config: str, samples: int, reps: int) -> dict:
+    cores = host_cores()
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-worker", "--config", config,
+           "--samples", str(samples), "--reps", str(reps)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = cores
+    return out
+
+
+def cpu_baseline(config: str, target_s: float) -> dict:
+    """Oracle rows/s on a bounded sample sized to take about target_s."""
+    probe = run_oracle(config, 1, 1)
+    per_sample = max(probe["times"][0], 1e-3)
+    samples = int(max(1, min(64, target_s / per_sample)))
+    res = run_oracle(config, samples, 1)
+    t = res["times"][0]
+    rows = res["rows"]
+    return {"value": rows / t, "unit": "rows/s", "cores": res["cores"], "kind": "oracle",
+            "sample": f"{samples} of the workload's samples ({rows} rows), one float64 forward+backward "
+                      f"in numpy, {t:.2f} s; BLAS threads = cores"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def dist_setup(n_gpus: int):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, local, ws
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, ws: int) -> float:
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(rows_per_rank: int, ms_max: float, ws: int) -> float:
+    """Whole-job throughput: rows of every rank over the slowest rank's time."""
+    return rows_per_rank * ws / (ms_max / 1e3)
+
+
+def run_ours(args) -> dict | None:
+    import numpy as np
+    import torch
+
+    from ffn_block_gb300 import binding as B
+    from ffn_block_gb300 import inputs as I
+    from ffn_block_gb300.device import RankMixerDevice
+
+    rank, local, ws = dist_setup(args.gpus)
+    shape = I.shape_of(args.config)
+    arrays = I.make_inputs(shape, seed=I.DEFAULT_SEED + rank)
+    blk = RankMixerDevice(shape, arrays, device=f"cuda:{torch.cuda.current_device()}")
+    del arrays
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+
+    for _ in range(max(args.warmup, 0)):
+        blk.step(stream)
+    torch.cuda.synchronize()
+    B.check(B.rmx_check(stream), "warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_selector(torch.cuda.current_device()))
+    sampler.start()
+    time.sleep(0.3)
+    B.rmx_profile_read()
+    launches0 = B.rmx_launch_count()
+    B.rmx_profile_enable(True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                                    # L2 flush, outside the events
+        starts[i].record(stream)
+        blk.step(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - wall0
+    B.rmx_profile_enable(False)
+    launches = B.rmx_launch_count() - launches0
+    clocks = sampler.stop()
+    B.check(B.rmx_check(stream), "timed region")
+    prof = B.rmx_profile_read()
+    samples = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = float(np.mean(samples))
+    ms_max = reduce_max(ms, ws)
+    rows = shape.B * shape.T
+    value = aggregate(rows, ms_max, ws)
+
+    # ---- end to end through the host-memory entry point
+    e2e = None
+    if not args.no_e2e:
+        hx = blk.x.cpu().pin_memory()
+        hdy = blk.dy.cpu().pin_memory()
+        hy = torch.empty_like(hx).pin_memory()
+        hdx = torch.empty_like(hx).pin_memory()
+        staging = [torch.empty_like(blk.x) for _ in range(4)]
+        dev = B.rmx_device_io(*[t.data_ptr() for t in staging])
+        host = B.rmx_host_io(hx.data_ptr(), hdy.data_ptr(), hy.data_ptr(), hdx.data_ptr())
+
+        def host_step():
+            B.check(B.rmx_step_host(blk.cfg, host, dev, blk.c_params, blk.c_grads, blk.saved,
+                                    blk.saved_bytes, blk.ws, blk.ws_bytes, stream), "rmx_step_host")
+
+        for _ in range(max(args.warmup, 1)):
+            host_step()
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(ws)
+        for i in range(args.steps):
+            flush.zero_()
+            es[i].record(stream)
+            host_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize()
+        B.check(B.rmx_check(stream), "e2e")
+        e_ms = reduce_max(float(np.mean([a.elapsed_time(b) for a, b in zip(es, ee)])), ws)
+        nbytes = hx.numel() * hx.element_size()
+        e2e = {"value": aggregate(rows, e_ms, ws), "unit": "rows/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes}
+
+    if rank != 0:
+        return None
+
+    # ---- roofline of the dominant kernel and of the whole step
+    peaks, peak_src = load_peaks()
+    kernels = {k: {"launches": n, "ms_total": t, "ms_per_launch": t / max(n, 1)} for k, (n, t) in prof.items()}
+    total_ms = sum(v["ms_total"] for v in kernels.values()) or 1.0
+    for v in kernels.values():
+        v["share"] = v["ms_total"] / total_ms
+    dom = max(kernels, key=lambda k: kernels[k]["ms_total"]) if kernels else None
+    gflops, rbytes = gemm_flops_per_launch(shape), row_bytes_per_launch(shape)
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    roofline = None
+    if dom is not None:
+        per = kernels[dom]["ms_per_launch"] / 1e3
+        if dom in gflops:
+            ach = gflops[dom] / per / 1e12
+            peak = sustained if shape.dtype != "f32" else None
+            roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                        "frac": (ach / peak) if peak else None,
+                        "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step)",
+                        "traffic": profiled_traffic(dom, args.config)}
+        else:
+            ach = rbytes.get(dom, 0.0) / per / 1e9
+            roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs",
+                        "traffic": profiled_traffic(dom, args.config)}
+    for k, v in kernels.items():
+        per = v["ms_per_launch"] / 1e3
+        if k in gflops and shape.dtype != "f32":
+            v["tflops"] = gflops[k] / per / 1e12
+            v["frac_of_peak"] = v["tflops"] / sustained
+        elif k in rbytes:
+            v["gbs"] = rbytes[k] / per / 1e9
+            v["frac_of_peak"] = v["gbs"] / peaks["hbm_gbs"]
+    t_compute = flops_per_step(shape) / (sustained * 1e12) if shape.dtype != "f32" else None
+    t_mem = min_bytes_per_step(shape) / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_compute or 0.0, t_mem)
+    step_roofline = {"bound": "tensor" if (t_compute or 0) >= t_mem else "hbm", "t_ms": t_roof * 1e3,
+                     "flops": flops_per_step(shape), "min_bytes": min_bytes_per_step(shape),
+                     "frac": (t_roof * 1e3) / ms, "peaks": f"{peak_src}: bf16_tflops_sustained={sustained}, "
+                                                            f"hbm_gbs={peaks['hbm_gbs']}"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "f16": "f16"}[shape.dtype],
+        "data": "synthetic (seeded he-uniform weights, standard-normal x and dy)",
+        "config": {"workload": WORKLOAD_NAMES.get(args.config, args.config), "B": shape.B, "T": shape.T,
+                   "D": shape.D, "H": shape.H, "storage": shape.dtype, "parallelism": f"replicas x{ws}",
+                   "l2": "flushed before every step (outside the timed region)"},
+        "step_roofline": step_roofline,
+        "roofline": roofline,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "wall_s": wall,
+        "samples_ms": samples,
+        "kernels": kernels,
+    }
+    return line
+
+
+def run_reference(args) -> dict | None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from ffn_block_gb300 import inputs as I
+    shape = I.shape_of(args.config)
+    probe = run_oracle(args.config, 1, 1)
+    per_sample = max(probe["times"][0], 1e-3)
+    # Keep the whole run within a few minutes: each step is a bounded sample.
+    budget_per_step = max(2.0, 150.0 / max(args.steps + args.warmup, 1))
+    samples = int(max(1, min(16, budget_per_step / per_sample)))
+    res = run_oracle(args.config, samples, args.steps + args.warmup)
+    times = res["times"][args.warmup:] or res["times"]
+    t = sum(times) / len(times)
+    rows = samples * shape.T
+    value = rows / t
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 1,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES.get(args.config, args.config), "B": shape.B, "T": shape.T,
+                   "D": shape.D, "H": shape.H, "storage": shape.dtype},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": res["cores"], "kind": "oracle",
+                         "sample": f"{samples} samples ({rows} rows) of the workload per step"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_worker:
+        oracle_worker(args)
+        return
+    if args.impl == "reference":
+        line = run_reference(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line = run_ours(args)
+    if line is None:
+        return
+    if not args.no_cpu_baseline and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+        try:
+            line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+        except Exception as e:  # report, do not hide the GPU number
+            line["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
+    elif int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        line["cpu_baseline"] = None
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

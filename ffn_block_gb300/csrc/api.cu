@@ -1,0 +1,524 @@
+// C-ABI layer of the RankMixer library: argument checks, the layout of the
+// saved and scratch buffers, and the launch sequences of the forward and
+// backward passes (all on the caller's stream; nothing here allocates device
+// memory or synchronises, except rmx_check and rmx_profile_read).
+//
+// Forward (page "Subgraph-fusion-based Mega-kernel Generation", section
+// "Exact computation"):
+//   1. norm0 -> token mix -> + x -> norm1          -> out1        (row pass)
+//   2. Z = out1[:,t] @ w1[t] + b1[t]                -> Z           (GEMM, bias)
+//   3. hidden = LN_x(U) * silu(LN_gate(G))          -> hidden      (row pass)
+//   4. s2 = hidden[:,t] @ wout[t] + bout[t] + out1  -> s2          (GEMM, bias+residual)
+//   5. y = norm2(s2)                                               (row pass)
+// Backward (chain rule through the same steps, in reverse):
+//   1. ds2 = norm2-backward(dy), partials of dgamma2/dbeta2/dbout
+//   2. dh = ds2[:,t] @ wout[t]^T                                   (GEMM, NT)
+//   3. dwout[t] = hidden[:,t]^T @ ds2[:,t]                         (GEMM, TN)
+//   4. dZ = gate/inner-LN backward(dh), partials of their params and db1
+//   5. dout1 = dZ[:,t] @ w1[t]^T + ds2                             (GEMM, NT, residual)
+//   6. dw1[t] = out1[:,t]^T @ dZ[:,t]                              (GEMM, TN)
+//   7. dx = norm1/mix/norm0 backward(dout1), partials of their params
+//   8. fixed-order column sums of every partial
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/rmx.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmx {
+
+__device__ unsigned int g_rmx_error_word;
+
+unsigned int* device_error_word() {
+  static unsigned int* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_rmx_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned int*>(p);
+  }
+  return addr[dev];
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline int esize(int dtype) { return dtype == RMX_F32 ? 4 : 2; }
+
+// ------------------------------------------------------------------ layouts
+struct Layout {
+  // saved (filled by the forward)
+  size_t out1, Z, hidden, s2, stats, saved_total;
+  // backward scratch
+  size_t ds2, dh, dZ, dout1, ds1, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
+  RowArgs ra;
+};
+
+bool config_ok(const rmx_config* c) {
+  if (!c) return false;
+  if (c->B < 0 || c->T < 1 || c->D < 1 || c->H < 1) return false;
+  if (c->D % c->T) return false;
+  if (c->dtype != RMX_F32 && c->dtype != RMX_BF16 && c->dtype != RMX_F16) return false;
+  const long long rows = (long long)c->B * c->T;
+  if (rows > (1ll << 30) || (long long)c->D > (1 << 20) || (long long)c->H > (1 << 20)) return false;
+  return true;
+}
+
+Layout layout_of(const rmx_config& c) {
+  Layout L;
+  const size_t e = esize(c.dtype);
+  const size_t N = (size_t)c.B * c.T, D = c.D, H = c.H;
+  size_t o = 0;
+  L.out1 = o; o = up(o + N * D * e);
+  L.Z = o; o = up(o + N * 2 * H * e);
+  L.hidden = o; o = up(o + N * H * e);
+  L.s2 = o; o = up(o + N * D * e);
+  L.stats = o; o = up(o + 10 * N * sizeof(float));
+  L.saved_total = o;
+
+  L.ra.B = c.B;
+  L.ra.T = c.T;
+  L.ra.D = c.D;
+  L.ra.H = c.H;
+  L.ra.dtype = c.dtype;
+  int nb = (c.B + 15) / 16;
+  nb = nb < 1 ? 1 : (nb > 64 ? 64 : nb);
+  L.ra.nb = nb;
+  L.ra.nbblk = c.B > 0 ? (c.B + nb - 1) / nb : 0;
+  const size_t P = (size_t)L.ra.nbblk * c.T;
+
+  o = 0;
+  L.ds2 = o; o = up(o + N * D * e);
+  L.dh = o; o = up(o + N * H * e);
+  L.dZ = o; o = up(o + N * 2 * H * e);
+  L.dout1 = o; o = up(o + N * D * e);
+  L.ds1 = o; o = up(o + N * D * sizeof(float));
+  L.pg2 = o; o = up(o + P * D * sizeof(float));
+  L.pb2 = o; o = up(o + P * D * sizeof(float));
+  L.pbo = o; o = up(o + P * D * sizeof(float));
+  L.pwx = o; o = up(o + P * H * sizeof(float));
+  L.pbx = o; o = up(o + P * H * sizeof(float));
+  L.pwg = o; o = up(o + P * H * sizeof(float));
+  L.pbg = o; o = up(o + P * H * sizeof(float));
+  L.pb1 = o; o = up(o + P * 2 * H * sizeof(float));
+  L.pg0 = o; o = up(o + (size_t)c.B * D * sizeof(float));
+  L.pb0 = o; o = up(o + (size_t)c.B * D * sizeof(float));
+  L.pg1 = o; o = up(o + (size_t)c.B * D * sizeof(float));
+  L.pbe1 = o; o = up(o + (size_t)c.B * D * sizeof(float));
+  L.ws_total = o;
+  return L;
+}
+
+// What the kernels can do (beyond what makes a valid block).
+rmx_status kernels_support(const rmx_config& c) {
+  const int V = 16 / esize(c.dtype);
+  if (c.D % V || c.H % V) return RMX_ERR_UNSUPPORTED;  // rows must be whole 16-byte vectors
+  if (c.D / V > kRowThreadsMax || c.H / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
+  if ((c.D + 31) / 32 > 40) return RMX_ERR_UNSUPPORTED;  // norm0/norm1: 40 values per lane
+  if ((c.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // norm2: 10 vectors per lane
+  return RMX_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rmx_status check_params(const rmx_params* p) {
+  if (!p) return RMX_ERR_INVALID_ARG;
+  const void* v[] = {p->w1, p->b1, p->wout, p->bout, p->gamma0, p->beta0, p->gamma1,
+                     p->beta1, p->gamma2, p->beta2, p->lnx_w, p->lnx_b, p->lng_w, p->lng_b};
+  for (const void* q : v) {
+    if (!q) return RMX_ERR_INVALID_ARG;
+    if (!aligned16(q)) return RMX_ERR_ALIGNMENT;
+  }
+  return RMX_OK;
+}
+
+rmx_status check_grads(const rmx_grads* g) {
+  if (!g) return RMX_ERR_INVALID_ARG;
+  void* v[] = {g->w1, g->b1, g->wout, g->bout, g->gamma0, g->beta0, g->gamma1,
+               g->beta1, g->gamma2, g->beta2, g->lnx_w, g->lnx_b, g->lng_w, g->lng_b};
+  for (void* q : v) {
+    if (!q) return RMX_ERR_INVALID_ARG;
+    if (!aligned16(q)) return RMX_ERR_ALIGNMENT;
+  }
+  return RMX_OK;
+}
+
+rmx_status check_ptr(const void* p) {
+  if (!p) return RMX_ERR_INVALID_ARG;
+  if (!aligned16(p)) return RMX_ERR_ALIGNMENT;
+  return RMX_OK;
+}
+
+// ------------------------------------------------------------------ instrumentation
+std::atomic<long long> g_launches{0};
+std::atomic<bool> g_prof{false};
+std::mutex g_mu;
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t pool_event() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one kernel launch: counts it and, when profiling is on, records
+// events around it on its stream.
+class Launch {
+ public:
+  Launch(const char* name, cudaStream_t st) : name_(name), st_(st) {
+    if (g_prof.load()) {
+      a_ = pool_event();
+      if (a_) cudaEventRecord(a_, st_);
+    }
+  }
+  rmx_status done(cudaError_t e) {
+    g_launches.fetch_add(1);
+    if (a_) {
+      cudaEvent_t b = pool_event();
+      if (b) {
+        cudaEventRecord(b, st_);
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_recs.push_back({name_, a_, b});
+      }
+    }
+    return e == cudaSuccess ? RMX_OK : RMX_ERR_CUDA;
+  }
+
+ private:
+  const char* name_;
+  cudaStream_t st_;
+  cudaEvent_t a_ = nullptr;
+};
+
+#define RMX_TRY(expr)                  \
+  do {                                 \
+    rmx_status s_ = (expr);            \
+    if (s_ != RMX_OK) return s_;       \
+  } while (0)
+
+rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
+  Launch l(name, st);
+  cudaError_t e;
+  if (d.dtype != RMX_F32 && gemm_tc_supported(d))
+    e = gemm_tc_launch(d, device_error_word(), st);
+  else
+    e = gemm_simt_launch(d, st);
+  return l.done(e);
+}
+
+inline char* at(void* base, size_t off) { return static_cast<char*>(base) + off; }
+inline const char* at(const void* base, size_t off) { return static_cast<const char*>(base) + off; }
+
+struct Stats {
+  float *mu0, *r0, *mu1, *r1, *mu2, *r2, *muU, *rU, *muG, *rG;
+};
+Stats stats_of(const void* saved, const Layout& L, size_t N) {
+  float* s = reinterpret_cast<float*>(const_cast<char*>(at(saved, L.stats)));
+  Stats st;
+  st.mu0 = s;
+  st.r0 = s + N;
+  st.mu1 = s + 2 * N;
+  st.r1 = s + 3 * N;
+  st.mu2 = s + 4 * N;
+  st.r2 = s + 5 * N;
+  st.muU = s + 6 * N;
+  st.rU = s + 7 * N;
+  st.muG = s + 8 * N;
+  st.rG = s + 9 * N;
+  return st;
+}
+
+rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p, void* saved, void* y,
+                        cudaStream_t st) {
+  const Layout L = layout_of(c);
+  const size_t N = (size_t)c.B * c.T;
+  void* out1 = at(saved, L.out1);
+  void* Z = at(saved, L.Z);
+  void* hidden = at(saved, L.hidden);
+  void* s2 = at(saved, L.s2);
+  Stats S = stats_of(saved, L, N);
+  {
+    Launch l("ln0_mix_ln1_fwd", st);
+    RMX_TRY(l.done(launch_ln0_mix_ln1_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, out1, S.mu0, S.r0,
+                                          S.mu1, S.r1, st)));
+  }
+  {
+    GemmDesc d{GEMM_FWD, EPI_BIAS, c.dtype, c.B, 2 * c.H, c.D, c.T, out1, p.w1, Z, p.b1, nullptr};
+    RMX_TRY(run_gemm("gemm1_fwd", d, st));
+  }
+  {
+    Launch l("gate_fwd", st);
+    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b, hidden, S.muU, S.rU, S.muG,
+                                   S.rG, st)));
+  }
+  {
+    GemmDesc d{GEMM_FWD, EPI_BIAS_RESID, c.dtype, c.B, c.D, c.H, c.T, hidden, p.wout, s2, p.bout, out1};
+    RMX_TRY(run_gemm("gemm2_fwd", d, st));
+  }
+  {
+    Launch l("ln2_fwd", st);
+    RMX_TRY(l.done(launch_ln_rows_fwd(L.ra, s2, p.gamma2, p.beta2, y, S.mu2, S.r2, st)));
+  }
+  return RMX_OK;
+}
+
+rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, const void* saved,
+                         const rmx_params& p, void* dx, const rmx_grads& g, void* ws, cudaStream_t st) {
+  const Layout L = layout_of(c);
+  const size_t N = (size_t)c.B * c.T;
+  const void* out1 = at(saved, L.out1);
+  const void* Z = at(saved, L.Z);
+  const void* hidden = at(saved, L.hidden);
+  const void* s2 = at(saved, L.s2);
+  Stats S = stats_of(saved, L, N);
+  void* ds2 = at(ws, L.ds2);
+  void* dh = at(ws, L.dh);
+  void* dZ = at(ws, L.dZ);
+  void* dout1 = at(ws, L.dout1);
+  float* ds1 = reinterpret_cast<float*>(at(ws, L.ds1));
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(at(ws, off)); };
+
+  {
+    Launch l("ln2_bwd", st);
+    RMX_TRY(l.done(launch_ln2_bwd(L.ra, dy, s2, S.mu2, S.r2, p.gamma2, ds2, F(L.pg2), F(L.pb2), F(L.pbo), st)));
+  }
+  {
+    GemmDesc d{GEMM_DGRAD, EPI_STORE, c.dtype, c.B, c.H, c.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
+    RMX_TRY(run_gemm("gemm2_dgrad", d, st));
+  }
+  {
+    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
+    RMX_TRY(run_gemm("gemm2_wgrad", d, st));
+  }
+  {
+    Launch l("gate_bwd", st);
+    RMX_TRY(l.done(launch_gate_bwd(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
+                                   dZ, F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1), st)));
+  }
+  {
+    GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
+    RMX_TRY(run_gemm("gemm1_dgrad", d, st));
+  }
+  {
+    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
+    RMX_TRY(run_gemm("gemm1_wgrad", d, st));
+  }
+  {
+    Launch l("ln1_mix_ln0_bwd", st);
+    RMX_TRY(l.done(launch_ln1_mix_ln0_bwd(L.ra, x, dout1, S.mu0, S.r0, S.mu1, S.r1, p.gamma0, p.beta0,
+                                          p.gamma1, ds1, dx, F(L.pg0), F(L.pb0), F(L.pg1), F(L.pbe1), st)));
+  }
+  {
+    const int P = L.ra.nbblk * c.T, Pb = L.ra.nbblk;
+    ColsumJob jobs[12] = {
+        {F(L.pg2), g.gamma2, P, c.D},          {F(L.pb2), g.beta2, P, c.D},
+        {F(L.pbo), g.bout, Pb, c.T * c.D},     {F(L.pwx), g.lnx_w, P, c.H},
+        {F(L.pbx), g.lnx_b, P, c.H},           {F(L.pwg), g.lng_w, P, c.H},
+        {F(L.pbg), g.lng_b, P, c.H},           {F(L.pb1), g.b1, Pb, c.T * 2 * c.H},
+        {F(L.pg1), g.gamma1, c.B, c.D},        {F(L.pbe1), g.beta1, c.B, c.D},
+        {F(L.pg0), g.gamma0, c.B, c.D},        {F(L.pb0), g.beta0, c.B, c.D},
+    };
+    Launch l("colsums", st);
+    cudaError_t e = launch_colsums(jobs, 12, c.dtype, st);
+    RMX_TRY(l.done(e));
+  }
+  return RMX_OK;
+}
+
+rmx_status zero_grads(const rmx_config& c, const rmx_grads& g, cudaStream_t st) {
+  const size_t e = esize(c.dtype), T = c.T, D = c.D, H = c.H;
+  struct {
+    void* p;
+    size_t n;
+  } z[] = {{g.w1, T * D * 2 * H}, {g.b1, T * 2 * H}, {g.wout, T * H * D}, {g.bout, T * D},
+           {g.gamma0, D},         {g.beta0, D},      {g.gamma1, D},       {g.beta1, D},
+           {g.gamma2, D},         {g.beta2, D},      {g.lnx_w, H},        {g.lnx_b, H},
+           {g.lng_w, H},          {g.lng_b, H}};
+  for (auto& q : z)
+    if (cudaMemsetAsync(q.p, 0, q.n * e, st) != cudaSuccess) return RMX_ERR_CUDA;
+  return RMX_OK;
+}
+
+}  // namespace
+}  // namespace rmx
+
+using namespace rmx;
+
+extern "C" {
+
+size_t rmx_saved_bytes(const rmx_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return layout_of(*cfg).saved_total;
+}
+
+size_t rmx_workspace_bytes(const rmx_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return layout_of(*cfg).ws_total;
+}
+
+rmx_status rmx_forward(const rmx_config* cfg, const void* x, const rmx_params* params, void* saved,
+                       size_t saved_bytes, void* y, rmx_stream stream) {
+  if (!config_ok(cfg)) return RMX_ERR_INVALID_ARG;
+  RMX_TRY(check_params(params));
+  if (cfg->B == 0) return RMX_OK;
+  RMX_TRY(check_ptr(x));
+  RMX_TRY(check_ptr(y));
+  RMX_TRY(check_ptr(saved));
+  if (x == y) return RMX_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  if (saved_bytes < L.saved_total) return RMX_ERR_WORKSPACE;
+  RMX_TRY(kernels_support(*cfg));
+  RowArgs ra = L.ra;
+  if (per_sample_smem_bytes(ra) > (size_t)max_dynamic_smem_bytes()) return RMX_ERR_UNSUPPORTED;
+  return forward_impl(*cfg, x, *params, saved, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rmx_status rmx_backward(const rmx_config* cfg, const void* x, const void* dy, const void* saved,
+                        size_t saved_bytes, const rmx_params* params, void* dx, const rmx_grads* grads,
+                        void* ws, size_t ws_bytes, rmx_stream stream) {
+  if (!config_ok(cfg)) return RMX_ERR_INVALID_ARG;
+  RMX_TRY(check_params(params));
+  RMX_TRY(check_grads(grads));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->B == 0) return zero_grads(*cfg, *grads, st);
+  RMX_TRY(check_ptr(x));
+  RMX_TRY(check_ptr(dy));
+  RMX_TRY(check_ptr(saved));
+  RMX_TRY(check_ptr(dx));
+  RMX_TRY(check_ptr(ws));
+  const Layout L = layout_of(*cfg);
+  if (saved_bytes < L.saved_total || ws_bytes < L.ws_total) return RMX_ERR_WORKSPACE;
+  RMX_TRY(kernels_support(*cfg));
+  if (per_sample_smem_bytes(L.ra) > (size_t)max_dynamic_smem_bytes()) return RMX_ERR_UNSUPPORTED;
+  return backward_impl(*cfg, x, dy, saved, *params, dx, *grads, ws, st);
+}
+
+rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host, const rmx_device_io* dev,
+                         const rmx_params* params, const rmx_grads* grads, void* saved, size_t saved_bytes,
+                         void* ws, size_t ws_bytes, rmx_stream stream) {
+  if (!config_ok(cfg) || !host || !dev) return RMX_ERR_INVALID_ARG;
+  if (!host->x || !host->dy || !host->y || !host->dx) return RMX_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)cfg->B * cfg->T * cfg->D * esize(cfg->dtype);
+  if (cfg->B > 0) {
+    RMX_TRY(check_ptr(dev->x));
+    RMX_TRY(check_ptr(dev->dy));
+    if (cudaMemcpyAsync(dev->x, host->x, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return RMX_ERR_CUDA;
+    if (cudaMemcpyAsync(dev->dy, host->dy, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return RMX_ERR_CUDA;
+  }
+  RMX_TRY(rmx_forward(cfg, dev->x, params, saved, saved_bytes, dev->y, stream));
+  RMX_TRY(rmx_backward(cfg, dev->x, dev->dy, saved, saved_bytes, params, dev->dx, grads, ws, ws_bytes, stream));
+  if (cfg->B > 0) {
+    if (cudaMemcpyAsync(host->y, dev->y, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return RMX_ERR_CUDA;
+    if (cudaMemcpyAsync(host->dx, dev->dx, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return RMX_ERR_CUDA;
+  }
+  return RMX_OK;
+}
+
+rmx_status rmx_check(rmx_stream stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMX_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_rmx_error_word, sizeof(v)) != cudaSuccess) return RMX_ERR_CUDA;
+  if (v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_rmx_error_word, &zero, sizeof(zero)) != cudaSuccess) return RMX_ERR_CUDA;
+    return RMX_ERR_TIMEOUT;
+  }
+  return RMX_OK;
+}
+
+const char* rmx_status_str(rmx_status s) {
+  switch (s) {
+    case RMX_OK: return "RMX_OK";
+    case RMX_ERR_INVALID_ARG: return "RMX_ERR_INVALID_ARG";
+    case RMX_ERR_UNSUPPORTED: return "RMX_ERR_UNSUPPORTED";
+    case RMX_ERR_ALIGNMENT: return "RMX_ERR_ALIGNMENT";
+    case RMX_ERR_WORKSPACE: return "RMX_ERR_WORKSPACE";
+    case RMX_ERR_CUDA: return "RMX_ERR_CUDA";
+    case RMX_ERR_TIMEOUT: return "RMX_ERR_TIMEOUT";
+  }
+  return "RMX_ERR_UNKNOWN";
+}
+
+int rmx_version(void) { return 100; }
+
+long long rmx_launch_count(void) { return g_launches.load(); }
+
+rmx_status rmx_profile_enable(int on) {
+  g_prof.store(on != 0);
+  return RMX_OK;
+}
+
+int rmx_profile_read(const char** names, long long* launches, double* total_ms, int cap) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    recs.swap(g_recs);
+  }
+  std::map<std::string, std::pair<long long, double>> agg;
+  std::map<std::string, const char*> keep;
+  std::vector<std::string> order;
+  for (auto& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      std::string k(r.name);
+      if (!agg.count(k)) {
+        order.push_back(k);
+        keep[k] = r.name;
+      }
+      agg[k].first += 1;
+      agg[k].second += ms;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  int n = 0;
+  for (auto& k : order) {
+    if (n < cap && names && launches && total_ms) {
+      names[n] = keep[k];
+      launches[n] = agg[k].first;
+      total_ms[n] = agg[k].second;
+    }
+    ++n;
+  }
+  return n;
+}
+
+rmx_status rmx_test_bounded_wait(int limit_us, rmx_stream stream) {
+  if (limit_us <= 0 || limit_us > 10 * 1000 * 1000) return RMX_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Launch l("bounded_wait_test", st);
+  return l.done(launch_bounded_wait_test(device_error_word(), (unsigned long long)limit_us * 1000ull, st));
+}
+
+rmx_status rmx_test_gemm(int kind, int dtype, int M, int N, int K, int G, const void* A, const void* Bm, void* C,
+                         rmx_stream stream) {
+  if (kind < 0 || kind > 2 || dtype < 0 || dtype > 2) return RMX_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || G <= 0) return RMX_ERR_INVALID_ARG;
+  RMX_TRY(check_ptr(A));
+  RMX_TRY(check_ptr(Bm));
+  RMX_TRY(check_ptr(C));
+  GemmDesc d{kind, EPI_STORE, dtype, M, N, K, G, A, Bm, C, nullptr, nullptr};
+  return run_gemm("test_gemm", d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,144 @@
+// Shared device helpers for the RankMixer kernels: storage types, 16-byte
+// vector access, warp/block reductions, the device error word and bounded
+// waits.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace rmx {
+
+typedef __nv_bfloat16 bf16;
+typedef __half f16;
+
+// Device error word: bit flags set by kernels, read and cleared by rmx_check.
+enum : unsigned int {
+  ERRBIT_WAIT_PRODUCER = 1u << 0,
+  ERRBIT_WAIT_MMA = 1u << 1,
+  ERRBIT_WAIT_EPILOGUE = 1u << 2,
+  ERRBIT_WAIT_DRAIN = 1u << 3,
+  ERRBIT_WAIT_TEST = 1u << 4,
+};
+
+unsigned int* device_error_word();  // host: device address of the error word
+
+// ---------------------------------------------------------------- conversions
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f(f16 v) { return __half2float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ f16 from_f<f16>(float v) { return __float2half_rn(v); }
+
+// Elements of T in one 16-byte vector.
+template <typename T> struct VecN { static constexpr int value = 16 / (int)sizeof(T); };
+
+// Load / store one 16-byte vector of T as floats.  p must be 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float* v) {
+  uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+  for (int i = 0; i < VecN<T>::value; ++i) v[i] = to_f(e[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_vec(T* p, const float* v) {
+  uint4 raw;
+  T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+  for (int i = 0; i < VecN<T>::value; ++i) e[i] = from_f<T>(v[i]);
+  *reinterpret_cast<uint4*>(p) = raw;
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sums NV floats over the whole block.  `red` is shared scratch of at least
+// 2 * 32 * NV floats; `slot` alternates between calls so that one
+// __syncthreads per call suffices.  Every thread gets the same result, summed
+// in a fixed order (deterministic).
+template <int NV>
+__device__ __forceinline__ void block_sum(float* v, float* red, int& slot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = warp_sum(v[i]);
+  float* r = red + slot * 32 * NV;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r[warp * NV + i] = v[i];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += r[w * NV + i];
+    v[i] = s;
+  }
+  slot ^= 1;
+}
+
+// ---------------------------------------------------------------- timing / waits
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits until the phase of `bar` with the given parity has completed, for at
+// most `limit_ns` nanoseconds.  On expiry sets `errbit` in the device error
+// word and `*abort` (shared), and returns false.  Returns false at once if
+// `*abort` is already set.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                  unsigned int* err, unsigned int errbit,
+                                                  volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (((++n) & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicOr(err, errbit);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Default limit for the GEMM pipeline waits: far longer than any tile takes,
+// short enough that a broken pipeline returns instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 2000ull * 1000ull * 1000ull;  // 2 s
+
+}  // namespace rmx

@@ -1,0 +1,530 @@
+// Grouped GEMM on Blackwell tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// Computes the four per-token contractions of the RankMixer block (page
+// "Subgraph-fusion-based Mega-kernel Generation", section "Exact
+// computation": Z[b,t] = out1[b,t] @ w1[t] + b1[t] and out2[b,t] =
+// hidden[b,t] @ wout[t] + bout[t]) and the dgrad / wgrad contractions of
+// their backward, for 16-bit storage (bf16 or fp16) with fp32 accumulation.
+//
+// Design (one CTA per SM, persistent over tiles):
+//   warp 0     TMA producer: loads 128x64 A and 256x64 B tiles into a
+//              4-stage shared-memory ring (128-byte swizzle), signalling
+//              `full` mbarriers with the transaction byte count;
+//   warp 1     allocates 512 TMEM columns and issues tcgen05.mma
+//              (M=128, N=256, K=16) from one thread; each stage is released
+//              back to the producer by tcgen05.commit on its `empty` barrier;
+//              the accumulator alternates between two 256-column TMEM halves
+//              so the epilogue of tile i overlaps the main loop of tile i+1;
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, add
+//              bias / residual in fp32, round to the storage type, store.
+// Operands are addressed through rank-3 tensor maps so that per-token slices
+// of [B,T,X] activations and [T,X,Y] weights need no copies; K-major and
+// MN-major shared-memory layouts cover the NN (forward), NT (dgrad) and TN
+// (wgrad) cases without transposes.  TMA zero-fills out-of-range rows and
+// columns, so ragged M, N and K need no special path.
+//
+// Every mbarrier wait is bounded (common.cuh); on expiry the kernel records
+// an error bit, drains what it has in flight and frees its TMEM.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmx {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, UMMA_K = 16;
+constexpr int A_BYTES = BM * BK * 2;           // 16 KB
+constexpr int B_BYTES = BN * BK * 2;           // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KB
+constexpr int MN_CHUNK_BYTES = BK * 128;       // one 64-wide MN chunk of an MN-major tile
+constexpr int NUM_ACC = 2;
+constexpr int TMEM_COLS = NUM_ACC * BN;        // 512
+constexpr int THREADS = 192;
+constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+constexpr uint64_t kDrainLimitNs = 50ull * 1000ull * 1000ull;
+
+struct Params {
+  int M, N, K, G;
+  int tiles_m, tiles_n, tiles_per_group, num_tiles, num_kb;
+  void* out;
+  long long out_rs, out_gs;
+  const void* bias;
+  long long bias_gs;
+  const void* resid;
+  long long res_rs, res_gs;
+  unsigned int* err;
+  unsigned long long wait_limit_ns;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 or bf16 in, fp32 out).
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns; thread i of the warp gets lane
+// (quarter base + i).  The wait is in the same statement so that no use of
+// the registers can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld_32x32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled tile:
+// start address, leading-dimension byte offset, stride-dimension byte offset
+// (all >> 4), the fixed descriptor version bit (46) and the swizzle mode
+// (bits 61-63: 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A/B type
+// (bits 7-9 / 10-12: 0 = fp16, 1 = bf16), A/B major (bits 15 / 16:
+// 0 = K-major, 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+template <typename T, bool A_MN, bool B_MN>
+__host__ __device__ constexpr uint32_t make_idesc() {
+  constexpr uint32_t ab = std::is_same<T, bf16>::value ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+template <int KIND> struct KindTraits;
+// forward:  A = activation [M,G,K] K-major; B = weight [G,K,N] MN-major
+template <> struct KindTraits<GEMM_FWD> { static constexpr bool A_MN = false, B_MN = true, B_ACT = false; };
+// dgrad:    A = activation [M,G,K] K-major; B = weight [G,N,K] K-major
+template <> struct KindTraits<GEMM_DGRAD> { static constexpr bool A_MN = false, B_MN = false, B_ACT = false; };
+// wgrad:    A = activation [K,G,M] MN-major; B = activation [K,G,N] MN-major
+template <> struct KindTraits<GEMM_WGRAD> { static constexpr bool A_MN = true, B_MN = true, B_ACT = true; };
+
+__device__ __forceinline__ void tile_coords(const Params& p, int tile, int& g, int& m0, int& n0) {
+  g = tile / p.tiles_per_group;
+  const int rem = tile - g * p.tiles_per_group;
+  const int tn = rem / p.tiles_m;
+  const int tm = rem - tn * p.tiles_m;
+  m0 = tm * BM;
+  n0 = tn * BN;
+}
+
+template <typename T, int EPI>
+__device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, int n_base, const float* v) {
+  constexpr int V = VecN<T>::value;
+  T* orow = reinterpret_cast<T*>(p.out) + (size_t)g * p.out_gs + (size_t)m * p.out_rs;
+#pragma unroll
+  for (int c = 0; c < 32; c += V) {
+    const int n = n_base + c;
+    if (n < p.N) {
+      float o[V];
+#pragma unroll
+      for (int e = 0; e < V; ++e) o[e] = v[c + e];
+      if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID) {
+        float bv[V];
+        load_vec(reinterpret_cast<const T*>(p.bias) + (size_t)g * p.bias_gs + n, bv);
+#pragma unroll
+        for (int e = 0; e < V; ++e) o[e] += bv[e];
+      }
+      if (EPI == EPI_RESID || EPI == EPI_BIAS_RESID) {
+        float rv[V];
+        load_vec(reinterpret_cast<const T*>(p.resid) + (size_t)g * p.res_gs + (size_t)m * p.res_rs + n, rv);
+#pragma unroll
+        for (int e = 0; e < V; ++e) o[e] += rv[e];
+      }
+      store_vec(orow + n, o);
+    }
+  }
+}
+
+template <typename T, int KIND, int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using KT = KindTraits<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sA = smem_u32(smem);
+  const uint32_t sB = sA + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + NUM_ACC + a); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 2 * NUM_ACC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < NUM_ACC; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_map(&tmA);
+    prefetch_map(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int g, m0, n0;
+        tile_coords(p, tile, g, m0, n0);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, p.wait_limit_ns, p.err, ERRBIT_WAIT_PRODUCER,
+                                 abort_flag)) {
+            ok = false;
+            break;
+          }
+          // MN-major tiles are loaded as 64-wide chunks; chunks lying wholly
+          // past M or N are skipped (they only feed discarded output rows or
+          // columns), and the expected byte count covers what is requested.
+          const int a_chunks = KT::A_MN ? min(BM / 64, (p.M - m0 + 63) / 64) : 1;
+          const int b_chunks = KT::B_MN ? min(BN / 64, (p.N - n0 + 63) / 64) : 1;
+          const uint32_t bytes = (KT::A_MN ? a_chunks * MN_CHUNK_BYTES : A_BYTES) +
+                                 (KT::B_MN ? b_chunks * MN_CHUNK_BYTES : B_BYTES);
+          mbar_expect_tx(full_bar(s), bytes);
+          const int k0 = kb * BK;
+          const uint32_t a_dst = sA + s * A_BYTES, b_dst = sB + s * B_BYTES;
+          if (!KT::A_MN) {
+            tma_load_3d(a_dst, &tmA, full_bar(s), k0, g, m0);                 // map {K, G, M}
+          } else {
+            for (int c = 0; c < a_chunks; ++c)                                  // map {M, G, K}
+              tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, full_bar(s), m0 + 64 * c, g, k0);
+          }
+          if (!KT::B_MN) {
+            tma_load_3d(b_dst, &tmB, full_bar(s), k0, n0, g);                 // map {K, N, G}
+          } else if (!KT::B_ACT) {
+            for (int c = 0; c < b_chunks; ++c)                                  // map {N, K, G}
+              tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, k0, g);
+          } else {
+            for (int c = 0; c < b_chunks; ++c)                                  // map {N, G, K}
+              tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, g, k0);
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA can exit.
+        const int first = it > STAGES ? it - STAGES : 0;
+        for (int j = first; j < it; ++j) {
+          volatile int no_abort = 0;
+          mbar_wait_bounded(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, kDrainLimitNs, p.err,
+                            ERRBIT_WAIT_DRAIN, &no_abort);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc<T, KT::A_MN, KT::B_MN>();
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++lt) {
+        const int acc = lt & 1;
+        const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait_bounded(tempty_bar(acc), aph ^ 1u, p.wait_limit_ns, p.err, ERRBIT_WAIT_MMA, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(full_bar(s), ph, p.wait_limit_ns, p.err, ERRBIT_WAIT_MMA, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = sA + s * A_BYTES, b_base = sB + s * B_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // K-major: advance 16 elements (32 bytes) inside the swizzle atom;
+            // MN-major: advance 16 rows of 128 bytes.
+            const uint64_t adesc = KT::A_MN ? sw128_desc(a_base + k * 2048, MN_CHUNK_BYTES, 1024)
+                                            : sw128_desc(a_base + k * 32, 16, 1024);
+            const uint64_t bdesc = KT::B_MN ? sw128_desc(b_base + k * 2048, MN_CHUNK_BYTES, 1024)
+                                            : sw128_desc(b_base + k * 32, 16, 1024);
+            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+      }
+      if (!ok) {
+        // Make sure no MMA is still writing TMEM before it is freed.
+        umma_commit(drain_bar);
+        volatile int no_abort = 0;
+        mbar_wait_bounded(drain_bar, 0, kDrainLimitNs, p.err, ERRBIT_WAIT_DRAIN, &no_abort);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
+      int g, m0, n0;
+      tile_coords(p, tile, g, m0, n0);
+      const int acc = lt & 1;
+      const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(tfull_bar(acc), aph, p.wait_limit_ns, p.err, ERRBIT_WAIT_EPILOGUE, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int m = m0 + q * 32 + lane;
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      for (int j0 = 0; j0 < BN; j0 += 32) {
+        if (n0 + j0 >= p.N) break;  // warp-uniform
+        float v[32];
+        tmem_ld_32x32(t_row + (uint32_t)j0, v);
+        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + j0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+__global__ void k_bounded_wait_test(unsigned int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the wait must give up after limit_ns.
+  if (threadIdx.x == 0)
+    mbar_wait_bounded(smem_u32(&bar), 0, limit_ns, err, ERRBIT_WAIT_TEST, (volatile int*)&abort_flag);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Rank-3 tiled map with 128-byte swizzle; dims innermost first, strides in
+// bytes for dims 1 and 2.
+bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+              uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename T, int KIND, int EPI>
+cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+  auto k = k_gemm_tc<T, KIND, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+  k<<<grid, THREADS, SMEM_BYTES, st>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                        cudaStream_t st) {
+  switch (d.kind * 4 + d.epi) {
+    case GEMM_FWD * 4 + EPI_STORE: return launch_tc<T, GEMM_FWD, EPI_STORE>(a, b, p, st);
+    case GEMM_FWD * 4 + EPI_BIAS: return launch_tc<T, GEMM_FWD, EPI_BIAS>(a, b, p, st);
+    case GEMM_FWD * 4 + EPI_BIAS_RESID: return launch_tc<T, GEMM_FWD, EPI_BIAS_RESID>(a, b, p, st);
+    case GEMM_DGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE>(a, b, p, st);
+    case GEMM_DGRAD * 4 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID>(a, b, p, st);
+    case GEMM_WGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE>(a, b, p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (n[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 1;
+  }
+  return n[dev];
+}
+
+bool gemm_tc_supported(const GemmDesc& d) {
+  if (d.dtype != 1 && d.dtype != 2) return false;
+  if (d.M <= 0 || d.N <= 0 || d.K <= 0 || d.G <= 0) return false;
+  // 16-byte row strides for the tensor maps and the vector epilogue.
+  if (d.N % 8 || d.K % 8) return false;
+  if (d.kind == GEMM_WGRAD && d.M % 8) return false;
+  const int ok_epi = (d.kind == GEMM_FWD && (d.epi == EPI_STORE || d.epi == EPI_BIAS || d.epi == EPI_BIAS_RESID)) ||
+                     (d.kind == GEMM_DGRAD && (d.epi == EPI_STORE || d.epi == EPI_RESID)) ||
+                     (d.kind == GEMM_WGRAD && d.epi == EPI_STORE);
+  return ok_epi && encode_fn() != nullptr;
+}
+
+cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st) {
+  if (!gemm_tc_supported(d)) return cudaErrorInvalidValue;
+  const uint64_t e = 2, M = d.M, N = d.N, K = d.K, G = d.G;
+  CUtensorMap ma, mb;
+  bool ok = true;
+  if (d.kind == GEMM_FWD || d.kind == GEMM_DGRAD) {
+    ok &= make_map(&ma, d.A, d.dtype, K, G, M, K * e, G * K * e, BK, 1, BM);          // A [M,G,K]
+    if (d.kind == GEMM_FWD)
+      ok &= make_map(&mb, d.Bm, d.dtype, N, K, G, N * e, K * N * e, 64, BK, 1);      // W [G,K,N]
+    else
+      ok &= make_map(&mb, d.Bm, d.dtype, K, N, G, K * e, N * K * e, BK, BN, 1);      // W [G,N,K]
+  } else {
+    ok &= make_map(&ma, d.A, d.dtype, M, G, K, M * e, G * M * e, 64, 1, BK);          // A [K,G,M]
+    ok &= make_map(&mb, d.Bm, d.dtype, N, G, K, N * e, G * N * e, 64, 1, BK);         // B [K,G,N]
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  Params p;
+  p.M = d.M;
+  p.N = d.N;
+  p.K = d.K;
+  p.G = d.G;
+  p.tiles_m = (d.M + BM - 1) / BM;
+  p.tiles_n = (d.N + BN - 1) / BN;
+  p.tiles_per_group = p.tiles_m * p.tiles_n;
+  p.num_tiles = p.tiles_per_group * d.G;
+  p.num_kb = (d.K + BK - 1) / BK;
+  p.out = d.C;
+  if (d.kind == GEMM_WGRAD) {
+    p.out_rs = d.N;
+    p.out_gs = (long long)d.M * d.N;
+  } else {
+    p.out_rs = (long long)d.G * d.N;
+    p.out_gs = d.N;
+  }
+  p.bias = d.bias;
+  p.bias_gs = d.N;
+  p.resid = d.resid;
+  p.res_rs = p.out_rs;
+  p.res_gs = p.out_gs;
+  p.err = err;
+  p.wait_limit_ns = kWaitLimitNs;
+  if (d.dtype == 1) return dispatch_tc<bf16>(d, ma, mb, p, st);
+  return dispatch_tc<f16>(d, ma, mb, p, st);
+}
+
+cudaError_t launch_bounded_wait_test(unsigned int* err, unsigned long long limit_ns, cudaStream_t st) {
+  k_bounded_wait_test<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace rmx

@@ -1,0 +1,86 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace rmx {
+
+// ------------------------------------------------------------------ row passes
+struct RowArgs {
+  int B, T, D, H, dtype;
+  int nb;      // samples per CTA in the per-token (b-block, t) passes
+  int nbblk;   // ceil(B / nb)
+};
+
+// Forward: LN0 -> token mix -> + x -> LN1.  One CTA per sample.
+cudaError_t launch_ln0_mix_ln1_fwd(const RowArgs& a, const void* x, const void* g0, const void* be0,
+                                   const void* g1, const void* be1, void* out1, float* mu0, float* r0,
+                                   float* mu1, float* r1, cudaStream_t st);
+// Forward: y = LN(s) per row (norm2).
+cudaError_t launch_ln_rows_fwd(const RowArgs& a, const void* s, const void* g, const void* be, void* y,
+                               float* mu, float* rs, cudaStream_t st);
+// Forward: hidden = LN_x(U) * silu(LN_gate(G)) from Z = [U | G].
+cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const void* wx, const void* bx,
+                            const void* wg, const void* bg, void* hidden, float* muU, float* rU,
+                            float* muG, float* rG, cudaStream_t st);
+// Backward of norm2: ds2 plus partial sums for gamma2, beta2, bout.
+cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
+                           const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
+                           float* pbo, cudaStream_t st);
+// Backward of the gate and both inner LNs: dZ plus partial sums.
+cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU,
+                            const float* rU, const float* muG, const float* rG, const void* wx,
+                            const void* bx, const void* wg, const void* bg, void* dZ, float* pwx,
+                            float* pbx, float* pwg, float* pbg, float* pb1, cudaStream_t st);
+// Backward of norm1, the token mix and norm0: dx plus partial sums.
+cudaError_t launch_ln1_mix_ln0_bwd(const RowArgs& a, const void* x, const void* dout1,
+                                   const float* mu0, const float* r0, const float* mu1,
+                                   const float* r1, const void* g0, const void* be0, const void* g1,
+                                   float* ds1, void* dx, float* pg0, float* pb0, float* pg1,
+                                   float* pbe1, cudaStream_t st);
+
+// Deterministic column sums: out[j] = sum_{p<P} part[p*J + j], cast to dtype.
+struct ColsumJob {
+  const float* part;
+  void* out;
+  int P, J;
+};
+constexpr int kMaxColsumJobs = 12;
+cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStream_t st);
+
+// Shared-memory need of the per-sample passes (bytes), and the largest
+// thread count a row pass may use (one thread per 16-byte vector of a row).
+size_t per_sample_smem_bytes(const RowArgs& a);
+constexpr int kRowThreadsMax = 512;
+int max_dynamic_smem_bytes();
+
+// ------------------------------------------------------------------ GEMMs
+enum GemmKind { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
+enum GemmEpi { EPI_STORE = 0, EPI_BIAS = 1, EPI_BIAS_RESID = 2, EPI_RESID = 3 };
+
+// One grouped GEMM over G groups (the tokens t).  Layouts, all row-major:
+//   FWD:   C[m,g,:] = A[m,g,:] @ Bm[g]        A [M,G,K], Bm [G,K,N], C [M,G,N]
+//   DGRAD: C[m,g,:] = A[m,g,:] @ Bm[g]^T      A [M,G,K], Bm [G,N,K], C [M,G,N]
+//   WGRAD: C[g]     = A[:,g,:]^T @ Bm[:,g,:]  A [K,G,M], Bm [K,G,N], C [G,M,N]
+// Epilogue: + bias[g,n] (bias [G,N]) and/or + resid (same layout as C).
+struct GemmDesc {
+  int kind, epi, dtype;
+  int M, N, K, G;
+  const void* A;
+  const void* Bm;
+  void* C;
+  const void* bias;
+  const void* resid;
+};
+
+bool gemm_tc_supported(const GemmDesc& d);
+cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st);
+cudaError_t gemm_simt_launch(const GemmDesc& d, cudaStream_t st);
+
+// Test hook: a kernel that waits on an mbarrier nothing completes.
+cudaError_t launch_bounded_wait_test(unsigned int* err, unsigned long long limit_ns, cudaStream_t st);
+
+int sm_count();
+
+}  // namespace rmx

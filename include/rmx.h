@@ -1,0 +1,173 @@
+/*
+ * rmx.h -- C ABI of the fused RankMixer block (forward + backward) for GB300.
+ *
+ * The operation is the RankMixer block of the page "Subgraph-fusion-based
+ * Mega-kernel Generation", section "Exact computation":
+ *
+ *   out1   = norm1(token_mixer(norm0(x)) + x)          outer LNs: eps 1e-3
+ *   Z[b,t] = out1[b,t] @ w1[t] + b1[t];  (U, G) = split(Z) into halves
+ *   hidden = LN_x(U) * silu(LN_gate(G))                 inner LNs: eps 1e-5
+ *   out2[b,t] = hidden[b,t] @ wout[t] + bout[t]
+ *   y      = norm2(out1 + out2)
+ *
+ * token_mixer: reshape [B,T,D] to [B,T,T,D/T], swap the two T axes, reshape
+ * back.  The backward returns the gradient of sum(dy * y) with respect to x
+ * and to every parameter (section "Workload and interfaces": the runner
+ * differentiates the complete block with a same-shape upstream gradient).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are dense, row-major, in the storage dtype of the config
+ *    (float32, bfloat16 or float16) unless stated otherwise.  Arithmetic,
+ *    statistics and accumulation are float32 on the device.
+ *  - Device pointers are allocated and owned by the caller.  The library never
+ *    allocates device memory and never synchronises a stream, except
+ *    rmx_check() and the *_sync helpers that say so.
+ *  - Every device pointer must be 16-byte aligned.
+ *  - Calls enqueue work on `stream` (NULL = the legacy default stream) and
+ *    return once it is enqueued.  Errors found on the host (arguments, sizes,
+ *    alignment) are returned before anything is enqueued.  A device-side wait
+ *    that gave up (RMX_ERR_TIMEOUT) is reported by rmx_check().
+ *  - Gradients are overwritten, never accumulated (the page's timed loop
+ *    sets gradients to None before every step).
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef RMX_H
+#define RMX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle; identical to cudaStream_t / CUstream. */
+typedef struct CUstream_st* rmx_stream;
+
+typedef enum {
+  RMX_OK = 0,
+  RMX_ERR_INVALID_ARG = 1,   /* bad shape, null pointer, bad dtype           */
+  RMX_ERR_UNSUPPORTED = 2,   /* valid block, but outside what the kernels do */
+  RMX_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned             */
+  RMX_ERR_WORKSPACE = 4,     /* a caller buffer is smaller than required     */
+  RMX_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed            */
+  RMX_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up           */
+} rmx_status;
+
+typedef enum { RMX_F32 = 0, RMX_BF16 = 1, RMX_F16 = 2 } rmx_dtype;
+
+/* Block shape.  x, y, dy, dx are [B,T,D]; H is the FFN width (H = k*D on the
+ * page, k in {2,3}).  Requires B >= 0, T >= 1, D >= 1, H >= 1, D % T == 0.
+ * B == 0 is an empty batch: the forward does nothing and the backward writes
+ * zero gradients. */
+typedef struct {
+  int B, T, D, H;
+  int dtype; /* rmx_dtype */
+} rmx_config;
+
+/* Parameters (device pointers, storage dtype), section "Workload and
+ * interfaces": w1 [T,D,2H], b1 [T,2H], wout [T,H,D], bout [T,D]; the three
+ * outer NezhaLayerNorms' gamma/beta [D]; the inner LayerNorms' weight/bias
+ * [H] (lnx_* = norm_x applied to U, lng_* = norm_gate applied to G). */
+typedef struct {
+  const void *w1, *b1, *wout, *bout;
+  const void *gamma0, *beta0, *gamma1, *beta1, *gamma2, *beta2;
+  const void *lnx_w, *lnx_b, *lng_w, *lng_b;
+} rmx_params;
+
+/* Parameter gradients, same shapes and dtype as rmx_params (device). */
+typedef struct {
+  void *w1, *b1, *wout, *bout;
+  void *gamma0, *beta0, *gamma1, *beta1, *gamma2, *beta2;
+  void *lnx_w, *lnx_b, *lng_w, *lng_b;
+} rmx_grads;
+
+/* Bytes of the `saved` buffer that rmx_forward fills and rmx_backward reads:
+ * out1 [B,T,D], Z [B,T,2H], hidden [B,T,H], s2 = out1 + out2 [B,T,D] in the
+ * storage dtype, and ten float32 row statistics (mean and 1/sqrt(var+eps) of
+ * norm0, norm1, norm2, LN_x, LN_gate) of length B*T.  Returns 0 for an
+ * invalid config. */
+size_t rmx_saved_bytes(const rmx_config* cfg);
+
+/* Bytes of backward scratch (device, caller-owned, contents undefined between
+ * calls).  Returns 0 for an invalid config. */
+size_t rmx_workspace_bytes(const rmx_config* cfg);
+
+/* Forward pass.  x [B,T,D] (device) -> y [B,T,D] (device), filling `saved`
+ * (device, >= rmx_saved_bytes) for the backward.  x and y may not alias. */
+rmx_status rmx_forward(const rmx_config* cfg, const void* x, const rmx_params* params,
+                       void* saved, size_t saved_bytes, void* y, rmx_stream stream);
+
+/* Backward pass for upstream gradient dy [B,T,D] (device).  x must be the
+ * same input buffer, unchanged, that was passed to the matching rmx_forward
+ * (the backward reads it instead of keeping a copy, as autograd keeps a
+ * reference to a LayerNorm input); `saved` is that call's saved buffer and
+ * params the same parameters.  Writes dx [B,T,D] and every gradient in
+ * `grads` (all 14 must be non-null).  ws: scratch of >= rmx_workspace_bytes.
+ * Parameter gradients reduce over the rows that used them: w1, b1, wout,
+ * bout over b for each token t; the LayerNorm gammas/betas/weights/biases
+ * over all B*T rows.  The reductions run in a fixed order, so repeated calls
+ * are bitwise identical. */
+rmx_status rmx_backward(const rmx_config* cfg, const void* x, const void* dy, const void* saved,
+                        size_t saved_bytes, const rmx_params* params, void* dx,
+                        const rmx_grads* grads, void* ws, size_t ws_bytes,
+                        rmx_stream stream);
+
+/* Host-memory staging for rmx_step_host.  Host buffers should be pinned
+ * (page-locked) for the copies to be asynchronous. */
+typedef struct { const void* x; const void* dy; void* y; void* dx; } rmx_host_io;
+typedef struct { void* x; void* dy; void* y; void* dx; } rmx_device_io;
+
+/* One end-to-end step from host memory: copies x and dy host->device into
+ * `dev` (device, [B,T,D] each), runs rmx_forward and rmx_backward, and copies
+ * y and dx device->host.  Parameters and gradients stay on the device.  Uses
+ * one cudaMemcpyAsync per copy on `stream` and returns once enqueued; the
+ * caller synchronises before reading host y/dx. */
+rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host,
+                         const rmx_device_io* dev, const rmx_params* params,
+                         const rmx_grads* grads, void* saved, size_t saved_bytes,
+                         void* ws, size_t ws_bytes, rmx_stream stream);
+
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word.  Returns RMX_ERR_TIMEOUT if a bounded wait in a kernel gave up since
+ * the last check, RMX_ERR_CUDA if the stream reported an error, else RMX_OK. */
+rmx_status rmx_check(rmx_stream stream);
+
+/* Human-readable name of a status code (static string). */
+const char* rmx_status_str(rmx_status s);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int rmx_version(void);
+
+/* Number of kernel launches this library has enqueued since load (host-side
+ * counter, all threads). */
+long long rmx_launch_count(void);
+
+/* Per-kernel timing.  When enabled, every launch is bracketed by CUDA events
+ * recorded on the launching stream.  rmx_profile_read synchronises on the
+ * recorded events, fills up to `cap` entries (name, launches, total ms) and
+ * returns how many kernel names were seen; it then resets the counters. */
+rmx_status rmx_profile_enable(int on);
+int rmx_profile_read(const char** names, long long* launches, double* total_ms, int cap);
+
+/* Test hook (no production use): launches one tiny kernel that waits on an
+ * mbarrier that nothing will ever complete, with a limit of `limit_us`
+ * microseconds, so that the bounded-wait path can be exercised without a
+ * hang.  The timeout is then reported by rmx_check(). */
+rmx_status rmx_test_bounded_wait(int limit_us, rmx_stream stream);
+
+/* Test hook: one grouped GEMM of the kind the block uses, without the rest of
+ * the block, on device buffers in the config's storage dtype.  kind 0 =
+ * forward (C[g] = A[g] @ W[g], A rows strided by G*K, W [G,K,N]);
+ * kind 1 = dgrad (C[g] = A[g] @ W[g]^T, W [G,N,K]); kind 2 = wgrad
+ * (C[g] = A[g]^T @ Bm[g], A [R,G,M], Bm [R,G,N], C [G,M,N]).  For kinds 0/1
+ * A is [M,G,K] and C is [M,G,N].  Used to check the GEMM engine in
+ * isolation. */
+rmx_status rmx_test_gemm(int kind, int dtype, int M, int N, int K, int G, const void* A,
+                         const void* Bm, void* C, rmx_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMX_H */

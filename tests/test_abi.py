@@ -1,0 +1,121 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/rmx.h declares, and rejects bad arguments on the host before any CUDA
+call."""
+
+import ctypes
+import os
+
+import pytest
+
+from ffn_block_gb300 import binding as B
+from ffn_block_gb300 import inputs as I
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from ffn_block_gb300 import build
+        build.build()
+    return B.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = B.header_functions()
+    assert "rmx_forward" in names and "rmx_backward" in names
+    for n in names:
+        assert hasattr(lib, n), f"librmx.so does not export {n}"
+
+
+def test_status_strings_and_version(lib):
+    assert B.status_str(B.RMX_OK) == "RMX_OK"
+    assert B.status_str(B.RMX_ERR_TIMEOUT) == "RMX_ERR_TIMEOUT"
+    assert B.rmx_version() >= 100
+
+
+def _expected_saved(s):
+    e = 4 if s.dtype == "f32" else 2
+    N = s.B * s.T
+    up = lambda v: (v + 255) // 256 * 256
+    total = 0
+    for n in (N * s.D * e, N * 2 * s.H * e, N * s.H * e, N * s.D * e, 10 * N * 4):
+        total = up(total + n)
+    return total
+
+
+@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3", "c4"])
+def test_saved_bytes_layout(lib, name):
+    s = I.shape_of(name)
+    cfg = B.make_config(s.B, s.T, s.D, s.H, s.dtype)
+    assert B.rmx_saved_bytes(cfg) == _expected_saved(s)
+    assert B.rmx_workspace_bytes(cfg) > 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(B=-1, T=8, D=64, H=128), dict(B=2, T=0, D=64, H=128), dict(B=2, T=8, D=60, H=128),
+    dict(B=2, T=8, D=64, H=0), dict(B=2, T=8, D=0, H=128)])
+def test_invalid_config_rejected(lib, bad):
+    cfg = B.make_config(dtype="f32", **bad)
+    assert B.rmx_saved_bytes(cfg) == 0
+    assert B.rmx_workspace_bytes(cfg) == 0
+    p = B.rmx_params(*([0x1000] * 14))
+    assert B.rmx_forward(cfg, 0x1000, p, 0x2000, 1 << 20, 0x3000) == B.RMX_ERR_INVALID_ARG
+
+
+def test_bad_dtype_rejected(lib):
+    cfg = B.rmx_config(2, 8, 64, 128, 7)
+    assert B.rmx_saved_bytes(cfg) == 0
+
+
+def test_null_and_misaligned_pointers(lib):
+    cfg = B.make_config(2, 8, 64, 128, "f32")
+    nbytes = B.rmx_saved_bytes(cfg)
+    good = B.rmx_params(*([0x1000] * 14))
+    nullp = B.rmx_params(*([0x1000] * 13 + [None]))
+    mis = B.rmx_params(*([0x1000] * 13 + [0x1008]))
+    assert B.rmx_forward(cfg, 0x1000, nullp, 0x2000, nbytes, 0x3000) == B.RMX_ERR_INVALID_ARG
+    assert B.rmx_forward(cfg, 0x1000, mis, 0x2000, nbytes, 0x3000) == B.RMX_ERR_ALIGNMENT
+    assert B.rmx_forward(cfg, 0x1004, good, 0x2000, nbytes, 0x3000) == B.RMX_ERR_ALIGNMENT
+    assert B.rmx_forward(cfg, None, good, 0x2000, nbytes, 0x3000) == B.RMX_ERR_INVALID_ARG
+    assert B.rmx_forward(cfg, 0x1000, good, 0x2000, nbytes, 0x1000) == B.RMX_ERR_INVALID_ARG  # x aliases y
+
+
+def test_small_saved_buffer_rejected(lib):
+    cfg = B.make_config(2, 8, 64, 128, "f32")
+    nbytes = B.rmx_saved_bytes(cfg)
+    p = B.rmx_params(*([0x1000] * 14))
+    assert B.rmx_forward(cfg, 0x1000, p, 0x2000, nbytes - 1, 0x3000) == B.RMX_ERR_WORKSPACE
+    g = B.rmx_grads(*([0x1000] * 14))
+    ws = B.rmx_workspace_bytes(cfg)
+    assert B.rmx_backward(cfg, 0x1000, 0x1100, 0x2000, nbytes, p, 0x3000, g, 0x4000, ws - 1) == B.RMX_ERR_WORKSPACE
+    assert B.rmx_backward(cfg, 0x1000, 0x1100, 0x2000, nbytes, p, 0x3000, B.rmx_grads(*([None] * 14)),
+                          0x4000, ws) == B.RMX_ERR_INVALID_ARG
+
+
+def test_unsupported_row_width(lib):
+    # bf16 rows must be whole 16-byte vectors: D = 36 (D % T == 0 with T = 4) is not.
+    cfg = B.make_config(2, 4, 36, 64, "bf16")
+    p = B.rmx_params(*([0x1000] * 14))
+    assert B.rmx_forward(cfg, 0x1000, p, 0x2000, B.rmx_saved_bytes(cfg), 0x3000) == B.RMX_ERR_UNSUPPORTED
+
+
+def test_empty_batch_forward_is_a_no_op(lib):
+    cfg = B.make_config(0, 8, 64, 128, "bf16")
+    p = B.rmx_params(*([0x1000] * 14))
+    before = B.rmx_launch_count()
+    assert B.rmx_forward(cfg, None, p, None, 0, None) == B.RMX_OK
+    assert B.rmx_launch_count() == before
+
+
+def test_host_step_rejects_missing_buffers(lib):
+    cfg = B.make_config(2, 8, 64, 128, "f32")
+    host = B.rmx_host_io(None, None, None, None)
+    dev = B.rmx_device_io(0x1000, 0x1100, 0x1200, 0x1300)
+    p = B.rmx_params(*([0x1000] * 14))
+    g = B.rmx_grads(*([0x1000] * 14))
+    assert B.rmx_step_host(cfg, host, dev, p, g, 0x2000, 1 << 20, 0x3000, 1 << 20) == B.RMX_ERR_INVALID_ARG
+
+
+def test_test_hooks_validate_arguments(lib):
+    assert B.rmx_test_bounded_wait(0) == B.RMX_ERR_INVALID_ARG
+    assert B.rmx_test_gemm(3, "bf16", 8, 8, 8, 1, 0x1000, 0x1000, 0x1000) == B.RMX_ERR_INVALID_ARG
+    assert B.rmx_test_gemm(0, "bf16", 8, 8, 8, 1, 0x1008, 0x1000, 0x1000) == B.RMX_ERR_ALIGNMENT
