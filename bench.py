@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c3")
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
+    ap.add_argument("--tokens", type=int, default=None, help="override T (profiling a smaller case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -294,6 +296,23 @@ def aggregate(rows_per_rank: int, ms_max: float, ws: int) -> float:
     return rows_per_rank * ws / (ms_max / 1e3)
 
 
+def workload_name(args, shape) -> str:
+    base = WORKLOAD_NAMES.get(args.config, args.config)
+    if args.batch is None and args.tokens is None:
+        return base
+    return f"RankMixer block B={shape.B} T={shape.T} D={shape.D} H={shape.H} {shape.dtype} (reduced case)"
+
+
+def workload_shape(args):
+    from ffn_block_gb300 import inputs as I
+    d = dict(I.CONFIGS[args.config])
+    if args.batch is not None:
+        d["B"] = args.batch
+    if args.tokens is not None:
+        d["T"] = args.tokens
+    return I.Shape(**d)
+
+
 def run_ours(args) -> dict | None:
     import numpy as np
     import torch
@@ -303,7 +322,7 @@ def run_ours(args) -> dict | None:
     from ffn_block_gb300.device import RankMixerDevice
 
     rank, local, ws = dist_setup(args.gpus)
-    shape = I.shape_of(args.config)
+    shape = workload_shape(args)
     arrays = I.make_inputs(shape, seed=I.DEFAULT_SEED + rank)
     blk = RankMixerDevice(shape, arrays, device=f"cuda:{torch.cuda.current_device()}")
     del arrays
@@ -427,7 +446,7 @@ def run_ours(args) -> dict | None:
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "f16": "f16"}[shape.dtype],
         "data": "synthetic (seeded he-uniform weights, standard-normal x and dy)",
-        "config": {"workload": WORKLOAD_NAMES.get(args.config, args.config), "B": shape.B, "T": shape.T,
+        "config": {"workload": workload_name(args, shape), "B": shape.B, "T": shape.T,
                    "D": shape.D, "H": shape.H, "storage": shape.dtype, "parallelism": f"replicas x{ws}",
                    "l2": "flushed before every step (outside the timed region)"},
         "step_roofline": step_roofline,

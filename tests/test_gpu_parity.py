@@ -27,7 +27,16 @@ def _full_case(shape, ln="random", seed=I.DEFAULT_SEED):
     arrays = I.make_inputs(shape, seed=seed, ln_params=ln)
     got = _gpu(shape, arrays)
     ref = oracle_outputs(arrays)
-    return compare(got, ref, TOL[shape.dtype])
+    names = NAMES
+    if shape.D == shape.T:
+        # With one column per token chunk, dbeta0 sums the rows of norm1's
+        # backward, which are zero: the exact gradient is 0, so it is checked
+        # against the scale of its sibling dgamma0 instead of relatively.
+        names = tuple(n for n in NAMES if n != "beta0")
+        scale = np.abs(ref["gamma0"]).max()
+        assert np.abs(ref["beta0"]).max() <= 1e-12 * scale
+        assert np.abs(got["beta0"]).max() <= 1e-3 * scale
+    return compare(got, ref, TOL[shape.dtype], names=names)
 
 
 @pytest.mark.parametrize("ln", ["init", "random"])

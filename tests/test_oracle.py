@@ -178,6 +178,17 @@ def test_zero_w1_closed_form():
     np.testing.assert_array_equal(grads["wout"], 0.0)
 
 
+def test_beta0_gradient_vanishes_when_D_equals_T():
+    # With D == T each token chunk is one column, so dbeta0[d] = sum over b, j
+    # of ds1[b, d, j]: row sums of a LayerNorm backward, which are zero.
+    inp = _inputs(I.Shape(B=3, T=8, D=8, H=16))
+    _, _, grads = O.forward_backward(inp["x"], inp["dy"], _params(inp))
+    assert np.abs(grads["beta0"]).max() <= 1e-13 * np.abs(grads["gamma0"]).max()
+    inp = _inputs(I.Shape(B=3, T=4, D=8, H=16))           # C = 2: no longer zero
+    _, _, grads = O.forward_backward(inp["x"], inp["dy"], _params(inp))
+    assert np.abs(grads["beta0"]).max() > 1e-3 * np.abs(grads["gamma0"]).max()
+
+
 def test_per_token_gemm_is_textbook_matmul():
     rng = np.random.default_rng(7)
     inp = rng.standard_normal((3, 2, 5))
