@@ -76,6 +76,7 @@ _SIGNATURES = {
     "rmx_profile_read": (_I, [_P(ctypes.c_char_p), _P(ctypes.c_longlong), _P(ctypes.c_double), _I]),
     "rmx_test_bounded_wait": (_I, [_I, _VP]),
     "rmx_test_gemm": (_I, [_I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP]),
+    "rmx_ln2_backward_noalloc": (_I, [_P(rmx_config), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
 }
 
 _lib = None
@@ -201,3 +202,11 @@ def rmx_test_bounded_wait(limit_us: int, stream=None) -> int:
 def rmx_test_gemm(kind: int, dtype, M: int, N: int, K: int, G: int, A, Bm, C, stream=None) -> int:
     code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
     return lib().rmx_test_gemm(kind, code, M, N, K, G, _ptr(A), _ptr(Bm), _ptr(C), _stream(stream))
+
+
+def rmx_ln2_backward_noalloc(cfg, dy, s2, mean2, rstd2, gamma2, ds2, dgamma2, dbeta2, dbout,
+                             stream=None) -> int:
+    """norm2 backward with the library's fixed scratch array (no allocation)."""
+    return lib().rmx_ln2_backward_noalloc(ctypes.byref(cfg), _ptr(dy), _ptr(s2), _ptr(mean2), _ptr(rstd2),
+                                          _ptr(gamma2), _ptr(ds2), _ptr(dgamma2), _ptr(dbeta2), _ptr(dbout),
+                                          _stream(stream))

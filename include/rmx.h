@@ -166,6 +166,36 @@ rmx_status rmx_test_bounded_wait(int limit_us, rmx_stream stream);
 rmx_status rmx_test_gemm(int kind, int dtype, int M, int N, int K, int G, const void* A,
                          const void* Bm, void* C, rmx_stream stream);
 
+/* No-allocation variant of the norm2 backward.  The pages have no
+ * counterpart: this entry point exists for callers that cannot provide
+ * scratch memory -- a host framework that owns all device memory through its
+ * own pool and passes a plugin only its inputs and outputs, or a deployment
+ * that must keep a fixed memory footprint with no allocation after start-up.
+ *
+ * Computes, for y = norm2(s2): ds2 [B,T,D] = the gradient w.r.t. s2 for
+ * upstream dy [B,T,D], and the gradients dgamma2 [D], dbeta2 [D] (summed over
+ * all B*T rows) and dbout [T,D] (summed over b), all in the config's storage
+ * dtype -- the same values rmx_backward produces for these tensors.  s2,
+ * mean2 and rstd2 are norm2's input and float32 row statistics [B*T] as
+ * rmx_forward stores them in its saved buffer (s2 is the fourth tensor,
+ * mean2/rstd2 the fifth and sixth statistic vectors).
+ *
+ * Scratch: the partial sums live in a fixed device array of 8 MiB inside
+ * the library, reserved on each GPU when the library is first used there and
+ * held until the process exits.  This call allocates nothing.  Shapes whose
+ * partial sums for one block of samples (3*T*D floats) exceed 8 MiB, and
+ * B == 0, are rejected (RMX_ERR_UNSUPPORTED / RMX_ERR_INVALID_ARG) before any
+ * launch.  The first call on each device looks up the array's device address
+ * with the device current; make that first call before any stream capture.
+ * Every call uses the same array: calls that overlap on the GPU (on
+ * different streams, or from several threads) race and must be serialised
+ * by the caller.  Each call writes every scratch value it reads, so nothing
+ * carries over from a previous call. */
+rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void* dy, const void* s2,
+                                    const float* mean2, const float* rstd2, const void* gamma2,
+                                    void* ds2, void* dgamma2, void* dbeta2, void* dbout,
+                                    rmx_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
