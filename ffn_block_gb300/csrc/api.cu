@@ -108,10 +108,13 @@ Layout layout_of(const rmx_config& c) {
   L.pwg = o; o = up(o + P * H * sizeof(float));
   L.pbg = o; o = up(o + P * H * sizeof(float));
   L.pb1 = o; o = up(o + P * 2 * H * sizeof(float));
-  L.pg0 = o; o = up(o + (size_t)c.B * D * sizeof(float));
-  L.pb0 = o; o = up(o + (size_t)c.B * D * sizeof(float));
-  L.pg1 = o; o = up(o + (size_t)c.B * D * sizeof(float));
-  L.pbe1 = o; o = up(o + (size_t)c.B * D * sizeof(float));
+  // norm0/norm1 partial rows: one per sample (generic pass) or one per CTA
+  // of the cluster pass (at most kMixPartialRowsMax).
+  const size_t P01 = (size_t)(c.B > kMixPartialRowsMax ? c.B : kMixPartialRowsMax);
+  L.pg0 = o; o = up(o + P01 * D * sizeof(float));
+  L.pb0 = o; o = up(o + P01 * D * sizeof(float));
+  L.pg1 = o; o = up(o + P01 * D * sizeof(float));
+  L.pbe1 = o; o = up(o + P01 * D * sizeof(float));
   L.ws_total = o;
   return L;
 }
@@ -255,7 +258,11 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   void* hidden = at(saved, L.hidden);
   void* s2 = at(saved, L.s2);
   Stats S = stats_of(saved, L, N);
-  {
+  if (mix_supported(L.ra)) {
+    Launch l("ln0_mix_ln1_fwd", st);
+    RMX_TRY(l.done(launch_mix_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, out1, S.mu0, S.r0, S.mu1, S.r1,
+                                  st)));
+  } else {
     Launch l("ln0_mix_ln1_fwd", st);
     RMX_TRY(l.done(launch_ln0_mix_ln1_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, out1, S.mu0, S.r0,
                                           S.mu1, S.r1, st)));
@@ -321,7 +328,13 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm1_wgrad", d, st));
   }
-  {
+  int P01 = c.B;
+  if (mix_supported(L.ra)) {
+    P01 = mix_bwd_partial_rows(L.ra);
+    Launch l("ln1_mix_ln0_bwd", st);
+    RMX_TRY(l.done(launch_mix_bwd(L.ra, x, dout1, S.mu0, S.r0, S.mu1, S.r1, p.gamma0, p.beta0, p.gamma1, dx,
+                                  F(L.pg0), F(L.pb0), F(L.pg1), F(L.pbe1), st)));
+  } else {
     Launch l("ln1_mix_ln0_bwd", st);
     RMX_TRY(l.done(launch_ln1_mix_ln0_bwd(L.ra, x, dout1, S.mu0, S.r0, S.mu1, S.r1, p.gamma0, p.beta0,
                                           p.gamma1, ds1, dx, F(L.pg0), F(L.pb0), F(L.pg1), F(L.pbe1), st)));
@@ -333,8 +346,8 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
         {F(L.pbo), g.bout, Pb, c.T * c.D},     {F(L.pwx), g.lnx_w, P, c.H},
         {F(L.pbx), g.lnx_b, P, c.H},           {F(L.pwg), g.lng_w, P, c.H},
         {F(L.pbg), g.lng_b, P, c.H},           {F(L.pb1), g.b1, Pb, c.T * 2 * c.H},
-        {F(L.pg1), g.gamma1, c.B, c.D},        {F(L.pbe1), g.beta1, c.B, c.D},
-        {F(L.pg0), g.gamma0, c.B, c.D},        {F(L.pb0), g.beta0, c.B, c.D},
+        {F(L.pg1), g.gamma1, P01, c.D},        {F(L.pbe1), g.beta1, P01, c.D},
+        {F(L.pg0), g.gamma0, P01, c.D},        {F(L.pb0), g.beta0, P01, c.D},
     };
     Launch l("colsums", st);
     cudaError_t e = launch_colsums(jobs, 12, c.dtype, st);

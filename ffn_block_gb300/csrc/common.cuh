@@ -142,3 +142,53 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 constexpr uint64_t kWaitLimitNs = 2000ull * 1000ull * 1000ull;  // 2 s
 
 }  // namespace rmx
+
+namespace rmx {
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Bulk copy global -> shared (no tensor map): both addresses 16-byte aligned,
+// size a multiple of 16; completion is counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Chan / Golub / LeVeque merge of (count, mean, M2) partial statistics.
+struct Moments {
+  float n, mean, m2;
+};
+__device__ __forceinline__ Moments merge_moments(const Moments& a, const Moments& b) {
+  const float n = a.n + b.n;
+  if (n == 0.f) return a;
+  const float d = b.mean - a.mean;
+  const float wb = b.n / n;
+  Moments r;
+  r.n = n;
+  r.mean = a.mean + d * wb;
+  r.m2 = a.m2 + b.m2 + d * d * a.n * wb;
+  return r;
+}
+__device__ __forceinline__ Moments warp_merge_moments(Moments m) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Moments other;
+    other.n = __shfl_xor_sync(0xffffffffu, m.n, o);
+    other.mean = __shfl_xor_sync(0xffffffffu, m.mean, o);
+    other.m2 = __shfl_xor_sync(0xffffffffu, m.m2, o);
+    // Merge in a fixed order (lower lane first) so every lane gets the same bits.
+    m = ((threadIdx.x & o) == 0) ? merge_moments(m, other) : merge_moments(other, m);
+  }
+  return m;
+}
+
+}  // namespace rmx

@@ -17,6 +17,12 @@
 //              so the epilogue of tile i overlaps the main loop of tile i+1;
 //   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, add
 //              bias / residual in fp32, round to the storage type, store.
+// Paired mode (M spans at least two tiles): a cluster of two CTAs computes
+// the two M-adjacent tiles that share one B tile.  Each CTA loads its own A
+// tile and half of the B tile, multicasting that half into both CTAs' shared
+// memory, so L2 delivers 32 KB instead of 48 KB per CTA and k-block; each MMA
+// completion is signalled to the `empty` barriers of both CTAs, so a stage is
+// refilled only when both have consumed it.
 // Operands are addressed through rank-3 tensor maps so that per-token slices
 // of [B,T,X] activations and [T,X,Y] weights need no copies; K-major and
 // MN-major shared-memory layouts cover the NN (forward), NT (dgrad) and TN
@@ -29,6 +35,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <type_traits>
 
 #include "common.cuh"
@@ -53,6 +60,7 @@ constexpr uint64_t kDrainLimitNs = 50ull * 1000ull * 1000ull;
 struct Params {
   int M, N, K, G;
   int tiles_m, tiles_n, tiles_per_group, num_tiles, num_kb;
+  int pairs_m, pair_tiles_per_group, num_pair_tiles;  // paired mode
   void* out;
   long long out_rs, out_gs;
   const void* bias;
@@ -79,6 +87,34 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+// Same copy, written to the same shared offset of every CTA in `mask` and
+// counted on each CTA's barrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                               int c2, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%4, %5, %6}], [%2], %3;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "h"(mask), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -113,6 +149,14 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+// Arrive on the barrier at `bar`'s offset in every CTA of `mask` once the
+// tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
 }
 // 32 lanes x 32 consecutive fp32 columns; thread i of the warp gets lane
 // (quarter base + i).  The wait is in the same statement so that no use of
@@ -176,6 +220,16 @@ __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& g, i
   n0 = tn * BN;
 }
 
+// Paired mode: pair tile -> (group, this CTA's m0, n0).
+__device__ __forceinline__ void pair_tile_coords(const Params& p, int pt, int rank, int& g, int& m0, int& n0) {
+  g = pt / p.pair_tiles_per_group;
+  const int rem = pt - g * p.pair_tiles_per_group;
+  const int tn = rem / p.pairs_m;
+  const int tp = rem - tn * p.pairs_m;
+  m0 = (2 * tp + rank) * BM;
+  n0 = tn * BN;
+}
+
 template <typename T, int EPI>
 __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, int n_base, const float* v) {
   constexpr int V = VecN<T>::value;
@@ -204,7 +258,7 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, in
   }
 }
 
-template <typename T, int KIND, int EPI>
+template <typename T, int KIND, int EPI, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
   using KT = KindTraits<KIND>;
@@ -223,11 +277,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 2 * NUM_ACC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = PAIR ? (int)cluster_rank() : 0;
+  // Work list: single tiles (this CTA), or pair tiles (this cluster).
+  const int first = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int stride = PAIR ? (int)num_clusters_x() : (int)gridDim.x;
+  const int count = PAIR ? p.num_pair_tiles : p.num_tiles;
+  auto coords = [&](int it, int& g, int& m0, int& n0) {
+    if (PAIR) pair_tile_coords(p, it, rank, g, m0, n0);
+    else tile_coords(p, it, g, m0, n0);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), PAIR ? 2 : 1);  // paired: both CTAs' MMAs release a stage
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -242,6 +305,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  // Paired: the peer's barriers are initialised before any multicast lands.
+  if (PAIR) cluster_barrier();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -250,9 +315,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = first; ok && tile < count; tile += stride) {
         int g, m0, n0;
-        tile_coords(p, tile, g, m0, n0);
+        coords(tile, g, m0, n0);
+        // Pieces of the tiles this CTA requests.  MN-major tiles come as
+        // 64-wide chunks; chunks or tiles wholly past M or N are skipped
+        // (they only feed discarded outputs) and not counted.
+        const int a_chunks = KT::A_MN ? max(0, min(BM / 64, (p.M - m0 + 63) / 64)) : (m0 < p.M ? 1 : 0);
+        const int b_chunks = KT::B_MN ? min(BN / 64, (p.N - n0 + 63) / 64) : 0;
+        // K-major B in paired mode: two 128-row halves, one per CTA.
+        const int b_halves = KT::B_MN ? 0 : (PAIR ? ((p.N - n0 > 128) ? 2 : 1) : 1);
+        const uint32_t a_bytes = KT::A_MN ? a_chunks * MN_CHUNK_BYTES : a_chunks * A_BYTES;
+        const uint32_t b_bytes = KT::B_MN ? b_chunks * MN_CHUNK_BYTES : (PAIR ? b_halves * (B_BYTES / 2) : B_BYTES);
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -261,37 +335,56 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          // MN-major tiles are loaded as 64-wide chunks; chunks lying wholly
-          // past M or N are skipped (they only feed discarded output rows or
-          // columns), and the expected byte count covers what is requested.
-          const int a_chunks = KT::A_MN ? min(BM / 64, (p.M - m0 + 63) / 64) : 1;
-          const int b_chunks = KT::B_MN ? min(BN / 64, (p.N - n0 + 63) / 64) : 1;
-          const uint32_t bytes = (KT::A_MN ? a_chunks * MN_CHUNK_BYTES : A_BYTES) +
-                                 (KT::B_MN ? b_chunks * MN_CHUNK_BYTES : B_BYTES);
-          mbar_expect_tx(full_bar(s), bytes);
+          mbar_expect_tx(full_bar(s), a_bytes + b_bytes);
           const int k0 = kb * BK;
           const uint32_t a_dst = sA + s * A_BYTES, b_dst = sB + s * B_BYTES;
           if (!KT::A_MN) {
-            tma_load_3d(a_dst, &tmA, full_bar(s), k0, g, m0);                 // map {K, G, M}
+            if (a_chunks) tma_load_3d(a_dst, &tmA, full_bar(s), k0, g, m0);          // map {K, G, M}
           } else {
-            for (int c = 0; c < a_chunks; ++c)                                  // map {M, G, K}
+            for (int c = 0; c < a_chunks; ++c)                                         // map {M, G, K}
               tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, full_bar(s), m0 + 64 * c, g, k0);
           }
-          if (!KT::B_MN) {
-            tma_load_3d(b_dst, &tmB, full_bar(s), k0, n0, g);                 // map {K, N, G}
-          } else if (!KT::B_ACT) {
-            for (int c = 0; c < b_chunks; ++c)                                  // map {N, K, G}
-              tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, k0, g);
+          if (!PAIR) {
+            if (!KT::B_MN) {
+              tma_load_3d(b_dst, &tmB, full_bar(s), k0, n0, g);                      // map {K, N, G}
+            } else {
+              for (int c = 0; c < b_chunks; ++c) {
+                if (!KT::B_ACT)                                                        // map {N, K, G}
+                  tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, k0, g);
+                else                                                                   // map {N, G, K}
+                  tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, g, k0);
+              }
+            }
           } else {
-            for (int c = 0; c < b_chunks; ++c)                                  // map {N, G, K}
-              tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, g, k0);
+            if (!KT::B_MN) {
+              // Half `rank` of the 256-row K-major tile, to both CTAs.
+              if (rank < b_halves)
+                tma_load_3d_mc(b_dst + rank * (B_BYTES / 2), &tmB, full_bar(s), k0, n0 + 128 * rank, g, 0x3);
+            } else {
+              // Chunks 2*rank and 2*rank+1 of the MN-major tile, to both CTAs.
+              for (int c = 2 * rank; c < 2 * rank + 2 && c < b_chunks; ++c) {
+                if (!KT::B_ACT)
+                  tma_load_3d_mc(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, k0, g, 0x3);
+                else
+                  tma_load_3d_mc(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, g, k0, 0x3);
+              }
+            }
           }
         }
       }
+      if (ok && PAIR) {
+        // Wait until both CTAs' MMAs have released the last stages, so no
+        // arrival from the peer is still on its way to this CTA's barriers
+        // when the cluster finishes.
+        const int first_j = it > STAGES ? it - STAGES : 0;
+        for (int j = first_j; j < it; ++j)
+          mbar_wait_bounded(empty_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, p.wait_limit_ns, p.err,
+                            ERRBIT_WAIT_DRAIN, abort_flag);
+      }
       if (!ok) {
         // Let the copies already issued land before the CTA can exit.
-        const int first = it > STAGES ? it - STAGES : 0;
-        for (int j = first; j < it; ++j) {
+        const int first_j = it > STAGES ? it - STAGES : 0;
+        for (int j = first_j; j < it; ++j) {
           volatile int no_abort = 0;
           mbar_wait_bounded(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, kDrainLimitNs, p.err,
                             ERRBIT_WAIT_DRAIN, &no_abort);
@@ -305,7 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc = make_idesc<T, KT::A_MN, KT::B_MN>();
       int it = 0, lt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++lt) {
+      for (int tile = first; ok && tile < count; tile += stride, ++lt) {
         const int acc = lt & 1;
         const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
         if (!mbar_wait_bounded(tempty_bar(acc), aph ^ 1u, p.wait_limit_ns, p.err, ERRBIT_WAIT_MMA, abort_flag)) {
@@ -333,7 +426,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             : sw128_desc(b_base + k * 32, 16, 1024);
             umma_f16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(empty_bar(s));
+          if (PAIR) umma_commit_mc(empty_bar(s), 0x3);
+          else umma_commit(empty_bar(s));
         }
         if (!ok) break;
         umma_commit(tfull_bar(acc));
@@ -350,9 +444,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int lt = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
+    for (int tile = first; tile < count; tile += stride, ++lt) {
       int g, m0, n0;
-      tile_coords(p, tile, g, m0, n0);
+      coords(tile, g, m0, n0);
       const int acc = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
       int ok = 1;
@@ -364,7 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m = m0 + q * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       for (int j0 = 0; j0 < BN; j0 += 32) {
-        if (n0 + j0 >= p.N) break;  // warp-uniform
+        if (n0 + j0 >= p.N || m0 >= p.M) break;  // warp-uniform
         float v[32];
         tmem_ld_32x32(t_row + (uint32_t)j0, v);
         if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + j0, v);
@@ -377,6 +471,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Paired: neither CTA leaves while the other may still multicast into its
+  // shared memory or arrive on its barriers.
+  if (PAIR) cluster_barrier();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -427,26 +524,42 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t
   return r == CUDA_SUCCESS;
 }
 
-template <typename T, int KIND, int EPI>
+template <typename T, int KIND, int EPI, bool PAIR>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
-  auto k = k_gemm_tc<T, KIND, EPI>;
+  auto k = k_gemm_tc<T, KIND, EPI, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-  k<<<grid, THREADS, SMEM_BYTES, st>>>(a, b, p);
-  return cudaGetLastError();
+  if (!PAIR) {
+    const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+    k<<<grid, THREADS, SMEM_BYTES, st>>>(a, b, p);
+    return cudaGetLastError();
+  }
+  const int clusters = p.num_pair_tiles < sm_count() / 2 ? p.num_pair_tiles : sm_count() / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (clusters > 0 ? clusters : 1), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, b, p);
 }
 
-template <typename T>
+template <typename T, bool PAIR>
 cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorMap& b, const Params& p,
                         cudaStream_t st) {
   switch (d.kind * 4 + d.epi) {
-    case GEMM_FWD * 4 + EPI_STORE: return launch_tc<T, GEMM_FWD, EPI_STORE>(a, b, p, st);
-    case GEMM_FWD * 4 + EPI_BIAS: return launch_tc<T, GEMM_FWD, EPI_BIAS>(a, b, p, st);
-    case GEMM_FWD * 4 + EPI_BIAS_RESID: return launch_tc<T, GEMM_FWD, EPI_BIAS_RESID>(a, b, p, st);
-    case GEMM_DGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE>(a, b, p, st);
-    case GEMM_DGRAD * 4 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID>(a, b, p, st);
-    case GEMM_WGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE>(a, b, p, st);
+    case GEMM_FWD * 4 + EPI_STORE: return launch_tc<T, GEMM_FWD, EPI_STORE, PAIR>(a, b, p, st);
+    case GEMM_FWD * 4 + EPI_BIAS: return launch_tc<T, GEMM_FWD, EPI_BIAS, PAIR>(a, b, p, st);
+    case GEMM_FWD * 4 + EPI_BIAS_RESID: return launch_tc<T, GEMM_FWD, EPI_BIAS_RESID, PAIR>(a, b, p, st);
+    case GEMM_DGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE, PAIR>(a, b, p, st);
+    case GEMM_DGRAD * 4 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID, PAIR>(a, b, p, st);
+    case GEMM_WGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE, PAIR>(a, b, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -480,6 +593,13 @@ bool gemm_tc_supported(const GemmDesc& d) {
 cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st) {
   if (!gemm_tc_supported(d)) return cudaErrorInvalidValue;
   const uint64_t e = 2, M = d.M, N = d.N, K = d.K, G = d.G;
+  // Paired mode whenever M spans at least two tiles (and the env switch
+  // RMX_GEMM_PAIRS=0 is not set).
+  static const bool pairs_on = [] {
+    const char* v = getenv("RMX_GEMM_PAIRS");
+    return !(v && v[0] == '0');
+  }();
+  const bool pair = pairs_on && d.M > BM;
   CUtensorMap ma, mb;
   bool ok = true;
   if (d.kind == GEMM_FWD || d.kind == GEMM_DGRAD) {
@@ -487,7 +607,7 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
     if (d.kind == GEMM_FWD)
       ok &= make_map(&mb, d.Bm, d.dtype, N, K, G, N * e, K * N * e, 64, BK, 1);      // W [G,K,N]
     else
-      ok &= make_map(&mb, d.Bm, d.dtype, K, N, G, K * e, N * K * e, BK, BN, 1);      // W [G,N,K]
+      ok &= make_map(&mb, d.Bm, d.dtype, K, N, G, K * e, N * K * e, BK, pair ? BN / 2 : BN, 1);  // W [G,N,K]
   } else {
     ok &= make_map(&ma, d.A, d.dtype, M, G, K, M * e, G * M * e, 64, 1, BK);          // A [K,G,M]
     ok &= make_map(&mb, d.Bm, d.dtype, N, G, K, N * e, G * N * e, 64, 1, BK);         // B [K,G,N]
@@ -503,6 +623,9 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.tiles_per_group = p.tiles_m * p.tiles_n;
   p.num_tiles = p.tiles_per_group * d.G;
   p.num_kb = (d.K + BK - 1) / BK;
+  p.pairs_m = (p.tiles_m + 1) / 2;
+  p.pair_tiles_per_group = p.pairs_m * p.tiles_n;
+  p.num_pair_tiles = p.pair_tiles_per_group * d.G;
   p.out = d.C;
   if (d.kind == GEMM_WGRAD) {
     p.out_rs = d.N;
@@ -518,8 +641,8 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.res_gs = p.out_gs;
   p.err = err;
   p.wait_limit_ns = kWaitLimitNs;
-  if (d.dtype == 1) return dispatch_tc<bf16>(d, ma, mb, p, st);
-  return dispatch_tc<f16>(d, ma, mb, p, st);
+  if (d.dtype == 1) return pair ? dispatch_tc<bf16, true>(d, ma, mb, p, st) : dispatch_tc<bf16, false>(d, ma, mb, p, st);
+  return pair ? dispatch_tc<f16, true>(d, ma, mb, p, st) : dispatch_tc<f16, false>(d, ma, mb, p, st);
 }
 
 cudaError_t launch_bounded_wait_test(unsigned int* err, unsigned long long limit_ns, cudaStream_t st) {

@@ -40,6 +40,20 @@ cudaError_t launch_ln1_mix_ln0_bwd(const RowArgs& a, const void* x, const void* 
                                    float* ds1, void* dx, float* pg0, float* pb0, float* pg1,
                                    float* pbe1, cudaStream_t st);
 
+// Cluster versions of the two per-sample passes (token mix through
+// distributed shared memory).  mix_supported() says whether the shape fits
+// (T <= 64, rows of <= 320 16-byte vectors, shared memory).  The backward
+// writes one partial row per CTA: mix_bwd_partial_rows() of them (<= 1024).
+bool mix_supported(const RowArgs& a);
+int mix_bwd_partial_rows(const RowArgs& a);
+constexpr int kMixPartialRowsMax = 1024;
+cudaError_t launch_mix_fwd(const RowArgs& a, const void* x, const void* g0, const void* be0, const void* g1,
+                           const void* be1, void* out1, float* mu0, float* r0, float* mu1, float* r1,
+                           cudaStream_t st);
+cudaError_t launch_mix_bwd(const RowArgs& a, const void* x, const void* dout1, const float* mu0, const float* r0,
+                           const float* mu1, const float* r1, const void* g0, const void* be0, const void* g1,
+                           void* dx, float* pg0, float* pb0, float* pg1, float* pbe1, cudaStream_t st);
+
 // Deterministic column sums: out[j] = sum_{p<P} part[p*J + j], cast to dtype.
 struct ColsumJob {
   const float* part;

@@ -193,23 +193,74 @@ __global__ void __launch_bounds__(256) k_ln_rows_fwd(const T* __restrict__ s, co
   }
 }
 
+// -------------------------------------------------------------------------
+// Row streaming for the per-token passes.  Each CTA walks a list of rows; its
+// first thread keeps S rows in flight with cp.async.bulk copies into a ring
+// of shared-memory stages (one mbarrier per stage, completion counted in
+// bytes).  A stage is refilled right after the block-wide reduction of the
+// row that used it, when every thread has finished reading it.  Waits are
+// bounded; a wait that gives up sets the device error word and the block
+// leaves the loop together after its next barrier.
+// -------------------------------------------------------------------------
+constexpr int kRingStages = 4;
+constexpr uint64_t kRowWaitLimitNs = 2000ull * 1000ull * 1000ull;
+
+struct RowRing {
+  uint32_t base;        // shared address of stage 0
+  uint32_t stage_bytes; // bytes per stage (multiple of 128)
+  uint32_t bars;        // shared address of the S mbarriers
+  __device__ uint32_t stage(int i) const { return base + (uint32_t)(i % kRingStages) * stage_bytes; }
+  __device__ uint32_t bar(int i) const { return bars + 8u * (uint32_t)(i % kRingStages); }
+};
+
+__device__ __forceinline__ RowRing ring_setup(unsigned char* sm, uint32_t stage_bytes, volatile int* abort_flag) {
+  RowRing r;
+  r.base = smem_u32(sm);
+  r.stage_bytes = stage_bytes;
+  r.bars = r.base + kRingStages * stage_bytes;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRingStages; ++i) mbar_init(r.bars + 8u * i, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  return r;
+}
+
+// Thread 0: after an abort, wait (bounded) for the copies still in flight so
+// the CTA does not exit while they write its shared memory.
+__device__ __forceinline__ void ring_drain(const RowRing& r, int consumed, int issued, unsigned int* err) {
+  if (threadIdx.x != 0) return;
+  volatile int no_abort = 0;
+  for (int j = consumed; j < issued; ++j)
+    mbar_wait_bounded(r.bar(j), (uint32_t)(j / kRingStages) & 1u, 50ull * 1000ull * 1000ull, err,
+                      ERRBIT_WAIT_DRAIN, &no_abort);
+}
+
+__host__ __device__ inline uint32_t ring_stage_bytes(size_t row_bytes) { return (uint32_t)((row_bytes + 127) / 128 * 128); }
+inline size_t ring_smem_bytes(size_t row_bytes) { return (size_t)kRingStages * ring_stage_bytes(row_bytes) + 64; }
+
 // =========================================================================
 // F3: hidden = LN_x(U) * silu(LN_gate(G)), Z = [U | G] per row.  A CTA walks
 // `rpc` consecutive rows; thread v owns columns h = v*V .. v*V+V-1 of both
-// halves, so the product needs no exchange.  Statistics come from the stored
-// Z values.
+// halves, so the product needs no exchange.  Row statistics (from the stored
+// Z values) are merged as (count, mean, M2) in a fixed order: one barrier
+// per row.
 // =========================================================================
 template <typename T>
 __global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const T* __restrict__ wx,
-                                                   const T* __restrict__ bx, const T* __restrict__ wg,
-                                                   const T* __restrict__ bg, T* __restrict__ hidden,
-                                                   float* __restrict__ muU, float* __restrict__ rU,
-                                                   float* __restrict__ muG, float* __restrict__ rG,
-                                                   int N, int H, int rpc, float eps) {
+                                                  const T* __restrict__ bx, const T* __restrict__ wg,
+                                                  const T* __restrict__ bg, T* __restrict__ hidden,
+                                                  float* __restrict__ muU, float* __restrict__ rU,
+                                                  float* __restrict__ muG, float* __restrict__ rG,
+                                                  int N, int H, int rpc, float eps, unsigned int* err) {
   constexpr int V = VecN<T>::value;
-  __shared__ float red[2 * 32 * 2];
-  int slot = 0;
-  const int v = threadIdx.x;
+  extern __shared__ __align__(16) unsigned char sm[];
+  __shared__ float red[2][32][6];
+  __shared__ int abort_flag;
+  const size_t row_bytes = (size_t)2 * H * sizeof(T);
+  const RowRing ring = ring_setup(sm, ring_stage_bytes(row_bytes), &abort_flag);
+  const int v = threadIdx.x, lane = v & 31, warp = v >> 5, nw = blockDim.x >> 5;
   const bool act = v * V < H;
   const int h0 = v * V;
   float fwx[V], fbx[V], fwg[V], fbg[V];
@@ -219,53 +270,81 @@ __global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const
     load_vec(wg + h0, fwg);
     load_vec(bg + h0, fbg);
   }
-  const float invH = 1.0f / (float)H;
-  const int r_begin = blockIdx.x * rpc;
-  const int r_end = min(N, r_begin + rpc);
-  for (int r = r_begin; r < r_end; ++r) {
-    const T* zr = Z + (size_t)r * 2 * H;
+  const int r0 = blockIdx.x * rpc;
+  const int nrows = max(0, min(N, r0 + rpc) - r0);
+  auto issue = [&](int i) {
+    mbar_arrive_expect_tx(ring.bar(i), (uint32_t)row_bytes);
+    bulk_g2s(ring.stage(i), Z + (size_t)(r0 + i) * 2 * H, (uint32_t)row_bytes, ring.bar(i));
+  };
+  int issued = 0;
+  if (v == 0)
+    for (; issued < min(kRingStages, nrows); ++issued) issue(issued);
+  int i = 0;
+  for (; i < nrows; ++i) {
+    mbar_wait_bounded(ring.bar(i), (uint32_t)(i / kRingStages) & 1u, kRowWaitLimitNs, err, ERRBIT_WAIT_PRODUCER,
+                      &abort_flag);
+    const unsigned char* st = sm + (size_t)(i % kRingStages) * ring.stage_bytes;
     float u[V], g[V];
-    float sums[2] = {0.f, 0.f};
+    Moments mu = {0.f, 0.f, 0.f}, mg = {0.f, 0.f, 0.f};
     if (act) {
-      load_vec(zr + h0, u);
-      load_vec(zr + H + h0, g);
+      load_vec(reinterpret_cast<const T*>(st) + h0, u);
+      load_vec(reinterpret_cast<const T*>(st) + H + h0, g);
+      float su = 0.f, sg = 0.f;
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        sums[0] += u[e];
-        sums[1] += g[e];
+        su += u[e];
+        sg += g[e];
       }
-    }
-    block_sum<2>(sums, red, slot);
-    const float mU = sums[0] * invH, mG = sums[1] * invH;
-    float sq[2] = {0.f, 0.f};
-    if (act) {
+      mu.n = mg.n = (float)V;
+      mu.mean = su * (1.0f / V);
+      mg.mean = sg * (1.0f / V);
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        const float cu = u[e] - mU, cg = g[e] - mG;
-        sq[0] += cu * cu;
-        sq[1] += cg * cg;
+        const float a = u[e] - mu.mean, c = g[e] - mg.mean;
+        mu.m2 += a * a;
+        mg.m2 += c * c;
       }
     }
-    block_sum<2>(sq, red, slot);
-    const float rsU = 1.0f / sqrtf(sq[0] * invH + eps);
-    const float rsG = 1.0f / sqrtf(sq[1] * invH + eps);
+    mu = warp_merge_moments(mu);
+    mg = warp_merge_moments(mg);
+    const int slot = i & 1;
+    if (lane == 0) {
+      red[slot][warp][0] = mu.n; red[slot][warp][1] = mu.mean; red[slot][warp][2] = mu.m2;
+      red[slot][warp][3] = mg.n; red[slot][warp][4] = mg.mean; red[slot][warp][5] = mg.m2;
+    }
+    __syncthreads();
+    if (abort_flag) break;
+    if (v == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue(issued++);
+    }
+    Moments tu = {red[slot][0][0], red[slot][0][1], red[slot][0][2]};
+    Moments tg = {red[slot][0][3], red[slot][0][4], red[slot][0][5]};
+    for (int w = 1; w < nw; ++w) {
+      tu = merge_moments(tu, Moments{red[slot][w][0], red[slot][w][1], red[slot][w][2]});
+      tg = merge_moments(tg, Moments{red[slot][w][3], red[slot][w][4], red[slot][w][5]});
+    }
+    const float rsU = 1.0f / sqrtf(tu.m2 / (float)H + eps);
+    const float rsG = 1.0f / sqrtf(tg.m2 / (float)H + eps);
+    const size_t r = (size_t)r0 + i;
     if (act) {
       float o[V];
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        const float uu = (u[e] - mU) * rsU * fwx[e] + fbx[e];
-        const float gg = (g[e] - mG) * rsG * fwg[e] + fbg[e];
+        const float uu = (u[e] - tu.mean) * rsU * fwx[e] + fbx[e];
+        const float gg = (g[e] - tg.mean) * rsG * fwg[e] + fbg[e];
         o[e] = uu * (gg / (1.0f + expf(-gg)));
       }
-      store_vec(hidden + (size_t)r * H + h0, o);
+      store_vec(hidden + r * H + h0, o);
     }
-    if (threadIdx.x == 0) {
-      muU[r] = mU;
+    if (v == 0) {
+      muU[r] = tu.mean;
       rU[r] = rsU;
-      muG[r] = mG;
+      muG[r] = tg.mean;
       rG[r] = rsG;
     }
   }
+  if (abort_flag) ring_drain(ring, i, issued, err);
 }
 
 // =========================================================================
@@ -274,15 +353,21 @@ __global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const
 // xh = (s2 - mean) * rstd:
 //   ds2 = rstd * (g - mean(g) - xh * mean(g * xh)),
 //   dgamma2 += dy * xh, dbeta2 += dy, dbout[t] += ds2 (per-CTA partials).
+// Rows stream through the shared-memory ring (dy row, then s2 row).
 // =========================================================================
 template <typename T>
 __global__ void __launch_bounds__(512) k_ln2_bwd(const T* __restrict__ dy, const T* __restrict__ s2,
-                                                  const float* __restrict__ mu2, const float* __restrict__ r2,
-                                                  const T* __restrict__ g2, T* __restrict__ ds2,
-                                                  float* __restrict__ pg2, float* __restrict__ pb2,
-                                                  float* __restrict__ pbo, int B, int Tn, int D, int nb) {
+                                                 const float* __restrict__ mu2, const float* __restrict__ r2,
+                                                 const T* __restrict__ g2, T* __restrict__ ds2,
+                                                 float* __restrict__ pg2, float* __restrict__ pb2,
+                                                 float* __restrict__ pbo, int B, int Tn, int D, int nb,
+                                                 unsigned int* err) {
   constexpr int V = VecN<T>::value;
+  extern __shared__ __align__(16) unsigned char sm[];
   __shared__ float red[2 * 32 * 2];
+  __shared__ int abort_flag;
+  const size_t half = (size_t)D * sizeof(T);
+  const RowRing ring = ring_setup(sm, ring_stage_bytes(2 * half), &abort_flag);
   int slot = 0;
   const int bblk = blockIdx.x, t = blockIdx.y;
   const int v = threadIdx.x;
@@ -293,16 +378,30 @@ __global__ void __launch_bounds__(512) k_ln2_bwd(const T* __restrict__ dy, const
   for (int e = 0; e < V; ++e) ag[e] = ab[e] = ao[e] = 0.f;
   if (act) load_vec(g2 + d0, gam);
   const float invD = 1.0f / (float)D;
-  const int b_end = min(B, (bblk + 1) * nb);
-  for (int b = bblk * nb; b < b_end; ++b) {
-    const size_t r = (size_t)b * Tn + t;
+  const int b0 = bblk * nb;
+  const int nrows = max(0, min(B, b0 + nb) - b0);
+  auto issue = [&](int i) {
+    const size_t r = (size_t)(b0 + i) * Tn + t;
+    mbar_arrive_expect_tx(ring.bar(i), (uint32_t)(2 * half));
+    bulk_g2s(ring.stage(i), dy + r * D, (uint32_t)half, ring.bar(i));
+    bulk_g2s(ring.stage(i) + (uint32_t)half, s2 + r * D, (uint32_t)half, ring.bar(i));
+  };
+  int issued = 0;
+  if (v == 0)
+    for (; issued < min(kRingStages, nrows); ++issued) issue(issued);
+  int i = 0;
+  for (; i < nrows; ++i) {
+    mbar_wait_bounded(ring.bar(i), (uint32_t)(i / kRingStages) & 1u, kRowWaitLimitNs, err, ERRBIT_WAIT_PRODUCER,
+                      &abort_flag);
+    const T* st = reinterpret_cast<const T*>(sm + (size_t)(i % kRingStages) * ring.stage_bytes);
+    const size_t r = (size_t)(b0 + i) * Tn + t;
     const float mean = mu2[r], rstd = r2[r];
     float dyv[V], xh[V], g[V];
     float sums[2] = {0.f, 0.f};
     if (act) {
       float sv[V];
-      load_vec(dy + r * D + d0, dyv);
-      load_vec(s2 + r * D + d0, sv);
+      load_vec(st + d0, dyv);
+      load_vec(st + D + d0, sv);
 #pragma unroll
       for (int e = 0; e < V; ++e) {
         xh[e] = (sv[e] - mean) * rstd;
@@ -312,6 +411,11 @@ __global__ void __launch_bounds__(512) k_ln2_bwd(const T* __restrict__ dy, const
       }
     }
     block_sum<2>(sums, red, slot);
+    if (abort_flag) break;
+    if (v == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue(issued++);
+    }
     const float mg = sums[0] * invD, mgx = sums[1] * invD;
     if (act) {
       float o[V];
@@ -325,6 +429,7 @@ __global__ void __launch_bounds__(512) k_ln2_bwd(const T* __restrict__ dy, const
       store_vec(ds2 + r * D + d0, o);
     }
   }
+  if (abort_flag) ring_drain(ring, i, issued, err);
   if (act) {
     const size_t p = (size_t)bblk * Tn + t;
 #pragma unroll
@@ -345,6 +450,7 @@ __global__ void __launch_bounds__(512) k_ln2_bwd(const T* __restrict__ dy, const
 //   dU = rU * (gU - mean(gU) - Uh * mean(gU * Uh)), same for dG,
 //   dZ = [dU | dG];   partials: dwx += du*Uh, dbx += du, dwg += dg*Gh,
 //   dbg += dg, db1[t] += dZ.
+// Rows stream through the shared-memory ring (dh row, then the Z row).
 // =========================================================================
 template <typename T>
 __global__ void __launch_bounds__(512) k_gate_bwd(
@@ -353,9 +459,13 @@ __global__ void __launch_bounds__(512) k_gate_bwd(
     const T* __restrict__ wx, const T* __restrict__ bx, const T* __restrict__ wg,
     const T* __restrict__ bg, T* __restrict__ dZ, float* __restrict__ pwx, float* __restrict__ pbx,
     float* __restrict__ pwg, float* __restrict__ pbg, float* __restrict__ pb1, int B, int Tn, int H,
-    int nb) {
+    int nb, unsigned int* err) {
   constexpr int V = VecN<T>::value;
+  extern __shared__ __align__(16) unsigned char sm[];
   __shared__ float red[2 * 32 * 4];
+  __shared__ int abort_flag;
+  const size_t hb = (size_t)H * sizeof(T);
+  const RowRing ring = ring_setup(sm, ring_stage_bytes(3 * hb), &abort_flag);
   int slot = 0;
   const int bblk = blockIdx.x, t = blockIdx.y;
   const int v = threadIdx.x;
@@ -372,17 +482,31 @@ __global__ void __launch_bounds__(512) k_gate_bwd(
     load_vec(bg + h0, fbg);
   }
   const float invH = 1.0f / (float)H;
-  const int b_end = min(B, (bblk + 1) * nb);
-  for (int b = bblk * nb; b < b_end; ++b) {
-    const size_t r = (size_t)b * Tn + t;
+  const int b0 = bblk * nb;
+  const int nrows = max(0, min(B, b0 + nb) - b0);
+  auto issue = [&](int i) {
+    const size_t r = (size_t)(b0 + i) * Tn + t;
+    mbar_arrive_expect_tx(ring.bar(i), (uint32_t)(3 * hb));
+    bulk_g2s(ring.stage(i), dh + r * H, (uint32_t)hb, ring.bar(i));
+    bulk_g2s(ring.stage(i) + (uint32_t)hb, Z + r * 2 * H, (uint32_t)(2 * hb), ring.bar(i));
+  };
+  int issued = 0;
+  if (v == 0)
+    for (; issued < min(kRingStages, nrows); ++issued) issue(issued);
+  int i = 0;
+  for (; i < nrows; ++i) {
+    mbar_wait_bounded(ring.bar(i), (uint32_t)(i / kRingStages) & 1u, kRowWaitLimitNs, err, ERRBIT_WAIT_PRODUCER,
+                      &abort_flag);
+    const T* st = reinterpret_cast<const T*>(sm + (size_t)(i % kRingStages) * ring.stage_bytes);
+    const size_t r = (size_t)(b0 + i) * Tn + t;
     const float mU = muU[r], sU = rU[r], mG = muG[r], sG = rG[r];
     float Uh[V], Gh[V], gU[V], gG[V], du[V], dg[V];
     float sums[4] = {0.f, 0.f, 0.f, 0.f};
     if (act) {
       float dhv[V], zu[V], zg[V];
-      load_vec(dh + r * H + h0, dhv);
-      load_vec(Z + r * 2 * H + h0, zu);
-      load_vec(Z + r * 2 * H + H + h0, zg);
+      load_vec(st + h0, dhv);
+      load_vec(st + H + h0, zu);
+      load_vec(st + 2 * H + h0, zg);
 #pragma unroll
       for (int e = 0; e < V; ++e) {
         Uh[e] = (zu[e] - mU) * sU;
@@ -401,6 +525,11 @@ __global__ void __launch_bounds__(512) k_gate_bwd(
       }
     }
     block_sum<4>(sums, red, slot);
+    if (abort_flag) break;
+    if (v == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue(issued++);
+    }
     if (act) {
       const float m0 = sums[0] * invH, m1 = sums[1] * invH, m2 = sums[2] * invH, m3 = sums[3] * invH;
       float oU[V], oG[V];
@@ -419,6 +548,7 @@ __global__ void __launch_bounds__(512) k_gate_bwd(
       store_vec(dZ + r * 2 * H + H + h0, oG);
     }
   }
+  if (abort_flag) ring_drain(ring, i, issued, err);
   if (act) {
     const size_t p = (size_t)bblk * Tn + t;
 #pragma unroll
@@ -732,13 +862,18 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const void* wx, con
   const int N = a.B * a.T;
   const int threads = round32(a.H / vec_elems(a.dtype));
   if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
-  const int rpc = 4;
+  const int rpc = 64;
   const int grid = (N + rpc - 1) / rpc;
+  const size_t smem = ring_smem_bytes((size_t)2 * a.H * elem_bytes(a.dtype));
+  cudaError_t err = cudaSuccess;
   RMX_DISPATCH_T(a.dtype, {
-    k_gate_fwd<T><<<grid, threads, 0, st>>>((const T*)Z, (const T*)wx, (const T*)bx, (const T*)wg,
-                                            (const T*)bg, (T*)hidden, muU, rU, muG, rG, N, a.H, rpc,
-                                            1e-5f);
+    auto k = k_gate_fwd<T>;
+    err = set_smem(k, smem);
+    if (err == cudaSuccess)
+      k<<<grid, threads, smem, st>>>((const T*)Z, (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg,
+                                     (T*)hidden, muU, rU, muG, rG, N, a.H, rpc, 1e-5f, device_error_word());
   });
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -748,10 +883,16 @@ cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, con
   const int threads = round32(a.D / vec_elems(a.dtype));
   if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
   dim3 grid(a.nbblk, a.T);
+  const size_t smem = ring_smem_bytes((size_t)2 * a.D * elem_bytes(a.dtype));
+  cudaError_t err = cudaSuccess;
   RMX_DISPATCH_T(a.dtype, {
-    k_ln2_bwd<T><<<grid, threads, 0, st>>>((const T*)dy, (const T*)s2, mu2, r2, (const T*)g2, (T*)ds2,
-                                           pg2, pb2, pbo, a.B, a.T, a.D, a.nb);
+    auto k = k_ln2_bwd<T>;
+    err = set_smem(k, smem);
+    if (err == cudaSuccess)
+      k<<<grid, threads, smem, st>>>((const T*)dy, (const T*)s2, mu2, r2, (const T*)g2, (T*)ds2, pg2, pb2, pbo,
+                                     a.B, a.T, a.D, a.nb, device_error_word());
   });
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -762,11 +903,17 @@ cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, con
   const int threads = round32(a.H / vec_elems(a.dtype));
   if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
   dim3 grid(a.nbblk, a.T);
+  const size_t smem = ring_smem_bytes((size_t)3 * a.H * elem_bytes(a.dtype));
+  cudaError_t err = cudaSuccess;
   RMX_DISPATCH_T(a.dtype, {
-    k_gate_bwd<T><<<grid, threads, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, (const T*)wx,
-                                            (const T*)bx, (const T*)wg, (const T*)bg, (T*)dZ, pwx, pbx,
-                                            pwg, pbg, pb1, a.B, a.T, a.H, a.nb);
+    auto k = k_gate_bwd<T>;
+    err = set_smem(k, smem);
+    if (err == cudaSuccess)
+      k<<<grid, threads, smem, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, (const T*)wx, (const T*)bx,
+                                     (const T*)wg, (const T*)bg, (T*)dZ, pwx, pbx, pwg, pbg, pb1, a.B, a.T, a.H,
+                                     a.nb, device_error_word());
   });
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

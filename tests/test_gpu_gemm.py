@@ -62,3 +62,25 @@ def test_grouped_gemm(kind, dtype, shape):
     assert np.all(np.isfinite(got))
     err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert err < TOL[dtype], err
+
+
+# Paired-CTA mode (a cluster of two CTAs shares each B tile) engages when M
+# spans two or more 128-row tiles; an odd tile count leaves the second CTA of
+# the last pair with rows wholly past M.
+PAIR_SHAPES = [
+    (300, 136, 72, 2),     # 3 M-tiles: last pair half empty; N < 256
+    (384, 640, 1000, 1),   # 3 M-tiles, long ragged K
+    (129, 264, 64, 2),     # 2 M-tiles, second one holds a single row
+    (520, 200, 88, 3),     # M-major and N-major tails together
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_grouped_gemm_paired_tiles(kind, dtype, shape):
+    M, N, K, G = shape
+    got, ref = _run(kind, dtype, M, N, K, G, seed=3)
+    assert np.all(np.isfinite(got))
+    err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err < TOL[dtype], err
