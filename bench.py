@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--config", default="c3")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (profiling a smaller case)")
+    ap.add_argument("--dim", type=int, default=None, help="override D (profiling a smaller case)")
+    ap.add_argument("--hidden", type=int, default=None, help="override H (profiling a smaller case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -298,7 +300,7 @@ def aggregate(rows_per_rank: int, ms_max: float, ws: int) -> float:
 
 def workload_name(args, shape) -> str:
     base = WORKLOAD_NAMES.get(args.config, args.config)
-    if args.batch is None and args.tokens is None:
+    if all(v is None for v in (args.batch, args.tokens, args.dim, args.hidden)):
         return base
     return f"RankMixer block B={shape.B} T={shape.T} D={shape.D} H={shape.H} {shape.dtype} (reduced case)"
 
@@ -310,6 +312,10 @@ def workload_shape(args):
         d["B"] = args.batch
     if args.tokens is not None:
         d["T"] = args.tokens
+    if args.dim is not None:
+        d["D"] = args.dim
+    if args.hidden is not None:
+        d["H"] = args.hidden
     return I.Shape(**d)
 
 
