@@ -55,9 +55,9 @@ inline int esize(int dtype) { return dtype == RMX_F32 ? 4 : 2; }
 // ------------------------------------------------------------------ layouts
 struct Layout {
   // saved (filled by the forward)
-  size_t out1, Z, hidden, s2, stats, saved_total;
+  size_t out1, Z, hidden, s2, stats, zstats, saved_total;
   // backward scratch
-  size_t ds2, dh, dZ, dout1, ds1, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
+  size_t ds2, dh, dZ, dout1, ds1, rowsum, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
   RowArgs ra;
 };
 
@@ -81,6 +81,7 @@ Layout layout_of(const rmx_config& c) {
   L.hidden = o; o = up(o + N * H * e);
   L.s2 = o; o = up(o + N * D * e);
   L.stats = o; o = up(o + 10 * N * sizeof(float));
+  L.zstats = o; o = up(o + N * (size_t)zstats_tiles(c.H) * 4 * sizeof(float));  // forward scratch
   L.saved_total = o;
 
   L.ra.B = c.B;
@@ -100,6 +101,7 @@ Layout layout_of(const rmx_config& c) {
   L.dZ = o; o = up(o + N * 2 * H * e);
   L.dout1 = o; o = up(o + N * D * e);
   L.ds1 = o; o = up(o + N * D * sizeof(float));
+  L.rowsum = o; o = up(o + N * 4 * sizeof(float));
   L.pg2 = o; o = up(o + P * D * sizeof(float));
   L.pb2 = o; o = up(o + P * D * sizeof(float));
   L.pbo = o; o = up(o + P * D * sizeof(float));
@@ -267,14 +269,21 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
     RMX_TRY(l.done(launch_ln0_mix_ln1_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, out1, S.mu0, S.r0,
                                           S.mu1, S.r1, st)));
   }
+  float* zstats = reinterpret_cast<float*>(at(saved, L.zstats));
   {
-    GemmDesc d{GEMM_FWD, EPI_BIAS, c.dtype, c.B, 2 * c.H, c.D, c.T, out1, p.w1, Z, p.b1, nullptr};
+    GemmDesc d{GEMM_FWD, EPI_BIAS_ZSTATS, c.dtype, c.B, 2 * c.H, c.D, c.T, out1, p.w1, Z, p.b1, nullptr,
+               zstats, c.H};
+    const bool epilogue_stats = c.dtype != RMX_F32 && gemm_tc_supported(d);
     RMX_TRY(run_gemm("gemm1_fwd", d, st));
+    if (!epilogue_stats) {
+      Launch l("zstats", st);
+      RMX_TRY(l.done(launch_zstats(L.ra, Z, zstats, st)));
+    }
   }
   {
     Launch l("gate_fwd", st);
-    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b, hidden, S.muU, S.rU, S.muG,
-                                   S.rG, st)));
+    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, zstats, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b, hidden, S.muU, S.rU,
+                                   S.muG, S.rG, st)));
   }
   {
     GemmDesc d{GEMM_FWD, EPI_BIAS_RESID, c.dtype, c.B, c.D, c.H, c.T, hidden, p.wout, s2, p.bout, out1};
@@ -318,7 +327,7 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   {
     Launch l("gate_bwd", st);
     RMX_TRY(l.done(launch_gate_bwd(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
-                                   dZ, F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1), st)));
+                                   dZ, F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1), F(L.rowsum), st)));
   }
   {
     GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};

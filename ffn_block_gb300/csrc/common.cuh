@@ -55,6 +55,40 @@ __device__ __forceinline__ void store_vec(T* p, const float* v) {
   *reinterpret_cast<uint4*>(p) = raw;
 }
 
+// Load / store N consecutive elements (N * sizeof(T) = 8 or 16 bytes, aligned).
+template <typename T, int N>
+__device__ __forceinline__ void load_n(const T* p, float* v) {
+  static_assert(N * sizeof(T) == 8 || N * sizeof(T) == 16, "8- or 16-byte access");
+  if (N * sizeof(T) == 16) {
+    uint4 raw = *reinterpret_cast<const uint4*>(p);
+    const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = to_f(e[i]);
+  } else {
+    uint2 raw = *reinterpret_cast<const uint2*>(p);
+    const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = to_f(e[i]);
+  }
+}
+template <typename T, int N>
+__device__ __forceinline__ void store_n(T* p, const float* v) {
+  static_assert(N * sizeof(T) == 8 || N * sizeof(T) == 16, "8- or 16-byte access");
+  if (N * sizeof(T) == 16) {
+    uint4 raw;
+    T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < N; ++i) e[i] = from_f<T>(v[i]);
+    *reinterpret_cast<uint4*>(p) = raw;
+  } else {
+    uint2 raw;
+    T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < N; ++i) e[i] = from_f<T>(v[i]);
+    *reinterpret_cast<uint2*>(p) = raw;
+  }
+}
+
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

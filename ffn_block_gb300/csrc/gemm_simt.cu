@@ -98,7 +98,10 @@ cudaError_t dispatch_simt(const SimtParams& p, int epi, cudaStream_t st) {
   dim3 grid((p.N + TN - 1) / TN, (p.M + TM - 1) / TM, p.G);
   switch (epi) {
     case EPI_STORE: k_gemm_simt<T, EPI_STORE><<<grid, 256, 0, st>>>(p); break;
-    case EPI_BIAS: k_gemm_simt<T, EPI_BIAS><<<grid, 256, 0, st>>>(p); break;
+    case EPI_BIAS:
+    case EPI_BIAS_ZSTATS:  // statistics are taken by launch_zstats on this path
+      k_gemm_simt<T, EPI_BIAS><<<grid, 256, 0, st>>>(p);
+      break;
     case EPI_BIAS_RESID: k_gemm_simt<T, EPI_BIAS_RESID><<<grid, 256, 0, st>>>(p); break;
     case EPI_RESID: k_gemm_simt<T, EPI_RESID><<<grid, 256, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;

@@ -69,6 +69,8 @@ struct Params {
   long long res_rs, res_gs;
   unsigned int* err;
   unsigned long long wait_limit_ns;
+  float* zstats;  // EPI_BIAS_ZSTATS
+  int split;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -231,7 +233,8 @@ __device__ __forceinline__ void pair_tile_coords(const Params& p, int pt, int ra
 }
 
 template <typename T, int EPI>
-__device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, int n_base, const float* v) {
+__device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, int n_base, const float* v,
+                                               Moments* zst) {
   constexpr int V = VecN<T>::value;
   T* orow = reinterpret_cast<T*>(p.out) + (size_t)g * p.out_gs + (size_t)m * p.out_rs;
 #pragma unroll
@@ -241,7 +244,7 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, in
       float o[V];
 #pragma unroll
       for (int e = 0; e < V; ++e) o[e] = v[c + e];
-      if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID) {
+      if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_ZSTATS) {
         float bv[V];
         load_vec(reinterpret_cast<const T*>(p.bias) + (size_t)g * p.bias_gs + n, bv);
 #pragma unroll
@@ -254,6 +257,22 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, in
         for (int e = 0; e < V; ++e) o[e] += rv[e];
       }
       store_vec(orow + n, o);
+      if (EPI == EPI_BIAS_ZSTATS) {
+        // Exact moments of the V stored (rounded) values, merged into the
+        // running moments of their half (vectors never straddle the split).
+        float r[V], sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          r[e] = to_f(from_f<T>(o[e]));
+          sum += r[e];
+        }
+        const float mean = sum * (1.0f / V);
+        float m2 = 0.f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) m2 += (r[e] - mean) * (r[e] - mean);
+        const int h = n < p.split ? 0 : 1;
+        zst[h] = merge_moments(zst[h], Moments{(float)V, mean, m2});
+      }
     }
   }
 }
@@ -457,11 +476,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int m = m0 + q * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      Moments zst[2] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
       for (int j0 = 0; j0 < BN; j0 += 32) {
         if (n0 + j0 >= p.N || m0 >= p.M) break;  // warp-uniform
         float v[32];
         tmem_ld_32x32(t_row + (uint32_t)j0, v);
-        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + j0, v);
+        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + j0, v, zst);
+      }
+      if (EPI == EPI_BIAS_ZSTATS && m < p.M) {
+        float4 w = make_float4(zst[0].mean, zst[0].m2, zst[1].mean, zst[1].m2);
+        *reinterpret_cast<float4*>(p.zstats + (((size_t)m * p.G + g) * p.tiles_n + n0 / BN) * 4) = w;
       }
       tc_fence_before();
       __syncwarp();
@@ -553,13 +577,14 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const Params& 
 template <typename T, bool PAIR>
 cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorMap& b, const Params& p,
                         cudaStream_t st) {
-  switch (d.kind * 4 + d.epi) {
-    case GEMM_FWD * 4 + EPI_STORE: return launch_tc<T, GEMM_FWD, EPI_STORE, PAIR>(a, b, p, st);
-    case GEMM_FWD * 4 + EPI_BIAS: return launch_tc<T, GEMM_FWD, EPI_BIAS, PAIR>(a, b, p, st);
-    case GEMM_FWD * 4 + EPI_BIAS_RESID: return launch_tc<T, GEMM_FWD, EPI_BIAS_RESID, PAIR>(a, b, p, st);
-    case GEMM_DGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE, PAIR>(a, b, p, st);
-    case GEMM_DGRAD * 4 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID, PAIR>(a, b, p, st);
-    case GEMM_WGRAD * 4 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE, PAIR>(a, b, p, st);
+  switch (d.kind * 8 + d.epi) {
+    case GEMM_FWD * 8 + EPI_STORE: return launch_tc<T, GEMM_FWD, EPI_STORE, PAIR>(a, b, p, st);
+    case GEMM_FWD * 8 + EPI_BIAS: return launch_tc<T, GEMM_FWD, EPI_BIAS, PAIR>(a, b, p, st);
+    case GEMM_FWD * 8 + EPI_BIAS_RESID: return launch_tc<T, GEMM_FWD, EPI_BIAS_RESID, PAIR>(a, b, p, st);
+    case GEMM_FWD * 8 + EPI_BIAS_ZSTATS: return launch_tc<T, GEMM_FWD, EPI_BIAS_ZSTATS, PAIR>(a, b, p, st);
+    case GEMM_DGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE, PAIR>(a, b, p, st);
+    case GEMM_DGRAD * 8 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID, PAIR>(a, b, p, st);
+    case GEMM_WGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE, PAIR>(a, b, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -584,7 +609,9 @@ bool gemm_tc_supported(const GemmDesc& d) {
   // 16-byte row strides for the tensor maps and the vector epilogue.
   if (d.N % 8 || d.K % 8) return false;
   if (d.kind == GEMM_WGRAD && d.M % 8) return false;
-  const int ok_epi = (d.kind == GEMM_FWD && (d.epi == EPI_STORE || d.epi == EPI_BIAS || d.epi == EPI_BIAS_RESID)) ||
+  if (d.epi == EPI_BIAS_ZSTATS && (BN != kZStatsTile || !d.zstats || d.split % 8)) return false;
+  const int ok_epi = (d.kind == GEMM_FWD && (d.epi == EPI_STORE || d.epi == EPI_BIAS || d.epi == EPI_BIAS_RESID ||
+                                             d.epi == EPI_BIAS_ZSTATS)) ||
                      (d.kind == GEMM_DGRAD && (d.epi == EPI_STORE || d.epi == EPI_RESID)) ||
                      (d.kind == GEMM_WGRAD && d.epi == EPI_STORE);
   return ok_epi && encode_fn() != nullptr;
@@ -641,6 +668,8 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.res_gs = p.out_gs;
   p.err = err;
   p.wait_limit_ns = kWaitLimitNs;
+  p.zstats = d.zstats;
+  p.split = d.split;
   if (d.dtype == 1) return pair ? dispatch_tc<bf16, true>(d, ma, mb, p, st) : dispatch_tc<bf16, false>(d, ma, mb, p, st);
   return pair ? dispatch_tc<f16, true>(d, ma, mb, p, st) : dispatch_tc<f16, false>(d, ma, mb, p, st);
 }

@@ -20,19 +20,21 @@ cudaError_t launch_ln0_mix_ln1_fwd(const RowArgs& a, const void* x, const void* 
 // Forward: y = LN(s) per row (norm2).
 cudaError_t launch_ln_rows_fwd(const RowArgs& a, const void* s, const void* g, const void* be, void* y,
                                float* mu, float* rs, cudaStream_t st);
-// Forward: hidden = LN_x(U) * silu(LN_gate(G)) from Z = [U | G].
-cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const void* wx, const void* bx,
-                            const void* wg, const void* bg, void* hidden, float* muU, float* rU,
-                            float* muG, float* rG, cudaStream_t st);
+// Forward: hidden = LN_x(U) * silu(LN_gate(G)) from Z = [U | G], with the
+// row statistics merged from `zstats` (see below).
+cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, const void* wx,
+                            const void* bx, const void* wg, const void* bg, void* hidden, float* muU,
+                            float* rU, float* muG, float* rG, cudaStream_t st);
 // Backward of norm2: ds2 plus partial sums for gamma2, beta2, bout.
 cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
                            const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
                            float* pbo, cudaStream_t st);
-// Backward of the gate and both inner LNs: dZ plus partial sums.
+// Backward of the gate and both inner LNs: dZ plus partial sums.  `rowsum`
+// ([B*T][4] floats) is scratch for the row sums of the first pass.
 cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU,
                             const float* rU, const float* muG, const float* rG, const void* wx,
                             const void* bx, const void* wg, const void* bg, void* dZ, float* pwx,
-                            float* pbx, float* pwg, float* pbg, float* pb1, cudaStream_t st);
+                            float* pbx, float* pwg, float* pbg, float* pb1, float* rowsum, cudaStream_t st);
 // Backward of norm1, the token mix and norm0: dx plus partial sums.
 cudaError_t launch_ln1_mix_ln0_bwd(const RowArgs& a, const void* x, const void* dout1,
                                    const float* mu0, const float* r0, const float* mu1,
@@ -71,7 +73,17 @@ int max_dynamic_smem_bytes();
 
 // ------------------------------------------------------------------ GEMMs
 enum GemmKind { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
-enum GemmEpi { EPI_STORE = 0, EPI_BIAS = 1, EPI_BIAS_RESID = 2, EPI_RESID = 3 };
+enum GemmEpi { EPI_STORE = 0, EPI_BIAS = 1, EPI_BIAS_RESID = 2, EPI_RESID = 3, EPI_BIAS_ZSTATS = 4 };
+
+// Row statistics of Z = [U | G] in 256-column tiles: for row r and tile j
+// (columns [256 j, 256 j + 256) of the 2H-wide row), zstats[(r * tiles + j)
+// * 4 + {0,1,2,3}] = {mean, M2} of the tile's U columns and {mean, M2} of its
+// G columns, taken from the stored (rounded) Z values.  M2 = sum of squared
+// deviations from the mean.  Written by the GEMM1 epilogue (EPI_BIAS_ZSTATS)
+// or by launch_zstats; merged per row by the gate forward.
+constexpr int kZStatsTile = 256;
+__host__ __device__ inline int zstats_tiles(int H) { return (2 * H + kZStatsTile - 1) / kZStatsTile; }
+cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaStream_t st);
 
 // One grouped GEMM over G groups (the tokens t).  Layouts, all row-major:
 //   FWD:   C[m,g,:] = A[m,g,:] @ Bm[g]        A [M,G,K], Bm [G,K,N], C [M,G,N]
@@ -86,6 +98,8 @@ struct GemmDesc {
   void* C;
   const void* bias;
   const void* resid;
+  float* zstats;  // EPI_BIAS_ZSTATS only
+  int split;      // EPI_BIAS_ZSTATS: first column of the G half (H)
 };
 
 bool gemm_tc_supported(const GemmDesc& d);

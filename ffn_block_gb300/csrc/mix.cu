@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kMaxCluster = 8;
 constexpr int kMaxRows = 8;       // rows per CTA held in registers (T <= 64)
-constexpr int kMixThreads = 320;  // one thread per 16-byte column vector (D/V <= 320)
+constexpr int kMixThreads = 320;  // one thread per 4 columns (D <= 1280)
 constexpr int kMaxMixPartialRows = kMixPartialRowsMax;
 
 __host__ __device__ inline size_t a16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -48,51 +48,76 @@ inline MixGeom mix_geom(int T, int D) {
   return g;
 }
 
-// Writes n consecutive values of row `src_row` (columns d0 .. d0+n-1) into
-// the destination rows of the token mix: column d = i*C + c of row j goes to
-// row i, column j*C + c.  `dst` maps a cluster rank to that CTA's receive
-// buffer [R][D].  Pairs are written as one 2-element store when C is even.
-template <typename E>
-__device__ __forceinline__ void push_mixed(cg::cluster_group& cluster, E* dst_local, const float* vals, int n,
-                                           int d0, int src_row, int C, int D, int R) {
-  if ((C & 1) == 0 && (d0 & 1) == 0 && (n & 1) == 0) {
-    for (int e = 0; e < n; e += 2) {
-      const int d = d0 + e;
-      const int i = d / C, c = d - i * C;
-      const int rank = i / R, il = i - rank * R;
-      E* dst = cluster.map_shared_rank(dst_local, rank) + (size_t)il * D + src_row * C + c;
-      if (sizeof(E) == 4) {
-        float2 p = make_float2(vals[e], vals[e + 1]);
-        *reinterpret_cast<float2*>(dst) = p;
+// Per-thread geometry: thread tid owns columns k0 .. k0+E-1 of every row.
+// For column d = i*C + c (chunk i, offset c) the token mix sends row j's
+// element to row i, column j*C + c; the CTA owning row i is i / R and it is
+// that CTA's local row i % R.  All of this depends on the column only, so it
+// is computed once per thread.
+constexpr int E = 4;
+
+struct ColMap {
+  int chunk[E];    // i = d / C  (also: source row of mixed column d)
+  int off[E];      // c = d % C
+  int rank[E];     // owner CTA of row i
+  int dst[E];      // (i % R) * D + c: destination offset before adding j*C
+};
+
+__device__ __forceinline__ ColMap col_map(int k0, int C, int D, int R) {
+  ColMap m;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int d = k0 + e;
+    const int i = d / C, c = d - i * C;
+    m.chunk[e] = i;
+    m.off[e] = c;
+    m.rank[e] = i / R;
+    m.dst[e] = (i - m.rank[e] * R) * D + c;
+  }
+  return m;
+}
+
+// Writes this thread's E values of source row j into the receive buffers of
+// the rows they belong to after the mix.  Element pairs that share a chunk go
+// as one store (C even).
+template <typename Elt>
+__device__ __forceinline__ void push_row(cg::cluster_group& cluster, Elt* recv, const ColMap& m, const float* vals,
+                                         int j, int C, bool pairs) {
+  if (pairs) {
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      Elt* dst = cluster.map_shared_rank(recv, m.rank[e]) + m.dst[e] + j * C;
+      if (sizeof(Elt) == 4) {
+        *reinterpret_cast<float2*>(dst) = make_float2(vals[e], vals[e + 1]);
       } else {
-        E pair[2] = {from_f<E>(vals[e]), from_f<E>(vals[e + 1])};
-        *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(pair);
+        Elt pr[2] = {from_f<Elt>(vals[e]), from_f<Elt>(vals[e + 1])};
+        *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(pr);
       }
     }
   } else {
-    for (int e = 0; e < n; ++e) {
-      const int d = d0 + e;
-      const int i = d / C, c = d - i * C;
-      const int rank = i / R, il = i - rank * R;
-      E* dst = cluster.map_shared_rank(dst_local, rank) + (size_t)il * D + src_row * C + c;
-      *dst = from_f<E>(vals[e]);
-    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) *(cluster.map_shared_rank(recv, m.rank[e]) + m.dst[e] + j * C) = from_f<Elt>(vals[e]);
   }
+}
+
+// Sum of one value per (row, warp) written by the warps' lane 0.
+__device__ __forceinline__ float row_total(const float* red, int row, int nw) {
+  float s = 0.f;
+  for (int w = 0; w < nw; ++w) s += red[row * nw + w];
+  return s;
 }
 
 // =========================================================================
 // Forward: norm0 -> token mix -> + x -> norm1.  One cluster per sample.
-// Shared memory: xs [R][D] own rows of x, xmix [R][D] received chunks of
-// norm0(x) (storage type), stats of all T rows, row-sum scratch.
+// Shared memory: amix [R][D] fp32 (received chunks of norm0(x)), gamma0 and
+// beta0 as fp32, row-sum scratch [R][nw].
 // =========================================================================
 template <typename T>
 __global__ void __launch_bounds__(kMixThreads) k_mix_fwd(const T* __restrict__ x, const T* __restrict__ g0,
-                                                 const T* __restrict__ be0, const T* __restrict__ g1,
-                                                 const T* __restrict__ be1, T* __restrict__ out1,
-                                                 float* __restrict__ mu0, float* __restrict__ r0,
-                                                 float* __restrict__ mu1, float* __restrict__ r1, int Tn, int D,
-                                                 int C, int R, float eps) {
-  constexpr int V = VecN<T>::value;
+                                                         const T* __restrict__ be0, const T* __restrict__ g1,
+                                                         const T* __restrict__ be1, T* __restrict__ out1,
+                                                         float* __restrict__ mu0, float* __restrict__ r0,
+                                                         float* __restrict__ mu1, float* __restrict__ r1, int Tn,
+                                                         int D, int C, int R, float eps) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char sm[];
   const int CL = (int)cluster.num_blocks();
@@ -101,81 +126,67 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_fwd(const T* __restrict__ x
   const int row0 = rank * R;
   const int nr = max(0, min(Tn, row0 + R) - row0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  T* xs = reinterpret_cast<T*>(sm);
-  float* amix = reinterpret_cast<float*>(sm + a16((size_t)R * D * sizeof(T)));  // [R][D] received norm0(x)
-  float* red = amix + (size_t)R * D;                                             // [R][nw]
-  float* rowv = red + (size_t)R * nw;                                            // [R] per-row values
+  float* amix = reinterpret_cast<float*>(sm);  // [R][D]
+  float* red = amix + (size_t)R * D;           // [R][nw]
   const size_t base = (size_t)b * Tn * D;
-
-  // Own rows of x -> shared memory (16-byte vectors, contiguous block).
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(x + base + (size_t)row0 * D);
-    uint4* dst = reinterpret_cast<uint4*>(xs);
-    const int n16 = (int)((size_t)nr * D * sizeof(T) / 16);
-    for (int q = tid; q < n16; q += blockDim.x) dst[q] = src[q];
-  }
-  // Also makes sure every CTA of the cluster runs before any remote store.
-  cluster.sync();
-  const bool act = tid * V < D;
-  const int k0 = tid * V;
+  const bool act = tid * E < D;
+  const int k0 = tid * E;
   const float invD = 1.0f / (float)D;
+  const bool pairs = (C & 1) == 0;
+  const ColMap cm = col_map(act ? k0 : 0, C, D, R);
+
+  float xv[kMaxRows][E];
+#pragma unroll
+  for (int il = 0; il < kMaxRows; ++il)
+    if (il < nr && act) load_n<T, E>(x + base + (size_t)(row0 + il) * D + k0, xv[il]);
+  cluster.sync();  // every CTA of the cluster runs before any remote store
 
   // norm0 statistics of the own rows: mean, then centred sum of squares.
-  float xv[kMaxRows][V];
 #pragma unroll
   for (int il = 0; il < kMaxRows; ++il) {
     if (il >= nr) break;
     float s = 0.f;
-    if (act) {
-      load_vec(xs + (size_t)il * D + k0, xv[il]);
+    if (act)
 #pragma unroll
-      for (int e = 0; e < V; ++e) s += xv[il][e];
-    }
+      for (int e = 0; e < E; ++e) s += xv[il][e];
     s = warp_sum(s);
     if (lane == 0) red[il * nw + warp] = s;
   }
   __syncthreads();
-  if (tid < nr) {
-    float s = 0.f;
-    for (int w = 0; w < nw; ++w) s += red[tid * nw + w];
-    rowv[tid] = s * invD;
-  }
+  float mean0[kMaxRows];
+#pragma unroll
+  for (int il = 0; il < kMaxRows; ++il) mean0[il] = il < nr ? row_total(red, il, nw) * invD : 0.f;
   __syncthreads();
 #pragma unroll
   for (int il = 0; il < kMaxRows; ++il) {
     if (il >= nr) break;
     float s = 0.f;
-    if (act) {
-      const float m = rowv[il];
+    if (act)
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float c = xv[il][e] - m;
-        s += c * c;
-      }
-    }
+      for (int e = 0; e < E; ++e) s += (xv[il][e] - mean0[il]) * (xv[il][e] - mean0[il]);
     s = warp_sum(s);
     if (lane == 0) red[il * nw + warp] = s;
   }
   __syncthreads();
-  // norm0(x) of the own rows, pushed to the CTAs that own the mixed rows.
+  float gg[E], bb[E];
+  if (act) {
+    load_n<T, E>(g0 + k0, gg);
+    load_n<T, E>(be0 + k0, bb);
+  }
+  // norm0(x) of the own rows, sent to the CTAs that own the mixed rows.
 #pragma unroll
   for (int il = 0; il < kMaxRows; ++il) {
     if (il >= nr) break;
-    float ss = 0.f;
-    for (int w = 0; w < nw; ++w) ss += red[il * nw + w];
-    const float mean = rowv[il];
-    const float rstd = 1.0f / sqrtf(ss * invD + eps);
+    const float rstd = 1.0f / sqrtf(row_total(red, il, nw) * invD + eps);
     if (tid == 0) {
-      mu0[(size_t)b * Tn + row0 + il] = mean;
+      mu0[(size_t)b * Tn + row0 + il] = mean0[il];
       r0[(size_t)b * Tn + row0 + il] = rstd;
     }
     if (act) {
-      float gg[V], bb[V], a[V];
-      load_vec(g0 + k0, gg);
-      load_vec(be0 + k0, bb);
+      float a[E];
 #pragma unroll
-      for (int e = 0; e < V; ++e) a[e] = (xv[il][e] - mean) * rstd * gg[e] + bb[e];
-      push_mixed<float>(cluster, amix, a, V, k0, row0 + il, C, D, R);
+      for (int e = 0; e < E; ++e) a[e] = (xv[il][e] - mean0[il]) * rstd * gg[e] + bb[e];
+      push_row<float>(cluster, amix, cm, a, row0 + il, C, pairs);
     }
   }
   cluster.sync();  // every chunk of the mixed rows has arrived
@@ -186,61 +197,50 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_fwd(const T* __restrict__ x
     if (il >= nr) break;
     float s = 0.f;
     if (act) {
-      const float* am = amix + (size_t)il * D + k0;
+      const float4 am = *reinterpret_cast<const float4*>(amix + (size_t)il * D + k0);
+      xv[il][0] += am.x;
+      xv[il][1] += am.y;
+      xv[il][2] += am.z;
+      xv[il][3] += am.w;
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        xv[il][e] += am[e];
-        s += xv[il][e];
-      }
+      for (int e = 0; e < E; ++e) s += xv[il][e];
     }
     s = warp_sum(s);
     if (lane == 0) red[il * nw + warp] = s;
   }
   __syncthreads();
-  if (tid < nr) {
-    float s = 0.f;
-    for (int w = 0; w < nw; ++w) s += red[tid * nw + w];
-    rowv[tid] = s * invD;
-  }
+#pragma unroll
+  for (int il = 0; il < kMaxRows; ++il) mean0[il] = il < nr ? row_total(red, il, nw) * invD : 0.f;
   __syncthreads();
 #pragma unroll
   for (int il = 0; il < kMaxRows; ++il) {
     if (il >= nr) break;
     float s = 0.f;
-    if (act) {
-      const float m = rowv[il];
+    if (act)
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float c = xv[il][e] - m;
-        s += c * c;
-      }
-    }
+      for (int e = 0; e < E; ++e) s += (xv[il][e] - mean0[il]) * (xv[il][e] - mean0[il]);
     s = warp_sum(s);
     if (lane == 0) red[il * nw + warp] = s;
   }
   __syncthreads();
-  float gg[V], bb[V];
   if (act) {
-    load_vec(g1 + k0, gg);
-    load_vec(be1 + k0, bb);
+    load_n<T, E>(g1 + k0, gg);
+    load_n<T, E>(be1 + k0, bb);
   }
 #pragma unroll
   for (int il = 0; il < kMaxRows; ++il) {
     if (il >= nr) break;
-    float ss = 0.f;
-    for (int w = 0; w < nw; ++w) ss += red[il * nw + w];
-    const float mean = rowv[il];
-    const float rstd = 1.0f / sqrtf(ss * invD + eps);
+    const float rstd = 1.0f / sqrtf(row_total(red, il, nw) * invD + eps);
     const size_t row = (size_t)b * Tn + row0 + il;
     if (tid == 0) {
-      mu1[row] = mean;
+      mu1[row] = mean0[il];
       r1[row] = rstd;
     }
     if (act) {
-      float o[V];
+      float o[E];
 #pragma unroll
-      for (int e = 0; e < V; ++e) o[e] = (xv[il][e] - mean) * rstd * gg[e] + bb[e];
-      store_vec(out1 + row * D + k0, o);
+      for (int e = 0; e < E; ++e) o[e] = (xv[il][e] - mean0[il]) * rstd * gg[e] + bb[e];
+      store_n<T, E>(out1 + row * D + k0, o);
     }
   }
 }
@@ -251,18 +251,16 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_fwd(const T* __restrict__ x
 // its partial sums of dgamma0, dbeta0, dgamma1, dbeta1 in registers and
 // writes one partial row at the end.
 // Shared memory: xs [R][D] own rows of x, xmix [R][D] received chunks of x,
-// da0 [R][D] fp32 received chunks of ds1, statistics, row-sum scratch.
+// da0 [R][D] fp32 received chunks of ds1, gamma0 / beta0 (fp32), statistics
+// of the sample, row-sum scratch [2][R][nw].
 // =========================================================================
 template <typename T>
-__global__ void __launch_bounds__(kMixThreads) k_mix_bwd(const T* __restrict__ x, const T* __restrict__ dout1,
-                                                 const float* __restrict__ mu0, const float* __restrict__ r0,
-                                                 const float* __restrict__ mu1, const float* __restrict__ r1,
-                                                 const T* __restrict__ g0, const T* __restrict__ be0,
-                                                 const T* __restrict__ g1, T* __restrict__ dx,
-                                                 float* __restrict__ pg0, float* __restrict__ pb0,
-                                                 float* __restrict__ pg1, float* __restrict__ pbe1, int B, int Tn,
-                                                 int D, int C, int R, int nclusters) {
-  constexpr int V = VecN<T>::value;
+__global__ void __launch_bounds__(kMixThreads) k_mix_bwd(
+    const T* __restrict__ x, const T* __restrict__ dout1, const float* __restrict__ mu0,
+    const float* __restrict__ r0, const float* __restrict__ mu1, const float* __restrict__ r1,
+    const T* __restrict__ g0, const T* __restrict__ be0, const T* __restrict__ g1, T* __restrict__ dx,
+    float* __restrict__ pg0, float* __restrict__ pb0, float* __restrict__ pg1, float* __restrict__ pbe1, int B,
+    int Tn, int D, int C, int R, int nclusters) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char sm[];
   const int CL = (int)cluster.num_blocks();
@@ -274,77 +272,78 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_bwd(const T* __restrict__ x
   T* xs = reinterpret_cast<T*>(sm);
   T* xmix = reinterpret_cast<T*>(sm + a16((size_t)R * D * sizeof(T)));
   float* da0 = reinterpret_cast<float*>(sm + 2 * a16((size_t)R * D * sizeof(T)));
-  float* s_mu0 = da0 + (size_t)R * D;  // [Tn]
-  float* s_r0 = s_mu0 + Tn;            // [Tn]
-  float* red = s_r0 + Tn;              // [2][R][nw]
-  const bool act = tid * V < D;
-  const int k0 = tid * V;
+  float* sg0 = da0 + (size_t)R * D;  // gamma0 [D]
+  float* sb0 = sg0 + D;              // beta0 [D]
+  float* s_mu0 = sb0 + D;            // [Tn]
+  float* s_r0 = s_mu0 + Tn;          // [Tn]
+  float* red = s_r0 + Tn;            // [2][R][nw]
+  const bool act = tid * E < D;
+  const int k0 = tid * E;
   const float invD = 1.0f / (float)D;
+  const bool pairs = (C & 1) == 0;
+  const ColMap cm = col_map(act ? k0 : 0, C, D, R);
 
-  float gam0[V], gam1[V], ag0[V], ab0[V], ag1[V], ab1[V];
-#pragma unroll
-  for (int e = 0; e < V; ++e) ag0[e] = ab0[e] = ag1[e] = ab1[e] = 0.f;
-  if (act) {
-    load_vec(g0 + k0, gam0);
-    load_vec(g1 + k0, gam1);
+  for (int i = tid; i < D; i += blockDim.x) {
+    sg0[i] = to_f(g0[i]);
+    sb0[i] = to_f(be0[i]);
   }
-  // Per element of a mixed row i (own column k = j*C + c): source row j and
-  // source column i*C + c of norm0.
-  auto a0_of = [&](int i, int e, float xval) {
-    const int k = k0 + e;
-    const int j = k / C, c = k - j * C, d = i * C + c;
-    return (xval - s_mu0[j]) * s_r0[j] * to_f(g0[d]) + to_f(be0[d]);
-  };
-  // xh1 of mixed row i (local il) for this thread's columns.
-  auto xhat1 = [&](int il, int i, float m1, float s1r, float* xh) {
-    float xm[V], xo[V];
-    load_vec(xmix + (size_t)il * D + k0, xm);
-    load_vec(xs + (size_t)il * D + k0, xo);
+  float gam0[E], gam1[E], ag0[E], ab0[E], ag1[E], ab1[E];
 #pragma unroll
-    for (int e = 0; e < V; ++e) xh[e] = (a0_of(i, e, xm[e]) + xo[e] - m1) * s1r;
-  };
+  for (int e = 0; e < E; ++e) ag0[e] = ab0[e] = ag1[e] = ab1[e] = 0.f;
+  if (act) {
+    load_n<T, E>(g0 + k0, gam0);
+    load_n<T, E>(g1 + k0, gam1);
+  }
+  cluster.sync();  // every CTA of the cluster runs before any remote store; sg0/sb0 ready
 
-  cluster.sync();  // every CTA of the cluster runs before any remote store
   for (int b = q; b < B; b += nclusters) {
     const size_t base = (size_t)b * Tn * D;
-    // ---- own rows of x, statistics of the sample.
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(x + base + (size_t)row0 * D);
-      uint4* dst = reinterpret_cast<uint4*>(xs);
-      const int n16 = (int)((size_t)nr * D * sizeof(T) / 16);
-      for (int p = tid; p < n16; p += blockDim.x) dst[p] = src[p];
-      for (int p = tid; p < Tn; p += blockDim.x) {
-        s_mu0[p] = mu0[(size_t)b * Tn + p];
-        s_r0[p] = r0[(size_t)b * Tn + p];
-      }
+    for (int p = tid; p < Tn; p += blockDim.x) {
+      s_mu0[p] = mu0[(size_t)b * Tn + p];
+      s_r0[p] = r0[(size_t)b * Tn + p];
     }
-    __syncthreads();
-    // ---- push the chunks of x the other rows of the mix need; load dout1.
-    float d1[kMaxRows][V];
+    // ---- own rows of x (kept for norm0's backward) sent to the mixed rows;
+    // dout1 of the own rows.
+    float d1[kMaxRows][E];
 #pragma unroll
     for (int il = 0; il < kMaxRows; ++il) {
-      if (il >= nr) break;
+      if (il >= nr) continue;
       if (act) {
-        float xv[V];
-        load_vec(xs + (size_t)il * D + k0, xv);
-        push_mixed<T>(cluster, xmix, xv, V, k0, row0 + il, C, D, R);
-        load_vec(dout1 + base + (size_t)(row0 + il) * D + k0, d1[il]);
+        float xv[E];
+        load_n<T, E>(x + base + (size_t)(row0 + il) * D + k0, xv);
+        store_n<T, E>(xs + (size_t)il * D + k0, xv);
+        push_row<T>(cluster, xmix, cm, xv, row0 + il, C, pairs);
+        load_n<T, E>(dout1 + base + (size_t)(row0 + il) * D + k0, d1[il]);
       }
     }
-    cluster.sync();  // (1) xmix complete
+    cluster.sync();  // (1) xmix complete; s_mu0 / s_r0 visible
+
+    // xh1 of own mixed row i for this thread's columns: element k = j*C + c
+    // is norm0(x)[j, i*C + c] + x[i, k].
+    auto xhat1 = [&](int il, float m1, float s1r, float* xh) {
+      const int i = row0 + il;
+      float xm[E], xo[E];
+      load_n<T, E>(xmix + (size_t)il * D + k0, xm);
+      load_n<T, E>(xs + (size_t)il * D + k0, xo);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int j = cm.chunk[e], d = i * C + cm.off[e];
+        const float a0 = (xm[e] - s_mu0[j]) * s_r0[j] * sg0[d] + sb0[d];
+        xh[e] = (a0 + xo[e] - m1) * s1r;
+      }
+    };
 
     // ---- norm1 backward, sweep 1: row sums of g = gamma1*dout1 and g*xh1.
 #pragma unroll
     for (int il = 0; il < kMaxRows; ++il) {
-      if (il >= nr) break;
-      const int i = row0 + il;
-      const float m1 = mu1[(size_t)b * Tn + i], s1r = r1[(size_t)b * Tn + i];
+      if (il >= nr) continue;
+      const size_t row = (size_t)b * Tn + row0 + il;
       float s0 = 0.f, s1 = 0.f;
       if (act) {
-        float xh[V];
-        xhat1(il, i, m1, s1r, xh);
+        float xh[E];
+        xhat1(il, mu1[row], r1[row], xh);
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
+        for (int e = 0; e < E; ++e) {
           const float g = gam1[e] * d1[il][e];
           s0 += g;
           s1 += g * xh[e];
@@ -359,30 +358,26 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_bwd(const T* __restrict__ x
     }
     __syncthreads();
     // ---- sweep 2: ds1 (kept in registers for the residual), partials, and
-    // the chunks of ds1 pushed to the rows of da0 = token_mix(ds1).
+    // the chunks of ds1 sent to the rows of da0 = token_mix(ds1).
 #pragma unroll
     for (int il = 0; il < kMaxRows; ++il) {
-      if (il >= nr) break;
-      const int i = row0 + il;
-      float t0 = 0.f, t1 = 0.f;
-      for (int w = 0; w < nw; ++w) {
-        t0 += red[(0 * R + il) * nw + w];
-        t1 += red[(1 * R + il) * nw + w];
-      }
-      const float mg = t0 * invD, mgx = t1 * invD;
-      const float m1 = mu1[(size_t)b * Tn + i], s1r = r1[(size_t)b * Tn + i];
+      if (il >= nr) continue;
+      const size_t row = (size_t)b * Tn + row0 + il;
+      const float mg = row_total(red, 0 * R + il, nw) * invD;
+      const float mgx = row_total(red, 1 * R + il, nw) * invD;
+      const float s1r = r1[row];
       if (act) {
-        float xh[V];
-        xhat1(il, i, m1, s1r, xh);
+        float xh[E];
+        xhat1(il, mu1[row], s1r, xh);
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
+        for (int e = 0; e < E; ++e) {
           const float dv = d1[il][e];
           const float g = gam1[e] * dv;
           ag1[e] += dv * xh[e];
           ab1[e] += dv;
           d1[il][e] = s1r * (g - mg - xh[e] * mgx);  // now ds1
         }
-        push_mixed<float>(cluster, da0, d1[il], V, k0, i, C, D, R);
+        push_row<float>(cluster, da0, cm, d1[il], row0 + il, C, pairs);
       }
     }
     cluster.sync();  // (2) da0 complete; every CTA is done reading xmix
@@ -390,19 +385,19 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_bwd(const T* __restrict__ x
     // ---- norm0 backward, sweep 1: row sums of g0 = gamma0*da0 and g0*xh0.
 #pragma unroll
     for (int jl = 0; jl < kMaxRows; ++jl) {
-      if (jl >= nr) break;
+      if (jl >= nr) continue;
       const int j = row0 + jl;
       float s0 = 0.f, s1 = 0.f;
       if (act) {
-        float xo[V];
-        load_vec(xs + (size_t)jl * D + k0, xo);
-        const float* dr = da0 + (size_t)jl * D + k0;
+        float xo[E];
+        load_n<T, E>(xs + (size_t)jl * D + k0, xo);
+        const float4 dr = *reinterpret_cast<const float4*>(da0 + (size_t)jl * D + k0);
+        const float dv[E] = {dr.x, dr.y, dr.z, dr.w};
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const float xh0 = (xo[e] - s_mu0[j]) * s_r0[j];
-          const float g = gam0[e] * dr[e];
+        for (int e = 0; e < E; ++e) {
+          const float g = gam0[e] * dv[e];
           s0 += g;
-          s1 += g * xh0;
+          s1 += g * (xo[e] - s_mu0[j]) * s_r0[j];
         }
       }
       s0 = warp_sum(s0);
@@ -416,27 +411,24 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_bwd(const T* __restrict__ x
     // ---- sweep 2: dx = ds1 + norm0-backward(da0), partials.
 #pragma unroll
     for (int jl = 0; jl < kMaxRows; ++jl) {
-      if (jl >= nr) break;
+      if (jl >= nr) continue;
       const int j = row0 + jl;
-      float t0 = 0.f, t1 = 0.f;
-      for (int w = 0; w < nw; ++w) {
-        t0 += red[(0 * R + jl) * nw + w];
-        t1 += red[(1 * R + jl) * nw + w];
-      }
-      const float mg = t0 * invD, mgx = t1 * invD;
+      const float mg = row_total(red, 0 * R + jl, nw) * invD;
+      const float mgx = row_total(red, 1 * R + jl, nw) * invD;
       if (act) {
-        float xo[V], o[V];
-        load_vec(xs + (size_t)jl * D + k0, xo);
-        const float* dr = da0 + (size_t)jl * D + k0;
+        float xo[E], o[E];
+        load_n<T, E>(xs + (size_t)jl * D + k0, xo);
+        const float4 dr = *reinterpret_cast<const float4*>(da0 + (size_t)jl * D + k0);
+        const float dv[E] = {dr.x, dr.y, dr.z, dr.w};
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
+        for (int e = 0; e < E; ++e) {
           const float xh0 = (xo[e] - s_mu0[j]) * s_r0[j];
-          const float g = gam0[e] * dr[e];
+          const float g = gam0[e] * dv[e];
           o[e] = d1[jl][e] + s_r0[j] * (g - mg - xh0 * mgx);
-          ag0[e] += dr[e] * xh0;
-          ab0[e] += dr[e];
+          ag0[e] += dv[e] * xh0;
+          ab0[e] += dv[e];
         }
-        store_vec(dx + base + (size_t)j * D + k0, o);
+        store_n<T, E>(dx + base + (size_t)j * D + k0, o);
       }
     }
     __syncthreads();  // xs, red and the statistics are reused by the next sample
@@ -444,7 +436,7 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_bwd(const T* __restrict__ x
   if (act) {
     const size_t p = (size_t)blockIdx.x * D + k0;
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
+    for (int e = 0; e < E; ++e) {
       pg0[p + e] = ag0[e];
       pb0[p + e] = ab0[e];
       pg1[p + e] = ag1[e];
@@ -474,19 +466,15 @@ cudaError_t launch_cluster(Kern k, int grid, int threads, size_t smem, int cl, c
   return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
-inline int mix_threads(int D, int dtype) {
-  const int V = dtype == 0 ? 4 : 8;
-  return (D / V + 31) / 32 * 32;
-}
+inline int mix_threads(int D, int /*dtype*/) { return (D / E + 31) / 32 * 32; }
 
-size_t mix_fwd_smem(const MixGeom& g, int dtype, int threads) {
-  const int e = dtype == 0 ? 4 : 2;
-  return a16((size_t)g.R * g.D * e) + (size_t)g.R * g.D * 4 + (size_t)g.R * (threads / 32) * 4 + (size_t)g.R * 4;
+size_t mix_fwd_smem(const MixGeom& g, int /*dtype*/, int threads) {
+  return (size_t)g.R * g.D * 4 + (size_t)g.R * (threads / 32) * 4;
 }
 
 size_t mix_bwd_smem(const MixGeom& g, int dtype, int threads) {
   const int e = dtype == 0 ? 4 : 2;
-  return 2 * a16((size_t)g.R * g.D * e) + (size_t)g.R * g.D * 4 + (size_t)2 * g.T * 4 +
+  return 2 * a16((size_t)g.R * g.D * e) + (size_t)g.R * g.D * 4 + (size_t)2 * g.D * 4 + (size_t)2 * g.T * 4 +
          (size_t)2 * g.R * (threads / 32) * 4;
 }
 
@@ -495,7 +483,7 @@ size_t mix_bwd_smem(const MixGeom& g, int dtype, int threads) {
 bool mix_supported(const RowArgs& a) {
   const MixGeom g = mix_geom(a.T, a.D);
   const int threads = mix_threads(a.D, a.dtype);
-  if (g.R > kMaxRows || threads > kMixThreads) return false;
+  if (g.R > kMaxRows || threads > kMixThreads || a.D % E) return false;
   const size_t lim = (size_t)max_dynamic_smem_bytes();
   return mix_fwd_smem(g, a.dtype, threads) <= lim && mix_bwd_smem(g, a.dtype, threads) <= lim;
 }

@@ -241,110 +241,120 @@ __host__ __device__ inline uint32_t ring_stage_bytes(size_t row_bytes) { return 
 inline size_t ring_smem_bytes(size_t row_bytes) { return (size_t)kRingStages * ring_stage_bytes(row_bytes) + 64; }
 
 // =========================================================================
-// F3: hidden = LN_x(U) * silu(LN_gate(G)), Z = [U | G] per row.  A CTA walks
-// `rpc` consecutive rows; thread v owns columns h = v*V .. v*V+V-1 of both
-// halves, so the product needs no exchange.  Row statistics (from the stored
-// Z values) are merged as (count, mean, M2) in a fixed order: one barrier
-// per row.
+// Z statistics for the FFMA path: one warp per (row, 256-column tile) of
+// Z = [U | G]; {mean, M2} of the tile's U columns and of its G columns, from
+// the stored values (the tensor-core GEMM writes the same numbers from its
+// epilogue).
 // =========================================================================
 template <typename T>
-__global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const T* __restrict__ wx,
-                                                  const T* __restrict__ bx, const T* __restrict__ wg,
-                                                  const T* __restrict__ bg, T* __restrict__ hidden,
-                                                  float* __restrict__ muU, float* __restrict__ rU,
-                                                  float* __restrict__ muG, float* __restrict__ rG,
-                                                  int N, int H, int rpc, float eps, unsigned int* err) {
+__global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* __restrict__ zstats, int N, int H,
+                                                int tiles) {
+  const int lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (item >= (long long)N * tiles) return;
+  const int r = (int)(item / tiles), j = (int)(item - (long long)r * tiles);
+  const T* zr = Z + (size_t)r * 2 * H;
+  float s[2] = {0.f, 0.f}, n[2] = {0.f, 0.f};
+  float v[kZStatsTile / 32];
+#pragma unroll
+  for (int q = 0; q < kZStatsTile / 32; ++q) {
+    const int col = j * kZStatsTile + lane + 32 * q;
+    v[q] = col < 2 * H ? to_f(zr[col]) : 0.f;
+    if (col < 2 * H) {
+      const int h = col < H ? 0 : 1;
+      s[h] += v[q];
+      n[h] += 1.f;
+    }
+  }
+  float mean[2], m2[2] = {0.f, 0.f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float tot = warp_sum(s[h]), cnt = warp_sum(n[h]);
+    mean[h] = cnt > 0.f ? tot / cnt : 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < kZStatsTile / 32; ++q) {
+    const int col = j * kZStatsTile + lane + 32 * q;
+    if (col < 2 * H) {
+      const int h = col < H ? 0 : 1;
+      m2[h] += (v[q] - mean[h]) * (v[q] - mean[h]);
+    }
+  }
+  m2[0] = warp_sum(m2[0]);
+  m2[1] = warp_sum(m2[1]);
+  if (lane == 0)
+    *reinterpret_cast<float4*>(zstats + ((size_t)r * tiles + j) * 4) = make_float4(mean[0], m2[0], mean[1], m2[1]);
+}
+
+// =========================================================================
+// F3: hidden = LN_x(U) * silu(LN_gate(G)), Z = [U | G] per row.  A CTA takes
+// `rpc` rows: first one thread per row merges the row's tile statistics
+// (Chan, Golub and LeVeque's pairwise update, tiles in order) into mean and
+// 1/sqrt(var + eps) of U and G; then thread v handles columns v*V .. v*V+V-1
+// of both halves of every row, so the pass is one read of Z and one write of
+// hidden with no per-row barrier.
+// =========================================================================
+constexpr int kGateRows = 16;
+
+template <typename T>
+__global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
+                                                  const T* __restrict__ wx, const T* __restrict__ bx,
+                                                  const T* __restrict__ wg, const T* __restrict__ bg,
+                                                  T* __restrict__ hidden, float* __restrict__ muU,
+                                                  float* __restrict__ rU, float* __restrict__ muG,
+                                                  float* __restrict__ rG, int N, int H, float eps) {
   constexpr int V = VecN<T>::value;
-  extern __shared__ __align__(16) unsigned char sm[];
-  __shared__ float red[2][32][6];
-  __shared__ int abort_flag;
-  const size_t row_bytes = (size_t)2 * H * sizeof(T);
-  const RowRing ring = ring_setup(sm, ring_stage_bytes(row_bytes), &abort_flag);
-  const int v = threadIdx.x, lane = v & 31, warp = v >> 5, nw = blockDim.x >> 5;
-  const bool act = v * V < H;
-  const int h0 = v * V;
-  float fwx[V], fbx[V], fwg[V], fbg[V];
-  if (act) {
+  __shared__ float st[kGateRows][4];
+  const int r0 = blockIdx.x * kGateRows;
+  const int nrows = min(kGateRows, N - r0);
+  const int tiles = zstats_tiles(H);
+  if ((int)threadIdx.x < nrows) {
+    const int r = r0 + threadIdx.x;
+    Moments u = {0.f, 0.f, 0.f}, g = {0.f, 0.f, 0.f};
+    for (int j = 0; j < tiles; ++j) {
+      const float4 t = *reinterpret_cast<const float4*>(zstats + ((size_t)r * tiles + j) * 4);
+      const int lo = j * kZStatsTile, hi = min(2 * H, lo + kZStatsTile);
+      const float nu = (float)max(0, min(H, hi) - lo);
+      const float ng = (float)max(0, hi - max(H, lo));
+      if (nu > 0.f) u = merge_moments(u, Moments{nu, t.x, t.y});
+      if (ng > 0.f) g = merge_moments(g, Moments{ng, t.z, t.w});
+    }
+    const float rsu = 1.0f / sqrtf(u.m2 / (float)H + eps);
+    const float rsg = 1.0f / sqrtf(g.m2 / (float)H + eps);
+    st[threadIdx.x][0] = u.mean;
+    st[threadIdx.x][1] = rsu;
+    st[threadIdx.x][2] = g.mean;
+    st[threadIdx.x][3] = rsg;
+    muU[r] = u.mean;
+    rU[r] = rsu;
+    muG[r] = g.mean;
+    rG[r] = rsg;
+  }
+  __syncthreads();
+  const int nv = H / V;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const int h0 = v * V;
+    float fwx[V], fbx[V], fwg[V], fbg[V];
     load_vec(wx + h0, fwx);
     load_vec(bx + h0, fbx);
     load_vec(wg + h0, fwg);
     load_vec(bg + h0, fbg);
-  }
-  const int r0 = blockIdx.x * rpc;
-  const int nrows = max(0, min(N, r0 + rpc) - r0);
-  auto issue = [&](int i) {
-    mbar_arrive_expect_tx(ring.bar(i), (uint32_t)row_bytes);
-    bulk_g2s(ring.stage(i), Z + (size_t)(r0 + i) * 2 * H, (uint32_t)row_bytes, ring.bar(i));
-  };
-  int issued = 0;
-  if (v == 0)
-    for (; issued < min(kRingStages, nrows); ++issued) issue(issued);
-  int i = 0;
-  for (; i < nrows; ++i) {
-    mbar_wait_bounded(ring.bar(i), (uint32_t)(i / kRingStages) & 1u, kRowWaitLimitNs, err, ERRBIT_WAIT_PRODUCER,
-                      &abort_flag);
-    const unsigned char* st = sm + (size_t)(i % kRingStages) * ring.stage_bytes;
-    float u[V], g[V];
-    Moments mu = {0.f, 0.f, 0.f}, mg = {0.f, 0.f, 0.f};
-    if (act) {
-      load_vec(reinterpret_cast<const T*>(st) + h0, u);
-      load_vec(reinterpret_cast<const T*>(st) + H + h0, g);
-      float su = 0.f, sg = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < nrows; ++i) {
+      const T* zr = Z + (size_t)(r0 + i) * 2 * H;
+      float u[V], g[V], o[V];
+      load_vec(zr + h0, u);
+      load_vec(zr + H + h0, g);
+      const float mU = st[i][0], sU = st[i][1], mG = st[i][2], sG = st[i][3];
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        su += u[e];
-        sg += g[e];
-      }
-      mu.n = mg.n = (float)V;
-      mu.mean = su * (1.0f / V);
-      mg.mean = sg * (1.0f / V);
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float a = u[e] - mu.mean, c = g[e] - mg.mean;
-        mu.m2 += a * a;
-        mg.m2 += c * c;
-      }
-    }
-    mu = warp_merge_moments(mu);
-    mg = warp_merge_moments(mg);
-    const int slot = i & 1;
-    if (lane == 0) {
-      red[slot][warp][0] = mu.n; red[slot][warp][1] = mu.mean; red[slot][warp][2] = mu.m2;
-      red[slot][warp][3] = mg.n; red[slot][warp][4] = mg.mean; red[slot][warp][5] = mg.m2;
-    }
-    __syncthreads();
-    if (abort_flag) break;
-    if (v == 0 && issued < nrows) {
-      fence_proxy_async_smem();
-      issue(issued++);
-    }
-    Moments tu = {red[slot][0][0], red[slot][0][1], red[slot][0][2]};
-    Moments tg = {red[slot][0][3], red[slot][0][4], red[slot][0][5]};
-    for (int w = 1; w < nw; ++w) {
-      tu = merge_moments(tu, Moments{red[slot][w][0], red[slot][w][1], red[slot][w][2]});
-      tg = merge_moments(tg, Moments{red[slot][w][3], red[slot][w][4], red[slot][w][5]});
-    }
-    const float rsU = 1.0f / sqrtf(tu.m2 / (float)H + eps);
-    const float rsG = 1.0f / sqrtf(tg.m2 / (float)H + eps);
-    const size_t r = (size_t)r0 + i;
-    if (act) {
-      float o[V];
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float uu = (u[e] - tu.mean) * rsU * fwx[e] + fbx[e];
-        const float gg = (g[e] - tg.mean) * rsG * fwg[e] + fbg[e];
+        const float uu = (u[e] - mU) * sU * fwx[e] + fbx[e];
+        const float gg = (g[e] - mG) * sG * fwg[e] + fbg[e];
         o[e] = uu * (gg / (1.0f + expf(-gg)));
       }
-      store_vec(hidden + r * H + h0, o);
-    }
-    if (v == 0) {
-      muU[r] = tu.mean;
-      rU[r] = rsU;
-      muG[r] = tg.mean;
-      rG[r] = rsG;
+      store_vec(hidden + (size_t)(r0 + i) * H + h0, o);
     }
   }
-  if (abort_flag) ring_drain(ring, i, issued, err);
 }
 
 // =========================================================================
@@ -442,124 +452,138 @@ __global__ void __launch_bounds__(512) k_ln2_bwd(const T* __restrict__ dy, const
 }
 
 // =========================================================================
-// G4: backward of hidden = LN_x(U) * silu(LN_gate(G)).  CTA (bblk, t);
-// thread v owns columns h = v*V ... of both halves.  With Uh, Gh the
+// G4: backward of hidden = LN_x(U) * silu(LN_gate(G)).  With Uh, Gh the
 // normalised halves, u = wx*Uh + bx, g = wg*Gh + bg, s = sigmoid(g):
 //   du = dh * g * s,  dg = dh * u * s * (1 + g * (1 - s)),
 //   gU = wx * du,     gG = wg * dg,
 //   dU = rU * (gU - mean(gU) - Uh * mean(gU * Uh)), same for dG,
-//   dZ = [dU | dG];   partials: dwx += du*Uh, dbx += du, dwg += dg*Gh,
-//   dbg += dg, db1[t] += dZ.
-// Rows stream through the shared-memory ring (dh row, then the Z row).
+//   dZ = [dU | dG];   dwx += du*Uh, dbx += du, dwg += dg*Gh, dbg += dg,
+//   db1[t] += dZ.
+// Two streaming passes: (1) one warp per row takes the four row sums
+// (sum gU, sum gU*Uh, sum gG, sum gG*Gh); (2) CTA (bblk, t), thread v owns
+// columns v*V ... of both halves for every row of its block, writes dZ and
+// keeps the column partial sums in registers.  No per-row barrier.
 // =========================================================================
-template <typename T>
-__global__ void __launch_bounds__(512) k_gate_bwd(
-    const T* __restrict__ dh, const T* __restrict__ Z, const float* __restrict__ muU,
-    const float* __restrict__ rU, const float* __restrict__ muG, const float* __restrict__ rG,
-    const T* __restrict__ wx, const T* __restrict__ bx, const T* __restrict__ wg,
-    const T* __restrict__ bg, T* __restrict__ dZ, float* __restrict__ pwx, float* __restrict__ pbx,
-    float* __restrict__ pwg, float* __restrict__ pbg, float* __restrict__ pb1, int B, int Tn, int H,
-    int nb, unsigned int* err) {
-  constexpr int V = VecN<T>::value;
-  extern __shared__ __align__(16) unsigned char sm[];
-  __shared__ float red[2 * 32 * 4];
-  __shared__ int abort_flag;
-  const size_t hb = (size_t)H * sizeof(T);
-  const RowRing ring = ring_setup(sm, ring_stage_bytes(3 * hb), &abort_flag);
-  int slot = 0;
-  const int bblk = blockIdx.x, t = blockIdx.y;
-  const int v = threadIdx.x;
-  const bool act = v * V < H;
-  const int h0 = v * V;
-  float fwx[V], fbx[V], fwg[V], fbg[V];
-  float awx[V], abx[V], awg[V], abg[V], a1u[V], a1g[V];
+template <int E>
+__device__ __forceinline__ void gate_bwd_elem(const float* dhv, const float* zu, const float* zg, float mU, float sU,
+                                              float mG, float sG, const float* fwx, const float* fbx,
+                                              const float* fwg, const float* fbg, float* Uh, float* Gh, float* du,
+                                              float* dg) {
 #pragma unroll
-  for (int e = 0; e < V; ++e) awx[e] = abx[e] = awg[e] = abg[e] = a1u[e] = a1g[e] = 0.f;
-  if (act) {
+  for (int e = 0; e < E; ++e) {
+    Uh[e] = (zu[e] - mU) * sU;
+    Gh[e] = (zg[e] - mG) * sG;
+    const float u = fwx[e] * Uh[e] + fbx[e];
+    const float g = fwg[e] * Gh[e] + fbg[e];
+    const float sg = 1.0f / (1.0f + expf(-g));
+    du[e] = dhv[e] * (g * sg);
+    dg[e] = dhv[e] * u * (sg * (1.0f + g * (1.0f - sg)));
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_gate_bwd_rowsums(
+    const T* __restrict__ dh, const T* __restrict__ Z, const float* __restrict__ muU, const float* __restrict__ rU,
+    const float* __restrict__ muG, const float* __restrict__ rG, const T* __restrict__ wx,
+    const T* __restrict__ bx, const T* __restrict__ wg, const T* __restrict__ bg, float* __restrict__ rowsum, int N,
+    int H) {
+  constexpr int V = VecN<T>::value;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= N) return;
+  const float mU = muU[r], sU = rU[r], mG = muG[r], sG = rG[r];
+  const T* dhr = dh + (size_t)r * H;
+  const T* zr = Z + (size_t)r * 2 * H;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const int nv = H / V;
+#pragma unroll 2
+  for (int v = lane; v < nv; v += 32) {
+    const int h0 = v * V;
+    float dhv[V], zu[V], zg[V], fwx[V], fbx[V], fwg[V], fbg[V];
+    load_vec(dhr + h0, dhv);
+    load_vec(zr + h0, zu);
+    load_vec(zr + H + h0, zg);
     load_vec(wx + h0, fwx);
     load_vec(bx + h0, fbx);
     load_vec(wg + h0, fwg);
     load_vec(bg + h0, fbg);
-  }
-  const float invH = 1.0f / (float)H;
-  const int b0 = bblk * nb;
-  const int nrows = max(0, min(B, b0 + nb) - b0);
-  auto issue = [&](int i) {
-    const size_t r = (size_t)(b0 + i) * Tn + t;
-    mbar_arrive_expect_tx(ring.bar(i), (uint32_t)(3 * hb));
-    bulk_g2s(ring.stage(i), dh + r * H, (uint32_t)hb, ring.bar(i));
-    bulk_g2s(ring.stage(i) + (uint32_t)hb, Z + r * 2 * H, (uint32_t)(2 * hb), ring.bar(i));
-  };
-  int issued = 0;
-  if (v == 0)
-    for (; issued < min(kRingStages, nrows); ++issued) issue(issued);
-  int i = 0;
-  for (; i < nrows; ++i) {
-    mbar_wait_bounded(ring.bar(i), (uint32_t)(i / kRingStages) & 1u, kRowWaitLimitNs, err, ERRBIT_WAIT_PRODUCER,
-                      &abort_flag);
-    const T* st = reinterpret_cast<const T*>(sm + (size_t)(i % kRingStages) * ring.stage_bytes);
-    const size_t r = (size_t)(b0 + i) * Tn + t;
-    const float mU = muU[r], sU = rU[r], mG = muG[r], sG = rG[r];
-    float Uh[V], Gh[V], gU[V], gG[V], du[V], dg[V];
-    float sums[4] = {0.f, 0.f, 0.f, 0.f};
-    if (act) {
-      float dhv[V], zu[V], zg[V];
-      load_vec(st + h0, dhv);
-      load_vec(st + H + h0, zu);
-      load_vec(st + 2 * H + h0, zg);
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        Uh[e] = (zu[e] - mU) * sU;
-        Gh[e] = (zg[e] - mG) * sG;
-        const float u = fwx[e] * Uh[e] + fbx[e];
-        const float g = fwg[e] * Gh[e] + fbg[e];
-        const float sg = 1.0f / (1.0f + expf(-g));
-        du[e] = dhv[e] * (g * sg);
-        dg[e] = dhv[e] * u * (sg * (1.0f + g * (1.0f - sg)));
-        gU[e] = fwx[e] * du[e];
-        gG[e] = fwg[e] * dg[e];
-        sums[0] += gU[e];
-        sums[1] += gU[e] * Uh[e];
-        sums[2] += gG[e];
-        sums[3] += gG[e] * Gh[e];
-      }
-    }
-    block_sum<4>(sums, red, slot);
-    if (abort_flag) break;
-    if (v == 0 && issued < nrows) {
-      fence_proxy_async_smem();
-      issue(issued++);
-    }
-    if (act) {
-      const float m0 = sums[0] * invH, m1 = sums[1] * invH, m2 = sums[2] * invH, m3 = sums[3] * invH;
-      float oU[V], oG[V];
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        oU[e] = sU * (gU[e] - m0 - Uh[e] * m1);
-        oG[e] = sG * (gG[e] - m2 - Gh[e] * m3);
-        awx[e] += du[e] * Uh[e];
-        abx[e] += du[e];
-        awg[e] += dg[e] * Gh[e];
-        abg[e] += dg[e];
-        a1u[e] += oU[e];
-        a1g[e] += oG[e];
-      }
-      store_vec(dZ + r * 2 * H + h0, oU);
-      store_vec(dZ + r * 2 * H + H + h0, oG);
-    }
-  }
-  if (abort_flag) ring_drain(ring, i, issued, err);
-  if (act) {
-    const size_t p = (size_t)bblk * Tn + t;
+    float Uh[V], Gh[V], du[V], dg[V];
+    gate_bwd_elem<V>(dhv, zu, zg, mU, sU, mG, sG, fwx, fbx, fwg, fbg, Uh, Gh, du, dg);
 #pragma unroll
     for (int e = 0; e < V; ++e) {
-      pwx[p * H + h0 + e] = awx[e];
-      pbx[p * H + h0 + e] = abx[e];
-      pwg[p * H + h0 + e] = awg[e];
-      pbg[p * H + h0 + e] = abg[e];
-      pb1[p * 2 * H + h0 + e] = a1u[e];
-      pb1[p * 2 * H + H + h0 + e] = a1g[e];
+      const float gU = fwx[e] * du[e], gG = fwg[e] * dg[e];
+      a0 += gU;
+      a1 += gU * Uh[e];
+      a2 += gG;
+      a3 += gG * Gh[e];
     }
+  }
+  a0 = warp_sum(a0);
+  a1 = warp_sum(a1);
+  a2 = warp_sum(a2);
+  a3 = warp_sum(a3);
+  if (lane == 0) *reinterpret_cast<float4*>(rowsum + (size_t)r * 4) = make_float4(a0, a1, a2, a3);
+}
+
+// Thread owns E = 4 columns of each half (8-byte accesses for 16-bit types)
+// so the six column partial sums fit in registers at good occupancy;
+// blockIdx.z picks which part of the H columns the CTA covers.
+template <typename T>
+__global__ void __launch_bounds__(512) k_gate_bwd_apply(
+    const T* __restrict__ dh, const T* __restrict__ Z, const float* __restrict__ muU, const float* __restrict__ rU,
+    const float* __restrict__ muG, const float* __restrict__ rG, const float* __restrict__ rowsum,
+    const T* __restrict__ wx, const T* __restrict__ bx, const T* __restrict__ wg, const T* __restrict__ bg,
+    T* __restrict__ dZ, float* __restrict__ pwx, float* __restrict__ pbx, float* __restrict__ pwg,
+    float* __restrict__ pbg, float* __restrict__ pb1, int B, int Tn, int H, int nb) {
+  constexpr int E = 4;
+  const int bblk = blockIdx.x, t = blockIdx.y;
+  const int h0 = (blockIdx.z * blockDim.x + threadIdx.x) * E;
+  if (h0 >= H) return;
+  const float invH = 1.0f / (float)H;
+  float fwx[E], fbx[E], fwg[E], fbg[E];
+  load_n<T, E>(wx + h0, fwx);
+  load_n<T, E>(bx + h0, fbx);
+  load_n<T, E>(wg + h0, fwg);
+  load_n<T, E>(bg + h0, fbg);
+  float awx[E], abx[E], awg[E], abg[E], a1u[E], a1g[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) awx[e] = abx[e] = awg[e] = abg[e] = a1u[e] = a1g[e] = 0.f;
+  const int b_end = min(B, (bblk + 1) * nb);
+#pragma unroll 2
+  for (int b = bblk * nb; b < b_end; ++b) {
+    const size_t r = (size_t)b * Tn + t;
+    float dhv[E], zu[E], zg[E];
+    load_n<T, E>(dh + r * H + h0, dhv);
+    load_n<T, E>(Z + r * 2 * H + h0, zu);
+    load_n<T, E>(Z + r * 2 * H + H + h0, zg);
+    const float4 rs = *reinterpret_cast<const float4*>(rowsum + r * 4);
+    const float sU = rU[r], sG = rG[r];
+    float Uh[E], Gh[E], du[E], dg[E], oU[E], oG[E];
+    gate_bwd_elem<E>(dhv, zu, zg, muU[r], sU, muG[r], sG, fwx, fbx, fwg, fbg, Uh, Gh, du, dg);
+    const float m0 = rs.x * invH, m1 = rs.y * invH, m2 = rs.z * invH, m3 = rs.w * invH;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      oU[e] = sU * (fwx[e] * du[e] - m0 - Uh[e] * m1);
+      oG[e] = sG * (fwg[e] * dg[e] - m2 - Gh[e] * m3);
+      awx[e] += du[e] * Uh[e];
+      abx[e] += du[e];
+      awg[e] += dg[e] * Gh[e];
+      abg[e] += dg[e];
+      a1u[e] += oU[e];
+      a1g[e] += oG[e];
+    }
+    store_n<T, E>(dZ + r * 2 * H + h0, oU);
+    store_n<T, E>(dZ + r * 2 * H + H + h0, oG);
+  }
+  const size_t p = (size_t)bblk * Tn + t;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    pwx[p * H + h0 + e] = awx[e];
+    pbx[p * H + h0 + e] = abx[e];
+    pwg[p * H + h0 + e] = awg[e];
+    pbg[p * H + h0 + e] = abg[e];
+    pb1[p * 2 * H + h0 + e] = a1u[e];
+    pb1[p * 2 * H + H + h0 + e] = a1g[e];
   }
 }
 
@@ -856,24 +880,26 @@ cudaError_t launch_ln_rows_fwd(const RowArgs& a, const void* s, const void* g, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const void* wx, const void* bx,
-                            const void* wg, const void* bg, void* hidden, float* muU, float* rU,
-                            float* muG, float* rG, cudaStream_t st) {
+cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaStream_t st) {
   const int N = a.B * a.T;
-  const int threads = round32(a.H / vec_elems(a.dtype));
-  if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
-  const int rpc = 64;
-  const int grid = (N + rpc - 1) / rpc;
-  const size_t smem = ring_smem_bytes((size_t)2 * a.H * elem_bytes(a.dtype));
-  cudaError_t err = cudaSuccess;
+  const int tiles = zstats_tiles(a.H);
+  const long long items = (long long)N * tiles;
+  const int grid = (int)((items + 7) / 8);
+  RMX_DISPATCH_T(a.dtype, { k_zstats<T><<<grid, 256, 0, st>>>((const T*)Z, zstats, N, a.H, tiles); });
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, const void* wx,
+                            const void* bx, const void* wg, const void* bg, void* hidden, float* muU,
+                            float* rU, float* muG, float* rG, cudaStream_t st) {
+  const int N = a.B * a.T;
+  int threads = round32(a.H / vec_elems(a.dtype));
+  if (threads > kRowThreadsMax) threads = kRowThreadsMax;
+  const int grid = (N + kGateRows - 1) / kGateRows;
   RMX_DISPATCH_T(a.dtype, {
-    auto k = k_gate_fwd<T>;
-    err = set_smem(k, smem);
-    if (err == cudaSuccess)
-      k<<<grid, threads, smem, st>>>((const T*)Z, (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg,
-                                     (T*)hidden, muU, rU, muG, rG, N, a.H, rpc, 1e-5f, device_error_word());
+    k_gate_fwd<T><<<grid, threads, 0, st>>>((const T*)Z, zstats, (const T*)wx, (const T*)bx, (const T*)wg,
+                                            (const T*)bg, (T*)hidden, muU, rU, muG, rG, N, a.H, 1e-5f);
   });
-  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -899,21 +925,25 @@ cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, con
 cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU,
                             const float* rU, const float* muG, const float* rG, const void* wx,
                             const void* bx, const void* wg, const void* bg, void* dZ, float* pwx,
-                            float* pbx, float* pwg, float* pbg, float* pb1, cudaStream_t st) {
+                            float* pbx, float* pwg, float* pbg, float* pb1, float* rowsum, cudaStream_t st) {
   const int threads = round32(a.H / vec_elems(a.dtype));
   if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
-  dim3 grid(a.nbblk, a.T);
-  const size_t smem = ring_smem_bytes((size_t)3 * a.H * elem_bytes(a.dtype));
-  cudaError_t err = cudaSuccess;
+  const int N = a.B * a.T;
   RMX_DISPATCH_T(a.dtype, {
-    auto k = k_gate_bwd<T>;
-    err = set_smem(k, smem);
-    if (err == cudaSuccess)
-      k<<<grid, threads, smem, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, (const T*)wx, (const T*)bx,
-                                     (const T*)wg, (const T*)bg, (T*)dZ, pwx, pbx, pwg, pbg, pb1, a.B, a.T, a.H,
-                                     a.nb, device_error_word());
+    k_gate_bwd_rowsums<T><<<(N + 7) / 8, 256, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, (const T*)wx,
+                                                       (const T*)bx, (const T*)wg, (const T*)bg, rowsum, N, a.H);
   });
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  // Apply pass: 4 columns per thread, at most 256 threads per CTA.
+  const int quads = a.H / 4;
+  const int athreads = quads < 256 ? round32(quads) : 256;
+  dim3 grid(a.nbblk, a.T, (quads + athreads - 1) / athreads);
+  RMX_DISPATCH_T(a.dtype, {
+    k_gate_bwd_apply<T><<<grid, athreads, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, rowsum,
+                                                   (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg, (T*)dZ,
+                                                   pwx, pbx, pwg, pbg, pb1, a.B, a.T, a.H, a.nb);
+  });
   return cudaGetLastError();
 }
 
