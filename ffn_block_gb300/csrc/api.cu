@@ -55,9 +55,9 @@ inline int esize(int dtype) { return dtype == RMX_F32 ? 4 : 2; }
 // ------------------------------------------------------------------ layouts
 struct Layout {
   // saved (filled by the forward)
-  size_t out1, Z, hidden, s2, stats, zstats, saved_total;
+  size_t out1, Z, hidden, s2, stats, zstats, mix0, saved_total;
   // backward scratch
-  size_t ds2, dh, dZ, dout1, ds1, rowsum, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
+  size_t ds2, dh, dZ, dout1, ds1, da0, rowsum, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
   RowArgs ra;
 };
 
@@ -82,6 +82,7 @@ Layout layout_of(const rmx_config& c) {
   L.s2 = o; o = up(o + N * D * e);
   L.stats = o; o = up(o + 10 * N * sizeof(float));
   L.zstats = o; o = up(o + N * (size_t)zstats_tiles(c.H) * 4 * sizeof(float));  // forward scratch
+  L.mix0 = o; o = up(o + N * D * e);  // token_mix(norm0(x)), read again by norm1's backward
   L.saved_total = o;
 
   L.ra.B = c.B;
@@ -100,7 +101,8 @@ Layout layout_of(const rmx_config& c) {
   L.dh = o; o = up(o + N * H * e);
   L.dZ = o; o = up(o + N * 2 * H * e);
   L.dout1 = o; o = up(o + N * D * e);
-  L.ds1 = o; o = up(o + N * D * sizeof(float));
+  L.ds1 = o; o = up(o + N * D * e);
+  L.da0 = o; o = up(o + N * D * e);
   L.rowsum = o; o = up(o + N * 4 * sizeof(float));
   L.pg2 = o; o = up(o + P * D * sizeof(float));
   L.pb2 = o; o = up(o + P * D * sizeof(float));
@@ -110,13 +112,10 @@ Layout layout_of(const rmx_config& c) {
   L.pwg = o; o = up(o + P * H * sizeof(float));
   L.pbg = o; o = up(o + P * H * sizeof(float));
   L.pb1 = o; o = up(o + P * 2 * H * sizeof(float));
-  // norm0/norm1 partial rows: one per sample (generic pass) or one per CTA
-  // of the cluster pass (at most kMixPartialRowsMax).
-  const size_t P01 = (size_t)(c.B > kMixPartialRowsMax ? c.B : kMixPartialRowsMax);
-  L.pg0 = o; o = up(o + P01 * D * sizeof(float));
-  L.pb0 = o; o = up(o + P01 * D * sizeof(float));
-  L.pg1 = o; o = up(o + P01 * D * sizeof(float));
-  L.pbe1 = o; o = up(o + P01 * D * sizeof(float));
+  L.pg0 = o; o = up(o + P * D * sizeof(float));
+  L.pb0 = o; o = up(o + P * D * sizeof(float));
+  L.pg1 = o; o = up(o + P * D * sizeof(float));
+  L.pbe1 = o; o = up(o + P * D * sizeof(float));
   L.ws_total = o;
   return L;
 }
@@ -126,8 +125,7 @@ rmx_status kernels_support(const rmx_config& c) {
   const int V = 16 / esize(c.dtype);
   if (c.D % V || c.H % V) return RMX_ERR_UNSUPPORTED;  // rows must be whole 16-byte vectors
   if (c.D / V > kRowThreadsMax || c.H / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
-  if ((c.D + 31) / 32 > 40) return RMX_ERR_UNSUPPORTED;  // norm0/norm1: 40 values per lane
-  if ((c.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // norm2: 10 vectors per lane
+  if ((c.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // LN forward: 10 vectors per lane
   return RMX_OK;
 }
 
@@ -260,14 +258,14 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   void* hidden = at(saved, L.hidden);
   void* s2 = at(saved, L.s2);
   Stats S = stats_of(saved, L, N);
-  if (mix_supported(L.ra)) {
-    Launch l("ln0_mix_ln1_fwd", st);
-    RMX_TRY(l.done(launch_mix_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, out1, S.mu0, S.r0, S.mu1, S.r1,
-                                  st)));
-  } else {
-    Launch l("ln0_mix_ln1_fwd", st);
-    RMX_TRY(l.done(launch_ln0_mix_ln1_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, out1, S.mu0, S.r0,
-                                          S.mu1, S.r1, st)));
+  void* mix0 = at(saved, L.mix0);
+  {
+    Launch l("ln0_fwd_mixed", st);
+    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_MIXED_OUT, x, nullptr, p.gamma0, p.beta0, mix0, S.mu0, S.r0, st)));
+  }
+  {
+    Launch l("ln1_fwd", st);
+    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_SUM_IN, mix0, x, p.gamma1, p.beta1, out1, S.mu1, S.r1, st)));
   }
   float* zstats = reinterpret_cast<float*>(at(saved, L.zstats));
   {
@@ -291,7 +289,7 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   }
   {
     Launch l("ln2_fwd", st);
-    RMX_TRY(l.done(launch_ln_rows_fwd(L.ra, s2, p.gamma2, p.beta2, y, S.mu2, S.r2, st)));
+    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_PLAIN, s2, nullptr, p.gamma2, p.beta2, y, S.mu2, S.r2, st)));
   }
   return RMX_OK;
 }
@@ -309,7 +307,9 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   void* dh = at(ws, L.dh);
   void* dZ = at(ws, L.dZ);
   void* dout1 = at(ws, L.dout1);
-  float* ds1 = reinterpret_cast<float*>(at(ws, L.ds1));
+  void* ds1 = at(ws, L.ds1);
+  void* da0 = at(ws, L.da0);
+  const void* mix0 = at(saved, L.mix0);
   auto F = [&](size_t off) { return reinterpret_cast<float*>(at(ws, off)); };
 
   {
@@ -337,16 +337,15 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm1_wgrad", d, st));
   }
-  int P01 = c.B;
-  if (mix_supported(L.ra)) {
-    P01 = mix_bwd_partial_rows(L.ra);
-    Launch l("ln1_mix_ln0_bwd", st);
-    RMX_TRY(l.done(launch_mix_bwd(L.ra, x, dout1, S.mu0, S.r0, S.mu1, S.r1, p.gamma0, p.beta0, p.gamma1, dx,
-                                  F(L.pg0), F(L.pb0), F(L.pg1), F(L.pbe1), st)));
-  } else {
-    Launch l("ln1_mix_ln0_bwd", st);
-    RMX_TRY(l.done(launch_ln1_mix_ln0_bwd(L.ra, x, dout1, S.mu0, S.r0, S.mu1, S.r1, p.gamma0, p.beta0,
-                                          p.gamma1, ds1, dx, F(L.pg0), F(L.pb0), F(L.pg1), F(L.pbe1), st)));
+  {
+    Launch l("ln1_bwd_mixed", st);
+    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_MIXED_TOO, dout1, mix0, x, S.mu1, S.r1, p.gamma1, nullptr, ds1, da0,
+                                 F(L.pg1), F(L.pbe1), nullptr, st)));
+  }
+  {
+    Launch l("ln0_bwd", st);
+    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_RESID, da0, x, nullptr, S.mu0, S.r0, p.gamma0, ds1, dx, nullptr,
+                                 F(L.pg0), F(L.pb0), nullptr, st)));
   }
   {
     const int P = L.ra.nbblk * c.T, Pb = L.ra.nbblk;
@@ -355,8 +354,8 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
         {F(L.pbo), g.bout, Pb, c.T * c.D},     {F(L.pwx), g.lnx_w, P, c.H},
         {F(L.pbx), g.lnx_b, P, c.H},           {F(L.pwg), g.lng_w, P, c.H},
         {F(L.pbg), g.lng_b, P, c.H},           {F(L.pb1), g.b1, Pb, c.T * 2 * c.H},
-        {F(L.pg1), g.gamma1, P01, c.D},        {F(L.pbe1), g.beta1, P01, c.D},
-        {F(L.pg0), g.gamma0, P01, c.D},        {F(L.pb0), g.beta0, P01, c.D},
+        {F(L.pg1), g.gamma1, P, c.D},          {F(L.pbe1), g.beta1, P, c.D},
+        {F(L.pg0), g.gamma0, P, c.D},          {F(L.pb0), g.beta0, P, c.D},
     };
     Launch l("colsums", st);
     cudaError_t e = launch_colsums(jobs, 12, c.dtype, st);
@@ -408,8 +407,6 @@ rmx_status rmx_forward(const rmx_config* cfg, const void* x, const rmx_params* p
   const Layout L = layout_of(*cfg);
   if (saved_bytes < L.saved_total) return RMX_ERR_WORKSPACE;
   RMX_TRY(kernels_support(*cfg));
-  RowArgs ra = L.ra;
-  if (per_sample_smem_bytes(ra) > (size_t)max_dynamic_smem_bytes()) return RMX_ERR_UNSUPPORTED;
   return forward_impl(*cfg, x, *params, saved, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -429,7 +426,6 @@ rmx_status rmx_backward(const rmx_config* cfg, const void* x, const void* dy, co
   const Layout L = layout_of(*cfg);
   if (saved_bytes < L.saved_total || ws_bytes < L.ws_total) return RMX_ERR_WORKSPACE;
   RMX_TRY(kernels_support(*cfg));
-  if (per_sample_smem_bytes(L.ra) > (size_t)max_dynamic_smem_bytes()) return RMX_ERR_UNSUPPORTED;
   return backward_impl(*cfg, x, dy, saved, *params, dx, *grads, ws, st);
 }
 

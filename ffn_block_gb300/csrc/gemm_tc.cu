@@ -15,8 +15,9 @@
 //              back to the producer by tcgen05.commit on its `empty` barrier;
 //              the accumulator alternates between two 256-column TMEM halves
 //              so the epilogue of tile i overlaps the main loop of tile i+1;
-//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, add
-//              bias / residual in fp32, round to the storage type, store.
+//   warps 2-9  epilogue: two warps per TMEM lane quarter, each draining half
+//              of the tile's columns with tcgen05.ld (32 lanes x 32 columns at
+//              a time); bias / residual in fp32, rounding, store.
 // Paired mode (M spans at least two tiles): a cluster of two CTAs computes
 // the two M-adjacent tiles that share one B tile.  Each CTA loads its own A
 // tile and half of the B tile, multicasting that half into both CTAs' shared
@@ -51,7 +52,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KB
 constexpr int MN_CHUNK_BYTES = BK * 128;       // one 64-wide MN chunk of an MN-major tile
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * BN;        // 512
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter
+constexpr int THREADS = 64 + 32 * EPI_WARPS;   // producer, MMA, epilogue
 constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
@@ -70,7 +72,7 @@ struct Params {
   unsigned int* err;
   unsigned long long wait_limit_ns;
   float* zstats;  // EPI_BIAS_ZSTATS
-  int split;
+  int split, zgroups;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -232,9 +234,14 @@ __device__ __forceinline__ void pair_tile_coords(const Params& p, int pt, int ra
   n0 = tn * BN;
 }
 
+// Shifted sums of one half of a Z row over one column group.
+struct ZSums {
+  float n, k, s, q;  // count, shift, sum(x - k), sum((x - k)^2)
+};
+
 template <typename T, int EPI>
 __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, int n_base, const float* v,
-                                               Moments* zst) {
+                                               ZSums* zs) {
   constexpr int V = VecN<T>::value;
   T* orow = reinterpret_cast<T*>(p.out) + (size_t)g * p.out_gs + (size_t)m * p.out_rs;
 #pragma unroll
@@ -258,20 +265,25 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, in
       }
       store_vec(orow + n, o);
       if (EPI == EPI_BIAS_ZSTATS) {
-        // Exact moments of the V stored (rounded) values, merged into the
-        // running moments of their half (vectors never straddle the split).
-        float r[V], sum = 0.f;
+        // Shifted sums of the stored (rounded) values of this half: the
+        // shift is the half's first value in this column group, so the
+        // centred second moment is formed without cancellation trouble.
+        float r[V];
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          r[e] = to_f(from_f<T>(o[e]));
-          sum += r[e];
-        }
-        const float mean = sum * (1.0f / V);
-        float m2 = 0.f;
+        for (int e = 0; e < V; ++e) r[e] = to_f(from_f<T>(o[e]));
+        // Constant indices only, so the sums stay in registers.
+        auto add = [&](ZSums& z) {
+          if (z.n == 0.f) z.k = r[0];
 #pragma unroll
-        for (int e = 0; e < V; ++e) m2 += (r[e] - mean) * (r[e] - mean);
-        const int h = n < p.split ? 0 : 1;
-        zst[h] = merge_moments(zst[h], Moments{(float)V, mean, m2});
+          for (int e = 0; e < V; ++e) {
+            const float dv = r[e] - z.k;
+            z.s += dv;
+            z.q = fmaf(dv, dv, z.q);
+          }
+          z.n += (float)V;
+        };
+        if (n < p.split) add(zs[0]);
+        else add(zs[1]);
       }
     }
   }
@@ -313,7 +325,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);  // one arrive per epilogue warp
+      mbar_init(tempty_bar(a), EPI_WARPS);  // one arrive per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -461,7 +473,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int ch = (warp - 2) >> 2;         // which half of the tile's columns
+    constexpr int COLS = BN / (EPI_WARPS / 4);
     int lt = 0;
     for (int tile = first; tile < count; tile += stride, ++lt) {
       int g, m0, n0;
@@ -475,17 +489,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const int m = m0 + q * 32 + lane;
-      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      Moments zst[2] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
-      for (int j0 = 0; j0 < BN; j0 += 32) {
-        if (n0 + j0 >= p.N || m0 >= p.M) break;  // warp-uniform
+      const int c0 = ch * COLS;
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
+      ZSums zs[2] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      for (int j0 = 0; j0 < COLS; j0 += 32) {
+        if (n0 + c0 + j0 >= p.N || m0 >= p.M) break;  // warp-uniform
         float v[32];
         tmem_ld_32x32(t_row + (uint32_t)j0, v);
-        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + j0, v, zst);
+        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + c0 + j0, v, zs);
       }
-      if (EPI == EPI_BIAS_ZSTATS && m < p.M) {
-        float4 w = make_float4(zst[0].mean, zst[0].m2, zst[1].mean, zst[1].m2);
-        *reinterpret_cast<float4*>(p.zstats + (((size_t)m * p.G + g) * p.tiles_n + n0 / BN) * 4) = w;
+      if (EPI == EPI_BIAS_ZSTATS && m < p.M && n0 + c0 < p.N) {
+        float4 w;
+        w.x = zs[0].n > 0.f ? zs[0].k + zs[0].s / zs[0].n : 0.f;
+        w.y = zs[0].n > 0.f ? fmaxf(zs[0].q - zs[0].s * zs[0].s / zs[0].n, 0.f) : 0.f;
+        w.z = zs[1].n > 0.f ? zs[1].k + zs[1].s / zs[1].n : 0.f;
+        w.w = zs[1].n > 0.f ? fmaxf(zs[1].q - zs[1].s * zs[1].s / zs[1].n, 0.f) : 0.f;
+        const int grp = (n0 + c0) / kZStatsTile;
+        *reinterpret_cast<float4*>(p.zstats + (((size_t)m * p.G + g) * p.zgroups + grp) * 4) = w;
       }
       tc_fence_before();
       __syncwarp();
@@ -609,7 +629,7 @@ bool gemm_tc_supported(const GemmDesc& d) {
   // 16-byte row strides for the tensor maps and the vector epilogue.
   if (d.N % 8 || d.K % 8) return false;
   if (d.kind == GEMM_WGRAD && d.M % 8) return false;
-  if (d.epi == EPI_BIAS_ZSTATS && (BN != kZStatsTile || !d.zstats || d.split % 8)) return false;
+  if (d.epi == EPI_BIAS_ZSTATS && (BN / (EPI_WARPS / 4) != kZStatsTile || !d.zstats || d.split % 8)) return false;
   const int ok_epi = (d.kind == GEMM_FWD && (d.epi == EPI_STORE || d.epi == EPI_BIAS || d.epi == EPI_BIAS_RESID ||
                                              d.epi == EPI_BIAS_ZSTATS)) ||
                      (d.kind == GEMM_DGRAD && (d.epi == EPI_STORE || d.epi == EPI_RESID)) ||
@@ -670,6 +690,7 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.wait_limit_ns = kWaitLimitNs;
   p.zstats = d.zstats;
   p.split = d.split;
+  p.zgroups = (d.N + kZStatsTile - 1) / kZStatsTile;
   if (d.dtype == 1) return pair ? dispatch_tc<bf16, true>(d, ma, mb, p, st) : dispatch_tc<bf16, false>(d, ma, mb, p, st);
   return pair ? dispatch_tc<f16, true>(d, ma, mb, p, st) : dispatch_tc<f16, false>(d, ma, mb, p, st);
 }

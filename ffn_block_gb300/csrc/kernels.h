@@ -13,48 +13,36 @@ struct RowArgs {
   int nbblk;   // ceil(B / nb)
 };
 
-// Forward: LN0 -> token mix -> + x -> LN1.  One CTA per sample.
-cudaError_t launch_ln0_mix_ln1_fwd(const RowArgs& a, const void* x, const void* g0, const void* be0,
-                                   const void* g1, const void* be1, void* out1, float* mu0, float* r0,
-                                   float* mu1, float* r1, cudaStream_t st);
-// Forward: y = LN(s) per row (norm2).
-cudaError_t launch_ln_rows_fwd(const RowArgs& a, const void* s, const void* g, const void* be, void* y,
-                               float* mu, float* rs, cudaStream_t st);
+// LayerNorm forward, one row per warp.  Modes: plain; output written
+// token-mixed (column i*C+c of row j lands in row i, column j*C+c of the same
+// sample, C = D/T); input is the sum of two tensors.
+enum LnFwdMode { LNF_PLAIN = 0, LNF_MIXED_OUT = 1, LNF_SUM_IN = 2 };
+cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
+                          const void* be, void* y, float* mu, float* rs, cudaStream_t st);
+// LayerNorm backward over CTAs (t, b-block); per-CTA partial sums of dgamma
+// and dbeta ([nbblk*T][D]).  Modes: LNB_BIAS also sums ds per token into
+// pbias; LNB_MIXED_TOO reads s + s_add and also writes token_mix(ds) to
+// out_mixed; LNB_RESID adds resid to the output.
+enum LnBwdMode { LNB_BIAS = 0, LNB_MIXED_TOO = 1, LNB_RESID = 2 };
+cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s, const void* s_add,
+                          const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
+                          void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st);
+// Backward of norm2 (launch_ln_bwd in LNB_BIAS mode): ds2 plus partial sums
+// for gamma2, beta2 and bout.
+cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
+                           const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
+                           float* pbo, cudaStream_t st);
 // Forward: hidden = LN_x(U) * silu(LN_gate(G)) from Z = [U | G], with the
 // row statistics merged from `zstats` (see below).
 cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, const void* wx,
                             const void* bx, const void* wg, const void* bg, void* hidden, float* muU,
                             float* rU, float* muG, float* rG, cudaStream_t st);
-// Backward of norm2: ds2 plus partial sums for gamma2, beta2, bout.
-cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
-                           const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
-                           float* pbo, cudaStream_t st);
 // Backward of the gate and both inner LNs: dZ plus partial sums.  `rowsum`
 // ([B*T][4] floats) is scratch for the row sums of the first pass.
 cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU,
                             const float* rU, const float* muG, const float* rG, const void* wx,
                             const void* bx, const void* wg, const void* bg, void* dZ, float* pwx,
                             float* pbx, float* pwg, float* pbg, float* pb1, float* rowsum, cudaStream_t st);
-// Backward of norm1, the token mix and norm0: dx plus partial sums.
-cudaError_t launch_ln1_mix_ln0_bwd(const RowArgs& a, const void* x, const void* dout1,
-                                   const float* mu0, const float* r0, const float* mu1,
-                                   const float* r1, const void* g0, const void* be0, const void* g1,
-                                   float* ds1, void* dx, float* pg0, float* pb0, float* pg1,
-                                   float* pbe1, cudaStream_t st);
-
-// Cluster versions of the two per-sample passes (token mix through
-// distributed shared memory).  mix_supported() says whether the shape fits
-// (T <= 64, rows of <= 320 16-byte vectors, shared memory).  The backward
-// writes one partial row per CTA: mix_bwd_partial_rows() of them (<= 1024).
-bool mix_supported(const RowArgs& a);
-int mix_bwd_partial_rows(const RowArgs& a);
-constexpr int kMixPartialRowsMax = 1024;
-cudaError_t launch_mix_fwd(const RowArgs& a, const void* x, const void* g0, const void* be0, const void* g1,
-                           const void* be1, void* out1, float* mu0, float* r0, float* mu1, float* r1,
-                           cudaStream_t st);
-cudaError_t launch_mix_bwd(const RowArgs& a, const void* x, const void* dout1, const float* mu0, const float* r0,
-                           const float* mu1, const float* r1, const void* g0, const void* be0, const void* g1,
-                           void* dx, float* pg0, float* pb0, float* pg1, float* pbe1, cudaStream_t st);
 
 // Deterministic column sums: out[j] = sum_{p<P} part[p*J + j], cast to dtype.
 struct ColsumJob {
@@ -65,9 +53,7 @@ struct ColsumJob {
 constexpr int kMaxColsumJobs = 12;
 cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStream_t st);
 
-// Shared-memory need of the per-sample passes (bytes), and the largest
-// thread count a row pass may use (one thread per 16-byte vector of a row).
-size_t per_sample_smem_bytes(const RowArgs& a);
+// Largest thread count a row pass may use (one thread per 16-byte vector).
 constexpr int kRowThreadsMax = 512;
 int max_dynamic_smem_bytes();
 
@@ -75,13 +61,13 @@ int max_dynamic_smem_bytes();
 enum GemmKind { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_BIAS = 1, EPI_BIAS_RESID = 2, EPI_RESID = 3, EPI_BIAS_ZSTATS = 4 };
 
-// Row statistics of Z = [U | G] in 256-column tiles: for row r and tile j
-// (columns [256 j, 256 j + 256) of the 2H-wide row), zstats[(r * tiles + j)
-// * 4 + {0,1,2,3}] = {mean, M2} of the tile's U columns and {mean, M2} of its
+// Row statistics of Z = [U | G] in 128-column groups: for row r and group j
+// (columns [128 j, 128 j + 128) of the 2H-wide row), zstats[(r * groups + j)
+// * 4 + {0,1,2,3}] = {mean, M2} of the group's U columns and {mean, M2} of its
 // G columns, taken from the stored (rounded) Z values.  M2 = sum of squared
 // deviations from the mean.  Written by the GEMM1 epilogue (EPI_BIAS_ZSTATS)
 // or by launch_zstats; merged per row by the gate forward.
-constexpr int kZStatsTile = 256;
+constexpr int kZStatsTile = 128;
 __host__ __device__ inline int zstats_tiles(int H) { return (2 * H + kZStatsTile - 1) / kZStatsTile; }
 cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaStream_t st);
 

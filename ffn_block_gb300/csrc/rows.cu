@@ -1,6 +1,7 @@
-// Row passes of the RankMixer block: the three outer LayerNorms with the
-// token mix and residuals, the LN-gated SiLU of the FFN, their backwards, and
-// the deterministic column reductions of the parameter gradients.
+// Row passes of the RankMixer block: the three outer LayerNorms (with the
+// token mix folded into how two of them read or write their rows), the
+// LN-gated SiLU of the FFN, their backwards, and the deterministic column
+// reductions of the parameter gradients.
 //
 // Operation: page "Subgraph-fusion-based Mega-kernel Generation", section
 // "Exact computation".  LN(z) = (z - mean) / sqrt(mean((z - mean)^2) + eps)
@@ -40,108 +41,49 @@ inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
 inline int round32(int v) { return (v + 31) / 32 * 32; }
 
 
-// =========================================================================
-// F1: norm0 -> token mix -> + x -> norm1, one CTA per sample b.
-// x[b] ([T,D], storage type) is staged in shared memory; warp w handles rows
-// w, w + nwarps, ...; each lane keeps its columns k = lane + 32 q in
-// registers (MAXQ >= ceil(D/32)).
-// =========================================================================
-template <typename T, int MAXQ>
-__global__ void __launch_bounds__(256) k_ln0_mix_ln1_fwd(
-    const T* __restrict__ x, const T* __restrict__ g0, const T* __restrict__ be0,
-    const T* __restrict__ g1, const T* __restrict__ be1, T* __restrict__ out1,
-    float* __restrict__ mu0, float* __restrict__ r0, float* __restrict__ mu1,
-    float* __restrict__ r1, int Tn, int D, int C, float eps) {
-  extern __shared__ __align__(16) unsigned char sm[];
-  T* xs = reinterpret_cast<T*>(sm);
-  float* smu = reinterpret_cast<float*>(sm + align16((size_t)Tn * D * sizeof(T)));
-  float* srs = smu + Tn;
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const size_t base = (size_t)b * Tn * D;
-
-  const int n16 = (int)((size_t)Tn * D * sizeof(T) / 16);
-  const uint4* src = reinterpret_cast<const uint4*>(x + base);
-  for (int i = threadIdx.x; i < n16; i += blockDim.x) reinterpret_cast<uint4*>(xs)[i] = src[i];
-  __syncthreads();
-
-  const float invD = 1.0f / (float)D;
-  // norm0 statistics of every row j of x[b].
-  for (int j = warp; j < Tn; j += nw) {
-    float v[MAXQ];
-    float s = 0.f;
+// -------------------------------------------------------------------------
+// Token mix as an addressing rule.  Mixing moves column d = i*C + c of row j
+// to row i, column j*C + c (within one sample); it is its own inverse.  The
+// forward writes norm0's output rows already mixed, and the backward of norm1
+// writes its gradient rows both as they are and mixed, so every LayerNorm
+// pass reads and writes whole rows.
+// -------------------------------------------------------------------------
+template <typename T, int V>
+__device__ __forceinline__ void store_mixed(T* sample_base, const float* v, int j, int d0, int C, int D) {
+  int i = d0 / C, c = d0 - i * C;
+  if ((C & 1) == 0) {
+    // d0 even and C even: elements (e, e+1) always share a chunk.
 #pragma unroll
-    for (int q = 0; q < MAXQ; ++q) {
-      const int k = lane + 32 * q;
-      v[q] = (k < D) ? to_f(xs[j * D + k]) : 0.f;
-      s += v[q];
+    for (int e = 0; e < V; e += 2) {
+      T pr[2] = {from_f<T>(v[e]), from_f<T>(v[e + 1])};
+      T* dst = sample_base + (size_t)i * D + j * C + c;
+      if (sizeof(T) == 2) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(pr);
+      else *reinterpret_cast<float2*>(dst) = make_float2(v[e], v[e + 1]);
+      c += 2;
+      while (c >= C) { c -= C; ++i; }
     }
-    const float mean = warp_sum(s) * invD;
-    float ss = 0.f;
+  } else {
 #pragma unroll
-    for (int q = 0; q < MAXQ; ++q) {
-      const int k = lane + 32 * q;
-      const float c = v[q] - mean;
-      ss += (k < D) ? c * c : 0.f;
-    }
-    const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + eps);
-    if (lane == 0) {
-      smu[j] = mean;
-      srs[j] = rstd;
-      mu0[(size_t)b * Tn + j] = mean;
-      r0[(size_t)b * Tn + j] = rstd;
-    }
-  }
-  __syncthreads();
-
-  // Row i of s1 = token_mix(norm0(x))[i] + x[i]; element k = j*C + c comes
-  // from row j, column d = i*C + c of norm0(x).
-  for (int i = warp; i < Tn; i += nw) {
-    float v[MAXQ];
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < MAXQ; ++q) {
-      const int k = lane + 32 * q;
-      float val = 0.f;
-      if (k < D) {
-        const int j = k / C, c = k - j * C, d = i * C + c;
-        const float a0 = (to_f(xs[j * D + d]) - smu[j]) * srs[j] * to_f(g0[d]) + to_f(be0[d]);
-        val = a0 + to_f(xs[i * D + k]);
-      }
-      v[q] = val;
-      s += val;
-    }
-    const float mean = warp_sum(s) * invD;
-    float ss = 0.f;
-#pragma unroll
-    for (int q = 0; q < MAXQ; ++q) {
-      const int k = lane + 32 * q;
-      const float c = v[q] - mean;
-      ss += (k < D) ? c * c : 0.f;
-    }
-    const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + eps);
-    T* orow = out1 + base + (size_t)i * D;
-#pragma unroll
-    for (int q = 0; q < MAXQ; ++q) {
-      const int k = lane + 32 * q;
-      if (k < D) orow[k] = from_f<T>((v[q] - mean) * rstd * to_f(g1[k]) + to_f(be1[k]));
-    }
-    if (lane == 0) {
-      mu1[(size_t)b * Tn + i] = mean;
-      r1[(size_t)b * Tn + i] = rstd;
+    for (int e = 0; e < V; ++e) {
+      sample_base[(size_t)i * D + j * C + c] = from_f<T>(v[e]);
+      if (++c == C) { c = 0; ++i; }
     }
   }
 }
 
 // =========================================================================
-// F5: y = LN(s) for every row (norm2).  One warp per row, 16-byte vectors;
-// lane owns vectors lane + 32 q (MAXV >= ceil(D / V / 32)).
+// LayerNorm forward, one warp per row, the row held in registers as 16-byte
+// vectors (lane owns vectors lane + 32 q, MAXV >= ceil(D / V / 32)):
+//   LNF_PLAIN      y = LN(s)                       (norm2)
+//   LNF_MIXED_OUT  y = LN(s), written token-mixed  (norm0: a0 -> mix)
+//   LNF_SUM_IN     y = LN(s + s_add)               (norm1: mix + x)
+// Saves the row mean and 1/sqrt(var + eps).
 // =========================================================================
-template <typename T, int MAXV>
-__global__ void __launch_bounds__(256) k_ln_rows_fwd(const T* __restrict__ s, const T* __restrict__ g,
-                                                     const T* __restrict__ be, T* __restrict__ y,
-                                                     float* __restrict__ mu, float* __restrict__ rs,
-                                                     int N, int D, float eps) {
+template <typename T, int MODE, int MAXV>
+__global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T* __restrict__ s_add,
+                                                const T* __restrict__ g, const T* __restrict__ be,
+                                                T* __restrict__ y, float* __restrict__ mu, float* __restrict__ rs,
+                                                int N, int Tn, int D, int C, float eps) {
   constexpr int V = VecN<T>::value;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -155,6 +97,12 @@ __global__ void __launch_bounds__(256) k_ln_rows_fwd(const T* __restrict__ s, co
     const int vi = lane + 32 * q;
     if (vi < nv) {
       load_vec(srow + vi * V, v[q]);
+      if (MODE == LNF_SUM_IN) {
+        float a[V];
+        load_vec(s_add + (size_t)row * D + vi * V, a);
+#pragma unroll
+        for (int e = 0; e < V; ++e) v[q][e] += a[e];
+      }
 #pragma unroll
       for (int e = 0; e < V; ++e) sum += v[q][e];
     }
@@ -174,7 +122,7 @@ __global__ void __launch_bounds__(256) k_ln_rows_fwd(const T* __restrict__ s, co
     }
   }
   const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + eps);
-  T* yrow = y + (size_t)row * D;
+  const int b = row / Tn, j = row - b * Tn;
 #pragma unroll
   for (int q = 0; q < MAXV; ++q) {
     const int vi = lane + 32 * q;
@@ -184,7 +132,8 @@ __global__ void __launch_bounds__(256) k_ln_rows_fwd(const T* __restrict__ s, co
       load_vec(be + vi * V, bb);
 #pragma unroll
       for (int e = 0; e < V; ++e) o[e] = (v[q][e] - mean) * rstd * gg[e] + bb[e];
-      store_vec(yrow + vi * V, o);
+      if (MODE == LNF_MIXED_OUT) store_mixed<T, V>(y + (size_t)b * Tn * D, o, j, vi * V, C, D);
+      else store_vec(y + (size_t)row * D + vi * V, o);
     }
   }
   if (lane == 0) {
@@ -193,52 +142,110 @@ __global__ void __launch_bounds__(256) k_ln_rows_fwd(const T* __restrict__ s, co
   }
 }
 
-// -------------------------------------------------------------------------
-// Row streaming for the per-token passes.  Each CTA walks a list of rows; its
-// first thread keeps S rows in flight with cp.async.bulk copies into a ring
-// of shared-memory stages (one mbarrier per stage, completion counted in
-// bytes).  A stage is refilled right after the block-wide reduction of the
-// row that used it, when every thread has finished reading it.  Waits are
-// bounded; a wait that gives up sets the device error word and the block
-// leaves the loop together after its next barrier.
-// -------------------------------------------------------------------------
-constexpr int kRingStages = 4;
-constexpr uint64_t kRowWaitLimitNs = 2000ull * 1000ull * 1000ull;
+constexpr int kLnBwdRows = 4;  // rows per barrier
 
-struct RowRing {
-  uint32_t base;        // shared address of stage 0
-  uint32_t stage_bytes; // bytes per stage (multiple of 128)
-  uint32_t bars;        // shared address of the S mbarriers
-  __device__ uint32_t stage(int i) const { return base + (uint32_t)(i % kRingStages) * stage_bytes; }
-  __device__ uint32_t bar(int i) const { return bars + 8u * (uint32_t)(i % kRingStages); }
-};
-
-__device__ __forceinline__ RowRing ring_setup(unsigned char* sm, uint32_t stage_bytes, volatile int* abort_flag) {
-  RowRing r;
-  r.base = smem_u32(sm);
-  r.stage_bytes = stage_bytes;
-  r.bars = r.base + kRingStages * stage_bytes;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kRingStages; ++i) mbar_init(r.bars + 8u * i, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
+// =========================================================================
+// LayerNorm backward for rows (b, t), CTA (t, b-block) -- t varies fastest
+// over the grid so concurrently running CTAs cover whole samples.  With
+// g = gamma * gin, xh = (s - mean) * rstd over the row:
+//   ds = rstd * (g - mean(g) - xh * mean(g * xh)),
+//   dgamma += gin * xh, dbeta += gin (per-CTA partial rows).
+// Modes:
+//   LNB_BIAS       out = ds; also dbias[t] += ds            (norm2; bias bout)
+//   LNB_MIXED_TOO  s = s + s_add; out = ds and out_mixed = token_mix(ds)
+//                                                           (norm1: s1 = mix + x)
+//   LNB_RESID      out = ds + resid                         (norm0 + residual)
+// Thread v owns columns v*V ..; kLnBwdRows rows share one block reduction.
+// =========================================================================
+template <typename T, int MODE>
+__global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const T* __restrict__ s,
+                                                const T* __restrict__ s_add, const float* __restrict__ mu,
+                                                const float* __restrict__ rs, const T* __restrict__ gamma,
+                                                const T* __restrict__ resid, T* __restrict__ out,
+                                                T* __restrict__ out_mixed, float* __restrict__ pg,
+                                                float* __restrict__ pb, float* __restrict__ pbias, int B, int Tn,
+                                                int D, int C, int nb) {
+  constexpr int V = VecN<T>::value;
+  constexpr int RB = kLnBwdRows;
+  __shared__ float red[2 * 32 * 2 * RB];
+  int slot = 0;
+  const int t = blockIdx.x, bblk = blockIdx.y;
+  const int v = threadIdx.x;
+  const bool act = v * V < D;
+  const int d0 = v * V;
+  float gam[V], ag[V], ab[V], ao[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) ag[e] = ab[e] = ao[e] = 0.f;
+  if (act) load_vec(gamma + d0, gam);
+  const float invD = 1.0f / (float)D;
+  const int b_begin = bblk * nb, b_end = min(B, b_begin + nb);
+  for (int b0 = b_begin; b0 < b_end; b0 += RB) {
+    float gv[RB][V], xh[RB][V], sums[2 * RB];
+    float rstd[RB];
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) {
+      sums[2 * rr] = sums[2 * rr + 1] = 0.f;
+      rstd[rr] = 0.f;
+      const int b = b0 + rr;
+      if (b < b_end) {
+        const size_t r = (size_t)b * Tn + t;
+        const float mean = mu[r];
+        rstd[rr] = rs[r];
+        if (act) {
+          float sv[V];
+          load_vec(gin + r * D + d0, gv[rr]);
+          load_vec(s + r * D + d0, sv);
+          if (MODE == LNB_MIXED_TOO) {
+            float a[V];
+            load_vec(s_add + r * D + d0, a);
+#pragma unroll
+            for (int e = 0; e < V; ++e) sv[e] += a[e];
+          }
+#pragma unroll
+          for (int e = 0; e < V; ++e) {
+            xh[rr][e] = (sv[e] - mean) * rstd[rr];
+            const float g = gam[e] * gv[rr][e];
+            sums[2 * rr] += g;
+            sums[2 * rr + 1] += g * xh[rr][e];
+          }
+        }
+      }
+    }
+    block_sum<2 * RB>(sums, red, slot);
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) {
+      const int b = b0 + rr;
+      if (b >= b_end || !act) continue;
+      const size_t r = (size_t)b * Tn + t;
+      const float mg = sums[2 * rr] * invD, mgx = sums[2 * rr + 1] * invD;
+      float o[V];
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        o[e] = rstd[rr] * (gam[e] * gv[rr][e] - mg - xh[rr][e] * mgx);
+        ag[e] += gv[rr][e] * xh[rr][e];
+        ab[e] += gv[rr][e];
+        if (MODE == LNB_BIAS) ao[e] += o[e];
+      }
+      if (MODE == LNB_MIXED_TOO) store_mixed<T, V>(out_mixed + (size_t)b * Tn * D, o, t, d0, C, D);
+      if (MODE == LNB_RESID) {
+        float rv[V];
+        load_vec(resid + r * D + d0, rv);
+#pragma unroll
+        for (int e = 0; e < V; ++e) o[e] += rv[e];
+      }
+      store_vec(out + r * D + d0, o);
+    }
   }
-  __syncthreads();
-  return r;
+  if (act) {
+    const size_t p = (size_t)bblk * Tn + t;
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      pg[p * D + d0 + e] = ag[e];
+      pb[p * D + d0 + e] = ab[e];
+      if (MODE == LNB_BIAS) pbias[p * D + d0 + e] = ao[e];
+    }
+  }
 }
-
-// Thread 0: after an abort, wait (bounded) for the copies still in flight so
-// the CTA does not exit while they write its shared memory.
-__device__ __forceinline__ void ring_drain(const RowRing& r, int consumed, int issued, unsigned int* err) {
-  if (threadIdx.x != 0) return;
-  volatile int no_abort = 0;
-  for (int j = consumed; j < issued; ++j)
-    mbar_wait_bounded(r.bar(j), (uint32_t)(j / kRingStages) & 1u, 50ull * 1000ull * 1000ull, err,
-                      ERRBIT_WAIT_DRAIN, &no_abort);
-}
-
-__host__ __device__ inline uint32_t ring_stage_bytes(size_t row_bytes) { return (uint32_t)((row_bytes + 127) / 128 * 128); }
-inline size_t ring_smem_bytes(size_t row_bytes) { return (size_t)kRingStages * ring_stage_bytes(row_bytes) + 64; }
 
 // =========================================================================
 // Z statistics for the FFMA path: one warp per (row, 256-column tile) of
@@ -353,100 +360,6 @@ __global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const
         o[e] = uu * (gg / (1.0f + expf(-gg)));
       }
       store_vec(hidden + (size_t)(r0 + i) * H + h0, o);
-    }
-  }
-}
-
-// =========================================================================
-// G1: backward of norm2.  CTA (bblk, t) handles rows (b, t) for b in its
-// block; thread v owns columns d = v*V ...  With g = gamma2 * dy and
-// xh = (s2 - mean) * rstd:
-//   ds2 = rstd * (g - mean(g) - xh * mean(g * xh)),
-//   dgamma2 += dy * xh, dbeta2 += dy, dbout[t] += ds2 (per-CTA partials).
-// Rows stream through the shared-memory ring (dy row, then s2 row).
-// =========================================================================
-template <typename T>
-__global__ void __launch_bounds__(512) k_ln2_bwd(const T* __restrict__ dy, const T* __restrict__ s2,
-                                                 const float* __restrict__ mu2, const float* __restrict__ r2,
-                                                 const T* __restrict__ g2, T* __restrict__ ds2,
-                                                 float* __restrict__ pg2, float* __restrict__ pb2,
-                                                 float* __restrict__ pbo, int B, int Tn, int D, int nb,
-                                                 unsigned int* err) {
-  constexpr int V = VecN<T>::value;
-  extern __shared__ __align__(16) unsigned char sm[];
-  __shared__ float red[2 * 32 * 2];
-  __shared__ int abort_flag;
-  const size_t half = (size_t)D * sizeof(T);
-  const RowRing ring = ring_setup(sm, ring_stage_bytes(2 * half), &abort_flag);
-  int slot = 0;
-  const int bblk = blockIdx.x, t = blockIdx.y;
-  const int v = threadIdx.x;
-  const bool act = v * V < D;
-  const int d0 = v * V;
-  float gam[V], ag[V], ab[V], ao[V];
-#pragma unroll
-  for (int e = 0; e < V; ++e) ag[e] = ab[e] = ao[e] = 0.f;
-  if (act) load_vec(g2 + d0, gam);
-  const float invD = 1.0f / (float)D;
-  const int b0 = bblk * nb;
-  const int nrows = max(0, min(B, b0 + nb) - b0);
-  auto issue = [&](int i) {
-    const size_t r = (size_t)(b0 + i) * Tn + t;
-    mbar_arrive_expect_tx(ring.bar(i), (uint32_t)(2 * half));
-    bulk_g2s(ring.stage(i), dy + r * D, (uint32_t)half, ring.bar(i));
-    bulk_g2s(ring.stage(i) + (uint32_t)half, s2 + r * D, (uint32_t)half, ring.bar(i));
-  };
-  int issued = 0;
-  if (v == 0)
-    for (; issued < min(kRingStages, nrows); ++issued) issue(issued);
-  int i = 0;
-  for (; i < nrows; ++i) {
-    mbar_wait_bounded(ring.bar(i), (uint32_t)(i / kRingStages) & 1u, kRowWaitLimitNs, err, ERRBIT_WAIT_PRODUCER,
-                      &abort_flag);
-    const T* st = reinterpret_cast<const T*>(sm + (size_t)(i % kRingStages) * ring.stage_bytes);
-    const size_t r = (size_t)(b0 + i) * Tn + t;
-    const float mean = mu2[r], rstd = r2[r];
-    float dyv[V], xh[V], g[V];
-    float sums[2] = {0.f, 0.f};
-    if (act) {
-      float sv[V];
-      load_vec(st + d0, dyv);
-      load_vec(st + D + d0, sv);
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        xh[e] = (sv[e] - mean) * rstd;
-        g[e] = gam[e] * dyv[e];
-        sums[0] += g[e];
-        sums[1] += g[e] * xh[e];
-      }
-    }
-    block_sum<2>(sums, red, slot);
-    if (abort_flag) break;
-    if (v == 0 && issued < nrows) {
-      fence_proxy_async_smem();
-      issue(issued++);
-    }
-    const float mg = sums[0] * invD, mgx = sums[1] * invD;
-    if (act) {
-      float o[V];
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        o[e] = rstd * (g[e] - mg - xh[e] * mgx);
-        ag[e] += dyv[e] * xh[e];
-        ab[e] += dyv[e];
-        ao[e] += o[e];
-      }
-      store_vec(ds2 + r * D + d0, o);
-    }
-  }
-  if (abort_flag) ring_drain(ring, i, issued, err);
-  if (act) {
-    const size_t p = (size_t)bblk * Tn + t;
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      pg2[p * D + d0 + e] = ag[e];
-      pb2[p * D + d0 + e] = ab[e];
-      pbo[p * D + d0 + e] = ao[e];
     }
   }
 }
@@ -588,194 +501,6 @@ __global__ void __launch_bounds__(512) k_gate_bwd_apply(
 }
 
 // =========================================================================
-// G7: backward of norm1, the token mix and norm0 for one sample b per CTA.
-// x[b] is staged in shared memory; s1 = token_mix(norm0(x)) + x is
-// recomputed from it and the saved statistics.  Thread v owns columns
-// k = v*V ... of every row.  Row sums are deferred: a first sweep writes one
-// partial per (row, warp), a second sweep finishes the rows, so each phase
-// needs one barrier instead of one per row.
-//   phase A: ds1 = LN1-backward(dout1)                  -> scratch (fp32)
-//   phase B: da0 = token_mix(ds1) (the mix is its own inverse),
-//            dx = ds1 + LN0-backward(da0)
-// =========================================================================
-template <typename T>
-__global__ void __launch_bounds__(512) k_ln1_mix_ln0_bwd(
-    const T* __restrict__ x, const T* __restrict__ dout1, const float* __restrict__ mu0,
-    const float* __restrict__ r0, const float* __restrict__ mu1, const float* __restrict__ r1,
-    const T* __restrict__ g0, const T* __restrict__ be0, const T* __restrict__ g1, float* ds1,
-    T* __restrict__ dx, float* __restrict__ pg0, float* __restrict__ pb0, float* __restrict__ pg1,
-    float* __restrict__ pbe1, int Tn, int D, int C) {
-  constexpr int V = VecN<T>::value;
-  extern __shared__ __align__(16) unsigned char sm[];
-  T* xs = reinterpret_cast<T*>(sm);
-  float* s_mu0 = reinterpret_cast<float*>(sm + align16((size_t)Tn * D * sizeof(T)));
-  float* s_r0 = s_mu0 + Tn;
-  float* s_mu1 = s_r0 + Tn;
-  float* s_r1 = s_mu1 + Tn;
-  float* red = s_r1 + Tn;  // [Tn][nw][2]
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nw = blockDim.x >> 5;
-  const size_t base = (size_t)b * Tn * D;
-
-  const int n16 = (int)((size_t)Tn * D * sizeof(T) / 16);
-  const uint4* src = reinterpret_cast<const uint4*>(x + base);
-  for (int i = tid; i < n16; i += blockDim.x) reinterpret_cast<uint4*>(xs)[i] = src[i];
-  for (int i = tid; i < Tn; i += blockDim.x) {
-    s_mu0[i] = mu0[(size_t)b * Tn + i];
-    s_r0[i] = r0[(size_t)b * Tn + i];
-    s_mu1[i] = mu1[(size_t)b * Tn + i];
-    s_r1[i] = r1[(size_t)b * Tn + i];
-  }
-  __syncthreads();
-
-  const bool act = tid * V < D;
-  const int k0 = tid * V;
-  const float invD = 1.0f / (float)D;
-  float gam0[V], gam1[V];
-  if (act) {
-    load_vec(g0 + k0, gam0);
-    load_vec(g1 + k0, gam1);
-  }
-
-  // xh1 of row i for this thread's columns (recomputed from x).
-  auto xhat1 = [&](int i, float* xh) {
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      const int k = k0 + e;
-      const int j = k / C, c = k - j * C, d = i * C + c;
-      const float a0 = (to_f(xs[j * D + d]) - s_mu0[j]) * s_r0[j] * to_f(g0[d]) + to_f(be0[d]);
-      const float s1 = a0 + to_f(xs[i * D + k]);
-      xh[e] = (s1 - s_mu1[i]) * s_r1[i];
-    }
-  };
-  // da0 of row j = token_mix(ds1)[j]: element k' = i*C + c is ds1[i, j*C + c].
-  auto gather_da0 = [&](int j, float* da) {
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      const int kp = k0 + e;
-      const int i = kp / C, c = kp - i * C;
-      da[e] = ds1[base + (size_t)i * D + j * C + c];
-    }
-  };
-
-  // ---- phase A, sweep 1: row partial sums of g = gamma1*dout1 and g*xh1.
-  for (int i = 0; i < Tn; ++i) {
-    float ps = 0.f, psx = 0.f;
-    if (act) {
-      float xh[V], d1[V];
-      xhat1(i, xh);
-      load_vec(dout1 + base + (size_t)i * D + k0, d1);
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float g = gam1[e] * d1[e];
-        ps += g;
-        psx += g * xh[e];
-      }
-    }
-    ps = warp_sum(ps);
-    psx = warp_sum(psx);
-    if (lane == 0) {
-      red[(i * nw + warp) * 2 + 0] = ps;
-      red[(i * nw + warp) * 2 + 1] = psx;
-    }
-  }
-  __syncthreads();
-  // ---- phase A, sweep 2: ds1 rows and the norm1 parameter partials.
-  {
-    float ag[V], ab[V];
-#pragma unroll
-    for (int e = 0; e < V; ++e) ag[e] = ab[e] = 0.f;
-    for (int i = 0; i < Tn; ++i) {
-      float t0 = 0.f, t1 = 0.f;
-      for (int w = 0; w < nw; ++w) {
-        t0 += red[(i * nw + w) * 2 + 0];
-        t1 += red[(i * nw + w) * 2 + 1];
-      }
-      if (act) {
-        const float mg = t0 * invD, mgx = t1 * invD, rs = s_r1[i];
-        float xh[V], d1[V];
-        xhat1(i, xh);
-        load_vec(dout1 + base + (size_t)i * D + k0, d1);
-        float* drow = ds1 + base + (size_t)i * D + k0;
-#pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const float g = gam1[e] * d1[e];
-          drow[e] = rs * (g - mg - xh[e] * mgx);
-          ag[e] += d1[e] * xh[e];
-          ab[e] += d1[e];
-        }
-      }
-    }
-    if (act) {
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        pg1[(size_t)b * D + k0 + e] = ag[e];
-        pbe1[(size_t)b * D + k0 + e] = ab[e];
-      }
-    }
-  }
-  __syncthreads();  // ds1 of this sample is complete and visible to the block
-
-  // ---- phase B, sweep 1: row partial sums for norm0's backward.
-  for (int j = 0; j < Tn; ++j) {
-    float ps = 0.f, psx = 0.f;
-    if (act) {
-      float da[V];
-      gather_da0(j, da);
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float xh0 = (to_f(xs[j * D + k0 + e]) - s_mu0[j]) * s_r0[j];
-        const float g = gam0[e] * da[e];
-        ps += g;
-        psx += g * xh0;
-      }
-    }
-    ps = warp_sum(ps);
-    psx = warp_sum(psx);
-    if (lane == 0) {
-      red[(j * nw + warp) * 2 + 0] = ps;
-      red[(j * nw + warp) * 2 + 1] = psx;
-    }
-  }
-  __syncthreads();
-  // ---- phase B, sweep 2: dx rows and the norm0 parameter partials.
-  {
-    float ag[V], ab[V];
-#pragma unroll
-    for (int e = 0; e < V; ++e) ag[e] = ab[e] = 0.f;
-    for (int j = 0; j < Tn; ++j) {
-      float t0 = 0.f, t1 = 0.f;
-      for (int w = 0; w < nw; ++w) {
-        t0 += red[(j * nw + w) * 2 + 0];
-        t1 += red[(j * nw + w) * 2 + 1];
-      }
-      if (act) {
-        const float mg = t0 * invD, mgx = t1 * invD, rs = s_r0[j];
-        float da[V], o[V];
-        gather_da0(j, da);
-        const float* drow = ds1 + base + (size_t)j * D + k0;
-#pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const float xh0 = (to_f(xs[j * D + k0 + e]) - s_mu0[j]) * s_r0[j];
-          const float g = gam0[e] * da[e];
-          o[e] = drow[e] + rs * (g - mg - xh0 * mgx);
-          ag[e] += da[e] * xh0;
-          ab[e] += da[e];
-        }
-        store_vec(dx + base + (size_t)j * D + k0, o);
-      }
-    }
-    if (act) {
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        pg0[(size_t)b * D + k0 + e] = ag[e];
-        pb0[(size_t)b * D + k0 + e] = ab[e];
-      }
-    }
-  }
-}
-
-// =========================================================================
 // R: column sums of partials, several jobs in one launch.  Block (32, 16):
 // x picks the column, y a stripe of partial rows p = y, y+16, ...; stripes
 // are combined in a fixed order.
@@ -807,13 +532,6 @@ __global__ void __launch_bounds__(512) k_colsums(const ColsumArgs a) {
   }
 }
 
-// ---------------------------------------------------------------- launch helpers
-template <typename Kern>
-cudaError_t set_smem(Kern k, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
 }  // namespace
 
 int max_dynamic_smem_bytes() {
@@ -823,61 +541,57 @@ int max_dynamic_smem_bytes() {
   return v;
 }
 
-size_t per_sample_smem_bytes(const RowArgs& a) {
-  const size_t xs = align16((size_t)a.T * a.D * elem_bytes(a.dtype));
-  const int nthreads = round32(a.D / vec_elems(a.dtype));
-  const size_t g7 = xs + (size_t)4 * a.T * 4 + (size_t)a.T * (nthreads / 32) * 2 * 4;
-  const size_t f1 = xs + (size_t)2 * a.T * 4;
-  return g7 > f1 ? g7 : f1;
-}
-
-cudaError_t launch_ln0_mix_ln1_fwd(const RowArgs& a, const void* x, const void* g0, const void* be0,
-                                   const void* g1, const void* be1, void* out1, float* mu0, float* r0,
-                                   float* mu1, float* r1, cudaStream_t st) {
-  const size_t smem = align16((size_t)a.T * a.D * elem_bytes(a.dtype)) + (size_t)2 * a.T * 4;
-  const int q = (a.D + 31) / 32;
-  const int C = a.D / a.T;
-  const float eps = 1e-3f;
-  cudaError_t err = cudaSuccess;
-#define RMX_F1(MAXQ)                                                                              \
-  RMX_DISPATCH_T(a.dtype, {                                                                       \
-    auto k = k_ln0_mix_ln1_fwd<T, MAXQ>;                                                          \
-    err = set_smem(k, smem);                                                                      \
-    if (err == cudaSuccess)                                                                       \
-      k<<<a.B, 256, smem, st>>>((const T*)x, (const T*)g0, (const T*)be0, (const T*)g1,           \
-                                (const T*)be1, (T*)out1, mu0, r0, mu1, r1, a.T, a.D, C, eps);      \
-  })
-  if (q <= 2) RMX_F1(2);
-  else if (q <= 4) RMX_F1(4);
-  else if (q <= 8) RMX_F1(8);
-  else if (q <= 16) RMX_F1(16);
-  else if (q <= 24) RMX_F1(24);
-  else if (q <= 40) RMX_F1(40);
-  else return cudaErrorInvalidValue;
-#undef RMX_F1
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
-}
-
-cudaError_t launch_ln_rows_fwd(const RowArgs& a, const void* s, const void* g, const void* be, void* y,
-                               float* mu, float* rs, cudaStream_t st) {
+cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
+                          const void* be, void* y, float* mu, float* rs, cudaStream_t st) {
   const int N = a.B * a.T;
   const int nv = a.D / vec_elems(a.dtype);
   const int q = (nv + 31) / 32;
   const int grid = (N + 7) / 8;
-#define RMX_F5(MAXV)                                                                               \
-  RMX_DISPATCH_T(a.dtype, {                                                                        \
-    k_ln_rows_fwd<T, MAXV><<<grid, 256, 0, st>>>((const T*)s, (const T*)g, (const T*)be, (T*)y, mu, \
-                                                 rs, N, a.D, 1e-3f);                               \
+  const int C = a.D / a.T;
+#define RMX_LNF(M, MAXV)                                                                                   \
+  RMX_DISPATCH_T(a.dtype, {                                                                                \
+    k_ln_fwd<T, M, MAXV><<<grid, 256, 0, st>>>((const T*)s, (const T*)s_add, (const T*)g, (const T*)be,     \
+                                               (T*)y, mu, rs, N, a.T, a.D, C, 1e-3f);                      \
   })
-  if (q <= 1) RMX_F5(1);
-  else if (q <= 2) RMX_F5(2);
-  else if (q <= 4) RMX_F5(4);
-  else if (q <= 6) RMX_F5(6);
-  else if (q <= 10) RMX_F5(10);
+#define RMX_LNF_Q(M)                          \
+  if (q <= 1) RMX_LNF(M, 1);                  \
+  else if (q <= 2) RMX_LNF(M, 2);             \
+  else if (q <= 4) RMX_LNF(M, 4);             \
+  else if (q <= 6) RMX_LNF(M, 6);             \
+  else if (q <= 10) RMX_LNF(M, 10);           \
   else return cudaErrorInvalidValue;
-#undef RMX_F5
+  if (mode == LNF_PLAIN) { RMX_LNF_Q(LNF_PLAIN) }
+  else if (mode == LNF_MIXED_OUT) { RMX_LNF_Q(LNF_MIXED_OUT) }
+  else { RMX_LNF_Q(LNF_SUM_IN) }
+#undef RMX_LNF_Q
+#undef RMX_LNF
   return cudaGetLastError();
+}
+
+cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s, const void* s_add,
+                          const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
+                          void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
+  const int threads = round32(a.D / vec_elems(a.dtype));
+  if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
+  dim3 grid(a.T, a.nbblk);
+  const int C = a.D / a.T;
+#define RMX_LNB(M)                                                                                             \
+  RMX_DISPATCH_T(a.dtype, {                                                                                    \
+    k_ln_bwd<T, M><<<grid, threads, 0, st>>>((const T*)gin, (const T*)s, (const T*)s_add, mu, rs,              \
+                                             (const T*)gamma, (const T*)resid, (T*)out, (T*)out_mixed, pg, pb, \
+                                             pbias, a.B, a.T, a.D, C, a.nb);                                   \
+  })
+  if (mode == LNB_BIAS) RMX_LNB(LNB_BIAS);
+  else if (mode == LNB_MIXED_TOO) RMX_LNB(LNB_MIXED_TOO);
+  else RMX_LNB(LNB_RESID);
+#undef RMX_LNB
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
+                           const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
+                           float* pbo, cudaStream_t st) {
+  return launch_ln_bwd(a, LNB_BIAS, dy, s2, nullptr, mu2, r2, g2, nullptr, ds2, nullptr, pg2, pb2, pbo, st);
 }
 
 cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaStream_t st) {
@@ -903,25 +617,6 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats
   return cudaGetLastError();
 }
 
-cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
-                           const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
-                           float* pbo, cudaStream_t st) {
-  const int threads = round32(a.D / vec_elems(a.dtype));
-  if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
-  dim3 grid(a.nbblk, a.T);
-  const size_t smem = ring_smem_bytes((size_t)2 * a.D * elem_bytes(a.dtype));
-  cudaError_t err = cudaSuccess;
-  RMX_DISPATCH_T(a.dtype, {
-    auto k = k_ln2_bwd<T>;
-    err = set_smem(k, smem);
-    if (err == cudaSuccess)
-      k<<<grid, threads, smem, st>>>((const T*)dy, (const T*)s2, mu2, r2, (const T*)g2, (T*)ds2, pg2, pb2, pbo,
-                                     a.B, a.T, a.D, a.nb, device_error_word());
-  });
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
-}
-
 cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU,
                             const float* rU, const float* muG, const float* rG, const void* wx,
                             const void* bx, const void* wg, const void* bg, void* dZ, float* pwx,
@@ -944,29 +639,6 @@ cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, con
                                                    (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg, (T*)dZ,
                                                    pwx, pbx, pwg, pbg, pb1, a.B, a.T, a.H, a.nb);
   });
-  return cudaGetLastError();
-}
-
-cudaError_t launch_ln1_mix_ln0_bwd(const RowArgs& a, const void* x, const void* dout1,
-                                   const float* mu0, const float* r0, const float* mu1,
-                                   const float* r1, const void* g0, const void* be0, const void* g1,
-                                   float* ds1, void* dx, float* pg0, float* pb0, float* pg1,
-                                   float* pbe1, cudaStream_t st) {
-  const int threads = round32(a.D / vec_elems(a.dtype));
-  if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
-  const size_t smem = align16((size_t)a.T * a.D * elem_bytes(a.dtype)) + (size_t)4 * a.T * 4 +
-                      (size_t)a.T * (threads / 32) * 2 * 4;
-  const int C = a.D / a.T;
-  cudaError_t err = cudaSuccess;
-  RMX_DISPATCH_T(a.dtype, {
-    auto k = k_ln1_mix_ln0_bwd<T>;
-    err = set_smem(k, smem);
-    if (err == cudaSuccess)
-      k<<<a.B, threads, smem, st>>>((const T*)x, (const T*)dout1, mu0, r0, mu1, r1, (const T*)g0,
-                                    (const T*)be0, (const T*)g1, ds1, (T*)dx, pg0, pb0, pg1, pbe1,
-                                    a.T, a.D, C);
-  });
-  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
