@@ -37,7 +37,7 @@ def _expected_saved(s):
     N = s.B * s.T
     up = lambda v: (v + 255) // 256 * 256
     total = 0
-    tiles = (2 * s.H + 255) // 256
+    tiles = (2 * s.H + 127) // 128     # Z statistics per 128-column group
     for n in (N * s.D * e, N * 2 * s.H * e, N * s.H * e, N * s.D * e, 10 * N * 4, N * tiles * 4 * 4, N * s.D * e):
         total = up(total + n)
     return total
