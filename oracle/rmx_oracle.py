@@ -152,11 +152,13 @@ def forward(x, p):
 # Backward (chain rule through the steps above, in reverse order).
 # ---------------------------------------------------------------------------
 
-def backward(dy, cache, p):
+def backward(dy, cache, p, intermediates=None):
     """Gradients of sum(dy * y) w.r.t. x and every parameter.
 
     Returns (dx, grads) where grads has one entry per parameter name, each
-    with the parameter's shape (reading R6 for the reductions).
+    with the parameter's shape (reading R6 for the reductions).  If
+    `intermediates` is a dict, the gradients w.r.t. s2, Z and s1 are stored
+    in it under "ds2", "dZ" and "ds1".
     """
     B, T, D = dy.shape
     H = p["wout"].shape[1]
@@ -197,6 +199,8 @@ def backward(dy, cache, p):
     # a0 = norm0(x)
     dx0, grads["gamma0"], grads["beta0"] = layer_norm_backward(da0, p["gamma0"], cache["st0"])
     dx += dx0
+    if intermediates is not None:
+        intermediates.update(ds2=ds2, dZ=dZ, ds1=ds1)
     return dx, grads
 
 

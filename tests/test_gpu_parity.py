@@ -11,6 +11,7 @@ from ffn_block_gb300 import binding as B
 from ffn_block_gb300 import inputs as I
 from ffn_block_gb300.device import RankMixerDevice
 
+from oracle import rmx_oracle as O
 from parity_util import NAMES, TOL, compare, oracle_outputs
 
 pytestmark = pytest.mark.gpu
@@ -29,13 +30,21 @@ def _full_case(shape, ln="random", seed=I.DEFAULT_SEED):
     ref = oracle_outputs(arrays)
     names = NAMES
     if shape.D == shape.T:
-        # With one column per token chunk, dbeta0 sums the rows of norm1's
-        # backward, which are zero: the exact gradient is 0, so it is checked
-        # against the scale of its sibling dgamma0 instead of relatively.
+        # With one column per token chunk, dbeta0[d] = sum over b, j of
+        # ds1[b, d, j]: row sums of norm1's backward, which are zero.  The
+        # exact gradient is 0; the CUDA path stores ds1 in the storage type
+        # before the mix, so its result is bounded by that rounding:
+        # |dbeta0[d]| <= u * sum |ds1[b, d, :]| (+ fp32 summation).
         names = tuple(n for n in NAMES if n != "beta0")
-        scale = np.abs(ref["gamma0"]).max()
-        assert np.abs(ref["beta0"]).max() <= 1e-12 * scale
-        assert np.abs(got["beta0"]).max() <= 1e-3 * scale
+        a = I.to_float64(arrays)
+        p = {k: a[k] for k in I.PARAM_NAMES}
+        _, cache = O.forward(a["x"], p)
+        inter = {}
+        O.backward(a["dy"], cache, p, intermediates=inter)
+        u = {"f32": 1e-6, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}[shape.dtype]
+        bound = u * np.abs(inter["ds1"]).sum(axis=(0, 2)) + 1e-6 * np.abs(ref["gamma0"]).max()
+        assert np.abs(ref["beta0"]).max() <= 1e-12 * np.abs(ref["gamma0"]).max()
+        assert np.all(np.abs(got["beta0"]) <= bound), (got["beta0"], bound)
     return compare(got, ref, TOL[shape.dtype], names=names)
 
 
