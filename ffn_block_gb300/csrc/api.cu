@@ -325,9 +325,15 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     RMX_TRY(run_gemm("gemm2_wgrad", d, st));
   }
   {
-    Launch l("gate_bwd", st);
-    RMX_TRY(l.done(launch_gate_bwd(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
-                                   dZ, F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1), F(L.rowsum), st)));
+    Launch l("gate_bwd_rowsums", st);
+    RMX_TRY(l.done(launch_gate_bwd_rowsums(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w,
+                                           p.lng_b, F(L.rowsum), st)));
+  }
+  {
+    Launch l("gate_bwd_apply", st);
+    RMX_TRY(l.done(launch_gate_bwd_apply(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, F(L.rowsum), p.lnx_w, p.lnx_b,
+                                         p.lng_w, p.lng_b, dZ, F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1),
+                                         st)));
   }
   {
     GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};

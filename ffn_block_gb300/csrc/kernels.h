@@ -37,12 +37,16 @@ cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, con
 cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, const void* wx,
                             const void* bx, const void* wg, const void* bg, void* hidden, float* muU,
                             float* rU, float* muG, float* rG, cudaStream_t st);
-// Backward of the gate and both inner LNs: dZ plus partial sums.  `rowsum`
-// ([B*T][4] floats) is scratch for the row sums of the first pass.
-cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU,
-                            const float* rU, const float* muG, const float* rG, const void* wx,
-                            const void* bx, const void* wg, const void* bg, void* dZ, float* pwx,
-                            float* pbx, float* pwg, float* pbg, float* pb1, float* rowsum, cudaStream_t st);
+// Backward of the gate and both inner LNs, two streaming passes:
+// (1) rowsum[r] = {sum gU, sum gU*Uh, sum gG, sum gG*Gh} ([B*T][4] floats);
+// (2) dZ plus per-CTA partial sums of dwx, dbx, dwg, dbg and db1.
+cudaError_t launch_gate_bwd_rowsums(const RowArgs& a, const void* dh, const void* Z, const float* muU,
+                                    const float* rU, const float* muG, const float* rG, const void* wx,
+                                    const void* bx, const void* wg, const void* bg, float* rowsum, cudaStream_t st);
+cudaError_t launch_gate_bwd_apply(const RowArgs& a, const void* dh, const void* Z, const float* muU,
+                                  const float* rU, const float* muG, const float* rG, const float* rowsum,
+                                  const void* wx, const void* bx, const void* wg, const void* bg, void* dZ,
+                                  float* pwx, float* pbx, float* pwg, float* pbg, float* pb1, cudaStream_t st);
 
 // Deterministic column sums: out[j] = sum_{p<P} part[p*J + j], cast to dtype.
 struct ColsumJob {

@@ -617,27 +617,29 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats
   return cudaGetLastError();
 }
 
-cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU,
-                            const float* rU, const float* muG, const float* rG, const void* wx,
-                            const void* bx, const void* wg, const void* bg, void* dZ, float* pwx,
-                            float* pbx, float* pwg, float* pbg, float* pb1, float* rowsum, cudaStream_t st) {
-  const int threads = round32(a.H / vec_elems(a.dtype));
-  if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
+cudaError_t launch_gate_bwd_rowsums(const RowArgs& a, const void* dh, const void* Z, const float* muU,
+                                    const float* rU, const float* muG, const float* rG, const void* wx,
+                                    const void* bx, const void* wg, const void* bg, float* rowsum, cudaStream_t st) {
   const int N = a.B * a.T;
   RMX_DISPATCH_T(a.dtype, {
     k_gate_bwd_rowsums<T><<<(N + 7) / 8, 256, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, (const T*)wx,
                                                        (const T*)bx, (const T*)wg, (const T*)bg, rowsum, N, a.H);
   });
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  // Apply pass: 4 columns per thread, at most 256 threads per CTA.
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_bwd_apply(const RowArgs& a, const void* dh, const void* Z, const float* muU,
+                                  const float* rU, const float* muG, const float* rG, const float* rowsum,
+                                  const void* wx, const void* bx, const void* wg, const void* bg, void* dZ,
+                                  float* pwx, float* pbx, float* pwg, float* pbg, float* pb1, cudaStream_t st) {
+  // 4 columns per thread, at most 256 threads per CTA.
   const int quads = a.H / 4;
-  const int athreads = quads < 256 ? round32(quads) : 256;
-  dim3 grid(a.nbblk, a.T, (quads + athreads - 1) / athreads);
+  const int threads = quads < 256 ? round32(quads) : 256;
+  dim3 grid(a.nbblk, a.T, (quads + threads - 1) / threads);
   RMX_DISPATCH_T(a.dtype, {
-    k_gate_bwd_apply<T><<<grid, athreads, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, rowsum,
-                                                   (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg, (T*)dZ,
-                                                   pwx, pbx, pwg, pbg, pb1, a.B, a.T, a.H, a.nb);
+    k_gate_bwd_apply<T><<<grid, threads, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, rowsum, (const T*)wx,
+                                                  (const T*)bx, (const T*)wg, (const T*)bg, (T*)dZ, pwx, pbx, pwg,
+                                                  pbg, pb1, a.B, a.T, a.H, a.nb);
   });
   return cudaGetLastError();
 }
