@@ -94,7 +94,12 @@ Layout layout_of(const rmx_config& c) {
   nb = nb < 1 ? 1 : (nb > 64 ? 64 : nb);
   L.ra.nb = nb;
   L.ra.nbblk = c.B > 0 ? (c.B + nb - 1) / nb : 0;
-  const size_t P = (size_t)L.ra.nbblk * c.T;
+  int nbl = (c.B + 31) / 32;
+  nbl = nbl < 1 ? 1 : (nbl > 32 ? 32 : nbl);
+  L.ra.nb_ln = nbl;
+  L.ra.nbblk_ln = c.B > 0 ? (c.B + nbl - 1) / nbl : 0;
+  const size_t P = (size_t)L.ra.nbblk * c.T;     // gate-backward partial rows
+  const size_t PL = (size_t)L.ra.nbblk_ln * c.T; // LayerNorm-backward partial rows
 
   o = 0;
   L.ds2 = o; o = up(o + N * D * e);
@@ -104,18 +109,18 @@ Layout layout_of(const rmx_config& c) {
   L.ds1 = o; o = up(o + N * D * e);
   L.da0 = o; o = up(o + N * D * e);
   L.rowsum = o; o = up(o + N * 4 * sizeof(float));
-  L.pg2 = o; o = up(o + P * D * sizeof(float));
-  L.pb2 = o; o = up(o + P * D * sizeof(float));
-  L.pbo = o; o = up(o + P * D * sizeof(float));
+  L.pg2 = o; o = up(o + PL * D * sizeof(float));
+  L.pb2 = o; o = up(o + PL * D * sizeof(float));
+  L.pbo = o; o = up(o + PL * D * sizeof(float));
   L.pwx = o; o = up(o + P * H * sizeof(float));
   L.pbx = o; o = up(o + P * H * sizeof(float));
   L.pwg = o; o = up(o + P * H * sizeof(float));
   L.pbg = o; o = up(o + P * H * sizeof(float));
   L.pb1 = o; o = up(o + P * 2 * H * sizeof(float));
-  L.pg0 = o; o = up(o + P * D * sizeof(float));
-  L.pb0 = o; o = up(o + P * D * sizeof(float));
-  L.pg1 = o; o = up(o + P * D * sizeof(float));
-  L.pbe1 = o; o = up(o + P * D * sizeof(float));
+  L.pg0 = o; o = up(o + PL * D * sizeof(float));
+  L.pb0 = o; o = up(o + PL * D * sizeof(float));
+  L.pg1 = o; o = up(o + PL * D * sizeof(float));
+  L.pbe1 = o; o = up(o + PL * D * sizeof(float));
   L.ws_total = o;
   return L;
 }
@@ -124,6 +129,7 @@ Layout layout_of(const rmx_config& c) {
 rmx_status kernels_support(const rmx_config& c) {
   const int V = 16 / esize(c.dtype);
   if (c.D % V || c.H % V) return RMX_ERR_UNSUPPORTED;  // rows must be whole 16-byte vectors
+  if (c.D / kLnBwdColsPerThread > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
   if (c.D / V > kRowThreadsMax || c.H / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
   if ((c.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // LN forward: 10 vectors per lane
   return RMX_OK;
@@ -227,6 +233,41 @@ rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
   return l.done(e);
 }
 
+// Second stream for the weight-gradient GEMMs, which do not feed the rest of
+// the backward: wgrad2 runs beside the gate backward and dgrad1, wgrad1
+// beside the norm1/norm0 backward.  One per device, created on first use;
+// host-side enqueue of a backward is serialised so the shared events are
+// recorded and waited on in order.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork1 = nullptr, fork2 = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+
+SideStream* side_stream() {
+  static SideStream side[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& ss = side[dev];
+  if (!ss.s) {
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&ss.fork1, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork2, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    ss.s = s;
+  }
+  return &ss;
+}
+
+// Makes `to` wait for everything enqueued on `from` so far.
+rmx_status stream_wait(cudaStream_t to, cudaStream_t from, cudaEvent_t ev) {
+  if (cudaEventRecord(ev, from) != cudaSuccess) return RMX_ERR_CUDA;
+  if (cudaStreamWaitEvent(to, ev, 0) != cudaSuccess) return RMX_ERR_CUDA;
+  return RMX_OK;
+}
+
 inline char* at(void* base, size_t off) { return static_cast<char*>(base) + off; }
 inline const char* at(const void* base, size_t off) { return static_cast<const char*>(base) + off; }
 
@@ -320,9 +361,13 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     GemmDesc d{GEMM_DGRAD, EPI_STORE, c.dtype, c.B, c.H, c.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm2_dgrad", d, st));
   }
+  std::lock_guard<std::mutex> side_lock(g_side_mu);
+  SideStream* side = side_stream();
+  cudaStream_t wst = side ? side->s : st;  // weight-gradient GEMMs
+  if (side) RMX_TRY(stream_wait(wst, st, side->fork1));
   {
     GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
-    RMX_TRY(run_gemm("gemm2_wgrad", d, st));
+    RMX_TRY(run_gemm("gemm2_wgrad", d, wst));
   }
   {
     Launch l("gate_bwd_rowsums", st);
@@ -339,9 +384,10 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
     RMX_TRY(run_gemm("gemm1_dgrad", d, st));
   }
+  if (side) RMX_TRY(stream_wait(wst, st, side->fork2));
   {
     GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
-    RMX_TRY(run_gemm("gemm1_wgrad", d, st));
+    RMX_TRY(run_gemm("gemm1_wgrad", d, wst));
   }
   {
     Launch l("ln1_bwd_mixed", st);
@@ -355,18 +401,20 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   }
   {
     const int P = L.ra.nbblk * c.T, Pb = L.ra.nbblk;
+    const int PL = L.ra.nbblk_ln * c.T, PLb = L.ra.nbblk_ln;
     ColsumJob jobs[12] = {
-        {F(L.pg2), g.gamma2, P, c.D},          {F(L.pb2), g.beta2, P, c.D},
-        {F(L.pbo), g.bout, Pb, c.T * c.D},     {F(L.pwx), g.lnx_w, P, c.H},
+        {F(L.pg2), g.gamma2, PL, c.D},         {F(L.pb2), g.beta2, PL, c.D},
+        {F(L.pbo), g.bout, PLb, c.T * c.D},     {F(L.pwx), g.lnx_w, P, c.H},
         {F(L.pbx), g.lnx_b, P, c.H},           {F(L.pwg), g.lng_w, P, c.H},
         {F(L.pbg), g.lng_b, P, c.H},           {F(L.pb1), g.b1, Pb, c.T * 2 * c.H},
-        {F(L.pg1), g.gamma1, P, c.D},          {F(L.pbe1), g.beta1, P, c.D},
-        {F(L.pg0), g.gamma0, P, c.D},          {F(L.pb0), g.beta0, P, c.D},
+        {F(L.pg1), g.gamma1, PL, c.D},         {F(L.pbe1), g.beta1, PL, c.D},
+        {F(L.pg0), g.gamma0, PL, c.D},         {F(L.pb0), g.beta0, PL, c.D},
     };
     Launch l("colsums", st);
     cudaError_t e = launch_colsums(jobs, 12, c.dtype, st);
     RMX_TRY(l.done(e));
   }
+  if (side) RMX_TRY(stream_wait(st, wst, side->join));
   return RMX_OK;
 }
 

@@ -9,8 +9,10 @@ namespace rmx {
 // ------------------------------------------------------------------ row passes
 struct RowArgs {
   int B, T, D, H, dtype;
-  int nb;      // samples per CTA in the per-token (b-block, t) passes
-  int nbblk;   // ceil(B / nb)
+  int nb;        // samples per CTA in the per-token gate backward
+  int nbblk;     // ceil(B / nb)
+  int nb_ln;     // samples per CTA in the LayerNorm backward
+  int nbblk_ln;  // ceil(B / nb_ln)
 };
 
 // LayerNorm forward, one row per warp.  Modes: plain; output written
@@ -20,7 +22,7 @@ enum LnFwdMode { LNF_PLAIN = 0, LNF_MIXED_OUT = 1, LNF_SUM_IN = 2 };
 cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
                           const void* be, void* y, float* mu, float* rs, cudaStream_t st);
 // LayerNorm backward over CTAs (t, b-block); per-CTA partial sums of dgamma
-// and dbeta ([nbblk*T][D]).  Modes: LNB_BIAS also sums ds per token into
+// and dbeta ([nbblk_ln*T][D]).  Modes: LNB_BIAS also sums ds per token into
 // pbias; LNB_MIXED_TOO reads s + s_add and also writes token_mix(ds) to
 // out_mixed; LNB_RESID adds resid to the output.
 enum LnBwdMode { LNB_BIAS = 0, LNB_MIXED_TOO = 1, LNB_RESID = 2 };
@@ -59,6 +61,7 @@ cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStre
 
 // Largest thread count a row pass may use (one thread per 16-byte vector).
 constexpr int kRowThreadsMax = 512;
+constexpr int kLnBwdColsPerThread = 4;
 int max_dynamic_smem_bytes();
 
 // ------------------------------------------------------------------ GEMMs

@@ -64,7 +64,7 @@ extern "C" rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void
   }
   const int e = cfg->dtype == RMX_F32 ? 4 : 2;
   const int V = 16 / e;
-  if (cfg->D % V || cfg->D / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
+  if (cfg->D % V || cfg->D / kLnBwdColsPerThread > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
 
   // Partial sums per block of nb samples: gamma2 and beta2 [nbblk*T, D] and
   // bout [nbblk, T*D].  Use as many sample blocks as the array holds (at most
@@ -82,6 +82,8 @@ extern "C" rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void
   ra.dtype = cfg->dtype;
   ra.nb = (cfg->B + nbblk - 1) / nbblk;
   ra.nbblk = (cfg->B + ra.nb - 1) / ra.nb;
+  ra.nb_ln = ra.nb;
+  ra.nbblk_ln = ra.nbblk;
 
   float* scratch = scratch_on_current_device();
   if (!scratch) return RMX_ERR_CUDA;

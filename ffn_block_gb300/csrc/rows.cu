@@ -90,21 +90,39 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
   if (row >= N) return;
   const int nv = D / V;
   const T* srow = s + (size_t)row * D;
-  float v[MAXV][V];
+  // The row stays in registers: packed as loaded when it is one tensor, as
+  // fp32 when it is the sum of two.
+  constexpr bool SUM = MODE == LNF_SUM_IN;
+  uint4 raw[SUM ? 1 : MAXV];
+  float vf[SUM ? MAXV : 1][V];
+  auto get = [&](int q, float* v) {
+    if (SUM) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) v[e] = vf[q][e];
+    } else {
+      const T* el = reinterpret_cast<const T*>(&raw[q]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) v[e] = to_f(el[e]);
+    }
+  };
   float sum = 0.f;
 #pragma unroll
   for (int q = 0; q < MAXV; ++q) {
     const int vi = lane + 32 * q;
     if (vi < nv) {
-      load_vec(srow + vi * V, v[q]);
-      if (MODE == LNF_SUM_IN) {
+      if (SUM) {
         float a[V];
+        load_vec(srow + vi * V, vf[q]);
         load_vec(s_add + (size_t)row * D + vi * V, a);
 #pragma unroll
-        for (int e = 0; e < V; ++e) v[q][e] += a[e];
+        for (int e = 0; e < V; ++e) vf[q][e] += a[e];
+      } else {
+        raw[q] = *reinterpret_cast<const uint4*>(srow + vi * V);
       }
+      float v[V];
+      get(q, v);
 #pragma unroll
-      for (int e = 0; e < V; ++e) sum += v[q][e];
+      for (int e = 0; e < V; ++e) sum += v[e];
     }
   }
   const float invD = 1.0f / (float)D;
@@ -114,9 +132,11 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
   for (int q = 0; q < MAXV; ++q) {
     const int vi = lane + 32 * q;
     if (vi < nv) {
+      float v[V];
+      get(q, v);
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        const float c = v[q][e] - mean;
+        const float c = v[e] - mean;
         ss += c * c;
       }
     }
@@ -127,11 +147,12 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
   for (int q = 0; q < MAXV; ++q) {
     const int vi = lane + 32 * q;
     if (vi < nv) {
-      float gg[V], bb[V], o[V];
+      float v[V], gg[V], bb[V], o[V];
+      get(q, v);
       load_vec(g + vi * V, gg);
       load_vec(be + vi * V, bb);
 #pragma unroll
-      for (int e = 0; e < V; ++e) o[e] = (v[q][e] - mean) * rstd * gg[e] + bb[e];
+      for (int e = 0; e < V; ++e) o[e] = (v[e] - mean) * rstd * gg[e] + bb[e];
       if (MODE == LNF_MIXED_OUT) store_mixed<T, V>(y + (size_t)b * Tn * D, o, j, vi * V, C, D);
       else store_vec(y + (size_t)row * D + vi * V, o);
     }
@@ -143,6 +164,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
 }
 
 constexpr int kLnBwdRows = 4;  // rows per barrier
+constexpr int kLnBwdCols = 4;  // columns per thread
 
 // =========================================================================
 // LayerNorm backward for rows (b, t), CTA (t, b-block) -- t varies fastest
@@ -155,7 +177,8 @@ constexpr int kLnBwdRows = 4;  // rows per barrier
 //   LNB_MIXED_TOO  s = s + s_add; out = ds and out_mixed = token_mix(ds)
 //                                                           (norm1: s1 = mix + x)
 //   LNB_RESID      out = ds + resid                         (norm0 + residual)
-// Thread v owns columns v*V ..; kLnBwdRows rows share one block reduction.
+// Thread v owns columns 4v .. 4v+3 (8- or 16-byte accesses); kLnBwdRows
+// rows share one block reduction.
 // =========================================================================
 template <typename T, int MODE>
 __global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const T* __restrict__ s,
@@ -165,22 +188,22 @@ __global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const
                                                 T* __restrict__ out_mixed, float* __restrict__ pg,
                                                 float* __restrict__ pb, float* __restrict__ pbias, int B, int Tn,
                                                 int D, int C, int nb) {
-  constexpr int V = VecN<T>::value;
+  constexpr int E = kLnBwdCols;
   constexpr int RB = kLnBwdRows;
   __shared__ float red[2 * 32 * 2 * RB];
   int slot = 0;
   const int t = blockIdx.x, bblk = blockIdx.y;
   const int v = threadIdx.x;
-  const bool act = v * V < D;
-  const int d0 = v * V;
-  float gam[V], ag[V], ab[V], ao[V];
+  const bool act = v * E < D;
+  const int d0 = v * E;
+  float gam[E], ag[E], ab[E], ao[E];
 #pragma unroll
-  for (int e = 0; e < V; ++e) ag[e] = ab[e] = ao[e] = 0.f;
-  if (act) load_vec(gamma + d0, gam);
+  for (int e = 0; e < E; ++e) ag[e] = ab[e] = ao[e] = 0.f;
+  if (act) load_n<T, E>(gamma + d0, gam);
   const float invD = 1.0f / (float)D;
   const int b_begin = bblk * nb, b_end = min(B, b_begin + nb);
   for (int b0 = b_begin; b0 < b_end; b0 += RB) {
-    float gv[RB][V], xh[RB][V], sums[2 * RB];
+    float gv[RB][E], xh[RB][E], sums[2 * RB];
     float rstd[RB];
 #pragma unroll
     for (int rr = 0; rr < RB; ++rr) {
@@ -192,17 +215,17 @@ __global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const
         const float mean = mu[r];
         rstd[rr] = rs[r];
         if (act) {
-          float sv[V];
-          load_vec(gin + r * D + d0, gv[rr]);
-          load_vec(s + r * D + d0, sv);
+          float sv[E];
+          load_n<T, E>(gin + r * D + d0, gv[rr]);
+          load_n<T, E>(s + r * D + d0, sv);
           if (MODE == LNB_MIXED_TOO) {
-            float a[V];
-            load_vec(s_add + r * D + d0, a);
+            float a[E];
+            load_n<T, E>(s_add + r * D + d0, a);
 #pragma unroll
-            for (int e = 0; e < V; ++e) sv[e] += a[e];
+            for (int e = 0; e < E; ++e) sv[e] += a[e];
           }
 #pragma unroll
-          for (int e = 0; e < V; ++e) {
+          for (int e = 0; e < E; ++e) {
             xh[rr][e] = (sv[e] - mean) * rstd[rr];
             const float g = gam[e] * gv[rr][e];
             sums[2 * rr] += g;
@@ -218,28 +241,28 @@ __global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const
       if (b >= b_end || !act) continue;
       const size_t r = (size_t)b * Tn + t;
       const float mg = sums[2 * rr] * invD, mgx = sums[2 * rr + 1] * invD;
-      float o[V];
+      float o[E];
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
+      for (int e = 0; e < E; ++e) {
         o[e] = rstd[rr] * (gam[e] * gv[rr][e] - mg - xh[rr][e] * mgx);
         ag[e] += gv[rr][e] * xh[rr][e];
         ab[e] += gv[rr][e];
         if (MODE == LNB_BIAS) ao[e] += o[e];
       }
-      if (MODE == LNB_MIXED_TOO) store_mixed<T, V>(out_mixed + (size_t)b * Tn * D, o, t, d0, C, D);
+      if (MODE == LNB_MIXED_TOO) store_mixed<T, E>(out_mixed + (size_t)b * Tn * D, o, t, d0, C, D);
       if (MODE == LNB_RESID) {
-        float rv[V];
-        load_vec(resid + r * D + d0, rv);
+        float rv[E];
+        load_n<T, E>(resid + r * D + d0, rv);
 #pragma unroll
-        for (int e = 0; e < V; ++e) o[e] += rv[e];
+        for (int e = 0; e < E; ++e) o[e] += rv[e];
       }
-      store_vec(out + r * D + d0, o);
+      store_n<T, E>(out + r * D + d0, o);
     }
   }
   if (act) {
     const size_t p = (size_t)bblk * Tn + t;
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
+    for (int e = 0; e < E; ++e) {
       pg[p * D + d0 + e] = ag[e];
       pb[p * D + d0 + e] = ab[e];
       if (MODE == LNB_BIAS) pbias[p * D + d0 + e] = ao[e];
@@ -315,27 +338,37 @@ __global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const
   const int r0 = blockIdx.x * kGateRows;
   const int nrows = min(kGateRows, N - r0);
   const int tiles = zstats_tiles(H);
-  if ((int)threadIdx.x < nrows) {
-    const int r = r0 + threadIdx.x;
-    Moments u = {0.f, 0.f, 0.f}, g = {0.f, 0.f, 0.f};
-    for (int j = 0; j < tiles; ++j) {
-      const float4 t = *reinterpret_cast<const float4*>(zstats + ((size_t)r * tiles + j) * 4);
-      const int lo = j * kZStatsTile, hi = min(2 * H, lo + kZStatsTile);
-      const float nu = (float)max(0, min(H, hi) - lo);
-      const float ng = (float)max(0, hi - max(H, lo));
-      if (nu > 0.f) u = merge_moments(u, Moments{nu, t.x, t.y});
-      if (ng > 0.f) g = merge_moments(g, Moments{ng, t.z, t.w});
+  // One warp per row merges the row's group statistics: lane l takes groups
+  // l, l+32, ... in order, then the lanes are merged pairwise (fixed order,
+  // every lane ends with the same values).
+  {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int i = warp; i < nrows; i += nw) {
+      const int r = r0 + i;
+      Moments u = {0.f, 0.f, 0.f}, g = {0.f, 0.f, 0.f};
+      for (int j = lane; j < tiles; j += 32) {
+        const float4 t = *reinterpret_cast<const float4*>(zstats + ((size_t)r * tiles + j) * 4);
+        const int lo = j * kZStatsTile, hi = min(2 * H, lo + kZStatsTile);
+        const float nu = (float)max(0, min(H, hi) - lo);
+        const float ng = (float)max(0, hi - max(H, lo));
+        if (nu > 0.f) u = merge_moments(u, Moments{nu, t.x, t.y});
+        if (ng > 0.f) g = merge_moments(g, Moments{ng, t.z, t.w});
+      }
+      u = warp_merge_moments(u);
+      g = warp_merge_moments(g);
+      if (lane == 0) {
+        const float rsu = 1.0f / sqrtf(u.m2 / (float)H + eps);
+        const float rsg = 1.0f / sqrtf(g.m2 / (float)H + eps);
+        st[i][0] = u.mean;
+        st[i][1] = rsu;
+        st[i][2] = g.mean;
+        st[i][3] = rsg;
+        muU[r] = u.mean;
+        rU[r] = rsu;
+        muG[r] = g.mean;
+        rG[r] = rsg;
+      }
     }
-    const float rsu = 1.0f / sqrtf(u.m2 / (float)H + eps);
-    const float rsg = 1.0f / sqrtf(g.m2 / (float)H + eps);
-    st[threadIdx.x][0] = u.mean;
-    st[threadIdx.x][1] = rsu;
-    st[threadIdx.x][2] = g.mean;
-    st[threadIdx.x][3] = rsg;
-    muU[r] = u.mean;
-    rU[r] = rsu;
-    muG[r] = g.mean;
-    rG[r] = rsg;
   }
   __syncthreads();
   const int nv = H / V;
@@ -357,7 +390,7 @@ __global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const
       for (int e = 0; e < V; ++e) {
         const float uu = (u[e] - mU) * sU * fwx[e] + fbx[e];
         const float gg = (g[e] - mG) * sG * fwg[e] + fbg[e];
-        o[e] = uu * (gg / (1.0f + expf(-gg)));
+        o[e] = uu * gg * __frcp_rn(1.0f + expf(-gg));
       }
       store_vec(hidden + (size_t)(r0 + i) * H + h0, o);
     }
@@ -388,7 +421,7 @@ __device__ __forceinline__ void gate_bwd_elem(const float* dhv, const float* zu,
     Gh[e] = (zg[e] - mG) * sG;
     const float u = fwx[e] * Uh[e] + fbx[e];
     const float g = fwg[e] * Gh[e] + fbg[e];
-    const float sg = 1.0f / (1.0f + expf(-g));
+    const float sg = __frcp_rn(1.0f + expf(-g));
     du[e] = dhv[e] * (g * sg);
     dg[e] = dhv[e] * u * (sg * (1.0f + g * (1.0f - sg)));
   }
@@ -571,15 +604,15 @@ cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void*
 cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s, const void* s_add,
                           const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
                           void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
-  const int threads = round32(a.D / vec_elems(a.dtype));
+  const int threads = round32(a.D / kLnBwdCols);
   if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
-  dim3 grid(a.T, a.nbblk);
+  dim3 grid(a.T, a.nbblk_ln);
   const int C = a.D / a.T;
 #define RMX_LNB(M)                                                                                             \
   RMX_DISPATCH_T(a.dtype, {                                                                                    \
     k_ln_bwd<T, M><<<grid, threads, 0, st>>>((const T*)gin, (const T*)s, (const T*)s_add, mu, rs,              \
                                              (const T*)gamma, (const T*)resid, (T*)out, (T*)out_mixed, pg, pb, \
-                                             pbias, a.B, a.T, a.D, C, a.nb);                                   \
+                                             pbias, a.B, a.T, a.D, C, a.nb_ln);                                \
   })
   if (mode == LNB_BIAS) RMX_LNB(LNB_BIAS);
   else if (mode == LNB_MIXED_TOO) RMX_LNB(LNB_MIXED_TOO);
