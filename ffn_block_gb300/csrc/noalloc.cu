@@ -23,8 +23,8 @@
 namespace rmx {
 namespace {
 
-// Capacity of the shared scratch array, in floats (8 MiB).
-constexpr size_t kNoAllocScratchFloats = size_t(2) << 20;
+// Capacity of the shared scratch array, in floats (16 MiB).
+constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
@@ -66,28 +66,24 @@ extern "C" rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void
   const int V = 16 / e;
   if (cfg->D % V || cfg->D / kLnBwdColsPerThread > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
 
-  // Partial sums per block of nb samples: gamma2 and beta2 [nbblk*T, D] and
-  // bout [nbblk, T*D].  Use as many sample blocks as the array holds (at most
-  // 16); a shape whose single block does not fit is rejected.
-  const size_t per_block = (size_t)3 * cfg->T * cfg->D;
-  if (per_block > kNoAllocScratchFloats) return RMX_ERR_UNSUPPORTED;
-  int nbblk = (int)(kNoAllocScratchFloats / per_block);
-  if (nbblk > 16) nbblk = 16;
-  if (nbblk > cfg->B) nbblk = cfg->B;
+  // Partial sums per block of up to 64 samples: gamma2 and beta2
+  // [nbblk*T, D] and bout [nbblk, T*D].  Shapes whose partial sums exceed the
+  // array are rejected.
   RowArgs ra;
   ra.B = cfg->B;
   ra.T = cfg->T;
   ra.D = cfg->D;
   ra.H = cfg->H;
   ra.dtype = cfg->dtype;
-  ra.nb = (cfg->B + nbblk - 1) / nbblk;
-  ra.nbblk = (cfg->B + ra.nb - 1) / ra.nb;
-  ra.nb_ln = ra.nb;
-  ra.nbblk_ln = ra.nbblk;
+  ra.nb_ln = cfg->B < 64 ? cfg->B : 64;
+  ra.nbblk_ln = (cfg->B + ra.nb_ln - 1) / ra.nb_ln;
+  ra.nb = ra.nb_ln;
+  ra.nbblk = ra.nbblk_ln;
+  if ((size_t)3 * ra.nbblk_ln * cfg->T * cfg->D > kNoAllocScratchFloats) return RMX_ERR_UNSUPPORTED;
 
   float* scratch = scratch_on_current_device();
   if (!scratch) return RMX_ERR_CUDA;
-  const size_t P = (size_t)ra.nbblk * cfg->T;
+  const size_t P = (size_t)ra.nbblk_ln * cfg->T;
   float* pg2 = scratch;
   float* pb2 = pg2 + P * cfg->D;
   float* pbo = pb2 + P * cfg->D;
@@ -99,7 +95,7 @@ extern "C" rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void
   ColsumJob jobs[3] = {
       {pg2, dgamma2, (int)P, cfg->D},
       {pb2, dbeta2, (int)P, cfg->D},
-      {pbo, dbout, ra.nbblk, cfg->T * cfg->D},
+      {pbo, dbout, ra.nbblk_ln, cfg->T * cfg->D},
   };
   if (launch_colsums(jobs, 3, cfg->dtype, st) != cudaSuccess) return RMX_ERR_CUDA;
   return RMX_OK;

@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
   }
 }
 
-constexpr int kLnBwdRows = 4;  // rows per barrier
-constexpr int kLnBwdCols = 4;  // columns per thread
+constexpr int kLnBwdCols = 4;      // columns per thread in the apply sweep
+constexpr int kLnBwdMaxRows = 64;  // rows per CTA (shared row sums)
 
 // =========================================================================
 // LayerNorm backward for rows (b, t), CTA (t, b-block) -- t varies fastest
@@ -177,8 +177,10 @@ constexpr int kLnBwdCols = 4;  // columns per thread
 //   LNB_MIXED_TOO  s = s + s_add; out = ds and out_mixed = token_mix(ds)
 //                                                           (norm1: s1 = mix + x)
 //   LNB_RESID      out = ds + resid                         (norm0 + residual)
-// Thread v owns columns 4v .. 4v+3 (8- or 16-byte accesses); kLnBwdRows
-// rows share one block reduction.
+// Two sweeps over the CTA's rows with one barrier between them: (1) one warp
+// per row takes the two row sums with 16-byte loads; (2) thread v owns
+// columns 4v .. 4v+3 of every row, re-reads them (now cache-resident),
+// writes the outputs and keeps the column partial sums in registers.
 // =========================================================================
 template <typename T, int MODE>
 __global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const T* __restrict__ s,
@@ -188,85 +190,92 @@ __global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const
                                                 T* __restrict__ out_mixed, float* __restrict__ pg,
                                                 float* __restrict__ pb, float* __restrict__ pbias, int B, int Tn,
                                                 int D, int C, int nb) {
+  constexpr int V = VecN<T>::value;
   constexpr int E = kLnBwdCols;
-  constexpr int RB = kLnBwdRows;
-  __shared__ float red[2 * 32 * 2 * RB];
-  int slot = 0;
+  __shared__ float2 rsum[kLnBwdMaxRows];
   const int t = blockIdx.x, bblk = blockIdx.y;
-  const int v = threadIdx.x;
-  const bool act = v * E < D;
-  const int d0 = v * E;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int b_begin = bblk * nb;
+  const int nrows = max(0, min(B, b_begin + nb) - b_begin);
+  const float invD = 1.0f / (float)D;
+
+  // ---- sweep 1: row sums of g and g * xh, one warp per row.
+  const int nv = D / V;
+  for (int i = warp; i < nrows; i += nw) {
+    const size_t r = (size_t)(b_begin + i) * Tn + t;
+    const float mean = mu[r], rstd = rs[r];
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 2
+    for (int vi = lane; vi < nv; vi += 32) {
+      float gv[V], sv[V], gm[V];
+      load_vec(gin + r * D + vi * V, gv);
+      load_vec(s + r * D + vi * V, sv);
+      load_vec(gamma + vi * V, gm);
+      if (MODE == LNB_MIXED_TOO) {
+        float av[V];
+        load_vec(s_add + r * D + vi * V, av);
+#pragma unroll
+        for (int e = 0; e < V; ++e) sv[e] += av[e];
+      }
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const float g = gm[e] * gv[e];
+        a0 += g;
+        a1 += g * (sv[e] - mean) * rstd;
+      }
+    }
+    a0 = warp_sum(a0);
+    a1 = warp_sum(a1);
+    if (lane == 0) rsum[i] = make_float2(a0, a1);
+  }
+  __syncthreads();
+
+  // ---- sweep 2: outputs and column partial sums.
+  const int d0 = threadIdx.x * E;
+  if (d0 >= D) return;
   float gam[E], ag[E], ab[E], ao[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) ag[e] = ab[e] = ao[e] = 0.f;
-  if (act) load_n<T, E>(gamma + d0, gam);
-  const float invD = 1.0f / (float)D;
-  const int b_begin = bblk * nb, b_end = min(B, b_begin + nb);
-  for (int b0 = b_begin; b0 < b_end; b0 += RB) {
-    float gv[RB][E], xh[RB][E], sums[2 * RB];
-    float rstd[RB];
+  load_n<T, E>(gamma + d0, gam);
+#pragma unroll 2
+  for (int i = 0; i < nrows; ++i) {
+    const int b = b_begin + i;
+    const size_t r = (size_t)b * Tn + t;
+    const float mean = mu[r], rstd = rs[r];
+    const float2 sm = rsum[i];
+    const float mg = sm.x * invD, mgx = sm.y * invD;
+    float gv[E], sv[E], o[E];
+    load_n<T, E>(gin + r * D + d0, gv);
+    load_n<T, E>(s + r * D + d0, sv);
+    if (MODE == LNB_MIXED_TOO) {
+      float av[E];
+      load_n<T, E>(s_add + r * D + d0, av);
 #pragma unroll
-    for (int rr = 0; rr < RB; ++rr) {
-      sums[2 * rr] = sums[2 * rr + 1] = 0.f;
-      rstd[rr] = 0.f;
-      const int b = b0 + rr;
-      if (b < b_end) {
-        const size_t r = (size_t)b * Tn + t;
-        const float mean = mu[r];
-        rstd[rr] = rs[r];
-        if (act) {
-          float sv[E];
-          load_n<T, E>(gin + r * D + d0, gv[rr]);
-          load_n<T, E>(s + r * D + d0, sv);
-          if (MODE == LNB_MIXED_TOO) {
-            float a[E];
-            load_n<T, E>(s_add + r * D + d0, a);
-#pragma unroll
-            for (int e = 0; e < E; ++e) sv[e] += a[e];
-          }
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            xh[rr][e] = (sv[e] - mean) * rstd[rr];
-            const float g = gam[e] * gv[rr][e];
-            sums[2 * rr] += g;
-            sums[2 * rr + 1] += g * xh[rr][e];
-          }
-        }
-      }
+      for (int e = 0; e < E; ++e) sv[e] += av[e];
     }
-    block_sum<2 * RB>(sums, red, slot);
-#pragma unroll
-    for (int rr = 0; rr < RB; ++rr) {
-      const int b = b0 + rr;
-      if (b >= b_end || !act) continue;
-      const size_t r = (size_t)b * Tn + t;
-      const float mg = sums[2 * rr] * invD, mgx = sums[2 * rr + 1] * invD;
-      float o[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        o[e] = rstd[rr] * (gam[e] * gv[rr][e] - mg - xh[rr][e] * mgx);
-        ag[e] += gv[rr][e] * xh[rr][e];
-        ab[e] += gv[rr][e];
-        if (MODE == LNB_BIAS) ao[e] += o[e];
-      }
-      if (MODE == LNB_MIXED_TOO) store_mixed<T, E>(out_mixed + (size_t)b * Tn * D, o, t, d0, C, D);
-      if (MODE == LNB_RESID) {
-        float rv[E];
-        load_n<T, E>(resid + r * D + d0, rv);
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] += rv[e];
-      }
-      store_n<T, E>(out + r * D + d0, o);
-    }
-  }
-  if (act) {
-    const size_t p = (size_t)bblk * Tn + t;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      pg[p * D + d0 + e] = ag[e];
-      pb[p * D + d0 + e] = ab[e];
-      if (MODE == LNB_BIAS) pbias[p * D + d0 + e] = ao[e];
+      const float xh = (sv[e] - mean) * rstd;
+      o[e] = rstd * (gam[e] * gv[e] - mg - xh * mgx);
+      ag[e] += gv[e] * xh;
+      ab[e] += gv[e];
+      if (MODE == LNB_BIAS) ao[e] += o[e];
     }
+    if (MODE == LNB_MIXED_TOO) store_mixed<T, E>(out_mixed + (size_t)b * Tn * D, o, t, d0, C, D);
+    if (MODE == LNB_RESID) {
+      float rv[E];
+      load_n<T, E>(resid + r * D + d0, rv);
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[e] += rv[e];
+    }
+    store_n<T, E>(out + r * D + d0, o);
+  }
+  const size_t p = (size_t)bblk * Tn + t;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    pg[p * D + d0 + e] = ag[e];
+    pb[p * D + d0 + e] = ab[e];
+    if (MODE == LNB_BIAS) pbias[p * D + d0 + e] = ao[e];
   }
 }
 
@@ -605,7 +614,7 @@ cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const voi
                           const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
                           void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
   const int threads = round32(a.D / kLnBwdCols);
-  if (threads > kRowThreadsMax) return cudaErrorInvalidValue;
+  if (threads > kRowThreadsMax || a.nb_ln > kLnBwdMaxRows) return cudaErrorInvalidValue;
   dim3 grid(a.T, a.nbblk_ln);
   const int C = a.D / a.T;
 #define RMX_LNB(M)                                                                                             \

@@ -182,11 +182,11 @@ rmx_status rmx_test_gemm(int kind, int dtype, int M, int N, int K, int G, const 
  * rmx_forward stores them in its saved buffer (s2 is the fourth tensor,
  * mean2/rstd2 the fifth and sixth statistic vectors).
  *
- * Scratch: the partial sums live in a fixed device array of 8 MiB inside
+ * Scratch: the partial sums live in a fixed device array of 16 MiB inside
  * the library, reserved on each GPU when the library is first used there and
  * held until the process exits.  This call allocates nothing.  Shapes whose
- * partial sums for one block of samples (3*T*D floats) exceed 8 MiB, and
- * B == 0, are rejected (RMX_ERR_UNSUPPORTED / RMX_ERR_INVALID_ARG) before any
+ * partial sums (3 * ceil(B/64) * T * D floats) exceed 16 MiB, and B == 0,
+ * are rejected (RMX_ERR_UNSUPPORTED / RMX_ERR_INVALID_ARG) before any
  * launch.  The first call on each device looks up the array's device address
  * with the device current; make that first call before any stream capture.
  * Every call uses the same array: calls that overlap on the GPU (on

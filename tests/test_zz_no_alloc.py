@@ -47,6 +47,7 @@ def _rel(a, ref):
 
 
 @pytest.mark.parametrize("dims,dtype", [
+    (dict(B=1024, T=64, D=1280, H=256), "bf16"),   # production B, T, D
     (dict(B=256, T=32, D=512, H=1536), "bf16"),
     (dict(B=37, T=8, D=240, H=360), "f16"),
     (dict(B=64, T=16, D=256, H=512), "f32"),
@@ -82,7 +83,7 @@ def test_noalloc_norm2_backward_matches_rmx_backward(dims, dtype):
 
 
 def test_noalloc_rejects_oversized_and_bad_arguments():
-    big = B.make_config(4, 256, 4096, 128, "bf16")       # 3*T*D floats > the 8 MiB array
+    big = B.make_config(4, 1024, 2048, 128, "bf16")      # 3*T*D floats > the 16 MiB array
     p = 0x1000
     assert B.rmx_ln2_backward_noalloc(big, p, p, p, p, p, p, p, p, p) == B.RMX_ERR_UNSUPPORTED
     cfg = B.make_config(4, 8, 64, 128, "bf16")
