@@ -57,7 +57,7 @@ struct Layout {
   // saved (filled by the forward)
   size_t out1, Z, hidden, s2, stats, zstats, mix0, saved_total;
   // backward scratch
-  size_t ds2, dh, dZ, dout1, ds1, da0, rowsum, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
+  size_t ds2, dh, dZ, dout1, ds1, da0, rowsum, rowpart, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
   RowArgs ra;
 };
 
@@ -109,6 +109,7 @@ Layout layout_of(const rmx_config& c) {
   L.ds1 = o; o = up(o + N * D * e);
   L.da0 = o; o = up(o + N * D * e);
   L.rowsum = o; o = up(o + N * 4 * sizeof(float));
+  L.rowpart = o; o = up(o + N * (size_t)rowpart_groups(c.H) * 4 * sizeof(float));
   L.pg2 = o; o = up(o + PL * D * sizeof(float));
   L.pb2 = o; o = up(o + PL * D * sizeof(float));
   L.pbo = o; o = up(o + PL * D * sizeof(float));
@@ -320,9 +321,13 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
     }
   }
   {
+    Launch l("gate_stats", st);
+    RMX_TRY(l.done(launch_zstats_merge(L.ra, zstats, S.muU, S.rU, S.muG, S.rG, st)));
+  }
+  {
     Launch l("gate_fwd", st);
-    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, zstats, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b, hidden, S.muU, S.rU,
-                                   S.muG, S.rG, st)));
+    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b, hidden,
+                                   st)));
   }
   {
     GemmDesc d{GEMM_FWD, EPI_BIAS_RESID, c.dtype, c.B, c.D, c.H, c.T, hidden, p.wout, s2, p.bout, out1};
@@ -357,8 +362,20 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     Launch l("ln2_bwd", st);
     RMX_TRY(l.done(launch_ln2_bwd(L.ra, dy, s2, S.mu2, S.r2, p.gamma2, ds2, F(L.pg2), F(L.pb2), F(L.pbo), st)));
   }
+  // dh = ds2 @ wout^T; on the tensor-core path the epilogue also takes the
+  // gate backward's row sums per column group.
+  bool gate_sums_fused = false;
   {
-    GemmDesc d{GEMM_DGRAD, EPI_STORE, c.dtype, c.B, c.H, c.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
+    GemmDesc d{GEMM_DGRAD, EPI_GATE_ROWSUMS, c.dtype, c.B, c.H, c.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
+    d.gz = Z;
+    d.gstats = S.muU;
+    d.gw[0] = p.lnx_w;
+    d.gw[1] = p.lnx_b;
+    d.gw[2] = p.lng_w;
+    d.gw[3] = p.lng_b;
+    d.rowpart = F(L.rowpart);
+    gate_sums_fused = c.dtype != RMX_F32 && gemm_tc_supported(d);
+    if (!gate_sums_fused) d.epi = EPI_STORE;
     RMX_TRY(run_gemm("gemm2_dgrad", d, st));
   }
   std::lock_guard<std::mutex> side_lock(g_side_mu);
@@ -369,7 +386,10 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm2_wgrad", d, wst));
   }
-  {
+  if (gate_sums_fused) {
+    Launch l("gate_bwd_rowsums", st);
+    RMX_TRY(l.done(launch_rowpart_sum(L.ra, F(L.rowpart), F(L.rowsum), st)));
+  } else {
     Launch l("gate_bwd_rowsums", st);
     RMX_TRY(l.done(launch_gate_bwd_rowsums(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w,
                                            p.lng_b, F(L.rowsum), st)));

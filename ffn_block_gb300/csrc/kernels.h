@@ -34,11 +34,14 @@ cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const voi
 cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
                            const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
                            float* pbo, cudaStream_t st);
-// Forward: hidden = LN_x(U) * silu(LN_gate(G)) from Z = [U | G], with the
-// row statistics merged from `zstats` (see below).
-cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, const void* wx,
-                            const void* bx, const void* wg, const void* bg, void* hidden, float* muU,
-                            float* rU, float* muG, float* rG, cudaStream_t st);
+// Forward of the gate: (1) per-row mean and 1/sqrt(var+eps) of U and G
+// merged from `zstats` (see below); (2) hidden = LN_x(U) * silu(LN_gate(G))
+// from Z = [U | G], elementwise.
+cudaError_t launch_zstats_merge(const RowArgs& a, const float* zstats, float* muU, float* rU, float* muG, float* rG,
+                                cudaStream_t st);
+cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* muU, const float* rU, const float* muG,
+                            const float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
+                            void* hidden, cudaStream_t st);
 // Backward of the gate and both inner LNs, two streaming passes:
 // (1) rowsum[r] = {sum gU, sum gU*Uh, sum gG, sum gG*Gh} ([B*T][4] floats);
 // (2) dZ plus per-CTA partial sums of dwx, dbx, dwg, dbg and db1.
@@ -66,7 +69,14 @@ int max_dynamic_smem_bytes();
 
 // ------------------------------------------------------------------ GEMMs
 enum GemmKind { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
-enum GemmEpi { EPI_STORE = 0, EPI_BIAS = 1, EPI_BIAS_RESID = 2, EPI_RESID = 3, EPI_BIAS_ZSTATS = 4 };
+enum GemmEpi {
+  EPI_STORE = 0,
+  EPI_BIAS = 1,
+  EPI_BIAS_RESID = 2,
+  EPI_RESID = 3,
+  EPI_BIAS_ZSTATS = 4,    // + per-group statistics of Z (GEMM1 forward)
+  EPI_GATE_ROWSUMS = 5,   // + per-group row sums of the gate backward (dgrad2)
+};
 
 // Row statistics of Z = [U | G] in 128-column groups: for row r and group j
 // (columns [128 j, 128 j + 128) of the 2H-wide row), zstats[(r * groups + j)
@@ -93,7 +103,21 @@ struct GemmDesc {
   const void* resid;
   float* zstats;  // EPI_BIAS_ZSTATS only
   int split;      // EPI_BIAS_ZSTATS: first column of the G half (H)
+  // EPI_GATE_ROWSUMS (C = dh [M,G,H]): Z [M,G,2H], the statistics of U and G
+  // (four consecutive float vectors mean_U, rstd_U, mean_G, rstd_G of length
+  // M*G), the four inner-LN parameter vectors wx, bx, wg, bg, and the output
+  // rowpart[(row * groups + j) * 4 + {0..3}] = partial sums over column group
+  // j (kZStatsTile columns) of gU, gU*Uh, gG, gG*Gh.
+  const void* gz;
+  const float* gstats;
+  const void* gw[4];
+  float* rowpart;
 };
+
+// Row sums of the gate backward from their per-group partials:
+// rowsum[r] = sum over groups of rowpart[r][j] (fixed order).
+cudaError_t launch_rowpart_sum(const RowArgs& a, const float* rowpart, float* rowsum, cudaStream_t st);
+inline int rowpart_groups(int H) { return (H + kZStatsTile - 1) / kZStatsTile; }
 
 bool gemm_tc_supported(const GemmDesc& d);
 cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st);

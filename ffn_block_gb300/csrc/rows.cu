@@ -326,84 +326,86 @@ __global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* 
 }
 
 // =========================================================================
-// F3: hidden = LN_x(U) * silu(LN_gate(G)), Z = [U | G] per row.  A CTA takes
-// `rpc` rows: first one thread per row merges the row's tile statistics
-// (Chan, Golub and LeVeque's pairwise update, tiles in order) into mean and
-// 1/sqrt(var + eps) of U and G; then thread v handles columns v*V .. v*V+V-1
-// of both halves of every row, so the pass is one read of Z and one write of
-// hidden with no per-row barrier.
+// F3a: per-row statistics of U and G from the group statistics: one warp per
+// row; lane l merges groups l, l+32, ... in order (Chan, Golub and LeVeque's
+// pairwise update), then the lanes merge pairwise in a fixed order.  Writes
+// mean and 1/sqrt(var + eps) of U and of G.
 // =========================================================================
-constexpr int kGateRows = 16;
-
-template <typename T>
-__global__ void __launch_bounds__(512) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
-                                                  const T* __restrict__ wx, const T* __restrict__ bx,
-                                                  const T* __restrict__ wg, const T* __restrict__ bg,
-                                                  T* __restrict__ hidden, float* __restrict__ muU,
-                                                  float* __restrict__ rU, float* __restrict__ muG,
-                                                  float* __restrict__ rG, int N, int H, float eps) {
-  constexpr int V = VecN<T>::value;
-  __shared__ float st[kGateRows][4];
-  const int r0 = blockIdx.x * kGateRows;
-  const int nrows = min(kGateRows, N - r0);
+__global__ void __launch_bounds__(256) k_zstats_merge(const float* __restrict__ zstats, float* __restrict__ muU,
+                                                      float* __restrict__ rU, float* __restrict__ muG,
+                                                      float* __restrict__ rG, int N, int H, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= N) return;
   const int tiles = zstats_tiles(H);
-  // One warp per row merges the row's group statistics: lane l takes groups
-  // l, l+32, ... in order, then the lanes are merged pairwise (fixed order,
-  // every lane ends with the same values).
-  {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int i = warp; i < nrows; i += nw) {
-      const int r = r0 + i;
-      Moments u = {0.f, 0.f, 0.f}, g = {0.f, 0.f, 0.f};
-      for (int j = lane; j < tiles; j += 32) {
-        const float4 t = *reinterpret_cast<const float4*>(zstats + ((size_t)r * tiles + j) * 4);
-        const int lo = j * kZStatsTile, hi = min(2 * H, lo + kZStatsTile);
-        const float nu = (float)max(0, min(H, hi) - lo);
-        const float ng = (float)max(0, hi - max(H, lo));
-        if (nu > 0.f) u = merge_moments(u, Moments{nu, t.x, t.y});
-        if (ng > 0.f) g = merge_moments(g, Moments{ng, t.z, t.w});
-      }
-      u = warp_merge_moments(u);
-      g = warp_merge_moments(g);
-      if (lane == 0) {
-        const float rsu = 1.0f / sqrtf(u.m2 / (float)H + eps);
-        const float rsg = 1.0f / sqrtf(g.m2 / (float)H + eps);
-        st[i][0] = u.mean;
-        st[i][1] = rsu;
-        st[i][2] = g.mean;
-        st[i][3] = rsg;
-        muU[r] = u.mean;
-        rU[r] = rsu;
-        muG[r] = g.mean;
-        rG[r] = rsg;
-      }
-    }
+  Moments u = {0.f, 0.f, 0.f}, g = {0.f, 0.f, 0.f};
+  for (int j = lane; j < tiles; j += 32) {
+    const float4 t = *reinterpret_cast<const float4*>(zstats + ((size_t)r * tiles + j) * 4);
+    const int lo = j * kZStatsTile, hi = min(2 * H, lo + kZStatsTile);
+    const float nu = (float)max(0, min(H, hi) - lo);
+    const float ng = (float)max(0, hi - max(H, lo));
+    if (nu > 0.f) u = merge_moments(u, Moments{nu, t.x, t.y});
+    if (ng > 0.f) g = merge_moments(g, Moments{ng, t.z, t.w});
   }
-  __syncthreads();
+  u = warp_merge_moments(u);
+  g = warp_merge_moments(g);
+  if (lane == 0) {
+    muU[r] = u.mean;
+    rU[r] = 1.0f / sqrtf(u.m2 / (float)H + eps);
+    muG[r] = g.mean;
+    rG[r] = 1.0f / sqrtf(g.m2 / (float)H + eps);
+  }
+}
+
+// =========================================================================
+// F3b: hidden = LN_x(U) * silu(LN_gate(G)), Z = [U | G]: one thread per
+// 16-byte vector of the hidden row (columns h .. h+V-1 of both halves), rows
+// consecutive over the grid; the row statistics come from F3a.
+// =========================================================================
+template <typename T>
+__global__ void __launch_bounds__(256) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ muU,
+                                                  const float* __restrict__ rU, const float* __restrict__ muG,
+                                                  const float* __restrict__ rG, const T* __restrict__ wx,
+                                                  const T* __restrict__ bx, const T* __restrict__ wg,
+                                                  const T* __restrict__ bg, T* __restrict__ hidden, int N, int H) {
+  constexpr int V = VecN<T>::value;
   const int nv = H / V;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    const int h0 = v * V;
-    float fwx[V], fbx[V], fwg[V], fbg[V];
-    load_vec(wx + h0, fwx);
-    load_vec(bx + h0, fbx);
-    load_vec(wg + h0, fwg);
-    load_vec(bg + h0, fbg);
-#pragma unroll 4
-    for (int i = 0; i < nrows; ++i) {
-      const T* zr = Z + (size_t)(r0 + i) * 2 * H;
-      float u[V], g[V], o[V];
-      load_vec(zr + h0, u);
-      load_vec(zr + H + h0, g);
-      const float mU = st[i][0], sU = st[i][1], mG = st[i][2], sG = st[i][3];
+  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= (long long)N * nv) return;
+  const int r = (int)(item / nv), v = (int)(item - (long long)r * nv);
+  const int h0 = v * V;
+  const T* zr = Z + (size_t)r * 2 * H;
+  float u[V], g[V], fwx[V], fbx[V], fwg[V], fbg[V], o[V];
+  load_vec(zr + h0, u);
+  load_vec(zr + H + h0, g);
+  load_vec(wx + h0, fwx);
+  load_vec(bx + h0, fbx);
+  load_vec(wg + h0, fwg);
+  load_vec(bg + h0, fbg);
+  const float mU = muU[r], sU = rU[r], mG = muG[r], sG = rG[r];
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float uu = (u[e] - mU) * sU * fwx[e] + fbx[e];
-        const float gg = (g[e] - mG) * sG * fwg[e] + fbg[e];
-        o[e] = uu * gg * __frcp_rn(1.0f + expf(-gg));
-      }
-      store_vec(hidden + (size_t)(r0 + i) * H + h0, o);
-    }
+  for (int e = 0; e < V; ++e) {
+    const float uu = (u[e] - mU) * sU * fwx[e] + fbx[e];
+    const float gg = (g[e] - mG) * sG * fwg[e] + fbg[e];
+    o[e] = uu * gg * __frcp_rn(1.0f + expf(-gg));
   }
+  store_vec(hidden + (size_t)r * H + h0, o);
+}
+
+// Row sums of the gate backward from the dgrad epilogue's per-group partials.
+__global__ void __launch_bounds__(256) k_rowpart_sum(const float* __restrict__ rowpart, float* __restrict__ rowsum,
+                                                     int N, int groups) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= N) return;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < groups; ++j) {
+    const float4 t = *reinterpret_cast<const float4*>(rowpart + ((size_t)r * groups + j) * 4);
+    a.x += t.x;
+    a.y += t.y;
+    a.z += t.z;
+    a.w += t.w;
+  }
+  *reinterpret_cast<float4*>(rowsum + (size_t)r * 4) = a;
 }
 
 // =========================================================================
@@ -645,17 +647,29 @@ cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, const void* wx,
-                            const void* bx, const void* wg, const void* bg, void* hidden, float* muU,
-                            float* rU, float* muG, float* rG, cudaStream_t st) {
+cudaError_t launch_zstats_merge(const RowArgs& a, const float* zstats, float* muU, float* rU, float* muG, float* rG,
+                                cudaStream_t st) {
   const int N = a.B * a.T;
-  int threads = round32(a.H / vec_elems(a.dtype));
-  if (threads > kRowThreadsMax) threads = kRowThreadsMax;
-  const int grid = (N + kGateRows - 1) / kGateRows;
+  k_zstats_merge<<<(N + 7) / 8, 256, 0, st>>>(zstats, muU, rU, muG, rG, N, a.H, 1e-5f);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* muU, const float* rU, const float* muG,
+                            const float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
+                            void* hidden, cudaStream_t st) {
+  const int N = a.B * a.T;
+  const long long items = (long long)N * (a.H / vec_elems(a.dtype));
+  const int grid = (int)((items + 255) / 256);
   RMX_DISPATCH_T(a.dtype, {
-    k_gate_fwd<T><<<grid, threads, 0, st>>>((const T*)Z, zstats, (const T*)wx, (const T*)bx, (const T*)wg,
-                                            (const T*)bg, (T*)hidden, muU, rU, muG, rG, N, a.H, 1e-5f);
+    k_gate_fwd<T><<<grid, 256, 0, st>>>((const T*)Z, muU, rU, muG, rG, (const T*)wx, (const T*)bx, (const T*)wg,
+                                        (const T*)bg, (T*)hidden, N, a.H);
   });
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rowpart_sum(const RowArgs& a, const float* rowpart, float* rowsum, cudaStream_t st) {
+  const int N = a.B * a.T;
+  k_rowpart_sum<<<(N + 255) / 256, 256, 0, st>>>(rowpart, rowsum, N, rowpart_groups(a.H));
   return cudaGetLastError();
 }
 
