@@ -97,8 +97,7 @@ def row_bytes_per_launch(s) -> dict:
         "gate_stats": N * ((2 * s.H + 127) // 128) * 16,  # per-group statistics in
         "ln2_fwd": 2 * BTD,                         # s2 in, y out
         "ln2_bwd": 3 * BTD,                         # dy, s2 in, ds2 out
-        "gate_bwd_rowsums": N * ((s.H + 127) // 128) * 16,  # per-group row sums in (dgrad2 epilogue)
-        "gate_bwd_apply": BTH + 2 * BTH + 2 * BTH,  # dh, Z in, dZ out
+        "gate_bwd": BTH + 2 * BTH + 2 * BTH,        # dh, Z in, dZ out (single pass)
         "ln1_bwd_mixed": 5 * BTD,                   # dout1, mix, x in; ds1 and token_mix(ds1) out
         "ln0_bwd": 4 * BTD,                         # token_mix(ds1), x, ds1 in, dx out
     }

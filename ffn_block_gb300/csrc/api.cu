@@ -57,7 +57,7 @@ struct Layout {
   // saved (filled by the forward)
   size_t out1, Z, hidden, s2, stats, zstats, mix0, saved_total;
   // backward scratch
-  size_t ds2, dh, dZ, dout1, ds1, da0, rowsum, rowpart, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
+  size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
   RowArgs ra;
 };
 
@@ -108,8 +108,6 @@ Layout layout_of(const rmx_config& c) {
   L.dout1 = o; o = up(o + N * D * e);
   L.ds1 = o; o = up(o + N * D * e);
   L.da0 = o; o = up(o + N * D * e);
-  L.rowsum = o; o = up(o + N * 4 * sizeof(float));
-  L.rowpart = o; o = up(o + N * (size_t)rowpart_groups(c.H) * 4 * sizeof(float));
   L.pg2 = o; o = up(o + PL * D * sizeof(float));
   L.pb2 = o; o = up(o + PL * D * sizeof(float));
   L.pbo = o; o = up(o + PL * D * sizeof(float));
@@ -133,6 +131,7 @@ rmx_status kernels_support(const rmx_config& c) {
   if (c.D / kLnBwdColsPerThread > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
   if (c.D / V > kRowThreadsMax || c.H / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
   if ((c.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // LN forward: 10 vectors per lane
+  if (!gate_bwd_fused_supported(layout_of(c).ra)) return RMX_ERR_UNSUPPORTED;
   return RMX_OK;
 }
 
@@ -235,13 +234,13 @@ rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
 }
 
 // Second stream for the weight-gradient GEMMs, which do not feed the rest of
-// the backward: wgrad2 runs beside the gate backward and dgrad1, wgrad1
-// beside the norm1/norm0 backward.  One per device, created on first use;
+// the backward: both run beside the norm1/norm0 backward.  One per device,
+// created on first use;
 // host-side enqueue of a backward is serialised so the shared events are
 // recorded and waited on in order.
 struct SideStream {
   cudaStream_t s = nullptr;
-  cudaEvent_t fork1 = nullptr, fork2 = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 std::mutex g_side_mu;
 
@@ -253,8 +252,7 @@ SideStream* side_stream() {
   if (!ss.s) {
     cudaStream_t s = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&ss.fork1, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ss.fork2, cudaEventDisableTiming) != cudaSuccess ||
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
       return nullptr;
     ss.s = s;
@@ -362,49 +360,30 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     Launch l("ln2_bwd", st);
     RMX_TRY(l.done(launch_ln2_bwd(L.ra, dy, s2, S.mu2, S.r2, p.gamma2, ds2, F(L.pg2), F(L.pb2), F(L.pbo), st)));
   }
-  // dh = ds2 @ wout^T; on the tensor-core path the epilogue also takes the
-  // gate backward's row sums per column group.
-  bool gate_sums_fused = false;
   {
-    GemmDesc d{GEMM_DGRAD, EPI_GATE_ROWSUMS, c.dtype, c.B, c.H, c.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
-    d.gz = Z;
-    d.gstats = S.muU;
-    d.gw[0] = p.lnx_w;
-    d.gw[1] = p.lnx_b;
-    d.gw[2] = p.lng_w;
-    d.gw[3] = p.lng_b;
-    d.rowpart = F(L.rowpart);
-    gate_sums_fused = c.dtype != RMX_F32 && gemm_tc_supported(d);
-    if (!gate_sums_fused) d.epi = EPI_STORE;
+    GemmDesc d{GEMM_DGRAD, EPI_STORE, c.dtype, c.B, c.H, c.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm2_dgrad", d, st));
   }
-  std::lock_guard<std::mutex> side_lock(g_side_mu);
-  SideStream* side = side_stream();
-  cudaStream_t wst = side ? side->s : st;  // weight-gradient GEMMs
-  if (side) RMX_TRY(stream_wait(wst, st, side->fork1));
   {
-    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
-    RMX_TRY(run_gemm("gemm2_wgrad", d, wst));
-  }
-  if (gate_sums_fused) {
-    Launch l("gate_bwd_rowsums", st);
-    RMX_TRY(l.done(launch_rowpart_sum(L.ra, F(L.rowpart), F(L.rowsum), st)));
-  } else {
-    Launch l("gate_bwd_rowsums", st);
-    RMX_TRY(l.done(launch_gate_bwd_rowsums(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w,
-                                           p.lng_b, F(L.rowsum), st)));
-  }
-  {
-    Launch l("gate_bwd_apply", st);
-    RMX_TRY(l.done(launch_gate_bwd_apply(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, F(L.rowsum), p.lnx_w, p.lnx_b,
-                                         p.lng_w, p.lng_b, dZ, F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1),
-                                         st)));
+    Launch l("gate_bwd", st);
+    RMX_TRY(l.done(launch_gate_bwd(L.ra, dh, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b, dZ,
+                                   F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1), st)));
   }
   {
     GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
     RMX_TRY(run_gemm("gemm1_dgrad", d, st));
   }
-  if (side) RMX_TRY(stream_wait(wst, st, side->fork2));
+  // The two weight-gradient GEMMs run on a side stream beside the LayerNorm
+  // backward passes (small shared-memory footprint, so they share SMs with
+  // the GEMM's CTAs); everything before them keeps the GPU to itself.
+  std::lock_guard<std::mutex> side_lock(g_side_mu);
+  SideStream* side = side_stream();
+  cudaStream_t wst = side ? side->s : st;
+  if (side) RMX_TRY(stream_wait(wst, st, side->fork));
+  {
+    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
+    RMX_TRY(run_gemm("gemm2_wgrad", d, wst));
+  }
   {
     GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm1_wgrad", d, wst));

@@ -20,6 +20,7 @@ enum : unsigned int {
   ERRBIT_WAIT_EPILOGUE = 1u << 2,
   ERRBIT_WAIT_DRAIN = 1u << 3,
   ERRBIT_WAIT_TEST = 1u << 4,
+  ERRBIT_WAIT_ROWS = 1u << 5,
 };
 
 unsigned int* device_error_word();  // host: device address of the error word
@@ -88,6 +89,11 @@ __device__ __forceinline__ void store_n(T* p, const float* v) {
     *reinterpret_cast<uint2*>(p) = raw;
   }
 }
+
+// Logistic function 1 / (1 + e^-g) from the fast exponential and division
+// intrinsics: a few ulp of error, far inside the block's tolerances; the
+// limits 0 and 1 come out exactly.
+__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {

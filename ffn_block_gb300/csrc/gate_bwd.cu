@@ -1,0 +1,336 @@
+// Backward of hidden = LN_x(U) * silu(LN_gate(G)) in one streaming pass.
+//
+// Page "Subgraph-fusion-based Mega-kernel Generation", section "Exact
+// computation" (the dense_ffn_v2 subgraph); the chain rule written out, with
+// Uh, Gh the normalised halves of Z, u = wx*Uh + bx, g = wg*Gh + bg and
+// s = sigmoid(g):
+//   du = dh * g * s,  dg = dh * u * s * (1 + g * (1 - s)),
+//   gU = wx * du,     gG = wg * dg,
+//   dU = rU * (gU - mean(gU) - Uh * mean(gU * Uh)), the same for dG,
+//   dZ = [dU | dG];   dwx += du*Uh, dbx += du, dwg += dg*Gh, dbg += dg,
+//   db1[t] += dZ.
+//
+// One CTA owns the rows b0 <= b < b1 of one token t and every column: thread
+// j holds the j-th 16-byte vector of columns of both halves.  The dh and Z
+// rows stream into shared memory through an S-stage ring of bulk copies (one
+// thread issues them; a byte-counting mbarrier per stage says when a row has
+// landed).  For each row the CTA takes the four row sums with one barrier,
+// then every thread finishes its own columns from registers, writes dZ and
+// keeps the column partial sums in registers.  dh and Z are read from HBM
+// once; every wait is bounded.
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmx {
+namespace {
+
+constexpr int kGateMaxStages = 8;
+
+// Sums v[0..3] over the 32 lanes of a warp with six shuffles.  On return,
+// lane l holds the sum of component 2 * bit4(l) + bit3(l); all lanes holding
+// the same component hold the same bits.
+__device__ __forceinline__ float warp_sum4_transposed(const float v[4]) {
+  const int lane = threadIdx.x & 31;
+  const bool b4 = lane & 16, b3 = lane & 8;
+  float k0 = b4 ? v[2] : v[0];
+  float k1 = b4 ? v[3] : v[1];
+  const float s0 = b4 ? v[0] : v[2];
+  const float s1 = b4 ? v[1] : v[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float k = b3 ? k1 : k0;
+  const float s = b3 ? k0 : k1;
+  k += __shfl_xor_sync(0xffffffffu, s, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
+struct GateBwdArgs {
+  const void* dh;        // [N, H]
+  const void* Z;         // [N, 2H]
+  const float* muU;      // [N] statistics of the forward's inner LayerNorms
+  const float* rU;
+  const float* muG;
+  const float* rG;
+  const void* wx;        // [H] LN_x weight / bias, LN_gate weight / bias
+  const void* bx;
+  const void* wg;
+  const void* bg;
+  void* dZ;              // [N, 2H]
+  float* pwx;            // [P, H] column partials, P = nbblk * T
+  float* pbx;
+  float* pwg;
+  float* pbg;
+  float* pb1;            // [P, 2H]
+  unsigned int* err;
+  int B, T, H, nb, stages;
+};
+
+// Loads E consecutive floats from 16-byte aligned shared memory.
+template <int E>
+__device__ __forceinline__ void lds_f32(const float* p, float* v) {
+#pragma unroll
+  for (int k = 0; k < E; k += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p + k);
+    v[k] = q.x;
+    v[k + 1] = q.y;
+    v[k + 2] = q.z;
+    v[k + 3] = q.w;
+  }
+}
+
+// Shared memory: stats [nb] float4 | red [2][4][32] float | weights [4][H]
+// float | stages x (dh row | Z row) | mbarriers.  Thread `tid` owns the
+// 16-byte vector of columns c0 = tid * E ... c0 + E - 1 of both halves.
+template <typename T>
+__global__ void __launch_bounds__(512, 1) k_gate_bwd(const GateBwdArgs a) {
+  constexpr int E = VecN<T>::value;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int H = a.H, S = a.stages;
+  const int bblk = blockIdx.x, t = blockIdx.y;
+  const int b0 = bblk * a.nb;
+  const int nrows = min(a.B, b0 + a.nb) - b0;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31, nw = nthreads >> 5;
+  const int c0 = tid * E;
+  const bool active = c0 < H;
+
+  float4* st_row = reinterpret_cast<float4*>(smem);                  // (rU, -mU*rU, rG, -mG*rG) per row
+  float* red = reinterpret_cast<float*>(smem + (size_t)a.nb * 16);   // [2][4][32]
+  float* wsm = red + 2 * 4 * 32;                                     // [4][H]
+  unsigned char* ring = reinterpret_cast<unsigned char*>(wsm + 4 * (size_t)H);
+  const size_t row_bytes = (size_t)3 * H * sizeof(T);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)S * row_bytes);
+  __shared__ int abort_flag;
+
+  const T* dh = reinterpret_cast<const T*>(a.dh);
+  const T* Z = reinterpret_cast<const T*>(a.Z);
+  auto issue = [&](int i, int s) {  // row i of this CTA into stage s
+    const size_t r = (size_t)(b0 + i) * a.T + t;
+    const uint32_t bar = smem_u32(&full[s]);
+    unsigned char* dst = ring + (size_t)s * row_bytes;
+    mbar_arrive_expect_tx(bar, (uint32_t)row_bytes);
+    bulk_g2s(smem_u32(dst), dh + r * H, (uint32_t)(H * sizeof(T)), bar);
+    bulk_g2s(smem_u32(dst + (size_t)H * sizeof(T)), Z + r * 2 * H, (uint32_t)(2 * H * sizeof(T)), bar);
+  };
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int i = 0; i < min(S, nrows); ++i) issue(i, i);
+  // Per-row statistics and the four weight vectors (as float) while the
+  // first rows are in flight.
+  for (int i = tid; i < nrows; i += nthreads) {
+    const size_t r = (size_t)(b0 + i) * a.T + t;
+    const float sU = a.rU[r], sG = a.rG[r];
+    st_row[i] = make_float4(sU, -a.muU[r] * sU, sG, -a.muG[r] * sG);
+  }
+  {
+    const T* w[4] = {reinterpret_cast<const T*>(a.wx), reinterpret_cast<const T*>(a.bx),
+                     reinterpret_cast<const T*>(a.wg), reinterpret_cast<const T*>(a.bg)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      for (int c = tid; c < H; c += nthreads) wsm[k * H + c] = to_f(w[k][c]);
+  }
+  __syncthreads();
+
+  float awx[E], abx[E], awg[E], abg[E], a1u[E], a1g[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) awx[e] = abx[e] = awg[e] = abg[e] = a1u[e] = a1g[e] = 0.f;
+
+  const float invH = 1.0f / (float)H;
+  T* dZrow = reinterpret_cast<T*>(a.dZ) + ((size_t)b0 * a.T + t) * 2 * H;
+  const size_t dZstep = (size_t)a.T * 2 * H;
+  int issued = min(S, nrows);
+  bool aborted = false;
+  int s = 0;          // stage of row i
+  uint32_t ph = 0;    // parity of that stage's current phase
+  for (int i = 0; i < nrows; ++i, dZrow += dZstep) {
+    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                      (volatile int*)&abort_flag);
+    const float4 sr = st_row[i];
+    const float sU = sr.x, cU = sr.y, sG = sr.z, cG = sr.w;
+    // Pass 1: everything that needs only this element, plus the row sums;
+    // gU, Uh, gG, Gh stay in registers for pass 2.
+    float kgU[E], kUh[E], kgG[E], kGh[E];
+    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok && active) {
+      const T* st_dh = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
+      float dhv[E], zu[E], zg[E], wx[E], bx[E], wg[E], bg[E];
+      load_vec(st_dh + c0, dhv);
+      load_vec(st_dh + H + c0, zu);
+      load_vec(st_dh + 2 * H + c0, zg);
+      lds_f32<E>(wsm + c0, wx);
+      lds_f32<E>(wsm + H + c0, bx);
+      lds_f32<E>(wsm + 2 * H + c0, wg);
+      lds_f32<E>(wsm + 3 * H + c0, bg);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float Uh = fmaf(zu[e], sU, cU);
+        const float Gh = fmaf(zg[e], sG, cG);
+        const float u = fmaf(wx[e], Uh, bx[e]);
+        const float g = fmaf(wg[e], Gh, bg[e]);
+        const float sg = sigmoid_fast(g);
+        const float gs = g * sg;                       // silu(g)
+        const float du = dhv[e] * gs;
+        const float dsilu = sg + fmaf(-gs, sg, gs);    // s * (1 + g * (1 - s))
+        const float dg = (dhv[e] * u) * dsilu;
+        const float gU = wx[e] * du, gG = wg[e] * dg;
+        rs[0] += gU;
+        rs[1] = fmaf(gU, Uh, rs[1]);
+        rs[2] += gG;
+        rs[3] = fmaf(gG, Gh, rs[3]);
+        awx[e] = fmaf(du, Uh, awx[e]);
+        abx[e] += du;
+        awg[e] = fmaf(dg, Gh, awg[e]);
+        abg[e] += dg;
+        kgU[e] = gU;
+        kUh[e] = Uh;
+        kgG[e] = gG;
+        kGh[e] = Gh;
+      }
+    }
+    // Row sums over the CTA: per warp (lane 8c holds sum c), then over the
+    // warps in a fixed order, the same bits in every thread.
+    float* rb = red + (i & 1) * 4 * 32;
+    {
+      const float k = warp_sum4_transposed(rs);
+      if ((lane & 7) == 0) rb[(lane >> 3) * 32 + warp] = k;
+    }
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    // Every thread is done reading stage s: refill it.
+    if (tid == 0 && issued < nrows) issue(issued++, s);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+    float m[4];
+    {
+      // Lane l adds warps (l & 7) and (l & 7) + 8 of sum l >> 3 (at most 16
+      // warps), then the eight lanes of each sum combine.
+      const int c = lane >> 3, w0 = lane & 7;
+      float v = (w0 < nw ? rb[c * 32 + w0] : 0.f) + (w0 + 8 < nw ? rb[c * 32 + w0 + 8] : 0.f);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m[k] = __shfl_sync(0xffffffffu, v, k * 8) * invH;
+    }
+    // Pass 2: dU = rU * (gU - m0 - Uh * m1), the same for dG.
+    if (active) {
+      const float pU = -m[1], qU = -sU * m[0], pG = -m[3], qG = -sG * m[2];
+      float oU[E], oG[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        oU[e] = fmaf(sU, fmaf(pU, kUh[e], kgU[e]), qU);
+        oG[e] = fmaf(sG, fmaf(pG, kGh[e], kgG[e]), qG);
+        a1u[e] += oU[e];
+        a1g[e] += oG[e];
+      }
+      store_vec(dZrow + c0, oU);
+      store_vec(dZrow + H + c0, oG);
+    }
+  }
+
+  if (aborted) {
+    // Wait (bounded) for the copies still in flight before the CTA's shared
+    // memory goes away: the newest copy issued into each stage.
+    if (tid == 0) {
+      volatile int no_abort = 0;
+      for (int i = max(0, issued - S); i < issued; ++i) {
+        mbar_wait_bounded(smem_u32(&full[i % S]), (uint32_t)((i / S) & 1), kWaitLimitNs, a.err,
+                          ERRBIT_WAIT_ROWS, &no_abort);
+      }
+    }
+    return;
+  }
+
+  if (active) {
+    const size_t p = (size_t)bblk * a.T + t;
+    auto put = [&](float* dst, const float* v) {
+#pragma unroll
+      for (int k = 0; k < E; k += 4)
+        *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+    };
+    put(a.pwx + p * H + c0, awx);
+    put(a.pbx + p * H + c0, abx);
+    put(a.pwg + p * H + c0, awg);
+    put(a.pbg + p * H + c0, abg);
+    put(a.pb1 + p * 2 * H + c0, a1u);
+    put(a.pb1 + p * 2 * H + H + c0, a1g);
+  }
+}
+
+template <typename T>
+cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
+  GateBwdArgs a = base;
+  constexpr int E = VecN<T>::value;
+  const int threads = (a.H / E + 31) / 32 * 32;
+  const size_t fixed = (size_t)a.nb * 16 + 2 * 4 * 32 * 4 + (size_t)4 * a.H * 4;
+  const size_t row_bytes = (size_t)3 * a.H * sizeof(T);
+  const int cap = max_dynamic_smem_bytes() - 1024;  // static shared memory and slack
+  const long long room = ((long long)cap - (long long)fixed) / (long long)(row_bytes + 8);
+  if (room < 2) return cudaErrorInvalidValue;
+  a.stages = (int)(room < kGateMaxStages ? room : kGateMaxStages);
+  const size_t smem = fixed + (size_t)a.stages * row_bytes + (size_t)a.stages * 8;
+  auto k = k_gate_bwd<T>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, threads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gate_bwd_fused_supported(const RowArgs& a) {
+  // One 16-byte vector of each half per thread, at most 512 threads.
+  const int V = a.dtype == 0 ? 4 : 8;
+  return a.H % V == 0 && a.H / V <= 512 && a.nb <= kGateBwdMaxRows;
+}
+
+cudaError_t launch_gate_bwd(const RowArgs& ra, const void* dh, const void* Z, const float* muU, const float* rU,
+                            const float* muG, const float* rG, const void* wx, const void* bx, const void* wg,
+                            const void* bg, void* dZ, float* pwx, float* pbx, float* pwg, float* pbg, float* pb1,
+                            cudaStream_t st) {
+  if (!gate_bwd_fused_supported(ra)) return cudaErrorInvalidValue;
+  GateBwdArgs a;
+  a.dh = dh;
+  a.Z = Z;
+  a.muU = muU;
+  a.rU = rU;
+  a.muG = muG;
+  a.rG = rG;
+  a.wx = wx;
+  a.bx = bx;
+  a.wg = wg;
+  a.bg = bg;
+  a.dZ = dZ;
+  a.pwx = pwx;
+  a.pbx = pbx;
+  a.pwg = pwg;
+  a.pbg = pbg;
+  a.pb1 = pb1;
+  a.err = device_error_word();
+  a.B = ra.B;
+  a.T = ra.T;
+  a.H = ra.H;
+  a.nb = ra.nb;
+  a.stages = 0;
+  if (!a.err) return cudaErrorInvalidValue;
+  const dim3 grid(ra.nbblk, ra.T);
+  if (ra.dtype == 0) return launch_typed<float>(a, st, grid);
+  if (ra.dtype == 1) return launch_typed<bf16>(a, st, grid);
+  return launch_typed<f16>(a, st, grid);
+}
+
+}  // namespace rmx

@@ -73,10 +73,6 @@ struct Params {
   unsigned long long wait_limit_ns;
   float* zstats;  // EPI_BIAS_ZSTATS
   int split, zgroups;
-  const void* gz;  // EPI_GATE_ROWSUMS
-  const float* gstats;
-  const void* gw[4];
-  float* rowpart;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -243,14 +239,9 @@ struct ZSums {
   float n, k, s, q;  // count, shift, sum(x - k), sum((x - k)^2)
 };
 
-// Row statistics of U and G for the gate-backward epilogue.
-struct GateRow {
-  float mU, sU, mG, sG;
-};
-
 template <typename T, int EPI>
 __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, int n_base, const float* v,
-                                               ZSums* zs, const GateRow& gr, float4& gacc) {
+                                               ZSums* zs) {
   constexpr int V = VecN<T>::value;
   T* orow = reinterpret_cast<T*>(p.out) + (size_t)g * p.out_gs + (size_t)m * p.out_rs;
 #pragma unroll
@@ -273,34 +264,6 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, in
         for (int e = 0; e < V; ++e) o[e] += rv[e];
       }
       store_vec(orow + n, o);
-      if (EPI == EPI_GATE_ROWSUMS) {
-        // Gate backward on the stored dh: du = dh * g * s,
-        // dg = dh * u * s * (1 + g * (1 - s)), gU = wx * du, gG = wg * dg.
-        const size_t zrow = ((size_t)m * p.G + g) * 2 * p.N;
-        float dhv[V], zu[V], zg[V], wx[V], bx[V], wg[V], bg[V];
-#pragma unroll
-        for (int e = 0; e < V; ++e) dhv[e] = to_f(from_f<T>(o[e]));
-        load_vec(reinterpret_cast<const T*>(p.gz) + zrow + n, zu);
-        load_vec(reinterpret_cast<const T*>(p.gz) + zrow + p.N + n, zg);
-        load_vec(reinterpret_cast<const T*>(p.gw[0]) + n, wx);
-        load_vec(reinterpret_cast<const T*>(p.gw[1]) + n, bx);
-        load_vec(reinterpret_cast<const T*>(p.gw[2]) + n, wg);
-        load_vec(reinterpret_cast<const T*>(p.gw[3]) + n, bg);
-#pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const float Uh = (zu[e] - gr.mU) * gr.sU;
-          const float Gh = (zg[e] - gr.mG) * gr.sG;
-          const float u = wx[e] * Uh + bx[e];
-          const float gg = wg[e] * Gh + bg[e];
-          const float sg = __frcp_rn(1.0f + expf(-gg));
-          const float gU = wx[e] * (dhv[e] * (gg * sg));
-          const float gG = wg[e] * (dhv[e] * u * (sg * (1.0f + gg * (1.0f - sg))));
-          gacc.x += gU;
-          gacc.y += gU * Uh;
-          gacc.z += gG;
-          gacc.w += gG * Gh;
-        }
-      }
       if (EPI == EPI_BIAS_ZSTATS) {
         // Shifted sums of the stored (rounded) values of this half: the
         // shift is the half's first value in this column group, so the
@@ -529,21 +492,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int c0 = ch * COLS;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
       ZSums zs[2] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      GateRow gr = {0.f, 0.f, 0.f, 0.f};
-      float4 gacc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (EPI == EPI_GATE_ROWSUMS && m < p.M) {
-        const size_t r = (size_t)m * p.G + g, NN = (size_t)p.M * p.G;
-        gr = GateRow{p.gstats[r], p.gstats[NN + r], p.gstats[2 * NN + r], p.gstats[3 * NN + r]};
-      }
       for (int j0 = 0; j0 < COLS; j0 += 32) {
         if (n0 + c0 + j0 >= p.N || m0 >= p.M) break;  // warp-uniform
         float v[32];
         tmem_ld_32x32(t_row + (uint32_t)j0, v);
-        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + c0 + j0, v, zs, gr, gacc);
-      }
-      if (EPI == EPI_GATE_ROWSUMS && m < p.M && n0 + c0 < p.N) {
-        const int grp = (n0 + c0) / kZStatsTile;
-        *reinterpret_cast<float4*>(p.rowpart + (((size_t)m * p.G + g) * p.zgroups + grp) * 4) = gacc;
+        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + c0 + j0, v, zs);
       }
       if (EPI == EPI_BIAS_ZSTATS && m < p.M && n0 + c0 < p.N) {
         float4 w;
@@ -651,7 +604,6 @@ cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorM
     case GEMM_FWD * 8 + EPI_BIAS_ZSTATS: return launch_tc<T, GEMM_FWD, EPI_BIAS_ZSTATS, PAIR>(a, b, p, st);
     case GEMM_DGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE, PAIR>(a, b, p, st);
     case GEMM_DGRAD * 8 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID, PAIR>(a, b, p, st);
-    case GEMM_DGRAD * 8 + EPI_GATE_ROWSUMS: return launch_tc<T, GEMM_DGRAD, EPI_GATE_ROWSUMS, PAIR>(a, b, p, st);
     case GEMM_WGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE, PAIR>(a, b, p, st);
     default: return cudaErrorInvalidValue;
   }
@@ -680,9 +632,7 @@ bool gemm_tc_supported(const GemmDesc& d) {
   if (d.epi == EPI_BIAS_ZSTATS && (BN / (EPI_WARPS / 4) != kZStatsTile || !d.zstats || d.split % 8)) return false;
   const int ok_epi = (d.kind == GEMM_FWD && (d.epi == EPI_STORE || d.epi == EPI_BIAS || d.epi == EPI_BIAS_RESID ||
                                              d.epi == EPI_BIAS_ZSTATS)) ||
-                     (d.kind == GEMM_DGRAD && (d.epi == EPI_STORE || d.epi == EPI_RESID ||
-                                               (d.epi == EPI_GATE_ROWSUMS && d.gz && d.gstats && d.rowpart &&
-                                                d.gw[0] && d.gw[1] && d.gw[2] && d.gw[3]))) ||
+                     (d.kind == GEMM_DGRAD && (d.epi == EPI_STORE || d.epi == EPI_RESID)) ||
                      (d.kind == GEMM_WGRAD && d.epi == EPI_STORE);
   return ok_epi && encode_fn() != nullptr;
 }
@@ -741,10 +691,6 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.zstats = d.zstats;
   p.split = d.split;
   p.zgroups = (d.N + kZStatsTile - 1) / kZStatsTile;
-  p.gz = d.gz;
-  p.gstats = d.gstats;
-  for (int i = 0; i < 4; ++i) p.gw[i] = d.gw[i];
-  p.rowpart = d.rowpart;
   if (d.dtype == 1) return pair ? dispatch_tc<bf16, true>(d, ma, mb, p, st) : dispatch_tc<bf16, false>(d, ma, mb, p, st);
   return pair ? dispatch_tc<f16, true>(d, ma, mb, p, st) : dispatch_tc<f16, false>(d, ma, mb, p, st);
 }

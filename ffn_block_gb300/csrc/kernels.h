@@ -42,16 +42,16 @@ cudaError_t launch_zstats_merge(const RowArgs& a, const float* zstats, float* mu
 cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* muU, const float* rU, const float* muG,
                             const float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
                             void* hidden, cudaStream_t st);
-// Backward of the gate and both inner LNs, two streaming passes:
-// (1) rowsum[r] = {sum gU, sum gU*Uh, sum gG, sum gG*Gh} ([B*T][4] floats);
-// (2) dZ plus per-CTA partial sums of dwx, dbx, dwg, dbg and db1.
-cudaError_t launch_gate_bwd_rowsums(const RowArgs& a, const void* dh, const void* Z, const float* muU,
-                                    const float* rU, const float* muG, const float* rG, const void* wx,
-                                    const void* bx, const void* wg, const void* bg, float* rowsum, cudaStream_t st);
-cudaError_t launch_gate_bwd_apply(const RowArgs& a, const void* dh, const void* Z, const float* muU,
-                                  const float* rU, const float* muG, const float* rG, const float* rowsum,
-                                  const void* wx, const void* bx, const void* wg, const void* bg, void* dZ,
-                                  float* pwx, float* pbx, float* pwg, float* pbg, float* pb1, cudaStream_t st);
+// Single-pass gate backward: dZ and the column partials of lnx_w, lnx_b,
+// lng_w, lng_b ([nbblk*T, H] each) and b1 ([nbblk, T, 2H]) from dh, Z and the
+// forward's inner-LayerNorm statistics.  CTA (bblk, t) owns up to nb <=
+// kGateBwdMaxRows rows of token t and the whole row.
+constexpr int kGateBwdMaxRows = 64;
+bool gate_bwd_fused_supported(const RowArgs& a);
+cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU, const float* rU,
+                            const float* muG, const float* rG, const void* wx, const void* bx, const void* wg,
+                            const void* bg, void* dZ, float* pwx, float* pbx, float* pwg, float* pbg, float* pb1,
+                            cudaStream_t st);
 
 // Deterministic column sums: out[j] = sum_{p<P} part[p*J + j], cast to dtype.
 struct ColsumJob {
@@ -75,7 +75,6 @@ enum GemmEpi {
   EPI_BIAS_RESID = 2,
   EPI_RESID = 3,
   EPI_BIAS_ZSTATS = 4,    // + per-group statistics of Z (GEMM1 forward)
-  EPI_GATE_ROWSUMS = 5,   // + per-group row sums of the gate backward (dgrad2)
 };
 
 // Row statistics of Z = [U | G] in 128-column groups: for row r and group j
@@ -103,21 +102,7 @@ struct GemmDesc {
   const void* resid;
   float* zstats;  // EPI_BIAS_ZSTATS only
   int split;      // EPI_BIAS_ZSTATS: first column of the G half (H)
-  // EPI_GATE_ROWSUMS (C = dh [M,G,H]): Z [M,G,2H], the statistics of U and G
-  // (four consecutive float vectors mean_U, rstd_U, mean_G, rstd_G of length
-  // M*G), the four inner-LN parameter vectors wx, bx, wg, bg, and the output
-  // rowpart[(row * groups + j) * 4 + {0..3}] = partial sums over column group
-  // j (kZStatsTile columns) of gU, gU*Uh, gG, gG*Gh.
-  const void* gz;
-  const float* gstats;
-  const void* gw[4];
-  float* rowpart;
 };
-
-// Row sums of the gate backward from their per-group partials:
-// rowsum[r] = sum over groups of rowpart[r][j] (fixed order).
-cudaError_t launch_rowpart_sum(const RowArgs& a, const float* rowpart, float* rowsum, cudaStream_t st);
-inline int rowpart_groups(int H) { return (H + kZStatsTile - 1) / kZStatsTile; }
 
 bool gemm_tc_supported(const GemmDesc& d);
 cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st);

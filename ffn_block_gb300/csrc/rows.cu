@@ -382,166 +382,14 @@ __global__ void __launch_bounds__(256) k_gate_fwd(const T* __restrict__ Z, const
   load_vec(bx + h0, fbx);
   load_vec(wg + h0, fwg);
   load_vec(bg + h0, fbg);
-  const float mU = muU[r], sU = rU[r], mG = muG[r], sG = rG[r];
+  const float sU = rU[r], cU = -muU[r] * sU, sG = rG[r], cG = -muG[r] * sG;
 #pragma unroll
   for (int e = 0; e < V; ++e) {
-    const float uu = (u[e] - mU) * sU * fwx[e] + fbx[e];
-    const float gg = (g[e] - mG) * sG * fwg[e] + fbg[e];
-    o[e] = uu * gg * __frcp_rn(1.0f + expf(-gg));
+    const float uu = fmaf(fmaf(u[e], sU, cU), fwx[e], fbx[e]);
+    const float gg = fmaf(fmaf(g[e], sG, cG), fwg[e], fbg[e]);
+    o[e] = uu * (gg * sigmoid_fast(gg));
   }
   store_vec(hidden + (size_t)r * H + h0, o);
-}
-
-// Row sums of the gate backward from the dgrad epilogue's per-group partials.
-__global__ void __launch_bounds__(256) k_rowpart_sum(const float* __restrict__ rowpart, float* __restrict__ rowsum,
-                                                     int N, int groups) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= N) return;
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < groups; ++j) {
-    const float4 t = *reinterpret_cast<const float4*>(rowpart + ((size_t)r * groups + j) * 4);
-    a.x += t.x;
-    a.y += t.y;
-    a.z += t.z;
-    a.w += t.w;
-  }
-  *reinterpret_cast<float4*>(rowsum + (size_t)r * 4) = a;
-}
-
-// =========================================================================
-// G4: backward of hidden = LN_x(U) * silu(LN_gate(G)).  With Uh, Gh the
-// normalised halves, u = wx*Uh + bx, g = wg*Gh + bg, s = sigmoid(g):
-//   du = dh * g * s,  dg = dh * u * s * (1 + g * (1 - s)),
-//   gU = wx * du,     gG = wg * dg,
-//   dU = rU * (gU - mean(gU) - Uh * mean(gU * Uh)), same for dG,
-//   dZ = [dU | dG];   dwx += du*Uh, dbx += du, dwg += dg*Gh, dbg += dg,
-//   db1[t] += dZ.
-// Two streaming passes: (1) one warp per row takes the four row sums
-// (sum gU, sum gU*Uh, sum gG, sum gG*Gh); (2) CTA (bblk, t), thread v owns
-// columns v*V ... of both halves for every row of its block, writes dZ and
-// keeps the column partial sums in registers.  No per-row barrier.
-// =========================================================================
-template <int E>
-__device__ __forceinline__ void gate_bwd_elem(const float* dhv, const float* zu, const float* zg, float mU, float sU,
-                                              float mG, float sG, const float* fwx, const float* fbx,
-                                              const float* fwg, const float* fbg, float* Uh, float* Gh, float* du,
-                                              float* dg) {
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    Uh[e] = (zu[e] - mU) * sU;
-    Gh[e] = (zg[e] - mG) * sG;
-    const float u = fwx[e] * Uh[e] + fbx[e];
-    const float g = fwg[e] * Gh[e] + fbg[e];
-    const float sg = __frcp_rn(1.0f + expf(-g));
-    du[e] = dhv[e] * (g * sg);
-    dg[e] = dhv[e] * u * (sg * (1.0f + g * (1.0f - sg)));
-  }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256) k_gate_bwd_rowsums(
-    const T* __restrict__ dh, const T* __restrict__ Z, const float* __restrict__ muU, const float* __restrict__ rU,
-    const float* __restrict__ muG, const float* __restrict__ rG, const T* __restrict__ wx,
-    const T* __restrict__ bx, const T* __restrict__ wg, const T* __restrict__ bg, float* __restrict__ rowsum, int N,
-    int H) {
-  constexpr int V = VecN<T>::value;
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (r >= N) return;
-  const float mU = muU[r], sU = rU[r], mG = muG[r], sG = rG[r];
-  const T* dhr = dh + (size_t)r * H;
-  const T* zr = Z + (size_t)r * 2 * H;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  const int nv = H / V;
-#pragma unroll 2
-  for (int v = lane; v < nv; v += 32) {
-    const int h0 = v * V;
-    float dhv[V], zu[V], zg[V], fwx[V], fbx[V], fwg[V], fbg[V];
-    load_vec(dhr + h0, dhv);
-    load_vec(zr + h0, zu);
-    load_vec(zr + H + h0, zg);
-    load_vec(wx + h0, fwx);
-    load_vec(bx + h0, fbx);
-    load_vec(wg + h0, fwg);
-    load_vec(bg + h0, fbg);
-    float Uh[V], Gh[V], du[V], dg[V];
-    gate_bwd_elem<V>(dhv, zu, zg, mU, sU, mG, sG, fwx, fbx, fwg, fbg, Uh, Gh, du, dg);
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      const float gU = fwx[e] * du[e], gG = fwg[e] * dg[e];
-      a0 += gU;
-      a1 += gU * Uh[e];
-      a2 += gG;
-      a3 += gG * Gh[e];
-    }
-  }
-  a0 = warp_sum(a0);
-  a1 = warp_sum(a1);
-  a2 = warp_sum(a2);
-  a3 = warp_sum(a3);
-  if (lane == 0) *reinterpret_cast<float4*>(rowsum + (size_t)r * 4) = make_float4(a0, a1, a2, a3);
-}
-
-// Thread owns E = 4 columns of each half (8-byte accesses for 16-bit types)
-// so the six column partial sums fit in registers at good occupancy;
-// blockIdx.z picks which part of the H columns the CTA covers.
-template <typename T>
-__global__ void __launch_bounds__(512) k_gate_bwd_apply(
-    const T* __restrict__ dh, const T* __restrict__ Z, const float* __restrict__ muU, const float* __restrict__ rU,
-    const float* __restrict__ muG, const float* __restrict__ rG, const float* __restrict__ rowsum,
-    const T* __restrict__ wx, const T* __restrict__ bx, const T* __restrict__ wg, const T* __restrict__ bg,
-    T* __restrict__ dZ, float* __restrict__ pwx, float* __restrict__ pbx, float* __restrict__ pwg,
-    float* __restrict__ pbg, float* __restrict__ pb1, int B, int Tn, int H, int nb) {
-  constexpr int E = 4;
-  const int bblk = blockIdx.x, t = blockIdx.y;
-  const int h0 = (blockIdx.z * blockDim.x + threadIdx.x) * E;
-  if (h0 >= H) return;
-  const float invH = 1.0f / (float)H;
-  float fwx[E], fbx[E], fwg[E], fbg[E];
-  load_n<T, E>(wx + h0, fwx);
-  load_n<T, E>(bx + h0, fbx);
-  load_n<T, E>(wg + h0, fwg);
-  load_n<T, E>(bg + h0, fbg);
-  float awx[E], abx[E], awg[E], abg[E], a1u[E], a1g[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) awx[e] = abx[e] = awg[e] = abg[e] = a1u[e] = a1g[e] = 0.f;
-  const int b_end = min(B, (bblk + 1) * nb);
-#pragma unroll 2
-  for (int b = bblk * nb; b < b_end; ++b) {
-    const size_t r = (size_t)b * Tn + t;
-    float dhv[E], zu[E], zg[E];
-    load_n<T, E>(dh + r * H + h0, dhv);
-    load_n<T, E>(Z + r * 2 * H + h0, zu);
-    load_n<T, E>(Z + r * 2 * H + H + h0, zg);
-    const float4 rs = *reinterpret_cast<const float4*>(rowsum + r * 4);
-    const float sU = rU[r], sG = rG[r];
-    float Uh[E], Gh[E], du[E], dg[E], oU[E], oG[E];
-    gate_bwd_elem<E>(dhv, zu, zg, muU[r], sU, muG[r], sG, fwx, fbx, fwg, fbg, Uh, Gh, du, dg);
-    const float m0 = rs.x * invH, m1 = rs.y * invH, m2 = rs.z * invH, m3 = rs.w * invH;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      oU[e] = sU * (fwx[e] * du[e] - m0 - Uh[e] * m1);
-      oG[e] = sG * (fwg[e] * dg[e] - m2 - Gh[e] * m3);
-      awx[e] += du[e] * Uh[e];
-      abx[e] += du[e];
-      awg[e] += dg[e] * Gh[e];
-      abg[e] += dg[e];
-      a1u[e] += oU[e];
-      a1g[e] += oG[e];
-    }
-    store_n<T, E>(dZ + r * 2 * H + h0, oU);
-    store_n<T, E>(dZ + r * 2 * H + H + h0, oG);
-  }
-  const size_t p = (size_t)bblk * Tn + t;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    pwx[p * H + h0 + e] = awx[e];
-    pbx[p * H + h0 + e] = abx[e];
-    pwg[p * H + h0 + e] = awg[e];
-    pbg[p * H + h0 + e] = abg[e];
-    pb1[p * 2 * H + h0 + e] = a1u[e];
-    pb1[p * 2 * H + H + h0 + e] = a1g[e];
-  }
 }
 
 // =========================================================================
@@ -663,39 +511,6 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* muU, c
   RMX_DISPATCH_T(a.dtype, {
     k_gate_fwd<T><<<grid, 256, 0, st>>>((const T*)Z, muU, rU, muG, rG, (const T*)wx, (const T*)bx, (const T*)wg,
                                         (const T*)bg, (T*)hidden, N, a.H);
-  });
-  return cudaGetLastError();
-}
-
-cudaError_t launch_rowpart_sum(const RowArgs& a, const float* rowpart, float* rowsum, cudaStream_t st) {
-  const int N = a.B * a.T;
-  k_rowpart_sum<<<(N + 255) / 256, 256, 0, st>>>(rowpart, rowsum, N, rowpart_groups(a.H));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gate_bwd_rowsums(const RowArgs& a, const void* dh, const void* Z, const float* muU,
-                                    const float* rU, const float* muG, const float* rG, const void* wx,
-                                    const void* bx, const void* wg, const void* bg, float* rowsum, cudaStream_t st) {
-  const int N = a.B * a.T;
-  RMX_DISPATCH_T(a.dtype, {
-    k_gate_bwd_rowsums<T><<<(N + 7) / 8, 256, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, (const T*)wx,
-                                                       (const T*)bx, (const T*)wg, (const T*)bg, rowsum, N, a.H);
-  });
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gate_bwd_apply(const RowArgs& a, const void* dh, const void* Z, const float* muU,
-                                  const float* rU, const float* muG, const float* rG, const float* rowsum,
-                                  const void* wx, const void* bx, const void* wg, const void* bg, void* dZ,
-                                  float* pwx, float* pbx, float* pwg, float* pbg, float* pb1, cudaStream_t st) {
-  // 4 columns per thread, at most 256 threads per CTA.
-  const int quads = a.H / 4;
-  const int threads = quads < 256 ? round32(quads) : 256;
-  dim3 grid(a.nbblk, a.T, (quads + threads - 1) / threads);
-  RMX_DISPATCH_T(a.dtype, {
-    k_gate_bwd_apply<T><<<grid, threads, 0, st>>>((const T*)dh, (const T*)Z, muU, rU, muG, rG, rowsum, (const T*)wx,
-                                                  (const T*)bx, (const T*)wg, (const T*)bg, (T*)dZ, pwx, pbx, pwg,
-                                                  pbg, pb1, a.B, a.T, a.H, a.nb);
   });
   return cudaGetLastError();
 }
