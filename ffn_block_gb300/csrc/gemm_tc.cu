@@ -45,18 +45,26 @@
 namespace rmx {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, UMMA_K = 16;
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
 constexpr int A_BYTES = BM * BK * 2;           // 16 KB
 constexpr int B_BYTES = BN * BK * 2;           // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KB
 constexpr int MN_CHUNK_BYTES = BK * 128;       // one 64-wide MN chunk of an MN-major tile
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * BN;        // 512
 constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter
 constexpr int THREADS = 64 + 32 * EPI_WARPS;   // producer, MMA, epilogue
-constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
-static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+
+// Shared-memory ring.  Single CTA: the whole 256-row B tile per stage, four
+// stages.  CTA pair: each CTA holds its 128 rows of A and its half of B, so a
+// stage is 32 KB and six fit.
+template <bool PAIR> struct Ring {
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int B_STAGE = PAIR ? B_BYTES / 2 : B_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_STAGE;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+  static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+};
 constexpr uint64_t kDrainLimitNs = 50ull * 1000ull * 1000ull;
 
 struct Params {
@@ -92,15 +100,57 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-// Same copy, written to the same shared offset of every CTA in `mask` and
-// counted on each CTA's barrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                               int c2, uint16_t mask) {
+// Same copy for a CTA pair: the data lands in this CTA's shared memory and
+// the byte count is signalled on `bar`, which may be the peer CTA's barrier
+// (a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                 int c1, int c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%4, %5, %6}], [%2], %3;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "h"(mask), "r"(c0), "r"(c1), "r"(c2)
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+// shared::cluster address of the variable at `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on a barrier that may live in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait_bounded with cluster-scope acquire (the arrivals come from the
+// peer CTA as well).
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                          unsigned int* err, unsigned int errbit,
+                                                          volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (((++n) & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicOr(err, errbit);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -129,37 +179,67 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// TMEM allocation.  For a CTA pair (cta_group::2) one warp of each CTA
+// executes these together.
+template <bool PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
 }
+template <bool PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  if (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 or bf16 in, fp32 out).
+// For a CTA pair (issued by the even CTA only) A and D are split by rows and
+// B by columns between the two CTAs, at the same shared / TMEM offsets.
+template <bool PAIR>
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
+template <bool PAIR>
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
+  if (PAIR)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
 }
-// Arrive on the barrier at `bar`'s offset in every CTA of `mask` once the
+// Pair: arrive on the barrier at `bar`'s offset in both CTAs once the
 // tcgen05 operations issued so far by this thread have completed.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
       : "memory");
 }
 // 32 lanes x 32 consecutive fp32 columns; thread i of the warp gets lane
@@ -200,11 +280,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A/B type
 // (bits 7-9 / 10-12: 0 = fp16, 1 = bf16), A/B major (bits 15 / 16:
 // 0 = K-major, 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-template <typename T, bool A_MN, bool B_MN>
+template <typename T, bool A_MN, bool B_MN, int UMMA_M>
 __host__ __device__ constexpr uint32_t make_idesc() {
   constexpr uint32_t ab = std::is_same<T, bf16>::value ? 1u : 0u;
   return (1u << 4) | (ab << 7) | (ab << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UMMA_M >> 4) << 24);
 }
 
 template <int KIND> struct KindTraits;
@@ -293,13 +373,15 @@ template <typename T, int KIND, int EPI, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
   using KT = KindTraits<KIND>;
+  using R = Ring<PAIR>;
+  constexpr int STAGES = R::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * R::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + R::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
@@ -313,19 +395,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int first = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
   const int stride = PAIR ? (int)num_clusters_x() : (int)gridDim.x;
   const int count = PAIR ? p.num_pair_tiles : p.num_tiles;
-  auto coords = [&](int it, int& g, int& m0, int& n0) {
-    if (PAIR) pair_tile_coords(p, it, rank, g, m0, n0);
+  auto coords = [&](int it, int r, int& g, int& m0, int& n0) {
+    if (PAIR) pair_tile_coords(p, it, r, g, m0, n0);
     else tile_coords(p, it, g, m0, n0);
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), PAIR ? 2 : 1);  // paired: both CTAs' MMAs release a stage
+      mbar_init(full_bar(s), 1);    // the (even) CTA's expect_tx arrival
+      mbar_init(empty_bar(s), 1);   // one MMA commit per use
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), EPI_WARPS);  // one arrive per epilogue warp
+      // One arrive per epilogue warp, of both CTAs for a pair.
+      mbar_init(tempty_bar(a), PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -333,10 +416,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_map(&tmA);
     prefetch_map(&tmB);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  // Paired: the peer's barriers are initialised before any multicast lands.
+  // Pair: the peer's barriers are initialised before anything is signalled
+  // on them.
   if (PAIR) cluster_barrier();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -347,17 +431,31 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int tile = first; ok && tile < count; tile += stride) {
-        int g, m0, n0;
-        coords(tile, g, m0, n0);
-        // Pieces of the tiles this CTA requests.  MN-major tiles come as
+        // Pieces of the tile that CTA r requests.  MN-major tiles come as
         // 64-wide chunks; chunks or tiles wholly past M or N are skipped
         // (they only feed discarded outputs) and not counted.
-        const int a_chunks = KT::A_MN ? max(0, min(BM / 64, (p.M - m0 + 63) / 64)) : (m0 < p.M ? 1 : 0);
-        const int b_chunks = KT::B_MN ? min(BN / 64, (p.N - n0 + 63) / 64) : 0;
-        // K-major B in paired mode: two 128-row halves, one per CTA.
-        const int b_halves = KT::B_MN ? 0 : (PAIR ? ((p.N - n0 > 128) ? 2 : 1) : 1);
-        const uint32_t a_bytes = KT::A_MN ? a_chunks * MN_CHUNK_BYTES : a_chunks * A_BYTES;
-        const uint32_t b_bytes = KT::B_MN ? b_chunks * MN_CHUNK_BYTES : (PAIR ? b_halves * (B_BYTES / 2) : B_BYTES);
+        auto a_pieces = [&](int m0) {
+          return KT::A_MN ? max(0, min(BM / 64, (p.M - m0 + 63) / 64)) : (m0 < p.M ? 1 : 0);
+        };
+        // B columns [nb0, nb0 + nw) held by CTA r: the whole tile alone, half
+        // of it in a pair.
+        auto b_pieces = [&](int nb0, int nw) {
+          return KT::B_MN ? max(0, min(nw / 64, (p.N - nb0 + 63) / 64)) : (nb0 < p.N ? 1 : 0);
+        };
+        constexpr int B_W = PAIR ? BN / 2 : BN;
+        int g, m0, n0;
+        coords(tile, rank, g, m0, n0);
+        const int nb0 = n0 + (PAIR ? rank * B_W : 0);
+        const int a_n = a_pieces(m0), b_n = b_pieces(nb0, B_W);
+        const uint32_t a_piece = KT::A_MN ? MN_CHUNK_BYTES : A_BYTES;
+        const uint32_t b_piece = KT::B_MN ? MN_CHUNK_BYTES : R::B_STAGE;
+        // The even CTA's full barrier counts the bytes of both CTAs.
+        uint32_t tx = a_n * a_piece + b_n * b_piece;
+        if (PAIR) {
+          int g1, m1, n1;
+          coords(tile, 1, g1, m1, n1);
+          tx += a_pieces(m1) * a_piece + b_pieces(n0 + B_W, B_W) * b_piece;
+        }
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -366,53 +464,37 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(full_bar(s), a_bytes + b_bytes);
+          const uint32_t fb = PAIR ? mapa_shared(full_bar(s), 0) : full_bar(s);
+          if (rank == 0) mbar_expect_tx(full_bar(s), tx);
+          auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+            if (PAIR) tma_load_3d_pair(dst, map, fb, c0, c1, c2);
+            else tma_load_3d(dst, map, fb, c0, c1, c2);
+          };
           const int k0 = kb * BK;
-          const uint32_t a_dst = sA + s * A_BYTES, b_dst = sB + s * B_BYTES;
+          const uint32_t a_dst = sA + s * A_BYTES, b_dst = sB + s * R::B_STAGE;
           if (!KT::A_MN) {
-            if (a_chunks) tma_load_3d(a_dst, &tmA, full_bar(s), k0, g, m0);          // map {K, G, M}
+            if (a_n) load(a_dst, &tmA, k0, g, m0);                                      // map {K, G, M}
           } else {
-            for (int c = 0; c < a_chunks; ++c)                                         // map {M, G, K}
-              tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, full_bar(s), m0 + 64 * c, g, k0);
+            for (int c = 0; c < a_n; ++c) load(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + 64 * c, g, k0);  // {M, G, K}
           }
-          if (!PAIR) {
-            if (!KT::B_MN) {
-              tma_load_3d(b_dst, &tmB, full_bar(s), k0, n0, g);                      // map {K, N, G}
-            } else {
-              for (int c = 0; c < b_chunks; ++c) {
-                if (!KT::B_ACT)                                                        // map {N, K, G}
-                  tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, k0, g);
-                else                                                                   // map {N, G, K}
-                  tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, g, k0);
-              }
-            }
+          if (!KT::B_MN) {
+            if (b_n) load(b_dst, &tmB, k0, nb0, g);                                     // map {K, N, G}
           } else {
-            if (!KT::B_MN) {
-              // Half `rank` of the 256-row K-major tile, to both CTAs.
-              if (rank < b_halves)
-                tma_load_3d_mc(b_dst + rank * (B_BYTES / 2), &tmB, full_bar(s), k0, n0 + 128 * rank, g, 0x3);
-            } else {
-              // Chunks 2*rank and 2*rank+1 of the MN-major tile, to both CTAs.
-              for (int c = 2 * rank; c < 2 * rank + 2 && c < b_chunks; ++c) {
-                if (!KT::B_ACT)
-                  tma_load_3d_mc(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, k0, g, 0x3);
-                else
-                  tma_load_3d_mc(b_dst + c * MN_CHUNK_BYTES, &tmB, full_bar(s), n0 + 64 * c, g, k0, 0x3);
-              }
+            for (int c = 0; c < b_n; ++c) {
+              if (!KT::B_ACT) load(b_dst + c * MN_CHUNK_BYTES, &tmB, nb0 + 64 * c, k0, g);  // map {N, K, G}
+              else load(b_dst + c * MN_CHUNK_BYTES, &tmB, nb0 + 64 * c, g, k0);            // map {N, G, K}
             }
           }
         }
       }
-      if (ok && PAIR) {
-        // Wait until both CTAs' MMAs have released the last stages, so no
-        // arrival from the peer is still on its way to this CTA's barriers
-        // when the cluster finishes.
+      if (ok) {
+        // Wait until the MMAs have released the last stages, so that no
+        // commit is still on its way to this CTA's barriers at the end.
         const int first_j = it > STAGES ? it - STAGES : 0;
         for (int j = first_j; j < it; ++j)
           mbar_wait_bounded(empty_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, p.wait_limit_ns, p.err,
                             ERRBIT_WAIT_DRAIN, abort_flag);
-      }
-      if (!ok) {
+      } else if (!PAIR) {
         // Let the copies already issued land before the CTA can exit.
         const int first_j = it > STAGES ? it - STAGES : 0;
         for (int j = first_j; j < it; ++j) {
@@ -420,19 +502,29 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait_bounded(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, kDrainLimitNs, p.err,
                             ERRBIT_WAIT_DRAIN, &no_abort);
         }
+      } else {
+        // A pair's copies are counted on the even CTA's barriers: give the
+        // ones in flight a fixed, ample time to land.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc<T, KT::A_MN, KT::B_MN>();
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = make_idesc<T, KT::A_MN, KT::B_MN, PAIR ? 2 * BM : BM>();
       int it = 0, lt = 0;
       bool ok = true;
       for (int tile = first; ok && tile < count; tile += stride, ++lt) {
         const int acc = lt & 1;
         const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
-        if (!mbar_wait_bounded(tempty_bar(acc), aph ^ 1u, p.wait_limit_ns, p.err, ERRBIT_WAIT_MMA, abort_flag)) {
+        const bool got = PAIR ? mbar_wait_bounded_cluster(tempty_bar(acc), aph ^ 1u, p.wait_limit_ns, p.err,
+                                                          ERRBIT_WAIT_MMA, abort_flag)
+                              : mbar_wait_bounded(tempty_bar(acc), aph ^ 1u, p.wait_limit_ns, p.err,
+                                                  ERRBIT_WAIT_MMA, abort_flag);
+        if (!got) {
           ok = false;
           break;
         }
@@ -446,7 +538,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = sA + s * A_BYTES, b_base = sB + s * B_BYTES;
+          const uint32_t a_base = sA + s * A_BYTES, b_base = sB + s * R::B_STAGE;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             // K-major: advance 16 elements (32 bytes) inside the swizzle atom;
@@ -455,17 +547,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             : sw128_desc(a_base + k * 32, 16, 1024);
             const uint64_t bdesc = KT::B_MN ? sw128_desc(b_base + k * 2048, MN_CHUNK_BYTES, 1024)
                                             : sw128_desc(b_base + k * 32, 16, 1024);
-            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_f16<PAIR>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          if (PAIR) umma_commit_mc(empty_bar(s), 0x3);
-          else umma_commit(empty_bar(s));
+          if (PAIR) umma_commit_pair(empty_bar(s));
+          else umma_commit<false>(empty_bar(s));
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        if (PAIR) umma_commit_pair(tfull_bar(acc));
+        else umma_commit<false>(tfull_bar(acc));
       }
       if (!ok) {
         // Make sure no MMA is still writing TMEM before it is freed.
-        umma_commit(drain_bar);
+        umma_commit<PAIR>(drain_bar);
         volatile int no_abort = 0;
         mbar_wait_bounded(drain_bar, 0, kDrainLimitNs, p.err, ERRBIT_WAIT_DRAIN, &no_abort);
       }
@@ -476,10 +569,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int ch = (warp - 2) >> 2;         // which half of the tile's columns
     constexpr int COLS = BN / (EPI_WARPS / 4);
+    // Accumulator-free arrivals go to the even CTA, which issues the MMAs.
+    const uint32_t te0 = PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    const uint32_t te1 = PAIR ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
     int lt = 0;
     for (int tile = first; tile < count; tile += stride, ++lt) {
       int g, m0, n0;
-      coords(tile, g, m0, n0);
+      coords(tile, rank, g, m0, n0);
       const int acc = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
       int ok = 1;
@@ -509,18 +605,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_remote(acc ? te1 : te0);
+        else mbar_arrive(tempty_bar(acc));
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  // Paired: neither CTA leaves while the other may still multicast into its
-  // shared memory or arrive on its barriers.
+  // Pair: neither CTA leaves while the other may still read its shared
+  // memory or signal its barriers, and TMEM is freed by both together.
   if (PAIR) cluster_barrier();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -571,6 +670,7 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t
 template <typename T, int KIND, int EPI, bool PAIR>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
   auto k = k_gemm_tc<T, KIND, EPI, PAIR>;
+  constexpr int SMEM_BYTES = Ring<PAIR>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (!PAIR) {
