@@ -128,7 +128,6 @@ Layout layout_of(const rmx_config& c) {
 rmx_status kernels_support(const rmx_config& c) {
   const int V = 16 / esize(c.dtype);
   if (c.D % V || c.H % V) return RMX_ERR_UNSUPPORTED;  // rows must be whole 16-byte vectors
-  if (c.D / kLnBwdColsPerThread > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
   if (c.D / V > kRowThreadsMax || c.H / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
   if ((c.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // LN forward: 10 vectors per lane
   if (!gate_bwd_fused_supported(layout_of(c).ra)) return RMX_ERR_UNSUPPORTED;

@@ -21,10 +21,12 @@ struct RowArgs {
 enum LnFwdMode { LNF_PLAIN = 0, LNF_MIXED_OUT = 1, LNF_SUM_IN = 2 };
 cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
                           const void* be, void* y, float* mu, float* rs, cudaStream_t st);
-// LayerNorm backward over CTAs (t, b-block); per-CTA partial sums of dgamma
-// and dbeta ([nbblk_ln*T][D]).  Modes: LNB_BIAS also sums ds per token into
-// pbias; LNB_MIXED_TOO reads s + s_add and also writes token_mix(ds) to
-// out_mixed; LNB_RESID adds resid to the output.
+// LayerNorm backward over CTAs (t, b-block) of up to nb_ln <= kLnBwdMaxRows
+// rows; per-CTA partial sums of dgamma and dbeta ([nbblk_ln*T][D]).  Modes:
+// LNB_BIAS also sums ds per token into pbias; LNB_MIXED_TOO reads s + s_add
+// and also writes token_mix(ds) to out_mixed; LNB_RESID adds resid to the
+// output.
+constexpr int kLnBwdMaxRows = 64;
 enum LnBwdMode { LNB_BIAS = 0, LNB_MIXED_TOO = 1, LNB_RESID = 2 };
 cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s, const void* s_add,
                           const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
@@ -64,7 +66,6 @@ cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStre
 
 // Largest thread count a row pass may use (one thread per 16-byte vector).
 constexpr int kRowThreadsMax = 512;
-constexpr int kLnBwdColsPerThread = 4;
 int max_dynamic_smem_bytes();
 
 // ------------------------------------------------------------------ GEMMs

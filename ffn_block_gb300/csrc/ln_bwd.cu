@@ -1,0 +1,331 @@
+// Backward of the three outer LayerNorms, one streaming pass per call.
+//
+// Page "Subgraph-fusion-based Mega-kernel Generation", section "Exact
+// computation": LN(z) = (z - mean) / sqrt(mean((z - mean)^2) + eps) * gamma
+// + beta over each row of D.  With xh the normalised row, g = gamma * gin and
+// the row means mg = mean(g), mgx = mean(g * xh):
+//   out = rstd * (g - mg - xh * mgx)     (+ a residual gradient, by mode)
+//   dgamma += gin * xh, dbeta += gin     (column partial sums)
+// Modes (kernels.h): LNB_BIAS also sums out over the batch per token (the
+// bias gradient of the GEMM that feeds norm2); LNB_MIXED_TOO reads the row as
+// s + s_add and writes out both plainly and token-mixed; LNB_RESID adds a
+// residual gradient to out.
+//
+// One CTA owns the rows b0 <= b < b1 of one token t.  Their input rows stream
+// into shared memory through an S-stage ring of bulk copies (one thread
+// issues them; a byte-counting mbarrier per stage); thread j owns the j-th
+// 16-byte vector of columns.  Per row the CTA takes the two row sums with one
+// barrier, then each thread writes its columns and keeps the column partial
+// sums in registers.  Every wait is bounded.
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmx {
+namespace {
+
+constexpr int kLnMaxStages = 8;
+constexpr int kLnSmemTarget = 52 * 1024;  // about four CTAs per SM
+
+// Sums v[0..1] over a warp with five shuffles: on return lane l holds the
+// sum of component bit4(l); lanes holding the same component hold the same
+// bits.
+__device__ __forceinline__ float warp_sum2_transposed(float v0, float v1) {
+  const int lane = threadIdx.x & 31;
+  const bool hi = lane & 16;
+  float k = hi ? v1 : v0;
+  const float s = hi ? v0 : v1;
+  k += __shfl_xor_sync(0xffffffffu, s, 16);
+  k += __shfl_xor_sync(0xffffffffu, k, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
+// Token mix as an addressing rule: column d = i*C + c of row j of a sample
+// goes to row i, column j*C + c.  Writes the V values of columns d0 .. d0+V-1
+// of row j to their mixed places (pairs when C is even).
+template <typename T, int V>
+__device__ __forceinline__ void store_mixed_row(T* sample_base, const float* v, int j, int d0, int C, int D) {
+  int i = d0 / C, c = d0 - i * C;
+  if ((C & 1) == 0) {
+#pragma unroll
+    for (int e = 0; e < V; e += 2) {
+      T* dst = sample_base + (size_t)i * D + j * C + c;
+      if (sizeof(T) == 2) {
+        T pr[2] = {from_f<T>(v[e]), from_f<T>(v[e + 1])};
+        *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(pr);
+      } else {
+        *reinterpret_cast<float2*>(dst) = make_float2(v[e], v[e + 1]);
+      }
+      c += 2;
+      while (c >= C) {
+        c -= C;
+        ++i;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      sample_base[(size_t)i * D + j * C + c] = from_f<T>(v[e]);
+      if (++c == C) {
+        c = 0;
+        ++i;
+      }
+    }
+  }
+}
+
+struct LnBwdArgs {
+  const void* gin;     // [N, D] upstream gradient
+  const void* s;       // [N, D] LayerNorm input (LNB_MIXED_TOO: its first term)
+  const void* s_add;   // [N, D] LNB_MIXED_TOO: second term of the input
+  const void* resid;   // [N, D] LNB_RESID: gradient added to the output
+  const float* mu;     // [N] forward statistics
+  const float* rs;
+  const void* gamma;   // [D]
+  void* out;           // [N, D]
+  void* out_mixed;     // [N, D] LNB_MIXED_TOO: token-mixed copy of out
+  float* pg;           // [nbblk*T, D] column partials of dgamma
+  float* pb;           // [nbblk*T, D] column partials of dbeta
+  float* pbias;        // [nbblk, T, D] LNB_BIAS: column partials of sum_b out
+  unsigned int* err;
+  int B, T, D, C, nb, stages;
+};
+
+// Per-row statistics area, rounded up so the ring starts 16-byte aligned.
+__host__ __device__ inline size_t stats_bytes(int nb) { return ((size_t)nb * 8 + 15) & ~(size_t)15; }
+
+template <int MODE> struct LnRows {
+  // Row tensors staged per row: gin, s, then s_add or resid.
+  static constexpr int value = (MODE == LNB_MIXED_TOO || MODE == LNB_RESID) ? 3 : 2;
+};
+
+// Shared memory: stats [nb] float2 | red [2][2][32] float | stages x rows |
+// mbarriers.
+template <typename T, int MODE>
+__global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
+  constexpr int E = VecN<T>::value;
+  constexpr int NR = LnRows<MODE>::value;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int D = a.D, S = a.stages;
+  const int t = blockIdx.x, bblk = blockIdx.y;
+  const int b0 = bblk * a.nb;
+  const int nrows = min(a.B, b0 + a.nb) - b0;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31, nw = nthreads >> 5;
+  const int c0 = tid * E;
+  const bool active = c0 < D;
+
+  float2* st_row = reinterpret_cast<float2*>(smem);                    // (rstd, -mean*rstd) per row
+  float* red = reinterpret_cast<float*>(smem + stats_bytes(a.nb));     // [2][2][32]
+  unsigned char* ring = reinterpret_cast<unsigned char*>(red + 2 * 2 * 32);
+  const size_t tensor_bytes = (size_t)D * sizeof(T);
+  const size_t row_bytes = NR * tensor_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)S * row_bytes);
+  __shared__ int abort_flag;
+
+  const T* third = reinterpret_cast<const T*>(MODE == LNB_MIXED_TOO ? a.s_add : a.resid);
+  auto issue = [&](int i, int s) {  // row i of this CTA into stage s
+    const size_t r = (size_t)(b0 + i) * a.T + t;
+    const uint32_t bar = smem_u32(&full[s]);
+    const uint32_t dst = smem_u32(ring + (size_t)s * row_bytes);
+    mbar_arrive_expect_tx(bar, (uint32_t)row_bytes);
+    bulk_g2s(dst, reinterpret_cast<const T*>(a.gin) + r * D, (uint32_t)tensor_bytes, bar);
+    bulk_g2s(dst + (uint32_t)tensor_bytes, reinterpret_cast<const T*>(a.s) + r * D, (uint32_t)tensor_bytes, bar);
+    if (NR == 3) bulk_g2s(dst + 2 * (uint32_t)tensor_bytes, third + r * D, (uint32_t)tensor_bytes, bar);
+  };
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int i = 0; i < min(S, nrows); ++i) issue(i, i);
+  for (int i = tid; i < nrows; i += nthreads) {
+    const size_t r = (size_t)(b0 + i) * a.T + t;
+    const float rstd = a.rs[r];
+    st_row[i] = make_float2(rstd, -a.mu[r] * rstd);
+  }
+  float gam[E];
+  if (active) load_vec(reinterpret_cast<const T*>(a.gamma) + c0, gam);
+  __syncthreads();
+
+  float ag[E], ab[E], ao[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) ag[e] = ab[e] = ao[e] = 0.f;
+
+  const float invD = 1.0f / (float)D;
+  const size_t row_step = (size_t)a.T * D;
+  T* out_row = reinterpret_cast<T*>(a.out) + ((size_t)b0 * a.T + t) * D;
+  int issued = min(S, nrows);
+  bool aborted = false;
+  int s = 0;
+  uint32_t ph = 0;
+  for (int i = 0; i < nrows; ++i, out_row += row_step) {
+    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                      (volatile int*)&abort_flag);
+    const float2 sr = st_row[i];
+    const float rstd = sr.x, cst = sr.y;
+    float g[E], xh[E], rv[E];
+    float r0 = 0.f, r1 = 0.f;
+    if (ok && active) {
+      const T* st = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
+      float gv[E], sv[E];
+      load_vec(st + c0, gv);
+      load_vec(st + D + c0, sv);
+      if (MODE == LNB_MIXED_TOO) {
+        float av[E];
+        load_vec(st + 2 * D + c0, av);
+#pragma unroll
+        for (int e = 0; e < E; ++e) sv[e] += av[e];
+      }
+      if (MODE == LNB_RESID) load_vec(st + 2 * D + c0, rv);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        xh[e] = fmaf(sv[e], rstd, cst);
+        g[e] = gam[e] * gv[e];
+        r0 += g[e];
+        r1 = fmaf(g[e], xh[e], r1);
+        ag[e] = fmaf(gv[e], xh[e], ag[e]);
+        ab[e] += gv[e];
+      }
+    }
+    float* rb = red + (i & 1) * 2 * 32;
+    {
+      const float k = warp_sum2_transposed(r0, r1);
+      if ((lane & 15) == 0) rb[(lane >> 4) * 32 + warp] = k;
+    }
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    if (tid == 0 && issued < nrows) issue(issued++, s);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+    float mg, mgx;
+    {
+      // Lane l adds the partials of warp l & 15 (at most 16 warps) for sum
+      // l >> 4; the sixteen lanes of each sum then combine.
+      const int c = lane >> 4, w = lane & 15;
+      float v = w < nw ? rb[c * 32 + w] : 0.f;
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      mg = __shfl_sync(0xffffffffu, v, 0) * invD;
+      mgx = __shfl_sync(0xffffffffu, v, 16) * invD;
+    }
+    if (active) {
+      const float q0 = -rstd * mg;
+      float o[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        o[e] = fmaf(rstd, fmaf(-mgx, xh[e], g[e]), q0);
+        if (MODE == LNB_BIAS) ao[e] += o[e];
+      }
+      if (MODE == LNB_MIXED_TOO)
+        store_mixed_row<T, E>(reinterpret_cast<T*>(a.out_mixed) + (size_t)(b0 + i) * a.T * D, o, t, c0, a.C, D);
+      if (MODE == LNB_RESID) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] += rv[e];
+      }
+      store_vec(out_row + c0, o);
+    }
+  }
+
+  if (aborted) {
+    // Wait (bounded) for the newest copy issued into each stage before the
+    // CTA's shared memory goes away.
+    if (tid == 0) {
+      volatile int no_abort = 0;
+      for (int i = max(0, issued - S); i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&full[i % S]), (uint32_t)((i / S) & 1), kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                          &no_abort);
+    }
+    return;
+  }
+  if (active) {
+    const size_t p = (size_t)bblk * a.T + t;
+    auto put = [&](float* dst, const float* v) {
+#pragma unroll
+      for (int k = 0; k < E; k += 4)
+        *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+    };
+    put(a.pg + p * D + c0, ag);
+    put(a.pb + p * D + c0, ab);
+    if (MODE == LNB_BIAS) put(a.pbias + p * D + c0, ao);
+  }
+}
+
+template <typename T, int MODE>
+cudaError_t launch_ring(const LnBwdArgs& base, cudaStream_t st) {
+  LnBwdArgs a = base;
+  constexpr int E = VecN<T>::value;
+  const int threads = (a.D / E + 31) / 32 * 32;
+  const size_t fixed = stats_bytes(a.nb) + 2 * 2 * 32 * 4;
+  const size_t row_bytes = (size_t)LnRows<MODE>::value * a.D * sizeof(T);
+  long long room = ((long long)kLnSmemTarget - (long long)fixed) / (long long)(row_bytes + 8);
+  if (room < 2) room = 2;
+  if (room > kLnMaxStages) room = kLnMaxStages;
+  a.stages = (int)room;
+  const size_t smem = fixed + (size_t)a.stages * (row_bytes + 8);
+  if ((long long)smem > (long long)max_dynamic_smem_bytes() - 1024) return cudaErrorInvalidValue;
+  auto k = k_ln_bwd_ring<T, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<dim3(a.T, (a.B + a.nb - 1) / a.nb), threads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_mode(const LnBwdArgs& a, int mode, cudaStream_t st) {
+  if (mode == LNB_BIAS) return launch_ring<T, LNB_BIAS>(a, st);
+  if (mode == LNB_MIXED_TOO) return launch_ring<T, LNB_MIXED_TOO>(a, st);
+  return launch_ring<T, LNB_RESID>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_ln_bwd(const RowArgs& ra, int mode, const void* gin, const void* s, const void* s_add,
+                          const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
+                          void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
+  const int V = ra.dtype == 0 ? 4 : 8;
+  if (ra.D % V || ra.D / V > 512 || ra.nb_ln < 1 || ra.nb_ln > kLnBwdMaxRows || ra.D % ra.T) return cudaErrorInvalidValue;
+  LnBwdArgs a;
+  a.gin = gin;
+  a.s = s;
+  a.s_add = s_add;
+  a.resid = resid;
+  a.mu = mu;
+  a.rs = rs;
+  a.gamma = gamma;
+  a.out = out;
+  a.out_mixed = out_mixed;
+  a.pg = pg;
+  a.pb = pb;
+  a.pbias = pbias;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidValue;
+  a.B = ra.B;
+  a.T = ra.T;
+  a.D = ra.D;
+  a.C = ra.D / ra.T;
+  a.nb = ra.nb_ln;
+  a.stages = 0;
+  if (ra.dtype == 0) return launch_mode<float>(a, mode, st);
+  if (ra.dtype == 1) return launch_mode<bf16>(a, mode, st);
+  return launch_mode<f16>(a, mode, st);
+}
+
+cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2, const float* r2,
+                           const void* g2, void* ds2, float* pg2, float* pb2, float* pbo, cudaStream_t st) {
+  return launch_ln_bwd(a, LNB_BIAS, dy, s2, nullptr, mu2, r2, g2, nullptr, ds2, nullptr, pg2, pb2, pbo, st);
+}
+
+}  // namespace rmx

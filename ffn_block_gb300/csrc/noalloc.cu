@@ -64,7 +64,7 @@ extern "C" rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void
   }
   const int e = cfg->dtype == RMX_F32 ? 4 : 2;
   const int V = 16 / e;
-  if (cfg->D % V || cfg->D / kLnBwdColsPerThread > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
+  if (cfg->D % V || cfg->D / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
 
   // Partial sums per block of up to 64 samples: gamma2 and beta2
   // [nbblk*T, D] and bout [nbblk, T*D].  Shapes whose partial sums exceed the

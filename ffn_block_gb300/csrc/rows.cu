@@ -163,122 +163,6 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
   }
 }
 
-constexpr int kLnBwdCols = 4;      // columns per thread in the apply sweep
-constexpr int kLnBwdMaxRows = 64;  // rows per CTA (shared row sums)
-
-// =========================================================================
-// LayerNorm backward for rows (b, t), CTA (t, b-block) -- t varies fastest
-// over the grid so concurrently running CTAs cover whole samples.  With
-// g = gamma * gin, xh = (s - mean) * rstd over the row:
-//   ds = rstd * (g - mean(g) - xh * mean(g * xh)),
-//   dgamma += gin * xh, dbeta += gin (per-CTA partial rows).
-// Modes:
-//   LNB_BIAS       out = ds; also dbias[t] += ds            (norm2; bias bout)
-//   LNB_MIXED_TOO  s = s + s_add; out = ds and out_mixed = token_mix(ds)
-//                                                           (norm1: s1 = mix + x)
-//   LNB_RESID      out = ds + resid                         (norm0 + residual)
-// Two sweeps over the CTA's rows with one barrier between them: (1) one warp
-// per row takes the two row sums with 16-byte loads; (2) thread v owns
-// columns 4v .. 4v+3 of every row, re-reads them (now cache-resident),
-// writes the outputs and keeps the column partial sums in registers.
-// =========================================================================
-template <typename T, int MODE>
-__global__ void __launch_bounds__(512) k_ln_bwd(const T* __restrict__ gin, const T* __restrict__ s,
-                                                const T* __restrict__ s_add, const float* __restrict__ mu,
-                                                const float* __restrict__ rs, const T* __restrict__ gamma,
-                                                const T* __restrict__ resid, T* __restrict__ out,
-                                                T* __restrict__ out_mixed, float* __restrict__ pg,
-                                                float* __restrict__ pb, float* __restrict__ pbias, int B, int Tn,
-                                                int D, int C, int nb) {
-  constexpr int V = VecN<T>::value;
-  constexpr int E = kLnBwdCols;
-  __shared__ float2 rsum[kLnBwdMaxRows];
-  const int t = blockIdx.x, bblk = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int b_begin = bblk * nb;
-  const int nrows = max(0, min(B, b_begin + nb) - b_begin);
-  const float invD = 1.0f / (float)D;
-
-  // ---- sweep 1: row sums of g and g * xh, one warp per row.
-  const int nv = D / V;
-  for (int i = warp; i < nrows; i += nw) {
-    const size_t r = (size_t)(b_begin + i) * Tn + t;
-    const float mean = mu[r], rstd = rs[r];
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll 2
-    for (int vi = lane; vi < nv; vi += 32) {
-      float gv[V], sv[V], gm[V];
-      load_vec(gin + r * D + vi * V, gv);
-      load_vec(s + r * D + vi * V, sv);
-      load_vec(gamma + vi * V, gm);
-      if (MODE == LNB_MIXED_TOO) {
-        float av[V];
-        load_vec(s_add + r * D + vi * V, av);
-#pragma unroll
-        for (int e = 0; e < V; ++e) sv[e] += av[e];
-      }
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float g = gm[e] * gv[e];
-        a0 += g;
-        a1 += g * (sv[e] - mean) * rstd;
-      }
-    }
-    a0 = warp_sum(a0);
-    a1 = warp_sum(a1);
-    if (lane == 0) rsum[i] = make_float2(a0, a1);
-  }
-  __syncthreads();
-
-  // ---- sweep 2: outputs and column partial sums.
-  const int d0 = threadIdx.x * E;
-  if (d0 >= D) return;
-  float gam[E], ag[E], ab[E], ao[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) ag[e] = ab[e] = ao[e] = 0.f;
-  load_n<T, E>(gamma + d0, gam);
-#pragma unroll 2
-  for (int i = 0; i < nrows; ++i) {
-    const int b = b_begin + i;
-    const size_t r = (size_t)b * Tn + t;
-    const float mean = mu[r], rstd = rs[r];
-    const float2 sm = rsum[i];
-    const float mg = sm.x * invD, mgx = sm.y * invD;
-    float gv[E], sv[E], o[E];
-    load_n<T, E>(gin + r * D + d0, gv);
-    load_n<T, E>(s + r * D + d0, sv);
-    if (MODE == LNB_MIXED_TOO) {
-      float av[E];
-      load_n<T, E>(s_add + r * D + d0, av);
-#pragma unroll
-      for (int e = 0; e < E; ++e) sv[e] += av[e];
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float xh = (sv[e] - mean) * rstd;
-      o[e] = rstd * (gam[e] * gv[e] - mg - xh * mgx);
-      ag[e] += gv[e] * xh;
-      ab[e] += gv[e];
-      if (MODE == LNB_BIAS) ao[e] += o[e];
-    }
-    if (MODE == LNB_MIXED_TOO) store_mixed<T, E>(out_mixed + (size_t)b * Tn * D, o, t, d0, C, D);
-    if (MODE == LNB_RESID) {
-      float rv[E];
-      load_n<T, E>(resid + r * D + d0, rv);
-#pragma unroll
-      for (int e = 0; e < E; ++e) o[e] += rv[e];
-    }
-    store_n<T, E>(out + r * D + d0, o);
-  }
-  const size_t p = (size_t)bblk * Tn + t;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    pg[p * D + d0 + e] = ag[e];
-    pb[p * D + d0 + e] = ab[e];
-    if (MODE == LNB_BIAS) pbias[p * D + d0 + e] = ao[e];
-  }
-}
-
 // =========================================================================
 // Z statistics for the FFMA path: one warp per (row, 256-column tile) of
 // Z = [U | G]; {mean, M2} of the tile's U columns and of its G columns, from
@@ -458,32 +342,6 @@ cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void*
 #undef RMX_LNF_Q
 #undef RMX_LNF
   return cudaGetLastError();
-}
-
-cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s, const void* s_add,
-                          const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
-                          void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
-  const int threads = round32(a.D / kLnBwdCols);
-  if (threads > kRowThreadsMax || a.nb_ln > kLnBwdMaxRows) return cudaErrorInvalidValue;
-  dim3 grid(a.T, a.nbblk_ln);
-  const int C = a.D / a.T;
-#define RMX_LNB(M)                                                                                             \
-  RMX_DISPATCH_T(a.dtype, {                                                                                    \
-    k_ln_bwd<T, M><<<grid, threads, 0, st>>>((const T*)gin, (const T*)s, (const T*)s_add, mu, rs,              \
-                                             (const T*)gamma, (const T*)resid, (T*)out, (T*)out_mixed, pg, pb, \
-                                             pbias, a.B, a.T, a.D, C, a.nb_ln);                                \
-  })
-  if (mode == LNB_BIAS) RMX_LNB(LNB_BIAS);
-  else if (mode == LNB_MIXED_TOO) RMX_LNB(LNB_MIXED_TOO);
-  else RMX_LNB(LNB_RESID);
-#undef RMX_LNB
-  return cudaGetLastError();
-}
-
-cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
-                           const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
-                           float* pbo, cudaStream_t st) {
-  return launch_ln_bwd(a, LNB_BIAS, dy, s2, nullptr, mu2, r2, g2, nullptr, ds2, nullptr, pg2, pb2, pbo, st);
 }
 
 cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaStream_t st) {
