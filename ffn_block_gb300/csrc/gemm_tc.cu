@@ -62,7 +62,7 @@ template <bool PAIR> struct Ring {
   static constexpr int B_STAGE = PAIR ? B_BYTES / 2 : B_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_STAGE;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_WARPS * 4096 + 256;
   static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
 };
 constexpr uint64_t kDrainLimitNs = 50ull * 1000ull * 1000ull;
@@ -319,18 +319,33 @@ struct ZSums {
   float n, k, s, q;  // count, shift, sum(x - k), sum((x - k)^2)
 };
 
+// Two floats rounded to the storage type, packed into 32 bits (lower
+// column in the low half).
+template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<bf16>(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <> __device__ __forceinline__ uint32_t pack2<f16>(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Epilogue of 32 consecutive columns n_base .. n_base+31 of row m: bias /
+// residual in fp32, the Z statistics, and the result rounded and packed into
+// pk[0..15].  Columns at or past N (and rows past M) are computed from
+// whatever the accumulator holds; the tensor store clips them.
 template <typename T, int EPI>
-__device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, int n_base, const float* v,
-                                               ZSums* zs) {
+__device__ __forceinline__ void epilogue_convert(const Params& p, int g, int m, int n_base, const float* v,
+                                                 ZSums* zs, uint32_t* pk) {
   constexpr int V = VecN<T>::value;
-  T* orow = reinterpret_cast<T*>(p.out) + (size_t)g * p.out_gs + (size_t)m * p.out_rs;
 #pragma unroll
   for (int c = 0; c < 32; c += V) {
     const int n = n_base + c;
-    if (n < p.N) {
-      float o[V];
+    float o[V];
 #pragma unroll
-      for (int e = 0; e < V; ++e) o[e] = v[c + e];
+    for (int e = 0; e < V; ++e) o[e] = v[c + e];
+    if (n < p.N && m < p.M) {
       if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_ZSTATS) {
         float bv[V];
         load_vec(reinterpret_cast<const T*>(p.bias) + (size_t)g * p.bias_gs + n, bv);
@@ -343,7 +358,6 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, in
 #pragma unroll
         for (int e = 0; e < V; ++e) o[e] += rv[e];
       }
-      store_vec(orow + n, o);
       if (EPI == EPI_BIAS_ZSTATS) {
         // Shifted sums of the stored (rounded) values of this half: the
         // shift is the half's first value in this column group, so the
@@ -366,12 +380,32 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int g, int m, in
         else add(zs[1]);
       }
     }
+#pragma unroll
+    for (int e = 0; e < V; e += 2) pk[(c + e) >> 1] = pack2<T>(o[e], o[e + 1]);
   }
+}
+
+// Tensor store of a shared-memory box (bulk async group).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the shared memory of every committed store has been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 template <typename T, int KIND, int EPI, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const Params p) {
   using KT = KindTraits<KIND>;
   using R = Ring<PAIR>;
   constexpr int STAGES = R::STAGES;
@@ -380,7 +414,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * R::STAGE_BYTES);
+  // Output staging: one 32-row x 64-column box (4 KB, 128-byte swizzle) per
+  // epilogue warp, after the ring (1024-byte aligned).
+  const uint32_t sStage = sA + STAGES * R::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * R::STAGE_BYTES + EPI_WARPS * 4096);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + R::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
@@ -415,6 +452,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_map(&tmA);
     prefetch_map(&tmB);
+    prefetch_map(&tmC);
   }
   if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
@@ -572,6 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Accumulator-free arrivals go to the even CTA, which issues the MMAs.
     const uint32_t te0 = PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     const uint32_t te1 = PAIR ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
+    const uint32_t stage = sStage + (uint32_t)(warp - 2) * 4096u;
     int lt = 0;
     for (int tile = first; tile < count; tile += stride, ++lt) {
       int g, m0, n0;
@@ -588,11 +627,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int c0 = ch * COLS;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
       ZSums zs[2] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int j0 = 0; j0 < COLS; j0 += 32) {
-        if (n0 + c0 + j0 >= p.N || m0 >= p.M) break;  // warp-uniform
-        float v[32];
-        tmem_ld_32x32(t_row + (uint32_t)j0, v);
-        if (m < p.M) epilogue_store<T, EPI>(p, g, m, n0 + c0 + j0, v, zs);
+      for (int j0 = 0; j0 < COLS; j0 += 64) {
+        if (n0 + c0 + j0 >= p.N || m0 + q * 32 >= p.M) break;  // warp-uniform
+        uint32_t pk[32];
+        {
+          float v[32];
+          tmem_ld_32x32(t_row + (uint32_t)j0, v);
+          epilogue_convert<T, EPI>(p, g, m, n0 + c0 + j0, v, zs, pk);
+          tmem_ld_32x32(t_row + (uint32_t)(j0 + 32), v);
+          epilogue_convert<T, EPI>(p, g, m, n0 + c0 + j0 + 32, v, zs, pk + 16);
+        }
+        // The previous box must have been read out of the staging buffer.
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        // Row `lane` of the box: eight 16-byte chunks, chunk j at position
+        // j ^ (row % 8) (the tensor map's 128-byte swizzle).
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(stage + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), pk[4 * j], pk[4 * j + 1],
+                       pk[4 * j + 2], pk[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (KIND == GEMM_WGRAD) tma_store_3d(&tmC, stage, n0 + c0 + j0, m0 + q * 32, g);   // map {N, M, G}
+          else tma_store_3d(&tmC, stage, n0 + c0 + j0, g, m0 + q * 32);                    // map {N, G, M}
+          bulk_commit();
+        }
       }
       if (EPI == EPI_BIAS_ZSTATS && m < p.M && n0 + c0 < p.N) {
         float4 w;
@@ -610,6 +670,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         else mbar_arrive(tempty_bar(acc));
       }
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -668,14 +730,15 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t
 }
 
 template <typename T, int KIND, int EPI, bool PAIR>
-cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const Params& p,
+                      cudaStream_t st) {
   auto k = k_gemm_tc<T, KIND, EPI, PAIR>;
   constexpr int SMEM_BYTES = Ring<PAIR>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (!PAIR) {
     const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-    k<<<grid, THREADS, SMEM_BYTES, st>>>(a, b, p);
+    k<<<grid, THREADS, SMEM_BYTES, st>>>(a, b, c, p);
     return cudaGetLastError();
   }
   const int clusters = p.num_pair_tiles < sm_count() / 2 ? p.num_pair_tiles : sm_count() / 2;
@@ -691,20 +754,20 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const Params& 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, c, p);
 }
 
 template <typename T, bool PAIR>
-cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                        cudaStream_t st) {
+cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const Params& p, cudaStream_t st) {
   switch (d.kind * 8 + d.epi) {
-    case GEMM_FWD * 8 + EPI_STORE: return launch_tc<T, GEMM_FWD, EPI_STORE, PAIR>(a, b, p, st);
-    case GEMM_FWD * 8 + EPI_BIAS: return launch_tc<T, GEMM_FWD, EPI_BIAS, PAIR>(a, b, p, st);
-    case GEMM_FWD * 8 + EPI_BIAS_RESID: return launch_tc<T, GEMM_FWD, EPI_BIAS_RESID, PAIR>(a, b, p, st);
-    case GEMM_FWD * 8 + EPI_BIAS_ZSTATS: return launch_tc<T, GEMM_FWD, EPI_BIAS_ZSTATS, PAIR>(a, b, p, st);
-    case GEMM_DGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE, PAIR>(a, b, p, st);
-    case GEMM_DGRAD * 8 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID, PAIR>(a, b, p, st);
-    case GEMM_WGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE, PAIR>(a, b, p, st);
+    case GEMM_FWD * 8 + EPI_STORE: return launch_tc<T, GEMM_FWD, EPI_STORE, PAIR>(a, b, c, p, st);
+    case GEMM_FWD * 8 + EPI_BIAS: return launch_tc<T, GEMM_FWD, EPI_BIAS, PAIR>(a, b, c, p, st);
+    case GEMM_FWD * 8 + EPI_BIAS_RESID: return launch_tc<T, GEMM_FWD, EPI_BIAS_RESID, PAIR>(a, b, c, p, st);
+    case GEMM_FWD * 8 + EPI_BIAS_ZSTATS: return launch_tc<T, GEMM_FWD, EPI_BIAS_ZSTATS, PAIR>(a, b, c, p, st);
+    case GEMM_DGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_DGRAD, EPI_STORE, PAIR>(a, b, c, p, st);
+    case GEMM_DGRAD * 8 + EPI_RESID: return launch_tc<T, GEMM_DGRAD, EPI_RESID, PAIR>(a, b, c, p, st);
+    case GEMM_WGRAD * 8 + EPI_STORE: return launch_tc<T, GEMM_WGRAD, EPI_STORE, PAIR>(a, b, c, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -747,7 +810,7 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
     return !(v && v[0] == '0');
   }();
   const bool pair = pairs_on && d.M > BM;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
   bool ok = true;
   if (d.kind == GEMM_FWD || d.kind == GEMM_DGRAD) {
     ok &= make_map(&ma, d.A, d.dtype, K, G, M, K * e, G * K * e, BK, 1, BM);          // A [M,G,K]
@@ -759,6 +822,9 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
     ok &= make_map(&ma, d.A, d.dtype, M, G, K, M * e, G * M * e, 64, 1, BK);          // A [K,G,M]
     ok &= make_map(&mb, d.Bm, d.dtype, N, G, K, N * e, G * N * e, 64, 1, BK);         // B [K,G,N]
   }
+  // Output boxes of 32 rows x 64 columns, written by the epilogue warps.
+  if (d.kind == GEMM_WGRAD) ok &= make_map(&mc, d.C, d.dtype, N, M, G, N * e, M * N * e, 64, 32, 1);  // C [G,M,N]
+  else ok &= make_map(&mc, d.C, d.dtype, N, G, M, N * e, G * N * e, 64, 1, 32);                       // C [M,G,N]
   if (!ok) return cudaErrorInvalidValue;
   Params p;
   p.M = d.M;
@@ -791,8 +857,9 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.zstats = d.zstats;
   p.split = d.split;
   p.zgroups = (d.N + kZStatsTile - 1) / kZStatsTile;
-  if (d.dtype == 1) return pair ? dispatch_tc<bf16, true>(d, ma, mb, p, st) : dispatch_tc<bf16, false>(d, ma, mb, p, st);
-  return pair ? dispatch_tc<f16, true>(d, ma, mb, p, st) : dispatch_tc<f16, false>(d, ma, mb, p, st);
+  if (d.dtype == 1)
+    return pair ? dispatch_tc<bf16, true>(d, ma, mb, mc, p, st) : dispatch_tc<bf16, false>(d, ma, mb, mc, p, st);
+  return pair ? dispatch_tc<f16, true>(d, ma, mb, mc, p, st) : dispatch_tc<f16, false>(d, ma, mb, mc, p, st);
 }
 
 cudaError_t launch_bounded_wait_test(unsigned int* err, unsigned long long limit_ns, cudaStream_t st) {
