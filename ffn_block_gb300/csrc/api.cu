@@ -19,6 +19,8 @@
 //   6. dw1[t] = out1[:,t]^T @ dZ[:,t]                              (GEMM, TN)
 //   7. dx = norm1/mix/norm0 backward(dout1), partials of their params
 //   8. fixed-order column sums of every partial
+// The backward is launched on the caller's stream in the order 1 2 4 5 7 3 6
+// 8: the weight gradients, which nothing else consumes, come last.
 
 #include <atomic>
 #include <map>
@@ -232,40 +234,6 @@ rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
   return l.done(e);
 }
 
-// Second stream for the weight-gradient GEMMs, which do not feed the rest of
-// the backward: both run beside the norm1/norm0 backward.  One per device,
-// created on first use;
-// host-side enqueue of a backward is serialised so the shared events are
-// recorded and waited on in order.
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex g_side_mu;
-
-SideStream* side_stream() {
-  static SideStream side[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  SideStream& ss = side[dev];
-  if (!ss.s) {
-    cudaStream_t s = nullptr;
-    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
-      return nullptr;
-    ss.s = s;
-  }
-  return &ss;
-}
-
-// Makes `to` wait for everything enqueued on `from` so far.
-rmx_status stream_wait(cudaStream_t to, cudaStream_t from, cudaEvent_t ev) {
-  if (cudaEventRecord(ev, from) != cudaSuccess) return RMX_ERR_CUDA;
-  if (cudaStreamWaitEvent(to, ev, 0) != cudaSuccess) return RMX_ERR_CUDA;
-  return RMX_OK;
-}
-
 inline char* at(void* base, size_t off) { return static_cast<char*>(base) + off; }
 inline const char* at(const void* base, size_t off) { return static_cast<const char*>(base) + off; }
 
@@ -372,21 +340,6 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
     RMX_TRY(run_gemm("gemm1_dgrad", d, st));
   }
-  // The two weight-gradient GEMMs run on a side stream beside the LayerNorm
-  // backward passes (small shared-memory footprint, so they share SMs with
-  // the GEMM's CTAs); everything before them keeps the GPU to itself.
-  std::lock_guard<std::mutex> side_lock(g_side_mu);
-  SideStream* side = side_stream();
-  cudaStream_t wst = side ? side->s : st;
-  if (side) RMX_TRY(stream_wait(wst, st, side->fork));
-  {
-    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
-    RMX_TRY(run_gemm("gemm2_wgrad", d, wst));
-  }
-  {
-    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
-    RMX_TRY(run_gemm("gemm1_wgrad", d, wst));
-  }
   {
     Launch l("ln1_bwd_mixed", st);
     RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_MIXED_TOO, dout1, mix0, x, S.mu1, S.r1, p.gamma1, nullptr, ds1, da0,
@@ -396,6 +349,16 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     Launch l("ln0_bwd", st);
     RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_RESID, da0, x, nullptr, S.mu0, S.r0, p.gamma0, ds1, dx, nullptr,
                                  F(L.pg0), F(L.pb0), nullptr, st)));
+  }
+  // Weight gradients last: every SM is busy with one GEMM CTA, so there is
+  // nothing for a second stream to overlap them with.
+  {
+    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
+    RMX_TRY(run_gemm("gemm2_wgrad", d, st));
+  }
+  {
+    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
+    RMX_TRY(run_gemm("gemm1_wgrad", d, st));
   }
   {
     const int P = L.ra.nbblk * c.T, Pb = L.ra.nbblk;
@@ -412,7 +375,6 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     cudaError_t e = launch_colsums(jobs, 12, c.dtype, st);
     RMX_TRY(l.done(e));
   }
-  if (side) RMX_TRY(stream_wait(st, wst, side->join));
   return RMX_OK;
 }
 
