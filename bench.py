@@ -93,8 +93,7 @@ def row_bytes_per_launch(s) -> dict:
     return {
         "ln0_fwd_mixed": 2 * BTD,                   # x in, token_mix(norm0(x)) out
         "ln1_fwd": 3 * BTD,                         # mix, x in, out1 out
-        "gate_fwd": 2 * BTH + BTH,                  # Z in, hidden out
-        "gate_stats": N * ((2 * s.H + 127) // 128) * 16,  # per-group statistics in
+        "gate_fwd": 2 * BTH + BTH,                  # Z in, hidden out (row statistics merged in-pass)
         "ln2_fwd": 2 * BTD,                         # s2 in, y out
         "ln2_bwd": 3 * BTD,                         # dy, s2 in, ds2 out
         "gate_bwd": BTH + 2 * BTH + 2 * BTH,        # dh, Z in, dZ out (single pass)

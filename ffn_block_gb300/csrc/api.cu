@@ -286,13 +286,9 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
     }
   }
   {
-    Launch l("gate_stats", st);
-    RMX_TRY(l.done(launch_zstats_merge(L.ra, zstats, S.muU, S.rU, S.muG, S.rG, st)));
-  }
-  {
     Launch l("gate_fwd", st);
-    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b, hidden,
-                                   st)));
+    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, zstats, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
+                                   hidden, st)));
   }
   {
     GemmDesc d{GEMM_FWD, EPI_BIAS_RESID, c.dtype, c.B, c.D, c.H, c.T, hidden, p.wout, s2, p.bout, out1};

@@ -36,13 +36,11 @@ cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const voi
 cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
                            const float* r2, const void* g2, void* ds2, float* pg2, float* pb2,
                            float* pbo, cudaStream_t st);
-// Forward of the gate: (1) per-row mean and 1/sqrt(var+eps) of U and G
-// merged from `zstats` (see below); (2) hidden = LN_x(U) * silu(LN_gate(G))
-// from Z = [U | G], elementwise.
-cudaError_t launch_zstats_merge(const RowArgs& a, const float* zstats, float* muU, float* rU, float* muG, float* rG,
-                                cudaStream_t st);
-cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* muU, const float* rU, const float* muG,
-                            const float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
+// Forward of the gate, one pass: the per-row mean and 1/sqrt(var+eps) of U
+// and G merged from `zstats` (see below) and written to muU, rU, muG, rG;
+// then hidden = LN_x(U) * silu(LN_gate(G)) from Z = [U | G].
+cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, float* muU, float* rU,
+                            float* muG, float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
                             void* hidden, cudaStream_t st);
 // Single-pass gate backward: dZ and the column partials of lnx_w, lnx_b,
 // lng_w, lng_b ([nbblk*T, H] each) and b1 ([nbblk, T, 2H]) from dh, Z and the

@@ -210,14 +210,22 @@ __global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* 
 }
 
 // =========================================================================
-// F3a: per-row statistics of U and G from the group statistics: one warp per
-// row; lane l merges groups l, l+32, ... in order (Chan, Golub and LeVeque's
-// pairwise update), then the lanes merge pairwise in a fixed order.  Writes
-// mean and 1/sqrt(var + eps) of U and of G.
+// F3: hidden = LN_x(U) * silu(LN_gate(G)), Z = [U | G], one warp per row.
+// The warp first merges the row's group statistics (lane l takes groups l,
+// l+32, ... in order with Chan, Golub and LeVeque's pairwise update, then
+// the lanes merge pairwise in a fixed order, so every lane holds the same
+// bits), writes mean and 1/sqrt(var + eps) of U and G for the backward, and
+// then streams the row: lane l owns the 16-byte vectors l, l+32, ... of both
+// halves.
 // =========================================================================
-__global__ void __launch_bounds__(256) k_zstats_merge(const float* __restrict__ zstats, float* __restrict__ muU,
-                                                      float* __restrict__ rU, float* __restrict__ muG,
-                                                      float* __restrict__ rG, int N, int H, float eps) {
+template <typename T>
+__global__ void __launch_bounds__(256) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
+                                                  float* __restrict__ muU, float* __restrict__ rU,
+                                                  float* __restrict__ muG, float* __restrict__ rG,
+                                                  const T* __restrict__ wx, const T* __restrict__ bx,
+                                                  const T* __restrict__ wg, const T* __restrict__ bg,
+                                                  T* __restrict__ hidden, int N, int H, float eps) {
+  constexpr int V = VecN<T>::value;
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= N) return;
@@ -233,47 +241,35 @@ __global__ void __launch_bounds__(256) k_zstats_merge(const float* __restrict__ 
   }
   u = warp_merge_moments(u);
   g = warp_merge_moments(g);
+  const float sU = 1.0f / sqrtf(u.m2 / (float)H + eps), sG = 1.0f / sqrtf(g.m2 / (float)H + eps);
   if (lane == 0) {
     muU[r] = u.mean;
-    rU[r] = 1.0f / sqrtf(u.m2 / (float)H + eps);
+    rU[r] = sU;
     muG[r] = g.mean;
-    rG[r] = 1.0f / sqrtf(g.m2 / (float)H + eps);
+    rG[r] = sG;
   }
-}
-
-// =========================================================================
-// F3b: hidden = LN_x(U) * silu(LN_gate(G)), Z = [U | G]: one thread per
-// 16-byte vector of the hidden row (columns h .. h+V-1 of both halves), rows
-// consecutive over the grid; the row statistics come from F3a.
-// =========================================================================
-template <typename T>
-__global__ void __launch_bounds__(256) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ muU,
-                                                  const float* __restrict__ rU, const float* __restrict__ muG,
-                                                  const float* __restrict__ rG, const T* __restrict__ wx,
-                                                  const T* __restrict__ bx, const T* __restrict__ wg,
-                                                  const T* __restrict__ bg, T* __restrict__ hidden, int N, int H) {
-  constexpr int V = VecN<T>::value;
-  const int nv = H / V;
-  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (item >= (long long)N * nv) return;
-  const int r = (int)(item / nv), v = (int)(item - (long long)r * nv);
-  const int h0 = v * V;
+  const float cU = -u.mean * sU, cG = -g.mean * sG;
   const T* zr = Z + (size_t)r * 2 * H;
-  float u[V], g[V], fwx[V], fbx[V], fwg[V], fbg[V], o[V];
-  load_vec(zr + h0, u);
-  load_vec(zr + H + h0, g);
-  load_vec(wx + h0, fwx);
-  load_vec(bx + h0, fbx);
-  load_vec(wg + h0, fwg);
-  load_vec(bg + h0, fbg);
-  const float sU = rU[r], cU = -muU[r] * sU, sG = rG[r], cG = -muG[r] * sG;
+  T* hr = hidden + (size_t)r * H;
+  const int nv = H / V;
+#pragma unroll 2
+  for (int v = lane; v < nv; v += 32) {
+    const int h0 = v * V;
+    float zu[V], zg[V], fwx[V], fbx[V], fwg[V], fbg[V], o[V];
+    load_vec(zr + h0, zu);
+    load_vec(zr + H + h0, zg);
+    load_vec(wx + h0, fwx);
+    load_vec(bx + h0, fbx);
+    load_vec(wg + h0, fwg);
+    load_vec(bg + h0, fbg);
 #pragma unroll
-  for (int e = 0; e < V; ++e) {
-    const float uu = fmaf(fmaf(u[e], sU, cU), fwx[e], fbx[e]);
-    const float gg = fmaf(fmaf(g[e], sG, cG), fwg[e], fbg[e]);
-    o[e] = uu * (gg * sigmoid_fast(gg));
+    for (int e = 0; e < V; ++e) {
+      const float uu = fmaf(fmaf(zu[e], sU, cU), fwx[e], fbx[e]);
+      const float gg = fmaf(fmaf(zg[e], sG, cG), fwg[e], fbg[e]);
+      o[e] = uu * (gg * sigmoid_fast(gg));
+    }
+    store_vec(hr + h0, o);
   }
-  store_vec(hidden + (size_t)r * H + h0, o);
 }
 
 // =========================================================================
@@ -353,22 +349,13 @@ cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_zstats_merge(const RowArgs& a, const float* zstats, float* muU, float* rU, float* muG, float* rG,
-                                cudaStream_t st) {
-  const int N = a.B * a.T;
-  k_zstats_merge<<<(N + 7) / 8, 256, 0, st>>>(zstats, muU, rU, muG, rG, N, a.H, 1e-5f);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* muU, const float* rU, const float* muG,
-                            const float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
+cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, float* muU, float* rU,
+                            float* muG, float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
                             void* hidden, cudaStream_t st) {
   const int N = a.B * a.T;
-  const long long items = (long long)N * (a.H / vec_elems(a.dtype));
-  const int grid = (int)((items + 255) / 256);
   RMX_DISPATCH_T(a.dtype, {
-    k_gate_fwd<T><<<grid, 256, 0, st>>>((const T*)Z, muU, rU, muG, rG, (const T*)wx, (const T*)bx, (const T*)wg,
-                                        (const T*)bg, (T*)hidden, N, a.H);
+    k_gate_fwd<T><<<(N + 7) / 8, 256, 0, st>>>((const T*)Z, zstats, muU, rU, muG, rG, (const T*)wx, (const T*)bx,
+                                               (const T*)wg, (const T*)bg, (T*)hidden, N, a.H, 1e-5f);
   });
   return cudaGetLastError();
 }
