@@ -622,12 +622,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int c0 = ch * COLS;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
       ZSums zs[2] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // The accumulator is released as soon as its last columns are in
+      // registers, before they are converted and stored, so that the store
+      // path never delays the next tile's MMAs.
+      bool released = false;
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR) mbar_arrive_remote(acc ? te1 : te0);
+          else mbar_arrive(tempty_bar(acc));
+        }
+        released = true;
+      };
       for (int j0 = 0; j0 < COLS; j0 += 64) {
         if (n0 + c0 + j0 >= p.N || m0 + q * 32 >= p.M) break;  // warp-uniform
         uint32_t pk[32];
         {
           float v[64];
           tmem_ld_32x64(t_row + (uint32_t)j0, v);
+          if (j0 + 64 >= COLS || n0 + c0 + j0 + 64 >= p.N) release();
           epilogue_convert<T, EPI>(p, g, m, n0 + c0 + j0, v, zs, pk);
           epilogue_convert<T, EPI>(p, g, m, n0 + c0 + j0 + 32, v + 32, zs, pk + 16);
         }
@@ -648,6 +662,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           bulk_commit();
         }
       }
+      if (!released) release();
       if (EPI == EPI_BIAS_ZSTATS && m < p.M && n0 + c0 < p.N) {
         float4 w;
         w.x = zs[0].n > 0.f ? zs[0].k + zs[0].s / zs[0].n : 0.f;
@@ -656,12 +671,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         w.w = zs[1].n > 0.f ? fmaxf(zs[1].q - zs[1].s * zs[1].s / zs[1].n, 0.f) : 0.f;
         const int grp = (n0 + c0) / kZStatsTile;
         *reinterpret_cast<float4*>(p.zstats + (((size_t)m * p.G + g) * p.zgroups + grp) * 4) = w;
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR) mbar_arrive_remote(acc ? te1 : te0);
-        else mbar_arrive(tempty_bar(acc));
       }
     }
     if (lane == 0) bulk_wait_all();
