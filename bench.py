@@ -91,13 +91,14 @@ def row_bytes_per_launch(s) -> dict:
     N = s.B * s.T
     BTD, BTH = N * s.D * e, N * s.H * e
     return {
-        "ln0_fwd_mixed": 2 * BTD,                   # x in, token_mix(norm0(x)) out
-        "ln1_fwd": 3 * BTD,                         # mix, x in, out1 out
+        "ln01_fwd": 3 * BTD,                        # x in; s1 and out1 out (one CTA per sample)
+        "ln0_fwd_mixed": 2 * BTD,                   # x in, token_mix(norm0(x)) out (large samples)
+        "ln1_fwd": 4 * BTD,                         # mix, x in; s1 and out1 out (large samples)
         "gate_fwd": 2 * BTH + BTH,                  # Z in, hidden out (row statistics merged in-pass)
         "ln2_fwd": 2 * BTD,                         # s2 in, y out
         "ln2_bwd": 3 * BTD,                         # dy, s2 in, ds2 out
         "gate_bwd": BTH + 2 * BTH + 2 * BTH,        # dh, Z in, dZ out (single pass)
-        "ln1_bwd_mixed": 5 * BTD,                   # dout1, mix, x in; ds1 and token_mix(ds1) out
+        "ln1_bwd_mixed": 4 * BTD,                   # dout1, s1 in; ds1 and token_mix(ds1) out
         "ln0_bwd": 4 * BTD,                         # token_mix(ds1), x, ds1 in, dx out
     }
 

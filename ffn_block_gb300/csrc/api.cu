@@ -57,7 +57,7 @@ inline int esize(int dtype) { return dtype == RMX_F32 ? 4 : 2; }
 // ------------------------------------------------------------------ layouts
 struct Layout {
   // saved (filled by the forward)
-  size_t out1, Z, hidden, s2, stats, zstats, mix0, saved_total;
+  size_t out1, Z, hidden, s2, stats, zstats, s1, saved_total;
   // backward scratch
   size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
   RowArgs ra;
@@ -84,7 +84,7 @@ Layout layout_of(const rmx_config& c) {
   L.s2 = o; o = up(o + N * D * e);
   L.stats = o; o = up(o + 10 * N * sizeof(float));
   L.zstats = o; o = up(o + N * (size_t)zstats_tiles(c.H) * 4 * sizeof(float));  // forward scratch
-  L.mix0 = o; o = up(o + N * D * e);  // token_mix(norm0(x)), read again by norm1's backward
+  L.s1 = o; o = up(o + N * D * e);  // norm1's input token_mix(norm0(x)) + x, read by its backward
   L.saved_total = o;
 
   L.ra.B = c.B;
@@ -265,14 +265,23 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   void* hidden = at(saved, L.hidden);
   void* s2 = at(saved, L.s2);
   Stats S = stats_of(saved, L, N);
-  void* mix0 = at(saved, L.mix0);
-  {
-    Launch l("ln0_fwd_mixed", st);
-    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_MIXED_OUT, x, nullptr, p.gamma0, p.beta0, mix0, S.mu0, S.r0, st)));
-  }
-  {
-    Launch l("ln1_fwd", st);
-    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_SUM_IN, mix0, x, p.gamma1, p.beta1, out1, S.mu1, S.r1, st)));
+  void* s1 = at(saved, L.s1);
+  if (ln01_fwd_supported(L.ra)) {
+    Launch l("ln01_fwd", st);
+    RMX_TRY(l.done(launch_ln01_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, s1, out1, S.mu0, S.r0, S.mu1,
+                                   S.r1, st)));
+  } else {
+    // Samples too large to stage: norm0 writes its output token-mixed into
+    // the s1 buffer, norm1 adds x in place.
+    {
+      Launch l("ln0_fwd_mixed", st);
+      RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_MIXED_OUT, x, nullptr, p.gamma0, p.beta0, s1, S.mu0, S.r0, nullptr,
+                                   st)));
+    }
+    {
+      Launch l("ln1_fwd", st);
+      RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_SUM_IN, s1, x, p.gamma1, p.beta1, out1, S.mu1, S.r1, s1, st)));
+    }
   }
   float* zstats = reinterpret_cast<float*>(at(saved, L.zstats));
   {
@@ -296,7 +305,7 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   }
   {
     Launch l("ln2_fwd", st);
-    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_PLAIN, s2, nullptr, p.gamma2, p.beta2, y, S.mu2, S.r2, st)));
+    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_PLAIN, s2, nullptr, p.gamma2, p.beta2, y, S.mu2, S.r2, nullptr, st)));
   }
   return RMX_OK;
 }
@@ -316,7 +325,7 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   void* dout1 = at(ws, L.dout1);
   void* ds1 = at(ws, L.ds1);
   void* da0 = at(ws, L.da0);
-  const void* mix0 = at(saved, L.mix0);
+  const void* s1 = at(saved, L.s1);
   auto F = [&](size_t off) { return reinterpret_cast<float*>(at(ws, off)); };
 
   {
@@ -338,12 +347,12 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   }
   {
     Launch l("ln1_bwd_mixed", st);
-    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_MIXED_TOO, dout1, mix0, x, S.mu1, S.r1, p.gamma1, nullptr, ds1, da0,
+    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_MIXED_TOO, dout1, s1, S.mu1, S.r1, p.gamma1, nullptr, ds1, da0,
                                  F(L.pg1), F(L.pbe1), nullptr, st)));
   }
   {
     Launch l("ln0_bwd", st);
-    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_RESID, da0, x, nullptr, S.mu0, S.r0, p.gamma0, ds1, dx, nullptr,
+    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_RESID, da0, x, S.mu0, S.r0, p.gamma0, ds1, dx, nullptr,
                                  F(L.pg0), F(L.pb0), nullptr, st)));
   }
   // Weight gradients last: every SM is busy with one GEMM CTA, so there is

@@ -18,17 +18,26 @@ struct RowArgs {
 // LayerNorm forward, one row per warp.  Modes: plain; output written
 // token-mixed (column i*C+c of row j lands in row i, column j*C+c of the same
 // sample, C = D/T); input is the sum of two tensors.
+// LNF_SUM_IN rounds s + s_add to the storage type, normalises those values
+// and also writes them to s_out (which may be s itself).
 enum LnFwdMode { LNF_PLAIN = 0, LNF_MIXED_OUT = 1, LNF_SUM_IN = 2 };
 cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
-                          const void* be, void* y, float* mu, float* rs, cudaStream_t st);
+                          const void* be, void* y, float* mu, float* rs, void* s_out, cudaStream_t st);
+// norm0 -> token mix -> + x -> norm1 with one CTA per sample (the sample's
+// rows staged in shared memory): writes s1 (norm1's input, rounded to the
+// storage type), out1 and both row statistics.  Supported when the sample
+// fits in shared memory.
+bool ln01_fwd_supported(const RowArgs& a);
+cudaError_t launch_ln01_fwd(const RowArgs& a, const void* x, const void* gamma0, const void* beta0,
+                            const void* gamma1, const void* beta1, void* s1, void* out1, float* mu0, float* r0,
+                            float* mu1, float* r1, cudaStream_t st);
 // LayerNorm backward over CTAs (t, b-block) of up to nb_ln <= kLnBwdMaxRows
 // rows; per-CTA partial sums of dgamma and dbeta ([nbblk_ln*T][D]).  Modes:
-// LNB_BIAS also sums ds per token into pbias; LNB_MIXED_TOO reads s + s_add
-// and also writes token_mix(ds) to out_mixed; LNB_RESID adds resid to the
-// output.
+// LNB_BIAS also sums ds per token into pbias; LNB_MIXED_TOO also writes
+// token_mix(ds) to out_mixed; LNB_RESID adds resid to the output.
 constexpr int kLnBwdMaxRows = 64;
 enum LnBwdMode { LNB_BIAS = 0, LNB_MIXED_TOO = 1, LNB_RESID = 2 };
-cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s, const void* s_add,
+cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s,
                           const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
                           void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st);
 // Backward of norm2 (launch_ln_bwd in LNB_BIAS mode): ds2 plus partial sums

@@ -7,9 +7,8 @@
 //   out = rstd * (g - mg - xh * mgx)     (+ a residual gradient, by mode)
 //   dgamma += gin * xh, dbeta += gin     (column partial sums)
 // Modes (kernels.h): LNB_BIAS also sums out over the batch per token (the
-// bias gradient of the GEMM that feeds norm2); LNB_MIXED_TOO reads the row as
-// s + s_add and writes out both plainly and token-mixed; LNB_RESID adds a
-// residual gradient to out.
+// bias gradient of the GEMM that feeds norm2); LNB_MIXED_TOO writes out both
+// plainly and token-mixed; LNB_RESID adds a residual gradient to out.
 //
 // One CTA owns the rows b0 <= b < b1 of one token t.  Their input rows stream
 // into shared memory through an S-stage ring of bulk copies (one thread
@@ -79,8 +78,7 @@ __device__ __forceinline__ void store_mixed_row(T* sample_base, const float* v, 
 
 struct LnBwdArgs {
   const void* gin;     // [N, D] upstream gradient
-  const void* s;       // [N, D] LayerNorm input (LNB_MIXED_TOO: its first term)
-  const void* s_add;   // [N, D] LNB_MIXED_TOO: second term of the input
+  const void* s;       // [N, D] LayerNorm input
   const void* resid;   // [N, D] LNB_RESID: gradient added to the output
   const float* mu;     // [N] forward statistics
   const float* rs;
@@ -98,8 +96,8 @@ struct LnBwdArgs {
 __host__ __device__ inline size_t stats_bytes(int nb) { return ((size_t)nb * 8 + 15) & ~(size_t)15; }
 
 template <int MODE> struct LnRows {
-  // Row tensors staged per row: gin, s, then s_add or resid.
-  static constexpr int value = (MODE == LNB_MIXED_TOO || MODE == LNB_RESID) ? 3 : 2;
+  // Row tensors staged per row: gin, s, then resid.
+  static constexpr int value = MODE == LNB_RESID ? 3 : 2;
 };
 
 // Shared memory: stats [nb] float2 | red [2][2][32] float | stages x rows |
@@ -126,7 +124,7 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)S * row_bytes);
   __shared__ int abort_flag;
 
-  const T* third = reinterpret_cast<const T*>(MODE == LNB_MIXED_TOO ? a.s_add : a.resid);
+  const T* third = reinterpret_cast<const T*>(a.resid);
   auto issue = [&](int i, int s) {  // row i of this CTA into stage s
     const size_t r = (size_t)(b0 + i) * a.T + t;
     const uint32_t bar = smem_u32(&full[s]);
@@ -177,12 +175,6 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
       float gv[E], sv[E];
       load_vec(st + c0, gv);
       load_vec(st + D + c0, sv);
-      if (MODE == LNB_MIXED_TOO) {
-        float av[E];
-        load_vec(st + 2 * D + c0, av);
-#pragma unroll
-        for (int e = 0; e < E; ++e) sv[e] += av[e];
-      }
       if (MODE == LNB_RESID) load_vec(st + 2 * D + c0, rv);
 #pragma unroll
       for (int e = 0; e < E; ++e) {
@@ -292,15 +284,13 @@ cudaError_t launch_mode(const LnBwdArgs& a, int mode, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_ln_bwd(const RowArgs& ra, int mode, const void* gin, const void* s, const void* s_add,
-                          const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
-                          void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
+cudaError_t launch_ln_bwd(const RowArgs& ra, int mode, const void* gin, const void* s, const float* mu,
+                          const float* rs, const void* gamma, const void* resid, void* out, void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
   const int V = ra.dtype == 0 ? 4 : 8;
   if (ra.D % V || ra.D / V > 512 || ra.nb_ln < 1 || ra.nb_ln > kLnBwdMaxRows || ra.D % ra.T) return cudaErrorInvalidValue;
   LnBwdArgs a;
   a.gin = gin;
   a.s = s;
-  a.s_add = s_add;
   a.resid = resid;
   a.mu = mu;
   a.rs = rs;
@@ -325,7 +315,7 @@ cudaError_t launch_ln_bwd(const RowArgs& ra, int mode, const void* gin, const vo
 
 cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2, const float* r2,
                            const void* g2, void* ds2, float* pg2, float* pb2, float* pbo, cudaStream_t st) {
-  return launch_ln_bwd(a, LNB_BIAS, dy, s2, nullptr, mu2, r2, g2, nullptr, ds2, nullptr, pg2, pb2, pbo, st);
+  return launch_ln_bwd(a, LNB_BIAS, dy, s2, mu2, r2, g2, nullptr, ds2, nullptr, pg2, pb2, pbo, st);
 }
 
 }  // namespace rmx

@@ -83,7 +83,7 @@ template <typename T, int MODE, int MAXV>
 __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T* __restrict__ s_add,
                                                 const T* __restrict__ g, const T* __restrict__ be,
                                                 T* __restrict__ y, float* __restrict__ mu, float* __restrict__ rs,
-                                                int N, int Tn, int D, int C, float eps) {
+                                                T* __restrict__ s_out, int N, int Tn, int D, int C, float eps) {
   constexpr int V = VecN<T>::value;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
         load_vec(srow + vi * V, vf[q]);
         load_vec(s_add + (size_t)row * D + vi * V, a);
 #pragma unroll
-        for (int e = 0; e < V; ++e) vf[q][e] += a[e];
+        for (int e = 0; e < V; ++e) vf[q][e] = to_f(from_f<T>(vf[q][e] + a[e]));
       } else {
         raw[q] = *reinterpret_cast<const uint4*>(srow + vi * V);
       }
@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
       for (int e = 0; e < V; ++e) o[e] = (v[e] - mean) * rstd * gg[e] + bb[e];
       if (MODE == LNF_MIXED_OUT) store_mixed<T, V>(y + (size_t)b * Tn * D, o, j, vi * V, C, D);
       else store_vec(y + (size_t)row * D + vi * V, o);
+      if (SUM) store_vec(s_out + (size_t)row * D + vi * V, v);
     }
   }
   if (lane == 0) {
@@ -314,7 +315,7 @@ int max_dynamic_smem_bytes() {
 }
 
 cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
-                          const void* be, void* y, float* mu, float* rs, cudaStream_t st) {
+                          const void* be, void* y, float* mu, float* rs, void* s_out, cudaStream_t st) {
   const int N = a.B * a.T;
   const int nv = a.D / vec_elems(a.dtype);
   const int q = (nv + 31) / 32;
@@ -323,7 +324,7 @@ cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void*
 #define RMX_LNF(M, MAXV)                                                                                   \
   RMX_DISPATCH_T(a.dtype, {                                                                                \
     k_ln_fwd<T, M, MAXV><<<grid, 256, 0, st>>>((const T*)s, (const T*)s_add, (const T*)g, (const T*)be,     \
-                                               (T*)y, mu, rs, N, a.T, a.D, C, 1e-3f);                      \
+                                               (T*)y, mu, rs, (T*)s_out, N, a.T, a.D, C, 1e-3f);           \
   })
 #define RMX_LNF_Q(M)                          \
   if (q <= 1) RMX_LNF(M, 1);                  \

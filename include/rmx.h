@@ -86,8 +86,9 @@ typedef struct {
  * out1 [B,T,D], Z [B,T,2H], hidden [B,T,H], s2 = out1 + out2 [B,T,D] in the
  * storage dtype, then ten float32 row statistics (mean and 1/sqrt(var+eps) of
  * norm0, norm1, norm2, LN_x, LN_gate) of length B*T, then forward-only
- * scratch (per-tile partial statistics of Z), then token_mix(norm0(x))
- * [B,T,D] in the storage dtype.  Each segment starts on a 256-byte boundary.
+ * scratch (per-tile partial statistics of Z), then norm1's input
+ * s1 = token_mix(norm0(x)) + x [B,T,D] in the storage dtype.  Each segment
+ * starts on a 256-byte boundary.
  * Returns 0 for an invalid config. */
 size_t rmx_saved_bytes(const rmx_config* cfg);
 
