@@ -113,11 +113,14 @@ def load_peaks() -> tuple[dict, str]:
 
 
 def kernel_source_hash() -> str:
+    """Hash of every kernel source file: a profile taken on other sources is stale."""
     h = hashlib.sha256()
-    for rel in ("ffn_block_gb300/csrc/gemm_tc.cu", "ffn_block_gb300/csrc/common.cuh",
-                "ffn_block_gb300/csrc/rows.cu"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    csrc = os.path.join(ROOT, "ffn_block_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
