@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* 
 // halves.
 // =========================================================================
 template <typename T>
-__global__ void __launch_bounds__(256) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
+__global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
                                                   float* __restrict__ muU, float* __restrict__ rU,
                                                   float* __restrict__ muG, float* __restrict__ rG,
                                                   const T* __restrict__ wx, const T* __restrict__ bx,
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(256) k_gate_fwd(const T* __restrict__ Z, const
   const T* zr = Z + (size_t)r * 2 * H;
   T* hr = hidden + (size_t)r * H;
   const int nv = H / V;
-#pragma unroll 2
+#pragma unroll 1
   for (int v = lane; v < nv; v += 32) {
     const int h0 = v * V;
     float zu[V], zg[V], fwx[V], fbx[V], fwg[V], fbg[V], o[V];
