@@ -85,8 +85,10 @@ __device__ __forceinline__ void lds_f32(const float* p, float* v) {
 // Shared memory: stats [nb] float4 | red [2][4][32] float | weights [4][H]
 // float | stages x (dh row | Z row) | mbarriers.  Thread `tid` owns the
 // 16-byte vector of columns c0 = tid * E ... c0 + E - 1 of both halves.
-template <typename T>
-__global__ void __launch_bounds__(512, 1) k_gate_bwd(const GateBwdArgs a) {
+// WREG: the thread's weights stay in registers (one CTA per SM leaves room
+// for them when the CTA has at most 384 threads).
+template <typename T, bool WREG>
+__global__ void __launch_bounds__(WREG ? 384 : 512, 1) k_gate_bwd(const GateBwdArgs a) {
   constexpr int E = VecN<T>::value;
   extern __shared__ __align__(16) unsigned char smem[];
   const int H = a.H, S = a.stages;
@@ -144,6 +146,13 @@ __global__ void __launch_bounds__(512, 1) k_gate_bwd(const GateBwdArgs a) {
   float awx[E], abx[E], awg[E], abg[E], a1u[E], a1g[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) awx[e] = abx[e] = awg[e] = abg[e] = a1u[e] = a1g[e] = 0.f;
+  float rwx[WREG ? E : 1], rbx[WREG ? E : 1], rwg[WREG ? E : 1], rbg[WREG ? E : 1];
+  if (WREG && active) {
+    lds_f32<E>(wsm + c0, rwx);
+    lds_f32<E>(wsm + H + c0, rbx);
+    lds_f32<E>(wsm + 2 * H + c0, rwg);
+    lds_f32<E>(wsm + 3 * H + c0, rbg);
+  }
 
   const float invH = 1.0f / (float)H;
   T* dZrow = reinterpret_cast<T*>(a.dZ) + ((size_t)b0 * a.T + t) * 2 * H;
@@ -167,10 +176,20 @@ __global__ void __launch_bounds__(512, 1) k_gate_bwd(const GateBwdArgs a) {
       load_vec(st_dh + c0, dhv);
       load_vec(st_dh + H + c0, zu);
       load_vec(st_dh + 2 * H + c0, zg);
-      lds_f32<E>(wsm + c0, wx);
-      lds_f32<E>(wsm + H + c0, bx);
-      lds_f32<E>(wsm + 2 * H + c0, wg);
-      lds_f32<E>(wsm + 3 * H + c0, bg);
+      if (WREG) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          wx[e] = rwx[WREG ? e : 0];
+          bx[e] = rbx[WREG ? e : 0];
+          wg[e] = rwg[WREG ? e : 0];
+          bg[e] = rbg[WREG ? e : 0];
+        }
+      } else {
+        lds_f32<E>(wsm + c0, wx);
+        lds_f32<E>(wsm + H + c0, bx);
+        lds_f32<E>(wsm + 2 * H + c0, wg);
+        lds_f32<E>(wsm + 3 * H + c0, bg);
+      }
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const float Uh = fmaf(zu[e], sU, cU);
@@ -271,7 +290,7 @@ __global__ void __launch_bounds__(512, 1) k_gate_bwd(const GateBwdArgs a) {
   }
 }
 
-template <typename T>
+template <typename T, bool WREG>
 cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
   GateBwdArgs a = base;
   constexpr int E = VecN<T>::value;
@@ -283,7 +302,7 @@ cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
   if (room < 2) return cudaErrorInvalidValue;
   a.stages = (int)(room < kGateMaxStages ? room : kGateMaxStages);
   const size_t smem = fixed + (size_t)a.stages * row_bytes + (size_t)a.stages * 8;
-  auto k = k_gate_bwd<T>;
+  auto k = k_gate_bwd<T, WREG>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k<<<grid, threads, smem, st>>>(a);
@@ -328,9 +347,10 @@ cudaError_t launch_gate_bwd(const RowArgs& ra, const void* dh, const void* Z, co
   a.stages = 0;
   if (!a.err) return cudaErrorInvalidValue;
   const dim3 grid(ra.nbblk, ra.T);
-  if (ra.dtype == 0) return launch_typed<float>(a, st, grid);
-  if (ra.dtype == 1) return launch_typed<bf16>(a, st, grid);
-  return launch_typed<f16>(a, st, grid);
+  const bool wreg = ra.H / (ra.dtype == 0 ? 4 : 8) <= 384;
+  if (ra.dtype == 0) return wreg ? launch_typed<float, true>(a, st, grid) : launch_typed<float, false>(a, st, grid);
+  if (ra.dtype == 1) return wreg ? launch_typed<bf16, true>(a, st, grid) : launch_typed<bf16, false>(a, st, grid);
+  return wreg ? launch_typed<f16, true>(a, st, grid) : launch_typed<f16, false>(a, st, grid);
 }
 
 }  // namespace rmx
