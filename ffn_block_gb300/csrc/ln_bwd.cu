@@ -42,6 +42,27 @@ __device__ __forceinline__ float warp_sum2_transposed(float v0, float v1) {
   return k;
 }
 
+// Sums v[0..3] over a warp with six shuffles: on return lane l holds the sum
+// of component 2 * bit4(l) + bit3(l); lanes holding the same component hold
+// the same bits.
+__device__ __forceinline__ float warp_sum4_transposed(float v0, float v1, float v2, float v3) {
+  const int lane = threadIdx.x & 31;
+  const bool b4 = lane & 16, b3 = lane & 8;
+  float k0 = b4 ? v2 : v0;
+  float k1 = b4 ? v3 : v1;
+  const float s0 = b4 ? v0 : v2;
+  const float s1 = b4 ? v1 : v3;
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float k = b3 ? k1 : k0;
+  const float s = b3 ? k0 : k1;
+  k += __shfl_xor_sync(0xffffffffu, s, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
 // Token mix as an addressing rule: column d = i*C + c of row j of a sample
 // goes to row i, column j*C + c.  Writes the V values of columns d0 .. d0+V-1
 // of row j to their mixed places (pairs when C is even).
@@ -100,8 +121,9 @@ template <int MODE> struct LnRows {
   static constexpr int value = MODE == LNB_RESID ? 3 : 2;
 };
 
-// Shared memory: stats [nb] float2 | red [2][2][32] float | stages x rows |
-// mbarriers.
+// Shared memory: stats [nb] float2 | red [2][4][32] float | stages x rows |
+// mbarriers.  Two rows are taken per barrier: their four row sums are reduced
+// together, which halves the per-row reduction and barrier work.
 template <typename T, int MODE>
 __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
   constexpr int E = VecN<T>::value;
@@ -117,8 +139,8 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
   const bool active = c0 < D;
 
   float2* st_row = reinterpret_cast<float2*>(smem);                    // (rstd, -mean*rstd) per row
-  float* red = reinterpret_cast<float*>(smem + stats_bytes(a.nb));     // [2][2][32]
-  unsigned char* ring = reinterpret_cast<unsigned char*>(red + 2 * 2 * 32);
+  float* red = reinterpret_cast<float*>(smem + stats_bytes(a.nb));     // [2][4][32]
+  unsigned char* ring = reinterpret_cast<unsigned char*>(red + 2 * 4 * 32);
   const size_t tensor_bytes = (size_t)D * sizeof(T);
   const size_t row_bytes = NR * tensor_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)S * row_bytes);
@@ -163,71 +185,92 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
   bool aborted = false;
   int s = 0;
   uint32_t ph = 0;
-  for (int i = 0; i < nrows; ++i, out_row += row_step) {
-    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
-                                      (volatile int*)&abort_flag);
-    const float2 sr = st_row[i];
-    const float rstd = sr.x, cst = sr.y;
-    float g[E], xh[E], rv[E];
-    float r0 = 0.f, r1 = 0.f;
-    if (ok && active) {
-      const T* st = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
-      float gv[E], sv[E];
-      load_vec(st + c0, gv);
-      load_vec(st + D + c0, sv);
-      if (MODE == LNB_RESID) load_vec(st + 2 * D + c0, rv);
+  for (int i = 0; i < nrows; i += 2, out_row += 2 * row_step) {
+    const int nr = min(2, nrows - i);  // rows in this step
+    const int s1 = s + 1 == S ? 0 : s + 1;
+    const uint32_t ph1 = s + 1 == S ? ph ^ 1u : ph;
+    bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                (volatile int*)&abort_flag);
+    if (nr == 2)
+      ok = ok && mbar_wait_bounded(smem_u32(&full[s1]), ph1, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                   (volatile int*)&abort_flag);
+    float g[2][E], xh[2][E], rv[2][E];
+    float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+    float rstd[2];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        xh[e] = fmaf(sv[e], rstd, cst);
-        g[e] = gam[e] * gv[e];
-        r0 += g[e];
-        r1 = fmaf(g[e], xh[e], r1);
-        ag[e] = fmaf(gv[e], xh[e], ag[e]);
-        ab[e] += gv[e];
+    for (int r = 0; r < 2; ++r) {
+      const float2 sr = st_row[min(i + r, nrows - 1)];
+      rstd[r] = sr.x;
+      if (ok && active && r < nr) {
+        const T* st = reinterpret_cast<const T*>(ring + (size_t)(r == 0 ? s : s1) * row_bytes);
+        float gv[E], sv[E];
+        load_vec(st + c0, gv);
+        load_vec(st + D + c0, sv);
+        if (MODE == LNB_RESID) load_vec(st + 2 * D + c0, rv[r]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          xh[r][e] = fmaf(sv[e], sr.x, sr.y);
+          g[r][e] = gam[e] * gv[e];
+          rsum[2 * r] += g[r][e];
+          rsum[2 * r + 1] = fmaf(g[r][e], xh[r][e], rsum[2 * r + 1]);
+          ag[e] = fmaf(gv[e], xh[r][e], ag[e]);
+          ab[e] += gv[e];
+        }
       }
     }
-    float* rb = red + (i & 1) * 2 * 32;
+    float* rb = red + ((i >> 1) & 1) * 4 * 32;
     {
-      const float k = warp_sum2_transposed(r0, r1);
-      if ((lane & 15) == 0) rb[(lane >> 4) * 32 + warp] = k;
+      const float k = warp_sum4_transposed(rsum[0], rsum[1], rsum[2], rsum[3]);
+      if ((lane & 7) == 0) rb[(lane >> 3) * 32 + warp] = k;
     }
     if (__syncthreads_or(!ok)) {
       aborted = true;
       break;
     }
-    if (tid == 0 && issued < nrows) issue(issued++, s);
-    if (++s == S) {
-      s = 0;
-      ph ^= 1u;
+    if (tid == 0) {
+      if (issued < nrows) issue(issued++, s);
+      if (nr == 2 && issued < nrows) issue(issued++, s1);
     }
-    float mg, mgx;
+    for (int r = 0; r < nr; ++r) {
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    float m[4];
     {
-      // Lane l adds the partials of warp l & 15 (at most 16 warps) for sum
-      // l >> 4; the sixteen lanes of each sum then combine.
-      const int c = lane >> 4, w = lane & 15;
-      float v = w < nw ? rb[c * 32 + w] : 0.f;
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      // Lane l adds warps (l & 7) and (l & 7) + 8 (at most 16 warps) of sum
+      // l >> 3; the eight lanes of each sum then combine.
+      const int c = lane >> 3, w0 = lane & 7;
+      float v = (w0 < nw ? rb[c * 32 + w0] : 0.f) + (w0 + 8 < nw ? rb[c * 32 + w0 + 8] : 0.f);
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       v += __shfl_xor_sync(0xffffffffu, v, 1);
-      mg = __shfl_sync(0xffffffffu, v, 0) * invD;
-      mgx = __shfl_sync(0xffffffffu, v, 16) * invD;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m[k] = __shfl_sync(0xffffffffu, v, k * 8) * invD;
     }
     if (active) {
-      const float q0 = -rstd * mg;
-      float o[E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        o[e] = fmaf(rstd, fmaf(-mgx, xh[e], g[e]), q0);
-        if (MODE == LNB_BIAS) ao[e] += o[e];
-      }
-      if (MODE == LNB_MIXED_TOO)
-        store_mixed_row<T, E>(reinterpret_cast<T*>(a.out_mixed) + (size_t)(b0 + i) * a.T * D, o, t, c0, a.C, D);
-      if (MODE == LNB_RESID) {
+      for (int r = 0; r < 2; ++r) {
+        if (r < nr) {
+          const float mg = m[2 * r], mgx = m[2 * r + 1];
+          const float q0 = -rstd[r] * mg;
+          float o[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] += rv[e];
+          for (int e = 0; e < E; ++e) {
+            o[e] = fmaf(rstd[r], fmaf(-mgx, xh[r][e], g[r][e]), q0);
+            if (MODE == LNB_BIAS) ao[e] += o[e];
+          }
+          if (MODE == LNB_MIXED_TOO)
+            store_mixed_row<T, E>(reinterpret_cast<T*>(a.out_mixed) + (size_t)(b0 + i + r) * a.T * D, o, t, c0,
+                                  a.C, D);
+          if (MODE == LNB_RESID) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] += rv[r][e];
+          }
+          store_vec(out_row + r * row_step + c0, o);
+        }
       }
-      store_vec(out_row + c0, o);
     }
   }
 
@@ -260,7 +303,7 @@ cudaError_t launch_ring(const LnBwdArgs& base, cudaStream_t st) {
   LnBwdArgs a = base;
   constexpr int E = VecN<T>::value;
   const int threads = (a.D / E + 31) / 32 * 32;
-  const size_t fixed = stats_bytes(a.nb) + 2 * 2 * 32 * 4;
+  const size_t fixed = stats_bytes(a.nb) + 2 * 4 * 32 * 4;
   const size_t row_bytes = (size_t)LnRows<MODE>::value * a.D * sizeof(T);
   long long room = ((long long)kLnSmemTarget - (long long)fixed) / (long long)(row_bytes + 8);
   if (room < 2) room = 2;
