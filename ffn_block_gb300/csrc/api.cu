@@ -234,6 +234,30 @@ rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
   return l.done(e);
 }
 
+// Copy stream of rmx_step_host, one per device, created on first use; the
+// events are shared, so a call's enqueue sequence holds g_copy_mu.
+struct CopyStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t start = nullptr, dy_in = nullptr, fwd_done = nullptr, y_out = nullptr;
+};
+std::mutex g_copy_mu;
+
+CopyStream* copy_stream() {
+  static CopyStream cs[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  CopyStream& c = cs[dev];
+  if (!c.s) {
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    cudaEvent_t* ev[4] = {&c.start, &c.dy_in, &c.fwd_done, &c.y_out};
+    for (cudaEvent_t* e : ev)
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    c.s = s;
+  }
+  return &c;
+}
+
 inline char* at(void* base, size_t off) { return static_cast<char*>(base) + off; }
 inline const char* at(const void* base, size_t off) { return static_cast<const char*>(base) + off; }
 
@@ -455,18 +479,34 @@ rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host, const r
   if (!host->x || !host->dy || !host->y || !host->dx) return RMX_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)cfg->B * cfg->T * cfg->D * esize(cfg->dtype);
-  if (cfg->B > 0) {
-    RMX_TRY(check_ptr(dev->x));
-    RMX_TRY(check_ptr(dev->dy));
-    if (cudaMemcpyAsync(dev->x, host->x, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return RMX_ERR_CUDA;
-    if (cudaMemcpyAsync(dev->dy, host->dy, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return RMX_ERR_CUDA;
+  if (cfg->B == 0) {
+    RMX_TRY(rmx_forward(cfg, dev->x, params, saved, saved_bytes, dev->y, stream));
+    return rmx_backward(cfg, dev->x, dev->dy, saved, saved_bytes, params, dev->dx, grads, ws, ws_bytes, stream);
   }
+  RMX_TRY(check_ptr(dev->x));
+  RMX_TRY(check_ptr(dev->dy));
+  RMX_TRY(check_ptr(dev->y));
+  RMX_TRY(check_ptr(dev->dx));
+  // dy is not needed before the backward and y is final after the forward:
+  // both copies run on the library's copy stream, beside the compute, and
+  // everything is joined back to `stream` before the call's last copy.
+  std::lock_guard<std::mutex> lock(g_copy_mu);
+  CopyStream* cs = copy_stream();
+  if (!cs) return RMX_ERR_CUDA;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // The copy stream must not overwrite dev->dy while earlier work on `stream` may read it.
+  if (!ok(cudaEventRecord(cs->start, st)) || !ok(cudaStreamWaitEvent(cs->s, cs->start, 0))) return RMX_ERR_CUDA;
+  if (!ok(cudaMemcpyAsync(dev->x, host->x, bytes, cudaMemcpyHostToDevice, st))) return RMX_ERR_CUDA;
+  if (!ok(cudaMemcpyAsync(dev->dy, host->dy, bytes, cudaMemcpyHostToDevice, cs->s))) return RMX_ERR_CUDA;
+  if (!ok(cudaEventRecord(cs->dy_in, cs->s))) return RMX_ERR_CUDA;
   RMX_TRY(rmx_forward(cfg, dev->x, params, saved, saved_bytes, dev->y, stream));
+  if (!ok(cudaEventRecord(cs->fwd_done, st)) || !ok(cudaStreamWaitEvent(cs->s, cs->fwd_done, 0))) return RMX_ERR_CUDA;
+  if (!ok(cudaMemcpyAsync(host->y, dev->y, bytes, cudaMemcpyDeviceToHost, cs->s))) return RMX_ERR_CUDA;
+  if (!ok(cudaEventRecord(cs->y_out, cs->s))) return RMX_ERR_CUDA;
+  if (!ok(cudaStreamWaitEvent(st, cs->dy_in, 0))) return RMX_ERR_CUDA;
   RMX_TRY(rmx_backward(cfg, dev->x, dev->dy, saved, saved_bytes, params, dev->dx, grads, ws, ws_bytes, stream));
-  if (cfg->B > 0) {
-    if (cudaMemcpyAsync(host->y, dev->y, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return RMX_ERR_CUDA;
-    if (cudaMemcpyAsync(host->dx, dev->dx, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return RMX_ERR_CUDA;
-  }
+  if (!ok(cudaMemcpyAsync(host->dx, dev->dx, bytes, cudaMemcpyDeviceToHost, st))) return RMX_ERR_CUDA;
+  if (!ok(cudaStreamWaitEvent(st, cs->y_out, 0))) return RMX_ERR_CUDA;
   return RMX_OK;
 }
 
