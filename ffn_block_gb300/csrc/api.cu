@@ -238,7 +238,7 @@ rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
 // events are shared, so a call's enqueue sequence holds g_copy_mu.
 struct CopyStream {
   cudaStream_t s = nullptr;
-  cudaEvent_t start = nullptr, dy_in = nullptr, fwd_done = nullptr, y_out = nullptr;
+  cudaEvent_t start = nullptr, dy_in = nullptr, fwd_done = nullptr, dx_ready = nullptr, done = nullptr;
 };
 std::mutex g_copy_mu;
 
@@ -250,7 +250,7 @@ CopyStream* copy_stream() {
   if (!c.s) {
     cudaStream_t s = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    cudaEvent_t* ev[4] = {&c.start, &c.dy_in, &c.fwd_done, &c.y_out};
+    cudaEvent_t* ev[5] = {&c.start, &c.dy_in, &c.fwd_done, &c.dx_ready, &c.done};
     for (cudaEvent_t* e : ev)
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     c.s = s;
@@ -334,8 +334,10 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   return RMX_OK;
 }
 
+// dx_ready (may be null) is recorded on `st` as soon as dx is final.
 rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, const void* saved,
-                         const rmx_params& p, void* dx, const rmx_grads& g, void* ws, cudaStream_t st) {
+                         const rmx_params& p, void* dx, const rmx_grads& g, void* ws, cudaStream_t st,
+                         cudaEvent_t dx_ready) {
   const Layout L = layout_of(c);
   const size_t N = (size_t)c.B * c.T;
   const void* out1 = at(saved, L.out1);
@@ -379,6 +381,7 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_RESID, da0, x, S.mu0, S.r0, p.gamma0, ds1, dx, nullptr,
                                  F(L.pg0), F(L.pb0), nullptr, st)));
   }
+  if (dx_ready && cudaEventRecord(dx_ready, st) != cudaSuccess) return RMX_ERR_CUDA;
   // Weight gradients last: every SM is busy with one GEMM CTA, so there is
   // nothing for a second stream to overlap them with.
   {
@@ -421,6 +424,25 @@ rmx_status zero_grads(const rmx_config& c, const rmx_grads& g, cudaStream_t st) 
   return RMX_OK;
 }
 
+rmx_status backward_checked(const rmx_config* cfg, const void* x, const void* dy, const void* saved,
+                            size_t saved_bytes, const rmx_params* params, void* dx, const rmx_grads* grads,
+                            void* ws, size_t ws_bytes, rmx_stream stream, cudaEvent_t dx_ready) {
+  if (!config_ok(cfg)) return RMX_ERR_INVALID_ARG;
+  RMX_TRY(check_params(params));
+  RMX_TRY(check_grads(grads));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->B == 0) return zero_grads(*cfg, *grads, st);
+  RMX_TRY(check_ptr(x));
+  RMX_TRY(check_ptr(dy));
+  RMX_TRY(check_ptr(saved));
+  RMX_TRY(check_ptr(dx));
+  RMX_TRY(check_ptr(ws));
+  const Layout L = layout_of(*cfg);
+  if (saved_bytes < L.saved_total || ws_bytes < L.ws_total) return RMX_ERR_WORKSPACE;
+  RMX_TRY(kernels_support(*cfg));
+  return backward_impl(*cfg, x, dy, saved, *params, dx, *grads, ws, st, dx_ready);
+}
+
 }  // namespace
 }  // namespace rmx
 
@@ -453,23 +475,11 @@ rmx_status rmx_forward(const rmx_config* cfg, const void* x, const rmx_params* p
   return forward_impl(*cfg, x, *params, saved, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
+
 rmx_status rmx_backward(const rmx_config* cfg, const void* x, const void* dy, const void* saved,
                         size_t saved_bytes, const rmx_params* params, void* dx, const rmx_grads* grads,
                         void* ws, size_t ws_bytes, rmx_stream stream) {
-  if (!config_ok(cfg)) return RMX_ERR_INVALID_ARG;
-  RMX_TRY(check_params(params));
-  RMX_TRY(check_grads(grads));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cfg->B == 0) return zero_grads(*cfg, *grads, st);
-  RMX_TRY(check_ptr(x));
-  RMX_TRY(check_ptr(dy));
-  RMX_TRY(check_ptr(saved));
-  RMX_TRY(check_ptr(dx));
-  RMX_TRY(check_ptr(ws));
-  const Layout L = layout_of(*cfg);
-  if (saved_bytes < L.saved_total || ws_bytes < L.ws_total) return RMX_ERR_WORKSPACE;
-  RMX_TRY(kernels_support(*cfg));
-  return backward_impl(*cfg, x, dy, saved, *params, dx, *grads, ws, st);
+  return backward_checked(cfg, x, dy, saved, saved_bytes, params, dx, grads, ws, ws_bytes, stream, nullptr);
 }
 
 rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host, const rmx_device_io* dev,
@@ -487,9 +497,9 @@ rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host, const r
   RMX_TRY(check_ptr(dev->dy));
   RMX_TRY(check_ptr(dev->y));
   RMX_TRY(check_ptr(dev->dx));
-  // dy is not needed before the backward and y is final after the forward:
-  // both copies run on the library's copy stream, beside the compute, and
-  // everything is joined back to `stream` before the call's last copy.
+  // dy is not needed before the backward, y is final after the forward and
+  // dx before the weight gradients: those copies run on the library's copy
+  // stream, beside the compute, and are joined back to `stream` at the end.
   std::lock_guard<std::mutex> lock(g_copy_mu);
   CopyStream* cs = copy_stream();
   if (!cs) return RMX_ERR_CUDA;
@@ -502,11 +512,15 @@ rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host, const r
   RMX_TRY(rmx_forward(cfg, dev->x, params, saved, saved_bytes, dev->y, stream));
   if (!ok(cudaEventRecord(cs->fwd_done, st)) || !ok(cudaStreamWaitEvent(cs->s, cs->fwd_done, 0))) return RMX_ERR_CUDA;
   if (!ok(cudaMemcpyAsync(host->y, dev->y, bytes, cudaMemcpyDeviceToHost, cs->s))) return RMX_ERR_CUDA;
-  if (!ok(cudaEventRecord(cs->y_out, cs->s))) return RMX_ERR_CUDA;
   if (!ok(cudaStreamWaitEvent(st, cs->dy_in, 0))) return RMX_ERR_CUDA;
-  RMX_TRY(rmx_backward(cfg, dev->x, dev->dy, saved, saved_bytes, params, dev->dx, grads, ws, ws_bytes, stream));
-  if (!ok(cudaMemcpyAsync(host->dx, dev->dx, bytes, cudaMemcpyDeviceToHost, st))) return RMX_ERR_CUDA;
-  if (!ok(cudaStreamWaitEvent(st, cs->y_out, 0))) return RMX_ERR_CUDA;
+  // dx is final before the weight gradients are computed: its download runs
+  // beside them.
+  RMX_TRY(backward_checked(cfg, dev->x, dev->dy, saved, saved_bytes, params, dev->dx, grads, ws, ws_bytes, stream,
+                           cs->dx_ready));
+  if (!ok(cudaStreamWaitEvent(cs->s, cs->dx_ready, 0))) return RMX_ERR_CUDA;
+  if (!ok(cudaMemcpyAsync(host->dx, dev->dx, bytes, cudaMemcpyDeviceToHost, cs->s))) return RMX_ERR_CUDA;
+  if (!ok(cudaEventRecord(cs->done, cs->s))) return RMX_ERR_CUDA;
+  if (!ok(cudaStreamWaitEvent(st, cs->done, 0))) return RMX_ERR_CUDA;
   return RMX_OK;
 }
 
