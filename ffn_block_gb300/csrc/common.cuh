@@ -90,10 +90,19 @@ __device__ __forceinline__ void store_n(T* p, const float* v) {
   }
 }
 
-// Logistic function 1 / (1 + e^-g) from the fast exponential and division
-// intrinsics: a few ulp of error, far inside the block's tolerances; the
-// limits 0 and 1 come out exactly.
-__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+// Logistic function 1 / (1 + e^-g), with e^-g = 2^(-g * log2(e)) (change of
+// base) on the hardware's base-2 exponential and its reciprocal, both the
+// flush-to-zero approximations of the PTX ISA (ex2.approx.ftz,
+// rcp.approx.ftz): a few ulp of error, far inside the block's tolerances.
+// The limits come out exactly: e^-g flushes to 0 for large g (result 1) and
+// overflows to +inf for very negative g (result 0).
+__device__ __forceinline__ float sigmoid_fast(float g) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -kLog2e));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return r;
+}
 
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {

@@ -15,6 +15,17 @@
 // backward reads the stored s1, so norm1 is taken of exactly those values),
 // takes norm1's statistics of the row held in registers and writes s1 and
 // out1.  x is read from HBM once; nothing token-mixed is written.
+//
+// k_ln01_cluster splits a sample over a cluster of T/8 CTAs, each owning 8
+// output rows i0 <= i < i0 + 8.  Output row i needs, from every row j, the
+// columns i*C ... i*C + C - 1, so the CTA stages its own 8 rows plus that
+// column stripe (T pieces of 8*C elements) of all T rows; the stripe's bytes
+// belong to the other CTAs' own rows and mostly come from L2.  norm0 needs
+// whole rows, so each CTA takes the statistics of its own rows and stores
+// them into every CTA of the cluster (distributed shared memory); a cluster
+// barrier later every CTA has all T of them.  About 42 KB of shared memory per
+// CTA lets several clusters share an SM, so one sample's loads overlap
+// another's arithmetic.
 
 #include "common.cuh"
 #include "kernels.h"
@@ -185,6 +196,325 @@ __global__ void __launch_bounds__(512, 1) k_ln01_fwd(const Ln01Args a) {
   }
 }
 
+// ---------------------------------------------------------------- cluster form
+constexpr int kLn01Rows = 8;  // output rows per CTA (one warp each)
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cta_rank_in_cluster() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Stores (v0, v1) at the shared variable `addr` of CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_f2(uint32_t addr, uint32_t rank, float v0, float v1) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v0), "f"(v1) : "memory");
+}
+
+// N consecutive elements of T (N * sizeof(T) = 2, 4, 8 or 16 bytes, aligned
+// to that size) between shared memory and floats.
+template <typename T, int N>
+__device__ __forceinline__ void lds_elems(const unsigned char* p, float* v) {
+  constexpr int W = N * (int)sizeof(T);
+  if constexpr (W == 16) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    const T* e = reinterpret_cast<const T*>(&r);
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = to_f(e[k]);
+  } else if constexpr (W == 8) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    const T* e = reinterpret_cast<const T*>(&r);
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = to_f(e[k]);
+  } else if constexpr (W == 4) {
+    const uint32_t r = *reinterpret_cast<const uint32_t*>(p);
+    const T* e = reinterpret_cast<const T*>(&r);
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = to_f(e[k]);
+  } else {
+    static_assert(W == 2, "2, 4, 8 or 16 bytes");
+    v[0] = to_f(*reinterpret_cast<const T*>(p));
+  }
+}
+template <typename T, int N>
+__device__ __forceinline__ void sts_elems(unsigned char* p, const float* v) {
+  constexpr int W = N * (int)sizeof(T);
+  if constexpr (W == 16) {
+    uint4 r;
+    T* e = reinterpret_cast<T*>(&r);
+#pragma unroll
+    for (int k = 0; k < N; ++k) e[k] = from_f<T>(v[k]);
+    *reinterpret_cast<uint4*>(p) = r;
+  } else if constexpr (W == 8) {
+    uint2 r;
+    T* e = reinterpret_cast<T*>(&r);
+#pragma unroll
+    for (int k = 0; k < N; ++k) e[k] = from_f<T>(v[k]);
+    *reinterpret_cast<uint2*>(p) = r;
+  } else if constexpr (W == 4) {
+    uint32_t r;
+    T* e = reinterpret_cast<T*>(&r);
+#pragma unroll
+    for (int k = 0; k < N; ++k) e[k] = from_f<T>(v[k]);
+    *reinterpret_cast<uint32_t*>(p) = r;
+  } else {
+    static_assert(W == 2, "2, 4, 8 or 16 bytes");
+    *reinterpret_cast<T*>(p) = from_f<T>(v[0]);
+  }
+}
+
+struct Ln01ClusterGeom {
+  int cs;           // CTAs per sample (cluster size) = T / 8
+  int own_pitch;    // bytes between staged own rows (D * e)
+  int piece;        // bytes of one stripe piece (8 * C * e)
+  int stripe_pitch; // bytes between staged stripe pieces (piece padded, pitch / 16 odd)
+  size_t off_gb, off_own, off_stripe, off_bar, smem;
+};
+
+__host__ __device__ inline size_t round16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+__host__ __device__ inline Ln01ClusterGeom ln01_cluster_geom(int Tn, int D, int esize) {
+  Ln01ClusterGeom g;
+  const int C = D / Tn;
+  g.cs = Tn / kLn01Rows;
+  g.own_pitch = D * esize;
+  g.piece = kLn01Rows * C * esize;
+  // Lanes read the stripe at the same column of consecutive pieces: a pitch
+  // that is an odd number of 16-byte units spreads them over the banks.
+  g.stripe_pitch = (int)round16((size_t)g.piece);
+  if ((g.stripe_pitch / 16) % 2 == 0) g.stripe_pitch += 16;
+  g.off_gb = round16((size_t)Tn * 8);
+  g.off_own = g.off_gb + round16((size_t)kLn01Rows * C * 8);
+  g.off_stripe = g.off_own + (size_t)kLn01Rows * g.own_pitch;
+  g.off_bar = g.off_stripe + (size_t)Tn * g.stripe_pitch;
+  g.smem = g.off_bar + 16;
+  return g;
+}
+
+// One CTA: sample b, output rows i0 ... i0 + 7 (i0 = 8 * rank).  Shared
+// memory: st0 [T] float2 (norm0 mean, rstd of every row of the sample) |
+// gb0 [8*C] float2 (gamma0, beta0 of the stripe's columns) | own rows [8][D]
+// | stripe [T][8*C] | mbarrier.  NE elements per shared-memory access in the
+// gather (NE * e bytes divide C * e).
+template <typename T, int NE>
+__global__ void __launch_bounds__(32 * kLn01Rows) k_ln01_cluster(const Ln01Args a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int e = (int)sizeof(T);
+  constexpr int V = VecN<T>::value;
+  const int Tn = a.T, D = a.D, C = a.C;
+  const Ln01ClusterGeom geo = ln01_cluster_geom(Tn, D, e);
+  const int rank = (int)cta_rank_in_cluster();
+  const int b = blockIdx.x / geo.cs;
+  const int i0 = rank * kLn01Rows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float2* st0 = reinterpret_cast<float2*>(smem);
+  float2* gb0 = reinterpret_cast<float2*>(smem + geo.off_gb);
+  unsigned char* own = smem + geo.off_own;
+  unsigned char* stripe = smem + geo.off_stripe;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + geo.off_bar);
+  __shared__ int abort_flag;
+
+  // Every CTA of the cluster must be running before another stores into its
+  // shared memory: arrive now, wait just before the first such store.
+  cluster_arrive_relaxed();
+
+  const T* xb = reinterpret_cast<const T*>(a.x) + (size_t)b * Tn * D;
+  const uint32_t total = (uint32_t)(kLn01Rows * geo.own_pitch + Tn * geo.piece);
+  if (warp == 0) {
+    if (lane == 0) {
+      abort_flag = 0;
+      mbar_init(smem_u32(bar), 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(smem_u32(bar), total);
+    }
+    __syncwarp();
+    for (int k = lane; k < kLn01Rows + Tn; k += 32) {
+      if (k < kLn01Rows)
+        bulk_g2s(smem_u32(own + (size_t)k * geo.own_pitch), xb + (size_t)(i0 + k) * D, (uint32_t)geo.own_pitch,
+                 smem_u32(bar));
+      else
+        bulk_g2s(smem_u32(stripe + (size_t)(k - kLn01Rows) * geo.stripe_pitch),
+                 xb + (size_t)(k - kLn01Rows) * D + (size_t)i0 * C, (uint32_t)geo.piece, smem_u32(bar));
+    }
+  }
+  {
+    const T* g0 = reinterpret_cast<const T*>(a.gamma0);
+    const T* bt0 = reinterpret_cast<const T*>(a.beta0);
+    for (int k = tid; k < kLn01Rows * C; k += blockDim.x) {
+      const int col = i0 * C + k;
+      gb0[k] = make_float2(to_f(g0[col]), to_f(bt0[col]));
+    }
+  }
+  __syncthreads();
+  const bool ok = __syncthreads_and(
+      mbar_wait_bounded(smem_u32(bar), 0, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS, (volatile int*)&abort_flag));
+
+  // (1) norm0 statistics of the own rows, one warp per row, published to
+  // every CTA of the cluster.
+  cluster_wait_acquire();
+  const float invD = 1.0f / (float)D;
+  const int nv = D / V;
+  if (ok) {
+    const int il = warp;
+    const T* row = reinterpret_cast<const T*>(own + (size_t)il * geo.own_pitch);
+    float sum = 0.f;
+    for (int vi = lane; vi < nv; vi += 32) {
+      float v[V];
+      load_vec(row + vi * V, v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) sum += v[q];
+    }
+    const float mean = warp_sum(sum) * invD;
+    float ss = 0.f;
+    for (int vi = lane; vi < nv; vi += 32) {
+      float v[V];
+      load_vec(row + vi * V, v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) {
+        const float c = v[q] - mean;
+        ss = fmaf(c, c, ss);
+      }
+    }
+    const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + a.eps);
+    const size_t r = (size_t)b * Tn + i0 + il;
+    if (lane == 0) {
+      a.mu0[r] = mean;
+      a.r0[r] = rstd;
+    }
+    if (lane < geo.cs) st_cluster_f2(smem_u32(&st0[i0 + il]), (uint32_t)lane, mean, rstd);
+  }
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  if (!ok) {
+    if (tid == 0) {
+      // Give the copies in flight a bounded time to land before the CTA's
+      // shared memory goes away.
+      volatile int no_abort = 0;
+      mbar_wait_bounded(smem_u32(bar), 0, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS, &no_abort);
+    }
+    return;
+  }
+
+  // (2) output row i = i0 + il, one warp: lane j builds the C elements that
+  // come from row j, s1[i, j*C + c] = norm0(x)[j, i*C + c] + x[i, j*C + c],
+  // rounded to the storage type and written over x[i, j*C + c] in the own
+  // row; then norm1's statistics (two passes) and the 16-byte writes of s1
+  // and out1.
+  {
+    const int il = warp;
+    const int i = i0 + il;
+    unsigned char* orow = own + (size_t)il * geo.own_pitch;
+    const int nch = C / NE;
+    float sum = 0.f;
+    for (int j = lane; j < Tn; j += 32) {
+      const float2 sj = st0[j];
+      const unsigned char* sp = stripe + (size_t)j * geo.stripe_pitch + (size_t)il * C * e;
+      unsigned char* op = orow + (size_t)j * C * e;
+      const float2* gb = gb0 + il * C;
+      for (int ch = 0; ch < nch; ++ch) {
+        float xs[NE], xo[NE], sv[NE];
+        lds_elems<T, NE>(sp + ch * NE * e, xs);
+        lds_elems<T, NE>(op + ch * NE * e, xo);
+#pragma unroll
+        for (int q = 0; q < NE; ++q) {
+          const float2 w = gb[ch * NE + q];
+          const float a0 = fmaf((xs[q] - sj.x) * sj.y, w.x, w.y);
+          sv[q] = to_f(from_f<T>(a0 + xo[q]));
+          sum += sv[q];
+        }
+        sts_elems<T, NE>(op + ch * NE * e, sv);
+      }
+    }
+    const float mean = warp_sum(sum) * invD;
+    __syncwarp();
+    const T* srow = reinterpret_cast<const T*>(orow);
+    float ss = 0.f;
+    for (int vi = lane; vi < nv; vi += 32) {
+      float v[V];
+      load_vec(srow + vi * V, v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) {
+        const float c = v[q] - mean;
+        ss = fmaf(c, c, ss);
+      }
+    }
+    const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + a.eps);
+    const size_t r = (size_t)b * Tn + i;
+    if (lane == 0) {
+      a.mu1[r] = mean;
+      a.r1[r] = rstd;
+    }
+    const T* gm1 = reinterpret_cast<const T*>(a.gamma1);
+    const T* bt1 = reinterpret_cast<const T*>(a.beta1);
+    T* s1row = reinterpret_cast<T*>(a.s1) + r * D;
+    T* orow_out = reinterpret_cast<T*>(a.out1) + r * D;
+    for (int vi = lane; vi < nv; vi += 32) {
+      const int d0 = vi * V;
+      const uint4 raw = *reinterpret_cast<const uint4*>(srow + d0);
+      *reinterpret_cast<uint4*>(s1row + d0) = raw;
+      float v[V], gg[V], bb[V], o[V];
+      const T* el = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int q = 0; q < V; ++q) v[q] = to_f(el[q]);
+      load_vec(gm1 + d0, gg);
+      load_vec(bt1 + d0, bb);
+#pragma unroll
+      for (int q = 0; q < V; ++q) o[q] = fmaf((v[q] - mean) * rstd, gg[q], bb[q]);
+      store_vec(orow_out + d0, o);
+    }
+  }
+}
+
+template <typename T, int NE>
+cudaError_t launch_cluster_typed(const Ln01Args& a, cudaStream_t st) {
+  const Ln01ClusterGeom g = ln01_cluster_geom(a.T, a.D, (int)sizeof(T));
+  auto k = k_ln01_cluster<T, NE>;
+  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * g.cs), 1, 1);
+  cfg.blockDim = dim3(32 * kLn01Rows, 1, 1);
+  cfg.dynamicSmemBytes = g.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)g.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+// Widest access (2, 4, 8 or 16 bytes) that divides a C-element piece.
+template <typename T>
+cudaError_t launch_cluster(const Ln01Args& a, cudaStream_t st) {
+  const int pb = a.C * (int)sizeof(T);
+  if (pb % 16 == 0) return launch_cluster_typed<T, 16 / sizeof(T)>(a, st);
+  if (pb % 8 == 0) return launch_cluster_typed<T, 8 / sizeof(T)>(a, st);
+  if (pb % 4 == 0) return launch_cluster_typed<T, 4 / sizeof(T)>(a, st);
+  if constexpr (sizeof(T) == 2) return launch_cluster_typed<T, 1>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+bool ln01_cluster_supported(const RowArgs& ra) {
+  const int e = ra.dtype == 0 ? 4 : 2;
+  if (ra.T % kLn01Rows || ra.T / kLn01Rows > 8 || ra.D % ra.T) return false;
+  if ((ra.D * e) % 16) return false;
+  const Ln01ClusterGeom g = ln01_cluster_geom(ra.T, ra.D, e);
+  if ((long long)kLn01Rows * g.own_pitch + (long long)ra.T * g.piece >= (1ll << 20)) return false;
+  return (long long)g.smem <= (long long)max_dynamic_smem_bytes() - 1024;
+}
+
 size_t ln01_smem_bytes(int Tn, int D, int esize) {
   return (((size_t)Tn * 8 + 15) & ~(size_t)15) + (size_t)2 * D * 4 + (size_t)Tn * ((size_t)D * esize + 16) + 16;
 }
@@ -212,6 +542,7 @@ cudaError_t launch_v(const Ln01Args& a, int q, cudaStream_t st) {
 }  // namespace
 
 bool ln01_fwd_supported(const RowArgs& ra) {
+  if (ln01_cluster_supported(ra)) return true;
   const int e = ra.dtype == 0 ? 4 : 2, V = 16 / e;
   if (ra.D % V || ra.D % ra.T) return false;
   if ((ra.D / V + 31) / 32 > 10) return false;
@@ -242,6 +573,12 @@ cudaError_t launch_ln01_fwd(const RowArgs& ra, const void* x, const void* gamma0
   a.D = ra.D;
   a.C = ra.D / ra.T;
   a.eps = 1e-3f;
+  if (ra.B == 0) return cudaSuccess;
+  if (ln01_cluster_supported(ra)) {
+    if (ra.dtype == 0) return launch_cluster<float>(a, st);
+    if (ra.dtype == 1) return launch_cluster<bf16>(a, st);
+    return launch_cluster<f16>(a, st);
+  }
   const int V = ra.dtype == 0 ? 4 : 8;
   const int q = (ra.D / V + 31) / 32;
   if (ra.dtype == 0) return launch_v<float>(a, q, st);
