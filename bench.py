@@ -98,6 +98,8 @@ def row_bytes_per_launch(s) -> dict:
         "ln2_fwd": 2 * BTD,                         # s2 in, y out
         "ln2_bwd": 3 * BTD,                         # dy, s2 in, ds2 out
         "gate_bwd": BTH + 2 * BTH + 2 * BTH,        # dh, Z in, dZ out (single pass)
+        "ln1_bwd": 3 * BTD,                         # dout1, s1 in; ds1 out
+        "ln0_bwd_gather": 3 * BTD,                  # ds1, x in, dx out (the mix read from a stripe of ds1)
         "ln1_bwd_mixed": 4 * BTD,                   # dout1, s1 in; ds1 and token_mix(ds1) out
         "ln0_bwd": 4 * BTD,                         # token_mix(ds1), x, ds1 in, dx out
     }

@@ -59,7 +59,8 @@ struct Layout {
   // saved (filled by the forward)
   size_t out1, Z, hidden, s2, stats, zstats, s1, saved_total;
   // backward scratch
-  size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
+  size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, colsum_scratch,
+      colsum_scratch_floats, ws_total;
   RowArgs ra;
 };
 
@@ -72,6 +73,9 @@ bool config_ok(const rmx_config* c) {
   if (rows > (1ll << 30) || (long long)c->D > (1 << 20) || (long long)c->H > (1 << 20)) return false;
   return true;
 }
+
+constexpr int kColsumJobs = 12;
+void colsum_jobs(const Layout& L, const rmx_config& c, const rmx_grads* g, void* ws, ColsumJob* jobs);
 
 Layout layout_of(const rmx_config& c) {
   Layout L;
@@ -102,6 +106,7 @@ Layout layout_of(const rmx_config& c) {
   L.ra.nbblk_ln = c.B > 0 ? (c.B + nbl - 1) / nbl : 0;
   const size_t P = (size_t)L.ra.nbblk * c.T;     // gate-backward partial rows
   const size_t PL = (size_t)L.ra.nbblk_ln * c.T; // LayerNorm-backward partial rows
+  const size_t P0 = ln0_bwd_gather_supported(L.ra) ? (size_t)ln0_bwd_partial_rows(L.ra) : PL;  // norm0's
 
   o = 0;
   L.ds2 = o; o = up(o + N * D * e);
@@ -118,12 +123,36 @@ Layout layout_of(const rmx_config& c) {
   L.pwg = o; o = up(o + P * H * sizeof(float));
   L.pbg = o; o = up(o + P * H * sizeof(float));
   L.pb1 = o; o = up(o + P * 2 * H * sizeof(float));
-  L.pg0 = o; o = up(o + PL * D * sizeof(float));
-  L.pb0 = o; o = up(o + PL * D * sizeof(float));
+  L.pg0 = o; o = up(o + P0 * D * sizeof(float));
+  L.pb0 = o; o = up(o + P0 * D * sizeof(float));
   L.pg1 = o; o = up(o + PL * D * sizeof(float));
   L.pbe1 = o; o = up(o + PL * D * sizeof(float));
+  {
+    ColsumJob jobs[kColsumJobs];
+    colsum_jobs(L, c, nullptr, nullptr, jobs);
+    L.colsum_scratch_floats = colsums_scratch_floats(jobs, kColsumJobs);
+  }
+  L.colsum_scratch = o; o = up(o + L.colsum_scratch_floats * sizeof(float));
   L.ws_total = o;
   return L;
+}
+
+// The backward's column-sum jobs: every partial buffer of `ws` and the
+// gradient it reduces into (both null when only the sizes are wanted).
+void colsum_jobs(const Layout& L, const rmx_config& c, const rmx_grads* g, void* ws, ColsumJob* jobs) {
+  auto F = [&](size_t off) { return ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + off) : nullptr; };
+  const int P = L.ra.nbblk * c.T, Pb = L.ra.nbblk;
+  const int PL = L.ra.nbblk_ln * c.T, PLb = L.ra.nbblk_ln;
+  const int P0 = ln0_bwd_gather_supported(L.ra) ? ln0_bwd_partial_rows(L.ra) : PL;
+  const ColsumJob j[kColsumJobs] = {
+      {F(L.pg2), g ? g->gamma2 : nullptr, PL, c.D},  {F(L.pb2), g ? g->beta2 : nullptr, PL, c.D},
+      {F(L.pbo), g ? g->bout : nullptr, PLb, c.T * c.D}, {F(L.pwx), g ? g->lnx_w : nullptr, P, c.H},
+      {F(L.pbx), g ? g->lnx_b : nullptr, P, c.H},    {F(L.pwg), g ? g->lng_w : nullptr, P, c.H},
+      {F(L.pbg), g ? g->lng_b : nullptr, P, c.H},    {F(L.pb1), g ? g->b1 : nullptr, Pb, c.T * 2 * c.H},
+      {F(L.pg1), g ? g->gamma1 : nullptr, PL, c.D},  {F(L.pbe1), g ? g->beta1 : nullptr, PL, c.D},
+      {F(L.pg0), g ? g->gamma0 : nullptr, P0, c.D},  {F(L.pb0), g ? g->beta0 : nullptr, P0, c.D},
+  };
+  for (int k = 0; k < kColsumJobs; ++k) jobs[k] = j[k];
 }
 
 // What the kernels can do (beyond what makes a valid block).
@@ -371,15 +400,30 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
     RMX_TRY(run_gemm("gemm1_dgrad", d, st));
   }
-  {
-    Launch l("ln1_bwd_mixed", st);
-    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_MIXED_TOO, dout1, s1, S.mu1, S.r1, p.gamma1, nullptr, ds1, da0,
-                                 F(L.pg1), F(L.pbe1), nullptr, st)));
-  }
-  {
-    Launch l("ln0_bwd", st);
-    RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_RESID, da0, x, S.mu0, S.r0, p.gamma0, ds1, dx, nullptr,
-                                 F(L.pg0), F(L.pb0), nullptr, st)));
+  const bool gather0 = ln0_bwd_gather_supported(L.ra);
+  if (gather0) {
+    // norm1's backward writes ds1 alone; norm0's gathers its mixed-back
+    // input from ds1 directly.
+    {
+      Launch l("ln1_bwd", st);
+      RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_PLAIN, dout1, s1, S.mu1, S.r1, p.gamma1, nullptr, ds1, nullptr,
+                                   F(L.pg1), F(L.pbe1), nullptr, st)));
+    }
+    {
+      Launch l("ln0_bwd_gather", st);
+      RMX_TRY(l.done(launch_ln0_bwd_gather(L.ra, ds1, x, S.mu0, S.r0, p.gamma0, dx, F(L.pg0), F(L.pb0), st)));
+    }
+  } else {
+    {
+      Launch l("ln1_bwd_mixed", st);
+      RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_MIXED_TOO, dout1, s1, S.mu1, S.r1, p.gamma1, nullptr, ds1, da0,
+                                   F(L.pg1), F(L.pbe1), nullptr, st)));
+    }
+    {
+      Launch l("ln0_bwd", st);
+      RMX_TRY(l.done(launch_ln_bwd(L.ra, LNB_RESID, da0, x, S.mu0, S.r0, p.gamma0, ds1, dx, nullptr,
+                                   F(L.pg0), F(L.pb0), nullptr, st)));
+    }
   }
   if (dx_ready && cudaEventRecord(dx_ready, st) != cudaSuccess) return RMX_ERR_CUDA;
   // Weight gradients last: every SM is busy with one GEMM CTA, so there is
@@ -393,19 +437,19 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     RMX_TRY(run_gemm("gemm1_wgrad", d, st));
   }
   {
-    const int P = L.ra.nbblk * c.T, Pb = L.ra.nbblk;
-    const int PL = L.ra.nbblk_ln * c.T, PLb = L.ra.nbblk_ln;
-    ColsumJob jobs[12] = {
-        {F(L.pg2), g.gamma2, PL, c.D},         {F(L.pb2), g.beta2, PL, c.D},
-        {F(L.pbo), g.bout, PLb, c.T * c.D},     {F(L.pwx), g.lnx_w, P, c.H},
-        {F(L.pbx), g.lnx_b, P, c.H},           {F(L.pwg), g.lng_w, P, c.H},
-        {F(L.pbg), g.lng_b, P, c.H},           {F(L.pb1), g.b1, Pb, c.T * 2 * c.H},
-        {F(L.pg1), g.gamma1, PL, c.D},         {F(L.pbe1), g.beta1, PL, c.D},
-        {F(L.pg0), g.gamma0, PL, c.D},         {F(L.pb0), g.beta0, PL, c.D},
-    };
-    Launch l("colsums", st);
-    cudaError_t e = launch_colsums(jobs, 12, c.dtype, st);
-    RMX_TRY(l.done(e));
+    ColsumJob jobs[kColsumJobs];
+    colsum_jobs(L, c, &g, ws, jobs);
+    bool fin = false;
+    {
+      Launch l("colsums", st);
+      RMX_TRY(l.done(
+          launch_colsums(jobs, kColsumJobs, c.dtype, F(L.colsum_scratch), L.colsum_scratch_floats, st, &fin)));
+    }
+    if (fin) {
+      Launch l("colsums_final", st);
+      RMX_TRY(l.done(
+          launch_colsums_final(jobs, kColsumJobs, c.dtype, F(L.colsum_scratch), L.colsum_scratch_floats, st)));
+    }
   }
   return RMX_OK;
 }

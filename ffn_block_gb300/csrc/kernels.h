@@ -35,11 +35,24 @@ cudaError_t launch_ln01_fwd(const RowArgs& a, const void* x, const void* gamma0,
 // rows; per-CTA partial sums of dgamma and dbeta ([nbblk_ln*T][D]).  Modes:
 // LNB_BIAS also sums ds per token into pbias; LNB_MIXED_TOO also writes
 // token_mix(ds) to out_mixed; LNB_RESID adds resid to the output.
+// LNB_PLAIN writes only the gradient.
 constexpr int kLnBwdMaxRows = 64;
-enum LnBwdMode { LNB_BIAS = 0, LNB_MIXED_TOO = 1, LNB_RESID = 2 };
+enum LnBwdMode { LNB_BIAS = 0, LNB_MIXED_TOO = 1, LNB_RESID = 2, LNB_PLAIN = 3 };
 cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s,
                           const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
                           void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st);
+// Backward of norm0 from ds1 (the gradient at norm1's input) without a
+// token-mixed intermediate: dx = ds1 + LN0_backward(da0) with da0 = ds1 mixed
+// back, gathered from a column stripe of ds1 staged in shared memory.  A CTA
+// owns 8 rows of kLn0SamplesPerCta consecutive samples; partial sums of
+// dgamma0 and dbeta0 go to [ln0_bwd_partial_rows][D].  Supported when
+// T % 8 == 0 and a row is at most 160 16-byte vectors.
+constexpr int kLn0SamplesPerCta = 4;
+int ln0_bwd_partial_rows(const RowArgs& a);
+bool ln0_bwd_gather_supported(const RowArgs& a);
+cudaError_t launch_ln0_bwd_gather(const RowArgs& a, const void* ds1, const void* x, const float* mu0,
+                                  const float* r0, const void* gamma0, void* dx, float* pg0, float* pb0,
+                                  cudaStream_t st);
 // Backward of norm2 (launch_ln_bwd in LNB_BIAS mode): ds2 plus partial sums
 // for gamma2, beta2 and bout.
 cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, const float* mu2,
@@ -68,8 +81,18 @@ struct ColsumJob {
   void* out;
   int P, J;
 };
+// With scratch of at least colsums_scratch_floats(jobs) floats (and every J a
+// multiple of 4), jobs longer than 256 partial rows are summed in chunks of
+// 256 rows in parallel (launch_colsums sets *needs_final) and
+// launch_colsums_final, called with the same arguments, adds the chunks;
+// otherwise launch_colsums sums every column in one pass.  Both orders are
+// fixed.
 constexpr int kMaxColsumJobs = 12;
-cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStream_t st);
+size_t colsums_scratch_floats(const ColsumJob* jobs, int njobs);
+cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
+                           cudaStream_t st, bool* needs_final);
+cudaError_t launch_colsums_final(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
+                                 cudaStream_t st);
 
 // Largest thread count a row pass may use (one thread per 16-byte vector).
 constexpr int kRowThreadsMax = 512;

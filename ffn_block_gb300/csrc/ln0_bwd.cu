@@ -1,0 +1,373 @@
+// Backward of norm0 with the inverse token mix folded into its loads.
+//
+// Page "Subgraph-fusion-based Mega-kernel Generation", section "Exact
+// computation": s1 = token_mixer(norm0(x)) + x, so with ds1 the gradient at
+// s1 (norm1's backward), dx = ds1 + LN0_backward(da0), where da0 is ds1
+// mixed back (the mix swaps the two T axes of [T, T, C] and is its own
+// inverse): da0[j, i*C + c] = ds1[i, j*C + c].  LN0_backward is the usual
+// LayerNorm backward: with xh = (x - mean) * rstd, g = gamma0 * da0,
+//   out = rstd * (g - mean(g) - xh * mean(g * xh)),
+//   dgamma0 += da0 * xh, dbeta0 += da0 (column partial sums).
+//
+// CTA (q, sample group) owns rows j = 8q ... 8q + 7 of a few consecutive
+// samples.  Row j of da0 takes, from every row i of ds1, the C columns
+// j*C ... j*C + C - 1, so for its eight rows the CTA stages one column stripe
+// of ds1 (T pieces of 8*C elements, bulk copies) next to its own rows of ds1
+// and x.  Thread v owns the 16-byte vector of columns d = v*E ... v*E + E - 1
+// of all eight rows: it gathers da0[j, d] = stripe[i][(j - 8q)*C + c] with
+// d = i*C + c, takes the sixteen row sums of its columns, one block reduction
+// per sample gives their totals, and the column partials stay in registers
+// across the samples.  Nothing token-mixed goes through HBM.  Every wait is
+// bounded.
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmx {
+namespace {
+
+constexpr int kRowsPerCta = 8;
+// Threads per CTA at most (one per 16-byte vector of a row), chosen so that
+// three CTAs of that size share an SM with the registers a thread needs.
+constexpr int kLn0MaxThreads = 160;
+
+struct Ln0GatherArgs {
+  const void* ds1;     // [N, D] gradient at norm1's input
+  const void* x;       // [N, D] the block's input (norm0's input)
+  const float* mu;     // [N] norm0's row statistics from the forward
+  const float* rs;
+  const void* gamma;   // [D]
+  void* dx;            // [N, D]
+  float* pg;           // [P0, D] column partials of dgamma0, P0 = ceil(B/spc) * T/8
+  float* pb;           // [P0, D] column partials of dbeta0
+  unsigned int* err;
+  int B, T, D, C, spc;
+};
+
+struct Ln0Geom {
+  int piece;         // bytes of one stripe piece (8 * C * e)
+  int stripe_pitch;  // piece padded to an odd number of 16-byte units
+  int row_bytes;     // D * e
+  size_t off_ownd, off_ownx, off_red, off_means, off_st, off_bar, smem;
+};
+
+__host__ __device__ inline size_t r16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+__host__ __device__ inline Ln0Geom ln0_geom(int Tn, int D, int esize) {
+  Ln0Geom g;
+  const int C = D / Tn;
+  g.piece = kRowsPerCta * C * esize;
+  g.stripe_pitch = (int)r16((size_t)g.piece);
+  if ((g.stripe_pitch / 16) % 2 == 0) g.stripe_pitch += 16;
+  g.row_bytes = D * esize;
+  g.off_ownd = (size_t)Tn * g.stripe_pitch;
+  g.off_ownx = g.off_ownd + (size_t)kRowsPerCta * g.row_bytes;
+  g.off_red = g.off_ownx + (size_t)kRowsPerCta * g.row_bytes;
+  g.off_means = g.off_red + 16 * 32 * sizeof(float);
+  g.off_st = g.off_means + 16 * sizeof(float);
+  g.off_bar = g.off_st + 2 * kRowsPerCta * sizeof(float2);
+  g.smem = g.off_bar + 16;
+  return g;
+}
+
+// Sums v[0..15] over the 32 lanes of a warp with sixteen shuffles.  On
+// return lanes 2k and 2k + 1 hold the sum of component k (the same bits).
+__device__ __forceinline__ float warp_sum16_transposed(const float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+  float w8[8], w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float keep = b4 ? v[k + 8] : v[k];
+    const float send = b4 ? v[k] : v[k + 8];
+    w8[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float keep = b3 ? w8[k + 4] : w8[k];
+    const float send = b3 ? w8[k] : w8[k + 4];
+    w4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float keep = b2 ? w4[k + 2] : w4[k];
+    const float send = b2 ? w4[k] : w4[k + 2];
+    w2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  float w = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
+  w += __shfl_xor_sync(0xffffffffu, w, 1);
+  return w;
+}
+
+// Two elements of da0 from the stripe: one access at p0 when PAIRS (C even,
+// so a pair never straddles a piece and sits on a 2-element boundary), else
+// one at p0 and one at p1.
+template <typename T, bool PAIRS>
+__device__ __forceinline__ void lds_gather2(const unsigned char* p0, const unsigned char* p1, float* v) {
+  if (PAIRS) {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t r = *reinterpret_cast<const uint32_t*>(p0);
+      const T* e = reinterpret_cast<const T*>(&r);
+      v[0] = to_f(e[0]);
+      v[1] = to_f(e[1]);
+    } else {
+      const float2 r = *reinterpret_cast<const float2*>(p0);
+      v[0] = r.x;
+      v[1] = r.y;
+    }
+  } else {
+    v[0] = to_f(*reinterpret_cast<const T*>(p0));
+    v[1] = to_f(*reinterpret_cast<const T*>(p1));
+  }
+}
+
+// Shared memory: stripe [T][pitch] | own ds1 rows [8][D] | own x rows [8][D]
+// | red [16][32] float | means [16] float | row statistics [2][8] float2
+// (rstd, -mean * rstd; by sample parity) | two mbarriers (stripe, own rows).
+// Both passes gather da0 from the stripe, so the next sample's copies are
+// issued once the second pass is done.
+template <typename T, bool PAIRS>
+__global__ void __launch_bounds__(kLn0MaxThreads, 3) k_ln0_bwd_gather(const Ln0GatherArgs a) {
+  constexpr int E = VecN<T>::value;
+  constexpr int es = (int)sizeof(T);
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int Tn = a.T, D = a.D, C = a.C;
+  const Ln0Geom geo = ln0_geom(Tn, D, es);
+  const int j0 = blockIdx.x * kRowsPerCta;
+  const int bbeg = blockIdx.y * a.spc;
+  const int ns = min(a.B, bbeg + a.spc) - bbeg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int c0 = tid * E;
+  const bool active = c0 < D;
+
+  unsigned char* stripe = smem;
+  unsigned char* ownd = smem + geo.off_ownd;
+  unsigned char* ownx = smem + geo.off_ownx;
+  float* red = reinterpret_cast<float*>(smem + geo.off_red);
+  float* means = reinterpret_cast<float*>(smem + geo.off_means);
+  float2* rowst = reinterpret_cast<float2*>(smem + geo.off_st);
+  // Threads 0..7 stage the norm0 statistics of sample index si's rows.
+  auto load_stats = [&](int si) {
+    if (tid < kRowsPerCta) {
+      const size_t row = (size_t)(bbeg + si) * Tn + j0 + tid;
+      const float r = a.rs[row];
+      rowst[(si & 1) * kRowsPerCta + tid] = make_float2(r, -a.mu[row] * r);
+    }
+  };
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + geo.off_bar);  // [0] stripe, [1] own rows
+  __shared__ int abort_flag;
+
+  const T* ds1 = reinterpret_cast<const T*>(a.ds1);
+  const T* xg = reinterpret_cast<const T*>(a.x);
+  // Warp 0 issues a sample's copies: lane 0 arms the barrier, the lanes
+  // share the copies.
+  auto issue_stripe = [&](int b) {
+    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bar[0]), (uint32_t)(Tn * geo.piece));
+    __syncwarp();
+    for (int i = lane; i < Tn; i += 32)
+      bulk_g2s(smem_u32(stripe + (size_t)i * geo.stripe_pitch), ds1 + ((size_t)b * Tn + i) * D + (size_t)j0 * C,
+               (uint32_t)geo.piece, smem_u32(&bar[0]));
+  };
+  auto issue_own = [&](int b) {
+    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bar[1]), (uint32_t)(2 * kRowsPerCta * geo.row_bytes));
+    __syncwarp();
+    if (lane < 2 * kRowsPerCta) {
+      const int jl = lane & (kRowsPerCta - 1);
+      const T* src = (lane < kRowsPerCta ? ds1 : xg) + ((size_t)b * Tn + j0 + jl) * D;
+      unsigned char* dst = (lane < kRowsPerCta ? ownd : ownx) + (size_t)jl * geo.row_bytes;
+      bulk_g2s(smem_u32(dst), src, (uint32_t)geo.row_bytes, smem_u32(&bar[1]));
+    }
+  };
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar[0]), 1);
+    mbar_init(smem_u32(&bar[1]), 1);
+    fence_mbar_init();
+  }
+  if (ns > 0) load_stats(0);
+  __syncthreads();
+  if (warp == 0 && ns > 0) {
+    issue_stripe(bbeg);
+    issue_own(bbeg);
+  }
+
+  // Stripe byte offsets of the thread's columns (row 0 of the eight).
+  int soff[E];
+  float gam[E], pg[E], pb[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int d = min(c0 + e, D - 1);
+    const int i = d / C;
+    soff[e] = i * geo.stripe_pitch + (d - i * C) * es;
+    pg[e] = pb[e] = 0.f;
+  }
+  if (active) load_vec(reinterpret_cast<const T*>(a.gamma) + c0, gam);
+
+  const float invD = 1.0f / (float)D;
+  const size_t piece_row = (size_t)C * es;  // stripe bytes between consecutive own rows
+  int si = 0;
+  bool aborted = false;
+  for (; si < ns; ++si) {
+    const int b = bbeg + si;
+    const uint32_t ph = (uint32_t)(si & 1);
+    bool ok = mbar_wait_bounded(smem_u32(&bar[0]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                (volatile int*)&abort_flag);
+    ok = ok && mbar_wait_bounded(smem_u32(&bar[1]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                 (volatile int*)&abort_flag);
+    // Pass 1: gather da0, g = gamma0 * da0, the row sums and column partials.
+    float sums[16];
+#pragma unroll
+    for (int jl = 0; jl < kRowsPerCta; ++jl) {
+      const float2 rc = rowst[(si & 1) * kRowsPerCta + jl];
+      const float r = rc.x, cst = rc.y;
+      float s0 = 0.f, s1 = 0.f;
+      if (ok && active) {
+        float xv[E];
+        load_vec(reinterpret_cast<const T*>(ownx + (size_t)jl * geo.row_bytes) + c0, xv);
+        const unsigned char* sp = stripe + (size_t)jl * piece_row;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          float da[2];
+          lds_gather2<T, PAIRS>(sp + soff[e], sp + soff[e + 1], da);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float xh = fmaf(xv[e + k], r, cst);
+            const float gg = gam[e + k] * da[k];
+            s0 += gg;
+            s1 = fmaf(gg, xh, s1);
+            pg[e + k] = fmaf(da[k], xh, pg[e + k]);
+            pb[e + k] += da[k];
+          }
+        }
+      }
+      sums[2 * jl] = s0;
+      sums[2 * jl + 1] = s1;
+    }
+    {
+      const float k = warp_sum16_transposed(sums);
+      if ((lane & 1) == 0) red[(lane >> 1) * 32 + warp] = k;
+    }
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    if (tid < 16) {
+      float v = 0.f;
+      for (int w = 0; w < nw; ++w) v += red[tid * 32 + w];
+      means[tid] = v * invD;
+    }
+    __syncthreads();
+    // Pass 2: with xh = x * r + cst, out = r * (g - mg - xh * mgx)
+    //   = r * g + (-r * r * mgx) * x + (-r * mg - r * mgx * cst); dx = out + ds1.
+    if (active) {
+#pragma unroll
+      for (int jl = 0; jl < kRowsPerCta; ++jl) {
+        const size_t row = (size_t)b * Tn + j0 + jl;
+        const float2 rc = rowst[(si & 1) * kRowsPerCta + jl];
+        const float r = rc.x, cst = rc.y;
+        const float mg = means[2 * jl], mgx = means[2 * jl + 1];
+        const float A = -r * r * mgx, Bc = -r * mg - r * mgx * cst;
+        float xv[E], dv[E], o[E];
+        load_vec(reinterpret_cast<const T*>(ownx + (size_t)jl * geo.row_bytes) + c0, xv);
+        load_vec(reinterpret_cast<const T*>(ownd + (size_t)jl * geo.row_bytes) + c0, dv);
+        const unsigned char* sp = stripe + (size_t)jl * piece_row;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          float da[2];
+          lds_gather2<T, PAIRS>(sp + soff[e], sp + soff[e + 1], da);
+          o[e] = fmaf(r, gam[e] * da[0], fmaf(A, xv[e], Bc)) + dv[e];
+          o[e + 1] = fmaf(r, gam[e + 1] * da[1], fmaf(A, xv[e + 1], Bc)) + dv[e + 1];
+        }
+        store_vec(reinterpret_cast<T*>(a.dx) + row * D + c0, o);
+      }
+    }
+    // The next sample's statistics go to the other parity slot: its last
+    // reader was the previous sample's second pass, before the last barrier.
+    if (si + 1 < ns) load_stats(si + 1);
+    __syncthreads();
+    // Every thread is done with the stripe and the own rows: fetch the next
+    // sample's.
+    if (warp == 0 && si + 1 < ns) {
+      issue_stripe(b + 1);
+      issue_own(b + 1);
+    }
+  }
+
+  if (aborted) {
+    // Give this sample's copies (the only ones that can be in flight) a
+    // bounded time to land before the CTA's shared memory goes away.
+    if (tid == 0) {
+      volatile int no_abort = 0;
+      const uint32_t ph = (uint32_t)(si & 1);
+      mbar_wait_bounded(smem_u32(&bar[0]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS, &no_abort);
+      mbar_wait_bounded(smem_u32(&bar[1]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS, &no_abort);
+    }
+    return;
+  }
+  if (active) {
+    const size_t p = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+#pragma unroll
+    for (int k = 0; k < E; k += 4) {
+      *reinterpret_cast<float4*>(a.pg + p * D + c0 + k) = make_float4(pg[k], pg[k + 1], pg[k + 2], pg[k + 3]);
+      *reinterpret_cast<float4*>(a.pb + p * D + c0 + k) = make_float4(pb[k], pb[k + 1], pb[k + 2], pb[k + 3]);
+    }
+  }
+}
+
+template <typename T, bool PAIRS>
+cudaError_t launch_typed(const Ln0GatherArgs& a, cudaStream_t st) {
+  constexpr int E = VecN<T>::value;
+  const Ln0Geom g = ln0_geom(a.T, a.D, (int)sizeof(T));
+  auto k = k_ln0_bwd_gather<T, PAIRS>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+  if (e != cudaSuccess) return e;
+  const int threads = (a.D / E + 31) / 32 * 32;
+  const dim3 grid(a.T / kRowsPerCta, (a.B + a.spc - 1) / a.spc);
+  k<<<grid, threads, g.smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int ln0_bwd_partial_rows(const RowArgs& ra) {
+  return ra.B > 0 ? (ra.B + kLn0SamplesPerCta - 1) / kLn0SamplesPerCta * (ra.T / kRowsPerCta) : 0;
+}
+
+bool ln0_bwd_gather_supported(const RowArgs& ra) {
+  const int e = ra.dtype == 0 ? 4 : 2, V = 16 / e;
+  if (ra.T % kRowsPerCta || ra.D % ra.T || ra.D % V) return false;
+  if ((ra.D / V + 31) / 32 * 32 > kLn0MaxThreads) return false;
+  if ((long long)2 * kRowsPerCta * ra.D * e >= (1ll << 20)) return false;  // one mbarrier counts the own rows
+  const Ln0Geom g = ln0_geom(ra.T, ra.D, e);
+  return (long long)g.smem <= (long long)max_dynamic_smem_bytes() - 1024;
+}
+
+cudaError_t launch_ln0_bwd_gather(const RowArgs& ra, const void* ds1, const void* x, const float* mu0,
+                                  const float* r0, const void* gamma0, void* dx, float* pg0, float* pb0,
+                                  cudaStream_t st) {
+  if (!ln0_bwd_gather_supported(ra)) return cudaErrorInvalidValue;
+  if (ra.B == 0) return cudaSuccess;
+  Ln0GatherArgs a;
+  a.ds1 = ds1;
+  a.x = x;
+  a.mu = mu0;
+  a.rs = r0;
+  a.gamma = gamma0;
+  a.dx = dx;
+  a.pg = pg0;
+  a.pb = pb0;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidValue;
+  a.B = ra.B;
+  a.T = ra.T;
+  a.D = ra.D;
+  a.C = ra.D / ra.T;
+  a.spc = kLn0SamplesPerCta;
+  const bool pairs = a.C % 2 == 0;
+  if (ra.dtype == 0) return pairs ? launch_typed<float, true>(a, st) : launch_typed<float, false>(a, st);
+  if (ra.dtype == 1) return pairs ? launch_typed<bf16, true>(a, st) : launch_typed<bf16, false>(a, st);
+  return pairs ? launch_typed<f16, true>(a, st) : launch_typed<f16, false>(a, st);
+}
+
+}  // namespace rmx

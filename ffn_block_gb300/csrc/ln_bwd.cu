@@ -8,7 +8,8 @@
 //   dgamma += gin * xh, dbeta += gin     (column partial sums)
 // Modes (kernels.h): LNB_BIAS also sums out over the batch per token (the
 // bias gradient of the GEMM that feeds norm2); LNB_MIXED_TOO writes out both
-// plainly and token-mixed; LNB_RESID adds a residual gradient to out.
+// plainly and token-mixed; LNB_RESID adds a residual gradient to out;
+// LNB_PLAIN writes out alone.
 //
 // One CTA owns the rows b0 <= b < b1 of one token t.  Their input rows stream
 // into shared memory through an S-stage ring of bulk copies (one thread
@@ -322,6 +323,7 @@ template <typename T>
 cudaError_t launch_mode(const LnBwdArgs& a, int mode, cudaStream_t st) {
   if (mode == LNB_BIAS) return launch_ring<T, LNB_BIAS>(a, st);
   if (mode == LNB_MIXED_TOO) return launch_ring<T, LNB_MIXED_TOO>(a, st);
+  if (mode == LNB_PLAIN) return launch_ring<T, LNB_PLAIN>(a, st);
   return launch_ring<T, LNB_RESID>(a, st);
 }
 

@@ -274,21 +274,103 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
 }
 
 // =========================================================================
-// R: column sums of partials, several jobs in one launch.  Block (32, 16):
-// x picks the column, y a stripe of partial rows p = y, y+16, ...; stripes
-// are combined in a fixed order.
+// R: column sums of partials, several jobs per launch, fixed summation order.
+//
+// Chunked form (when the caller provides scratch): a block of 256 threads
+// takes 128 columns (a float4 per lane) of one chunk of at most 256 partial
+// rows; warp w sums rows w, w+8, ... of the chunk with four loads in flight,
+// and the eight warps are combined in order.  A job with one chunk is written
+// out at once; for longer jobs each chunk's sums go to scratch and a second
+// small launch adds the chunks in order.  One-pass form (no scratch): block
+// (32, 16), x the column, y a stripe of rows p = y, y+16, ..., stripes
+// combined in order.
 // =========================================================================
+constexpr int kColsumChunkRows = 256;
+constexpr int kColsumCols = 128;  // columns per block (32 lanes x float4)
+
 struct ColsumArgs {
   ColsumJob job[kMaxColsumJobs];
+  float* chunk_out[kMaxColsumJobs];  // [nchunks][J] when nchunks > 1
+  int nchunks[kMaxColsumJobs];
+  int ncg[kMaxColsumJobs];           // column groups of kColsumCols
   int block_start[kMaxColsumJobs + 1];
   int njobs;
 };
 
-template <typename T>
-__global__ void __launch_bounds__(512) k_colsums(const ColsumArgs a) {
-  __shared__ float part[16][33];
+__device__ __forceinline__ int colsum_job_of(const ColsumArgs& a) {
   int jb = 0;
   while (jb + 1 < a.njobs && (int)blockIdx.x >= a.block_start[jb + 1]) ++jb;
+  return jb;
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(void* out, int j, float4 v) {
+  T* o = reinterpret_cast<T*>(out) + j;
+  o[0] = from_f<T>(v.x);
+  o[1] = from_f<T>(v.y);
+  o[2] = from_f<T>(v.z);
+  o[3] = from_f<T>(v.w);
+}
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_colsums_chunks(const ColsumArgs a) {
+  __shared__ float4 part[8][32];
+  const int jb = colsum_job_of(a);
+  const ColsumJob& job = a.job[jb];
+  const int local = blockIdx.x - a.block_start[jb];
+  const int ch = local / a.ncg[jb], cg = local - ch * a.ncg[jb];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j = cg * kColsumCols + lane * 4;
+  const int p0 = ch * kColsumChunkRows, p1 = min(job.P, p0 + kColsumChunkRows);
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (j < job.J) {
+    const float* col = job.part + j;
+    const size_t J = (size_t)job.J;
+    int p = p0 + warp;
+    for (; p + 24 < p1; p += 32) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] = add4(acc[k], *reinterpret_cast<const float4*>(col + (size_t)(p + 8 * k) * J));
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      if (p + 8 * k < p1) acc[k] = add4(acc[k], *reinterpret_cast<const float4*>(col + (size_t)(p + 8 * k) * J));
+  }
+  part[warp][lane] = add4(add4(acc[0], acc[1]), add4(acc[2], acc[3]));
+  __syncthreads();
+  if (warp == 0 && j < job.J) {
+    float4 tot = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) tot = add4(tot, part[w][lane]);
+    if (a.nchunks[jb] == 1)
+      store4<T>(job.out, j, tot);
+    else
+      *reinterpret_cast<float4*>(a.chunk_out[jb] + (size_t)ch * job.J + j) = tot;
+  }
+}
+
+// Adds the chunk sums of the jobs with more than one chunk, in chunk order.
+template <typename T>
+__global__ void __launch_bounds__(128) k_colsums_final(const ColsumArgs a) {
+  const int jb = colsum_job_of(a);
+  const ColsumJob& job = a.job[jb];
+  const int j = ((int)blockIdx.x - a.block_start[jb]) * 512 + threadIdx.x * 4;
+  if (j >= job.J) return;
+  float4 tot = *reinterpret_cast<const float4*>(a.chunk_out[jb] + j);
+  for (int ch = 1; ch < a.nchunks[jb]; ++ch)
+    tot = add4(tot, *reinterpret_cast<const float4*>(a.chunk_out[jb] + (size_t)ch * job.J + j));
+  store4<T>(job.out, j, tot);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) k_colsums_onepass(const ColsumArgs a) {
+  __shared__ float part[16][33];
+  const int jb = colsum_job_of(a);
   const ColsumJob& job = a.job[jb];
   const int j = (blockIdx.x - a.block_start[jb]) * 32 + threadIdx.x;
   float s = 0.f;
@@ -361,19 +443,71 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats
   return cudaGetLastError();
 }
 
-cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStream_t st) {
-  if (njobs <= 0 || njobs > kMaxColsumJobs) return cudaErrorInvalidValue;
-  ColsumArgs a;
+size_t colsums_scratch_floats(const ColsumJob* jobs, int njobs) {
+  size_t n = 0;
+  for (int i = 0; i < njobs; ++i) {
+    const int nch = (jobs[i].P + kColsumChunkRows - 1) / kColsumChunkRows;
+    if (nch > 1) n += (size_t)nch * jobs[i].J;
+  }
+  return n;
+}
+
+namespace {
+// Fills the launch arguments; returns false for the one-pass form.
+bool colsum_plan(const ColsumJob* jobs, int njobs, float* scratch, size_t scratch_floats, ColsumArgs& a) {
   a.njobs = njobs;
+  bool chunked = scratch != nullptr && colsums_scratch_floats(jobs, njobs) <= scratch_floats;
+  for (int i = 0; i < njobs; ++i) chunked = chunked && jobs[i].J % 4 == 0 && jobs[i].P > 0;
   int blocks = 0;
+  float* next = scratch;
   for (int i = 0; i < njobs; ++i) {
     a.job[i] = jobs[i];
+    a.ncg[i] = (jobs[i].J + kColsumCols - 1) / kColsumCols;
+    a.nchunks[i] = chunked ? (jobs[i].P + kColsumChunkRows - 1) / kColsumChunkRows : 1;
+    a.chunk_out[i] = nullptr;
+    if (a.nchunks[i] > 1) {
+      a.chunk_out[i] = next;
+      next += (size_t)a.nchunks[i] * jobs[i].J;
+    }
     a.block_start[i] = blocks;
-    blocks += (jobs[i].J + 31) / 32;
+    blocks += chunked ? a.ncg[i] * a.nchunks[i] : (jobs[i].J + 31) / 32;
   }
   a.block_start[njobs] = blocks;
+  return chunked;
+}
+}  // namespace
+
+cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
+                           cudaStream_t st, bool* needs_final) {
+  if (needs_final) *needs_final = false;
+  if (njobs <= 0 || njobs > kMaxColsumJobs) return cudaErrorInvalidValue;
+  ColsumArgs a;
+  const bool chunked = colsum_plan(jobs, njobs, scratch, scratch_floats, a);
+  const int blocks = a.block_start[njobs];
   if (blocks == 0) return cudaSuccess;
-  RMX_DISPATCH_T(dtype, { k_colsums<T><<<blocks, dim3(32, 16), 0, st>>>(a); });
+  if (!chunked) {
+    RMX_DISPATCH_T(dtype, { k_colsums_onepass<T><<<blocks, dim3(32, 16), 0, st>>>(a); });
+    return cudaGetLastError();
+  }
+  RMX_DISPATCH_T(dtype, { k_colsums_chunks<T><<<blocks, 256, 0, st>>>(a); });
+  if (needs_final)
+    for (int i = 0; i < njobs; ++i) *needs_final = *needs_final || a.nchunks[i] > 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsums_final(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
+                                 cudaStream_t st) {
+  if (njobs <= 0 || njobs > kMaxColsumJobs) return cudaErrorInvalidValue;
+  ColsumArgs a;
+  if (!colsum_plan(jobs, njobs, scratch, scratch_floats, a)) return cudaErrorInvalidValue;
+  int fb = 0;
+  for (int i = 0; i < njobs; ++i) {
+    a.block_start[i] = fb;
+    if (a.nchunks[i] > 1) fb += (jobs[i].J + 511) / 512;
+  }
+  a.block_start[njobs] = fb;
+  if (fb == 0) return cudaErrorInvalidValue;
+  RMX_DISPATCH_T(dtype, { k_colsums_final<T><<<fb, 128, 0, st>>>(a); });
   return cudaGetLastError();
 }
 

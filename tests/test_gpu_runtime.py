@@ -120,6 +120,6 @@ def test_profiler_counts_every_launch():
     prof = B.rmx_profile_read()
     launched = B.rmx_launch_count() - before
     assert sum(n for n, _ in prof.values()) == launched
-    assert {"gemm1_fwd", "gemm2_fwd", "gemm1_wgrad", "gemm2_dgrad", "ln01_fwd", "ln1_bwd_mixed", "gate_bwd",
-            "ln0_bwd"} <= set(prof)
+    assert {"gemm1_fwd", "gemm2_fwd", "gemm1_wgrad", "gemm2_dgrad", "ln01_fwd", "ln1_bwd", "gate_bwd",
+            "ln0_bwd_gather"} <= set(prof)
     assert all(ms >= 0.0 for _, ms in prof.values())
