@@ -349,13 +349,27 @@ def run_ours(args) -> dict | None:
     torch.cuda.synchronize()
     B.check(B.rmx_check(stream), "warm-up")
 
+    # Per-kernel breakdown from a separate pass (every launch bracketed by
+    # events): it names the dominant kernel.  The timed region below brackets
+    # only that kernel's launches, so the step runs as it does unprofiled.
+    B.rmx_profile_read()
+    B.rmx_profile_select(None)
+    B.rmx_profile_enable(True)
+    for _ in range(max(1, min(args.steps, 3))):
+        flush.zero_()
+        blk.step(stream)
+    torch.cuda.synchronize()
+    B.rmx_profile_enable(False)
+    breakdown = B.rmx_profile_read()
+    dom = max(breakdown, key=lambda k: breakdown[k][1]) if breakdown else None
+
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(gpu_selector(torch.cuda.current_device()))
     sampler.start()
     time.sleep(0.3)
-    B.rmx_profile_read()
     launches0 = B.rmx_launch_count()
+    B.rmx_profile_select(dom)
     B.rmx_profile_enable(True)
     barrier(ws)
     torch.cuda.synchronize()
@@ -369,10 +383,11 @@ def run_ours(args) -> dict | None:
     barrier(ws)
     wall = time.perf_counter() - wall0
     B.rmx_profile_enable(False)
+    B.rmx_profile_select(None)
     launches = B.rmx_launch_count() - launches0
     clocks = sampler.stop()
     B.check(B.rmx_check(stream), "timed region")
-    prof = B.rmx_profile_read()
+    live = B.rmx_profile_read()  # the dominant kernel, timed inside the timed region
     samples = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = float(np.mean(samples))
     ms_max = reduce_max(ms, ws)
@@ -417,16 +432,18 @@ def run_ours(args) -> dict | None:
 
     # ---- roofline of the dominant kernel and of the whole step
     peaks, peak_src = load_peaks()
-    kernels = {k: {"launches": n, "ms_total": t, "ms_per_launch": t / max(n, 1)} for k, (n, t) in prof.items()}
+    kernels = {k: {"launches": n, "ms_total": t, "ms_per_launch": t / max(n, 1)} for k, (n, t) in breakdown.items()}
     total_ms = sum(v["ms_total"] for v in kernels.values()) or 1.0
     for v in kernels.values():
         v["share"] = v["ms_total"] / total_ms
-    dom = max(kernels, key=lambda k: kernels[k]["ms_total"]) if kernels else None
+    if dom is not None and dom in live:
+        n_live, t_live = live[dom]
+        kernels[dom]["ms_per_launch_timed_region"] = t_live / max(n_live, 1)
     gflops, rbytes = gemm_flops_per_launch(shape), row_bytes_per_launch(shape)
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     roofline = None
     if dom is not None:
-        per = kernels[dom]["ms_per_launch"] / 1e3
+        per = kernels[dom].get("ms_per_launch_timed_region", kernels[dom]["ms_per_launch"]) / 1e3
         if dom in gflops:
             ach = gflops[dom] / per / 1e12
             peak = sustained if shape.dtype != "f32" else None
@@ -471,6 +488,8 @@ def run_ours(args) -> dict | None:
         "wall_s": wall,
         "samples_ms": samples,
         "kernels": kernels,
+        "kernels_note": "per-kernel times from a separate pass with every launch bracketed by events; "
+                        "the timed region brackets only the dominant kernel (ms_per_launch_timed_region)",
     }
     return line
 

@@ -73,6 +73,7 @@ _SIGNATURES = {
     "rmx_version": (_I, []),
     "rmx_launch_count": (ctypes.c_longlong, []),
     "rmx_profile_enable": (_I, [_I]),
+    "rmx_profile_select": (_I, [ctypes.c_char_p]),
     "rmx_profile_read": (_I, [_P(ctypes.c_char_p), _P(ctypes.c_longlong), _P(ctypes.c_double), _I]),
     "rmx_test_bounded_wait": (_I, [_I, _VP]),
     "rmx_test_gemm": (_I, [_I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP]),
@@ -185,6 +186,10 @@ def rmx_launch_count() -> int:
 
 def rmx_profile_enable(on: bool) -> int:
     return lib().rmx_profile_enable(1 if on else 0)
+
+
+def rmx_profile_select(name) -> int:
+    return lib().rmx_profile_select(name.encode() if name else None)
 
 
 def rmx_profile_read(cap: int = 64) -> dict:

@@ -75,6 +75,27 @@ bool config_ok(const rmx_config* c) {
 }
 
 constexpr int kColsumJobs = 12;
+
+// Rows per CTA (at most max_rows) for a grid of T x ceil(B / nb) CTAs of
+// which `slots` are resident at once: the one with the shortest estimated
+// run, (waves, rounded up) x nb; among equals the largest nb (fewer CTAs and
+// partial rows).  A grid that is a whole number of waves wastes no tail.
+int rows_per_cta(int B, int T, int slots, int max_rows) {
+  if (B <= 0) return 1;
+  if (slots < 1) slots = 1;
+  int best = 1;
+  long long best_cost = -1;
+  for (int nb = max_rows < B ? max_rows : B; nb >= 1; --nb) {
+    const long long blocks = (B + nb - 1) / nb;
+    const long long waves = ((long long)T * blocks + slots - 1) / slots;
+    const long long cost = waves * nb;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = nb;
+    }
+  }
+  return best;
+}
 void colsum_jobs(const Layout& L, const rmx_config& c, const rmx_grads* g, void* ws, ColsumJob* jobs);
 
 Layout layout_of(const rmx_config& c) {
@@ -96,12 +117,12 @@ Layout layout_of(const rmx_config& c) {
   L.ra.D = c.D;
   L.ra.H = c.H;
   L.ra.dtype = c.dtype;
-  int nb = (c.B + 15) / 16;
-  nb = nb < 1 ? 1 : (nb > 64 ? 64 : nb);
+  // Rows per CTA of the per-token row passes (grid T x ceil(B / nb)).
+  const int sms = c.B > 0 ? sm_count() : 1;
+  const int nb = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? gate_bwd_ctas_per_sm(L.ra) : 1), kGateBwdMaxRows);
   L.ra.nb = nb;
   L.ra.nbblk = c.B > 0 ? (c.B + nb - 1) / nb : 0;
-  int nbl = (c.B + 31) / 32;
-  nbl = nbl < 1 ? 1 : (nbl > 32 ? 32 : nbl);
+  const int nbl = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? ln_bwd_ctas_per_sm(L.ra) : 1), kLnBwdMaxRows);
   L.ra.nb_ln = nbl;
   L.ra.nbblk_ln = c.B > 0 ? (c.B + nbl - 1) / nbl : 0;
   const size_t P = (size_t)L.ra.nbblk * c.T;     // gate-backward partial rows
@@ -199,6 +220,7 @@ rmx_status check_ptr(const void* p) {
 std::atomic<long long> g_launches{0};
 std::atomic<bool> g_prof{false};
 std::mutex g_mu;
+std::string g_prof_only;  // when not empty, only launches of this name are timed (under g_mu)
 struct ProfRec {
   const char* name;
   cudaEvent_t a, b;
@@ -218,12 +240,17 @@ cudaEvent_t pool_event() {
   return e;
 }
 
-// Brackets one kernel launch: counts it and, when profiling is on, records
-// events around it on its stream.
+bool selected(const char* name) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_prof_only.empty() || g_prof_only == name;
+}
+
+// Brackets one kernel launch: counts it and, when profiling is on (for its
+// name), records events around it on its stream.
 class Launch {
  public:
   Launch(const char* name, cudaStream_t st) : name_(name), st_(st) {
-    if (g_prof.load()) {
+    if (g_prof.load() && selected(name)) {
       a_ = pool_event();
       if (a_) cudaEventRecord(a_, st_);
     }
@@ -599,6 +626,12 @@ long long rmx_launch_count(void) { return g_launches.load(); }
 
 rmx_status rmx_profile_enable(int on) {
   g_prof.store(on != 0);
+  return RMX_OK;
+}
+
+rmx_status rmx_profile_select(const char* name) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof_only = name ? name : "";
   return RMX_OK;
 }
 

@@ -14,38 +14,51 @@
 // j holds the j-th 16-byte vector of columns of both halves.  The dh and Z
 // rows stream into shared memory through an S-stage ring of bulk copies (one
 // thread issues them; a byte-counting mbarrier per stage says when a row has
-// landed).  For each row the CTA takes the four row sums with one barrier,
-// then every thread finishes its own columns from registers, writes dZ and
-// keeps the column partial sums in registers.  dh and Z are read from HBM
-// once; every wait is bounded.
+// landed).  R rows at a time (two when the weights stay in registers) the
+// CTA takes their 4R row sums with one barrier, then every thread finishes
+// its own columns from registers, writes dZ and keeps the column partial sums
+// in registers.  dh and Z are read from HBM once; every wait is bounded.
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace rmx {
 namespace {
 
 constexpr int kGateMaxStages = 8;
 
-// Sums v[0..3] over the 32 lanes of a warp with six shuffles.  On return,
-// lane l holds the sum of component 2 * bit4(l) + bit3(l); all lanes holding
-// the same component hold the same bits.
-__device__ __forceinline__ float warp_sum4_transposed(const float v[4]) {
+// Sums v[0..NS-1] (NS = 4 or 8) over the 32 lanes of a warp.  The first
+// log2(NS) exchanges each halve the values a lane carries (it keeps one half
+// and sends the other), the rest are plain butterflies.  On return lane l
+// holds the sum of component l / (32 / NS); all lanes holding a component
+// hold the same bits.
+template <int NS>
+__device__ __forceinline__ float warp_sum_transposed(const float (&v)[NS]) {
+  static_assert(NS == 4 || NS == 8, "4 or 8 sums");
   const int lane = threadIdx.x & 31;
-  const bool b4 = lane & 16, b3 = lane & 8;
-  float k0 = b4 ? v[2] : v[0];
-  float k1 = b4 ? v[3] : v[1];
-  const float s0 = b4 ? v[0] : v[2];
-  const float s1 = b4 ? v[1] : v[3];
-  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-  float k = b3 ? k1 : k0;
-  const float s = b3 ? k0 : k1;
-  k += __shfl_xor_sync(0xffffffffu, s, 8);
-  k += __shfl_xor_sync(0xffffffffu, k, 4);
-  k += __shfl_xor_sync(0xffffffffu, k, 2);
-  k += __shfl_xor_sync(0xffffffffu, k, 1);
-  return k;
+  float w[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) w[k] = v[k];
+  int n = NS;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (n > 1) {
+      const bool hi = lane & off;
+      const int h = n / 2;
+#pragma unroll
+      for (int k = 0; k < NS / 2; ++k)
+        if (k < h) w[k] = (hi ? w[k + h] : w[k]) + __shfl_xor_sync(0xffffffffu, hi ? w[k] : w[k + h], off);
+      n = h;
+    } else {
+      w[0] += __shfl_xor_sync(0xffffffffu, w[0], off);
+    }
+  }
+  return w[0];
 }
 
 struct GateBwdArgs {
@@ -82,14 +95,18 @@ __device__ __forceinline__ void lds_f32(const float* p, float* v) {
   }
 }
 
-// Shared memory: stats [nb] float4 | red [2][4][32] float | weights [4][H]
+// Shared memory: stats [nb] float4 | red [2][8][32] float | weights [4][H]
 // float | stages x (dh row | Z row) | mbarriers.  Thread `tid` owns the
 // 16-byte vector of columns c0 = tid * E ... c0 + E - 1 of both halves.
 // WREG: the thread's weights stay in registers (one CTA per SM leaves room
-// for them when the CTA has at most 384 threads).
+// for them when the CTA has at most 320 threads, with two rows per step).
 template <typename T, bool WREG>
-__global__ void __launch_bounds__(WREG ? 384 : 512, 1) k_gate_bwd(const GateBwdArgs a) {
+__global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdArgs a) {
+  pdl_enter();
   constexpr int E = VecN<T>::value;
+  constexpr int R = WREG ? 2 : 1;  // rows per barrier
+  constexpr int NS = 4 * R;        // row sums per barrier
+  constexpr int LPS = 32 / NS;     // lanes holding one sum after the warp reduction
   extern __shared__ __align__(16) unsigned char smem[];
   const int H = a.H, S = a.stages;
   const int bblk = blockIdx.x, t = blockIdx.y;
@@ -101,8 +118,8 @@ __global__ void __launch_bounds__(WREG ? 384 : 512, 1) k_gate_bwd(const GateBwdA
   const bool active = c0 < H;
 
   float4* st_row = reinterpret_cast<float4*>(smem);                  // (rU, -mU*rU, rG, -mG*rG) per row
-  float* red = reinterpret_cast<float*>(smem + (size_t)a.nb * 16);   // [2][4][32]
-  float* wsm = red + 2 * 4 * 32;                                     // [4][H]
+  float* red = reinterpret_cast<float*>(smem + (size_t)a.nb * 16);   // [2][8][32]
+  float* wsm = red + 2 * 8 * 32;                                     // [4][H]
   unsigned char* ring = reinterpret_cast<unsigned char*>(wsm + 4 * (size_t)H);
   const size_t row_bytes = (size_t)3 * H * sizeof(T);
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)S * row_bytes);
@@ -161,103 +178,127 @@ __global__ void __launch_bounds__(WREG ? 384 : 512, 1) k_gate_bwd(const GateBwdA
   bool aborted = false;
   int s = 0;          // stage of row i
   uint32_t ph = 0;    // parity of that stage's current phase
-  for (int i = 0; i < nrows; ++i, dZrow += dZstep) {
-    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
-                                      (volatile int*)&abort_flag);
-    const float4 sr = st_row[i];
-    const float sU = sr.x, cU = sr.y, sG = sr.z, cG = sr.w;
+  for (int i = 0; i < nrows; i += R, dZrow += R * dZstep) {
+    const int nr = min(R, nrows - i);  // rows in this step
+    const int s1 = s + 1 == S ? 0 : s + 1;
+    const uint32_t ph1 = s + 1 == S ? ph ^ 1u : ph;
+    bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                (volatile int*)&abort_flag);
+    if (nr == 2)
+      ok = ok && mbar_wait_bounded(smem_u32(&full[s1]), ph1, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                   (volatile int*)&abort_flag);
     // Pass 1: everything that needs only this element, plus the row sums;
     // gU, Uh, gG, Gh stay in registers for pass 2.
-    float kgU[E], kUh[E], kgG[E], kGh[E];
-    float rs[4] = {0.f, 0.f, 0.f, 0.f};
-    if (ok && active) {
-      const T* st_dh = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
-      float dhv[E], zu[E], zg[E], wx[E], bx[E], wg[E], bg[E];
-      load_vec(st_dh + c0, dhv);
-      load_vec(st_dh + H + c0, zu);
-      load_vec(st_dh + 2 * H + c0, zg);
-      if (WREG) {
+    float kgU[R][E], kUh[R][E], kgG[R][E], kGh[R][E];
+    float rs[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) rs[k] = 0.f;
+    float sUr[R], sGr[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float4 sr = st_row[min(i + r, nrows - 1)];
+      sUr[r] = sr.x;
+      sGr[r] = sr.z;
+      if (ok && active && r < nr) {
+        const T* st_dh = reinterpret_cast<const T*>(ring + (size_t)(r == 0 ? s : s1) * row_bytes);
+        float dhv[E], zu[E], zg[E], wx[E], bx[E], wg[E], bg[E];
+        load_vec(st_dh + c0, dhv);
+        load_vec(st_dh + H + c0, zu);
+        load_vec(st_dh + 2 * H + c0, zg);
+        if (WREG) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            wx[e] = rwx[WREG ? e : 0];
+            bx[e] = rbx[WREG ? e : 0];
+            wg[e] = rwg[WREG ? e : 0];
+            bg[e] = rbg[WREG ? e : 0];
+          }
+        } else {
+          lds_f32<E>(wsm + c0, wx);
+          lds_f32<E>(wsm + H + c0, bx);
+          lds_f32<E>(wsm + 2 * H + c0, wg);
+          lds_f32<E>(wsm + 3 * H + c0, bg);
+        }
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          wx[e] = rwx[WREG ? e : 0];
-          bx[e] = rbx[WREG ? e : 0];
-          wg[e] = rwg[WREG ? e : 0];
-          bg[e] = rbg[WREG ? e : 0];
+          const float Uh = fmaf(zu[e], sr.x, sr.y);
+          const float Gh = fmaf(zg[e], sr.z, sr.w);
+          const float u = fmaf(wx[e], Uh, bx[e]);
+          const float g = fmaf(wg[e], Gh, bg[e]);
+          const float sg = sigmoid_fast(g);
+          const float gs = g * sg;
+          const float du = dhv[e] * gs;
+          const float dsilu = sg + fmaf(-gs, sg, gs);
+          const float dg = (dhv[e] * u) * dsilu;
+          const float gU = wx[e] * du, gG = wg[e] * dg;
+          rs[4 * r + 0] += gU;
+          rs[4 * r + 1] = fmaf(gU, Uh, rs[4 * r + 1]);
+          rs[4 * r + 2] += gG;
+          rs[4 * r + 3] = fmaf(gG, Gh, rs[4 * r + 3]);
+          awx[e] = fmaf(du, Uh, awx[e]);
+          abx[e] += du;
+          awg[e] = fmaf(dg, Gh, awg[e]);
+          abg[e] += dg;
+          kgU[r][e] = gU;
+          kUh[r][e] = Uh;
+          kgG[r][e] = gG;
+          kGh[r][e] = Gh;
         }
-      } else {
-        lds_f32<E>(wsm + c0, wx);
-        lds_f32<E>(wsm + H + c0, bx);
-        lds_f32<E>(wsm + 2 * H + c0, wg);
-        lds_f32<E>(wsm + 3 * H + c0, bg);
-      }
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float Uh = fmaf(zu[e], sU, cU);
-        const float Gh = fmaf(zg[e], sG, cG);
-        const float u = fmaf(wx[e], Uh, bx[e]);
-        const float g = fmaf(wg[e], Gh, bg[e]);
-        const float sg = sigmoid_fast(g);
-        const float gs = g * sg;                       // silu(g)
-        const float du = dhv[e] * gs;
-        const float dsilu = sg + fmaf(-gs, sg, gs);    // s * (1 + g * (1 - s))
-        const float dg = (dhv[e] * u) * dsilu;
-        const float gU = wx[e] * du, gG = wg[e] * dg;
-        rs[0] += gU;
-        rs[1] = fmaf(gU, Uh, rs[1]);
-        rs[2] += gG;
-        rs[3] = fmaf(gG, Gh, rs[3]);
-        awx[e] = fmaf(du, Uh, awx[e]);
-        abx[e] += du;
-        awg[e] = fmaf(dg, Gh, awg[e]);
-        abg[e] += dg;
-        kgU[e] = gU;
-        kUh[e] = Uh;
-        kgG[e] = gG;
-        kGh[e] = Gh;
       }
     }
-    // Row sums over the CTA: per warp (lane 8c holds sum c), then over the
-    // warps in a fixed order, the same bits in every thread.
-    float* rb = red + (i & 1) * 4 * 32;
+    // Row sums over the CTA: per warp (lane LPS*c holds sum c), then over
+    // the warps in a fixed order, the same bits in every thread.
+    float* rb = red + ((i / R) & 1) * 8 * 32;
     {
-      const float k = warp_sum4_transposed(rs);
-      if ((lane & 7) == 0) rb[(lane >> 3) * 32 + warp] = k;
+      const float k = warp_sum_transposed<NS>(rs);
+      if (lane % LPS == 0) rb[(lane / LPS) * 32 + warp] = k;
     }
     if (__syncthreads_or(!ok)) {
       aborted = true;
       break;
     }
-    // Every thread is done reading stage s: refill it.
-    if (tid == 0 && issued < nrows) issue(issued++, s);
-    if (++s == S) {
-      s = 0;
-      ph ^= 1u;
+    if (tid == 0) {
+      if (issued < nrows) issue(issued++, s);
+      if (nr == 2 && issued < nrows) issue(issued++, s1);
     }
-    float m[4];
-    {
-      // Lane l adds warps (l & 7) and (l & 7) + 8 of sum l >> 3 (at most 16
-      // warps), then the eight lanes of each sum combine.
-      const int c = lane >> 3, w0 = lane & 7;
-      float v = (w0 < nw ? rb[c * 32 + w0] : 0.f) + (w0 + 8 < nw ? rb[c * 32 + w0 + 8] : 0.f);
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) m[k] = __shfl_sync(0xffffffffu, v, k * 8) * invH;
-    }
-    // Pass 2: dU = rU * (gU - m0 - Uh * m1), the same for dG.
-    if (active) {
-      const float pU = -m[1], qU = -sU * m[0], pG = -m[3], qG = -sG * m[2];
-      float oU[E], oG[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        oU[e] = fmaf(sU, fmaf(pU, kUh[e], kgU[e]), qU);
-        oG[e] = fmaf(sG, fmaf(pG, kGh[e], kgG[e]), qG);
-        a1u[e] += oU[e];
-        a1g[e] += oG[e];
+    for (int r = 0; r < nr; ++r) {
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
       }
-      store_vec(dZrow + c0, oU);
-      store_vec(dZrow + H + c0, oG);
+    }
+    float m[NS];
+    {
+      // Lane l adds warps (l % LPS) + LPS*k of sum l / LPS (at most 16 warps),
+      // then the LPS lanes of each sum combine.
+      const int c = lane / LPS, w0 = lane % LPS;
+      float v = 0.f;
+#pragma unroll
+      for (int w = w0; w < 16; w += LPS)
+        if (w < nw) v += rb[c * 32 + w];
+#pragma unroll
+      for (int off = LPS / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+#pragma unroll
+      for (int k = 0; k < NS; ++k) m[k] = __shfl_sync(0xffffffffu, v, k * LPS) * invH;
+    }
+    if (active) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (r < nr) {
+          const float sU = sUr[r], sG = sGr[r];
+          const float pU = -m[4 * r + 1], qU = -sU * m[4 * r], pG = -m[4 * r + 3], qG = -sG * m[4 * r + 2];
+          float oU[E], oG[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            oU[e] = fmaf(sU, fmaf(pU, kUh[r][e], kgU[r][e]), qU);
+            oG[e] = fmaf(sG, fmaf(pG, kGh[r][e], kgG[r][e]), qG);
+            a1u[e] += oU[e];
+            a1g[e] += oG[e];
+          }
+          store_vec(dZrow + r * dZstep + c0, oU);
+          store_vec(dZrow + r * dZstep + H + c0, oG);
+        }
+      }
     }
   }
 
@@ -290,26 +331,65 @@ __global__ void __launch_bounds__(WREG ? 384 : 512, 1) k_gate_bwd(const GateBwdA
   }
 }
 
+// Threads, ring stages and shared memory of a CTA of nb rows (0 if even two
+// stages do not fit).
+template <typename T>
+size_t gate_shape(int H, int nb, int& threads, int& stages) {
+  constexpr int E = VecN<T>::value;
+  threads = (H / E + 31) / 32 * 32;
+  const size_t fixed = (size_t)nb * 16 + 2 * 8 * 32 * 4 + (size_t)4 * H * 4;
+  const size_t row_bytes = (size_t)3 * H * sizeof(T);
+  const int cap = max_dynamic_smem_bytes() - 1024;  // static shared memory and slack
+  const long long room = ((long long)cap - (long long)fixed) / (long long)(row_bytes + 8);
+  if (room < 2) return 0;
+  stages = (int)(room < kGateMaxStages ? room : kGateMaxStages);
+  return fixed + (size_t)stages * row_bytes + (size_t)stages * 8;
+}
+
+template <typename T, bool WREG>
+int gate_ctas_per_sm(int H) {
+  int threads = 0, stages = 0;
+  const size_t smem = gate_shape<T>(H, kGateBwdMaxRows, threads, stages);
+  if (smem == 0) return 1;
+  auto k = k_gate_bwd<T, WREG>;
+  int n = 0;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
 template <typename T, bool WREG>
 cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
   GateBwdArgs a = base;
-  constexpr int E = VecN<T>::value;
-  const int threads = (a.H / E + 31) / 32 * 32;
-  const size_t fixed = (size_t)a.nb * 16 + 2 * 4 * 32 * 4 + (size_t)4 * a.H * 4;
-  const size_t row_bytes = (size_t)3 * a.H * sizeof(T);
-  const int cap = max_dynamic_smem_bytes() - 1024;  // static shared memory and slack
-  const long long room = ((long long)cap - (long long)fixed) / (long long)(row_bytes + 8);
-  if (room < 2) return cudaErrorInvalidValue;
-  a.stages = (int)(room < kGateMaxStages ? room : kGateMaxStages);
-  const size_t smem = fixed + (size_t)a.stages * row_bytes + (size_t)a.stages * 8;
+  int threads = 0;
+  const size_t smem = gate_shape<T>(a.H, a.nb, threads, a.stages);
+  if (smem == 0) return cudaErrorInvalidValue;
   auto k = k_gate_bwd<T, WREG>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, threads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(k, grid, dim3(threads), smem, st, 1, a);
 }
 
 }  // namespace
+
+int gate_bwd_ctas_per_sm(const RowArgs& ra) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  const auto key = std::make_tuple(dev, ra.dtype, ra.H);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const bool wreg = ra.H / (ra.dtype == 0 ? 4 : 8) <= 320;
+  int n = 1;
+  if (ra.dtype == 0) n = wreg ? gate_ctas_per_sm<float, true>(ra.H) : gate_ctas_per_sm<float, false>(ra.H);
+  else if (ra.dtype == 1) n = wreg ? gate_ctas_per_sm<bf16, true>(ra.H) : gate_ctas_per_sm<bf16, false>(ra.H);
+  else n = wreg ? gate_ctas_per_sm<f16, true>(ra.H) : gate_ctas_per_sm<f16, false>(ra.H);
+  cache[key] = n;
+  return n;
+}
 
 bool gate_bwd_fused_supported(const RowArgs& a) {
   // One 16-byte vector of each half per thread, at most 512 threads.
@@ -347,7 +427,7 @@ cudaError_t launch_gate_bwd(const RowArgs& ra, const void* dh, const void* Z, co
   a.stages = 0;
   if (!a.err) return cudaErrorInvalidValue;
   const dim3 grid(ra.nbblk, ra.T);
-  const bool wreg = ra.H / (ra.dtype == 0 ? 4 : 8) <= 384;
+  const bool wreg = ra.H / (ra.dtype == 0 ? 4 : 8) <= 320;
   if (ra.dtype == 0) return wreg ? launch_typed<float, true>(a, st, grid) : launch_typed<float, false>(a, st, grid);
   if (ra.dtype == 1) return wreg ? launch_typed<bf16, true>(a, st, grid) : launch_typed<bf16, false>(a, st, grid);
   return wreg ? launch_typed<f16, true>(a, st, grid) : launch_typed<f16, false>(a, st, grid);

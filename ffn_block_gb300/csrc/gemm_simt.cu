@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace rmx {
 namespace {
@@ -31,6 +32,7 @@ struct SimtParams {
 
 template <typename T, int EPI>
 __global__ void __launch_bounds__(256) k_gemm_simt(const SimtParams p) {
+  pdl_enter();
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   const int g = blockIdx.z, m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
@@ -97,16 +99,14 @@ template <typename T>
 cudaError_t dispatch_simt(const SimtParams& p, int epi, cudaStream_t st) {
   dim3 grid((p.N + TN - 1) / TN, (p.M + TM - 1) / TM, p.G);
   switch (epi) {
-    case EPI_STORE: k_gemm_simt<T, EPI_STORE><<<grid, 256, 0, st>>>(p); break;
+    case EPI_STORE: return launch_k(k_gemm_simt<T, EPI_STORE>, grid, dim3(256), 0, st, 1, p);
     case EPI_BIAS:
     case EPI_BIAS_ZSTATS:  // statistics are taken by launch_zstats on this path
-      k_gemm_simt<T, EPI_BIAS><<<grid, 256, 0, st>>>(p);
-      break;
-    case EPI_BIAS_RESID: k_gemm_simt<T, EPI_BIAS_RESID><<<grid, 256, 0, st>>>(p); break;
-    case EPI_RESID: k_gemm_simt<T, EPI_RESID><<<grid, 256, 0, st>>>(p); break;
+      return launch_k(k_gemm_simt<T, EPI_BIAS>, grid, dim3(256), 0, st, 1, p);
+    case EPI_BIAS_RESID: return launch_k(k_gemm_simt<T, EPI_BIAS_RESID>, grid, dim3(256), 0, st, 1, p);
+    case EPI_RESID: return launch_k(k_gemm_simt<T, EPI_RESID>, grid, dim3(256), 0, st, 1, p);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -41,6 +41,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace rmx {
 namespace {
@@ -401,6 +402,9 @@ template <typename T, int KIND, int EPI, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const Params p) {
+  // Setup (barriers, TMEM, tensor-map prefetch) overlaps the previous
+  // kernel's tail; global memory is touched only after pdl_wait().
+  pdl_trigger();
   using KT = KindTraits<KIND>;
   using R = Ring<PAIR>;
   constexpr int STAGES = R::STAGES;
@@ -457,6 +461,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (PAIR) cluster_barrier();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -689,6 +694,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 __global__ void k_bounded_wait_test(unsigned int* err, unsigned long long limit_ns) {
+  pdl_enter();
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -741,23 +747,10 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   if (e != cudaSuccess) return e;
   if (!PAIR) {
     const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-    k<<<grid, THREADS, SMEM_BYTES, st>>>(a, b, c, p);
-    return cudaGetLastError();
+    return launch_k(k, dim3(grid), dim3(THREADS), SMEM_BYTES, st, 1, a, b, c, p);
   }
   const int clusters = p.num_pair_tiles < sm_count() / 2 ? p.num_pair_tiles : sm_count() / 2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (clusters > 0 ? clusters : 1), 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, c, p);
+  return launch_k(k, dim3(2 * (clusters > 0 ? clusters : 1)), dim3(THREADS), SMEM_BYTES, st, 2, a, b, c, p);
 }
 
 template <typename T, bool PAIR>
@@ -866,7 +859,8 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
 }
 
 cudaError_t launch_bounded_wait_test(unsigned int* err, unsigned long long limit_ns, cudaStream_t st) {
-  k_bounded_wait_test<<<1, 32, 0, st>>>(err, limit_ns);
+  cudaError_t e = launch_k(k_bounded_wait_test, dim3(1), dim3(32), 0, st, 1, err, limit_ns);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -37,6 +37,9 @@ cudaError_t launch_ln01_fwd(const RowArgs& a, const void* x, const void* gamma0,
 // token_mix(ds) to out_mixed; LNB_RESID adds resid to the output.
 // LNB_PLAIN writes only the gradient.
 constexpr int kLnBwdMaxRows = 64;
+// CTAs of the LayerNorm backward ring resident per SM (occupancy of the
+// launch shape with kLnBwdMaxRows rows), for choosing nb_ln.
+int ln_bwd_ctas_per_sm(const RowArgs& a);
 enum LnBwdMode { LNB_BIAS = 0, LNB_MIXED_TOO = 1, LNB_RESID = 2, LNB_PLAIN = 3 };
 cudaError_t launch_ln_bwd(const RowArgs& a, int mode, const void* gin, const void* s,
                           const float* mu, const float* rs, const void* gamma, const void* resid, void* out,
@@ -69,6 +72,7 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats
 // forward's inner-LayerNorm statistics.  CTA (bblk, t) owns up to nb <=
 // kGateBwdMaxRows rows of token t and the whole row.
 constexpr int kGateBwdMaxRows = 64;
+int gate_bwd_ctas_per_sm(const RowArgs& a);
 bool gate_bwd_fused_supported(const RowArgs& a);
 cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU, const float* rU,
                             const float* muG, const float* rG, const void* wx, const void* bx, const void* wg,

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace rmx {
 namespace {
@@ -54,6 +55,7 @@ struct Ln01Args {
 // (norm0's gamma and beta) | x rows [T][D + pad] | mbarrier.
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(512, 1) k_ln01_fwd(const Ln01Args a) {
+  pdl_enter();
   constexpr int V = VecN<T>::value;
   extern __shared__ __align__(16) unsigned char smem[];
   const int Tn = a.T, D = a.D, C = a.C;
@@ -307,6 +309,7 @@ __host__ __device__ inline Ln01ClusterGeom ln01_cluster_geom(int Tn, int D, int 
 // gather (NE * e bytes divide C * e).
 template <typename T, int NE>
 __global__ void __launch_bounds__(32 * kLn01Rows) k_ln01_cluster(const Ln01Args a) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int e = (int)sizeof(T);
   constexpr int V = VecN<T>::value;
@@ -480,19 +483,7 @@ cudaError_t launch_cluster_typed(const Ln01Args& a, cudaStream_t st) {
   auto k = k_ln01_cluster<T, NE>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.B * g.cs), 1, 1);
-  cfg.blockDim = dim3(32 * kLn01Rows, 1, 1);
-  cfg.dynamicSmemBytes = g.smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)g.cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a);
+  return launch_k(k, dim3((unsigned)(a.B * g.cs)), dim3(32 * kLn01Rows), g.smem, st, (unsigned)g.cs, a);
 }
 
 // Widest access (2, 4, 8 or 16 bytes) that divides a C-element piece.
@@ -526,8 +517,7 @@ cudaError_t launch_typed(const Ln01Args& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int warps = a.T < 16 ? a.T : 16;
-  k<<<a.B, 32 * warps, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(k, dim3(a.B), dim3(32 * warps), smem, st, 1, a);
 }
 
 template <typename T>

@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace rmx {
 namespace {
@@ -128,6 +129,7 @@ __device__ __forceinline__ void lds_gather2(const unsigned char* p0, const unsig
 // issued once the second pass is done.
 template <typename T, bool PAIRS>
 __global__ void __launch_bounds__(kLn0MaxThreads, 3) k_ln0_bwd_gather(const Ln0GatherArgs a) {
+  pdl_enter();
   constexpr int E = VecN<T>::value;
   constexpr int es = (int)sizeof(T);
   extern __shared__ __align__(16) unsigned char smem[];
@@ -324,8 +326,7 @@ cudaError_t launch_typed(const Ln0GatherArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int threads = (a.D / E + 31) / 32 * 32;
   const dim3 grid(a.T / kRowsPerCta, (a.B + a.spc - 1) / a.spc);
-  k<<<grid, threads, g.smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(k, grid, dim3(threads), g.smem, st, 1, a);
 }
 
 }  // namespace

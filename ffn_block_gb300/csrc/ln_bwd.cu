@@ -18,8 +18,13 @@
 // barrier, then each thread writes its columns and keeps the column partial
 // sums in registers.  Every wait is bounded.
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace rmx {
 namespace {
@@ -127,6 +132,7 @@ template <int MODE> struct LnRows {
 // together, which halves the per-row reduction and barrier work.
 template <typename T, int MODE>
 __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
+  pdl_enter();
   constexpr int E = VecN<T>::value;
   constexpr int NR = LnRows<MODE>::value;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -299,24 +305,42 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
   }
 }
 
+// Threads, ring stages and shared memory of a ring CTA of nb rows.
 template <typename T, int MODE>
-cudaError_t launch_ring(const LnBwdArgs& base, cudaStream_t st) {
-  LnBwdArgs a = base;
+size_t ring_shape(int D, int nb, int& threads, int& stages) {
   constexpr int E = VecN<T>::value;
-  const int threads = (a.D / E + 31) / 32 * 32;
-  const size_t fixed = stats_bytes(a.nb) + 2 * 4 * 32 * 4;
-  const size_t row_bytes = (size_t)LnRows<MODE>::value * a.D * sizeof(T);
+  threads = (D / E + 31) / 32 * 32;
+  const size_t fixed = stats_bytes(nb) + 2 * 4 * 32 * 4;
+  const size_t row_bytes = (size_t)LnRows<MODE>::value * D * sizeof(T);
   long long room = ((long long)kLnSmemTarget - (long long)fixed) / (long long)(row_bytes + 8);
   if (room < 2) room = 2;
   if (room > kLnMaxStages) room = kLnMaxStages;
-  a.stages = (int)room;
-  const size_t smem = fixed + (size_t)a.stages * (row_bytes + 8);
+  stages = (int)room;
+  return fixed + (size_t)stages * (row_bytes + 8);
+}
+
+template <typename T, int MODE>
+int ring_ctas_per_sm(int D) {
+  int threads = 0, stages = 0;
+  const size_t smem = ring_shape<T, MODE>(D, kLnBwdMaxRows, threads, stages);
+  auto k = k_ln_bwd_ring<T, MODE>;
+  int n = 0;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
+template <typename T, int MODE>
+cudaError_t launch_ring(const LnBwdArgs& base, cudaStream_t st) {
+  LnBwdArgs a = base;
+  int threads = 0;
+  const size_t smem = ring_shape<T, MODE>(a.D, a.nb, threads, a.stages);
   if ((long long)smem > (long long)max_dynamic_smem_bytes() - 1024) return cudaErrorInvalidValue;
   auto k = k_ln_bwd_ring<T, MODE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<dim3(a.T, (a.B + a.nb - 1) / a.nb), threads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(k, dim3(a.T, (a.B + a.nb - 1) / a.nb), dim3(threads), smem, st, 1, a);
 }
 
 template <typename T>
@@ -328,6 +352,22 @@ cudaError_t launch_mode(const LnBwdArgs& a, int mode, cudaStream_t st) {
 }
 
 }  // namespace
+
+int ln_bwd_ctas_per_sm(const RowArgs& ra) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  const auto key = std::make_tuple(dev, ra.dtype, ra.D);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const int n = ra.dtype == 0 ? ring_ctas_per_sm<float, LNB_BIAS>(ra.D)
+                : ra.dtype == 1 ? ring_ctas_per_sm<bf16, LNB_BIAS>(ra.D)
+                                : ring_ctas_per_sm<f16, LNB_BIAS>(ra.D);
+  cache[key] = n;
+  return n;
+}
 
 cudaError_t launch_ln_bwd(const RowArgs& ra, int mode, const void* gin, const void* s, const float* mu,
                           const float* rs, const void* gamma, const void* resid, void* out, void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {

@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace rmx {
 
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
                                                 const T* __restrict__ g, const T* __restrict__ be,
                                                 T* __restrict__ y, float* __restrict__ mu, float* __restrict__ rs,
                                                 T* __restrict__ s_out, int N, int Tn, int D, int C, float eps) {
+  pdl_enter();
   constexpr int V = VecN<T>::value;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
 template <typename T>
 __global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* __restrict__ zstats, int N, int H,
                                                 int tiles) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (item >= (long long)N * tiles) return;
@@ -226,6 +229,7 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
                                                   const T* __restrict__ wx, const T* __restrict__ bx,
                                                   const T* __restrict__ wg, const T* __restrict__ bg,
                                                   T* __restrict__ hidden, int N, int H, float eps) {
+  pdl_enter();
   constexpr int V = VecN<T>::value;
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -318,6 +322,7 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_colsums_chunks(const ColsumArgs a) {
+  pdl_enter();
   __shared__ float4 part[8][32];
   const int jb = colsum_job_of(a);
   const ColsumJob& job = a.job[jb];
@@ -357,6 +362,7 @@ __global__ void __launch_bounds__(256) k_colsums_chunks(const ColsumArgs a) {
 // Adds the chunk sums of the jobs with more than one chunk, in chunk order.
 template <typename T>
 __global__ void __launch_bounds__(128) k_colsums_final(const ColsumArgs a) {
+  pdl_enter();
   const int jb = colsum_job_of(a);
   const ColsumJob& job = a.job[jb];
   const int j = ((int)blockIdx.x - a.block_start[jb]) * 512 + threadIdx.x * 4;
@@ -369,6 +375,7 @@ __global__ void __launch_bounds__(128) k_colsums_final(const ColsumArgs a) {
 
 template <typename T>
 __global__ void __launch_bounds__(512) k_colsums_onepass(const ColsumArgs a) {
+  pdl_enter();
   __shared__ float part[16][33];
   const int jb = colsum_job_of(a);
   const ColsumJob& job = a.job[jb];
@@ -403,10 +410,11 @@ cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void*
   const int q = (nv + 31) / 32;
   const int grid = (N + 7) / 8;
   const int C = a.D / a.T;
-#define RMX_LNF(M, MAXV)                                                                                   \
-  RMX_DISPATCH_T(a.dtype, {                                                                                \
-    k_ln_fwd<T, M, MAXV><<<grid, 256, 0, st>>>((const T*)s, (const T*)s_add, (const T*)g, (const T*)be,     \
-                                               (T*)y, mu, rs, (T*)s_out, N, a.T, a.D, C, 1e-3f);           \
+  cudaError_t err = cudaSuccess;
+#define RMX_LNF(M, MAXV)                                                                                    \
+  RMX_DISPATCH_T(a.dtype, {                                                                                 \
+    err = launch_k(k_ln_fwd<T, M, MAXV>, dim3(grid), dim3(256), 0, st, 1, (const T*)s, (const T*)s_add,     \
+                   (const T*)g, (const T*)be, (T*)y, mu, rs, (T*)s_out, N, a.T, a.D, C, 1e-3f);             \
   })
 #define RMX_LNF_Q(M)                          \
   if (q <= 1) RMX_LNF(M, 1);                  \
@@ -420,7 +428,7 @@ cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void*
   else { RMX_LNF_Q(LNF_SUM_IN) }
 #undef RMX_LNF_Q
 #undef RMX_LNF
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaStream_t st) {
@@ -428,19 +436,23 @@ cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaSt
   const int tiles = zstats_tiles(a.H);
   const long long items = (long long)N * tiles;
   const int grid = (int)((items + 7) / 8);
-  RMX_DISPATCH_T(a.dtype, { k_zstats<T><<<grid, 256, 0, st>>>((const T*)Z, zstats, N, a.H, tiles); });
-  return cudaGetLastError();
+  cudaError_t err = cudaSuccess;
+  RMX_DISPATCH_T(a.dtype, {
+    err = launch_k(k_zstats<T>, dim3(grid), dim3(256), 0, st, 1, (const T*)Z, zstats, N, a.H, tiles);
+  });
+  return err;
 }
 
 cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, float* muU, float* rU,
                             float* muG, float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
                             void* hidden, cudaStream_t st) {
   const int N = a.B * a.T;
+  cudaError_t err = cudaSuccess;
   RMX_DISPATCH_T(a.dtype, {
-    k_gate_fwd<T><<<(N + 7) / 8, 256, 0, st>>>((const T*)Z, zstats, muU, rU, muG, rG, (const T*)wx, (const T*)bx,
-                                               (const T*)wg, (const T*)bg, (T*)hidden, N, a.H, 1e-5f);
+    err = launch_k(k_gate_fwd<T>, dim3((N + 7) / 8), dim3(256), 0, st, 1, (const T*)Z, zstats, muU, rU, muG, rG,
+                   (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg, (T*)hidden, N, a.H, 1e-5f);
   });
-  return cudaGetLastError();
+  return err;
 }
 
 size_t colsums_scratch_floats(const ColsumJob* jobs, int njobs) {
@@ -485,14 +497,15 @@ cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, float* s
   const bool chunked = colsum_plan(jobs, njobs, scratch, scratch_floats, a);
   const int blocks = a.block_start[njobs];
   if (blocks == 0) return cudaSuccess;
+  cudaError_t err = cudaSuccess;
   if (!chunked) {
-    RMX_DISPATCH_T(dtype, { k_colsums_onepass<T><<<blocks, dim3(32, 16), 0, st>>>(a); });
-    return cudaGetLastError();
+    RMX_DISPATCH_T(dtype, { err = launch_k(k_colsums_onepass<T>, dim3(blocks), dim3(32, 16), 0, st, 1, a); });
+    return err;
   }
-  RMX_DISPATCH_T(dtype, { k_colsums_chunks<T><<<blocks, 256, 0, st>>>(a); });
+  RMX_DISPATCH_T(dtype, { err = launch_k(k_colsums_chunks<T>, dim3(blocks), dim3(256), 0, st, 1, a); });
   if (needs_final)
     for (int i = 0; i < njobs; ++i) *needs_final = *needs_final || a.nchunks[i] > 1;
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_colsums_final(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
@@ -507,8 +520,9 @@ cudaError_t launch_colsums_final(const ColsumJob* jobs, int njobs, int dtype, fl
   }
   a.block_start[njobs] = fb;
   if (fb == 0) return cudaErrorInvalidValue;
-  RMX_DISPATCH_T(dtype, { k_colsums_final<T><<<fb, 128, 0, st>>>(a); });
-  return cudaGetLastError();
+  cudaError_t err = cudaSuccess;
+  RMX_DISPATCH_T(dtype, { err = launch_k(k_colsums_final<T>, dim3(fb), dim3(128), 0, st, 1, a); });
+  return err;
 }
 
 }  // namespace rmx

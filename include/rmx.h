@@ -156,6 +156,11 @@ long long rmx_launch_count(void);
  * returns how many kernel names were seen; it then resets the counters. */
 rmx_status rmx_profile_enable(int on);
 int rmx_profile_read(const char** names, long long* launches, double* total_ms, int cap);
+/* Restricts the per-kernel timing to launches of the kernel called `name`
+ * (a name rmx_profile_read reports); NULL or "" times every launch again.
+ * Timing one kernel brackets only its launches with events, so the others
+ * run back to back as they do unprofiled.  The name is copied. */
+rmx_status rmx_profile_select(const char* name);
 
 /* Test hook (no production use): launches one tiny kernel that waits on an
  * mbarrier that nothing will ever complete, with a limit of `limit_us`

@@ -123,3 +123,20 @@ def test_profiler_counts_every_launch():
     assert {"gemm1_fwd", "gemm2_fwd", "gemm1_wgrad", "gemm2_dgrad", "ln01_fwd", "ln1_bwd", "gate_bwd",
             "ln0_bwd_gather"} <= set(prof)
     assert all(ms >= 0.0 for _, ms in prof.values())
+
+
+def test_profiler_select_times_one_kernel():
+    shape = I.shape_of("c1")
+    blk = RankMixerDevice(shape, I.make_inputs(shape))
+    B.rmx_profile_read()
+    before = B.rmx_launch_count()
+    B.rmx_profile_select("gate_bwd")
+    B.rmx_profile_enable(True)
+    try:
+        blk.step()
+    finally:
+        B.rmx_profile_enable(False)
+        B.rmx_profile_select(None)
+    prof = B.rmx_profile_read()
+    assert set(prof) == {"gate_bwd"} and prof["gate_bwd"][0] == 1
+    assert B.rmx_launch_count() - before > 1  # every launch is still counted
