@@ -23,10 +23,11 @@ struct RowArgs {
 enum LnFwdMode { LNF_PLAIN = 0, LNF_MIXED_OUT = 1, LNF_SUM_IN = 2 };
 cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
                           const void* be, void* y, float* mu, float* rs, void* s_out, cudaStream_t st);
-// norm0 -> token mix -> + x -> norm1 with one CTA per sample (the sample's
-// rows staged in shared memory): writes s1 (norm1's input, rounded to the
-// storage type), out1 and both row statistics.  Supported when the sample
-// fits in shared memory.
+// norm0 -> token mix -> + x -> norm1: writes s1 (norm1's input, rounded to
+// the storage type), out1 and both row statistics.  With T a multiple of 8
+// (up to 64) a cluster of T/8 CTAs per sample, each staging its 8 rows and
+// the column stripe of the sample they need; otherwise one CTA per sample
+// staging all its rows.  Supported when that fits in shared memory.
 bool ln01_fwd_supported(const RowArgs& a);
 cudaError_t launch_ln01_fwd(const RowArgs& a, const void* x, const void* gamma0, const void* beta0,
                             const void* gamma1, const void* beta1, void* s1, void* out1, float* mu0, float* r0,
