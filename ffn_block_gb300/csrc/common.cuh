@@ -212,6 +212,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// One box of a rank-2 tensor map into shared memory (128-byte aligned),
+// completion counted on `bar` in bytes (the whole box, zero-filled parts
+// included).  c0 is the inner coordinate in elements.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // Chan / Golub / LeVeque merge of (count, mean, M2) partial statistics.
 struct Moments {
   float n, mean, m2;

@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -148,5 +149,11 @@ cudaError_t gemm_simt_launch(const GemmDesc& d, cudaStream_t st);
 cudaError_t launch_bounded_wait_test(unsigned int* err, unsigned long long limit_ns, cudaStream_t st);
 
 int sm_count();
+
+// Rank-2 tiled tensor map without swizzle over a row-major [d1][d0] array of
+// the storage dtype (0 f32, 1 bf16, 2 f16), row stride s1 bytes, box
+// {b0, b1}; out-of-range elements of a box read as zero.
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t d1, uint64_t s1,
+                        uint32_t b0, uint32_t b1);
 
 }  // namespace rmx

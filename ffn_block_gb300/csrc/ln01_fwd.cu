@@ -19,13 +19,17 @@
 // k_ln01_cluster splits a sample over a cluster of T/8 CTAs, each owning 8
 // output rows i0 <= i < i0 + 8.  Output row i needs, from every row j, the
 // columns i*C ... i*C + C - 1, so the CTA stages its own 8 rows plus that
-// column stripe (T pieces of 8*C elements) of all T rows; the stripe's bytes
-// belong to the other CTAs' own rows and mostly come from L2.  norm0 needs
+// column stripe (T rows of 8*C elements, one TMA box of a rank-2 map over x,
+// a few columns wider so that its rows land an odd number of 16-byte units
+// apart) of all T rows; the stripe's bytes belong to the other CTAs' own rows
+// and mostly come from L2.  norm0 needs
 // whole rows, so each CTA takes the statistics of its own rows and stores
 // them into every CTA of the cluster (distributed shared memory); a cluster
 // barrier later every CTA has all T of them.  About 42 KB of shared memory per
 // CTA lets several clusters share an SM, so one sample's loads overlap
 // another's arithmetic.
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -278,8 +282,8 @@ struct Ln01ClusterGeom {
   int cs;           // CTAs per sample (cluster size) = T / 8
   int own_pitch;    // bytes between staged own rows (D * e)
   int piece;        // bytes of one stripe piece (8 * C * e)
-  int stripe_pitch; // bytes between staged stripe pieces (piece padded, pitch / 16 odd)
-  size_t off_gb, off_own, off_stripe, off_bar, smem;
+  int stripe_pitch; // bytes between staged stripe rows (piece padded, pitch / 16 odd; the TMA box width)
+  size_t off_st0, off_gb, off_own, off_bar, smem;  // the stripe comes first (128-byte aligned)
 };
 
 __host__ __device__ inline size_t round16(size_t v) { return (v + 15) & ~(size_t)15; }
@@ -294,23 +298,25 @@ __host__ __device__ inline Ln01ClusterGeom ln01_cluster_geom(int Tn, int D, int 
   // that is an odd number of 16-byte units spreads them over the banks.
   g.stripe_pitch = (int)round16((size_t)g.piece);
   if ((g.stripe_pitch / 16) % 2 == 0) g.stripe_pitch += 16;
-  g.off_gb = round16((size_t)Tn * 8);
+  g.off_st0 = (size_t)Tn * g.stripe_pitch;
+  g.off_gb = g.off_st0 + round16((size_t)Tn * 8);
   g.off_own = g.off_gb + round16((size_t)kLn01Rows * C * 8);
-  g.off_stripe = g.off_own + (size_t)kLn01Rows * g.own_pitch;
-  g.off_bar = g.off_stripe + (size_t)Tn * g.stripe_pitch;
-  g.smem = g.off_bar + 16;
+  g.off_bar = g.off_own + (size_t)kLn01Rows * g.own_pitch;
+  g.smem = g.off_bar + 16 + 128;  // + slack to align the stripe to 128 bytes
   return g;
 }
 
 // One CTA: sample b, output rows i0 ... i0 + 7 (i0 = 8 * rank).  Shared
-// memory: st0 [T] float2 (norm0 mean, rstd of every row of the sample) |
-// gb0 [8*C] float2 (gamma0, beta0 of the stripe's columns) | own rows [8][D]
-// | stripe [T][8*C] | mbarrier.  NE elements per shared-memory access in the
+// memory: stripe [T][8*C + pad] | st0 [T] float2 (norm0 mean, rstd of every
+// row of the sample) | gb0 [8*C] float2 (gamma0, beta0 of the stripe's
+// columns) | own rows [8][D] | mbarrier.  NE elements per shared-memory access in the
 // gather (NE * e bytes divide C * e).
 template <typename T, int NE>
-__global__ void __launch_bounds__(32 * kLn01Rows) k_ln01_cluster(const Ln01Args a) {
+__global__ void __launch_bounds__(32 * kLn01Rows)
+    k_ln01_cluster(const __grid_constant__ CUtensorMap stripe_map, const Ln01Args a) {
   pdl_enter();
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   constexpr int e = (int)sizeof(T);
   constexpr int V = VecN<T>::value;
   const int Tn = a.T, D = a.D, C = a.C;
@@ -319,10 +325,10 @@ __global__ void __launch_bounds__(32 * kLn01Rows) k_ln01_cluster(const Ln01Args 
   const int b = blockIdx.x / geo.cs;
   const int i0 = rank * kLn01Rows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float2* st0 = reinterpret_cast<float2*>(smem);
+  unsigned char* stripe = smem;
+  float2* st0 = reinterpret_cast<float2*>(smem + geo.off_st0);
   float2* gb0 = reinterpret_cast<float2*>(smem + geo.off_gb);
   unsigned char* own = smem + geo.off_own;
-  unsigned char* stripe = smem + geo.off_stripe;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + geo.off_bar);
   __shared__ int abort_flag;
 
@@ -331,7 +337,7 @@ __global__ void __launch_bounds__(32 * kLn01Rows) k_ln01_cluster(const Ln01Args 
   cluster_arrive_relaxed();
 
   const T* xb = reinterpret_cast<const T*>(a.x) + (size_t)b * Tn * D;
-  const uint32_t total = (uint32_t)(kLn01Rows * geo.own_pitch + Tn * geo.piece);
+  const uint32_t total = (uint32_t)(kLn01Rows * geo.own_pitch + Tn * geo.stripe_pitch);
   if (warp == 0) {
     if (lane == 0) {
       abort_flag = 0;
@@ -340,14 +346,11 @@ __global__ void __launch_bounds__(32 * kLn01Rows) k_ln01_cluster(const Ln01Args 
       mbar_arrive_expect_tx(smem_u32(bar), total);
     }
     __syncwarp();
-    for (int k = lane; k < kLn01Rows + Tn; k += 32) {
-      if (k < kLn01Rows)
-        bulk_g2s(smem_u32(own + (size_t)k * geo.own_pitch), xb + (size_t)(i0 + k) * D, (uint32_t)geo.own_pitch,
-                 smem_u32(bar));
-      else
-        bulk_g2s(smem_u32(stripe + (size_t)(k - kLn01Rows) * geo.stripe_pitch),
-                 xb + (size_t)(k - kLn01Rows) * D + (size_t)i0 * C, (uint32_t)geo.piece, smem_u32(bar));
-    }
+    if (lane < kLn01Rows)
+      bulk_g2s(smem_u32(own + (size_t)lane * geo.own_pitch), xb + (size_t)(i0 + lane) * D,
+               (uint32_t)geo.own_pitch, smem_u32(bar));
+    else if (lane == kLn01Rows)
+      tma_load_2d(smem_u32(stripe), &stripe_map, smem_u32(bar), i0 * C, b * Tn);
   }
   {
     const T* g0 = reinterpret_cast<const T*>(a.gamma0);
@@ -479,11 +482,18 @@ __global__ void __launch_bounds__(32 * kLn01Rows) k_ln01_cluster(const Ln01Args 
 
 template <typename T, int NE>
 cudaError_t launch_cluster_typed(const Ln01Args& a, cudaStream_t st) {
-  const Ln01ClusterGeom g = ln01_cluster_geom(a.T, a.D, (int)sizeof(T));
+  constexpr int es = (int)sizeof(T);
+  const Ln01ClusterGeom g = ln01_cluster_geom(a.T, a.D, es);
+  // x as [B*T][D]; one box = the stripe of one sample (T rows).
+  CUtensorMap map;
+  const int dtype = es == 4 ? 0 : (std::is_same<T, bf16>::value ? 1 : 2);
+  if (!make_tensor_map_2d(&map, a.x, dtype, (uint64_t)a.D, (uint64_t)a.B * a.T, (uint64_t)a.D * es,
+                          (uint32_t)(g.stripe_pitch / es), (uint32_t)a.T))
+    return cudaErrorInvalidValue;
   auto k = k_ln01_cluster<T, NE>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
   if (err != cudaSuccess) return err;
-  return launch_k(k, dim3((unsigned)(a.B * g.cs)), dim3(32 * kLn01Rows), g.smem, st, (unsigned)g.cs, a);
+  return launch_k(k, dim3((unsigned)(a.B * g.cs)), dim3(32 * kLn01Rows), g.smem, st, (unsigned)g.cs, map, a);
 }
 
 // Widest access (2, 4, 8 or 16 bytes) that divides a C-element piece.
@@ -502,7 +512,8 @@ bool ln01_cluster_supported(const RowArgs& ra) {
   if (ra.T % kLn01Rows || ra.T / kLn01Rows > 8 || ra.D % ra.T) return false;
   if ((ra.D * e) % 16) return false;
   const Ln01ClusterGeom g = ln01_cluster_geom(ra.T, ra.D, e);
-  if ((long long)kLn01Rows * g.own_pitch + (long long)ra.T * g.piece >= (1ll << 20)) return false;
+  if ((long long)kLn01Rows * g.own_pitch + (long long)ra.T * g.stripe_pitch >= (1ll << 20)) return false;
+  if (g.stripe_pitch / e > 256 || ra.T > 256) return false;  // TMA box limits
   return (long long)g.smem <= (long long)max_dynamic_smem_bytes() - 1024;
 }
 

@@ -12,8 +12,9 @@
 // CTA (q, sample group) owns rows j = 8q ... 8q + 7 of a few consecutive
 // samples.  Row j of da0 takes, from every row i of ds1, the C columns
 // j*C ... j*C + C - 1, so for its eight rows the CTA stages one column stripe
-// of ds1 (T pieces of 8*C elements, bulk copies) next to its own rows of ds1
-// and x.  Thread v owns the 16-byte vector of columns d = v*E ... v*E + E - 1
+// of ds1 (T rows of 8*C elements: one TMA box of a rank-2 map over ds1, the
+// box a few columns wider so that its rows land an odd number of 16-byte
+// units apart) next to its own rows of ds1 and x (bulk copies).  Thread v owns the 16-byte vector of columns d = v*E ... v*E + E - 1
 // of all eight rows: it gathers da0[j, d] = stripe[i][(j - 8q)*C + c] with
 // d = i*C + c, takes the sixteen row sums of its columns, one block reduction
 // per sample gives their totals, and the column partials stay in registers
@@ -47,7 +48,7 @@ struct Ln0GatherArgs {
 
 struct Ln0Geom {
   int piece;         // bytes of one stripe piece (8 * C * e)
-  int stripe_pitch;  // piece padded to an odd number of 16-byte units
+  int stripe_pitch;  // piece padded to an odd number of 16-byte units (the TMA box width)
   int row_bytes;     // D * e
   size_t off_ownd, off_ownx, off_red, off_means, off_st, off_bar, smem;
 };
@@ -67,7 +68,7 @@ __host__ __device__ inline Ln0Geom ln0_geom(int Tn, int D, int esize) {
   g.off_means = g.off_red + 16 * 32 * sizeof(float);
   g.off_st = g.off_means + 16 * sizeof(float);
   g.off_bar = g.off_st + 2 * kRowsPerCta * sizeof(float2);
-  g.smem = g.off_bar + 16;
+  g.smem = g.off_bar + 16 + 128;  // + slack to align the stripe to 128 bytes
   return g;
 }
 
@@ -128,11 +129,13 @@ __device__ __forceinline__ void lds_gather2(const unsigned char* p0, const unsig
 // Both passes gather da0 from the stripe, so the next sample's copies are
 // issued once the second pass is done.
 template <typename T, bool PAIRS>
-__global__ void __launch_bounds__(kLn0MaxThreads, 3) k_ln0_bwd_gather(const Ln0GatherArgs a) {
+__global__ void __launch_bounds__(kLn0MaxThreads, 3)
+    k_ln0_bwd_gather(const __grid_constant__ CUtensorMap stripe_map, const Ln0GatherArgs a) {
   pdl_enter();
   constexpr int E = VecN<T>::value;
   constexpr int es = (int)sizeof(T);
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int Tn = a.T, D = a.D, C = a.C;
   const Ln0Geom geo = ln0_geom(Tn, D, es);
   const int j0 = blockIdx.x * kRowsPerCta;
@@ -164,11 +167,10 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3) k_ln0_bwd_gather(const Ln0G
   // Warp 0 issues a sample's copies: lane 0 arms the barrier, the lanes
   // share the copies.
   auto issue_stripe = [&](int b) {
-    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bar[0]), (uint32_t)(Tn * geo.piece));
-    __syncwarp();
-    for (int i = lane; i < Tn; i += 32)
-      bulk_g2s(smem_u32(stripe + (size_t)i * geo.stripe_pitch), ds1 + ((size_t)b * Tn + i) * D + (size_t)j0 * C,
-               (uint32_t)geo.piece, smem_u32(&bar[0]));
+    if (lane == 0) {
+      mbar_arrive_expect_tx(smem_u32(&bar[0]), (uint32_t)(Tn * geo.stripe_pitch));
+      tma_load_2d(smem_u32(stripe), &stripe_map, smem_u32(&bar[0]), j0 * C, b * Tn);
+    }
   };
   auto issue_own = [&](int b) {
     if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bar[1]), (uint32_t)(2 * kRowsPerCta * geo.row_bytes));
@@ -318,15 +320,21 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3) k_ln0_bwd_gather(const Ln0G
 }
 
 template <typename T, bool PAIRS>
-cudaError_t launch_typed(const Ln0GatherArgs& a, cudaStream_t st) {
+cudaError_t launch_typed(const Ln0GatherArgs& a, int dtype, cudaStream_t st) {
   constexpr int E = VecN<T>::value;
-  const Ln0Geom g = ln0_geom(a.T, a.D, (int)sizeof(T));
+  constexpr int es = (int)sizeof(T);
+  const Ln0Geom g = ln0_geom(a.T, a.D, es);
+  // ds1 as [B*T][D]; one box = the stripe of one sample (T rows).
+  CUtensorMap map;
+  if (!make_tensor_map_2d(&map, a.ds1, dtype, (uint64_t)a.D, (uint64_t)a.B * a.T, (uint64_t)a.D * es,
+                          (uint32_t)(g.stripe_pitch / es), (uint32_t)a.T))
+    return cudaErrorInvalidValue;
   auto k = k_ln0_bwd_gather<T, PAIRS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
   if (e != cudaSuccess) return e;
   const int threads = (a.D / E + 31) / 32 * 32;
   const dim3 grid(a.T / kRowsPerCta, (a.B + a.spc - 1) / a.spc);
-  return launch_k(k, grid, dim3(threads), g.smem, st, 1, a);
+  return launch_k(k, grid, dim3(threads), g.smem, st, 1, map, a);
 }
 
 }  // namespace
@@ -341,6 +349,7 @@ bool ln0_bwd_gather_supported(const RowArgs& ra) {
   if ((ra.D / V + 31) / 32 * 32 > kLn0MaxThreads) return false;
   if ((long long)2 * kRowsPerCta * ra.D * e >= (1ll << 20)) return false;  // one mbarrier counts the own rows
   const Ln0Geom g = ln0_geom(ra.T, ra.D, e);
+  if (g.stripe_pitch / e > 256 || ra.T > 256) return false;  // TMA box limits
   return (long long)g.smem <= (long long)max_dynamic_smem_bytes() - 1024;
 }
 
@@ -366,9 +375,9 @@ cudaError_t launch_ln0_bwd_gather(const RowArgs& ra, const void* ds1, const void
   a.C = ra.D / ra.T;
   a.spc = kLn0SamplesPerCta;
   const bool pairs = a.C % 2 == 0;
-  if (ra.dtype == 0) return pairs ? launch_typed<float, true>(a, st) : launch_typed<float, false>(a, st);
-  if (ra.dtype == 1) return pairs ? launch_typed<bf16, true>(a, st) : launch_typed<bf16, false>(a, st);
-  return pairs ? launch_typed<f16, true>(a, st) : launch_typed<f16, false>(a, st);
+  if (ra.dtype == 0) return pairs ? launch_typed<float, true>(a, 0, st) : launch_typed<float, false>(a, 0, st);
+  if (ra.dtype == 1) return pairs ? launch_typed<bf16, true>(a, 1, st) : launch_typed<bf16, false>(a, 1, st);
+  return pairs ? launch_typed<f16, true>(a, 2, st) : launch_typed<f16, false>(a, 2, st);
 }
 
 }  // namespace rmx
