@@ -346,10 +346,10 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
       mbar_arrive_expect_tx(smem_u32(bar), total);
     }
     __syncwarp();
-    if (lane < kLn01Rows)
-      bulk_g2s(smem_u32(own + (size_t)lane * geo.own_pitch), xb + (size_t)(i0 + lane) * D,
-               (uint32_t)geo.own_pitch, smem_u32(bar));
-    else if (lane == kLn01Rows)
+    // The own rows are consecutive in memory: one copy.
+    if (lane == 0)
+      bulk_g2s(smem_u32(own), xb + (size_t)i0 * D, (uint32_t)(kLn01Rows * geo.own_pitch), smem_u32(bar));
+    else if (lane == 1)
       tma_load_2d(smem_u32(stripe), &stripe_map, smem_u32(bar), i0 * C, b * Tn);
   }
   {

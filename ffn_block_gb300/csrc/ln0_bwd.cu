@@ -175,11 +175,10 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
   auto issue_own = [&](int b) {
     if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bar[1]), (uint32_t)(2 * kRowsPerCta * geo.row_bytes));
     __syncwarp();
-    if (lane < 2 * kRowsPerCta) {
-      const int jl = lane & (kRowsPerCta - 1);
-      const T* src = (lane < kRowsPerCta ? ds1 : xg) + ((size_t)b * Tn + j0 + jl) * D;
-      unsigned char* dst = (lane < kRowsPerCta ? ownd : ownx) + (size_t)jl * geo.row_bytes;
-      bulk_g2s(smem_u32(dst), src, (uint32_t)geo.row_bytes, smem_u32(&bar[1]));
+    // The eight own rows are consecutive in memory: one copy per tensor.
+    if (lane < 2) {
+      const T* src = (lane == 0 ? ds1 : xg) + ((size_t)b * Tn + j0) * D;
+      bulk_g2s(smem_u32(lane == 0 ? ownd : ownx), src, (uint32_t)(kRowsPerCta * geo.row_bytes), smem_u32(&bar[1]));
     }
   };
 
