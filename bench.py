@@ -114,15 +114,29 @@ def load_peaks() -> tuple[dict, str]:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of every kernel source file: a profile taken on other sources is stale."""
+# Source file of each kernel (besides the headers every kernel includes).
+KERNEL_SOURCES = {
+    "gemm": "gemm_tc.cu", "gate_bwd": "gate_bwd.cu", "ln01_fwd": "ln01_fwd.cu", "ln0_bwd_gather": "ln0_bwd.cu",
+    "ln1_bwd": "ln_bwd.cu", "ln2_bwd": "ln_bwd.cu", "gate_fwd": "rows.cu", "ln2_fwd": "rows.cu", "colsums": "rows.cu",
+}
+SHARED_SOURCES = ("common.cuh", "launch.cuh", "kernels.h")
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the sources a kernel is built from (its file and the shared
+    headers; every kernel file when `kernel` is None or unknown): a profile
+    taken on other sources is stale."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ffn_block_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    key = "gemm" if kernel and kernel.startswith("gemm") else kernel
+    if key in KERNEL_SOURCES:
+        names = sorted({KERNEL_SOURCES[key], *SHARED_SOURCES})
+    else:
+        names = sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -137,7 +151,7 @@ def profiled_traffic(kernel: str, workload: str):
         if ":" in line and line.startswith("- "):
             k, v = line[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_hash") != kernel_source_hash():
+    if fields.get("source_hash") != kernel_source_hash(kernel):
         return None
     try:
         return float(fields["dram_bytes_per_launch"])

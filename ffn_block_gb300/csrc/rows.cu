@@ -21,8 +21,6 @@ namespace rmx {
 
 namespace {
 
-__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
-
 #define RMX_DISPATCH_T(dtype, ...)                 \
   do {                                             \
     if ((dtype) == 0) {                            \
@@ -39,7 +37,6 @@ __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(
 
 inline int elem_bytes(int dtype) { return dtype == 0 ? 4 : 2; }
 inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
-inline int round32(int v) { return (v + 31) / 32 * 32; }
 
 
 // -------------------------------------------------------------------------
@@ -222,18 +219,13 @@ __global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* 
 // then streams the row: lane l owns the 16-byte vectors l, l+32, ... of both
 // halves.
 // =========================================================================
-template <typename T>
-__global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
-                                                  float* __restrict__ muU, float* __restrict__ rU,
-                                                  float* __restrict__ muG, float* __restrict__ rG,
-                                                  const T* __restrict__ wx, const T* __restrict__ bx,
-                                                  const T* __restrict__ wg, const T* __restrict__ bg,
-                                                  T* __restrict__ hidden, int N, int H, float eps) {
-  pdl_enter();
-  constexpr int V = VecN<T>::value;
+// Row r's statistics of U and G from its group statistics (every lane of
+// the warp ends with the same bits); lane 0 writes them for the backward.
+__device__ __forceinline__ void gate_row_stats(const float* __restrict__ zstats, long long r, int H, float eps,
+                                               float* __restrict__ muU, float* __restrict__ rU,
+                                               float* __restrict__ muG, float* __restrict__ rG, float& sU,
+                                               float& cU, float& sG, float& cG) {
   const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (r >= N) return;
   const int tiles = zstats_tiles(H);
   Moments u = {0.f, 0.f, 0.f}, g = {0.f, 0.f, 0.f};
   for (int j = lane; j < tiles; j += 32) {
@@ -246,23 +238,31 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
   }
   u = warp_merge_moments(u);
   g = warp_merge_moments(g);
-  const float sU = 1.0f / sqrtf(u.m2 / (float)H + eps), sG = 1.0f / sqrtf(g.m2 / (float)H + eps);
+  sU = 1.0f / sqrtf(u.m2 / (float)H + eps);
+  sG = 1.0f / sqrtf(g.m2 / (float)H + eps);
   if (lane == 0) {
     muU[r] = u.mean;
     rU[r] = sU;
     muG[r] = g.mean;
     rG[r] = sG;
   }
-  const float cU = -u.mean * sU, cG = -g.mean * sG;
-  const T* zr = Z + (size_t)r * 2 * H;
-  T* hr = hidden + (size_t)r * H;
+  cU = -u.mean * sU;
+  cG = -g.mean * sG;
+}
+
+// hidden row from the U and G vectors v = lane, lane+32, ... read by `load`.
+template <typename T, typename LoadZ>
+__device__ __forceinline__ void gate_row_out(LoadZ load, const T* __restrict__ wx, const T* __restrict__ bx,
+                                             const T* __restrict__ wg, const T* __restrict__ bg, T* hr, int H,
+                                             float sU, float cU, float sG, float cG) {
+  constexpr int V = VecN<T>::value;
+  const int lane = threadIdx.x & 31;
   const int nv = H / V;
 #pragma unroll 1
   for (int v = lane; v < nv; v += 32) {
     const int h0 = v * V;
     float zu[V], zg[V], fwx[V], fbx[V], fwg[V], fbg[V], o[V];
-    load_vec(zr + h0, zu);
-    load_vec(zr + H + h0, zg);
+    load(h0, zu, zg);
     load_vec(wx + h0, fwx);
     load_vec(bx + h0, fbx);
     load_vec(wg + h0, fwg);
@@ -275,6 +275,25 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
     }
     store_vec(hr + h0, o);
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
+                                                  float* __restrict__ muU, float* __restrict__ rU,
+                                                  float* __restrict__ muG, float* __restrict__ rG,
+                                                  const T* __restrict__ wx, const T* __restrict__ bx,
+                                                  const T* __restrict__ wg, const T* __restrict__ bg,
+                                                  T* __restrict__ hidden, int N, int H, float eps) {
+  pdl_enter();
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= N) return;
+  float sU, cU, sG, cG;
+  gate_row_stats(zstats, r, H, eps, muU, rU, muG, rG, sU, cU, sG, cG);
+  const T* zr = Z + (size_t)r * 2 * H;
+  gate_row_out<T>([&](int h0, float* zu, float* zg) {
+    load_vec(zr + h0, zu);
+    load_vec(zr + H + h0, zg);
+  }, wx, bx, wg, bg, hidden + (size_t)r * H, H, sU, cU, sG, cG);
 }
 
 // =========================================================================
