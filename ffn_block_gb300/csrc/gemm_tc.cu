@@ -82,6 +82,10 @@ struct Params {
   unsigned long long wait_limit_ns;
   float* zstats;  // EPI_BIAS_ZSTATS
   int split, zgroups;
+  // 1: the MN-major operands come through rank-5 maps that lay a stage out as
+  // [K group of 8][64-wide MN chunk][8 K rows][64 MN] (swizzle atoms of the
+  // chunks of one K group adjacent), one TMA copy per operand and stage.
+  int mn_il;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -110,6 +114,23 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// Rank-5 forms of the two copies above (the interleaved MN-major operands).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                 int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
 }
 // shared::cluster address of the variable at `addr` in CTA `rank` of the cluster.
@@ -487,12 +508,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int a_n = a_pieces(m0), b_n = b_pieces(nb0, B_W);
         const uint32_t a_piece = KT::A_MN ? MN_CHUNK_BYTES : A_BYTES;
         const uint32_t b_piece = KT::B_MN ? MN_CHUNK_BYTES : R::B_STAGE;
+        // Bytes of `n` requested pieces: an interleaved MN-major operand comes
+        // as one box of the whole stage (its chunks past M or N zero-filled).
+        auto a_bytes = [&](int n) { return (KT::A_MN && p.mn_il) ? (n > 0 ? (uint32_t)A_BYTES : 0u) : n * a_piece; };
+        auto b_bytes = [&](int n) {
+          return (KT::B_MN && p.mn_il) ? (n > 0 ? (uint32_t)R::B_STAGE : 0u) : n * b_piece;
+        };
         // The even CTA's full barrier counts the bytes of both CTAs.
-        uint32_t tx = a_n * a_piece + b_n * b_piece;
+        uint32_t tx = a_bytes(a_n) + b_bytes(b_n);
         if (PAIR) {
           int g1, m1, n1;
           coords(tile, 1, g1, m1, n1);
-          tx += a_pieces(m1) * a_piece + b_pieces(n0 + B_W, B_W) * b_piece;
+          tx += a_bytes(a_pieces(m1)) + b_bytes(b_pieces(n0 + B_W, B_W));
         }
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % STAGES;
@@ -508,15 +535,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (PAIR) tma_load_3d_pair(dst, map, fb, c0, c1, c2);
             else tma_load_3d(dst, map, fb, c0, c1, c2);
           };
+          auto load5 = [&](uint32_t dst, const CUtensorMap* map, int mn, int k, int gg) {
+            // map {64, 8, MN / 64, K / 8, G}: whole stage from chunk mn / 64, K group k / 8
+            if (PAIR) tma_load_5d_pair(dst, map, fb, 0, 0, mn / 64, k / 8, gg);
+            else tma_load_5d(dst, map, fb, 0, 0, mn / 64, k / 8, gg);
+          };
           const int k0 = kb * BK;
           const uint32_t a_dst = sA + s * A_BYTES, b_dst = sB + s * R::B_STAGE;
           if (!KT::A_MN) {
             if (a_n) load(a_dst, &tmA, k0, g, m0);                                      // map {K, G, M}
+          } else if (p.mn_il) {
+            if (a_n) load5(a_dst, &tmA, m0, k0, g);
           } else {
             for (int c = 0; c < a_n; ++c) load(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + 64 * c, g, k0);  // {M, G, K}
           }
           if (!KT::B_MN) {
             if (b_n) load(b_dst, &tmB, k0, nb0, g);                                     // map {K, N, G}
+          } else if (p.mn_il) {
+            if (b_n) load5(b_dst, &tmB, nb0, k0, g);
           } else {
             for (int c = 0; c < b_n; ++c) {
               if (!KT::B_ACT) load(b_dst + c * MN_CHUNK_BYTES, &tmB, nb0 + 64 * c, k0, g);  // map {N, K, G}
@@ -579,12 +615,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_base = sA + s * A_BYTES, b_base = sB + s * R::B_STAGE;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            // K-major: advance 16 elements (32 bytes) inside the swizzle atom;
-            // MN-major: advance 16 rows of 128 bytes.
-            const uint64_t adesc = KT::A_MN ? sw128_desc(a_base + k * 2048, MN_CHUNK_BYTES, 1024)
-                                            : sw128_desc(a_base + k * 32, 16, 1024);
-            const uint64_t bdesc = KT::B_MN ? sw128_desc(b_base + k * 2048, MN_CHUNK_BYTES, 1024)
-                                            : sw128_desc(b_base + k * 32, 16, 1024);
+            // K-major: advance 16 elements (32 bytes) inside the swizzle atom.
+            // MN-major by chunks: advance 16 rows of 128 bytes; MN atoms one
+            // chunk apart, K groups 1 KB apart.  Interleaved MN-major: advance
+            // two K groups; MN atoms 1 KB apart, K groups (chunks x 1 KB) apart.
+            constexpr uint32_t A_CH = BM / 64, B_CH = (PAIR ? BN / 2 : BN) / 64;
+            const uint64_t adesc =
+                KT::A_MN ? (p.mn_il ? sw128_desc(a_base + k * 2 * A_CH * 1024, 1024, A_CH * 1024)
+                                    : sw128_desc(a_base + k * 2048, MN_CHUNK_BYTES, 1024))
+                         : sw128_desc(a_base + k * 32, 16, 1024);
+            const uint64_t bdesc =
+                KT::B_MN ? (p.mn_il ? sw128_desc(b_base + k * 2 * B_CH * 1024, 1024, B_CH * 1024)
+                                    : sw128_desc(b_base + k * 2048, MN_CHUNK_BYTES, 1024))
+                         : sw128_desc(b_base + k * 32, 16, 1024);
             umma_f16<PAIR>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           if (PAIR) umma_commit_pair(empty_bar(s));
@@ -738,6 +781,26 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t
   return r == CUDA_SUCCESS;
 }
 
+// Rank-5 map of an MN-major operand for the interleaved stage layout:
+// element (mn, k, g) at mn * e + k * k_stride + g * g_stride bytes; dims
+// {64, 8, MN / 64, K / 8, G}, box {64, 8, chunks, 8, 1} (one stage), 128-byte
+// swizzle.  Needs MN % 64 == 0 and K % 8 == 0 (no box reaches past the
+// tensor: K groups past K / 8 and chunks past MN / 64 are out of range and
+// read as zero).
+bool make_map_mn5(CUtensorMap* m, const void* base, int dtype, uint64_t mn, uint64_t k, uint64_t g,
+                  uint64_t k_stride, uint64_t g_stride, uint32_t chunks) {
+  auto enc = encode_fn();
+  if (!enc || mn % 64 || k % 8) return false;
+  cuuint64_t dims[5] = {64, 8, mn / 64, k / 8, g};
+  cuuint64_t strides[4] = {k_stride, 128, 8 * k_stride, g_stride};
+  cuuint32_t box[5] = {64, 8, chunks, BK / 8, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUtensorMapDataType dt = dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(m, dt, 5, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <typename T, int KIND, int EPI, bool PAIR>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const Params& p,
                       cudaStream_t st) {
@@ -808,21 +871,34 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   const bool pair = pairs_on && d.M > BM;
   CUtensorMap ma, mb, mc;
   bool ok = true;
+  const uint32_t b_chunks = (pair ? BN / 2 : BN) / 64;
+  // Interleaved MN-major stages where the extents allow it (make_map_mn5
+  // checks them; else the operand comes as separate 64-wide chunks through
+  // rank-3 maps).
+  bool il = true;
   if (d.kind == GEMM_FWD || d.kind == GEMM_DGRAD) {
     ok &= make_map(&ma, d.A, d.dtype, K, G, M, K * e, G * K * e, BK, 1, BM);          // A [M,G,K]
-    if (d.kind == GEMM_FWD)
-      ok &= make_map(&mb, d.Bm, d.dtype, N, K, G, N * e, K * N * e, 64, BK, 1);      // W [G,K,N]
-    else
+    if (d.kind == GEMM_FWD) {
+      il = il && make_map_mn5(&mb, d.Bm, d.dtype, N, K, G, N * e, K * N * e, b_chunks);  // W [G,K,N]
+      if (!il) ok &= make_map(&mb, d.Bm, d.dtype, N, K, G, N * e, K * N * e, 64, BK, 1);
+    } else {
       ok &= make_map(&mb, d.Bm, d.dtype, K, N, G, K * e, N * K * e, BK, pair ? BN / 2 : BN, 1);  // W [G,N,K]
+    }
   } else {
-    ok &= make_map(&ma, d.A, d.dtype, M, G, K, M * e, G * M * e, 64, 1, BK);          // A [K,G,M]
-    ok &= make_map(&mb, d.Bm, d.dtype, N, G, K, N * e, G * N * e, 64, 1, BK);         // B [K,G,N]
+    il = il && make_map_mn5(&ma, d.A, d.dtype, M, K, G, G * M * e, M * e, BM / 64) &&   // A [K,G,M]
+         make_map_mn5(&mb, d.Bm, d.dtype, N, K, G, G * N * e, N * e, b_chunks);        // B [K,G,N]
+    if (!il) {
+      ok &= make_map(&ma, d.A, d.dtype, M, G, K, M * e, G * M * e, 64, 1, BK);
+      ok &= make_map(&mb, d.Bm, d.dtype, N, G, K, N * e, G * N * e, 64, 1, BK);
+    }
   }
+  if (d.kind == GEMM_DGRAD) il = false;  // no MN-major operand
   // Output boxes of 32 rows x 64 columns, written by the epilogue warps.
   if (d.kind == GEMM_WGRAD) ok &= make_map(&mc, d.C, d.dtype, N, M, G, N * e, M * N * e, 64, 32, 1);  // C [G,M,N]
   else ok &= make_map(&mc, d.C, d.dtype, N, G, M, N * e, G * N * e, 64, 1, 32);                       // C [M,G,N]
   if (!ok) return cudaErrorInvalidValue;
   Params p;
+  p.mn_il = il ? 1 : 0;
   p.M = d.M;
   p.N = d.N;
   p.K = d.K;

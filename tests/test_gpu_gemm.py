@@ -72,6 +72,7 @@ PAIR_SHAPES = [
     (384, 640, 1000, 1),   # 3 M-tiles, long ragged K
     (129, 264, 64, 2),     # 2 M-tiles, second one holds a single row
     (520, 200, 88, 3),     # M-major and N-major tails together
+    (512, 384, 264, 2),    # MN extents multiples of 64: interleaved MN-major stages, ragged K
 ]
 
 
