@@ -217,7 +217,10 @@ __global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* 
 // the lanes merge pairwise in a fixed order, so every lane holds the same
 // bits), writes mean and 1/sqrt(var + eps) of U and G for the backward, and
 // then streams the row: lane l owns the 16-byte vectors l, l+32, ... of both
-// halves.
+// halves.  Each lane's next kGateFwdDepth vectors are in flight through
+// cp.async into a per-warp shared-memory buffer (the first before the
+// statistics merge), which keeps several row loads per warp outstanding
+// without the registers a deeper unroll would take.
 // =========================================================================
 // Row r's statistics of U and G from its group statistics (every lane of
 // the warp ends with the same bits); lane 0 writes them for the backward.
@@ -277,6 +280,16 @@ __device__ __forceinline__ void gate_row_out(LoadZ load, const T* __restrict__ w
   }
 }
 
+// cp.async (16 bytes, bypassing L1) into shared memory and its group waits.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kGateFwdDepth = 3;  // iterations of each lane's Z vectors in flight
+
 template <typename T>
 __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, const float* __restrict__ zstats,
                                                   float* __restrict__ muU, float* __restrict__ rU,
@@ -285,15 +298,54 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
                                                   const T* __restrict__ wg, const T* __restrict__ bg,
                                                   T* __restrict__ hidden, int N, int H, float eps) {
   pdl_enter();
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  constexpr int V = VecN<T>::value;
+  // Per warp: kGateFwdDepth slots x (U, G) x 32 lanes x 16 bytes.
+  __shared__ __align__(16) unsigned char zbuf[8][kGateFwdDepth][2][32 * 16];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = blockIdx.x * (blockDim.x >> 5) + warp;
   if (r >= N) return;
+  const T* zr = Z + (size_t)r * 2 * H;
+  const int nv = H / V;
+  const int iters = nv > lane ? (nv - lane + 31) / 32 : 0;
+  // Each lane copies, and later reads, only its own 16-byte slots.
+  auto fetch = [&](int it) {
+    if (it < iters) {
+      const int h0 = (lane + 32 * it) * V;
+      const int sl = it % kGateFwdDepth;
+      cp_async16(smem_u32(&zbuf[warp][sl][0][lane * 16]), zr + h0);
+      cp_async16(smem_u32(&zbuf[warp][sl][1][lane * 16]), zr + H + h0);
+    }
+    cp_async_commit();  // an empty group keeps the counting uniform
+  };
+#pragma unroll
+  for (int it = 0; it < kGateFwdDepth; ++it) fetch(it);
   float sU, cU, sG, cG;
   gate_row_stats(zstats, r, H, eps, muU, rU, muG, rG, sU, cU, sG, cG);
-  const T* zr = Z + (size_t)r * 2 * H;
-  gate_row_out<T>([&](int h0, float* zu, float* zg) {
-    load_vec(zr + h0, zu);
-    load_vec(zr + H + h0, zg);
-  }, wx, bx, wg, bg, hidden + (size_t)r * H, H, sU, cU, sG, cG);
+  T* hr = hidden + (size_t)r * H;
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+    cp_async_wait<kGateFwdDepth - 1>();  // this iteration's group has landed
+    const int h0 = (lane + 32 * it) * V;
+    const int sl = it % kGateFwdDepth;
+    float zu[V], zg[V], fwx[V], fbx[V], fwg[V], fbg[V], o[V];
+    load_vec(reinterpret_cast<const T*>(&zbuf[warp][sl][0][lane * 16]), zu);
+    load_vec(reinterpret_cast<const T*>(&zbuf[warp][sl][1][lane * 16]), zg);
+    load_vec(wx + h0, fwx);
+    load_vec(bx + h0, fbx);
+    load_vec(wg + h0, fwg);
+    load_vec(bg + h0, fbg);
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      const float uu = fmaf(fmaf(zu[e], sU, cU), fwx[e], fbx[e]);
+      const float gg = fmaf(fmaf(zg[e], sG, cG), fwg[e], fbg[e]);
+      o[e] = uu * (gg * sigmoid_fast(gg));
+    }
+    // Refill the slot just read: its values are consumed above, so this
+    // lane's shared-memory reads of it are complete.
+    fetch(it + kGateFwdDepth);
+    store_vec(hr + h0, o);
+  }
+  cp_async_wait<0>();
 }
 
 // =========================================================================
