@@ -44,7 +44,10 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--impl", choices=["ours", "reference", "unfused"], default="ours",
+                    help="ours; reference = the float64 oracle on the host cores; unfused = a plain PyTorch "
+                         "eager composition of the block on the GPU (the per-op sequence the fused path is "
+                         "compared with for time, memory and DRAM bytes)")
     ap.add_argument("--config", default="c3")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (profiling a smaller case)")
@@ -352,16 +355,20 @@ def run_ours(args) -> dict | None:
     rank, local, ws = dist_setup(args.gpus)
     shape = workload_shape(args)
     arrays = I.make_inputs(shape, seed=I.DEFAULT_SEED + rank)
+    torch.cuda.reset_peak_memory_stats()
     blk = RankMixerDevice(shape, arrays, device=f"cuda:{torch.cuda.current_device()}")
     del arrays
     stream = torch.cuda.current_stream()
-    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
 
     for _ in range(max(args.warmup, 0)):
         blk.step(stream)
     torch.cuda.synchronize()
     B.check(B.rmx_check(stream), "warm-up")
+    memory = {"peak_allocated_bytes": torch.cuda.max_memory_allocated(),
+              "saved_bytes": blk.saved_bytes, "workspace_bytes": blk.ws_bytes,
+              "note": "every device buffer of the step: inputs, outputs, parameters, gradients, saved, scratch"}
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
 
     # Per-kernel breakdown from a separate pass (every launch bracketed by
     # events): it names the dominant kernel.  The timed region below brackets
@@ -390,9 +397,11 @@ def run_ours(args) -> dict | None:
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()                                    # L2 flush, outside the events
+        torch.cuda.nvtx.range_push("rmx_step")
         starts[i].record(stream)
         blk.step(stream)
         ends[i].record(stream)
+        torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(ws)
     wall = time.perf_counter() - wall0
@@ -501,6 +510,7 @@ def run_ours(args) -> dict | None:
         "gpu_launches": launches,
         "wall_s": wall,
         "samples_ms": samples,
+        "memory": memory,
         "kernels": kernels,
         "kernels_note": "per-kernel times from a separate pass with every launch bracketed by events; "
                         "the timed region brackets only the dominant kernel (ms_per_launch_timed_region)",
@@ -536,13 +546,82 @@ def run_reference(args) -> dict | None:
     }
 
 
+def unfused_forward_backward(x, dy, p):
+    """The block as a plain PyTorch eager composition (one op per step of the
+    page's "Exact computation" section, autograd for the backward): the
+    unfused per-op sequence the fused path is compared with.  x, dy [B,T,D]
+    and the parameters in their page layouts, all on one device and dtype.
+    Returns y, dx and the parameter gradients."""
+    import torch
+    import torch.nn.functional as F
+    B_, T, D = x.shape
+    H = p["lnx_w"].shape[0]
+    C = D // T
+    x = x.detach().requires_grad_(True)
+    q = {k: v.detach().requires_grad_(True) for k, v in p.items()}
+    a0 = F.layer_norm(x, (D,), q["gamma0"], q["beta0"], 1e-3)
+    mixed = a0.reshape(B_, T, T, C).transpose(1, 2).reshape(B_, T, D)      # swap the two T axes
+    out1 = F.layer_norm(mixed + x, (D,), q["gamma1"], q["beta1"], 1e-3)
+    Z = torch.baddbmm(q["b1"].unsqueeze(1), out1.transpose(0, 1), q["w1"])  # [T, B, 2H]
+    U, G = Z.split(H, dim=-1)
+    hidden = F.layer_norm(U, (H,), q["lnx_w"], q["lnx_b"], 1e-5) * F.silu(
+        F.layer_norm(G, (H,), q["lng_w"], q["lng_b"], 1e-5))
+    out2 = torch.baddbmm(q["bout"].unsqueeze(1), hidden, q["wout"])        # [T, B, D]
+    y = F.layer_norm(out1 + out2.transpose(0, 1), (D,), q["gamma2"], q["beta2"], 1e-3)
+    y.backward(dy)
+    return y.detach(), x.grad, {k: v.grad for k, v in q.items()}
+
+
+def run_unfused(args) -> dict | None:
+    import numpy as np
+    import torch
+
+    from ffn_block_gb300 import inputs as I
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    shape = workload_shape(args)
+    arrays = I.make_inputs(shape, seed=I.DEFAULT_SEED)
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[shape.dtype]
+    dev = torch.device("cuda")
+    torch.cuda.reset_peak_memory_stats()
+    x = torch.from_numpy(np.ascontiguousarray(arrays["x"], dtype=np.float32)).to(dev, dt)
+    dy = torch.from_numpy(np.ascontiguousarray(arrays["dy"], dtype=np.float32)).to(dev, dt)
+    p = {k: torch.from_numpy(np.ascontiguousarray(arrays[k], dtype=np.float32)).to(dev, dt) for k in I.PARAM_NAMES}
+    del arrays
+    for _ in range(max(args.warmup, 0)):
+        unfused_forward_backward(x, dy, p)
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stream = torch.cuda.current_stream()
+    for i in range(args.steps):
+        flush.zero_()
+        torch.cuda.nvtx.range_push("rmx_step")
+        starts[i].record(stream)
+        unfused_forward_backward(x, dy, p)
+        ends[i].record(stream)
+        torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    rows = shape.B * shape.T
+    return {"impl": "unfused", "metric": METRIC, "value": rows / (ms / 1e3), "unit": "rows/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": shape.dtype, "data": "synthetic (the same seeded inputs as the fused path)",
+            "config": {"workload": workload_name(args, shape), "B": shape.B, "T": shape.T, "D": shape.D,
+                       "H": shape.H, "storage": shape.dtype},
+            "memory": {"peak_allocated_bytes": peak}}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.oracle_worker:
         oracle_worker(args)
         return
-    if args.impl == "reference":
-        line = run_reference(args)
+    if args.impl in ("reference", "unfused"):
+        line = run_reference(args) if args.impl == "reference" else run_unfused(args)
         if line is not None:
             print(json.dumps(line), flush=True)
         return

@@ -78,9 +78,11 @@ constexpr int kColsumJobs = 12;
 
 // Rows per CTA (at most max_rows) for a grid of T x ceil(B / nb) CTAs of
 // which `slots` are resident at once: the one with the shortest estimated
-// run, (waves, rounded up) x nb; among equals the largest nb (fewer CTAs and
-// partial rows).  A grid that is a whole number of waves wastes no tail.
-int rows_per_cta(int B, int T, int slots, int max_rows) {
+// run, (waves, rounded up) x (nb + overhead), where `overhead` is a CTA's
+// fixed cost in rows (its prologue, ring fill and partial-sum writes); among
+// equals the largest nb (fewer CTAs and partial rows).  A grid that is a
+// whole number of waves wastes no tail.
+int rows_per_cta(int B, int T, int slots, int max_rows, int overhead) {
   if (B <= 0) return 1;
   if (slots < 1) slots = 1;
   int best = 1;
@@ -88,7 +90,7 @@ int rows_per_cta(int B, int T, int slots, int max_rows) {
   for (int nb = max_rows < B ? max_rows : B; nb >= 1; --nb) {
     const long long blocks = (B + nb - 1) / nb;
     const long long waves = ((long long)T * blocks + slots - 1) / slots;
-    const long long cost = waves * nb;
+    const long long cost = waves * (nb + overhead);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = nb;
@@ -119,10 +121,13 @@ Layout layout_of(const rmx_config& c) {
   L.ra.dtype = c.dtype;
   // Rows per CTA of the per-token row passes (grid T x ceil(B / nb)).
   const int sms = c.B > 0 ? sm_count() : 1;
-  const int nb = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? gate_bwd_ctas_per_sm(L.ra) : 1), kGateBwdMaxRows);
+  // A gate CTA also loads the four weight vectors and writes six column
+  // partials of H floats (about eight rows' worth of traffic); a LayerNorm
+  // ring CTA's fixed cost is small next to its rows.
+  const int nb = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? gate_bwd_ctas_per_sm(L.ra) : 1), kGateBwdMaxRows, 8);
   L.ra.nb = nb;
   L.ra.nbblk = c.B > 0 ? (c.B + nb - 1) / nb : 0;
-  const int nbl = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? ln_bwd_ctas_per_sm(L.ra) : 1), kLnBwdMaxRows);
+  const int nbl = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? ln_bwd_ctas_per_sm(L.ra) : 1), kLnBwdMaxRows, 0);
   L.ra.nb_ln = nbl;
   L.ra.nbblk_ln = c.B > 0 ? (c.B + nbl - 1) / nbl : 0;
   const size_t P = (size_t)L.ra.nbblk * c.T;     // gate-backward partial rows
@@ -131,11 +136,14 @@ Layout layout_of(const rmx_config& c) {
 
   o = 0;
   L.ds2 = o; o = up(o + N * D * e);
-  L.dh = o; o = up(o + N * H * e);
+  // dh, then (once the gate backward has consumed it) dout1, then ds1 in
+  // place of dout1 (norm1's backward reads each row before writing it).
+  L.dh = o; o = up(o + N * (H > D ? H : D) * e);
+  L.dout1 = L.dh;
+  L.ds1 = L.dh;
   L.dZ = o; o = up(o + N * 2 * H * e);
-  L.dout1 = o; o = up(o + N * D * e);
-  L.ds1 = o; o = up(o + N * D * e);
-  L.da0 = o; o = up(o + N * D * e);
+  L.da0 = o;  // token_mix(ds1): only when norm0's backward cannot gather it
+  if (!ln0_bwd_gather_supported(L.ra)) o = up(o + N * D * e);
   L.pg2 = o; o = up(o + PL * D * sizeof(float));
   L.pb2 = o; o = up(o + PL * D * sizeof(float));
   L.pbo = o; o = up(o + PL * D * sizeof(float));
