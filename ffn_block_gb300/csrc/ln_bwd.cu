@@ -32,22 +32,6 @@ namespace {
 constexpr int kLnMaxStages = 8;
 constexpr int kLnSmemTarget = 52 * 1024;  // about four CTAs per SM
 
-// Sums v[0..1] over a warp with five shuffles: on return lane l holds the
-// sum of component bit4(l); lanes holding the same component hold the same
-// bits.
-__device__ __forceinline__ float warp_sum2_transposed(float v0, float v1) {
-  const int lane = threadIdx.x & 31;
-  const bool hi = lane & 16;
-  float k = hi ? v1 : v0;
-  const float s = hi ? v0 : v1;
-  k += __shfl_xor_sync(0xffffffffu, s, 16);
-  k += __shfl_xor_sync(0xffffffffu, k, 8);
-  k += __shfl_xor_sync(0xffffffffu, k, 4);
-  k += __shfl_xor_sync(0xffffffffu, k, 2);
-  k += __shfl_xor_sync(0xffffffffu, k, 1);
-  return k;
-}
-
 // Sums v[0..3] over a warp with six shuffles: on return lane l holds the sum
 // of component 2 * bit4(l) + bit3(l); lanes holding the same component hold
 // the same bits.

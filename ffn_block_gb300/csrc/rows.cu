@@ -253,33 +253,6 @@ __device__ __forceinline__ void gate_row_stats(const float* __restrict__ zstats,
   cG = -g.mean * sG;
 }
 
-// hidden row from the U and G vectors v = lane, lane+32, ... read by `load`.
-template <typename T, typename LoadZ>
-__device__ __forceinline__ void gate_row_out(LoadZ load, const T* __restrict__ wx, const T* __restrict__ bx,
-                                             const T* __restrict__ wg, const T* __restrict__ bg, T* hr, int H,
-                                             float sU, float cU, float sG, float cG) {
-  constexpr int V = VecN<T>::value;
-  const int lane = threadIdx.x & 31;
-  const int nv = H / V;
-#pragma unroll 1
-  for (int v = lane; v < nv; v += 32) {
-    const int h0 = v * V;
-    float zu[V], zg[V], fwx[V], fbx[V], fwg[V], fbg[V], o[V];
-    load(h0, zu, zg);
-    load_vec(wx + h0, fwx);
-    load_vec(bx + h0, fbx);
-    load_vec(wg + h0, fwg);
-    load_vec(bg + h0, fbg);
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      const float uu = fmaf(fmaf(zu[e], sU, cU), fwx[e], fbx[e]);
-      const float gg = fmaf(fmaf(zg[e], sG, cG), fwg[e], fbg[e]);
-      o[e] = uu * (gg * sigmoid_fast(gg));
-    }
-    store_vec(hr + h0, o);
-  }
-}
-
 // cp.async (16 bytes, bypassing L1) into shared memory and its group waits.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
