@@ -190,7 +190,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
                  "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -388,7 +388,13 @@ def run_ours(args) -> dict | None:
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(gpu_selector(torch.cuda.current_device()))
     sampler.start()
-    time.sleep(0.3)
+    # Keep the GPU under load while the sampler starts (about half a second of
+    # untimed steps), so that the clock samples around the short timed region
+    # are taken at work, not idle.
+    soak_end = time.perf_counter() + 0.5
+    while time.perf_counter() < soak_end:
+        blk.step(stream)
+        torch.cuda.synchronize()
     launches0 = B.rmx_launch_count()
     B.rmx_profile_select(dom)
     B.rmx_profile_enable(True)
