@@ -7,28 +7,33 @@
 // their backward, for 16-bit storage (bf16 or fp16) with fp32 accumulation.
 //
 // Design (one CTA per SM, persistent over tiles):
-//   warp 0     TMA producer: loads 128x64 A and 256x64 B tiles into a
-//              4-stage shared-memory ring (128-byte swizzle), signalling
-//              `full` mbarriers with the transaction byte count;
-//   warp 1     allocates 512 TMEM columns and issues tcgen05.mma
-//              (M=128, N=256, K=16) from one thread; each stage is released
-//              back to the producer by tcgen05.commit on its `empty` barrier;
-//              the accumulator alternates between two 256-column TMEM halves
-//              so the epilogue of tile i overlaps the main loop of tile i+1;
+//   warp 0     TMA producer: loads each k-block's A and B slices into a
+//              shared-memory ring (128-byte swizzle): six stages of 32 KB
+//              for a CTA pair, four of 48 KB for a CTA alone; the `full`
+//              mbarriers count the bytes;
+//   warp 1     allocates 512 TMEM columns; one thread issues tcgen05.mma
+//              (kind::f16, K=16); each stage goes back to the producer by
+//              tcgen05.commit on its `empty` barrier; the accumulator
+//              alternates between two 256-column TMEM halves so the epilogue
+//              of tile i overlaps the main loop of tile i+1;
 //   warps 2-9  epilogue: two warps per TMEM lane quarter, each draining half
-//              of the tile's columns with tcgen05.ld (32 lanes x 32 columns at
-//              a time); bias / residual in fp32, rounding, store.
-// Paired mode (M spans at least two tiles): a cluster of two CTAs computes
-// the two M-adjacent tiles that share one B tile.  Each CTA loads its own A
-// tile and half of the B tile, multicasting that half into both CTAs' shared
-// memory, so L2 delivers 32 KB instead of 48 KB per CTA and k-block; each MMA
-// completion is signalled to the `empty` barriers of both CTAs, so a stage is
-// refilled only when both have consumed it.
-// Operands are addressed through rank-3 tensor maps so that per-token slices
-// of [B,T,X] activations and [T,X,Y] weights need no copies; K-major and
+//              of the tile's columns 64 at a time (tcgen05.ld), releasing the
+//              accumulator after its last load, applying bias / residual /
+//              Z statistics in fp32 and writing 32x64 boxes through a
+//              swizzled staging buffer with TMA stores.
+// Paired mode (M spans at least two 128-row tiles): a cluster of two CTAs
+// owns a 256x256 output tile.  The even CTA issues
+// tcgen05.mma.cta_group::2 (M=256, N=256) over A split by rows and B split by
+// columns between the two CTAs' shared memory; the odd CTA's copies count
+// their bytes on the even CTA's `full` barrier, and the even CTA's commits
+// are multicast to both CTAs' barriers.
+// Operands are addressed through tensor maps so that per-token slices of
+// [B,T,X] activations and [T,X,Y] weights need no copies; K-major and
 // MN-major shared-memory layouts cover the NN (forward), NT (dgrad) and TN
-// (wgrad) cases without transposes.  TMA zero-fills out-of-range rows and
-// columns, so ragged M, N and K need no special path.
+// (wgrad) cases without transposes.  An MN-major operand whose MN extent is a
+// multiple of 64 comes through a rank-5 map that stages the 1 KB swizzle
+// atoms of one K group next to each other (see Params::mn_il).  TMA zero-fills
+// out-of-range rows and columns, so ragged M, N and K need no special path.
 //
 // Every mbarrier wait is bounded (common.cuh); on expiry the kernel records
 // an error bit, drains what it has in flight and frees its TMEM.
