@@ -37,15 +37,19 @@ namespace rmx {
 __device__ unsigned int g_rmx_error_word;
 
 unsigned int* device_error_word() {
-  static unsigned int* addr[64] = {nullptr};
+  // Per-device address, cached; several host threads may look it up at once
+  // (they all store the same value).
+  static std::atomic<unsigned int*> addr[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
+  unsigned int* a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_rmx_error_word) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<unsigned int*>(p);
+    a = static_cast<unsigned int*>(p);
+    addr[dev].store(a, std::memory_order_release);
   }
-  return addr[dev];
+  return a;
 }
 
 namespace {

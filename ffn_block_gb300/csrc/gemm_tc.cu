@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <type_traits>
 
@@ -573,8 +574,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = first_j; j < it; ++j)
           mbar_wait_bounded(empty_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, p.wait_limit_ns, p.err,
                             ERRBIT_WAIT_DRAIN, abort_flag);
-      } else if (!PAIR) {
-        // Let the copies already issued land before the CTA can exit.
+      } else if (!PAIR || rank == 0) {
+        // Let the copies already issued land before the CTA can exit.  A
+        // pair's full barriers live in the even CTA and count the bytes of
+        // both CTAs, so the even CTA's drain also covers the odd CTA's copies
+        // of every stage it had armed; the pair's final cluster barrier keeps
+        // the odd CTA alive until then.
         const int first_j = it > STAGES ? it - STAGES : 0;
         for (int j = first_j; j < it; ++j) {
           volatile int no_abort = 0;
@@ -582,8 +587,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             ERRBIT_WAIT_DRAIN, &no_abort);
         }
       } else {
-        // A pair's copies are counted on the even CTA's barriers: give the
-        // ones in flight a fixed, ample time to land.
+        // The odd CTA of a pair has no barrier of its own to wait on: copies
+        // of a stage the even CTA never armed get a fixed, ample time to land.
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 200000ull) {
         }
@@ -839,15 +844,17 @@ cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorM
 }  // namespace
 
 int sm_count() {
-  static int n[64] = {0};
+  static std::atomic<int> n[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (n[dev] == 0) {
+  int c = n[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n[dev] = v > 0 ? v : 1;
+    c = v > 0 ? v : 1;
+    n[dev].store(c, std::memory_order_relaxed);
   }
-  return n[dev];
+  return c;
 }
 
 bool gemm_tc_supported(const GemmDesc& d) {

@@ -16,6 +16,8 @@
 // real address with cudaGetSymbolAddress while that device is current, and
 // every launch receives that pointer.
 
+#include <atomic>
+
 #include "../../include/rmx.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -29,19 +31,24 @@ constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
 constexpr int kMaxDevices = 64;
-float* g_scratch_ptr[kMaxDevices] = {nullptr};
+// Cached device address per device.  Atomic because host threads may make
+// their first call on the same device at the same time; they look up (and
+// store) the same address, so whichever store lands is correct.
+std::atomic<float*> g_scratch_ptr[kMaxDevices];
 
 // Device address of the scratch array on the current device (looked up once
 // per device).  Returns nullptr if the lookup fails.
 float* scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_scratch_ptr[dev]) {
+  float* cached = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!cached) {
     float* p = nullptr;
     if (cudaGetSymbolAddress((void**)&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
+    cached = p;
   }
-  return g_scratch_ptr[dev];
+  return cached;
 }
 
 bool ok16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

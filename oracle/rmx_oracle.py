@@ -11,19 +11,25 @@ per-token contractions).  The backward is the chain rule applied by hand to
 the same steps; there is no fusion, blocking or reordering beyond what the
 definitions state.
 
-Readings taken where the page leaves a step open (each is listed with its
-reason in the design notes):
-  R1  (U, G) = split of Z into two H-wide halves, U the first half.
+Readings taken where the page leaves a step open (each the plainest one that
+the rest of the page supports):
+  R1  (U, G) = split of Z into two H-wide halves, U the first half (the
+      order in which a split along the last axis returns its pieces).
   R2  the outer LayerNorms use the same biased-variance formula as the
-      page's LN(z), with epsilon inside the square root.
-  R3  norm1's residual is the raw block input, norm2's residual is out1.
-  R4  H = k * D.
-  R5  silu(g) = g * sigmoid(g), exact.
+      page's LN(z), with epsilon inside the square root (the page names only
+      their epsilon, 1e-3).
+  R3  norm1's residual is the raw block input (the page writes
+      norm1(out1 + inputs)); norm2's residual is out1 (norm2(out1 + out2)).
+  R4  H = k * D (the page's shape line pairs D=1280 and k=2 with H=2560).
+  R5  silu(g) = g * sigmoid(g), exact (no approximation is named).
   R6  parameter gradients are summed over every row that used the parameter:
       w1, b1, wout, bout over the batch b for their own token t; every
-      gamma/beta and inner weight/bias over all B*T rows.
-  R7  the token-mixing backward is the same permutation (it is an
-      involution).
+      gamma/beta and inner weight/bias over all B*T rows (each token has its
+      own w1[t], b1[t], wout[t], bout[t]; the LayerNorm parameters are one
+      vector shared by all rows).
+  R7  the token-mixing backward is the same permutation (swapping the two T
+      axes twice gives the identity, so the swap is its own inverse and its
+      transpose).
 
 Parity pins (tests/test_oracle.py): the page's token-mixing worked example,
 the involution, the D == T transpose special case, LayerNorm invariants,
@@ -36,8 +42,8 @@ from __future__ import annotations
 
 import numpy as np
 
-EPS_OUTER = 1e-3   # norm0, norm1, norm2 ("LayerNorm with epsilon=1e-3")
-EPS_INNER = 1e-5   # norm_x, norm_gate ("PyTorch LayerNorm with epsilon=1e-5")
+EPS_OUTER = 1e-3   # norm0, norm1, norm2: the outer LayerNorms' epsilon on the page
+EPS_INNER = 1e-5   # norm_x, norm_gate: the inner LayerNorms' epsilon on the page
 
 
 # ---------------------------------------------------------------------------

@@ -34,6 +34,29 @@ def oracle_outputs(arrays: dict, samples=None) -> dict:
     return out
 
 
+def oracle_outputs_chunked(arrays: dict, chunk: int = 128) -> dict:
+    """Oracle y, dx and gradients of the whole batch, run on consecutive
+    chunks of samples to bound host memory.  Exact decomposition: y and dx of
+    a sample depend only on that sample, and every parameter gradient is a
+    sum over samples, so the chunks' gradients are summed (in float64)."""
+    a = I.to_float64(arrays)
+    p = {k: a[k] for k in I.PARAM_NAMES}
+    B = a["x"].shape[0]
+    ys, dxs, tot = [], [], None
+    for b0 in range(0, B, chunk):
+        y, dx, grads = O.forward_backward(a["x"][b0:b0 + chunk], a["dy"][b0:b0 + chunk], p)
+        ys.append(y)
+        dxs.append(dx)
+        if tot is None:
+            tot = {k: v.copy() for k, v in grads.items()}
+        else:
+            for k, v in grads.items():
+                tot[k] += v
+    out = {"y": np.concatenate(ys), "dx": np.concatenate(dxs)}
+    out.update(tot)
+    return out
+
+
 def compare(gpu: dict, ref: dict, tol: float, names=NAMES) -> dict:
     errs = {}
     for n in names:

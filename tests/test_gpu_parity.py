@@ -12,7 +12,7 @@ from ffn_block_gb300 import inputs as I
 from ffn_block_gb300.device import RankMixerDevice
 
 from oracle import rmx_oracle as O
-from parity_util import NAMES, TOL, compare, oracle_outputs
+from parity_util import NAMES, TOL, compare, oracle_outputs, oracle_outputs_chunked
 
 pytestmark = pytest.mark.gpu
 
@@ -134,3 +134,22 @@ def test_full_size_all_gradients_sparse_dy(name):
     compare(sub, ref, TOL[shape.dtype], names=NAMES)
     rest = np.setdiff1d(np.arange(shape.B), S)
     assert np.all(got["dx"][rest] == 0.0)
+
+
+# Dense dy over the whole production batch: every weight-gradient GEMM
+# reduces over all B samples (K = B) and the column sums run over every
+# partial row, with nothing zeroed.  The oracle runs the whole batch in
+# chunks of samples (exact: gradients are sums over samples).  Largest fp16
+# value is 65504; no gradient may come near it.
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["c4", "c3"])
+def test_full_size_dense_dy_all_gradients(name):
+    shape = I.shape_of(name)
+    arrays = I.make_inputs(shape)
+    got = _gpu(shape, arrays)
+    ref = oracle_outputs_chunked(arrays)
+    del arrays
+    compare(got, ref, TOL[shape.dtype], names=NAMES)
+    if shape.dtype == "f16":
+        for n in NAMES:
+            assert np.abs(got[n]).max() < 6.0e4, (n, float(np.abs(got[n]).max()))

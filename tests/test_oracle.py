@@ -333,3 +333,17 @@ def test_pins_catch_planted_mistakes(target, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught > 0, f"no pin caught the planted mistake in {name}"
+
+
+def test_chunked_oracle_equals_whole_batch():
+    # The full-batch parity test runs the oracle on chunks of samples and sums
+    # the parameter gradients; that must equal one call on the whole batch.
+    import sys, os
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from parity_util import oracle_outputs, oracle_outputs_chunked
+    shape = I.Shape(B=5, T=4, D=16, H=32, dtype="f32")
+    arrays = I.make_inputs(shape, ln_params="random")
+    whole = oracle_outputs(arrays)
+    parts = oracle_outputs_chunked(arrays, chunk=2)
+    for k, v in whole.items():
+        np.testing.assert_allclose(parts[k], v, rtol=1e-12, atol=1e-12 * max(1.0, np.abs(v).max()))
