@@ -90,6 +90,68 @@ __device__ __forceinline__ void store_n(T* p, const float* v) {
   }
 }
 
+// ---------------------------------------------------------------- packed pairs
+// Eight consecutive elements of T as four float2 pairs (element 2k in .x,
+// 2k+1 in .y), for the packed fp32x2 arithmetic of sm_100+ (__ffma2_rn,
+// __fadd2_rn, __fmul2_rn: each component rounds exactly as the scalar
+// operation does, so a pair costs one instruction and changes no result).
+// 16-bit types: one 16-byte access; float: two.  p must be 16-byte aligned.
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+  // bf16 is the top half of an fp32: shifting into place is exact.
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <typename T> __device__ __forceinline__ void ld8(const T* p, float2 (&v)[4]);
+template <> __device__ __forceinline__ void ld8<bf16>(const bf16* p, float2 (&v)[4]) {
+  const uint4 r = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16x2_to_f2(r.x);
+  v[1] = bf16x2_to_f2(r.y);
+  v[2] = bf16x2_to_f2(r.z);
+  v[3] = bf16x2_to_f2(r.w);
+}
+template <> __device__ __forceinline__ void ld8<f16>(const f16* p, float2 (&v)[4]) {
+  const uint4 r = *reinterpret_cast<const uint4*>(p);
+  const __half2* h = reinterpret_cast<const __half2*>(&r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = __half22float2(h[k]);
+}
+template <> __device__ __forceinline__ void ld8<float>(const float* p, float2 (&v)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = make_float2(a.x, a.y);
+  v[1] = make_float2(a.z, a.w);
+  v[2] = make_float2(b.x, b.y);
+  v[3] = make_float2(b.z, b.w);
+}
+template <typename T> __device__ __forceinline__ void st8(T* p, const float2 (&v)[4]);
+template <> __device__ __forceinline__ void st8<bf16>(bf16* p, const float2 (&v)[4]) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[k].x, v[k].y);
+    w[k] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = r;
+}
+template <> __device__ __forceinline__ void st8<f16>(f16* p, const float2 (&v)[4]) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __half2 h = __floats2half2_rn(v[k].x, v[k].y);
+    w[k] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = r;
+}
+template <> __device__ __forceinline__ void st8<float>(float* p, const float2 (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+}
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
 // Logistic function 1 / (1 + e^-g), with e^-g = 2^(-g * log2(e)) (change of
 // base) on the hardware's base-2 exponential and its reciprocal, both the
 // flush-to-zero approximations of the PTX ISA (ex2.approx.ftz,
@@ -101,6 +163,19 @@ __device__ __forceinline__ float sigmoid_fast(float g) {
   float e, r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -kLog2e));
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return r;
+}
+
+// The same function on a pair (identical results, component by component).
+__device__ __forceinline__ float2 sigmoid_fast2(float2 g) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float2 a = mul2(g, f2(-kLog2e));
+  float2 e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(a.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(a.y));
+  const float2 d = add2(f2(1.0f), e);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(d.y));
   return r;
 }
 

@@ -11,13 +11,15 @@
 //   db1[t] += dZ.
 //
 // One CTA owns the rows b0 <= b < b1 of one token t and every column: thread
-// j holds the j-th 16-byte vector of columns of both halves.  The dh and Z
-// rows stream into shared memory through an S-stage ring of bulk copies (one
-// thread issues them; a byte-counting mbarrier per stage says when a row has
-// landed).  R rows at a time (two when the weights stay in registers) the
-// CTA takes their 4R row sums with one barrier, then every thread finishes
-// its own columns from registers, writes dZ and keeps the column partial sums
-// in registers.  dh and Z are read from HBM once; every wait is bounded.
+// j holds columns 8j ... 8j + 7 of both halves.  The dh and Z rows stream
+// into shared memory through an S-stage ring of bulk copies (one thread
+// issues them; a byte-counting mbarrier per stage says when a row has
+// landed).  Two rows at a time the CTA takes their eight row sums with one
+// barrier, then every thread finishes its own columns from registers, writes
+// dZ and keeps the column partial sums in registers.  The element math runs
+// on column pairs with the packed fp32x2 instructions (the same roundings as
+// scalar fp32, half the instructions).  dh and Z are read from HBM once;
+// every wait is bounded.
 
 #include <map>
 #include <mutex>
@@ -82,29 +84,24 @@ struct GateBwdArgs {
   int B, T, H, nb, stages;
 };
 
-// Loads E consecutive floats from 16-byte aligned shared memory.
-template <int E>
-__device__ __forceinline__ void lds_f32(const float* p, float* v) {
-#pragma unroll
-  for (int k = 0; k < E; k += 4) {
-    const float4 q = *reinterpret_cast<const float4*>(p + k);
-    v[k] = q.x;
-    v[k + 1] = q.y;
-    v[k + 2] = q.z;
-    v[k + 3] = q.w;
-  }
-}
-
-// Shared memory: stats [nb] float4 | red [2][8][32] float | weights [4][H]
-// float | stages x (dh row | Z row) | mbarriers.  Thread `tid` owns the
-// 16-byte vector of columns c0 = tid * E ... c0 + E - 1 of both halves.
+// Shared memory: stats [nb] float4 | red [2][16][8] float | weights [4][H]
+// float (only when they do not stay in registers) | stages x (dh row | Z
+// row) | mbarriers.  Thread `tid` owns the eight columns c0 = 8 * tid ...
+// c0 + 7 of both halves (one 16-byte vector of a 16-bit type, two of
+// float), as four pairs for the packed fp32x2 arithmetic.
 // WREG: the thread's weights stay in registers (one CTA per SM leaves room
-// for them when the CTA has at most 320 threads, with two rows per step).
+// for them when the CTA has at most 320 threads).  Register caps: each of
+// the SM's four schedulers holds its warps' registers in its own quarter of
+// the register file (16384), so a CTA of 10 warps (3 on some scheduler) may
+// use at most 168 per thread, one of up to 16 warps at most 128.
+constexpr int kGateE = 8;             // columns per thread and half
+constexpr int kGateMaxThreads = 480;  // H up to 3840 (k = 3 at D = 1280)
+constexpr int kGateRedWarps = 16;     // reduction buffer rows (at least kGateMaxThreads / 32)
+
 template <typename T, bool WREG>
-__global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdArgs a) {
+__global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
   pdl_enter();
-  constexpr int E = VecN<T>::value;
-  constexpr int R = WREG ? 2 : 1;  // rows per barrier
+  constexpr int R = 2;             // rows per barrier
   constexpr int NS = 4 * R;        // row sums per barrier
   constexpr int LPS = 32 / NS;     // lanes holding one sum after the warp reduction
   extern __shared__ __align__(16) unsigned char smem[];
@@ -114,13 +111,13 @@ __global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdA
   const int nrows = min(a.B, b0 + a.nb) - b0;
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31, nw = nthreads >> 5;
-  const int c0 = tid * E;
+  const int c0 = tid * kGateE;
   const bool active = c0 < H;
 
   float4* st_row = reinterpret_cast<float4*>(smem);                  // (rU, -mU*rU, rG, -mG*rG) per row
-  float* red = reinterpret_cast<float*>(smem + (size_t)a.nb * 16);   // [2][8][32]
-  float* wsm = red + 2 * 8 * 32;                                     // [4][H]
-  unsigned char* ring = reinterpret_cast<unsigned char*>(wsm + 4 * (size_t)H);
+  float* red = reinterpret_cast<float*>(smem + (size_t)a.nb * 16);   // [2][16 warps][NS]
+  float* wsm = red + 2 * kGateRedWarps * NS;                         // [4][H] (not WREG)
+  unsigned char* ring = reinterpret_cast<unsigned char*>(wsm + (WREG ? 0 : 4 * (size_t)H));
   const size_t row_bytes = (size_t)3 * H * sizeof(T);
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)S * row_bytes);
   __shared__ int abort_flag;
@@ -144,32 +141,31 @@ __global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdA
   __syncthreads();
   if (tid == 0)
     for (int i = 0; i < min(S, nrows); ++i) issue(i, i);
-  // Per-row statistics and the four weight vectors (as float) while the
-  // first rows are in flight.
+  // Per-row statistics and the weights while the first rows are in flight.
   for (int i = tid; i < nrows; i += nthreads) {
     const size_t r = (size_t)(b0 + i) * a.T + t;
     const float sU = a.rU[r], sG = a.rG[r];
     st_row[i] = make_float4(sU, -a.muU[r] * sU, sG, -a.muG[r] * sG);
   }
-  {
-    const T* w[4] = {reinterpret_cast<const T*>(a.wx), reinterpret_cast<const T*>(a.bx),
-                     reinterpret_cast<const T*>(a.wg), reinterpret_cast<const T*>(a.bg)};
+  const T* wp[4] = {reinterpret_cast<const T*>(a.wx), reinterpret_cast<const T*>(a.bx),
+                    reinterpret_cast<const T*>(a.wg), reinterpret_cast<const T*>(a.bg)};
+  float2 rw[WREG ? 4 : 1][4];
+  if (WREG) {
+    if (active) {
+#pragma unroll
+      for (int k = 0; k < (WREG ? 4 : 1); ++k) ld8<T>(wp[k] + c0, rw[k]);
+    }
+  } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      for (int c = tid; c < H; c += nthreads) wsm[k * H + c] = to_f(w[k][c]);
+      for (int c = tid; c < H; c += nthreads) wsm[k * H + c] = to_f(wp[k][c]);
   }
   __syncthreads();
 
-  float awx[E], abx[E], awg[E], abg[E], a1u[E], a1g[E];
+  // Column partial sums of dwx, dbx, dwg, dbg and db1 (U and G halves).
+  float2 awx[4], abx[4], awg[4], abg[4], a1u[4], a1g[4];
 #pragma unroll
-  for (int e = 0; e < E; ++e) awx[e] = abx[e] = awg[e] = abg[e] = a1u[e] = a1g[e] = 0.f;
-  float rwx[WREG ? E : 1], rbx[WREG ? E : 1], rwg[WREG ? E : 1], rbg[WREG ? E : 1];
-  if (WREG && active) {
-    lds_f32<E>(wsm + c0, rwx);
-    lds_f32<E>(wsm + H + c0, rbx);
-    lds_f32<E>(wsm + 2 * H + c0, rwg);
-    lds_f32<E>(wsm + 3 * H + c0, rbg);
-  }
+  for (int k = 0; k < 4; ++k) awx[k] = abx[k] = awg[k] = abg[k] = a1u[k] = a1g[k] = f2(0.f);
 
   const float invH = 1.0f / (float)H;
   T* dZrow = reinterpret_cast<T*>(a.dZ) + ((size_t)b0 * a.T + t) * 2 * H;
@@ -189,69 +185,75 @@ __global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdA
                                    (volatile int*)&abort_flag);
     // Pass 1: everything that needs only this element, plus the row sums;
     // gU, Uh, gG, Gh stay in registers for pass 2.
-    float kgU[R][E], kUh[R][E], kgG[R][E], kGh[R][E];
-    float rs[NS];
-#pragma unroll
-    for (int k = 0; k < NS; ++k) rs[k] = 0.f;
+    float2 kgU[R][4], kUh[R][4], kgG[R][4], kGh[R][4];
+    float rsum[NS];
     float sUr[R], sGr[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const float4 sr = st_row[min(i + r, nrows - 1)];
       sUr[r] = sr.x;
       sGr[r] = sr.z;
+      float2 rs[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
       if (ok && active && r < nr) {
-        const T* st_dh = reinterpret_cast<const T*>(ring + (size_t)(r == 0 ? s : s1) * row_bytes);
-        float dhv[E], zu[E], zg[E], wx[E], bx[E], wg[E], bg[E];
-        load_vec(st_dh + c0, dhv);
-        load_vec(st_dh + H + c0, zu);
-        load_vec(st_dh + 2 * H + c0, zg);
+        const T* st = reinterpret_cast<const T*>(ring + (size_t)(r == 0 ? s : s1) * row_bytes);
+        float2 dhv[4], zu[4], zg[4], w[4][4];
+        ld8<T>(st + c0, dhv);
+        ld8<T>(st + H + c0, zu);
+        ld8<T>(st + 2 * H + c0, zg);
         if (WREG) {
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            wx[e] = rwx[WREG ? e : 0];
-            bx[e] = rbx[WREG ? e : 0];
-            wg[e] = rwg[WREG ? e : 0];
-            bg[e] = rbg[WREG ? e : 0];
-          }
-        } else {
-          lds_f32<E>(wsm + c0, wx);
-          lds_f32<E>(wsm + H + c0, bx);
-          lds_f32<E>(wsm + 2 * H + c0, wg);
-          lds_f32<E>(wsm + 3 * H + c0, bg);
-        }
+          for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float Uh = fmaf(zu[e], sr.x, sr.y);
-          const float Gh = fmaf(zg[e], sr.z, sr.w);
-          const float u = fmaf(wx[e], Uh, bx[e]);
-          const float g = fmaf(wg[e], Gh, bg[e]);
-          const float sg = sigmoid_fast(g);
-          const float gs = g * sg;
-          const float du = dhv[e] * gs;
-          const float dsilu = sg + fmaf(-gs, sg, gs);
-          const float dg = (dhv[e] * u) * dsilu;
-          const float gU = wx[e] * du, gG = wg[e] * dg;
-          rs[4 * r + 0] += gU;
-          rs[4 * r + 1] = fmaf(gU, Uh, rs[4 * r + 1]);
-          rs[4 * r + 2] += gG;
-          rs[4 * r + 3] = fmaf(gG, Gh, rs[4 * r + 3]);
-          awx[e] = fmaf(du, Uh, awx[e]);
-          abx[e] += du;
-          awg[e] = fmaf(dg, Gh, awg[e]);
-          abg[e] += dg;
-          kgU[r][e] = gU;
-          kUh[r][e] = Uh;
-          kgG[r][e] = gG;
-          kGh[r][e] = Gh;
+            for (int q = 0; q < 4; ++q) w[k][q] = rw[WREG ? k : 0][q];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 lo = *reinterpret_cast<const float4*>(wsm + k * H + c0);
+            const float4 hi = *reinterpret_cast<const float4*>(wsm + k * H + c0 + 4);
+            w[k][0] = make_float2(lo.x, lo.y);
+            w[k][1] = make_float2(lo.z, lo.w);
+            w[k][2] = make_float2(hi.x, hi.y);
+            w[k][3] = make_float2(hi.z, hi.w);
+          }
+        }
+        const float2 sU = f2(sr.x), cU = f2(sr.y), sG = f2(sr.z), cG = f2(sr.w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 Uh = fma2(zu[q], sU, cU);
+          const float2 Gh = fma2(zg[q], sG, cG);
+          const float2 u = fma2(w[0][q], Uh, w[1][q]);
+          const float2 g = fma2(w[2][q], Gh, w[3][q]);
+          const float2 sg = sigmoid_fast2(g);
+          const float2 gs = mul2(g, sg);
+          const float2 du = mul2(dhv[q], gs);
+          // silu'(g) = s + g s (1 - s) = s + (gs - gs * s)
+          const float2 dsilu = add2(sg, fma2(gs, make_float2(-sg.x, -sg.y), gs));
+          const float2 dg = mul2(mul2(dhv[q], u), dsilu);
+          const float2 gU = mul2(w[0][q], du), gG = mul2(w[2][q], dg);
+          rs[0] = add2(rs[0], gU);
+          rs[1] = fma2(gU, Uh, rs[1]);
+          rs[2] = add2(rs[2], gG);
+          rs[3] = fma2(gG, Gh, rs[3]);
+          awx[q] = fma2(du, Uh, awx[q]);
+          abx[q] = add2(abx[q], du);
+          awg[q] = fma2(dg, Gh, awg[q]);
+          abg[q] = add2(abg[q], dg);
+          kgU[r][q] = gU;
+          kUh[r][q] = Uh;
+          kgG[r][q] = gG;
+          kGh[r][q] = Gh;
         }
       }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) rsum[4 * r + k] = rs[k].x + rs[k].y;
     }
     // Row sums over the CTA: per warp (lane LPS*c holds sum c), then over
-    // the warps in a fixed order, the same bits in every thread.
-    float* rb = red + ((i / R) & 1) * 8 * 32;
+    // the warps in a fixed order, the same bits in every thread.  Stored
+    // warp-major, so that neither the stores nor the reads below conflict.
+    float* rb = red + ((i / R) & 1) * kGateRedWarps * NS;
     {
-      const float k = warp_sum_transposed<NS>(rs);
-      if (lane % LPS == 0) rb[(lane / LPS) * 32 + warp] = k;
+      const float k = warp_sum_transposed<NS>(rsum);
+      if (lane % LPS == 0) rb[warp * NS + lane / LPS] = k;
     }
     if (__syncthreads_or(!ok)) {
       aborted = true;
@@ -274,8 +276,8 @@ __global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdA
       const int c = lane / LPS, w0 = lane % LPS;
       float v = 0.f;
 #pragma unroll
-      for (int w = w0; w < 16; w += LPS)
-        if (w < nw) v += rb[c * 32 + w];
+      for (int w = w0; w < kGateRedWarps; w += LPS)
+        if (w < nw) v += rb[w * NS + c];
 #pragma unroll
       for (int off = LPS / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
 #pragma unroll
@@ -286,17 +288,18 @@ __global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdA
       for (int r = 0; r < R; ++r) {
         if (r < nr) {
           const float sU = sUr[r], sG = sGr[r];
-          const float pU = -m[4 * r + 1], qU = -sU * m[4 * r], pG = -m[4 * r + 3], qG = -sG * m[4 * r + 2];
-          float oU[E], oG[E];
+          const float2 pU = f2(-m[4 * r + 1]), qU = f2(-sU * m[4 * r]);
+          const float2 pG = f2(-m[4 * r + 3]), qG = f2(-sG * m[4 * r + 2]);
+          float2 oU[4], oG[4];
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            oU[e] = fmaf(sU, fmaf(pU, kUh[r][e], kgU[r][e]), qU);
-            oG[e] = fmaf(sG, fmaf(pG, kGh[r][e], kgG[r][e]), qG);
-            a1u[e] += oU[e];
-            a1g[e] += oG[e];
+          for (int q = 0; q < 4; ++q) {
+            oU[q] = fma2(f2(sU), fma2(pU, kUh[r][q], kgU[r][q]), qU);
+            oG[q] = fma2(f2(sG), fma2(pG, kGh[r][q], kgG[r][q]), qG);
+            a1u[q] = add2(a1u[q], oU[q]);
+            a1g[q] = add2(a1g[q], oG[q]);
           }
-          store_vec(dZrow + r * dZstep + c0, oU);
-          store_vec(dZrow + r * dZstep + H + c0, oG);
+          st8<T>(dZrow + r * dZstep + c0, oU);
+          st8<T>(dZrow + r * dZstep + H + c0, oG);
         }
       }
     }
@@ -317,10 +320,9 @@ __global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdA
 
   if (active) {
     const size_t p = (size_t)bblk * a.T + t;
-    auto put = [&](float* dst, const float* v) {
-#pragma unroll
-      for (int k = 0; k < E; k += 4)
-        *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+    auto put = [&](float* dst, const float2 (&v)[4]) {
+      *reinterpret_cast<float4*>(dst) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
     };
     put(a.pwx + p * H + c0, awx);
     put(a.pbx + p * H + c0, abx);
@@ -333,11 +335,10 @@ __global__ void __launch_bounds__(WREG ? 320 : 512, 1) k_gate_bwd(const GateBwdA
 
 // Threads, ring stages and shared memory of a CTA of nb rows (0 if even two
 // stages do not fit).
-template <typename T>
+template <typename T, bool WREG>
 size_t gate_shape(int H, int nb, int& threads, int& stages) {
-  constexpr int E = VecN<T>::value;
-  threads = (H / E + 31) / 32 * 32;
-  const size_t fixed = (size_t)nb * 16 + 2 * 8 * 32 * 4 + (size_t)4 * H * 4;
+  threads = (H / kGateE + 31) / 32 * 32;
+  const size_t fixed = (size_t)nb * 16 + 2 * kGateRedWarps * 8 * 4 + (WREG ? 0 : (size_t)4 * H * 4);
   const size_t row_bytes = (size_t)3 * H * sizeof(T);
   const int cap = max_dynamic_smem_bytes() - 1024;  // static shared memory and slack
   const long long room = ((long long)cap - (long long)fixed) / (long long)(row_bytes + 8);
@@ -349,7 +350,7 @@ size_t gate_shape(int H, int nb, int& threads, int& stages) {
 template <typename T, bool WREG>
 int gate_ctas_per_sm(int H) {
   int threads = 0, stages = 0;
-  const size_t smem = gate_shape<T>(H, kGateBwdMaxRows, threads, stages);
+  const size_t smem = gate_shape<T, WREG>(H, kGateBwdMaxRows, threads, stages);
   if (smem == 0) return 1;
   auto k = k_gate_bwd<T, WREG>;
   int n = 0;
@@ -363,7 +364,7 @@ template <typename T, bool WREG>
 cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
   GateBwdArgs a = base;
   int threads = 0;
-  const size_t smem = gate_shape<T>(a.H, a.nb, threads, a.stages);
+  const size_t smem = gate_shape<T, WREG>(a.H, a.nb, threads, a.stages);
   if (smem == 0) return cudaErrorInvalidValue;
   auto k = k_gate_bwd<T, WREG>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -382,7 +383,7 @@ int gate_bwd_ctas_per_sm(const RowArgs& ra) {
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  const bool wreg = ra.H / (ra.dtype == 0 ? 4 : 8) <= 320;
+  const bool wreg = ra.H / kGateE <= 320;
   int n = 1;
   if (ra.dtype == 0) n = wreg ? gate_ctas_per_sm<float, true>(ra.H) : gate_ctas_per_sm<float, false>(ra.H);
   else if (ra.dtype == 1) n = wreg ? gate_ctas_per_sm<bf16, true>(ra.H) : gate_ctas_per_sm<bf16, false>(ra.H);
@@ -392,9 +393,8 @@ int gate_bwd_ctas_per_sm(const RowArgs& ra) {
 }
 
 bool gate_bwd_fused_supported(const RowArgs& a) {
-  // One 16-byte vector of each half per thread, at most 512 threads.
-  const int V = a.dtype == 0 ? 4 : 8;
-  return a.H % V == 0 && a.H / V <= 512 && a.nb <= kGateBwdMaxRows;
+  // Eight columns of each half per thread, at most kGateMaxThreads threads.
+  return a.H % kGateE == 0 && (a.H / kGateE + 31) / 32 * 32 <= kGateMaxThreads && a.nb <= kGateBwdMaxRows;
 }
 
 cudaError_t launch_gate_bwd(const RowArgs& ra, const void* dh, const void* Z, const float* muU, const float* rU,
@@ -427,7 +427,7 @@ cudaError_t launch_gate_bwd(const RowArgs& ra, const void* dh, const void* Z, co
   a.stages = 0;
   if (!a.err) return cudaErrorInvalidValue;
   const dim3 grid(ra.nbblk, ra.T);
-  const bool wreg = ra.H / (ra.dtype == 0 ? 4 : 8) <= 320;
+  const bool wreg = ra.H / kGateE <= 320;
   if (ra.dtype == 0) return wreg ? launch_typed<float, true>(a, st, grid) : launch_typed<float, false>(a, st, grid);
   if (ra.dtype == 1) return wreg ? launch_typed<bf16, true>(a, st, grid) : launch_typed<bf16, false>(a, st, grid);
   return wreg ? launch_typed<f16, true>(a, st, grid) : launch_typed<f16, false>(a, st, grid);
