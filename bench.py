@@ -531,7 +531,9 @@ def run_ours(args) -> dict | None:
     tpeak = burst if peak_name == "burst" else sustained
     for k, v in kernels.items():
         per = v["ms_per_launch"] / 1e3
-        if k in gflops and shape.dtype != "f32":
+        if k.split(".")[0] in gflops and shape.dtype == "f32":
+            v["gflops"] = gflops[k.split(".")[0]] / per / 1e9   # CUDA-core (FFMA) contraction
+        elif k in gflops and shape.dtype != "f32":
             v["tflops"] = gflops[k] / per / 1e12
             v["frac_of_peak"] = v["tflops"] / tpeak
         elif k in rbytes:

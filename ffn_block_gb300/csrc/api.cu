@@ -23,6 +23,7 @@
 // 8: the weight gradients, which nothing else consumes, come last.
 
 #include <atomic>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <string>
@@ -59,14 +60,55 @@ inline size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 inline int esize(int dtype) { return dtype == RMX_F32 ? 4 : 2; }
 
 // ------------------------------------------------------------------ layouts
+constexpr int kNumParams = 14;
+
+// Offsets of the 14 parameter-shaped tensors (rmx_params order) in a buffer.
+struct ParamSet {
+  size_t off[kNumParams];
+};
+
 struct Layout {
+  // Row pitches the kernels see (multiples of 8) and the block's own sizes.
+  // When they differ, the block runs on zero-padded copies (`padded`).
+  int D, H, Dl, Hl;
+  bool padded;
   // saved (filled by the forward)
   size_t out1, Z, hidden, s2, stats, zstats, s1, saved_total;
+  // padded copies of x, y and the parameters (in `saved`), of dy, dx and
+  // the gradients (in `ws`)
+  size_t xp, yp, dyp, dxp;
+  ParamSet pp, gp;
   // backward scratch
   size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, colsum_scratch,
       colsum_scratch_floats, ws_total;
   RowArgs ra;
 };
+
+inline int pad8(int v) { return (v + 7) / 8 * 8; }
+
+// Logical and padded shape of each parameter, in rmx_params order: rows x
+// cols per outer index (w1 and b1 have their columns split into the U and G
+// halves).
+PadMap param_map(int k, int T, int D, int H, int Dp, int Hp) {
+  switch (k) {
+    case 0: return PadMap{T, D, Dp, 2 * H, 2 * Hp, 2};   // w1 [T, D, 2H]
+    case 1: return PadMap{1, T, T, 2 * H, 2 * Hp, 2};    // b1 [T, 2H]
+    case 2: return PadMap{T, H, Hp, D, Dp, 1};           // wout [T, H, D]
+    case 3: return PadMap{1, T, T, D, Dp, 1};            // bout [T, D]
+    default:
+      if (k < 10) return PadMap{1, 1, 1, D, Dp, 1};      // outer LayerNorms [D]
+      return PadMap{1, 1, 1, H, Hp, 1};                  // inner LayerNorms [H]
+  }
+}
+
+size_t lay_params(size_t o, int T, int Dp, int Hp, size_t e, ParamSet& ps, size_t (*up)(size_t)) {
+  for (int k = 0; k < kNumParams; ++k) {
+    const PadMap m = param_map(k, T, Dp, Hp, Dp, Hp);
+    ps.off[k] = o;
+    o = up(o + (size_t)m.outer * m.rows_p * m.cols_p * e);
+  }
+  return o;
+}
 
 bool config_ok(const rmx_config* c) {
   if (!c) return false;
@@ -106,22 +148,35 @@ void colsum_jobs(const Layout& L, const rmx_config& c, const rmx_grads* g, void*
 
 Layout layout_of(const rmx_config& c) {
   Layout L;
+  L.Dl = c.D;
+  L.Hl = c.H;
+  L.D = pad8(c.D);
+  L.H = pad8(c.H);
+  L.padded = L.D != L.Dl || L.H != L.Hl;
   const size_t e = esize(c.dtype);
-  const size_t N = (size_t)c.B * c.T, D = c.D, H = c.H;
+  const size_t N = (size_t)c.B * c.T, D = L.D, H = L.H;
   size_t o = 0;
   L.out1 = o; o = up(o + N * D * e);
   L.Z = o; o = up(o + N * 2 * H * e);
   L.hidden = o; o = up(o + N * H * e);
   L.s2 = o; o = up(o + N * D * e);
   L.stats = o; o = up(o + 10 * N * sizeof(float));
-  L.zstats = o; o = up(o + N * (size_t)zstats_tiles(c.H) * 4 * sizeof(float));  // forward scratch
+  L.zstats = o; o = up(o + N * (size_t)zstats_tiles(L.H) * 4 * sizeof(float));  // forward scratch
   L.s1 = o; o = up(o + N * D * e);  // norm1's input token_mix(norm0(x)) + x, read by its backward
+  L.xp = L.yp = 0;
+  if (L.padded) {
+    L.xp = o; o = up(o + N * D * e);
+    L.yp = o; o = up(o + N * D * e);
+    o = lay_params(o, c.T, L.D, L.H, e, L.pp, up);
+  }
   L.saved_total = o;
 
   L.ra.B = c.B;
   L.ra.T = c.T;
-  L.ra.D = c.D;
-  L.ra.H = c.H;
+  L.ra.D = L.D;
+  L.ra.H = L.H;
+  L.ra.Dl = L.Dl;
+  L.ra.Hl = L.Hl;
   L.ra.dtype = c.dtype;
   // Rows per CTA of the per-token row passes (grid T x ceil(B / nb)).
   const int sms = c.B > 0 ? sm_count() : 1;
@@ -166,6 +221,12 @@ Layout layout_of(const rmx_config& c) {
     L.colsum_scratch_floats = colsums_scratch_floats(jobs, kColsumJobs);
   }
   L.colsum_scratch = o; o = up(o + L.colsum_scratch_floats * sizeof(float));
+  L.dyp = L.dxp = 0;
+  if (L.padded) {
+    L.dyp = o; o = up(o + N * D * e);
+    L.dxp = o; o = up(o + N * D * e);
+    o = lay_params(o, c.T, L.D, L.H, e, L.gp, up);
+  }
   L.ws_total = o;
   return L;
 }
@@ -177,24 +238,27 @@ void colsum_jobs(const Layout& L, const rmx_config& c, const rmx_grads* g, void*
   const int P = L.ra.nbblk * c.T, Pb = L.ra.nbblk;
   const int PL = L.ra.nbblk_ln * c.T, PLb = L.ra.nbblk_ln;
   const int P0 = ln0_bwd_gather_supported(L.ra) ? ln0_bwd_partial_rows(L.ra) : PL;
+  const int D = L.D, H = L.H;
   const ColsumJob j[kColsumJobs] = {
-      {F(L.pg2), g ? g->gamma2 : nullptr, PL, c.D},  {F(L.pb2), g ? g->beta2 : nullptr, PL, c.D},
-      {F(L.pbo), g ? g->bout : nullptr, PLb, c.T * c.D}, {F(L.pwx), g ? g->lnx_w : nullptr, P, c.H},
-      {F(L.pbx), g ? g->lnx_b : nullptr, P, c.H},    {F(L.pwg), g ? g->lng_w : nullptr, P, c.H},
-      {F(L.pbg), g ? g->lng_b : nullptr, P, c.H},    {F(L.pb1), g ? g->b1 : nullptr, Pb, c.T * 2 * c.H},
-      {F(L.pg1), g ? g->gamma1 : nullptr, PL, c.D},  {F(L.pbe1), g ? g->beta1 : nullptr, PL, c.D},
-      {F(L.pg0), g ? g->gamma0 : nullptr, P0, c.D},  {F(L.pb0), g ? g->beta0 : nullptr, P0, c.D},
+      {F(L.pg2), g ? g->gamma2 : nullptr, PL, D},  {F(L.pb2), g ? g->beta2 : nullptr, PL, D},
+      {F(L.pbo), g ? g->bout : nullptr, PLb, c.T * D}, {F(L.pwx), g ? g->lnx_w : nullptr, P, H},
+      {F(L.pbx), g ? g->lnx_b : nullptr, P, H},    {F(L.pwg), g ? g->lng_w : nullptr, P, H},
+      {F(L.pbg), g ? g->lng_b : nullptr, P, H},    {F(L.pb1), g ? g->b1 : nullptr, Pb, c.T * 2 * H},
+      {F(L.pg1), g ? g->gamma1 : nullptr, PL, D},  {F(L.pbe1), g ? g->beta1 : nullptr, PL, D},
+      {F(L.pg0), g ? g->gamma0 : nullptr, P0, D},  {F(L.pb0), g ? g->beta0 : nullptr, P0, D},
   };
   for (int k = 0; k < kColsumJobs; ++k) jobs[k] = j[k];
 }
 
-// What the kernels can do (beyond what makes a valid block).
+// What the kernels can do (beyond what makes a valid block).  Rows of any
+// length run on copies padded to a multiple of 8 elements; the limits are on
+// the padded lengths.
 rmx_status kernels_support(const rmx_config& c) {
   const int V = 16 / esize(c.dtype);
-  if (c.D % V || c.H % V) return RMX_ERR_UNSUPPORTED;  // rows must be whole 16-byte vectors
-  if (c.D / V > kRowThreadsMax || c.H / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;
-  if ((c.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // LN forward: 10 vectors per lane
-  if (!gate_bwd_fused_supported(layout_of(c).ra)) return RMX_ERR_UNSUPPORTED;
+  const Layout L = layout_of(c);
+  if (L.D / V > kRowThreadsMax) return RMX_ERR_UNSUPPORTED;     // LN backward: a thread per 16-byte vector
+  if ((L.D / V + 31) / 32 > 10) return RMX_ERR_UNSUPPORTED;  // LN forward: 10 vectors per lane
+  if (!gate_bwd_fused_supported(L.ra)) return RMX_ERR_UNSUPPORTED;  // gate backward: 8 columns per thread
   return RMX_OK;
 }
 
@@ -292,13 +356,24 @@ class Launch {
     if (s_ != RMX_OK) return s_;       \
   } while (0)
 
+// Profile name of a GEMM that runs on the CUDA cores (the strict fp32
+// contract, or a 16-bit shape the tensor-core engine does not take).
+const char* ffma_label(const char* name) {
+  static const char* const kNames[][2] = {
+      {"gemm1_fwd", "gemm1_fwd.ffma"},     {"gemm2_fwd", "gemm2_fwd.ffma"},
+      {"gemm1_dgrad", "gemm1_dgrad.ffma"}, {"gemm2_dgrad", "gemm2_dgrad.ffma"},
+      {"gemm1_wgrad", "gemm1_wgrad.ffma"}, {"gemm2_wgrad", "gemm2_wgrad.ffma"},
+      {"test_gemm", "test_gemm.ffma"},
+  };
+  for (const auto& n : kNames)
+    if (std::strcmp(n[0], name) == 0) return n[1];
+  return name;
+}
+
 rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
-  Launch l(name, st);
-  cudaError_t e;
-  if (d.dtype != RMX_F32 && gemm_tc_supported(d))
-    e = gemm_tc_launch(d, device_error_word(), st);
-  else
-    e = gemm_simt_launch(d, st);
+  const bool tc = d.dtype != RMX_F32 && gemm_tc_supported(d);
+  Launch l(tc ? name : ffma_label(name), st);
+  const cudaError_t e = tc ? gemm_tc_launch(d, device_error_word(), st) : gemm_simt_launch(d, st);
   return l.done(e);
 }
 
@@ -377,8 +452,8 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   }
   float* zstats = reinterpret_cast<float*>(at(saved, L.zstats));
   {
-    GemmDesc d{GEMM_FWD, EPI_BIAS_ZSTATS, c.dtype, c.B, 2 * c.H, c.D, c.T, out1, p.w1, Z, p.b1, nullptr,
-               zstats, c.H};
+    GemmDesc d{GEMM_FWD, EPI_BIAS_ZSTATS, c.dtype, c.B, 2 * L.H, L.D, c.T, out1, p.w1, Z, p.b1, nullptr,
+               zstats, L.H};
     const bool epilogue_stats = c.dtype != RMX_F32 && gemm_tc_supported(d);
     RMX_TRY(run_gemm("gemm1_fwd", d, st));
     if (!epilogue_stats) {
@@ -392,7 +467,7 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
                                    hidden, st)));
   }
   {
-    GemmDesc d{GEMM_FWD, EPI_BIAS_RESID, c.dtype, c.B, c.D, c.H, c.T, hidden, p.wout, s2, p.bout, out1};
+    GemmDesc d{GEMM_FWD, EPI_BIAS_RESID, c.dtype, c.B, L.D, L.H, c.T, hidden, p.wout, s2, p.bout, out1};
     RMX_TRY(run_gemm("gemm2_fwd", d, st));
   }
   {
@@ -427,7 +502,7 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     RMX_TRY(l.done(launch_ln2_bwd(L.ra, dy, s2, S.mu2, S.r2, p.gamma2, ds2, F(L.pg2), F(L.pb2), F(L.pbo), st)));
   }
   {
-    GemmDesc d{GEMM_DGRAD, EPI_STORE, c.dtype, c.B, c.H, c.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
+    GemmDesc d{GEMM_DGRAD, EPI_STORE, c.dtype, c.B, L.H, L.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm2_dgrad", d, st));
   }
   {
@@ -436,7 +511,7 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
                                    F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1), st)));
   }
   {
-    GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, c.D, 2 * c.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
+    GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, L.D, 2 * L.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
     RMX_TRY(run_gemm("gemm1_dgrad", d, st));
   }
   const bool gather0 = ln0_bwd_gather_supported(L.ra);
@@ -468,11 +543,11 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   // Weight gradients last: every SM is busy with one GEMM CTA, so there is
   // nothing for a second stream to overlap them with.
   {
-    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.H, c.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
+    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, L.H, L.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm2_wgrad", d, st));
   }
   {
-    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, c.D, 2 * c.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
+    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, L.D, 2 * L.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
     RMX_TRY(run_gemm("gemm1_wgrad", d, st));
   }
   {
@@ -490,6 +565,69 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
           launch_colsums_final(jobs, kColsumJobs, c.dtype, F(L.colsum_scratch), L.colsum_scratch_floats, st)));
     }
   }
+  return RMX_OK;
+}
+
+// ------------------------------------------------------------------ padded blocks
+const void* const* param_slots(const rmx_params& p) { return reinterpret_cast<const void* const*>(&p); }
+void* const* grad_slots(const rmx_grads& g) { return reinterpret_cast<void* const*>(&g); }
+static_assert(sizeof(rmx_params) == kNumParams * sizeof(void*), "14 parameter pointers");
+static_assert(sizeof(rmx_grads) == kNumParams * sizeof(void*), "14 gradient pointers");
+
+rmx_params params_at(void* base, const ParamSet& ps) {
+  const void* v[kNumParams];
+  for (int k = 0; k < kNumParams; ++k) v[k] = at(base, ps.off[k]);
+  rmx_params p;
+  std::memcpy(&p, v, sizeof(p));
+  return p;
+}
+rmx_grads grads_at(void* base, const ParamSet& ps) {
+  void* v[kNumParams];
+  for (int k = 0; k < kNumParams; ++k) v[k] = at(base, ps.off[k]);
+  rmx_grads g;
+  std::memcpy(&g, v, sizeof(g));
+  return g;
+}
+
+rmx_status pad_copy(const char* name, const void* src, void* dst, int dtype, const PadMap& m, bool pack,
+                    cudaStream_t st) {
+  Launch l(name, st);
+  return l.done(launch_pad_copy(src, dst, dtype, m, pack, st));
+}
+
+// [B, T, D] activations between the caller's layout and the padded one.
+PadMap act_map(const Layout& L, const rmx_config& c) {
+  const int N = c.B * c.T;
+  return PadMap{1, N, N, L.Dl, L.D, 1};
+}
+
+// Forward of a block whose rows need padding: x and the parameters are
+// packed into `saved` (the backward reuses them), the padded block runs, and
+// y is unpacked.
+rmx_status forward_padded(const Layout& L, const rmx_config& c, const void* x, const rmx_params& p, void* saved,
+                          void* y, cudaStream_t st) {
+  RMX_TRY(pad_copy("pad_in", x, at(saved, L.xp), c.dtype, act_map(L, c), true, st));
+  const void* const* src = param_slots(p);
+  for (int k = 0; k < kNumParams; ++k)
+    RMX_TRY(pad_copy("pad_in", src[k], at(saved, L.pp.off[k]), c.dtype, param_map(k, c.T, L.Dl, L.Hl, L.D, L.H),
+                     true, st));
+  RMX_TRY(forward_impl(c, at(saved, L.xp), params_at(saved, L.pp), saved, at(saved, L.yp), st));
+  return pad_copy("pad_out", at(saved, L.yp), y, c.dtype, act_map(L, c), false, st);
+}
+
+rmx_status backward_padded(const Layout& L, const rmx_config& c, const void* dy, const void* saved, void* dx,
+                           const rmx_grads& g, void* ws, cudaStream_t st, cudaEvent_t dx_ready) {
+  void* sv = const_cast<void*>(saved);
+  RMX_TRY(pad_copy("pad_in", dy, at(ws, L.dyp), c.dtype, act_map(L, c), true, st));
+  const rmx_grads gp = grads_at(ws, L.gp);
+  RMX_TRY(backward_impl(c, at(sv, L.xp), at(ws, L.dyp), saved, params_at(sv, L.pp), at(ws, L.dxp), gp, ws, st,
+                        nullptr));
+  RMX_TRY(pad_copy("pad_out", at(ws, L.dxp), dx, c.dtype, act_map(L, c), false, st));
+  if (dx_ready && cudaEventRecord(dx_ready, st) != cudaSuccess) return RMX_ERR_CUDA;
+  void* const* dst = grad_slots(g);
+  void* const* srcp = grad_slots(gp);
+  for (int k = 0; k < kNumParams; ++k)
+    RMX_TRY(pad_copy("pad_out", srcp[k], dst[k], c.dtype, param_map(k, c.T, L.Dl, L.Hl, L.D, L.H), false, st));
   return RMX_OK;
 }
 
@@ -523,6 +661,7 @@ rmx_status backward_checked(const rmx_config* cfg, const void* x, const void* dy
   const Layout L = layout_of(*cfg);
   if (saved_bytes < L.saved_total || ws_bytes < L.ws_total) return RMX_ERR_WORKSPACE;
   RMX_TRY(kernels_support(*cfg));
+  if (L.padded) return backward_padded(L, *cfg, dy, saved, dx, *grads, ws, st, dx_ready);
   return backward_impl(*cfg, x, dy, saved, *params, dx, *grads, ws, st, dx_ready);
 }
 
@@ -555,6 +694,7 @@ rmx_status rmx_forward(const rmx_config* cfg, const void* x, const rmx_params* p
   const Layout L = layout_of(*cfg);
   if (saved_bytes < L.saved_total) return RMX_ERR_WORKSPACE;
   RMX_TRY(kernels_support(*cfg));
+  if (L.padded) return forward_padded(L, *cfg, x, *params, saved, y, reinterpret_cast<cudaStream_t>(stream));
   return forward_impl(*cfg, x, *params, saved, y, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -82,6 +82,7 @@ struct GateBwdArgs {
   float* pb1;            // [P, 2H]
   unsigned int* err;
   int B, T, H, nb, stages;
+  int Hl;                // real columns of each half of pitch H (the rest are zero padding)
 };
 
 // Shared memory: stats [nb] float4 | red [2][16][8] float | weights [4][H]
@@ -167,7 +168,8 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) awx[k] = abx[k] = awg[k] = abg[k] = a1u[k] = a1g[k] = f2(0.f);
 
-  const float invH = 1.0f / (float)H;
+  const float invH = 1.0f / (float)a.Hl;
+  const bool tail = c0 + kGateE > a.Hl;  // this thread owns padding columns (written as zeros)
   T* dZrow = reinterpret_cast<T*>(a.dZ) + ((size_t)b0 * a.T + t) * 2 * H;
   const size_t dZstep = (size_t)a.T * 2 * H;
   int issued = min(S, nrows);
@@ -295,6 +297,11 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
           for (int q = 0; q < 4; ++q) {
             oU[q] = fma2(f2(sU), fma2(pU, kUh[r][q], kgU[r][q]), qU);
             oG[q] = fma2(f2(sG), fma2(pG, kGh[r][q], kgG[r][q]), qG);
+            if (tail) {
+              const int c = c0 + 2 * q;
+              if (c >= a.Hl) oU[q].x = oG[q].x = 0.f;
+              if (c + 1 >= a.Hl) oU[q].y = oG[q].y = 0.f;
+            }
             a1u[q] = add2(a1u[q], oU[q]);
             a1g[q] = add2(a1g[q], oG[q]);
           }
@@ -423,6 +430,7 @@ cudaError_t launch_gate_bwd(const RowArgs& ra, const void* dh, const void* Z, co
   a.B = ra.B;
   a.T = ra.T;
   a.H = ra.H;
+  a.Hl = ra.Hl;
   a.nb = ra.nb;
   a.stages = 0;
   if (!a.err) return cudaErrorInvalidValue;

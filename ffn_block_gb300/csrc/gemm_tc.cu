@@ -860,8 +860,11 @@ int sm_count() {
 bool gemm_tc_supported(const GemmDesc& d) {
   if (d.dtype != 1 && d.dtype != 2) return false;
   if (d.M <= 0 || d.N <= 0 || d.K <= 0 || d.G <= 0) return false;
-  // 16-byte row strides for the tensor maps and the vector epilogue.
-  if (d.N % 8 || d.K % 8) return false;
+  // 16-byte row strides for the tensor maps and the vector epilogue.  The
+  // weight-gradient GEMMs reduce over K = B, the outermost dimension of both
+  // operands' maps (no stride of its own); a ragged last k-block is
+  // zero-filled by the copy.  K % 8 only selects the interleaved stages.
+  if (d.N % 8 || (d.kind != GEMM_WGRAD && d.K % 8)) return false;
   if (d.kind == GEMM_WGRAD && d.M % 8) return false;
   if (d.epi == EPI_BIAS_ZSTATS && (BN / (EPI_WARPS / 4) != kZStatsTile || !d.zstats || d.split % 8)) return false;
   const int ok_epi = (d.kind == GEMM_FWD && (d.epi == EPI_STORE || d.epi == EPI_BIAS || d.epi == EPI_BIAS_RESID ||

@@ -8,8 +8,15 @@
 namespace rmx {
 
 // ------------------------------------------------------------------ row passes
+// D and H are the row pitches of the tensors the kernels see (multiples of
+// 8); Dl and Hl the block's own sizes (Dl <= D, Hl <= H).  When they differ,
+// every tensor is a zero-padded copy: columns Dl .. D-1 (and, for Z = [U | G]
+// of pitch 2H, columns Hl .. H-1 of each half) hold zeros on input, means and
+// variances are taken over the Dl (Hl) real columns, and the kernels write
+// zeros there on output.
 struct RowArgs {
   int B, T, D, H, dtype;
+  int Dl, Hl;    // logical row lengths
   int nb;        // samples per CTA in the per-token gate backward
   int nbblk;     // ceil(B / nb)
   int nb_ln;     // samples per CTA in the LayerNorm backward
@@ -103,6 +110,17 @@ cudaError_t launch_colsums_final(const ColsumJob* jobs, int njobs, int dtype, fl
 // Largest thread count a row pass may use (one thread per 16-byte vector).
 constexpr int kRowThreadsMax = 512;
 int max_dynamic_smem_bytes();
+
+// ------------------------------------------------------------------ padding
+// Gathers between a tensor of logical shape [outer][rows][cols] (row-major)
+// and its zero-padded copy [outer][rows_p][cols_p]: the columns are split
+// into `halves` equal parts, part h landing at column h * cols_p / halves of
+// the padded row.  pack: padded <- logical (zeros in every padded place);
+// unpack: logical <- padded.  Element type by dtype (0 f32, 1 bf16, 2 f16).
+struct PadMap {
+  int outer, rows, rows_p, cols, cols_p, halves;
+};
+cudaError_t launch_pad_copy(const void* src, void* dst, int dtype, const PadMap& m, bool pack, cudaStream_t st);
 
 // ------------------------------------------------------------------ GEMMs
 enum GemmKind { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };

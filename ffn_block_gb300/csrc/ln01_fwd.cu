@@ -543,6 +543,7 @@ cudaError_t launch_v(const Ln01Args& a, int q, cudaStream_t st) {
 }  // namespace
 
 bool ln01_fwd_supported(const RowArgs& ra) {
+  if (ra.Dl != ra.D) return false;  // padded rows: the general two-pass form masks the padding
   if (ln01_cluster_supported(ra)) return true;
   const int e = ra.dtype == 0 ? 4 : 2, V = 16 / e;
   if (ra.D % V || ra.D % ra.T) return false;

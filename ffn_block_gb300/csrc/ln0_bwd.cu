@@ -343,6 +343,7 @@ int ln0_bwd_partial_rows(const RowArgs& ra) {
 }
 
 bool ln0_bwd_gather_supported(const RowArgs& ra) {
+  if (ra.Dl != ra.D) return false;  // padded rows: the general form masks the padding
   const int e = ra.dtype == 0 ? 4 : 2, V = 16 / e;
   if (ra.T % kRowsPerCta || ra.D % ra.T || ra.D % V) return false;
   if ((ra.D / V + 31) / 32 * 32 > kLn0MaxThreads) return false;

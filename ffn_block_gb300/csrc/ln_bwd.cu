@@ -55,19 +55,24 @@ __device__ __forceinline__ float warp_sum4_transposed(float v0, float v1, float 
 
 // Token mix as an addressing rule: column d = i*C + c of row j of a sample
 // goes to row i, column j*C + c.  Writes the V values of columns d0 .. d0+V-1
-// of row j to their mixed places (pairs when C is even).
+// of row j to their mixed places (pairs when C is even).  Columns d >= Dl
+// (the zero padding of a row of pitch D) stay in row j and are written as
+// zeros.
 template <typename T, int V>
-__device__ __forceinline__ void store_mixed_row(T* sample_base, const float* v, int j, int d0, int C, int D) {
+__device__ __forceinline__ void store_mixed_row(T* sample_base, const float* v, int j, int d0, int C, int D,
+                                                int Dl) {
   int i = d0 / C, c = d0 - i * C;
   if ((C & 1) == 0) {
 #pragma unroll
     for (int e = 0; e < V; e += 2) {
-      T* dst = sample_base + (size_t)i * D + j * C + c;
+      const bool pad = d0 + e >= Dl;  // Dl = T * C is even: pairs never straddle it
+      T* dst = pad ? sample_base + (size_t)j * D + d0 + e : sample_base + (size_t)i * D + j * C + c;
+      const float a = pad ? 0.f : v[e], b = pad ? 0.f : v[e + 1];
       if (sizeof(T) == 2) {
-        T pr[2] = {from_f<T>(v[e]), from_f<T>(v[e + 1])};
+        T pr[2] = {from_f<T>(a), from_f<T>(b)};
         *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(pr);
       } else {
-        *reinterpret_cast<float2*>(dst) = make_float2(v[e], v[e + 1]);
+        *reinterpret_cast<float2*>(dst) = make_float2(a, b);
       }
       c += 2;
       while (c >= C) {
@@ -78,7 +83,8 @@ __device__ __forceinline__ void store_mixed_row(T* sample_base, const float* v, 
   } else {
 #pragma unroll
     for (int e = 0; e < V; ++e) {
-      sample_base[(size_t)i * D + j * C + c] = from_f<T>(v[e]);
+      if (d0 + e >= Dl) sample_base[(size_t)j * D + d0 + e] = from_f<T>(0.f);
+      else sample_base[(size_t)i * D + j * C + c] = from_f<T>(v[e]);
       if (++c == C) {
         c = 0;
         ++i;
@@ -101,6 +107,7 @@ struct LnBwdArgs {
   float* pbias;        // [nbblk, T, D] LNB_BIAS: column partials of sum_b out
   unsigned int* err;
   int B, T, D, C, nb, stages;
+  int Dl;              // real columns of a row of pitch D (the rest are zero padding)
 };
 
 // Per-row statistics area, rounded up so the ring starts 16-byte aligned.
@@ -169,7 +176,8 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
 #pragma unroll
   for (int e = 0; e < E; ++e) ag[e] = ab[e] = ao[e] = 0.f;
 
-  const float invD = 1.0f / (float)D;
+  const float invD = 1.0f / (float)a.Dl;
+  const bool tail = c0 + E > a.Dl;  // this thread owns padding columns
   const size_t row_step = (size_t)a.T * D;
   T* out_row = reinterpret_cast<T*>(a.out) + ((size_t)b0 * a.T + t) * D;
   int issued = min(S, nrows);
@@ -250,11 +258,12 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
 #pragma unroll
           for (int e = 0; e < E; ++e) {
             o[e] = fmaf(rstd[r], fmaf(-mgx, xh[r][e], g[r][e]), q0);
+            if (tail && c0 + e >= a.Dl) o[e] = 0.f;
             if (MODE == LNB_BIAS) ao[e] += o[e];
           }
           if (MODE == LNB_MIXED_TOO)
             store_mixed_row<T, E>(reinterpret_cast<T*>(a.out_mixed) + (size_t)(b0 + i + r) * a.T * D, o, t, c0,
-                                  a.C, D);
+                                  a.C, D, a.Dl);
           if (MODE == LNB_RESID) {
 #pragma unroll
             for (int e = 0; e < E; ++e) o[e] += rv[r][e];
@@ -356,7 +365,8 @@ int ln_bwd_ctas_per_sm(const RowArgs& ra) {
 cudaError_t launch_ln_bwd(const RowArgs& ra, int mode, const void* gin, const void* s, const float* mu,
                           const float* rs, const void* gamma, const void* resid, void* out, void* out_mixed, float* pg, float* pb, float* pbias, cudaStream_t st) {
   const int V = ra.dtype == 0 ? 4 : 8;
-  if (ra.D % V || ra.D / V > 512 || ra.nb_ln < 1 || ra.nb_ln > kLnBwdMaxRows || ra.D % ra.T) return cudaErrorInvalidValue;
+  if (ra.D % V || ra.D / V > 512 || ra.nb_ln < 1 || ra.nb_ln > kLnBwdMaxRows || ra.Dl % ra.T || ra.Dl > ra.D)
+    return cudaErrorInvalidValue;
   LnBwdArgs a;
   a.gin = gin;
   a.s = s;
@@ -374,7 +384,8 @@ cudaError_t launch_ln_bwd(const RowArgs& ra, int mode, const void* gin, const vo
   a.B = ra.B;
   a.T = ra.T;
   a.D = ra.D;
-  a.C = ra.D / ra.T;
+  a.Dl = ra.Dl;
+  a.C = ra.Dl / ra.T;
   a.nb = ra.nb_ln;
   a.stages = 0;
   if (ra.dtype == 0) return launch_mode<float>(a, mode, st);

@@ -81,6 +81,8 @@ extern "C" rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void
   ra.T = cfg->T;
   ra.D = cfg->D;
   ra.H = cfg->H;
+  ra.Dl = cfg->D;
+  ra.Hl = cfg->H;
   ra.dtype = cfg->dtype;
   ra.nb_ln = cfg->B < 64 ? cfg->B : 64;
   ra.nbblk_ln = (cfg->B + ra.nb_ln - 1) / ra.nb_ln;

@@ -46,24 +46,29 @@ inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
 // writes its gradient rows both as they are and mixed, so every LayerNorm
 // pass reads and writes whole rows.
 // -------------------------------------------------------------------------
+// Columns d >= Dl (the zero padding of a row of pitch D) stay in row j and
+// are written as zeros.
 template <typename T, int V>
-__device__ __forceinline__ void store_mixed(T* sample_base, const float* v, int j, int d0, int C, int D) {
+__device__ __forceinline__ void store_mixed(T* sample_base, const float* v, int j, int d0, int C, int D, int Dl) {
   int i = d0 / C, c = d0 - i * C;
   if ((C & 1) == 0) {
-    // d0 even and C even: elements (e, e+1) always share a chunk.
+    // d0 even and C even: elements (e, e+1) always share a chunk (and Dl,
+    // a multiple of C, is even).
 #pragma unroll
     for (int e = 0; e < V; e += 2) {
-      T pr[2] = {from_f<T>(v[e]), from_f<T>(v[e + 1])};
-      T* dst = sample_base + (size_t)i * D + j * C + c;
+      const bool pad = d0 + e >= Dl;
+      T pr[2] = {from_f<T>(pad ? 0.f : v[e]), from_f<T>(pad ? 0.f : v[e + 1])};
+      T* dst = pad ? sample_base + (size_t)j * D + d0 + e : sample_base + (size_t)i * D + j * C + c;
       if (sizeof(T) == 2) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(pr);
-      else *reinterpret_cast<float2*>(dst) = make_float2(v[e], v[e + 1]);
+      else *reinterpret_cast<float2*>(dst) = make_float2(pad ? 0.f : v[e], pad ? 0.f : v[e + 1]);
       c += 2;
       while (c >= C) { c -= C; ++i; }
     }
   } else {
 #pragma unroll
     for (int e = 0; e < V; ++e) {
-      sample_base[(size_t)i * D + j * C + c] = from_f<T>(v[e]);
+      if (d0 + e >= Dl) sample_base[(size_t)j * D + d0 + e] = from_f<T>(0.f);
+      else sample_base[(size_t)i * D + j * C + c] = from_f<T>(v[e]);
       if (++c == C) { c = 0; ++i; }
     }
   }
@@ -75,13 +80,15 @@ __device__ __forceinline__ void store_mixed(T* sample_base, const float* v, int 
 //   LNF_PLAIN      y = LN(s)                       (norm2)
 //   LNF_MIXED_OUT  y = LN(s), written token-mixed  (norm0: a0 -> mix)
 //   LNF_SUM_IN     y = LN(s + s_add)               (norm1: mix + x)
-// Saves the row mean and 1/sqrt(var + eps).
+// Saves the row mean and 1/sqrt(var + eps).  Rows of pitch D hold Dl real
+// columns followed by zeros; the statistics cover the real columns.
 // =========================================================================
 template <typename T, int MODE, int MAXV>
 __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T* __restrict__ s_add,
                                                 const T* __restrict__ g, const T* __restrict__ be,
                                                 T* __restrict__ y, float* __restrict__ mu, float* __restrict__ rs,
-                                                T* __restrict__ s_out, int N, int Tn, int D, int C, float eps) {
+                                                T* __restrict__ s_out, int N, int Tn, int D, int C, float eps,
+                                                int Dl) {
   pdl_enter();
   constexpr int V = VecN<T>::value;
   const int lane = threadIdx.x & 31;
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
       for (int e = 0; e < V; ++e) sum += v[e];
     }
   }
-  const float invD = 1.0f / (float)D;
+  const float invD = 1.0f / (float)Dl;
   const float mean = warp_sum(sum) * invD;
   float ss = 0.f;
 #pragma unroll
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
       get(q, v);
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        const float c = v[e] - mean;
+        const float c = vi * V + e < Dl ? v[e] - mean : 0.f;
         ss += c * c;
       }
     }
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
       load_vec(be + vi * V, bb);
 #pragma unroll
       for (int e = 0; e < V; ++e) o[e] = (v[e] - mean) * rstd * gg[e] + bb[e];
-      if (MODE == LNF_MIXED_OUT) store_mixed<T, V>(y + (size_t)b * Tn * D, o, j, vi * V, C, D);
+      if (MODE == LNF_MIXED_OUT) store_mixed<T, V>(y + (size_t)b * Tn * D, o, j, vi * V, C, D, Dl);
       else store_vec(y + (size_t)row * D + vi * V, o);
       if (SUM) store_vec(s_out + (size_t)row * D + vi * V, v);
     }
@@ -224,8 +231,11 @@ __global__ void __launch_bounds__(256) k_zstats(const T* __restrict__ Z, float* 
 // =========================================================================
 // Row r's statistics of U and G from its group statistics (every lane of
 // the warp ends with the same bits); lane 0 writes them for the backward.
-__device__ __forceinline__ void gate_row_stats(const float* __restrict__ zstats, long long r, int H, float eps,
-                                               float* __restrict__ muU, float* __restrict__ rU,
+// Z rows of pitch 2H whose halves hold Hl real columns and H - Hl zeros: the
+// merged statistics then cover H values per half, and are converted to the
+// Hl real ones (same sum; the zeros add nothing to the sum of squares).
+__device__ __forceinline__ void gate_row_stats(const float* __restrict__ zstats, long long r, int H, int Hl,
+                                               float eps, float* __restrict__ muU, float* __restrict__ rU,
                                                float* __restrict__ muG, float* __restrict__ rG, float& sU,
                                                float& cU, float& sG, float& cG) {
   const int lane = threadIdx.x & 31;
@@ -241,8 +251,17 @@ __device__ __forceinline__ void gate_row_stats(const float* __restrict__ zstats,
   }
   u = warp_merge_moments(u);
   g = warp_merge_moments(g);
-  sU = 1.0f / sqrtf(u.m2 / (float)H + eps);
-  sG = 1.0f / sqrtf(g.m2 / (float)H + eps);
+  if (Hl != H) {
+    auto real_only = [&](Moments& m) {
+      const float mean = m.mean * ((float)H / (float)Hl);
+      m.m2 = fmaxf(m.m2 + (float)H * m.mean * m.mean - (float)Hl * mean * mean, 0.f);
+      m.mean = mean;
+    };
+    real_only(u);
+    real_only(g);
+  }
+  sU = 1.0f / sqrtf(u.m2 / (float)Hl + eps);
+  sG = 1.0f / sqrtf(g.m2 / (float)Hl + eps);
   if (lane == 0) {
     muU[r] = u.mean;
     rU[r] = sU;
@@ -269,7 +288,7 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
                                                   float* __restrict__ muG, float* __restrict__ rG,
                                                   const T* __restrict__ wx, const T* __restrict__ bx,
                                                   const T* __restrict__ wg, const T* __restrict__ bg,
-                                                  T* __restrict__ hidden, int N, int H, float eps) {
+                                                  T* __restrict__ hidden, int N, int H, float eps, int Hl) {
   pdl_enter();
   constexpr int V = VecN<T>::value;
   // Per warp: kGateFwdDepth slots x (U, G) x 32 lanes x 16 bytes.
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
 #pragma unroll
   for (int it = 0; it < kGateFwdDepth; ++it) fetch(it);
   float sU, cU, sG, cG;
-  gate_row_stats(zstats, r, H, eps, muU, rU, muG, rG, sU, cU, sG, cG);
+  gate_row_stats(zstats, r, H, Hl, eps, muU, rU, muG, rG, sU, cU, sG, cG);
   T* hr = hidden + (size_t)r * H;
 #pragma unroll 1
   for (int it = 0; it < iters; ++it) {
@@ -453,12 +472,12 @@ cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void*
   const int nv = a.D / vec_elems(a.dtype);
   const int q = (nv + 31) / 32;
   const int grid = (N + 7) / 8;
-  const int C = a.D / a.T;
+  const int C = a.Dl / a.T;
   cudaError_t err = cudaSuccess;
 #define RMX_LNF(M, MAXV)                                                                                    \
   RMX_DISPATCH_T(a.dtype, {                                                                                 \
     err = launch_k(k_ln_fwd<T, M, MAXV>, dim3(grid), dim3(256), 0, st, 1, (const T*)s, (const T*)s_add,     \
-                   (const T*)g, (const T*)be, (T*)y, mu, rs, (T*)s_out, N, a.T, a.D, C, 1e-3f);             \
+                   (const T*)g, (const T*)be, (T*)y, mu, rs, (T*)s_out, N, a.T, a.D, C, 1e-3f, a.Dl);       \
   })
 #define RMX_LNF_Q(M)                          \
   if (q <= 1) RMX_LNF(M, 1);                  \
@@ -494,7 +513,7 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats
   cudaError_t err = cudaSuccess;
   RMX_DISPATCH_T(a.dtype, {
     err = launch_k(k_gate_fwd<T>, dim3((N + 7) / 8), dim3(256), 0, st, 1, (const T*)Z, zstats, muU, rU, muG, rG,
-                   (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg, (T*)hidden, N, a.H, 1e-5f);
+                   (const T*)wx, (const T*)bx, (const T*)wg, (const T*)bg, (T*)hidden, N, a.H, 1e-5f, a.Hl);
   });
   return err;
 }

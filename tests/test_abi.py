@@ -93,10 +93,24 @@ def test_small_saved_buffer_rejected(lib):
 
 
 def test_unsupported_row_width(lib):
-    # bf16 rows must be whole 16-byte vectors: D = 36 (D % T == 0 with T = 4) is not.
-    cfg = B.make_config(2, 4, 36, 64, "bf16")
+    # The gate backward holds a whole FFN row per CTA: H above 3840 (k = 3 at
+    # D = 1280, the widest the page's held-out domain reaches) is refused.
+    cfg = B.make_config(2, 8, 64, 4096, "bf16")
     p = B.rmx_params(*([0x1000] * 14))
     assert B.rmx_forward(cfg, 0x1000, p, 0x2000, B.rmx_saved_bytes(cfg), 0x3000) == B.RMX_ERR_UNSUPPORTED
+
+
+def test_padded_rows_reserve_their_copies(lib):
+    # D = 36 is not a whole number of 16-byte bf16 vectors: the block runs on
+    # copies padded to 40 columns (H = 72 -> 72), kept in `saved` (x, y and the
+    # parameters) and in the scratch buffer (dy, dx and the gradients).
+    e, Bn, T, D, H = 2, 3, 4, 36, 72
+    cfg = B.make_config(Bn, T, D, H, "bf16")
+    aligned = B.make_config(Bn, T, 40, H, "bf16")
+    params_p = (T * 40 * 2 * H + T * 2 * H + T * H * 40 + T * 40 + 6 * 40 + 4 * H) * e
+    acts_p = 2 * Bn * T * 40 * e
+    assert B.rmx_saved_bytes(cfg) >= B.rmx_saved_bytes(aligned) + params_p + acts_p
+    assert B.rmx_workspace_bytes(cfg) >= B.rmx_workspace_bytes(aligned) + params_p + acts_p
 
 
 def test_empty_batch_forward_is_a_no_op(lib):

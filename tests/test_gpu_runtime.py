@@ -120,8 +120,9 @@ def test_profiler_counts_every_launch():
     prof = B.rmx_profile_read()
     launched = B.rmx_launch_count() - before
     assert sum(n for n, _ in prof.values()) == launched
-    assert {"gemm1_fwd", "gemm2_fwd", "gemm1_wgrad", "gemm2_dgrad", "ln01_fwd", "ln1_bwd", "gate_bwd",
-            "ln0_bwd_gather"} <= set(prof)
+    # c1 is the strict fp32 contract: its contractions run on the CUDA cores.
+    assert {"gemm1_fwd.ffma", "gemm2_fwd.ffma", "gemm1_wgrad.ffma", "gemm2_dgrad.ffma", "ln01_fwd", "ln1_bwd",
+            "gate_bwd", "ln0_bwd_gather"} <= set(prof)
     assert all(ms >= 0.0 for _, ms in prof.values())
 
 
