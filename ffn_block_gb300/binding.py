@@ -27,7 +27,8 @@ RMX_ERR_WORKSPACE = 4
 RMX_ERR_CUDA = 5
 RMX_ERR_TIMEOUT = 6
 
-DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2}
+# "tf32": float32 storage, contractions on the tensor cores with TF32 operands.
+DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2, "tf32": 3}
 
 
 class RmxError(RuntimeError):

@@ -57,7 +57,9 @@ namespace {
 
 constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
-inline int esize(int dtype) { return dtype == RMX_F32 ? 4 : 2; }
+inline int esize(int dtype) { return dtype == RMX_F32 || dtype == RMX_F32_TF32 ? 4 : 2; }
+// Storage type of a config's tensors: the TF32 contract stores fp32.
+inline int storage(int dtype) { return dtype == RMX_F32_TF32 ? RMX_F32 : dtype; }
 
 // ------------------------------------------------------------------ layouts
 constexpr int kNumParams = 14;
@@ -78,6 +80,11 @@ struct Layout {
   // the gradients (in `ws`)
   size_t xp, yp, dyp, dxp;
   ParamSet pp, gp;
+  // TF32 contract: K-major (transposed) copies of the operands the
+  // contractions read MN-major: w1, wout (saved), and hidden, ds2, out1, dZ
+  // with the batch as the contraction axis padded to Bp (scratch).
+  size_t w1T, woutT, hT, ds2T, out1T, dZT;
+  int Bp;
   // backward scratch
   size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, colsum_scratch,
       colsum_scratch_floats, ws_total;
@@ -114,7 +121,7 @@ bool config_ok(const rmx_config* c) {
   if (!c) return false;
   if (c->B < 0 || c->T < 1 || c->D < 1 || c->H < 1) return false;
   if (c->D % c->T) return false;
-  if (c->dtype != RMX_F32 && c->dtype != RMX_BF16 && c->dtype != RMX_F16) return false;
+  if (c->dtype != RMX_F32 && c->dtype != RMX_BF16 && c->dtype != RMX_F16 && c->dtype != RMX_F32_TF32) return false;
   const long long rows = (long long)c->B * c->T;
   if (rows > (1ll << 30) || (long long)c->D > (1 << 20) || (long long)c->H > (1 << 20)) return false;
   return true;
@@ -169,6 +176,14 @@ Layout layout_of(const rmx_config& c) {
     L.yp = o; o = up(o + N * D * e);
     o = lay_params(o, c.T, L.D, L.H, e, L.pp, up);
   }
+  const bool tf32 = c.dtype == RMX_F32_TF32;
+  const size_t T = c.T;
+  L.w1T = L.woutT = L.hT = L.ds2T = L.out1T = L.dZT = 0;
+  L.Bp = (c.B + 3) / 4 * 4;
+  if (tf32) {
+    L.w1T = o; o = up(o + T * 2 * H * D * e);
+    L.woutT = o; o = up(o + T * D * H * e);
+  }
   L.saved_total = o;
 
   L.ra.B = c.B;
@@ -177,7 +192,7 @@ Layout layout_of(const rmx_config& c) {
   L.ra.H = L.H;
   L.ra.Dl = L.Dl;
   L.ra.Hl = L.Hl;
-  L.ra.dtype = c.dtype;
+  L.ra.dtype = storage(c.dtype);
   // Rows per CTA of the per-token row passes (grid T x ceil(B / nb)).
   const int sms = c.B > 0 ? sm_count() : 1;
   // A gate CTA also loads the four weight vectors and writes six column
@@ -226,6 +241,13 @@ Layout layout_of(const rmx_config& c) {
     L.dyp = o; o = up(o + N * D * e);
     L.dxp = o; o = up(o + N * D * e);
     o = lay_params(o, c.T, L.D, L.H, e, L.gp, up);
+  }
+  if (tf32) {
+    const size_t Bp = L.Bp;
+    L.hT = o; o = up(o + T * H * Bp * e);
+    L.ds2T = o; o = up(o + T * D * Bp * e);
+    L.out1T = o; o = up(o + T * D * Bp * e);
+    L.dZT = o; o = up(o + T * 2 * H * Bp * e);
   }
   L.ws_total = o;
   return L;
@@ -370,8 +392,13 @@ const char* ffma_label(const char* name) {
   return name;
 }
 
+// Whether a contraction runs on the tensor cores: 16-bit storage, or fp32
+// under the TF32 contract; otherwise (the strict fp32 contract) on the CUDA
+// cores.
+bool tc_engine(const GemmDesc& d) { return (d.dtype != RMX_F32 || d.tf32) && gemm_tc_supported(d); }
+
 rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
-  const bool tc = d.dtype != RMX_F32 && gemm_tc_supported(d);
+  const bool tc = tc_engine(d);
   Launch l(tc ? name : ffma_label(name), st);
   const cudaError_t e = tc ? gemm_tc_launch(d, device_error_word(), st) : gemm_simt_launch(d, st);
   return l.done(e);
@@ -451,10 +478,22 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
     }
   }
   float* zstats = reinterpret_cast<float*>(at(saved, L.zstats));
+  const int sd = storage(c.dtype);
+  const bool tf32 = c.dtype == RMX_F32_TF32;
+  // TF32: the weights as [T, N, K] (K-major) for the dgrad-form contraction.
+  if (tf32) {
+    Launch l("tf32_transpose", st);
+    RMX_TRY(l.done(launch_transpose_f32(static_cast<const float*>(p.w1), reinterpret_cast<float*>(at(saved, L.w1T)),
+                                        c.T, L.D, 2 * L.H, (long long)L.D * 2 * L.H, 2 * L.H, L.D, st)));
+    Launch l2("tf32_transpose", st);
+    RMX_TRY(l2.done(launch_transpose_f32(static_cast<const float*>(p.wout),
+                                         reinterpret_cast<float*>(at(saved, L.woutT)), c.T, L.H, L.D,
+                                         (long long)L.H * L.D, L.D, L.H, st)));
+  }
   {
-    GemmDesc d{GEMM_FWD, EPI_BIAS_ZSTATS, c.dtype, c.B, 2 * L.H, L.D, c.T, out1, p.w1, Z, p.b1, nullptr,
-               zstats, L.H};
-    const bool epilogue_stats = c.dtype != RMX_F32 && gemm_tc_supported(d);
+    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, EPI_BIAS_ZSTATS, sd, c.B, 2 * L.H, L.D, c.T, out1,
+               tf32 ? at(saved, L.w1T) : p.w1, Z, p.b1, nullptr, zstats, L.H, tf32 ? 1 : 0};
+    const bool epilogue_stats = tc_engine(d);
     RMX_TRY(run_gemm("gemm1_fwd", d, st));
     if (!epilogue_stats) {
       Launch l("zstats", st);
@@ -467,7 +506,8 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
                                    hidden, st)));
   }
   {
-    GemmDesc d{GEMM_FWD, EPI_BIAS_RESID, c.dtype, c.B, L.D, L.H, c.T, hidden, p.wout, s2, p.bout, out1};
+    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, EPI_BIAS_RESID, sd, c.B, L.D, L.H, c.T, hidden,
+               tf32 ? at(saved, L.woutT) : p.wout, s2, p.bout, out1, nullptr, 0, tf32 ? 1 : 0};
     RMX_TRY(run_gemm("gemm2_fwd", d, st));
   }
   {
@@ -496,13 +536,16 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   void* da0 = at(ws, L.da0);
   const void* s1 = at(saved, L.s1);
   auto F = [&](size_t off) { return reinterpret_cast<float*>(at(ws, off)); };
+  const int sd = storage(c.dtype);
+  const bool tf32 = c.dtype == RMX_F32_TF32;
 
   {
     Launch l("ln2_bwd", st);
     RMX_TRY(l.done(launch_ln2_bwd(L.ra, dy, s2, S.mu2, S.r2, p.gamma2, ds2, F(L.pg2), F(L.pb2), F(L.pbo), st)));
   }
   {
-    GemmDesc d{GEMM_DGRAD, EPI_STORE, c.dtype, c.B, L.H, L.D, c.T, ds2, p.wout, dh, nullptr, nullptr};
+    GemmDesc d{GEMM_DGRAD, EPI_STORE, sd, c.B, L.H, L.D, c.T, ds2, p.wout, dh, nullptr, nullptr, nullptr, 0,
+               tf32 ? 1 : 0};
     RMX_TRY(run_gemm("gemm2_dgrad", d, st));
   }
   {
@@ -511,7 +554,8 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
                                    F(L.pwx), F(L.pbx), F(L.pwg), F(L.pbg), F(L.pb1), st)));
   }
   {
-    GemmDesc d{GEMM_DGRAD, EPI_RESID, c.dtype, c.B, L.D, 2 * L.H, c.T, dZ, p.w1, dout1, nullptr, ds2};
+    GemmDesc d{GEMM_DGRAD, EPI_RESID, sd, c.B, L.D, 2 * L.H, c.T, dZ, p.w1, dout1, nullptr, ds2, nullptr, 0,
+               tf32 ? 1 : 0};
     RMX_TRY(run_gemm("gemm1_dgrad", d, st));
   }
   const bool gather0 = ln0_bwd_gather_supported(L.ra);
@@ -542,13 +586,38 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   if (dx_ready && cudaEventRecord(dx_ready, st) != cudaSuccess) return RMX_ERR_CUDA;
   // Weight gradients last: every SM is busy with one GEMM CTA, so there is
   // nothing for a second stream to overlap them with.
-  {
-    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, L.H, L.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
-    RMX_TRY(run_gemm("gemm2_wgrad", d, st));
-  }
-  {
-    GemmDesc d{GEMM_WGRAD, EPI_STORE, c.dtype, L.D, 2 * L.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
-    RMX_TRY(run_gemm("gemm1_wgrad", d, st));
+  if (tf32) {
+    // TF32: both operands K-major, the batch (padded to Bp with zeros) as K:
+    // dW[t] = X[t] @ Y[t]^T with X = [T, M, Bp], Y = [T, N, Bp] transposed
+    // copies, written as [T, M, N].
+    auto tr = [&](const void* src, size_t off, int X) {
+      Launch l("tf32_transpose", st);
+      return l.done(launch_transpose_f32(static_cast<const float*>(src), reinterpret_cast<float*>(at(ws, off)),
+                                         c.T, c.B, X, X, (long long)c.T * X, L.Bp, st));
+    };
+    RMX_TRY(tr(hidden, L.hT, L.H));
+    RMX_TRY(tr(ds2, L.ds2T, L.D));
+    RMX_TRY(tr(out1, L.out1T, L.D));
+    RMX_TRY(tr(dZ, L.dZT, 2 * L.H));
+    auto wgrad = [&](const char* name, int M, int N, size_t a, size_t b, void* out) {
+      GemmDesc d{GEMM_DGRAD, EPI_STORE, sd, M, N, L.Bp, c.T, at(ws, a), at(ws, b), out, nullptr, nullptr, nullptr, 0, 1};
+      d.a_gs = (long long)M * L.Bp;
+      d.a_rs = L.Bp;
+      d.c_gs = (long long)M * N;
+      d.c_rs = N;
+      return run_gemm(name, d, st);
+    };
+    RMX_TRY(wgrad("gemm2_wgrad", L.H, L.D, L.hT, L.ds2T, g.wout));
+    RMX_TRY(wgrad("gemm1_wgrad", L.D, 2 * L.H, L.out1T, L.dZT, g.w1));
+  } else {
+    {
+      GemmDesc d{GEMM_WGRAD, EPI_STORE, sd, L.H, L.D, c.B, c.T, hidden, ds2, g.wout, nullptr, nullptr};
+      RMX_TRY(run_gemm("gemm2_wgrad", d, st));
+    }
+    {
+      GemmDesc d{GEMM_WGRAD, EPI_STORE, sd, L.D, 2 * L.H, c.B, c.T, out1, dZ, g.w1, nullptr, nullptr};
+      RMX_TRY(run_gemm("gemm1_wgrad", d, st));
+    }
   }
   {
     ColsumJob jobs[kColsumJobs];
@@ -557,12 +626,12 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
     {
       Launch l("colsums", st);
       RMX_TRY(l.done(
-          launch_colsums(jobs, kColsumJobs, c.dtype, F(L.colsum_scratch), L.colsum_scratch_floats, st, &fin)));
+          launch_colsums(jobs, kColsumJobs, sd, F(L.colsum_scratch), L.colsum_scratch_floats, st, &fin)));
     }
     if (fin) {
       Launch l("colsums_final", st);
       RMX_TRY(l.done(
-          launch_colsums_final(jobs, kColsumJobs, c.dtype, F(L.colsum_scratch), L.colsum_scratch_floats, st)));
+          launch_colsums_final(jobs, kColsumJobs, sd, F(L.colsum_scratch), L.colsum_scratch_floats, st)));
     }
   }
   return RMX_OK;
@@ -606,28 +675,28 @@ PadMap act_map(const Layout& L, const rmx_config& c) {
 // y is unpacked.
 rmx_status forward_padded(const Layout& L, const rmx_config& c, const void* x, const rmx_params& p, void* saved,
                           void* y, cudaStream_t st) {
-  RMX_TRY(pad_copy("pad_in", x, at(saved, L.xp), c.dtype, act_map(L, c), true, st));
+  RMX_TRY(pad_copy("pad_in", x, at(saved, L.xp), storage(c.dtype), act_map(L, c), true, st));
   const void* const* src = param_slots(p);
   for (int k = 0; k < kNumParams; ++k)
-    RMX_TRY(pad_copy("pad_in", src[k], at(saved, L.pp.off[k]), c.dtype, param_map(k, c.T, L.Dl, L.Hl, L.D, L.H),
+    RMX_TRY(pad_copy("pad_in", src[k], at(saved, L.pp.off[k]), storage(c.dtype), param_map(k, c.T, L.Dl, L.Hl, L.D, L.H),
                      true, st));
   RMX_TRY(forward_impl(c, at(saved, L.xp), params_at(saved, L.pp), saved, at(saved, L.yp), st));
-  return pad_copy("pad_out", at(saved, L.yp), y, c.dtype, act_map(L, c), false, st);
+  return pad_copy("pad_out", at(saved, L.yp), y, storage(c.dtype), act_map(L, c), false, st);
 }
 
 rmx_status backward_padded(const Layout& L, const rmx_config& c, const void* dy, const void* saved, void* dx,
                            const rmx_grads& g, void* ws, cudaStream_t st, cudaEvent_t dx_ready) {
   void* sv = const_cast<void*>(saved);
-  RMX_TRY(pad_copy("pad_in", dy, at(ws, L.dyp), c.dtype, act_map(L, c), true, st));
+  RMX_TRY(pad_copy("pad_in", dy, at(ws, L.dyp), storage(c.dtype), act_map(L, c), true, st));
   const rmx_grads gp = grads_at(ws, L.gp);
   RMX_TRY(backward_impl(c, at(sv, L.xp), at(ws, L.dyp), saved, params_at(sv, L.pp), at(ws, L.dxp), gp, ws, st,
                         nullptr));
-  RMX_TRY(pad_copy("pad_out", at(ws, L.dxp), dx, c.dtype, act_map(L, c), false, st));
+  RMX_TRY(pad_copy("pad_out", at(ws, L.dxp), dx, storage(c.dtype), act_map(L, c), false, st));
   if (dx_ready && cudaEventRecord(dx_ready, st) != cudaSuccess) return RMX_ERR_CUDA;
   void* const* dst = grad_slots(g);
   void* const* srcp = grad_slots(gp);
   for (int k = 0; k < kNumParams; ++k)
-    RMX_TRY(pad_copy("pad_out", srcp[k], dst[k], c.dtype, param_map(k, c.T, L.Dl, L.Hl, L.D, L.H), false, st));
+    RMX_TRY(pad_copy("pad_out", srcp[k], dst[k], storage(c.dtype), param_map(k, c.T, L.Dl, L.Hl, L.D, L.H), false, st));
   return RMX_OK;
 }
 
@@ -832,12 +901,13 @@ rmx_status rmx_test_bounded_wait(int limit_us, rmx_stream stream) {
 
 rmx_status rmx_test_gemm(int kind, int dtype, int M, int N, int K, int G, const void* A, const void* Bm, void* C,
                          rmx_stream stream) {
-  if (kind < 0 || kind > 2 || dtype < 0 || dtype > 2) return RMX_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 2 || dtype < 0 || dtype > 3) return RMX_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || G <= 0) return RMX_ERR_INVALID_ARG;
   RMX_TRY(check_ptr(A));
   RMX_TRY(check_ptr(Bm));
   RMX_TRY(check_ptr(C));
-  GemmDesc d{kind, EPI_STORE, dtype, M, N, K, G, A, Bm, C, nullptr, nullptr};
+  GemmDesc d{kind, EPI_STORE, storage(dtype), M, N, K, G, A, Bm, C, nullptr, nullptr, nullptr, 0,
+             dtype == RMX_F32_TF32 ? 1 : 0};
   return run_gemm("test_gemm", d, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -52,10 +52,17 @@
 namespace rmx {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;  // BK, UMMA_K: 16-bit elements
 constexpr int A_BYTES = BM * BK * 2;           // 16 KB
 constexpr int B_BYTES = BN * BK * 2;           // 32 KB
 constexpr int MN_CHUNK_BYTES = BK * 128;       // one 64-wide MN chunk of an MN-major tile
+// A k-block is one 128-byte swizzle row of every operand row: 64 elements of
+// a 16-bit type, 32 of fp32 (read by the tensor cores as TF32); one MMA
+// takes 32 bytes of K (16 or 8 elements), four per k-block either way.
+template <typename T> struct KBlock {
+  static constexpr int E = 128 / (int)sizeof(T);
+  static constexpr int MMA_K = 32 / (int)sizeof(T);
+};
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * BN;        // 512
 constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter
@@ -230,12 +237,30 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   else
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 or bf16 in, fp32 out).
-// For a CTA pair (issued by the even CTA only) A and D are split by rows and
-// B by columns between the two CTAs, at the same shared / TMEM offsets.
-template <bool PAIR>
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem]^T: kind::f16 (fp16 or bf16 in) or, for
+// fp32 operands, kind::tf32; fp32 accumulation.  For a CTA pair (issued by
+// the even CTA only) A and D are split by rows and B by columns between the
+// two CTAs, at the same shared / TMEM offsets.
+template <typename T, bool PAIR>
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+  if (std::is_same<T, float>::value) {
+    if (PAIR)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "setp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+          ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "setp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+          ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    return;
+  }
   if (PAIR)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -300,12 +325,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A/B type
-// (bits 7-9 / 10-12: 0 = fp16, 1 = bf16), A/B major (bits 15 / 16:
-// 0 = K-major, 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+// Instruction descriptor, kind::f16 / kind::tf32: D fp32 (bits 4-5 = 1),
+// A/B type (bits 7-9 / 10-12: 0 = fp16, 1 = bf16, 2 = tf32), A/B major
+// (bits 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 (bits 17-22), M >> 4
+// (bits 24-28).
 template <typename T, bool A_MN, bool B_MN, int UMMA_M>
 __host__ __device__ constexpr uint32_t make_idesc() {
-  constexpr uint32_t ab = std::is_same<T, bf16>::value ? 1u : 0u;
+  constexpr uint32_t ab = std::is_same<T, bf16>::value ? 1u : std::is_same<T, float>::value ? 2u : 0u;
   return (1u << 4) | (ab << 7) | (ab << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UMMA_M >> 4) << 24);
 }
@@ -356,8 +382,9 @@ template <> __device__ __forceinline__ uint32_t pack2<f16>(float a, float b) {
 
 // Epilogue of 32 consecutive columns n_base .. n_base+31 of row m: bias /
 // residual in fp32, the Z statistics, and the result rounded and packed into
-// pk[0..15].  Columns at or past N (and rows past M) are computed from
-// whatever the accumulator holds; the tensor store clips them.
+// pk[0..15] (16-bit output, two columns per word) or pk[0..31] (fp32 output).
+// Columns at or past N (and rows past M) are computed from whatever the
+// accumulator holds; the tensor store clips them.
 template <typename T, int EPI>
 __device__ __forceinline__ void epilogue_convert(const Params& p, int g, int m, int n_base, const float* v,
                                                  ZSums* zs, uint32_t* pk) {
@@ -403,8 +430,13 @@ __device__ __forceinline__ void epilogue_convert(const Params& p, int g, int m, 
         else add(zs[1]);
       }
     }
+    if constexpr (sizeof(T) == 4) {
 #pragma unroll
-    for (int e = 0; e < V; e += 2) pk[(c + e) >> 1] = pack2<T>(o[e], o[e + 1]);
+      for (int e = 0; e < V; ++e) pk[c + e] = __float_as_uint(o[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < V; e += 2) pk[(c + e) >> 1] = pack2<T>(o[e], o[e + 1]);
+    }
   }
 }
 
@@ -546,7 +578,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (PAIR) tma_load_5d_pair(dst, map, fb, 0, 0, mn / 64, k / 8, gg);
             else tma_load_5d(dst, map, fb, 0, 0, mn / 64, k / 8, gg);
           };
-          const int k0 = kb * BK;
+          const int k0 = kb * KBlock<T>::E;
           const uint32_t a_dst = sA + s * A_BYTES, b_dst = sB + s * R::B_STAGE;
           if (!KT::A_MN) {
             if (a_n) load(a_dst, &tmA, k0, g, m0);                                      // map {K, G, M}
@@ -624,7 +656,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t a_base = sA + s * A_BYTES, b_base = sB + s * R::B_STAGE;
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
+          for (int k = 0; k < 4; ++k) {
             // K-major: advance 16 elements (32 bytes) inside the swizzle atom.
             // MN-major by chunks: advance 16 rows of 128 bytes; MN atoms one
             // chunk apart, K groups 1 KB apart.  Interleaved MN-major: advance
@@ -638,7 +670,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 KT::B_MN ? (p.mn_il ? sw128_desc(b_base + k * 2 * B_CH * 1024, 1024, B_CH * 1024)
                                     : sw128_desc(b_base + k * 2048, MN_CHUNK_BYTES, 1024))
                          : sw128_desc(b_base + k * 32, 16, 1024);
-            umma_f16<PAIR>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma<T, PAIR>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           if (PAIR) umma_commit_pair(empty_bar(s));
           else umma_commit<false>(empty_bar(s));
@@ -693,31 +725,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         released = true;
       };
+      // A staged box is 32 rows x 128 bytes: 64 columns of a 16-bit output,
+      // 32 of fp32 (two boxes per 64 columns).
+      constexpr int OW = sizeof(T) == 4 ? 2 : 1;  // 32-bit words per output column pair
       for (int j0 = 0; j0 < COLS; j0 += 64) {
         if (n0 + c0 + j0 >= p.N || m0 + q * 32 >= p.M) break;  // warp-uniform
-        uint32_t pk[32];
+        uint32_t pk[32 * OW];
         {
           float v[64];
           tmem_ld_32x64(t_row + (uint32_t)j0, v);
           if (j0 + 64 >= COLS || n0 + c0 + j0 + 64 >= p.N) release();
           epilogue_convert<T, EPI>(p, g, m, n0 + c0 + j0, v, zs, pk);
-          epilogue_convert<T, EPI>(p, g, m, n0 + c0 + j0 + 32, v + 32, zs, pk + 16);
+          epilogue_convert<T, EPI>(p, g, m, n0 + c0 + j0 + 32, v + 32, zs, pk + 16 * OW);
         }
-        // The previous box must have been read out of the staging buffer.
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-        // Row `lane` of the box: eight 16-byte chunks, chunk j at position
-        // j ^ (row % 8) (the tensor map's 128-byte swizzle).
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_shared_v4(stage + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), pk[4 * j], pk[4 * j + 1],
-                       pk[4 * j + 2], pk[4 * j + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (KIND == GEMM_WGRAD) tma_store_3d(&tmC, stage, n0 + c0 + j0, m0 + q * 32, g);   // map {N, M, G}
-          else tma_store_3d(&tmC, stage, n0 + c0 + j0, g, m0 + q * 32);                    // map {N, G, M}
-          bulk_commit();
+        for (int h = 0; h < OW; ++h) {
+          const int nb = n0 + c0 + j0 + h * 32;
+          if (h > 0 && nb >= p.N) break;  // warp-uniform
+          // The previous box must have been read out of the staging buffer.
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          // Row `lane` of the box: eight 16-byte chunks, chunk j at position
+          // j ^ (row % 8) (the tensor map's 128-byte swizzle).
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(stage + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), pk[32 * h + 4 * j],
+                         pk[32 * h + 4 * j + 1], pk[32 * h + 4 * j + 2], pk[32 * h + 4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (KIND == GEMM_WGRAD) tma_store_3d(&tmC, stage, nb, m0 + q * 32, g);   // map {N, M, G}
+            else tma_store_3d(&tmC, stage, nb, g, m0 + q * 32);                    // map {N, G, M}
+            bulk_commit();
+          }
         }
       }
       if (!released) release();
@@ -785,7 +825,9 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t
   cuuint64_t strides[2] = {s1, s2};
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
-  const CUtensorMapDataType dt = dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = dtype == 0   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -826,6 +868,20 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   return launch_k(k, dim3(2 * (clusters > 0 ? clusters : 1)), dim3(THREADS), SMEM_BYTES, st, 2, a, b, c, p);
 }
 
+// fp32 operands (TF32 tensor cores): both operands K-major (the dgrad
+// form); the caller stages transposed copies of MN-major operands.
+template <bool PAIR>
+cudaError_t dispatch_tf32(const GemmDesc& d, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                          const Params& p, cudaStream_t st) {
+  switch (d.epi) {
+    case EPI_STORE: return launch_tc<float, GEMM_DGRAD, EPI_STORE, PAIR>(a, b, c, p, st);
+    case EPI_RESID: return launch_tc<float, GEMM_DGRAD, EPI_RESID, PAIR>(a, b, c, p, st);
+    case EPI_BIAS_RESID: return launch_tc<float, GEMM_DGRAD, EPI_BIAS_RESID, PAIR>(a, b, c, p, st);
+    case EPI_BIAS_ZSTATS: return launch_tc<float, GEMM_DGRAD, EPI_BIAS_ZSTATS, PAIR>(a, b, c, p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <typename T, bool PAIR>
 cudaError_t dispatch_tc(const GemmDesc& d, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                         const Params& p, cudaStream_t st) {
@@ -858,8 +914,17 @@ int sm_count() {
 }
 
 bool gemm_tc_supported(const GemmDesc& d) {
-  if (d.dtype != 1 && d.dtype != 2) return false;
+  if (d.dtype != 0 && d.dtype != 1 && d.dtype != 2) return false;
   if (d.M <= 0 || d.N <= 0 || d.K <= 0 || d.G <= 0) return false;
+  if (d.dtype == 0) {
+    // TF32: K-major operands only (the dgrad form), 16-byte row strides.
+    if (!d.tf32 || d.kind != GEMM_DGRAD || d.N % 8 || d.K % 4) return false;
+    if ((d.a_rs | d.a_gs | d.c_rs | d.c_gs) % 4) return false;
+    if (d.epi == EPI_BIAS_ZSTATS && (BN / (EPI_WARPS / 4) != kZStatsTile || !d.zstats || d.split % 8)) return false;
+    return (d.epi == EPI_STORE || d.epi == EPI_RESID || d.epi == EPI_BIAS_RESID || d.epi == EPI_BIAS_ZSTATS) &&
+           encode_fn() != nullptr;
+  }
+  if (d.a_rs || d.a_gs || d.c_rs || d.c_gs) return false;  // explicit strides: TF32 path only
   // 16-byte row strides for the tensor maps and the vector epilogue.  The
   // weight-gradient GEMMs reduce over K = B, the outermost dimension of both
   // operands' maps (no stride of its own); a ragged last k-block is
@@ -876,7 +941,8 @@ bool gemm_tc_supported(const GemmDesc& d) {
 
 cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st) {
   if (!gemm_tc_supported(d)) return cudaErrorInvalidValue;
-  const uint64_t e = 2, M = d.M, N = d.N, K = d.K, G = d.G;
+  const uint64_t e = d.dtype == 0 ? 4 : 2, M = d.M, N = d.N, K = d.K, G = d.G;
+  const uint32_t BKE = (uint32_t)(128 / e);  // elements of a k-block
   // Paired mode whenever M spans at least two tiles (and the env switch
   // RMX_GEMM_PAIRS=0 is not set).
   static const bool pairs_on = [] {
@@ -891,13 +957,16 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   // checks them; else the operand comes as separate 64-wide chunks through
   // rank-3 maps).
   bool il = true;
+  // Activation rows [M, G, K] (defaults) or any (g, m) strides given.
+  const uint64_t a_gs = d.a_gs ? (uint64_t)d.a_gs : K, a_rs = d.a_rs ? (uint64_t)d.a_rs : G * K;
+  const uint64_t c_gs = d.c_gs ? (uint64_t)d.c_gs : N, c_rs = d.c_rs ? (uint64_t)d.c_rs : G * N;
   if (d.kind == GEMM_FWD || d.kind == GEMM_DGRAD) {
-    ok &= make_map(&ma, d.A, d.dtype, K, G, M, K * e, G * K * e, BK, 1, BM);          // A [M,G,K]
+    ok &= make_map(&ma, d.A, d.dtype, K, G, M, a_gs * e, a_rs * e, BKE, 1, BM);       // A [M,G,K]
     if (d.kind == GEMM_FWD) {
       il = il && make_map_mn5(&mb, d.Bm, d.dtype, N, K, G, N * e, K * N * e, b_chunks);  // W [G,K,N]
       if (!il) ok &= make_map(&mb, d.Bm, d.dtype, N, K, G, N * e, K * N * e, 64, BK, 1);
     } else {
-      ok &= make_map(&mb, d.Bm, d.dtype, K, N, G, K * e, N * K * e, BK, pair ? BN / 2 : BN, 1);  // W [G,N,K]
+      ok &= make_map(&mb, d.Bm, d.dtype, K, N, G, K * e, N * K * e, BKE, pair ? BN / 2 : BN, 1);  // W [G,N,K]
     }
   } else {
     il = il && make_map_mn5(&ma, d.A, d.dtype, M, K, G, G * M * e, M * e, BM / 64) &&   // A [K,G,M]
@@ -909,8 +978,9 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   }
   if (d.kind == GEMM_DGRAD) il = false;  // no MN-major operand
   // Output boxes of 32 rows x 64 columns, written by the epilogue warps.
-  if (d.kind == GEMM_WGRAD) ok &= make_map(&mc, d.C, d.dtype, N, M, G, N * e, M * N * e, 64, 32, 1);  // C [G,M,N]
-  else ok &= make_map(&mc, d.C, d.dtype, N, G, M, N * e, G * N * e, 64, 1, 32);                       // C [M,G,N]
+  // (32 rows x 128 bytes: 64 columns of a 16-bit type, 32 of fp32.)
+  if (d.kind == GEMM_WGRAD) ok &= make_map(&mc, d.C, d.dtype, N, M, G, N * e, M * N * e, BKE, 32, 1);  // C [G,M,N]
+  else ok &= make_map(&mc, d.C, d.dtype, N, G, M, c_gs * e, c_rs * e, BKE, 1, 32);                    // C [M,G,N]
   if (!ok) return cudaErrorInvalidValue;
   Params p;
   p.mn_il = il ? 1 : 0;
@@ -922,7 +992,7 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.tiles_n = (d.N + BN - 1) / BN;
   p.tiles_per_group = p.tiles_m * p.tiles_n;
   p.num_tiles = p.tiles_per_group * d.G;
-  p.num_kb = (d.K + BK - 1) / BK;
+  p.num_kb = (d.K + (int)BKE - 1) / (int)BKE;
   p.pairs_m = (p.tiles_m + 1) / 2;
   p.pair_tiles_per_group = p.pairs_m * p.tiles_n;
   p.num_pair_tiles = p.pair_tiles_per_group * d.G;
@@ -931,8 +1001,8 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
     p.out_rs = d.N;
     p.out_gs = (long long)d.M * d.N;
   } else {
-    p.out_rs = (long long)d.G * d.N;
-    p.out_gs = d.N;
+    p.out_rs = (long long)c_rs;
+    p.out_gs = (long long)c_gs;
   }
   p.bias = d.bias;
   p.bias_gs = d.N;
@@ -944,6 +1014,7 @@ cudaError_t gemm_tc_launch(const GemmDesc& d, unsigned int* err, cudaStream_t st
   p.zstats = d.zstats;
   p.split = d.split;
   p.zgroups = (d.N + kZStatsTile - 1) / kZStatsTile;
+  if (d.dtype == 0) return pair ? dispatch_tf32<true>(d, ma, mb, mc, p, st) : dispatch_tf32<false>(d, ma, mb, mc, p, st);
   if (d.dtype == 1)
     return pair ? dispatch_tc<bf16, true>(d, ma, mb, mc, p, st) : dispatch_tc<bf16, false>(d, ma, mb, mc, p, st);
   return pair ? dispatch_tc<f16, true>(d, ma, mb, mc, p, st) : dispatch_tc<f16, false>(d, ma, mb, mc, p, st);

@@ -121,6 +121,10 @@ struct PadMap {
   int outer, rows, rows_p, cols, cols_p, halves;
 };
 cudaError_t launch_pad_copy(const void* src, void* dst, int dtype, const PadMap& m, bool pack, cudaStream_t st);
+// Batched fp32 transpose for the TF32 contractions, whose operands must be
+// K-major: dst[g][c][r] = src[g*gs + r*rs + c] (r < R), zero for R <= r < Rp.
+cudaError_t launch_transpose_f32(const float* src, float* dst, int G, int R, int Cc, long long gs, long long rs,
+                                 int Rp, cudaStream_t st);
 
 // ------------------------------------------------------------------ GEMMs
 enum GemmKind { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
@@ -157,6 +161,12 @@ struct GemmDesc {
   const void* resid;
   float* zstats;  // EPI_BIAS_ZSTATS only
   int split;      // EPI_BIAS_ZSTATS: first column of the G half (H)
+  // fp32 (dtype 0): 1 runs the contraction on the tensor cores with TF32
+  // operands (dgrad form only; see gemm_tc_supported), 0 on the CUDA cores.
+  int tf32 = 0;
+  // Optional element strides of A's (g, m) and C's (g, m) indices in the
+  // FWD / DGRAD forms (0: the [M, G, K] / [M, G, N] defaults); TF32 only.
+  long long a_gs = 0, a_rs = 0, c_gs = 0, c_rs = 0;
 };
 
 bool gemm_tc_supported(const GemmDesc& d);

@@ -42,7 +42,39 @@ __global__ void __launch_bounds__(256) k_pad_copy(const E* __restrict__ src, E* 
   }
 }
 
+// dst[g][c][r] = src[g * gs + r * rs + c] for r < R, 0 for R <= r < Rp: one
+// 32 x 32 tile per CTA through shared memory, reads along c and writes
+// along r coalesced.
+__global__ void __launch_bounds__(256) k_transpose_f32(const float* __restrict__ src, float* __restrict__ dst,
+                                                       int R, int Cc, long long gs, long long rs, int Rp) {
+  pdl_enter();
+  __shared__ float tile[32][33];
+  const int g = blockIdx.z, c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const float* s = src + (size_t)g * gs;
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int r = r0 + ty + k, c = c0 + tx;
+    tile[ty + k][tx] = (r < R && c < Cc) ? s[(size_t)r * rs + c] : 0.f;
+  }
+  __syncthreads();
+  float* d = dst + (size_t)g * Cc * Rp;
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int c = c0 + ty + k, r = r0 + tx;
+    if (c < Cc && r < Rp) d[(size_t)c * Rp + r] = tile[tx][ty + k];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_f32(const float* src, float* dst, int G, int R, int Cc, long long gs, long long rs,
+                                 int Rp, cudaStream_t st) {
+  if (G < 0 || R < 0 || Cc < 0 || Rp < R) return cudaErrorInvalidValue;
+  if (G == 0 || Cc == 0 || Rp == 0) return cudaSuccess;
+  const dim3 grid((Cc + 31) / 32, (Rp + 31) / 32, G);
+  return launch_k(k_transpose_f32, grid, dim3(256), 0, st, 1, src, dst, R, Cc, gs, rs, Rp);
+}
 
 cudaError_t launch_pad_copy(const void* src, void* dst, int dtype, const PadMap& m, bool pack, cudaStream_t st) {
   if (m.outer < 0 || m.rows < 0 || m.rows > m.rows_p || m.cols > m.cols_p || m.halves < 1 ||

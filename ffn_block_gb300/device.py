@@ -12,7 +12,7 @@ import torch
 from . import binding as B
 from .inputs import PARAM_NAMES, Shape
 
-TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "tf32": torch.float32}
 
 
 def _upload(a: np.ndarray, dt: torch.dtype, device) -> torch.Tensor:

@@ -96,7 +96,7 @@ def he_uniform(rng: np.random.Generator, shape) -> np.ndarray:
 def round_to_storage(a: np.ndarray, dtype: str) -> np.ndarray:
     """Round float32 values to the storage dtype; returns float32 holding them."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    if dtype == "f32":
+    if dtype in ("f32", "tf32"):   # tf32: float32 storage (only the contractions differ)
         return a
     if dtype == "f16":
         return a.astype(np.float16).astype(np.float32)

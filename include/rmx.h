@@ -54,7 +54,19 @@ typedef enum {
   RMX_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up           */
 } rmx_status;
 
-typedef enum { RMX_F32 = 0, RMX_BF16 = 1, RMX_F16 = 2 } rmx_dtype;
+/* Storage type of every tensor, and the contract of the four per-token
+ * contractions:
+ *   RMX_F32       float32, contractions in IEEE float32 on the CUDA cores
+ *                 (strict: no TF32);
+ *   RMX_BF16, RMX_F16  16-bit storage, contractions on the tensor cores with
+ *                 float32 accumulation;
+ *   RMX_F32_TF32  float32 storage, contractions on the tensor cores with the
+ *                 operands read as TF32 (10-bit mantissa; the hardware drops
+ *                 the low 13 bits of each float32 operand) and float32
+ *                 accumulation -- the page's "--dtype float32 --tf32" option
+ *                 (section "Run the benchmark").  Everything outside the
+ *                 contractions is float32 as under RMX_F32. */
+typedef enum { RMX_F32 = 0, RMX_BF16 = 1, RMX_F16 = 2, RMX_F32_TF32 = 3 } rmx_dtype;
 
 /* Block shape.  x, y, dy, dx are [B,T,D]; H is the FFN width (H = k*D on the
  * page, k in {2,3}).  Requires B >= 0, T >= 1, D >= 1, H >= 1, D % T == 0.
@@ -89,11 +101,18 @@ typedef struct {
  * scratch (per-tile partial statistics of Z), then norm1's input
  * s1 = token_mix(norm0(x)) + x [B,T,D] in the storage dtype.  Each segment
  * starts on a 256-byte boundary.
+ * Rows whose length is not a multiple of 8 elements (D or H) are processed
+ * as zero-padded copies of pitch roundup(D, 8) and roundup(H, 8): the
+ * tensors above then have those pitches, and `saved` also holds the padded
+ * copies of x, y and every parameter (the backward reuses them).  Under
+ * RMX_F32_TF32 it also holds transposed copies of w1 and wout.
  * Returns 0 for an invalid config. */
 size_t rmx_saved_bytes(const rmx_config* cfg);
 
 /* Bytes of backward scratch (device, caller-owned, contents undefined between
- * calls).  Returns 0 for an invalid config. */
+ * calls); for padded rows it includes the padded copies of dy, dx and every
+ * gradient, under RMX_F32_TF32 transposed copies of hidden, ds2, out1 and dZ.
+ * Returns 0 for an invalid config. */
 size_t rmx_workspace_bytes(const rmx_config* cfg);
 
 /* Forward pass.  x [B,T,D] (device) -> y [B,T,D] (device), filling `saved`
@@ -173,7 +192,9 @@ rmx_status rmx_test_bounded_wait(int limit_us, rmx_stream stream);
  * forward (C[g] = A[g] @ W[g], A rows strided by G*K, W [G,K,N]);
  * kind 1 = dgrad (C[g] = A[g] @ W[g]^T, W [G,N,K]); kind 2 = wgrad
  * (C[g] = A[g]^T @ Bm[g], A [R,G,M], Bm [R,G,N], C [G,M,N]).  For kinds 0/1
- * A is [M,G,K] and C is [M,G,N].  Used to check the GEMM engine in
+ * A is [M,G,K] and C is [M,G,N].  dtype is an rmx_dtype; RMX_F32_TF32 runs
+ * kind 1 on the tensor cores (the other kinds, whose operands are not both
+ * K-major, run in strict float32).  Used to check the GEMM engine in
  * isolation. */
 rmx_status rmx_test_gemm(int kind, int dtype, int M, int N, int K, int G, const void* A,
                          const void* Bm, void* C, rmx_stream stream);

@@ -7,7 +7,13 @@ from ffn_block_gb300 import inputs as I
 from oracle import rmx_oracle as O
 
 # Norm-relative tolerance per storage contract: strict fp32 1e-4, 16-bit 2e-2.
-TOL = {"f32": 1e-4, "bf16": 2e-2, "f16": 2e-2}
+# TF32 contractions (fp32 storage): the tensor cores read each fp32 operand
+# with a 10-bit mantissa, a relative error of at most 2^-10 per operand and
+# 2^-9 per product.  Summed over K with random signs, a contraction's result
+# is off by about 2^-10 of its norm; a gradient passes through up to three
+# contractions and the LayerNorm backwards between them, which can each
+# amplify it a few times: 5e-3 bounds that chain.
+TOL = {"f32": 1e-4, "bf16": 2e-2, "f16": 2e-2, "tf32": 5e-3}
 NAMES = ("y", "dx") + I.PARAM_NAMES
 
 

@@ -14,7 +14,10 @@ pytestmark = pytest.mark.gpu
 
 # Output is rounded to the storage type once: ~2^-9 (bf16) / 2^-12 (fp16)
 # relative, far below these bounds; fp32 accumulates in a different order.
-TOL = {"f32": 1e-5, "bf16": 6e-3, "f16": 2e-3}
+TOL = {"f32": 1e-5, "bf16": 6e-3, "f16": 2e-3,
+       # TF32 operands: at most 2^-9 relative error per product; random-sign
+       # sums keep the norm-relative error near 2^-10.
+       "tf32": 3e-3}
 
 
 def _run(kind, dtype, M, N, K, G, seed=0):
@@ -85,3 +88,23 @@ def test_grouped_gemm_paired_tiles(kind, dtype, shape):
     assert np.all(np.isfinite(got))
     err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert err < TOL[dtype], err
+
+
+# TF32 (fp32 storage): the dgrad form (both operands K-major) runs on the
+# tensor cores; the forward and weight-gradient forms read an operand
+# MN-major and run in strict fp32 (the block stages transposed copies so
+# that all of its contractions take the dgrad form).
+@pytest.mark.parametrize("shape", SHAPES + PAIR_SHAPES)
+def test_tf32_dgrad_form_on_tensor_cores(shape):
+    M, N, K, G = shape
+    B.rmx_profile_read()
+    B.rmx_profile_enable(True)
+    try:
+        got, ref = _run(1, "tf32", M, N, K, G, seed=5)
+    finally:
+        B.rmx_profile_enable(False)
+    assert set(B.rmx_profile_read()) == {"test_gemm"}
+    assert np.all(np.isfinite(got))
+    err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err < TOL["tf32"], err
+    assert err > 1e-7   # the operands really were read at TF32 precision
