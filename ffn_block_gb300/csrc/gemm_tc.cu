@@ -205,6 +205,11 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Prefetch of the 128-byte line holding p into L1 (a hint; no fault on any
+// address this kernel could read).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -363,9 +368,11 @@ __device__ __forceinline__ void pair_tile_coords(const Params& p, int pt, int ra
   n0 = tn * BN;
 }
 
-// Shifted sums of one half of a Z row over one column group.
+// Shifted sums of one half of a Z row over one column group, kept as pairs
+// (even and odd columns) for the packed fp32x2 arithmetic.
 struct ZSums {
-  float n, k, s, q;  // count, shift, sum(x - k), sum((x - k)^2)
+  float n, k;   // count, shift
+  float2 s, q;  // sum(x - k), sum((x - k)^2)
 };
 
 // Two floats rounded to the storage type, packed into 32 bits (lower
@@ -378,6 +385,12 @@ template <> __device__ __forceinline__ uint32_t pack2<bf16>(float a, float b) {
 template <> __device__ __forceinline__ uint32_t pack2<f16>(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+// The stored values of a packed word, back as floats (exact).
+template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack2<bf16>(uint32_t w) { return bf16x2_to_f2(w); }
+template <> __device__ __forceinline__ float2 unpack2<f16>(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 // Epilogue of 32 consecutive columns n_base .. n_base+31 of row m: bias /
@@ -395,7 +408,8 @@ __device__ __forceinline__ void epilogue_convert(const Params& p, int g, int m, 
     float o[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) o[e] = v[c + e];
-    if (n < p.N && m < p.M) {
+    const bool in = n < p.N && m < p.M;
+    if (in) {
       if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_ZSTATS) {
         float bv[V];
         load_vec(reinterpret_cast<const T*>(p.bias) + (size_t)g * p.bias_gs + n, bv);
@@ -408,27 +422,6 @@ __device__ __forceinline__ void epilogue_convert(const Params& p, int g, int m, 
 #pragma unroll
         for (int e = 0; e < V; ++e) o[e] += rv[e];
       }
-      if (EPI == EPI_BIAS_ZSTATS) {
-        // Shifted sums of the stored (rounded) values of this half: the
-        // shift is the half's first value in this column group, so the
-        // centred second moment is formed without cancellation trouble.
-        float r[V];
-#pragma unroll
-        for (int e = 0; e < V; ++e) r[e] = to_f(from_f<T>(o[e]));
-        // Constant indices only, so the sums stay in registers.
-        auto add = [&](ZSums& z) {
-          if (z.n == 0.f) z.k = r[0];
-#pragma unroll
-          for (int e = 0; e < V; ++e) {
-            const float dv = r[e] - z.k;
-            z.s += dv;
-            z.q = fmaf(dv, dv, z.q);
-          }
-          z.n += (float)V;
-        };
-        if (n < p.split) add(zs[0]);
-        else add(zs[1]);
-      }
     }
     if constexpr (sizeof(T) == 4) {
 #pragma unroll
@@ -436,6 +429,32 @@ __device__ __forceinline__ void epilogue_convert(const Params& p, int g, int m, 
     } else {
 #pragma unroll
       for (int e = 0; e < V; e += 2) pk[(c + e) >> 1] = pack2<T>(o[e], o[e + 1]);
+    }
+    if (EPI == EPI_BIAS_ZSTATS && in) {
+      // Shifted sums of the stored (rounded) values of this half, read back
+      // from the words just packed: the shift is the half's first value in
+      // this column group, so the centred second moment is formed without
+      // cancellation trouble.
+      float2 r[V / 2];
+#pragma unroll
+      for (int e = 0; e < V; e += 2) {
+        if constexpr (sizeof(T) == 4) r[e / 2] = make_float2(o[e], o[e + 1]);
+        else r[e / 2] = unpack2<T>(pk[(c + e) >> 1]);
+      }
+      // Constant indices only, so the sums stay in registers.
+      auto add = [&](ZSums& z) {
+        if (z.n == 0.f) z.k = r[0].x;
+        const float2 nk = f2(-z.k);
+#pragma unroll
+        for (int e = 0; e < V / 2; ++e) {
+          const float2 dv = add2(r[e], nk);
+          z.s = add2(z.s, dv);
+          z.q = fma2(dv, dv, z.q);
+        }
+        z.n += (float)V;
+      };
+      if (n < p.split) add(zs[0]);
+      else add(zs[1]);
     }
   }
 }
@@ -702,6 +721,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       coords(tile, rank, g, m0, n0);
       const int acc = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_ZSTATS) {
+        // While the accumulator is still being computed: pull the tile's
+        // bias columns into L1, so the epilogue's loads of them do not wait
+        // on L2.  (Prefetching the residual rows measured slower.)
+        const int n1 = n0 + ch * COLS;
+        if (lane < (COLS * (int)sizeof(T)) / 128 && n1 + lane * (128 / (int)sizeof(T)) < p.N)
+          prefetch_l1(reinterpret_cast<const T*>(p.bias) + (size_t)g * p.bias_gs + n1 + lane * (128 / sizeof(T)));
+      }
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait_bounded(tfull_bar(acc), aph, p.wait_limit_ns, p.err, ERRBIT_WAIT_EPILOGUE, abort_flag);
@@ -711,7 +738,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m = m0 + q * 32 + lane;
       const int c0 = ch * COLS;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
-      ZSums zs[2] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      ZSums zs[2] = {{0.f, 0.f, {0.f, 0.f}, {0.f, 0.f}}, {0.f, 0.f, {0.f, 0.f}, {0.f, 0.f}}};
       // The accumulator is released as soon as its last columns are in
       // registers, before they are converted and stored, so that the store
       // path never delays the next tile's MMAs.
@@ -763,10 +790,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!released) release();
       if (EPI == EPI_BIAS_ZSTATS && m < p.M && n0 + c0 < p.N) {
         float4 w;
-        w.x = zs[0].n > 0.f ? zs[0].k + zs[0].s / zs[0].n : 0.f;
-        w.y = zs[0].n > 0.f ? fmaxf(zs[0].q - zs[0].s * zs[0].s / zs[0].n, 0.f) : 0.f;
-        w.z = zs[1].n > 0.f ? zs[1].k + zs[1].s / zs[1].n : 0.f;
-        w.w = zs[1].n > 0.f ? fmaxf(zs[1].q - zs[1].s * zs[1].s / zs[1].n, 0.f) : 0.f;
+        const float s0 = zs[0].s.x + zs[0].s.y, q0 = zs[0].q.x + zs[0].q.y;
+        const float s1 = zs[1].s.x + zs[1].s.y, q1 = zs[1].q.x + zs[1].q.y;
+        w.x = zs[0].n > 0.f ? zs[0].k + s0 / zs[0].n : 0.f;
+        w.y = zs[0].n > 0.f ? fmaxf(q0 - s0 * s0 / zs[0].n, 0.f) : 0.f;
+        w.z = zs[1].n > 0.f ? zs[1].k + s1 / zs[1].n : 0.f;
+        w.w = zs[1].n > 0.f ? fmaxf(q1 - s1 * s1 / zs[1].n, 0.f) : 0.f;
         const int grp = (n0 + c0) / kZStatsTile;
         *reinterpret_cast<float4*>(p.zstats + (((size_t)m * p.G + g) * p.zgroups + grp) * 4) = w;
       }

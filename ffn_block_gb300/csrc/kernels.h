@@ -80,7 +80,7 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats
 // lng_w, lng_b ([nbblk*T, H] each) and b1 ([nbblk, T, 2H]) from dh, Z and the
 // forward's inner-LayerNorm statistics.  CTA (bblk, t) owns up to nb <=
 // kGateBwdMaxRows rows of token t and the whole row.
-constexpr int kGateBwdMaxRows = 64;
+constexpr int kGateBwdMaxRows = 256;
 int gate_bwd_ctas_per_sm(const RowArgs& a);
 bool gate_bwd_fused_supported(const RowArgs& a);
 cudaError_t launch_gate_bwd(const RowArgs& a, const void* dh, const void* Z, const float* muU, const float* rU,
