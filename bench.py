@@ -53,6 +53,9 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=None, help="override T (profiling a smaller case)")
     ap.add_argument("--dim", type=int, default=None, help="override D (profiling a smaller case)")
     ap.add_argument("--hidden", type=int, default=None, help="override H (profiling a smaller case)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step as a replay of a captured CUDA graph (rmx_graph_launch) instead of the "
+                         "two calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-reps", type=int, default=6, help="timed oracle calls of the CPU baseline")
@@ -427,6 +430,15 @@ def run_ours(args) -> dict | None:
         torch.cuda.synchronize()
     # Timed region: K steps with no event inside a step (the library's
     # per-kernel timing is off), so the kernels run back to back as in use.
+    graph = None
+    timed_step = lambda: blk.step(stream)
+    if args.graph:
+        graph = B.rmx_graph_create(blk.cfg, blk.x, blk.dy, blk.c_params, blk.saved, blk.saved_bytes, blk.y, blk.dx,
+                                   blk.c_grads, blk.ws, blk.ws_bytes)
+        timed_step = lambda: B.check(B.rmx_graph_launch(graph, stream), "rmx_graph_launch")
+        for _ in range(max(args.warmup, 1)):
+            timed_step()
+        torch.cuda.synchronize()
     launches0 = B.rmx_launch_count()
     barrier(ws)
     torch.cuda.synchronize()
@@ -435,13 +447,15 @@ def run_ours(args) -> dict | None:
         flush.zero_()                                    # L2 flush, outside the events
         torch.cuda.nvtx.range_push("rmx_step")
         starts[i].record(stream)
-        blk.step(stream)
+        timed_step()
         ends[i].record(stream)
         torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(ws)
     wall = time.perf_counter() - wall0
     launches = B.rmx_launch_count() - launches0
+    if graph is not None:
+        B.rmx_graph_destroy(graph)
     # The dominant kernel's own time from a second pass of K steps in which
     # only its launches are bracketed by events (on the stream they are
     # launched on), the others running back to back.
@@ -560,7 +574,8 @@ def run_ours(args) -> dict | None:
         "data": "synthetic (seeded he-uniform weights, standard-normal x and dy)",
         "config": {"workload": workload_name(args, shape), "B": shape.B, "T": shape.T,
                    "D": shape.D, "H": shape.H, "storage": shape.dtype, "parallelism": f"replicas x{ws}",
-                   "l2": "flushed before every step (outside the timed region)"},
+                   "l2": "flushed before every step (outside the timed region)",
+                   "launch": "CUDA graph replay" if args.graph else "rmx_forward + rmx_backward"},
         "step_roofline": step_roofline,
         "roofline": roofline,
         "e2e": e2e,

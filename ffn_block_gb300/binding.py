@@ -79,6 +79,10 @@ _SIGNATURES = {
     "rmx_test_bounded_wait": (_I, [_I, _VP]),
     "rmx_test_gemm": (_I, [_I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP]),
     "rmx_ln2_backward_noalloc": (_I, [_P(rmx_config), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "rmx_graph_create": (_I, [_P(rmx_config), _VP, _VP, _P(rmx_params), _VP, _SZ, _VP, _VP, _P(rmx_grads), _VP,
+                              _SZ, _P(_VP)]),
+    "rmx_graph_launch": (_I, [_VP, _VP]),
+    "rmx_graph_destroy": (_I, [_VP]),
 }
 
 _lib = None
@@ -216,3 +220,21 @@ def rmx_ln2_backward_noalloc(cfg, dy, s2, mean2, rstd2, gamma2, ds2, dgamma2, db
     return lib().rmx_ln2_backward_noalloc(ctypes.byref(cfg), _ptr(dy), _ptr(s2), _ptr(mean2), _ptr(rstd2),
                                           _ptr(gamma2), _ptr(ds2), _ptr(dgamma2), _ptr(dbeta2), _ptr(dbout),
                                           _stream(stream))
+
+
+def rmx_graph_create(cfg, x, dy, params: rmx_params, saved, saved_bytes: int, y, dx, grads: rmx_grads, ws,
+                     ws_bytes: int) -> int:
+    """Returns an opaque graph handle (an int); raises on failure."""
+    h = ctypes.c_void_p()
+    check(lib().rmx_graph_create(ctypes.byref(cfg), _ptr(x), _ptr(dy), ctypes.byref(params), _ptr(saved),
+                                 saved_bytes, _ptr(y), _ptr(dx), ctypes.byref(grads), _ptr(ws), ws_bytes,
+                                 ctypes.byref(h)), "rmx_graph_create")
+    return h.value
+
+
+def rmx_graph_launch(g: int, stream=None) -> int:
+    return lib().rmx_graph_launch(g, _stream(stream))
+
+
+def rmx_graph_destroy(g: int) -> int:
+    return lib().rmx_graph_destroy(g)

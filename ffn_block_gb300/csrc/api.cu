@@ -26,6 +26,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -814,6 +815,70 @@ rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host, const r
   if (!ok(cudaEventRecord(cs->done, cs->s))) return RMX_ERR_CUDA;
   if (!ok(cudaStreamWaitEvent(st, cs->done, 0))) return RMX_ERR_CUDA;
   return RMX_OK;
+}
+
+// ------------------------------------------------------------------ graph replay
+struct rmx_graph_st {
+  cudaGraphExec_t exec = nullptr;
+  long long launches = 0;  // kernel launches of one replay
+};
+
+rmx_status rmx_graph_create(const rmx_config* cfg, const void* x, const void* dy, const rmx_params* params,
+                            void* saved, size_t saved_bytes, void* y, void* dx, const rmx_grads* grads, void* ws,
+                            size_t ws_bytes, rmx_graph* out) {
+  if (!out) return RMX_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!config_ok(cfg)) return RMX_ERR_INVALID_ARG;
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return RMX_ERR_CUDA;
+  // Relaxed capture: the first use of the library on a device looks up
+  // symbol addresses and kernel attributes, which are not stream work.
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return RMX_ERR_CUDA;
+  }
+  const bool prof = g_prof.exchange(false);  // no profiling events inside a graph
+  const long long l0 = g_launches.load();
+  rmx_status st = rmx_forward(cfg, x, params, saved, saved_bytes, y, reinterpret_cast<rmx_stream>(cs));
+  if (st == RMX_OK)
+    st = rmx_backward(cfg, x, dy, saved, saved_bytes, params, dx, grads, ws, ws_bytes,
+                      reinterpret_cast<rmx_stream>(cs));
+  const long long n = g_launches.load() - l0;
+  g_prof.store(prof);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cs, &graph);
+  cudaStreamDestroy(cs);
+  if (st != RMX_OK || ec != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return st != RMX_OK ? st : RMX_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) return RMX_ERR_CUDA;
+  rmx_graph g = new (std::nothrow) rmx_graph_st;
+  if (!g) {
+    cudaGraphExecDestroy(exec);
+    return RMX_ERR_CUDA;
+  }
+  g->exec = exec;
+  g->launches = n;
+  *out = g;
+  return RMX_OK;
+}
+
+rmx_status rmx_graph_launch(rmx_graph g, rmx_stream stream) {
+  if (!g || !g->exec) return RMX_ERR_INVALID_ARG;
+  if (cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMX_ERR_CUDA;
+  g_launches.fetch_add(g->launches);
+  return RMX_OK;
+}
+
+rmx_status rmx_graph_destroy(rmx_graph g) {
+  if (!g) return RMX_OK;
+  const cudaError_t e = g->exec ? cudaGraphExecDestroy(g->exec) : cudaSuccess;
+  delete g;
+  return e == cudaSuccess ? RMX_OK : RMX_ERR_CUDA;
 }
 
 rmx_status rmx_check(rmx_stream stream) {

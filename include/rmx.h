@@ -154,6 +154,25 @@ rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host,
                          const rmx_grads* grads, void* saved, size_t saved_bytes,
                          void* ws, size_t ws_bytes, rmx_stream stream);
 
+/* CUDA-graph replay of one whole step (rmx_forward then rmx_backward) on
+ * fixed buffers.  rmx_graph_create captures the step's kernel launches, with
+ * the arguments given here, into an executable graph (nothing runs yet);
+ * rmx_graph_launch replays it on `stream`, which computes exactly what the
+ * two calls would (same kernels, same order, same results); the launches keep
+ * their programmatic dependencies as graph edges.  Replaying saves the host
+ * cost of the launches, which dominates small blocks.  The buffers, shapes
+ * and parameter pointers are those of the capture: to change any of them,
+ * create a new graph (the values in the buffers may change between replays:
+ * new x, dy or parameters).  The library allocates nothing on the device;
+ * the handle (host memory) lives until rmx_graph_destroy.  Per-kernel
+ * profiling (rmx_profile_enable) does not apply inside a graph. */
+typedef struct rmx_graph_st* rmx_graph;
+rmx_status rmx_graph_create(const rmx_config* cfg, const void* x, const void* dy, const rmx_params* params,
+                            void* saved, size_t saved_bytes, void* y, void* dx, const rmx_grads* grads, void* ws,
+                            size_t ws_bytes, rmx_graph* out);
+rmx_status rmx_graph_launch(rmx_graph g, rmx_stream stream);
+rmx_status rmx_graph_destroy(rmx_graph g);
+
 /* Synchronises `stream`, then reads and clears the library's device error
  * word.  Returns RMX_ERR_TIMEOUT if a bounded wait in a kernel gave up since
  * the last check, RMX_ERR_CUDA if the stream reported an error, else RMX_OK. */

@@ -134,3 +134,18 @@ def test_test_hooks_validate_arguments(lib):
     assert B.rmx_test_bounded_wait(0) == B.RMX_ERR_INVALID_ARG
     assert B.rmx_test_gemm(3, "bf16", 8, 8, 8, 1, 0x1000, 0x1000, 0x1000) == B.RMX_ERR_INVALID_ARG
     assert B.rmx_test_gemm(0, "bf16", 8, 8, 8, 1, 0x1008, 0x1000, 0x1000) == B.RMX_ERR_ALIGNMENT
+
+
+def test_graph_entry_points_validate_arguments(lib):
+    import ctypes
+    assert B.lib().rmx_graph_create(None, None, None, None, None, 0, None, None, None, None, 0, None) == \
+        B.RMX_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    bad = B.make_config(2, 3, 64, 128, "bf16")      # D % T != 0
+    p = B.rmx_params(*([0x1000] * 14))
+    g = B.rmx_grads(*([0x1000] * 14))
+    assert B.lib().rmx_graph_create(ctypes.byref(bad), 0x1000, 0x1000, ctypes.byref(p), 0x1000, 1 << 20, 0x1000,
+                                    0x1000, ctypes.byref(g), 0x1000, 1 << 20, ctypes.byref(h)) == B.RMX_ERR_INVALID_ARG
+    assert h.value is None
+    assert B.rmx_graph_launch(None) == B.RMX_ERR_INVALID_ARG
+    assert B.rmx_graph_destroy(None) == B.RMX_OK
