@@ -354,12 +354,18 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
 // =========================================================================
 constexpr int kColsumChunkRows = 256;
 constexpr int kColsumCols = 128;  // columns per block (32 lanes x float4)
+// Jobs of at most this many partial rows (per-token bias gradients summed
+// over a few sample blocks) are summed "wide": each warp takes 128 columns
+// of all rows, eight warps 1024 columns per block, so that a job of many
+// columns and few rows is not spread over thousands of nearly idle blocks.
+constexpr int kColsumWideRows = 32;
 
 struct ColsumArgs {
   ColsumJob job[kMaxColsumJobs];
   float* chunk_out[kMaxColsumJobs];  // [nchunks][J] when nchunks > 1
   int nchunks[kMaxColsumJobs];
   int ncg[kMaxColsumJobs];           // column groups of kColsumCols
+  int wide[kMaxColsumJobs];          // 1: summed wide (see kColsumWideRows)
   int block_start[kMaxColsumJobs + 1];
   int njobs;
 };
@@ -389,6 +395,24 @@ __global__ void __launch_bounds__(256) k_colsums_chunks(const ColsumArgs a) {
   __shared__ float4 part[8][32];
   const int jb = colsum_job_of(a);
   const ColsumJob& job = a.job[jb];
+  if (a.wide[jb]) {  // block-uniform
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int j = ((blockIdx.x - a.block_start[jb]) * 8 + warp) * kColsumCols + lane * 4;
+    if (j >= job.J) return;
+    const float* col = job.part + j;
+    const size_t J = (size_t)job.J;
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int p = 0;
+    for (; p + 3 < job.P; p += 4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] = add4(acc[k], *reinterpret_cast<const float4*>(col + (size_t)(p + k) * J));
+    }
+    for (; p < job.P; ++p) acc[0] = add4(acc[0], *reinterpret_cast<const float4*>(col + (size_t)p * J));
+    store4<T>(job.out, j, add4(add4(acc[0], acc[1]), add4(acc[2], acc[3])));
+    return;
+  }
   const int local = blockIdx.x - a.block_start[jb];
   const int ch = local / a.ncg[jb], cg = local - ch * a.ncg[jb];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -539,13 +563,14 @@ bool colsum_plan(const ColsumJob* jobs, int njobs, float* scratch, size_t scratc
     a.job[i] = jobs[i];
     a.ncg[i] = (jobs[i].J + kColsumCols - 1) / kColsumCols;
     a.nchunks[i] = chunked ? (jobs[i].P + kColsumChunkRows - 1) / kColsumChunkRows : 1;
+    a.wide[i] = chunked && jobs[i].P <= kColsumWideRows ? 1 : 0;
     a.chunk_out[i] = nullptr;
     if (a.nchunks[i] > 1) {
       a.chunk_out[i] = next;
       next += (size_t)a.nchunks[i] * jobs[i].J;
     }
     a.block_start[i] = blocks;
-    blocks += chunked ? a.ncg[i] * a.nchunks[i] : (jobs[i].J + 31) / 32;
+    blocks += !chunked ? (jobs[i].J + 31) / 32 : a.wide[i] ? (a.ncg[i] + 7) / 8 : a.ncg[i] * a.nchunks[i];
   }
   a.block_start[njobs] = blocks;
   return chunked;
