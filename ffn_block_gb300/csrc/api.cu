@@ -491,20 +491,30 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
                                          reinterpret_cast<float*>(at(saved, L.woutT)), c.T, L.H, L.D,
                                          (long long)L.H * L.D, L.D, L.H, st)));
   }
+  // 16-bit rows up to H = 2560: the gate pass takes the statistics of Z
+  // itself (row in registers) and GEMM1 stores Z with the bias alone;
+  // otherwise GEMM1's epilogue (or a statistics pass) writes per-group
+  // statistics of Z that the gate pass merges.
+  const bool rows_gate = gate_fwd_rows_supported(L.ra);
   {
-    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, EPI_BIAS_ZSTATS, sd, c.B, 2 * L.H, L.D, c.T, out1,
-               tf32 ? at(saved, L.w1T) : p.w1, Z, p.b1, nullptr, zstats, L.H, tf32 ? 1 : 0};
-    const bool epilogue_stats = tc_engine(d);
+    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, rows_gate ? EPI_BIAS : EPI_BIAS_ZSTATS, sd, c.B, 2 * L.H, L.D, c.T,
+               out1, tf32 ? at(saved, L.w1T) : p.w1, Z, p.b1, nullptr, rows_gate ? nullptr : zstats, L.H,
+               tf32 ? 1 : 0};
+    const bool epilogue_stats = !rows_gate && tc_engine(d);
     RMX_TRY(run_gemm("gemm1_fwd", d, st));
-    if (!epilogue_stats) {
+    if (!rows_gate && !epilogue_stats) {
       Launch l("zstats", st);
       RMX_TRY(l.done(launch_zstats(L.ra, Z, zstats, st)));
     }
   }
   {
     Launch l("gate_fwd", st);
-    RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, zstats, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
-                                   hidden, st)));
+    if (rows_gate)
+      RMX_TRY(l.done(launch_gate_fwd_rows(L.ra, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
+                                          hidden, st)));
+    else
+      RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, zstats, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w,
+                                     p.lng_b, hidden, st)));
   }
   {
     GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, EPI_BIAS_RESID, sd, c.B, L.D, L.H, c.T, hidden,

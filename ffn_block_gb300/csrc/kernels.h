@@ -76,6 +76,12 @@ cudaError_t launch_ln2_bwd(const RowArgs& a, const void* dy, const void* s2, con
 cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, float* muU, float* rU,
                             float* muG, float* rG, const void* wx, const void* bx, const void* wg, const void* bg,
                             void* hidden, cudaStream_t st);
+// The same with the statistics taken in-pass from the row held in
+// registers (16-bit storage, H <= 2560): Z needs no group statistics.
+bool gate_fwd_rows_supported(const RowArgs& a);
+cudaError_t launch_gate_fwd_rows(const RowArgs& a, const void* Z, float* muU, float* rU, float* muG, float* rG,
+                                 const void* wx, const void* bx, const void* wg, const void* bg, void* hidden,
+                                 cudaStream_t st);
 // Single-pass gate backward: dZ and the column partials of lnx_w, lnx_b,
 // lng_w, lng_b ([nbblk*T, H] each) and b1 ([nbblk, T, 2H]) from dh, Z and the
 // forward's inner-LayerNorm statistics.  CTA (bblk, t) owns up to nb <=

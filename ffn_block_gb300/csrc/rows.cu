@@ -341,6 +341,113 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
 }
 
 // =========================================================================
+// F3 with the statistics taken in-pass (16-bit rows of at most
+// kGateRowVecs 16-byte vectors per half and lane, H <= 2560): one warp per
+// row holds the row's U and G halves in registers as loaded (packed), takes
+// the mean and then the centred sum of squares of each half over the Hl real
+// columns (two passes over registers, exact), writes the statistics and
+// hidden = LN_x(U) * silu(LN_gate(G)).  The GEMM that produces Z then needs
+// no statistics epilogue.  Every lane's loads are issued before the first
+// use, so a warp has its whole row (10 KB at H = 2560) in flight.
+// =========================================================================
+constexpr int kGateRowVecs = 10;
+
+template <typename T>
+__global__ void __launch_bounds__(256, 2) k_gate_fwd_rows(const T* __restrict__ Z, float* __restrict__ muU,
+                                                          float* __restrict__ rU, float* __restrict__ muG,
+                                                          float* __restrict__ rG, const T* __restrict__ wx,
+                                                          const T* __restrict__ bx, const T* __restrict__ wg,
+                                                          const T* __restrict__ bg, T* __restrict__ hidden, int N,
+                                                          int H, float eps, int Hl) {
+  pdl_enter();
+  constexpr int V = 8;  // 16-bit: eight columns per 16-byte vector
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (r >= N) return;
+  const T* zr = Z + (size_t)r * 2 * H;
+  const int nv = H / V;
+  uint4 u[kGateRowVecs], g[kGateRowVecs];
+#pragma unroll
+  for (int q = 0; q < kGateRowVecs; ++q) {
+    const int vi = lane + 32 * q;
+    if (vi < nv) {
+      u[q] = __ldcs(reinterpret_cast<const uint4*>(zr + vi * V));
+      g[q] = __ldcs(reinterpret_cast<const uint4*>(zr + H + vi * V));
+    }
+  }
+  auto pairs = [](const uint4& w, float2 (&p)[4]) { ld8<T>(reinterpret_cast<const T*>(&w), p); };
+  // Pass 1: sums (the padding columns hold zeros).
+  float2 su = f2(0.f), sg = f2(0.f);
+#pragma unroll
+  for (int q = 0; q < kGateRowVecs; ++q) {
+    if (lane + 32 * q < nv) {
+      float2 a[4], b[4];
+      pairs(u[q], a);
+      pairs(g[q], b);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        su = add2(su, a[k]);
+        sg = add2(sg, b[k]);
+      }
+    }
+  }
+  const float inv = 1.0f / (float)Hl;
+  const float mU = warp_sum(su.x + su.y) * inv, mG = warp_sum(sg.x + sg.y) * inv;
+  // Pass 2: centred sums of squares over the real columns.
+  float2 qu = f2(0.f), qg = f2(0.f);
+  const float2 nmU = f2(-mU), nmG = f2(-mG);
+#pragma unroll
+  for (int q = 0; q < kGateRowVecs; ++q) {
+    const int vi = lane + 32 * q;
+    if (vi < nv) {
+      float2 a[4], b[4];
+      pairs(u[q], a);
+      pairs(g[q], b);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float2 du = add2(a[k], nmU), dg = add2(b[k], nmG);
+        const int c = vi * V + 2 * k;
+        if (c >= Hl) du.x = dg.x = 0.f;
+        if (c + 1 >= Hl) du.y = dg.y = 0.f;
+        qu = fma2(du, du, qu);
+        qg = fma2(dg, dg, qg);
+      }
+    }
+  }
+  const float sU = 1.0f / sqrtf(warp_sum(qu.x + qu.y) * inv + eps);
+  const float sG = 1.0f / sqrtf(warp_sum(qg.x + qg.y) * inv + eps);
+  if (lane == 0) {
+    muU[r] = mU;
+    rU[r] = sU;
+    muG[r] = mG;
+    rG[r] = sG;
+  }
+  const float2 sU2 = f2(sU), cU2 = f2(-mU * sU), sG2 = f2(sG), cG2 = f2(-mG * sG);
+  T* hr = hidden + (size_t)r * H;
+#pragma unroll
+  for (int q = 0; q < kGateRowVecs; ++q) {
+    const int vi = lane + 32 * q;
+    if (vi < nv) {
+      const int h0 = vi * V;
+      float2 a[4], b[4], w0[4], w1[4], w2[4], w3[4], o[4];
+      pairs(u[q], a);
+      pairs(g[q], b);
+      ld8<T>(wx + h0, w0);
+      ld8<T>(bx + h0, w1);
+      ld8<T>(wg + h0, w2);
+      ld8<T>(bg + h0, w3);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 uu = fma2(fma2(a[k], sU2, cU2), w0[k], w1[k]);
+        const float2 gg = fma2(fma2(b[k], sG2, cG2), w2[k], w3[k]);
+        o[k] = mul2(uu, mul2(gg, sigmoid_fast2(gg)));
+      }
+      st8<T>(hr + h0, o);
+    }
+  }
+}
+
+// =========================================================================
 // R: column sums of partials, several jobs per launch, fixed summation order.
 //
 // Chunked form (when the caller provides scratch): a block of 256 threads
@@ -528,6 +635,24 @@ cudaError_t launch_zstats(const RowArgs& a, const void* Z, float* zstats, cudaSt
     err = launch_k(k_zstats<T>, dim3(grid), dim3(256), 0, st, 1, (const T*)Z, zstats, N, a.H, tiles);
   });
   return err;
+}
+
+bool gate_fwd_rows_supported(const RowArgs& a) {
+  return a.dtype != 0 && a.H % 8 == 0 && a.H / 8 <= 32 * kGateRowVecs;
+}
+
+cudaError_t launch_gate_fwd_rows(const RowArgs& a, const void* Z, float* muU, float* rU, float* muG, float* rG,
+                                 const void* wx, const void* bx, const void* wg, const void* bg, void* hidden,
+                                 cudaStream_t st) {
+  if (!gate_fwd_rows_supported(a)) return cudaErrorInvalidValue;
+  const int N = a.B * a.T;
+  if (a.dtype == 1)
+    return launch_k(k_gate_fwd_rows<bf16>, dim3((N + 7) / 8), dim3(256), 0, st, 1, (const bf16*)Z, muU, rU, muG, rG,
+                    (const bf16*)wx, (const bf16*)bx, (const bf16*)wg, (const bf16*)bg, (bf16*)hidden, N, a.H,
+                    1e-5f, a.Hl);
+  return launch_k(k_gate_fwd_rows<f16>, dim3((N + 7) / 8), dim3(256), 0, st, 1, (const f16*)Z, muU, rU, muG, rG,
+                  (const f16*)wx, (const f16*)bx, (const f16*)wg, (const f16*)bg, (f16*)hidden, N, a.H, 1e-5f,
+                  a.Hl);
 }
 
 cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats, float* muU, float* rU,
