@@ -407,9 +407,14 @@ rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
 
 // Copy stream of rmx_step_host, one per device, created on first use; the
 // events are shared, so a call's enqueue sequence holds g_copy_mu.
+// x is uploaded in this many chunks of samples, so that the per-sample
+// norm0/norm1 pass starts on the first chunks while the rest is in flight.
+constexpr int kXChunks = 4;
+
 struct CopyStream {
   cudaStream_t s = nullptr;
   cudaEvent_t start = nullptr, dy_in = nullptr, fwd_done = nullptr, dx_ready = nullptr, done = nullptr;
+  cudaEvent_t x_in[kXChunks] = {};
 };
 std::mutex g_copy_mu;
 
@@ -424,6 +429,8 @@ CopyStream* copy_stream() {
     cudaEvent_t* ev[5] = {&c.start, &c.dy_in, &c.fwd_done, &c.dx_ready, &c.done};
     for (cudaEvent_t* e : ev)
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    for (cudaEvent_t& e : c.x_in)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     c.s = s;
   }
   return &c;
@@ -451,8 +458,14 @@ Stats stats_of(const void* saved, const Layout& L, size_t N) {
   return st;
 }
 
+// Samples [b0, b1) of chunk i of n (an even split of B).
+inline int chunk_begin(int B, int i, int n) { return (int)((long long)B * i / n); }
+
+// x_in (may be null): x arrives in kXChunks chunks of samples, event i
+// recorded once chunk i is in device memory; the per-sample norm0/norm1
+// pass then runs chunk by chunk, each after its event.
 rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p, void* saved, void* y,
-                        cudaStream_t st) {
+                        cudaStream_t st, const cudaEvent_t* x_in = nullptr) {
   const Layout L = layout_of(c);
   const size_t N = (size_t)c.B * c.T;
   void* out1 = at(saved, L.out1);
@@ -462,10 +475,23 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
   Stats S = stats_of(saved, L, N);
   void* s1 = at(saved, L.s1);
   if (ln01_fwd_supported(L.ra)) {
-    Launch l("ln01_fwd", st);
-    RMX_TRY(l.done(launch_ln01_fwd(L.ra, x, p.gamma0, p.beta0, p.gamma1, p.beta1, s1, out1, S.mu0, S.r0, S.mu1,
-                                   S.r1, st)));
+    const int n = x_in ? kXChunks : 1;
+    const size_t e = esize(c.dtype);
+    for (int i = 0; i < n; ++i) {
+      const int b0 = chunk_begin(c.B, i, n), b1 = chunk_begin(c.B, i + 1, n);
+      if (x_in && cudaStreamWaitEvent(st, x_in[i], 0) != cudaSuccess) return RMX_ERR_CUDA;
+      if (b1 == b0) continue;
+      RowArgs ra = L.ra;
+      ra.B = b1 - b0;
+      const size_t r0 = (size_t)b0 * c.T, off = r0 * L.D * e;
+      Launch l("ln01_fwd", st);
+      RMX_TRY(l.done(launch_ln01_fwd(ra, at(x, off), p.gamma0, p.beta0, p.gamma1, p.beta1, at(s1, off),
+                                     at(out1, off), S.mu0 + r0, S.r0 + r0, S.mu1 + r0, S.r1 + r0, st)));
+    }
   } else {
+    if (x_in)
+      for (int i = 0; i < kXChunks; ++i)
+        if (cudaStreamWaitEvent(st, x_in[i], 0) != cudaSuccess) return RMX_ERR_CUDA;
     // Samples too large to stage: norm0 writes its output token-mixed into
     // the s1 buffer, norm1 adds x in place.
     {
@@ -725,6 +751,28 @@ rmx_status zero_grads(const rmx_config& c, const rmx_grads& g, cudaStream_t st) 
   return RMX_OK;
 }
 
+// rmx_forward with x_in as in forward_impl (null: x is already there).
+rmx_status forward_checked(const rmx_config* cfg, const void* x, const rmx_params* params, void* saved,
+                           size_t saved_bytes, void* y, cudaStream_t st, const cudaEvent_t* x_in) {
+  if (!config_ok(cfg)) return RMX_ERR_INVALID_ARG;
+  RMX_TRY(check_params(params));
+  if (cfg->B == 0) return RMX_OK;
+  RMX_TRY(check_ptr(x));
+  RMX_TRY(check_ptr(y));
+  RMX_TRY(check_ptr(saved));
+  if (x == y) return RMX_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  if (saved_bytes < L.saved_total) return RMX_ERR_WORKSPACE;
+  RMX_TRY(kernels_support(*cfg));
+  if (L.padded) {
+    if (x_in)
+      for (int i = 0; i < kXChunks; ++i)
+        if (cudaStreamWaitEvent(st, x_in[i], 0) != cudaSuccess) return RMX_ERR_CUDA;
+    return forward_padded(L, *cfg, x, *params, saved, y, st);
+  }
+  return forward_impl(*cfg, x, *params, saved, y, st, x_in);
+}
+
 rmx_status backward_checked(const rmx_config* cfg, const void* x, const void* dy, const void* saved,
                             size_t saved_bytes, const rmx_params* params, void* dx, const rmx_grads* grads,
                             void* ws, size_t ws_bytes, rmx_stream stream, cudaEvent_t dx_ready) {
@@ -764,19 +812,9 @@ size_t rmx_workspace_bytes(const rmx_config* cfg) {
 
 rmx_status rmx_forward(const rmx_config* cfg, const void* x, const rmx_params* params, void* saved,
                        size_t saved_bytes, void* y, rmx_stream stream) {
-  if (!config_ok(cfg)) return RMX_ERR_INVALID_ARG;
-  RMX_TRY(check_params(params));
-  if (cfg->B == 0) return RMX_OK;
-  RMX_TRY(check_ptr(x));
-  RMX_TRY(check_ptr(y));
-  RMX_TRY(check_ptr(saved));
-  if (x == y) return RMX_ERR_INVALID_ARG;
-  const Layout L = layout_of(*cfg);
-  if (saved_bytes < L.saved_total) return RMX_ERR_WORKSPACE;
-  RMX_TRY(kernels_support(*cfg));
-  if (L.padded) return forward_padded(L, *cfg, x, *params, saved, y, reinterpret_cast<cudaStream_t>(stream));
-  return forward_impl(*cfg, x, *params, saved, y, reinterpret_cast<cudaStream_t>(stream));
+  return forward_checked(cfg, x, params, saved, saved_bytes, y, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
+
 
 
 rmx_status rmx_backward(const rmx_config* cfg, const void* x, const void* dy, const void* saved,
@@ -807,12 +845,23 @@ rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host, const r
   CopyStream* cs = copy_stream();
   if (!cs) return RMX_ERR_CUDA;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-  // The copy stream must not overwrite dev->dy while earlier work on `stream` may read it.
+  // The copy stream must not overwrite dev->x or dev->dy while earlier work
+  // on `stream` may read them.
   if (!ok(cudaEventRecord(cs->start, st)) || !ok(cudaStreamWaitEvent(cs->s, cs->start, 0))) return RMX_ERR_CUDA;
-  if (!ok(cudaMemcpyAsync(dev->x, host->x, bytes, cudaMemcpyHostToDevice, st))) return RMX_ERR_CUDA;
+  // x in chunks of samples (the forward's first pass follows chunk by
+  // chunk), then dy: one host->device engine serves them in that order.
+  const size_t sample_bytes = (size_t)cfg->T * cfg->D * esize(cfg->dtype);
+  for (int i = 0; i < kXChunks; ++i) {
+    const size_t o = (size_t)chunk_begin(cfg->B, i, kXChunks) * sample_bytes;
+    const size_t n = (size_t)chunk_begin(cfg->B, i + 1, kXChunks) * sample_bytes - o;
+    if (n && !ok(cudaMemcpyAsync(static_cast<char*>(dev->x) + o, static_cast<const char*>(host->x) + o, n,
+                                 cudaMemcpyHostToDevice, cs->s)))
+      return RMX_ERR_CUDA;
+    if (!ok(cudaEventRecord(cs->x_in[i], cs->s))) return RMX_ERR_CUDA;
+  }
   if (!ok(cudaMemcpyAsync(dev->dy, host->dy, bytes, cudaMemcpyHostToDevice, cs->s))) return RMX_ERR_CUDA;
   if (!ok(cudaEventRecord(cs->dy_in, cs->s))) return RMX_ERR_CUDA;
-  RMX_TRY(rmx_forward(cfg, dev->x, params, saved, saved_bytes, dev->y, stream));
+  RMX_TRY(forward_checked(cfg, dev->x, params, saved, saved_bytes, dev->y, st, cs->x_in));
   if (!ok(cudaEventRecord(cs->fwd_done, st)) || !ok(cudaStreamWaitEvent(cs->s, cs->fwd_done, 0))) return RMX_ERR_CUDA;
   if (!ok(cudaMemcpyAsync(host->y, dev->y, bytes, cudaMemcpyDeviceToHost, cs->s))) return RMX_ERR_CUDA;
   if (!ok(cudaStreamWaitEvent(st, cs->dy_in, 0))) return RMX_ERR_CUDA;

@@ -142,13 +142,15 @@ typedef struct { void* x; void* dy; void* y; void* dx; } rmx_device_io;
 
 /* One end-to-end step from host memory: copies x and dy host->device into
  * `dev` (device, [B,T,D] each), runs rmx_forward and rmx_backward, and copies
- * y and dx device->host.  Parameters and gradients stay on the device.  One
- * cudaMemcpyAsync per copy: x and dx on `stream`; dy (needed only by the
- * backward) and y (final after the forward) on a copy stream the library
- * keeps per device, so they overlap the compute, joined to `stream` by
- * events.  Returns once enqueued; everything the call does is ordered before
- * later work on `stream`, so the caller synchronises `stream` before reading
- * host y/dx.  The overlap needs pinned host buffers. */
+ * y and dx device->host.  Parameters and gradients stay on the device.  The
+ * copies run on a copy stream the library keeps per device, joined to
+ * `stream` by events, so that they overlap the compute: x in four chunks of
+ * samples (the forward's first, per-sample pass starts on each chunk as it
+ * lands), then dy (needed only by the backward); y once the forward is done
+ * (during the backward) and dx once it is final (during the weight
+ * gradients).  Returns once enqueued; everything the call does is ordered
+ * before later work on `stream`, so the caller synchronises `stream` before
+ * reading host y/dx.  The overlap needs pinned host buffers. */
 rmx_status rmx_step_host(const rmx_config* cfg, const rmx_host_io* host,
                          const rmx_device_io* dev, const rmx_params* params,
                          const rmx_grads* grads, void* saved, size_t saved_bytes,

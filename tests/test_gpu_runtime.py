@@ -85,9 +85,18 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     compare(blk.results(), oracle_outputs(arrays), TOL["f32"])
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_host_memory_step_matches_device_step(dtype):
-    shape = I.Shape(B=16, T=8, D=128, H=256, dtype=dtype)
+# x is uploaded in four chunks of samples (uneven or empty chunks when B is
+# not a multiple of four); padded rows take the whole-batch path.
+@pytest.mark.parametrize("dims", [
+    dict(B=16, T=8, D=128, H=256, dtype="f32"),
+    dict(B=16, T=8, D=128, H=256, dtype="bf16"),
+    dict(B=3, T=8, D=128, H=256, dtype="bf16"),
+    dict(B=7, T=16, D=64, H=192, dtype="f16"),
+    dict(B=6, T=9, D=81, H=243, dtype="bf16"),
+    dict(B=5, T=8, D=64, H=128, dtype="tf32"),
+], ids=lambda d: "B{B}_T{T}_D{D}_H{H}_{dtype}".format(**d))
+def test_host_memory_step_matches_device_step(dims):
+    shape = I.Shape(**dims)
     arrays = I.make_inputs(shape, ln_params="random")
     blk = RankMixerDevice(shape, arrays)
     blk.step()
