@@ -76,6 +76,8 @@ PAIR_SHAPES = [
     (129, 264, 64, 2),     # 2 M-tiles, second one holds a single row
     (520, 200, 88, 3),     # M-major and N-major tails together
     (512, 384, 264, 2),    # MN extents multiples of 64: interleaved MN-major stages, ragged K
+    (640, 1000, 136, 2),   # 5 M-tiles (an odd number of pairs), ragged N
+    (1024, 2560, 256, 8),  # 320 pair tiles: the persistent grid wraps several times
 ]
 
 
