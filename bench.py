@@ -509,10 +509,12 @@ def run_ours(args) -> dict | None:
             ee[i].record(stream)
         torch.cuda.synchronize()
         B.check(B.rmx_check(stream), "e2e")
-        e_ms = reduce_max(float(np.mean([a.elapsed_time(b) for a, b in zip(es, ee)])), ws)
+        e_samples = [a.elapsed_time(b) for a, b in zip(es, ee)]
+        e_ms = reduce_max(float(np.mean(e_samples)), ws)
         nbytes = hx.numel() * hx.element_size()
         e2e = {"value": aggregate(rows, e_ms, ws), "unit": "rows/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes}
+               "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
+               "samples_ms": [round(v, 4) for v in e_samples]}
 
     if rank != 0:
         return None

@@ -410,6 +410,10 @@ rmx_status run_gemm(const char* name, const GemmDesc& d, cudaStream_t st) {
 // x is uploaded in this many chunks of samples, so that the per-sample
 // norm0/norm1 pass starts on the first chunks while the rest is in flight.
 constexpr int kXChunks = 4;
+// Sample ranges of the forward in rmx_step_host: two measured faster end to
+// end than one (the upload of x no longer precedes all of the forward) and
+// than four (each range reads the weights again).
+constexpr int kFwdChunks = 2;
 
 struct CopyStream {
   cudaStream_t s = nullptr;
@@ -461,54 +465,97 @@ Stats stats_of(const void* saved, const Layout& L, size_t N) {
 // Samples [b0, b1) of chunk i of n (an even split of B).
 inline int chunk_begin(int B, int i, int n) { return (int)((long long)B * i / n); }
 
-// x_in (may be null): x arrives in kXChunks chunks of samples, event i
-// recorded once chunk i is in device memory; the per-sample norm0/norm1
-// pass then runs chunk by chunk, each after its event.
-rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p, void* saved, void* y,
-                        cudaStream_t st, const cudaEvent_t* x_in = nullptr) {
-  const Layout L = layout_of(c);
+// The forward over samples [b0, b1): every kernel of the forward works on
+// whole rows (a sample's T rows for norm0 / token mix / norm1, single rows
+// or per-token GEMM rows for the rest), so a range of samples is the same
+// computation on a sub-batch at an offset of every [B, T, ...] buffer.
+rmx_status forward_rows(const rmx_config& c, const Layout& L, const void* x, const rmx_params& p, void* saved,
+                        void* y, cudaStream_t st, int b0, int b1) {
   const size_t N = (size_t)c.B * c.T;
-  void* out1 = at(saved, L.out1);
-  void* Z = at(saved, L.Z);
-  void* hidden = at(saved, L.hidden);
-  void* s2 = at(saved, L.s2);
+  const size_t e = esize(c.dtype);
+  const size_t r0 = (size_t)b0 * c.T;
+  RowArgs ra = L.ra;
+  ra.B = b1 - b0;
+  if (ra.B <= 0) return RMX_OK;
+  // Byte offsets of row r0 in buffers of D, H and 2H storage elements per row.
+  const size_t oD = r0 * L.D * e, oH = r0 * L.H * e;
+  void* out1 = at(saved, L.out1 + oD);
+  void* Z = at(saved, L.Z + 2 * oH);
+  void* hidden = at(saved, L.hidden + oH);
+  void* s2 = at(saved, L.s2 + oD);
+  void* s1 = at(saved, L.s1 + oD);
+  const void* xr = at(x, oD);
+  void* yr = at(y, oD);
   Stats S = stats_of(saved, L, N);
-  void* s1 = at(saved, L.s1);
-  if (ln01_fwd_supported(L.ra)) {
-    const int n = x_in ? kXChunks : 1;
-    const size_t e = esize(c.dtype);
-    for (int i = 0; i < n; ++i) {
-      const int b0 = chunk_begin(c.B, i, n), b1 = chunk_begin(c.B, i + 1, n);
-      if (x_in && cudaStreamWaitEvent(st, x_in[i], 0) != cudaSuccess) return RMX_ERR_CUDA;
-      if (b1 == b0) continue;
-      RowArgs ra = L.ra;
-      ra.B = b1 - b0;
-      const size_t r0 = (size_t)b0 * c.T, off = r0 * L.D * e;
-      Launch l("ln01_fwd", st);
-      RMX_TRY(l.done(launch_ln01_fwd(ra, at(x, off), p.gamma0, p.beta0, p.gamma1, p.beta1, at(s1, off),
-                                     at(out1, off), S.mu0 + r0, S.r0 + r0, S.mu1 + r0, S.r1 + r0, st)));
-    }
+  for (float** v : {&S.mu0, &S.r0, &S.mu1, &S.r1, &S.mu2, &S.r2, &S.muU, &S.rU, &S.muG, &S.rG}) *v += r0;
+  if (ln01_fwd_supported(ra)) {
+    Launch l("ln01_fwd", st);
+    RMX_TRY(l.done(launch_ln01_fwd(ra, xr, p.gamma0, p.beta0, p.gamma1, p.beta1, s1, out1, S.mu0, S.r0, S.mu1,
+                                   S.r1, st)));
   } else {
-    if (x_in)
-      for (int i = 0; i < kXChunks; ++i)
-        if (cudaStreamWaitEvent(st, x_in[i], 0) != cudaSuccess) return RMX_ERR_CUDA;
     // Samples too large to stage: norm0 writes its output token-mixed into
     // the s1 buffer, norm1 adds x in place.
     {
       Launch l("ln0_fwd_mixed", st);
-      RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_MIXED_OUT, x, nullptr, p.gamma0, p.beta0, s1, S.mu0, S.r0, nullptr,
+      RMX_TRY(l.done(launch_ln_fwd(ra, LNF_MIXED_OUT, xr, nullptr, p.gamma0, p.beta0, s1, S.mu0, S.r0, nullptr,
                                    st)));
     }
     {
       Launch l("ln1_fwd", st);
-      RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_SUM_IN, s1, x, p.gamma1, p.beta1, out1, S.mu1, S.r1, s1, st)));
+      RMX_TRY(l.done(launch_ln_fwd(ra, LNF_SUM_IN, s1, xr, p.gamma1, p.beta1, out1, S.mu1, S.r1, s1, st)));
     }
   }
-  float* zstats = reinterpret_cast<float*>(at(saved, L.zstats));
+  float* zstats = reinterpret_cast<float*>(at(saved, L.zstats)) + r0 * (size_t)zstats_tiles(L.H) * 4;
   const int sd = storage(c.dtype);
   const bool tf32 = c.dtype == RMX_F32_TF32;
+  const int M = b1 - b0;
+  // 16-bit rows up to H = 2560: the gate pass takes the statistics of Z
+  // itself (row in registers) and GEMM1 stores Z with the bias alone;
+  // otherwise GEMM1's epilogue (or a statistics pass) writes per-group
+  // statistics of Z that the gate pass merges.
+  const bool rows_gate = gate_fwd_rows_supported(ra);
+  {
+    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, rows_gate ? EPI_BIAS : EPI_BIAS_ZSTATS, sd, M, 2 * L.H, L.D, c.T,
+               out1, tf32 ? at(saved, L.w1T) : p.w1, Z, p.b1, nullptr, rows_gate ? nullptr : zstats, L.H,
+               tf32 ? 1 : 0};
+    const bool epilogue_stats = !rows_gate && tc_engine(d);
+    RMX_TRY(run_gemm("gemm1_fwd", d, st));
+    if (!rows_gate && !epilogue_stats) {
+      Launch l("zstats", st);
+      RMX_TRY(l.done(launch_zstats(ra, Z, zstats, st)));
+    }
+  }
+  {
+    Launch l("gate_fwd", st);
+    if (rows_gate)
+      RMX_TRY(l.done(launch_gate_fwd_rows(ra, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
+                                          hidden, st)));
+    else
+      RMX_TRY(l.done(launch_gate_fwd(ra, Z, zstats, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w,
+                                     p.lng_b, hidden, st)));
+  }
+  {
+    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, EPI_BIAS_RESID, sd, M, L.D, L.H, c.T, hidden,
+               tf32 ? at(saved, L.woutT) : p.wout, s2, p.bout, out1, nullptr, 0, tf32 ? 1 : 0};
+    RMX_TRY(run_gemm("gemm2_fwd", d, st));
+  }
+  {
+    Launch l("ln2_fwd", st);
+    RMX_TRY(l.done(launch_ln_fwd(ra, LNF_PLAIN, s2, nullptr, p.gamma2, p.beta2, yr, S.mu2, S.r2, nullptr, st)));
+  }
+  return RMX_OK;
+}
+
+// x_in (may be null): x arrives in kXChunks chunks of samples, event i
+// recorded once chunk i is in device memory.  The forward then runs in
+// kFwdChunks ranges of samples, each after the events of the x chunks it
+// covers, so that its kernels overlap the rest of the upload (at the cost
+// of reading the weights once per range).
+rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p, void* saved, void* y,
+                        cudaStream_t st, const cudaEvent_t* x_in = nullptr) {
+  const Layout L = layout_of(c);
   // TF32: the weights as [T, N, K] (K-major) for the dgrad-form contraction.
-  if (tf32) {
+  if (c.dtype == RMX_F32_TF32) {
     Launch l("tf32_transpose", st);
     RMX_TRY(l.done(launch_transpose_f32(static_cast<const float*>(p.w1), reinterpret_cast<float*>(at(saved, L.w1T)),
                                         c.T, L.D, 2 * L.H, (long long)L.D * 2 * L.H, 2 * L.H, L.D, st)));
@@ -517,39 +564,15 @@ rmx_status forward_impl(const rmx_config& c, const void* x, const rmx_params& p,
                                          reinterpret_cast<float*>(at(saved, L.woutT)), c.T, L.H, L.D,
                                          (long long)L.H * L.D, L.D, L.H, st)));
   }
-  // 16-bit rows up to H = 2560: the gate pass takes the statistics of Z
-  // itself (row in registers) and GEMM1 stores Z with the bias alone;
-  // otherwise GEMM1's epilogue (or a statistics pass) writes per-group
-  // statistics of Z that the gate pass merges.
-  const bool rows_gate = gate_fwd_rows_supported(L.ra);
-  {
-    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, rows_gate ? EPI_BIAS : EPI_BIAS_ZSTATS, sd, c.B, 2 * L.H, L.D, c.T,
-               out1, tf32 ? at(saved, L.w1T) : p.w1, Z, p.b1, nullptr, rows_gate ? nullptr : zstats, L.H,
-               tf32 ? 1 : 0};
-    const bool epilogue_stats = !rows_gate && tc_engine(d);
-    RMX_TRY(run_gemm("gemm1_fwd", d, st));
-    if (!rows_gate && !epilogue_stats) {
-      Launch l("zstats", st);
-      RMX_TRY(l.done(launch_zstats(L.ra, Z, zstats, st)));
-    }
-  }
-  {
-    Launch l("gate_fwd", st);
-    if (rows_gate)
-      RMX_TRY(l.done(launch_gate_fwd_rows(L.ra, Z, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w, p.lng_b,
-                                          hidden, st)));
-    else
-      RMX_TRY(l.done(launch_gate_fwd(L.ra, Z, zstats, S.muU, S.rU, S.muG, S.rG, p.lnx_w, p.lnx_b, p.lng_w,
-                                     p.lng_b, hidden, st)));
-  }
-  {
-    GemmDesc d{tf32 ? GEMM_DGRAD : GEMM_FWD, EPI_BIAS_RESID, sd, c.B, L.D, L.H, c.T, hidden,
-               tf32 ? at(saved, L.woutT) : p.wout, s2, p.bout, out1, nullptr, 0, tf32 ? 1 : 0};
-    RMX_TRY(run_gemm("gemm2_fwd", d, st));
-  }
-  {
-    Launch l("ln2_fwd", st);
-    RMX_TRY(l.done(launch_ln_fwd(L.ra, LNF_PLAIN, s2, nullptr, p.gamma2, p.beta2, y, S.mu2, S.r2, nullptr, st)));
+  const int n = x_in ? kFwdChunks : 1;
+  for (int k = 0; k < n; ++k) {
+    const int b0 = chunk_begin(c.B, k, n), b1 = chunk_begin(c.B, k + 1, n);
+    if (x_in)
+      for (int i = 0; i < kXChunks; ++i)
+        if (chunk_begin(c.B, i, kXChunks) < b1 && chunk_begin(c.B, i + 1, kXChunks) > b0 &&
+            cudaStreamWaitEvent(st, x_in[i], 0) != cudaSuccess)
+          return RMX_ERR_CUDA;
+    RMX_TRY(forward_rows(c, L, x, p, saved, y, st, b0, b1));
   }
   return RMX_OK;
 }

@@ -14,9 +14,10 @@
 // j holds columns 8j ... 8j + 7 of both halves.  The dh and Z rows stream
 // into shared memory through an S-stage ring of bulk copies (one thread
 // issues them; a byte-counting mbarrier per stage says when a row has
-// landed).  Two rows at a time the CTA takes their eight row sums with one
-// barrier, then every thread finishes its own columns from registers, writes
-// dZ and keeps the column partial sums in registers.  The element math runs
+// landed).  A row at a time (two when the LayerNorm weights live in shared
+// memory) the CTA takes its four row sums with one barrier, then every
+// thread finishes its own columns from registers, writes dZ and keeps the
+// column partial sums in registers.  The element math runs
 // on column pairs with the packed fp32x2 instructions (the same roundings as
 // scalar fp32, half the instructions).  dh and Z are read from HBM once;
 // every wait is bounded.
@@ -99,10 +100,10 @@ constexpr int kGateE = 8;             // columns per thread and half
 constexpr int kGateMaxThreads = 480;  // H up to 3840 (k = 3 at D = 1280)
 constexpr int kGateRedWarps = 16;     // reduction buffer rows (at least kGateMaxThreads / 32)
 
-template <typename T, bool WREG>
+template <typename T, bool WREG, int R>
 __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
   pdl_enter();
-  constexpr int R = 2;             // rows per barrier
+  static_assert(R == 1 || R == 2, "rows per barrier");
   constexpr int NS = 4 * R;        // row sums per barrier
   constexpr int LPS = 32 / NS;     // lanes holding one sum after the warp reduction
   extern __shared__ __align__(16) unsigned char smem[];
@@ -340,6 +341,10 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
   }
 }
 
+// Rows per barrier: one with the weights in registers (measured 2% faster
+// than two at H = 2560), two when they live in shared memory.
+template <bool WREG> constexpr int gate_rows() { return WREG ? 1 : 2; }
+
 // Threads, ring stages and shared memory of a CTA of nb rows (0 if even two
 // stages do not fit).
 template <typename T, bool WREG>
@@ -359,7 +364,7 @@ int gate_ctas_per_sm(int H) {
   int threads = 0, stages = 0;
   const size_t smem = gate_shape<T, WREG>(H, kGateBwdMaxRows, threads, stages);
   if (smem == 0) return 1;
-  auto k = k_gate_bwd<T, WREG>;
+  auto k = k_gate_bwd<T, WREG, gate_rows<WREG>()>;
   int n = 0;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess || n < 1)
@@ -373,7 +378,7 @@ cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
   int threads = 0;
   const size_t smem = gate_shape<T, WREG>(a.H, a.nb, threads, a.stages);
   if (smem == 0) return cudaErrorInvalidValue;
-  auto k = k_gate_bwd<T, WREG>;
+  auto k = k_gate_bwd<T, WREG, gate_rows<WREG>()>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_k(k, grid, dim3(threads), smem, st, 1, a);

@@ -145,8 +145,10 @@ typedef struct { void* x; void* dy; void* y; void* dx; } rmx_device_io;
  * y and dx device->host.  Parameters and gradients stay on the device.  The
  * copies run on a copy stream the library keeps per device, joined to
  * `stream` by events, so that they overlap the compute: x in four chunks of
- * samples (the forward's first, per-sample pass starts on each chunk as it
- * lands), then dy (needed only by the backward); y once the forward is done
+ * samples, the forward running on the first half of the samples as soon as
+ * their chunks have landed and on the second half after that (every forward
+ * result is computed row by row, so it equals rmx_forward's bit for bit),
+ * then dy (needed only by the backward); y once the forward is done
  * (during the backward) and dx once it is final (during the weight
  * gradients).  Returns once enqueued; everything the call does is ordered
  * before later work on `stream`, so the caller synchronises `stream` before
