@@ -278,6 +278,56 @@ __device__ __forceinline__ void sts_elems(unsigned char* p, const float* v) {
   }
 }
 
+// NE (even) consecutive elements of T in shared memory (NE * sizeof(T)
+// bytes, aligned to that size) as NE / 2 float pairs.
+template <typename T, int NE>
+__device__ __forceinline__ void lds_pairs(const unsigned char* p, float2* v) {
+  constexpr int W = NE * (int)sizeof(T);
+  static_assert(NE % 2 == 0 && (W == 4 || W == 8 || W == 16), "pairs in one 4-, 8- or 16-byte access");
+  if constexpr (sizeof(T) == 4) {
+    if constexpr (W == 16) {
+      const float4 r = *reinterpret_cast<const float4*>(p);
+      v[0] = make_float2(r.x, r.y);
+      v[1] = make_float2(r.z, r.w);
+    } else {
+      v[0] = *reinterpret_cast<const float2*>(p);
+    }
+  } else if constexpr (W == 16) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    v[0] = unpack2w<T>(r.x);
+    v[1] = unpack2w<T>(r.y);
+    v[2] = unpack2w<T>(r.z);
+    v[3] = unpack2w<T>(r.w);
+  } else if constexpr (W == 8) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    v[0] = unpack2w<T>(r.x);
+    v[1] = unpack2w<T>(r.y);
+  } else {
+    v[0] = unpack2w<T>(*reinterpret_cast<const uint32_t*>(p));
+  }
+}
+// Stores NE / 2 float pairs as T (rounded to nearest even) and replaces them
+// by the stored values.
+template <typename T, int NE>
+__device__ __forceinline__ void sts_pairs_round(unsigned char* p, float2* v) {
+  constexpr int W = NE * (int)sizeof(T);
+  static_assert(NE % 2 == 0 && (W == 4 || W == 8 || W == 16), "pairs in one 4-, 8- or 16-byte access");
+  if constexpr (sizeof(T) == 4) {
+    if constexpr (W == 16) *reinterpret_cast<float4*>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+    else *reinterpret_cast<float2*>(p) = v[0];
+  } else {
+    uint32_t w[NE / 2];
+#pragma unroll
+    for (int k = 0; k < NE / 2; ++k) {
+      w[k] = pack2w<T>(v[k]);
+      v[k] = unpack2w<T>(w[k]);
+    }
+    if constexpr (W == 16) *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else if constexpr (W == 8) *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+    else *reinterpret_cast<uint32_t*>(p) = w[0];
+  }
+}
+
 struct Ln01ClusterGeom {
   int cs;           // CTAs per sample (cluster size) = T / 8
   int own_pitch;    // bytes between staged own rows (D * e)
@@ -308,9 +358,14 @@ __host__ __device__ inline Ln01ClusterGeom ln01_cluster_geom(int Tn, int D, int 
 
 // One CTA: sample b, output rows i0 ... i0 + 7 (i0 = 8 * rank).  Shared
 // memory: stripe [T][8*C + pad] | st0 [T] float2 (norm0 mean, rstd of every
-// row of the sample) | gb0 [8*C] float2 (gamma0, beta0 of the stripe's
-// columns) | own rows [8][D] | mbarrier.  NE elements per shared-memory access in the
-// gather (NE * e bytes divide C * e).
+// row of the sample) | gb0: gamma0, beta0 of the stripe's 8*C columns (a
+// float4 {g, g', b, b'} per column pair, or a float2 per column when NE is 1)
+// | own rows [8][D] | mbarrier.  NE elements per shared-memory access in the
+// gather (NE * e bytes divide C * e).  With NE even the gather's arithmetic
+// runs on column pairs with the packed fp32x2 instructions (each rounds as
+// the scalar one), as do the statistics and norm1's output everywhere.
+// (Staging gamma1 / beta1 in shared memory as well measured 30% slower:
+// fewer clusters fit.)
 template <typename T, int NE>
 __global__ void __launch_bounds__(32 * kLn01Rows)
     k_ln01_cluster(const __grid_constant__ CUtensorMap stripe_map, const Ln01Args a) {
@@ -330,6 +385,8 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
   float2* gb0 = reinterpret_cast<float2*>(smem + geo.off_gb);
   unsigned char* own = smem + geo.off_own;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + geo.off_bar);
+  constexpr bool PK = NE % 2 == 0;  // gather on column pairs
+  constexpr int P = V / 2;          // float pairs per 16-byte vector
   __shared__ int abort_flag;
 
   // Every CTA of the cluster must be running before another stores into its
@@ -355,9 +412,17 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
   {
     const T* g0 = reinterpret_cast<const T*>(a.gamma0);
     const T* bt0 = reinterpret_cast<const T*>(a.beta0);
-    for (int k = tid; k < kLn01Rows * C; k += blockDim.x) {
-      const int col = i0 * C + k;
-      gb0[k] = make_float2(to_f(g0[col]), to_f(bt0[col]));
+    if (PK) {
+      float4* gb4 = reinterpret_cast<float4*>(gb0);
+      for (int k = tid; k < kLn01Rows * C / 2; k += blockDim.x) {
+        const int col = i0 * C + 2 * k;
+        gb4[k] = make_float4(to_f(g0[col]), to_f(g0[col + 1]), to_f(bt0[col]), to_f(bt0[col + 1]));
+      }
+    } else {
+      for (int k = tid; k < kLn01Rows * C; k += blockDim.x) {
+        const int col = i0 * C + k;
+        gb0[k] = make_float2(to_f(g0[col]), to_f(bt0[col]));
+      }
     }
   }
   __syncthreads();
@@ -371,26 +436,27 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
   const int nv = D / V;
   if (ok) {
     const int il = warp;
-    const T* row = reinterpret_cast<const T*>(own + (size_t)il * geo.own_pitch);
-    float sum = 0.f;
+    const unsigned char* row = own + (size_t)il * geo.own_pitch;
+    float2 s2 = f2(0.f);
     for (int vi = lane; vi < nv; vi += 32) {
-      float v[V];
-      load_vec(row + vi * V, v);
+      float2 v[P];
+      ld16p<T>(row + (size_t)vi * 16, v);
 #pragma unroll
-      for (int q = 0; q < V; ++q) sum += v[q];
+      for (int k = 0; k < P; ++k) s2 = add2(s2, v[k]);
     }
-    const float mean = warp_sum(sum) * invD;
-    float ss = 0.f;
+    const float mean = warp_sum(s2.x + s2.y) * invD;
+    const float2 nm = f2(-mean);
+    float2 q2 = f2(0.f);
     for (int vi = lane; vi < nv; vi += 32) {
-      float v[V];
-      load_vec(row + vi * V, v);
+      float2 v[P];
+      ld16p<T>(row + (size_t)vi * 16, v);
 #pragma unroll
-      for (int q = 0; q < V; ++q) {
-        const float c = v[q] - mean;
-        ss = fmaf(c, c, ss);
+      for (int k = 0; k < P; ++k) {
+        const float2 c = add2(v[k], nm);
+        q2 = fma2(c, c, q2);
       }
     }
-    const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + a.eps);
+    const float rstd = 1.0f / sqrtf(warp_sum(q2.x + q2.y) * invD + a.eps);
     const size_t r = (size_t)b * Tn + i0 + il;
     if (lane == 0) {
       a.mu0[r] = mean;
@@ -420,62 +486,80 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
     const int i = i0 + il;
     unsigned char* orow = own + (size_t)il * geo.own_pitch;
     const int nch = C / NE;
-    float sum = 0.f;
+    float2 sum2 = f2(0.f);
     for (int j = lane; j < Tn; j += 32) {
       const float2 sj = st0[j];
       const unsigned char* sp = stripe + (size_t)j * geo.stripe_pitch + (size_t)il * C * e;
       unsigned char* op = orow + (size_t)j * C * e;
-      const float2* gb = gb0 + il * C;
-      for (int ch = 0; ch < nch; ++ch) {
-        float xs[NE], xo[NE], sv[NE];
-        lds_elems<T, NE>(sp + ch * NE * e, xs);
-        lds_elems<T, NE>(op + ch * NE * e, xo);
+      if constexpr (PK) {
+        const float2 nmj = f2(-sj.x), rj = f2(sj.y);
+        const float4* gb = reinterpret_cast<const float4*>(gb0) + il * C / 2;
+        for (int ch = 0; ch < nch; ++ch) {
+          float2 xs[NE / 2], xo[NE / 2];
+          lds_pairs<T, NE>(sp + ch * NE * e, xs);
+          lds_pairs<T, NE>(op + ch * NE * e, xo);
 #pragma unroll
-        for (int q = 0; q < NE; ++q) {
-          const float2 w = gb[ch * NE + q];
-          const float a0 = fmaf((xs[q] - sj.x) * sj.y, w.x, w.y);
-          sv[q] = to_f(from_f<T>(a0 + xo[q]));
-          sum += sv[q];
+          for (int k = 0; k < NE / 2; ++k) {
+            const float4 w = gb[ch * NE / 2 + k];
+            const float2 a0 = fma2(mul2(add2(xs[k], nmj), rj), make_float2(w.x, w.y), make_float2(w.z, w.w));
+            xo[k] = add2(a0, xo[k]);
+          }
+          // Rounded to the storage type in place; xo then holds the rounded values.
+          sts_pairs_round<T, NE>(op + ch * NE * e, xo);
+#pragma unroll
+          for (int k = 0; k < NE / 2; ++k) sum2 = add2(sum2, xo[k]);
         }
-        sts_elems<T, NE>(op + ch * NE * e, sv);
-      }
-    }
-    const float mean = warp_sum(sum) * invD;
-    __syncwarp();
-    const T* srow = reinterpret_cast<const T*>(orow);
-    float ss = 0.f;
-    for (int vi = lane; vi < nv; vi += 32) {
-      float v[V];
-      load_vec(srow + vi * V, v);
+      } else {
+        const float2* gb = gb0 + il * C;
+        for (int ch = 0; ch < nch; ++ch) {
+          float xs[NE], xo[NE], sv[NE];
+          lds_elems<T, NE>(sp + ch * NE * e, xs);
+          lds_elems<T, NE>(op + ch * NE * e, xo);
 #pragma unroll
-      for (int q = 0; q < V; ++q) {
-        const float c = v[q] - mean;
-        ss = fmaf(c, c, ss);
+          for (int q = 0; q < NE; ++q) {
+            const float2 w = gb[ch * NE + q];
+            const float a0 = fmaf((xs[q] - sj.x) * sj.y, w.x, w.y);
+            sv[q] = to_f(from_f<T>(a0 + xo[q]));
+            sum2.x += sv[q];
+          }
+          sts_elems<T, NE>(op + ch * NE * e, sv);
+        }
       }
     }
-    const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + a.eps);
+    const float mean = warp_sum(sum2.x + sum2.y) * invD;
+    const float2 nm = f2(-mean);
+    __syncwarp();
+    float2 q2 = f2(0.f);
+    for (int vi = lane; vi < nv; vi += 32) {
+      float2 v[P];
+      ld16p<T>(orow + (size_t)vi * 16, v);
+#pragma unroll
+      for (int k = 0; k < P; ++k) {
+        const float2 c = add2(v[k], nm);
+        q2 = fma2(c, c, q2);
+      }
+    }
+    const float rstd = 1.0f / sqrtf(warp_sum(q2.x + q2.y) * invD + a.eps);
+    const float2 r2 = f2(rstd);
     const size_t r = (size_t)b * Tn + i;
     if (lane == 0) {
       a.mu1[r] = mean;
       a.r1[r] = rstd;
     }
-    const T* gm1 = reinterpret_cast<const T*>(a.gamma1);
-    const T* bt1 = reinterpret_cast<const T*>(a.beta1);
-    T* s1row = reinterpret_cast<T*>(a.s1) + r * D;
-    T* orow_out = reinterpret_cast<T*>(a.out1) + r * D;
+    unsigned char* s1row = reinterpret_cast<unsigned char*>(reinterpret_cast<T*>(a.s1) + r * D);
+    unsigned char* orow_out = reinterpret_cast<unsigned char*>(reinterpret_cast<T*>(a.out1) + r * D);
+    const unsigned char* gm1 = reinterpret_cast<const unsigned char*>(a.gamma1);
+    const unsigned char* bt1 = reinterpret_cast<const unsigned char*>(a.beta1);
     for (int vi = lane; vi < nv; vi += 32) {
-      const int d0 = vi * V;
-      const uint4 raw = *reinterpret_cast<const uint4*>(srow + d0);
-      *reinterpret_cast<uint4*>(s1row + d0) = raw;
-      float v[V], gg[V], bb[V], o[V];
-      const T* el = reinterpret_cast<const T*>(&raw);
+      const uint4 raw = *reinterpret_cast<const uint4*>(orow + (size_t)vi * 16);
+      *reinterpret_cast<uint4*>(s1row + (size_t)vi * 16) = raw;
+      float2 v[P], gg[P], bb[P], o[P];
+      ld16p<T>(&raw, v);
+      ld16p<T>(gm1 + (size_t)vi * 16, gg);
+      ld16p<T>(bt1 + (size_t)vi * 16, bb);
 #pragma unroll
-      for (int q = 0; q < V; ++q) v[q] = to_f(el[q]);
-      load_vec(gm1 + d0, gg);
-      load_vec(bt1 + d0, bb);
-#pragma unroll
-      for (int q = 0; q < V; ++q) o[q] = fmaf((v[q] - mean) * rstd, gg[q], bb[q]);
-      store_vec(orow_out + d0, o);
+      for (int k = 0; k < P; ++k) o[k] = fma2(mul2(add2(v[k], nm), r2), gg[k], bb[k]);
+      st16p<T>(orow_out + (size_t)vi * 16, o);
     }
   }
 }
