@@ -101,26 +101,16 @@ __device__ __forceinline__ float warp_sum16_transposed(const float (&v)[16]) {
   return w;
 }
 
-// Two elements of da0 from the stripe: one access at p0 when PAIRS (C even,
-// so a pair never straddles a piece and sits on a 2-element boundary), else
-// one at p0 and one at p1.
+// Two elements of da0 from the stripe as a float pair: one access at p0
+// when PAIRS (C even, so a pair never straddles a piece and sits on a
+// 2-element boundary), else one at p0 and one at p1.
 template <typename T, bool PAIRS>
-__device__ __forceinline__ void lds_gather2(const unsigned char* p0, const unsigned char* p1, float* v) {
+__device__ __forceinline__ float2 lds_gather2(const unsigned char* p0, const unsigned char* p1) {
   if (PAIRS) {
-    if constexpr (sizeof(T) == 2) {
-      const uint32_t r = *reinterpret_cast<const uint32_t*>(p0);
-      const T* e = reinterpret_cast<const T*>(&r);
-      v[0] = to_f(e[0]);
-      v[1] = to_f(e[1]);
-    } else {
-      const float2 r = *reinterpret_cast<const float2*>(p0);
-      v[0] = r.x;
-      v[1] = r.y;
-    }
-  } else {
-    v[0] = to_f(*reinterpret_cast<const T*>(p0));
-    v[1] = to_f(*reinterpret_cast<const T*>(p1));
+    if constexpr (sizeof(T) == 2) return unpack2w<T>(*reinterpret_cast<const uint32_t*>(p0));
+    else return *reinterpret_cast<const float2*>(p0);
   }
+  return make_float2(to_f(*reinterpret_cast<const T*>(p0)), to_f(*reinterpret_cast<const T*>(p1)));
 }
 
 // Shared memory: stripe [T][pitch] | own ds1 rows [8][D] | own x rows [8][D]
@@ -195,17 +185,26 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
     issue_own(bbeg);
   }
 
-  // Stripe byte offsets of the thread's columns (row 0 of the eight).
-  int soff[E];
-  float gam[E], pg[E], pb[E];
+  // Stripe byte offsets of the thread's columns (row 0 of the eight).  The
+  // element math runs on column pairs with the packed fp32x2 instructions
+  // (each rounds as the scalar one).
+  constexpr int P = E / 2;
+  constexpr int NOFF = PAIRS ? P : E;  // a pair's second element follows its first when C is even
+  int soff[NOFF];
+  float2 gam[P], pg[P], pb[P];
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int d = min(c0 + e, D - 1);
+  for (int e = 0; e < NOFF; ++e) {
+    const int d = min(c0 + (PAIRS ? 2 * e : e), D - 1);
     const int i = d / C;
     soff[e] = i * geo.stripe_pitch + (d - i * C) * es;
-    pg[e] = pb[e] = 0.f;
   }
-  if (active) load_vec(reinterpret_cast<const T*>(a.gamma) + c0, gam);
+  auto gather = [&](const unsigned char* sp, int k) {
+    return PAIRS ? lds_gather2<T, true>(sp + soff[k], nullptr)
+                 : lds_gather2<T, false>(sp + soff[2 * k], sp + soff[(2 * k + 1) % NOFF]);
+  };
+#pragma unroll
+  for (int k = 0; k < P; ++k) pg[k] = pb[k] = f2(0.f);
+  if (active) ld16p<T>(reinterpret_cast<const T*>(a.gamma) + c0, gam);
 
   const float invD = 1.0f / (float)D;
   const size_t piece_row = (size_t)C * es;  // stripe bytes between consecutive own rows
@@ -223,29 +222,25 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
 #pragma unroll
     for (int jl = 0; jl < kRowsPerCta; ++jl) {
       const float2 rc = rowst[(si & 1) * kRowsPerCta + jl];
-      const float r = rc.x, cst = rc.y;
-      float s0 = 0.f, s1 = 0.f;
+      const float2 r = f2(rc.x), cst = f2(rc.y);
+      float2 s0 = f2(0.f), s1 = f2(0.f);
       if (ok && active) {
-        float xv[E];
-        load_vec(reinterpret_cast<const T*>(ownx + (size_t)jl * geo.row_bytes) + c0, xv);
+        float2 xv[P];
+        ld16p<T>(reinterpret_cast<const T*>(ownx + (size_t)jl * geo.row_bytes) + c0, xv);
         const unsigned char* sp = stripe + (size_t)jl * piece_row;
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          float da[2];
-          lds_gather2<T, PAIRS>(sp + soff[e], sp + soff[e + 1], da);
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const float xh = fmaf(xv[e + k], r, cst);
-            const float gg = gam[e + k] * da[k];
-            s0 += gg;
-            s1 = fmaf(gg, xh, s1);
-            pg[e + k] = fmaf(da[k], xh, pg[e + k]);
-            pb[e + k] += da[k];
-          }
+        for (int k = 0; k < P; ++k) {
+          const float2 da = gather(sp, k);
+          const float2 xh = fma2(xv[k], r, cst);
+          const float2 gg = mul2(gam[k], da);
+          s0 = add2(s0, gg);
+          s1 = fma2(gg, xh, s1);
+          pg[k] = fma2(da, xh, pg[k]);
+          pb[k] = add2(pb[k], da);
         }
       }
-      sums[2 * jl] = s0;
-      sums[2 * jl + 1] = s1;
+      sums[2 * jl] = s0.x + s0.y;
+      sums[2 * jl + 1] = s1.x + s1.y;
     }
     {
       const float k = warp_sum16_transposed(sums);
@@ -270,19 +265,17 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
         const float2 rc = rowst[(si & 1) * kRowsPerCta + jl];
         const float r = rc.x, cst = rc.y;
         const float mg = means[2 * jl], mgx = means[2 * jl + 1];
-        const float A = -r * r * mgx, Bc = -r * mg - r * mgx * cst;
-        float xv[E], dv[E], o[E];
-        load_vec(reinterpret_cast<const T*>(ownx + (size_t)jl * geo.row_bytes) + c0, xv);
-        load_vec(reinterpret_cast<const T*>(ownd + (size_t)jl * geo.row_bytes) + c0, dv);
+        const float2 A = f2(-r * r * mgx), Bc = f2(-r * mg - r * mgx * cst), r2 = f2(r);
+        float2 xv[P], dv[P], o[P];
+        ld16p<T>(reinterpret_cast<const T*>(ownx + (size_t)jl * geo.row_bytes) + c0, xv);
+        ld16p<T>(reinterpret_cast<const T*>(ownd + (size_t)jl * geo.row_bytes) + c0, dv);
         const unsigned char* sp = stripe + (size_t)jl * piece_row;
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          float da[2];
-          lds_gather2<T, PAIRS>(sp + soff[e], sp + soff[e + 1], da);
-          o[e] = fmaf(r, gam[e] * da[0], fmaf(A, xv[e], Bc)) + dv[e];
-          o[e + 1] = fmaf(r, gam[e + 1] * da[1], fmaf(A, xv[e + 1], Bc)) + dv[e + 1];
+        for (int k = 0; k < P; ++k) {
+          const float2 da = gather(sp, k);
+          o[k] = add2(fma2(r2, mul2(gam[k], da), fma2(A, xv[k], Bc)), dv[k]);
         }
-        store_vec(reinterpret_cast<T*>(a.dx) + row * D + c0, o);
+        st16p<T>(reinterpret_cast<T*>(a.dx) + row * D + c0, o);
       }
     }
     // The next sample's statistics go to the other parity slot: its last
@@ -311,9 +304,9 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
   if (active) {
     const size_t p = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
 #pragma unroll
-    for (int k = 0; k < E; k += 4) {
-      *reinterpret_cast<float4*>(a.pg + p * D + c0 + k) = make_float4(pg[k], pg[k + 1], pg[k + 2], pg[k + 3]);
-      *reinterpret_cast<float4*>(a.pb + p * D + c0 + k) = make_float4(pb[k], pb[k + 1], pb[k + 2], pb[k + 3]);
+    for (int k = 0; k < P; k += 2) {
+      *reinterpret_cast<float4*>(a.pg + p * D + c0 + 2 * k) = make_float4(pg[k].x, pg[k].y, pg[k + 1].x, pg[k + 1].y);
+      *reinterpret_cast<float4*>(a.pb + p * D + c0 + 2 * k) = make_float4(pb[k].x, pb[k].y, pb[k + 1].x, pb[k + 1].y);
     }
   }
 }

@@ -168,13 +168,16 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
     const float rstd = a.rs[r];
     st_row[i] = make_float2(rstd, -a.mu[r] * rstd);
   }
-  float gam[E];
-  if (active) load_vec(reinterpret_cast<const T*>(a.gamma) + c0, gam);
+  // The element math runs on column pairs with the packed fp32x2
+  // instructions (each rounds as the scalar one).
+  constexpr int P = E / 2;
+  float2 gam[P];
+  if (active) ld16p<T>(reinterpret_cast<const T*>(a.gamma) + c0, gam);
   __syncthreads();
 
-  float ag[E], ab[E], ao[E];
+  float2 ag[P], ab[P], ao[P];
 #pragma unroll
-  for (int e = 0; e < E; ++e) ag[e] = ab[e] = ao[e] = 0.f;
+  for (int k = 0; k < P; ++k) ag[k] = ab[k] = ao[k] = f2(0.f);
 
   const float invD = 1.0f / (float)a.Dl;
   const bool tail = c0 + E > a.Dl;  // this thread owns padding columns
@@ -193,8 +196,8 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
     if (nr == 2)
       ok = ok && mbar_wait_bounded(smem_u32(&full[s1]), ph1, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
                                    (volatile int*)&abort_flag);
-    float g[2][E], xh[2][E], rv[2][E];
-    float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 g[2][P], xh[2][P], rv[2][P];
+    float2 rs2[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
     float rstd[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -202,21 +205,23 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
       rstd[r] = sr.x;
       if (ok && active && r < nr) {
         const T* st = reinterpret_cast<const T*>(ring + (size_t)(r == 0 ? s : s1) * row_bytes);
-        float gv[E], sv[E];
-        load_vec(st + c0, gv);
-        load_vec(st + D + c0, sv);
-        if (MODE == LNB_RESID) load_vec(st + 2 * D + c0, rv[r]);
+        float2 gv[P], sv[P];
+        ld16p<T>(st + c0, gv);
+        ld16p<T>(st + D + c0, sv);
+        if (MODE == LNB_RESID) ld16p<T>(st + 2 * D + c0, rv[r]);
+        const float2 sa = f2(sr.x), sb = f2(sr.y);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          xh[r][e] = fmaf(sv[e], sr.x, sr.y);
-          g[r][e] = gam[e] * gv[e];
-          rsum[2 * r] += g[r][e];
-          rsum[2 * r + 1] = fmaf(g[r][e], xh[r][e], rsum[2 * r + 1]);
-          ag[e] = fmaf(gv[e], xh[r][e], ag[e]);
-          ab[e] += gv[e];
+        for (int k = 0; k < P; ++k) {
+          xh[r][k] = fma2(sv[k], sa, sb);
+          g[r][k] = mul2(gam[k], gv[k]);
+          rs2[2 * r] = add2(rs2[2 * r], g[r][k]);
+          rs2[2 * r + 1] = fma2(g[r][k], xh[r][k], rs2[2 * r + 1]);
+          ag[k] = fma2(gv[k], xh[r][k], ag[k]);
+          ab[k] = add2(ab[k], gv[k]);
         }
       }
     }
+    const float rsum[4] = {rs2[0].x + rs2[0].y, rs2[1].x + rs2[1].y, rs2[2].x + rs2[2].y, rs2[3].x + rs2[3].y};
     float* rb = red + ((i >> 1) & 1) * 4 * 32;
     {
       const float k = warp_sum4_transposed(rsum[0], rsum[1], rsum[2], rsum[3]);
@@ -252,23 +257,25 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         if (r < nr) {
-          const float mg = m[2 * r], mgx = m[2 * r + 1];
-          const float q0 = -rstd[r] * mg;
-          float o[E];
+          const float2 nmgx = f2(-m[2 * r + 1]), rs = f2(rstd[r]), q0 = f2(-rstd[r] * m[2 * r]);
+          float2 o[P];
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            o[e] = fmaf(rstd[r], fmaf(-mgx, xh[r][e], g[r][e]), q0);
-            if (tail && c0 + e >= a.Dl) o[e] = 0.f;
-            if (MODE == LNB_BIAS) ao[e] += o[e];
+          for (int k = 0; k < P; ++k) {
+            o[k] = fma2(rs, fma2(nmgx, xh[r][k], g[r][k]), q0);
+            if (tail) {
+              if (c0 + 2 * k >= a.Dl) o[k].x = 0.f;
+              if (c0 + 2 * k + 1 >= a.Dl) o[k].y = 0.f;
+            }
+            if (MODE == LNB_BIAS) ao[k] = add2(ao[k], o[k]);
           }
           if (MODE == LNB_MIXED_TOO)
-            store_mixed_row<T, E>(reinterpret_cast<T*>(a.out_mixed) + (size_t)(b0 + i + r) * a.T * D, o, t, c0,
-                                  a.C, D, a.Dl);
+            store_mixed_row<T, E>(reinterpret_cast<T*>(a.out_mixed) + (size_t)(b0 + i + r) * a.T * D,
+                                  reinterpret_cast<const float*>(o), t, c0, a.C, D, a.Dl);
           if (MODE == LNB_RESID) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] += rv[r][e];
+            for (int k = 0; k < P; ++k) o[k] = add2(o[k], rv[r][k]);
           }
-          store_vec(out_row + r * row_step + c0, o);
+          st16p<T>(out_row + r * row_step + c0, o);
         }
       }
     }
@@ -292,9 +299,9 @@ __global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
       for (int k = 0; k < E; k += 4)
         *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
     };
-    put(a.pg + p * D + c0, ag);
-    put(a.pb + p * D + c0, ab);
-    if (MODE == LNB_BIAS) put(a.pbias + p * D + c0, ao);
+    put(a.pg + p * D + c0, reinterpret_cast<const float*>(ag));
+    put(a.pb + p * D + c0, reinterpret_cast<const float*>(ab));
+    if (MODE == LNB_BIAS) put(a.pbias + p * D + c0, reinterpret_cast<const float*>(ao));
   }
 }
 
