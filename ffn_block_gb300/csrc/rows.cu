@@ -348,7 +348,11 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
 // columns (two passes over registers, exact), writes the statistics and
 // hidden = LN_x(U) * silu(LN_gate(G)).  The GEMM that produces Z then needs
 // no statistics epilogue.  Every lane's loads are issued before the first
-// use, so a warp has its whole row (10 KB at H = 2560) in flight.
+// use, so a warp has its whole row (10 KB at H = 2560) in flight.  The grid
+// is persistent (two CTAs per SM, the warps striding over the rows); each
+// CTA first stages the four LayerNorm weight vectors in shared memory as
+// fp32, a float4 {w, w', b, b'} per column pair laid out [LN][pair k of the
+// vector][vector], so that the lanes of a warp read consecutive 16 bytes.
 // =========================================================================
 constexpr int kGateRowVecs = 10;
 
@@ -361,11 +365,18 @@ __global__ void __launch_bounds__(256, 2) k_gate_fwd_rows(const T* __restrict__ 
                                                           int H, float eps, int Hl) {
   pdl_enter();
   constexpr int V = 8;  // 16-bit: eight columns per 16-byte vector
+  extern __shared__ float4 wsm[];  // [2][4][nv]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (r >= N) return;
-  const T* zr = Z + (size_t)r * 2 * H;
   const int nv = H / V;
+  for (int idx = threadIdx.x; idx < 4 * nv; idx += blockDim.x) {
+    const int k = idx / nv, vi = idx - k * nv, c = vi * V + 2 * k;
+    wsm[k * nv + vi] = make_float4(to_f(wx[c]), to_f(wx[c + 1]), to_f(bx[c]), to_f(bx[c + 1]));
+    wsm[(4 + k) * nv + vi] = make_float4(to_f(wg[c]), to_f(wg[c + 1]), to_f(bg[c]), to_f(bg[c + 1]));
+  }
+  __syncthreads();
+  const bool padded = Hl != H;
+  for (int r = blockIdx.x * (blockDim.x >> 5) + warp; r < N; r += gridDim.x * (blockDim.x >> 5)) {
+  const T* zr = Z + (size_t)r * 2 * H;
   uint4 u[kGateRowVecs], g[kGateRowVecs];
 #pragma unroll
   for (int q = 0; q < kGateRowVecs; ++q) {
@@ -406,9 +417,11 @@ __global__ void __launch_bounds__(256, 2) k_gate_fwd_rows(const T* __restrict__ 
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float2 du = add2(a[k], nmU), dg = add2(b[k], nmG);
-        const int c = vi * V + 2 * k;
-        if (c >= Hl) du.x = dg.x = 0.f;
-        if (c + 1 >= Hl) du.y = dg.y = 0.f;
+        if (padded) {
+          const int c = vi * V + 2 * k;
+          if (c >= Hl) du.x = dg.x = 0.f;
+          if (c + 1 >= Hl) du.y = dg.y = 0.f;
+        }
         qu = fma2(du, du, qu);
         qg = fma2(dg, dg, qg);
       }
@@ -429,21 +442,19 @@ __global__ void __launch_bounds__(256, 2) k_gate_fwd_rows(const T* __restrict__ 
     const int vi = lane + 32 * q;
     if (vi < nv) {
       const int h0 = vi * V;
-      float2 a[4], b[4], w0[4], w1[4], w2[4], w3[4], o[4];
+      float2 a[4], b[4], o[4];
       pairs(u[q], a);
       pairs(g[q], b);
-      ld8<T>(wx + h0, w0);
-      ld8<T>(bx + h0, w1);
-      ld8<T>(wg + h0, w2);
-      ld8<T>(bg + h0, w3);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 uu = fma2(fma2(a[k], sU2, cU2), w0[k], w1[k]);
-        const float2 gg = fma2(fma2(b[k], sG2, cG2), w2[k], w3[k]);
+        const float4 wu = wsm[k * nv + vi], wgt = wsm[(4 + k) * nv + vi];
+        const float2 uu = fma2(fma2(a[k], sU2, cU2), make_float2(wu.x, wu.y), make_float2(wu.z, wu.w));
+        const float2 gg = fma2(fma2(b[k], sG2, cG2), make_float2(wgt.x, wgt.y), make_float2(wgt.z, wgt.w));
         o[k] = mul2(uu, mul2(gg, sigmoid_fast2(gg)));
       }
       st8<T>(hr + h0, o);
     }
+  }
   }
 }
 
@@ -646,11 +657,14 @@ cudaError_t launch_gate_fwd_rows(const RowArgs& a, const void* Z, float* muU, fl
                                  cudaStream_t st) {
   if (!gate_fwd_rows_supported(a)) return cudaErrorInvalidValue;
   const int N = a.B * a.T;
+  if (N == 0) return cudaSuccess;
+  const size_t smem = (size_t)a.H * 4 * sizeof(float);  // 8 * (H / 8) float4
+  const int ctas = (N + 7) / 8 < 2 * sm_count() ? (N + 7) / 8 : 2 * sm_count();
   if (a.dtype == 1)
-    return launch_k(k_gate_fwd_rows<bf16>, dim3((N + 7) / 8), dim3(256), 0, st, 1, (const bf16*)Z, muU, rU, muG, rG,
+    return launch_k(k_gate_fwd_rows<bf16>, dim3(ctas), dim3(256), smem, st, 1, (const bf16*)Z, muU, rU, muG, rG,
                     (const bf16*)wx, (const bf16*)bx, (const bf16*)wg, (const bf16*)bg, (bf16*)hidden, N, a.H,
                     1e-5f, a.Hl);
-  return launch_k(k_gate_fwd_rows<f16>, dim3((N + 7) / 8), dim3(256), 0, st, 1, (const f16*)Z, muU, rU, muG, rG,
+  return launch_k(k_gate_fwd_rows<f16>, dim3(ctas), dim3(256), smem, st, 1, (const f16*)Z, muU, rU, muG, rG,
                   (const f16*)wx, (const f16*)bx, (const f16*)wg, (const f16*)bg, (f16*)hidden, N, a.H, 1e-5f,
                   a.Hl);
 }
