@@ -81,7 +81,11 @@ __device__ __forceinline__ void store_mixed(T* sample_base, const float* v, int 
 //   LNF_MIXED_OUT  y = LN(s), written token-mixed  (norm0: a0 -> mix)
 //   LNF_SUM_IN     y = LN(s + s_add)               (norm1: mix + x)
 // Saves the row mean and 1/sqrt(var + eps).  Rows of pitch D hold Dl real
-// columns followed by zeros; the statistics cover the real columns.
+// columns followed by zeros; the statistics cover the real columns.  The
+// grid is persistent (the warps stride over the rows); each CTA first stages
+// gamma and beta in shared memory as fp32, a float4 {g, g', b, b'} per column
+// pair laid out [pair k of the vector][vector].  The arithmetic runs on
+// column pairs with the packed fp32x2 instructions.
 // =========================================================================
 template <typename T, int MODE, int MAXV>
 __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T* __restrict__ s_add,
@@ -91,82 +95,99 @@ __global__ void __launch_bounds__(256) k_ln_fwd(const T* __restrict__ s, const T
                                                 int Dl) {
   pdl_enter();
   constexpr int V = VecN<T>::value;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= N) return;
+  constexpr int P = V / 2;
+  extern __shared__ float4 gsm[];  // [P][nv]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   const int nv = D / V;
-  const T* srow = s + (size_t)row * D;
-  // The row stays in registers: packed as loaded when it is one tensor, as
-  // fp32 when it is the sum of two.
-  constexpr bool SUM = MODE == LNF_SUM_IN;
-  uint4 raw[SUM ? 1 : MAXV];
-  float vf[SUM ? MAXV : 1][V];
-  auto get = [&](int q, float* v) {
-    if (SUM) {
-#pragma unroll
-      for (int e = 0; e < V; ++e) v[e] = vf[q][e];
-    } else {
-      const T* el = reinterpret_cast<const T*>(&raw[q]);
-#pragma unroll
-      for (int e = 0; e < V; ++e) v[e] = to_f(el[e]);
-    }
-  };
-  float sum = 0.f;
-#pragma unroll
-  for (int q = 0; q < MAXV; ++q) {
-    const int vi = lane + 32 * q;
-    if (vi < nv) {
-      if (SUM) {
-        float a[V];
-        load_vec(srow + vi * V, vf[q]);
-        load_vec(s_add + (size_t)row * D + vi * V, a);
-#pragma unroll
-        for (int e = 0; e < V; ++e) vf[q][e] = to_f(from_f<T>(vf[q][e] + a[e]));
-      } else {
-        raw[q] = *reinterpret_cast<const uint4*>(srow + vi * V);
-      }
-      float v[V];
-      get(q, v);
-#pragma unroll
-      for (int e = 0; e < V; ++e) sum += v[e];
-    }
+  for (int idx = threadIdx.x; idx < P * nv; idx += blockDim.x) {
+    const int k = idx / nv, vi = idx - k * nv, c = vi * V + 2 * k;
+    gsm[k * nv + vi] = make_float4(to_f(g[c]), to_f(g[c + 1]), to_f(be[c]), to_f(be[c + 1]));
   }
+  __syncthreads();
+  const bool padded = Dl != D;
   const float invD = 1.0f / (float)Dl;
-  const float mean = warp_sum(sum) * invD;
-  float ss = 0.f;
+  // The row stays in registers: packed as loaded when it is one tensor, as
+  // fp32 pairs when it is the sum of two.
+  constexpr bool SUM = MODE == LNF_SUM_IN;
+  for (int row = blockIdx.x * wpb + warp; row < N; row += gridDim.x * wpb) {
+    const T* srow = s + (size_t)row * D;
+    uint4 raw[SUM ? 1 : MAXV];
+    float2 vf[SUM ? MAXV : 1][P];
+    auto get = [&](int q, float2* v) {
+      if (SUM) {
 #pragma unroll
-  for (int q = 0; q < MAXV; ++q) {
-    const int vi = lane + 32 * q;
-    if (vi < nv) {
-      float v[V];
-      get(q, v);
+        for (int k = 0; k < P; ++k) v[k] = vf[q][k];
+      } else {
+        ld16p<T>(&raw[q], v);
+      }
+    };
+    float2 sum2 = f2(0.f);
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float c = vi * V + e < Dl ? v[e] - mean : 0.f;
-        ss += c * c;
+    for (int q = 0; q < MAXV; ++q) {
+      const int vi = lane + 32 * q;
+      if (vi < nv) {
+        if (SUM) {
+          float2 a[P];
+          ld16p<T>(srow + vi * V, vf[q]);
+          ld16p<T>(s_add + (size_t)row * D + vi * V, a);
+#pragma unroll
+          for (int k = 0; k < P; ++k) {
+            vf[q][k] = add2(vf[q][k], a[k]);
+            if constexpr (sizeof(T) == 2) vf[q][k] = unpack2w<T>(pack2w<T>(vf[q][k]));  // the stored s1
+          }
+        } else {
+          raw[q] = *reinterpret_cast<const uint4*>(srow + vi * V);
+        }
+        float2 v[P];
+        get(q, v);
+#pragma unroll
+        for (int k = 0; k < P; ++k) sum2 = add2(sum2, v[k]);
       }
     }
-  }
-  const float rstd = 1.0f / sqrtf(warp_sum(ss) * invD + eps);
-  const int b = row / Tn, j = row - b * Tn;
+    const float mean = warp_sum(sum2.x + sum2.y) * invD;
+    const float2 nm = f2(-mean);
+    float2 q2 = f2(0.f);
 #pragma unroll
-  for (int q = 0; q < MAXV; ++q) {
-    const int vi = lane + 32 * q;
-    if (vi < nv) {
-      float v[V], gg[V], bb[V], o[V];
-      get(q, v);
-      load_vec(g + vi * V, gg);
-      load_vec(be + vi * V, bb);
+    for (int q = 0; q < MAXV; ++q) {
+      const int vi = lane + 32 * q;
+      if (vi < nv) {
+        float2 v[P];
+        get(q, v);
 #pragma unroll
-      for (int e = 0; e < V; ++e) o[e] = (v[e] - mean) * rstd * gg[e] + bb[e];
-      if (MODE == LNF_MIXED_OUT) store_mixed<T, V>(y + (size_t)b * Tn * D, o, j, vi * V, C, D, Dl);
-      else store_vec(y + (size_t)row * D + vi * V, o);
-      if (SUM) store_vec(s_out + (size_t)row * D + vi * V, v);
+        for (int k = 0; k < P; ++k) {
+          float2 c = add2(v[k], nm);
+          if (padded) {
+            if (vi * V + 2 * k >= Dl) c.x = 0.f;
+            if (vi * V + 2 * k + 1 >= Dl) c.y = 0.f;
+          }
+          q2 = fma2(c, c, q2);
+        }
+      }
     }
-  }
-  if (lane == 0) {
-    mu[row] = mean;
-    rs[row] = rstd;
+    const float rstd = 1.0f / sqrtf(warp_sum(q2.x + q2.y) * invD + eps);
+    const float2 r2 = f2(rstd);
+    const int b = row / Tn, j = row - b * Tn;
+#pragma unroll
+    for (int q = 0; q < MAXV; ++q) {
+      const int vi = lane + 32 * q;
+      if (vi < nv) {
+        float2 v[P], o[P];
+        get(q, v);
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+          const float4 w = gsm[k * nv + vi];
+          o[k] = fma2(mul2(add2(v[k], nm), r2), make_float2(w.x, w.y), make_float2(w.z, w.w));
+        }
+        if (MODE == LNF_MIXED_OUT)
+          store_mixed<T, V>(y + (size_t)b * Tn * D, reinterpret_cast<const float*>(o), j, vi * V, C, D, Dl);
+        else st16p<T>(y + (size_t)row * D + vi * V, o);
+        if (SUM) st16p<T>(s_out + (size_t)row * D + vi * V, v);
+      }
+    }
+    if (lane == 0) {
+      mu[row] = mean;
+      rs[row] = rstd;
+    }
   }
 }
 
@@ -611,14 +632,19 @@ int max_dynamic_smem_bytes() {
 cudaError_t launch_ln_fwd(const RowArgs& a, int mode, const void* s, const void* s_add, const void* g,
                           const void* be, void* y, float* mu, float* rs, void* s_out, cudaStream_t st) {
   const int N = a.B * a.T;
+  if (N == 0) return cudaSuccess;
   const int nv = a.D / vec_elems(a.dtype);
   const int q = (nv + 31) / 32;
-  const int grid = (N + 7) / 8;
+  const size_t smem = (size_t)a.D / 2 * sizeof(float4);  // a float4 per column pair
+  // Persistent grid: as many 8-row CTAs as fit at once (registers bound it
+  // near four per SM; the staged parameters take at most 40 KB).
+  const int fit = 4 * sm_count();
+  const int grid = (N + 7) / 8 < fit ? (N + 7) / 8 : fit;
   const int C = a.Dl / a.T;
   cudaError_t err = cudaSuccess;
 #define RMX_LNF(M, MAXV)                                                                                    \
   RMX_DISPATCH_T(a.dtype, {                                                                                 \
-    err = launch_k(k_ln_fwd<T, M, MAXV>, dim3(grid), dim3(256), 0, st, 1, (const T*)s, (const T*)s_add,     \
+    err = launch_k(k_ln_fwd<T, M, MAXV>, dim3(grid), dim3(256), smem, st, 1, (const T*)s, (const T*)s_add,  \
                    (const T*)g, (const T*)be, (T*)y, mu, rs, (T*)s_out, N, a.T, a.D, C, 1e-3f, a.Dl);       \
   })
 #define RMX_LNF_Q(M)                          \
