@@ -32,6 +32,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "pairs.cuh"
 #include "kernels.h"
 #include "launch.cuh"
 

@@ -22,6 +22,7 @@
 // bounded.
 
 #include "common.cuh"
+#include "pairs.cuh"
 #include "kernels.h"
 #include "launch.cuh"
 

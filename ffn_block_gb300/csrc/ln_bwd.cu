@@ -23,6 +23,7 @@
 #include <tuple>
 
 #include "common.cuh"
+#include "pairs.cuh"
 #include "kernels.h"
 #include "launch.cuh"
 

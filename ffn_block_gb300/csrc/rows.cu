@@ -14,6 +14,7 @@
 // bitwise repeatable.
 
 #include "common.cuh"
+#include "pairs.cuh"
 #include "kernels.h"
 #include "launch.cuh"
 
