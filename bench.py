@@ -18,6 +18,7 @@ processed / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -444,6 +445,10 @@ def run_ours(args) -> dict | None:
             timed_step()
         torch.cuda.synchronize()
     launches0 = B.rmx_launch_count()
+    # No garbage-collection pause of the Python host loop inside the timed
+    # steps (with the launch queue full, the host paces the device).
+    gc.collect()
+    gc.disable()
     barrier(ws)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -455,6 +460,7 @@ def run_ours(args) -> dict | None:
         ends[i].record(stream)
         torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
+    gc.enable()
     barrier(ws)
     wall = time.perf_counter() - wall0
     launches = B.rmx_launch_count() - launches0
@@ -501,6 +507,8 @@ def run_ours(args) -> dict | None:
         torch.cuda.synchronize()
         es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        gc.collect()
+        gc.disable()
         barrier(ws)
         for i in range(args.steps):
             flush.zero_()
@@ -508,6 +516,7 @@ def run_ours(args) -> dict | None:
             host_step()
             ee[i].record(stream)
         torch.cuda.synchronize()
+        gc.enable()
         B.check(B.rmx_check(stream), "e2e")
         e_samples = [a.elapsed_time(b) for a, b in zip(es, ee)]
         e_ms = reduce_max(float(np.mean(e_samples)), ws)
