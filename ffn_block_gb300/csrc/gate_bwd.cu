@@ -14,13 +14,14 @@
 // j holds columns 8j ... 8j + 7 of both halves.  The dh and Z rows stream
 // into shared memory through an S-stage ring of bulk copies (one thread
 // issues them; a byte-counting mbarrier per stage says when a row has
-// landed).  A row at a time (two when the LayerNorm weights live in shared
-// memory) the CTA takes its four row sums with one barrier, then every
-// thread finishes its own columns from registers, writes dZ and keeps the
-// column partial sums in registers.  The element math runs
-// on column pairs with the packed fp32x2 instructions (the same roundings as
-// scalar fp32, half the instructions).  dh and Z are read from HBM once;
-// every wait is bounded.
+// landed).  A row at a time the CTA takes its four row sums with one
+// barrier, then every thread finishes its own columns and writes dZ.  Each
+// thread's LayerNorm weights and its 48 column partial sums live in tensor
+// memory (TMEM, otherwise unused here), not in registers, which lets two
+// CTAs share an SM; the element math runs on column pairs with the packed
+// fp32x2 instructions (the same roundings as scalar fp32, half the
+// instructions).  dh and Z are read from HBM once; every wait is bounded,
+// and the TMEM columns are freed on every exit.
 
 #include <map>
 #include <mutex>
@@ -84,28 +85,59 @@ struct GateBwdArgs {
   unsigned int* err;
   int B, T, H, nb, stages;
   int Hl;                // real columns of each half of pitch H (the rest are zero padding)
+  int tmem_cols;         // k_gate_bwd_tm: TMEM columns the CTA allocates
 };
 
-// Shared memory: stats [nb] float4 | red [2][16][8] float | weights [4][H]
-// float (only when they do not stay in registers) | stages x (dh row | Z
-// row) | mbarriers.  Thread `tid` owns the eight columns c0 = 8 * tid ...
-// c0 + 7 of both halves (one 16-byte vector of a 16-bit type, two of
-// float), as four pairs for the packed fp32x2 arithmetic.
-// WREG: the thread's weights stay in registers (one CTA per SM leaves room
-// for them when the CTA has at most 320 threads).  Register caps: each of
-// the SM's four schedulers holds its warps' registers in its own quarter of
-// the register file (16384), so a CTA of 10 warps (3 on some scheduler) may
-// use at most 168 per thread, one of up to 16 warps at most 128.
+// Thread `tid` owns the eight columns c0 = 8 * tid ... c0 + 7 of both
+// halves (one 16-byte vector of a 16-bit type, two of float), as four pairs
+// for the packed fp32x2 arithmetic.
 constexpr int kGateE = 8;             // columns per thread and half
 constexpr int kGateMaxThreads = 480;  // H up to 3840 (k = 3 at D = 1280)
 constexpr int kGateRedWarps = 16;     // reduction buffer rows (at least kGateMaxThreads / 32)
 
-template <typename T, bool WREG, int R>
-__global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
+// ---------------------------------------------------------------- the pass
+// Each thread owns 80 TMEM columns of its own lane (the warps of one lane
+// quarter side by side): its weights as fp32 ([wx | wg] then [bx | bg], 16
+// columns each) and its 48 partials ([dwx | dbx], [dwg | dbg], [db1 of U |
+// of G]), all for its eight column pairs.  Per row it loads the weights, adds
+// the row's terms to the partials with 16-column loads and stores, and takes
+// one barrier for the row sums.  Measured against the same pass with the
+// weights and partials in registers (one CTA per SM): 0.382 against 0.434 ms
+// at c3, 0.389 against 0.479 ms at c4.
+__device__ __forceinline__ void tm_ld16(uint32_t taddr, float2 (&v)[8]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+}
+__device__ __forceinline__ void tm_st16(uint32_t taddr, const float2 (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0].x)), "r"(__float_as_uint(v[0].y)), "r"(__float_as_uint(v[1].x)),
+        "r"(__float_as_uint(v[1].y)), "r"(__float_as_uint(v[2].x)), "r"(__float_as_uint(v[2].y)),
+        "r"(__float_as_uint(v[3].x)), "r"(__float_as_uint(v[3].y)), "r"(__float_as_uint(v[4].x)),
+        "r"(__float_as_uint(v[4].y)), "r"(__float_as_uint(v[5].x)), "r"(__float_as_uint(v[5].y)),
+        "r"(__float_as_uint(v[6].x)), "r"(__float_as_uint(v[6].y)), "r"(__float_as_uint(v[7].x)),
+        "r"(__float_as_uint(v[7].y))
+      : "memory");
+}
+__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tm_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tm_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+template <typename T>
+__global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
   pdl_enter();
-  static_assert(R == 1 || R == 2, "rows per barrier");
-  constexpr int NS = 4 * R;        // row sums per barrier
-  constexpr int LPS = 32 / NS;     // lanes holding one sum after the warp reduction
+  constexpr int NS = 4;         // row sums per barrier
+  constexpr int LPS = 32 / NS;  // lanes holding one sum after the warp reduction
   extern __shared__ __align__(16) unsigned char smem[];
   const int H = a.H, S = a.stages;
   const int bblk = blockIdx.x, t = blockIdx.y;
@@ -118,11 +150,11 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
 
   float4* st_row = reinterpret_cast<float4*>(smem);                  // (rU, -mU*rU, rG, -mG*rG) per row
   float* red = reinterpret_cast<float*>(smem + (size_t)a.nb * 16);   // [2][16 warps][NS]
-  float* wsm = red + 2 * kGateRedWarps * NS;                         // [4][H] (not WREG)
-  unsigned char* ring = reinterpret_cast<unsigned char*>(wsm + (WREG ? 0 : 4 * (size_t)H));
+  unsigned char* ring = reinterpret_cast<unsigned char*>(red + 2 * kGateRedWarps * NS);
   const size_t row_bytes = (size_t)3 * H * sizeof(T);
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)S * row_bytes);
   __shared__ int abort_flag;
+  __shared__ uint32_t tmem_slot;
 
   const T* dh = reinterpret_cast<const T*>(a.dh);
   const T* Z = reinterpret_cast<const T*>(a.Z);
@@ -135,39 +167,62 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
     bulk_g2s(smem_u32(dst + (size_t)H * sizeof(T)), Z + r * 2 * H, (uint32_t)(2 * H * sizeof(T)), bar);
   };
 
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
     fence_mbar_init();
   }
+  tm_fence_before();
   __syncthreads();
+  tm_fence_after();
+  const uint32_t tbase = tmem_slot;
+  // Lane quarter warp % 4 (the lanes a warp may access); the warps of one
+  // quarter take 80 columns each: weights at tw, partials at tp.
+  const uint32_t tw = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 80);
+  const uint32_t tp = tw + 32;
   if (tid == 0)
     for (int i = 0; i < min(S, nrows); ++i) issue(i, i);
-  // Per-row statistics and the weights while the first rows are in flight.
   for (int i = tid; i < nrows; i += nthreads) {
     const size_t r = (size_t)(b0 + i) * a.T + t;
     const float sU = a.rU[r], sG = a.rG[r];
     st_row[i] = make_float4(sU, -a.muU[r] * sU, sG, -a.muG[r] * sG);
   }
-  const T* wp[4] = {reinterpret_cast<const T*>(a.wx), reinterpret_cast<const T*>(a.bx),
-                    reinterpret_cast<const T*>(a.wg), reinterpret_cast<const T*>(a.bg)};
-  float2 rw[WREG ? 4 : 1][4];
-  if (WREG) {
+  {
+    float2 w[8], z[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = z[k] = f2(0.f);
     if (active) {
+      float2 v[4];
+      ld8<T>(reinterpret_cast<const T*>(a.wx) + c0, v);
 #pragma unroll
-      for (int k = 0; k < (WREG ? 4 : 1); ++k) ld8<T>(wp[k] + c0, rw[k]);
+      for (int q = 0; q < 4; ++q) w[q] = v[q];
+      ld8<T>(reinterpret_cast<const T*>(a.wg) + c0, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[4 + q] = v[q];
     }
-  } else {
+    tm_st16(tw, w);  // [wx | wg]
+    if (active) {
+      float2 v[4];
+      ld8<T>(reinterpret_cast<const T*>(a.bx) + c0, v);
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      for (int c = tid; c < H; c += nthreads) wsm[k * H + c] = to_f(wp[k][c]);
+      for (int q = 0; q < 4; ++q) w[q] = v[q];
+      ld8<T>(reinterpret_cast<const T*>(a.bg) + c0, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[4 + q] = v[q];
+    }
+    tm_st16(tw + 16, w);  // [bx | bg]
+    tm_st16(tp, z);
+    tm_st16(tp + 16, z);
+    tm_st16(tp + 32, z);
+    tm_wait_st();
   }
   __syncthreads();
-
-  // Column partial sums of dwx, dbx, dwg, dbg and db1 (U and G halves).
-  float2 awx[4], abx[4], awg[4], abg[4], a1u[4], a1g[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) awx[k] = abx[k] = awg[k] = abg[k] = a1u[k] = a1g[k] = f2(0.f);
 
   const float invH = 1.0f / (float)a.Hl;
   const bool tail = c0 + kGateE > a.Hl;  // this thread owns padding columns (written as zeros)
@@ -177,84 +232,71 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
   bool aborted = false;
   int s = 0;          // stage of row i
   uint32_t ph = 0;    // parity of that stage's current phase
-  for (int i = 0; i < nrows; i += R, dZrow += R * dZstep) {
-    const int nr = min(R, nrows - i);  // rows in this step
-    const int s1 = s + 1 == S ? 0 : s + 1;
-    const uint32_t ph1 = s + 1 == S ? ph ^ 1u : ph;
-    bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
-                                (volatile int*)&abort_flag);
-    if (nr == 2)
-      ok = ok && mbar_wait_bounded(smem_u32(&full[s1]), ph1, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
-                                   (volatile int*)&abort_flag);
-    // Pass 1: everything that needs only this element, plus the row sums;
-    // gU, Uh, gG, Gh stay in registers for pass 2.
-    float2 kgU[R][4], kUh[R][4], kgG[R][4], kGh[R][4];
-    float rsum[NS];
-    float sUr[R], sGr[R];
+  for (int i = 0; i < nrows; ++i, dZrow += dZstep) {
+    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
+                                      (volatile int*)&abort_flag);
+    const float4 sr = st_row[i];
+    // Pass 1: du, dg and the normalised halves stay in registers for pass 2.
+    float2 kdu[4], kUh[4], kdg[4], kGh[4];
+    float2 rs[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float4 sr = st_row[min(i + r, nrows - 1)];
-      sUr[r] = sr.x;
-      sGr[r] = sr.z;
-      float2 rs[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
-      if (ok && active && r < nr) {
-        const T* st = reinterpret_cast<const T*>(ring + (size_t)(r == 0 ? s : s1) * row_bytes);
-        float2 dhv[4], zu[4], zg[4], w[4][4];
-        ld8<T>(st + c0, dhv);
-        ld8<T>(st + H + c0, zu);
-        ld8<T>(st + 2 * H + c0, zg);
-        if (WREG) {
+    for (int q = 0; q < 4; ++q) kdu[q] = kUh[q] = kdg[q] = kGh[q] = f2(0.f);
+    float2 wa[8], wb[8];  // [wx | wg], [bx | bg]
+    tm_ld16(tw, wa);
+    tm_ld16(tw + 16, wb);
+    if (ok && active) {
+      const T* st = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
+      float2 dhv[4], zu[4], zg[4];
+      ld8<T>(st + c0, dhv);
+      ld8<T>(st + H + c0, zu);
+      ld8<T>(st + 2 * H + c0, zg);
+      const float2 sU = f2(sr.x), cU = f2(sr.y), sG = f2(sr.z), cG = f2(sr.w);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) w[k][q] = rw[WREG ? k : 0][q];
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float4 lo = *reinterpret_cast<const float4*>(wsm + k * H + c0);
-            const float4 hi = *reinterpret_cast<const float4*>(wsm + k * H + c0 + 4);
-            w[k][0] = make_float2(lo.x, lo.y);
-            w[k][1] = make_float2(lo.z, lo.w);
-            w[k][2] = make_float2(hi.x, hi.y);
-            w[k][3] = make_float2(hi.z, hi.w);
-          }
-        }
-        const float2 sU = f2(sr.x), cU = f2(sr.y), sG = f2(sr.z), cG = f2(sr.w);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 Uh = fma2(zu[q], sU, cU);
-          const float2 Gh = fma2(zg[q], sG, cG);
-          const float2 u = fma2(w[0][q], Uh, w[1][q]);
-          const float2 g = fma2(w[2][q], Gh, w[3][q]);
-          const float2 sg = sigmoid_fast2(g);
-          const float2 gs = mul2(g, sg);
-          const float2 du = mul2(dhv[q], gs);
-          // silu'(g) = s + g s (1 - s) = s + (gs - gs * s)
-          const float2 dsilu = add2(sg, fma2(gs, make_float2(-sg.x, -sg.y), gs));
-          const float2 dg = mul2(mul2(dhv[q], u), dsilu);
-          const float2 gU = mul2(w[0][q], du), gG = mul2(w[2][q], dg);
-          rs[0] = add2(rs[0], gU);
-          rs[1] = fma2(gU, Uh, rs[1]);
-          rs[2] = add2(rs[2], gG);
-          rs[3] = fma2(gG, Gh, rs[3]);
-          awx[q] = fma2(du, Uh, awx[q]);
-          abx[q] = add2(abx[q], du);
-          awg[q] = fma2(dg, Gh, awg[q]);
-          abg[q] = add2(abg[q], dg);
-          kgU[r][q] = gU;
-          kUh[r][q] = Uh;
-          kgG[r][q] = gG;
-          kGh[r][q] = Gh;
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float2 w0 = wa[q], w1 = wb[q], w2 = wa[4 + q], w3 = wb[4 + q];
+        const float2 Uh = fma2(zu[q], sU, cU);
+        const float2 Gh = fma2(zg[q], sG, cG);
+        const float2 u = fma2(w0, Uh, w1);
+        const float2 g = fma2(w2, Gh, w3);
+        const float2 sg = sigmoid_fast2(g);
+        const float2 gs = mul2(g, sg);
+        const float2 du = mul2(dhv[q], gs);
+        // silu'(g) = s + g s (1 - s) = s + (gs - gs * s)
+        const float2 dsilu = add2(sg, fma2(gs, make_float2(-sg.x, -sg.y), gs));
+        const float2 dg = mul2(mul2(dhv[q], u), dsilu);
+        const float2 gU = mul2(w0, du), gG = mul2(w2, dg);
+        rs[0] = add2(rs[0], gU);
+        rs[1] = fma2(gU, Uh, rs[1]);
+        rs[2] = add2(rs[2], gG);
+        rs[3] = fma2(gG, Gh, rs[3]);
+        kdu[q] = du;
+        kUh[q] = Uh;
+        kdg[q] = dg;
+        kGh[q] = Gh;
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) rsum[4 * r + k] = rs[k].x + rs[k].y;
     }
-    // Row sums over the CTA: per warp (lane LPS*c holds sum c), then over
-    // the warps in a fixed order, the same bits in every thread.  Stored
-    // warp-major, so that neither the stores nor the reads below conflict.
-    float* rb = red + ((i / R) & 1) * kGateRedWarps * NS;
     {
+      // Column partials of dwx, dbx, then dwg, dbg (inactive lanes add zeros).
+      float2 p[8];
+      tm_ld16(tp, p);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        p[q] = fma2(kdu[q], kUh[q], p[q]);
+        p[4 + q] = add2(p[4 + q], kdu[q]);
+      }
+      tm_st16(tp, p);
+      tm_ld16(tp + 16, p);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        p[q] = fma2(kdg[q], kGh[q], p[q]);
+        p[4 + q] = add2(p[4 + q], kdg[q]);
+      }
+      tm_st16(tp + 16, p);
+    }
+    // Row sums over the CTA: per warp, then over the warps in a fixed order.
+    float* rb = red + (i & 1) * kGateRedWarps * NS;
+    {
+      const float rsum[NS] = {rs[0].x + rs[0].y, rs[1].x + rs[1].y, rs[2].x + rs[2].y, rs[3].x + rs[3].y};
       const float k = warp_sum_transposed<NS>(rsum);
       if (lane % LPS == 0) rb[warp * NS + lane / LPS] = k;
     }
@@ -262,20 +304,13 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
       aborted = true;
       break;
     }
-    if (tid == 0) {
-      if (issued < nrows) issue(issued++, s);
-      if (nr == 2 && issued < nrows) issue(issued++, s1);
-    }
-    for (int r = 0; r < nr; ++r) {
-      if (++s == S) {
-        s = 0;
-        ph ^= 1u;
-      }
+    if (tid == 0 && issued < nrows) issue(issued++, s);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
     }
     float m[NS];
     {
-      // Lane l adds warps (l % LPS) + LPS*k of sum l / LPS (at most 16 warps),
-      // then the LPS lanes of each sum combine.
       const int c = lane / LPS, w0 = lane % LPS;
       float v = 0.f;
 #pragma unroll
@@ -286,34 +321,44 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
 #pragma unroll
       for (int k = 0; k < NS; ++k) m[k] = __shfl_sync(0xffffffffu, v, k * LPS) * invH;
     }
+    float2 oU[4], oG[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) oU[q] = oG[q] = f2(0.f);
+    tm_ld16(tw, wa);
     if (active) {
+      const float sU = sr.x, sG = sr.z;
+      const float2 pU = f2(-m[1]), qU = f2(-sU * m[0]);
+      const float2 pG = f2(-m[3]), qG = f2(-sG * m[2]);
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (r < nr) {
-          const float sU = sUr[r], sG = sGr[r];
-          const float2 pU = f2(-m[4 * r + 1]), qU = f2(-sU * m[4 * r]);
-          const float2 pG = f2(-m[4 * r + 3]), qG = f2(-sG * m[4 * r + 2]);
-          float2 oU[4], oG[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            oU[q] = fma2(f2(sU), fma2(pU, kUh[r][q], kgU[r][q]), qU);
-            oG[q] = fma2(f2(sG), fma2(pG, kGh[r][q], kgG[r][q]), qG);
-            if (tail) {
-              const int c = c0 + 2 * q;
-              if (c >= a.Hl) oU[q].x = oG[q].x = 0.f;
-              if (c + 1 >= a.Hl) oU[q].y = oG[q].y = 0.f;
-            }
-            a1u[q] = add2(a1u[q], oU[q]);
-            a1g[q] = add2(a1g[q], oG[q]);
-          }
-          st8<T>(dZrow + r * dZstep + c0, oU);
-          st8<T>(dZrow + r * dZstep + H + c0, oG);
+      for (int q = 0; q < 4; ++q) {
+        const float2 gU = mul2(wa[q], kdu[q]), gG = mul2(wa[4 + q], kdg[q]);
+        oU[q] = fma2(f2(sU), fma2(pU, kUh[q], gU), qU);
+        oG[q] = fma2(f2(sG), fma2(pG, kGh[q], gG), qG);
+        if (tail) {
+          const int c = c0 + 2 * q;
+          if (c >= a.Hl) oU[q].x = oG[q].x = 0.f;
+          if (c + 1 >= a.Hl) oU[q].y = oG[q].y = 0.f;
         }
       }
+      st8<T>(dZrow + c0, oU);
+      st8<T>(dZrow + H + c0, oG);
+    }
+    {
+      // db1 partials of the U and G halves.
+      float2 p[8];
+      tm_ld16(tp + 32, p);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        p[q] = add2(p[q], oU[q]);
+        p[4 + q] = add2(p[4 + q], oG[q]);
+      }
+      tm_st16(tp + 32, p);
+      tm_wait_st();
     }
   }
 
   if (aborted) {
+    tm_wait_st();
     // Wait (bounded) for the copies still in flight before the CTA's shared
     // memory goes away: the newest copy issued into each stage.
     if (tid == 0) {
@@ -323,62 +368,84 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
                           ERRBIT_WAIT_ROWS, &no_abort);
       }
     }
-    return;
+  } else {
+    float2 p0[8], p1[8], p2[8];
+    tm_ld16(tp, p0);
+    tm_ld16(tp + 16, p1);
+    tm_ld16(tp + 32, p2);
+    if (active) {
+      const size_t pr = (size_t)bblk * a.T + t;
+      auto put = [&](float* dst, const float2* v) {
+        *reinterpret_cast<float4*>(dst) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+      };
+      put(a.pwx + pr * H + c0, p0);
+      put(a.pbx + pr * H + c0, p0 + 4);
+      put(a.pwg + pr * H + c0, p1);
+      put(a.pbg + pr * H + c0, p1 + 4);
+      put(a.pb1 + pr * 2 * H + c0, p2);
+      put(a.pb1 + pr * 2 * H + H + c0, p2 + 4);
+    }
   }
-
-  if (active) {
-    const size_t p = (size_t)bblk * a.T + t;
-    auto put = [&](float* dst, const float2 (&v)[4]) {
-      *reinterpret_cast<float4*>(dst) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
-    };
-    put(a.pwx + p * H + c0, awx);
-    put(a.pbx + p * H + c0, abx);
-    put(a.pwg + p * H + c0, awg);
-    put(a.pbg + p * H + c0, abg);
-    put(a.pb1 + p * 2 * H + c0, a1u);
-    put(a.pb1 + p * 2 * H + H + c0, a1g);
+  // Every thread's tensor-memory accesses are complete: free the columns.
+  tm_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tm_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(a.tmem_cols) : "memory");
   }
 }
 
-// Rows per barrier: one with the weights in registers (measured 2% faster
-// than two at H = 2560), two when they live in shared memory.
-template <bool WREG> constexpr int gate_rows() { return WREG ? 1 : 2; }
-
-// Threads, ring stages and shared memory of a CTA of nb rows (0 if even two
-// stages do not fit).
-template <typename T, bool WREG>
-size_t gate_shape(int H, int nb, int& threads, int& stages) {
+// The tensor-memory columns a CTA of `threads` allocates (80 per warp of a
+// lane quarter, a power of two of at least 32), and the ring sized for the
+// CTAs per SM those columns allow.
+int gate_tm_cols(int threads) {
+  const int per_quarter = ((threads / 32) + 3) / 4;
+  int cols = 32;
+  while (cols < 80 * per_quarter) cols *= 2;
+  return cols;
+}
+int sm_smem_bytes() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) return 0;
+  return v;
+}
+template <typename T>
+size_t gate_tm_shape(int H, int nb, int& threads, int& stages) {
   threads = (H / kGateE + 31) / 32 * 32;
-  const size_t fixed = (size_t)nb * 16 + 2 * kGateRedWarps * 8 * 4 + (WREG ? 0 : (size_t)4 * H * 4);
+  const size_t fixed = (size_t)nb * 16 + 2 * kGateRedWarps * 4 * 4;
   const size_t row_bytes = (size_t)3 * H * sizeof(T);
-  const int cap = max_dynamic_smem_bytes() - 1024;  // static shared memory and slack
+  // As many CTAs per SM as the tensor memory holds (two, or one for rows
+  // wider than 2560), each with its reservation and static shared memory.
+  const int ctas = 512 / gate_tm_cols(threads);
+  const int cap = ctas >= 2 ? sm_smem_bytes() / 2 - 2048 : max_dynamic_smem_bytes() - 1024;
   const long long room = ((long long)cap - (long long)fixed) / (long long)(row_bytes + 8);
   if (room < 2) return 0;
   stages = (int)(room < kGateMaxStages ? room : kGateMaxStages);
   return fixed + (size_t)stages * row_bytes + (size_t)stages * 8;
 }
-
-template <typename T, bool WREG>
-int gate_ctas_per_sm(int H) {
+template <typename T>
+int gate_tm_ctas_per_sm(int H) {
   int threads = 0, stages = 0;
-  const size_t smem = gate_shape<T, WREG>(H, kGateBwdMaxRows, threads, stages);
+  const size_t smem = gate_tm_shape<T>(H, kGateBwdMaxRows, threads, stages);
   if (smem == 0) return 1;
-  auto k = k_gate_bwd<T, WREG, gate_rows<WREG>()>;
+  auto k = k_gate_bwd_tm<T>;
   int n = 0;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess || n < 1)
     return 1;
-  return n;
+  const int by_tmem = 512 / gate_tm_cols(threads);
+  return n < by_tmem ? n : by_tmem;
 }
-
-template <typename T, bool WREG>
-cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
+template <typename T>
+cudaError_t launch_tm(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
   GateBwdArgs a = base;
   int threads = 0;
-  const size_t smem = gate_shape<T, WREG>(a.H, a.nb, threads, a.stages);
+  const size_t smem = gate_tm_shape<T>(a.H, a.nb, threads, a.stages);
   if (smem == 0) return cudaErrorInvalidValue;
-  auto k = k_gate_bwd<T, WREG, gate_rows<WREG>()>;
+  a.tmem_cols = gate_tm_cols(threads);
+  auto k = k_gate_bwd_tm<T>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_k(k, grid, dim3(threads), smem, st, 1, a);
@@ -395,11 +462,9 @@ int gate_bwd_ctas_per_sm(const RowArgs& ra) {
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  const bool wreg = ra.H / kGateE <= 320;
-  int n = 1;
-  if (ra.dtype == 0) n = wreg ? gate_ctas_per_sm<float, true>(ra.H) : gate_ctas_per_sm<float, false>(ra.H);
-  else if (ra.dtype == 1) n = wreg ? gate_ctas_per_sm<bf16, true>(ra.H) : gate_ctas_per_sm<bf16, false>(ra.H);
-  else n = wreg ? gate_ctas_per_sm<f16, true>(ra.H) : gate_ctas_per_sm<f16, false>(ra.H);
+  const int n = ra.dtype == 0   ? gate_tm_ctas_per_sm<float>(ra.H)
+                : ra.dtype == 1 ? gate_tm_ctas_per_sm<bf16>(ra.H)
+                                : gate_tm_ctas_per_sm<f16>(ra.H);
   cache[key] = n;
   return n;
 }
@@ -438,12 +503,12 @@ cudaError_t launch_gate_bwd(const RowArgs& ra, const void* dh, const void* Z, co
   a.Hl = ra.Hl;
   a.nb = ra.nb;
   a.stages = 0;
+  a.tmem_cols = 0;
   if (!a.err) return cudaErrorInvalidValue;
   const dim3 grid(ra.nbblk, ra.T);
-  const bool wreg = ra.H / kGateE <= 320;
-  if (ra.dtype == 0) return wreg ? launch_typed<float, true>(a, st, grid) : launch_typed<float, false>(a, st, grid);
-  if (ra.dtype == 1) return wreg ? launch_typed<bf16, true>(a, st, grid) : launch_typed<bf16, false>(a, st, grid);
-  return wreg ? launch_typed<f16, true>(a, st, grid) : launch_typed<f16, false>(a, st, grid);
+  if (ra.dtype == 0) return launch_tm<float>(a, st, grid);
+  if (ra.dtype == 1) return launch_tm<bf16>(a, st, grid);
+  return launch_tm<f16>(a, st, grid);
 }
 
 }  // namespace rmx
