@@ -435,6 +435,7 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
   cluster_wait_acquire();
   const float invD = 1.0f / (float)D;
   const int nv = D / V;
+  float mean0 = 0.f, rstd0 = 0.f;
   if (ok) {
     const int il = warp;
     const unsigned char* row = own + (size_t)il * geo.own_pitch;
@@ -458,13 +459,13 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
       }
     }
     const float rstd = 1.0f / sqrtf(warp_sum(q2.x + q2.y) * invD + a.eps);
-    const size_t r = (size_t)b * Tn + i0 + il;
-    if (lane == 0) {
-      a.mu0[r] = mean;
-      a.r0[r] = rstd;
-    }
     if (lane < geo.cs) st_cluster_f2(smem_u32(&st0[i0 + il]), (uint32_t)lane, mean, rstd);
+    mean0 = mean;
+    rstd0 = rstd;
   }
+  // (The release orders the distributed-shared-memory stores above; the
+  // statistics' global stores come after the barrier, so that it does not
+  // wait for them.)
   cluster_arrive_release();
   cluster_wait_acquire();
   if (!ok) {
@@ -475,6 +476,11 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
       mbar_wait_bounded(smem_u32(bar), 0, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS, &no_abort);
     }
     return;
+  }
+  if (lane == 0) {
+    const size_t r = (size_t)b * Tn + i0 + warp;
+    a.mu0[r] = mean0;
+    a.r0[r] = rstd0;
   }
 
   // (2) output row i = i0 + il, one warp: lane j builds the C elements that
