@@ -198,11 +198,12 @@ Layout layout_of(const rmx_config& c) {
   const int sms = c.B > 0 ? sm_count() : 1;
   // A gate CTA also loads the four weight vectors and writes six column
   // partials of H floats (about eight rows' worth of traffic); a LayerNorm
-  // ring CTA's fixed cost is small next to its rows.
+  // ring CTA writes two or three partial rows of D floats, which the column
+  // sums read back (about four rows' worth).
   const int nb = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? gate_bwd_ctas_per_sm(L.ra) : 1), kGateBwdMaxRows, 8);
   L.ra.nb = nb;
   L.ra.nbblk = c.B > 0 ? (c.B + nb - 1) / nb : 0;
-  const int nbl = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? ln_bwd_ctas_per_sm(L.ra) : 1), kLnBwdMaxRows, 0);
+  const int nbl = rows_per_cta(c.B, c.T, sms * (c.B > 0 ? ln_bwd_ctas_per_sm(L.ra) : 1), kLnBwdMaxRows, 4);
   L.ra.nb_ln = nbl;
   L.ra.nbblk_ln = c.B > 0 ? (c.B + nbl - 1) / nbl : 0;
   const size_t P = (size_t)L.ra.nbblk * c.T;     // gate-backward partial rows
