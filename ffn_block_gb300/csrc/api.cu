@@ -87,8 +87,7 @@ struct Layout {
   size_t w1T, woutT, hT, ds2T, out1T, dZT;
   int Bp;
   // backward scratch
-  size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, colsum_scratch,
-      colsum_scratch_floats, ws_total;
+  size_t ds2, dh, dZ, dout1, ds1, da0, pg2, pb2, pbo, pwx, pbx, pwg, pbg, pb1, pg0, pb0, pg1, pbe1, ws_total;
   RowArgs ra;
 };
 
@@ -232,12 +231,6 @@ Layout layout_of(const rmx_config& c) {
   L.pb0 = o; o = up(o + P0 * D * sizeof(float));
   L.pg1 = o; o = up(o + PL * D * sizeof(float));
   L.pbe1 = o; o = up(o + PL * D * sizeof(float));
-  {
-    ColsumJob jobs[kColsumJobs];
-    colsum_jobs(L, c, nullptr, nullptr, jobs);
-    L.colsum_scratch_floats = colsums_scratch_floats(jobs, kColsumJobs);
-  }
-  L.colsum_scratch = o; o = up(o + L.colsum_scratch_floats * sizeof(float));
   L.dyp = L.dxp = 0;
   if (L.padded) {
     L.dyp = o; o = up(o + N * D * e);
@@ -683,17 +676,8 @@ rmx_status backward_impl(const rmx_config& c, const void* x, const void* dy, con
   {
     ColsumJob jobs[kColsumJobs];
     colsum_jobs(L, c, &g, ws, jobs);
-    bool fin = false;
-    {
-      Launch l("colsums", st);
-      RMX_TRY(l.done(
-          launch_colsums(jobs, kColsumJobs, sd, F(L.colsum_scratch), L.colsum_scratch_floats, st, &fin)));
-    }
-    if (fin) {
-      Launch l("colsums_final", st);
-      RMX_TRY(l.done(
-          launch_colsums_final(jobs, kColsumJobs, sd, F(L.colsum_scratch), L.colsum_scratch_floats, st)));
-    }
+    Launch l("colsums", st);
+    RMX_TRY(l.done(launch_colsums(jobs, kColsumJobs, sd, st)));
   }
   return RMX_OK;
 }

@@ -100,18 +100,9 @@ struct ColsumJob {
   void* out;
   int P, J;
 };
-// With scratch of at least colsums_scratch_floats(jobs) floats (and every J a
-// multiple of 4), jobs longer than 256 partial rows are summed in chunks of
-// 256 rows in parallel (launch_colsums sets *needs_final) and
-// launch_colsums_final, called with the same arguments, adds the chunks;
-// otherwise launch_colsums sums every column in one pass.  Both orders are
-// fixed.
+// One launch; the summation order is fixed (the same bits on every call).
 constexpr int kMaxColsumJobs = 12;
-size_t colsums_scratch_floats(const ColsumJob* jobs, int njobs);
-cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
-                           cudaStream_t st, bool* needs_final);
-cudaError_t launch_colsums_final(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
-                                 cudaStream_t st);
+cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStream_t st);
 
 // Largest thread count a row pass may use (one thread per 16-byte vector).
 constexpr int kRowThreadsMax = 512;

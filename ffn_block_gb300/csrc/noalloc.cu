@@ -106,11 +106,6 @@ extern "C" rmx_status rmx_ln2_backward_noalloc(const rmx_config* cfg, const void
       {pb2, dbeta2, (int)P, cfg->D},
       {pbo, dbout, ra.nbblk_ln, cfg->T * cfg->D},
   };
-  // The part of the array the partials leave free holds the chunk sums.
-  float* rest = pbo + (size_t)ra.nbblk_ln * cfg->T * cfg->D;
-  const size_t rest_floats = kNoAllocScratchFloats - (size_t)(rest - scratch);
-  bool fin = false;
-  if (launch_colsums(jobs, 3, cfg->dtype, rest, rest_floats, st, &fin) != cudaSuccess) return RMX_ERR_CUDA;
-  if (fin && launch_colsums_final(jobs, 3, cfg->dtype, rest, rest_floats, st) != cudaSuccess) return RMX_ERR_CUDA;
+  if (launch_colsums(jobs, 3, cfg->dtype, st) != cudaSuccess) return RMX_ERR_CUDA;
   return RMX_OK;
 }

@@ -483,29 +483,26 @@ __global__ void __launch_bounds__(256, 2) k_gate_fwd_rows(const T* __restrict__ 
 // =========================================================================
 // R: column sums of partials, several jobs per launch, fixed summation order.
 //
-// Chunked form (when the caller provides scratch): a block of 256 threads
-// takes 128 columns (a float4 per lane) of one chunk of at most 256 partial
-// rows; warp w sums rows w, w+8, ... of the chunk with four loads in flight,
-// and the eight warps are combined in order.  A job with one chunk is written
-// out at once; for longer jobs each chunk's sums go to scratch and a second
-// small launch adds the chunks in order.  One-pass form (no scratch): block
-// (32, 16), x the column, y a stripe of rows p = y, y+16, ..., stripes
-// combined in order.
+// Cluster form (every J a multiple of 4): one launch of clusters of
+// kColsumCluster CTAs of 256 threads, each cluster within one job.  A job of
+// more than kColsumWideRows partial rows takes one cluster per 128 columns (a
+// float4 per lane): CTA r sums rows [r*cr, r*cr + cr), cr = ceil(P / 8),
+// warp w rows w, w+8, ... of them with four loads in flight, the eight warps
+// combined in order; the CTAs' sums go to CTA 0 of the cluster through
+// distributed shared memory, which adds them in rank order and writes the
+// result.  A job of few rows (per-token bias gradients summed over a few
+// sample blocks) is summed wide: each warp takes 128 columns of all rows.
+// One-pass form (some J not a multiple of 4): block (32, 16), x the column,
+// y a stripe of rows p = y, y+16, ..., stripes combined in order.
 // =========================================================================
-constexpr int kColsumChunkRows = 256;
-constexpr int kColsumCols = 128;  // columns per block (32 lanes x float4)
-// Jobs of at most this many partial rows (per-token bias gradients summed
-// over a few sample blocks) are summed "wide": each warp takes 128 columns
-// of all rows, eight warps 1024 columns per block, so that a job of many
-// columns and few rows is not spread over thousands of nearly idle blocks.
+constexpr int kColsumCluster = 8;
+constexpr int kColsumCols = 128;  // columns per cluster or per warp (32 lanes x float4)
 constexpr int kColsumWideRows = 32;
 
 struct ColsumArgs {
   ColsumJob job[kMaxColsumJobs];
-  float* chunk_out[kMaxColsumJobs];  // [nchunks][J] when nchunks > 1
-  int nchunks[kMaxColsumJobs];
   int ncg[kMaxColsumJobs];           // column groups of kColsumCols
-  int wide[kMaxColsumJobs];          // 1: summed wide (see kColsumWideRows)
+  int wide[kMaxColsumJobs];          // 1: summed wide
   int block_start[kMaxColsumJobs + 1];
   int njobs;
 };
@@ -529,18 +526,59 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
+__device__ __forceinline__ void cs_cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cs_cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cs_cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cs_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Stores v at the shared address `addr` (this CTA's view) of CTA `rank` of the cluster.
+__device__ __forceinline__ void cs_st_cluster_f4(uint32_t addr, uint32_t rank, float4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
+// Sum of rows p, p + 8, ... below p1 of the four columns at col (J floats
+// per row), four loads in flight.
+__device__ __forceinline__ float4 colsum_rows(const float* col, size_t J, int p, int p1) {
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (; p + 24 < p1; p += 32) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = add4(acc[k], *reinterpret_cast<const float4*>(col + (size_t)(p + 8 * k) * J));
+  }
+#pragma unroll
+  for (int k = 0; k < 3; ++k)
+    if (p + 8 * k < p1) acc[k] = add4(acc[k], *reinterpret_cast<const float4*>(col + (size_t)(p + 8 * k) * J));
+  return add4(add4(acc[0], acc[1]), add4(acc[2], acc[3]));
+}
+
 template <typename T>
-__global__ void __launch_bounds__(256) k_colsums_chunks(const ColsumArgs a) {
+__global__ void __launch_bounds__(256) k_colsums_cluster(const ColsumArgs a) {
   pdl_enter();
   __shared__ float4 part[8][32];
+  __shared__ float4 chunk[kColsumCluster][32];
   const int jb = colsum_job_of(a);
   const ColsumJob& job = a.job[jb];
-  if (a.wide[jb]) {  // block-uniform
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int j = ((blockIdx.x - a.block_start[jb]) * 8 + warp) * kColsumCols + lane * 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int local = (int)blockIdx.x - a.block_start[jb];
+  const size_t J = (size_t)job.J;
+  if (a.wide[jb]) {  // the whole cluster: no exchange
+    const int j = (local * 8 + warp) * kColsumCols + lane * 4;
     if (j >= job.J) return;
     const float* col = job.part + j;
-    const size_t J = (size_t)job.J;
     float4 acc[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -553,51 +591,31 @@ __global__ void __launch_bounds__(256) k_colsums_chunks(const ColsumArgs a) {
     store4<T>(job.out, j, add4(add4(acc[0], acc[1]), add4(acc[2], acc[3])));
     return;
   }
-  const int local = blockIdx.x - a.block_start[jb];
-  const int ch = local / a.ncg[jb], cg = local - ch * a.ncg[jb];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // CTA 0's shared memory is written only once every CTA of the cluster is
+  // known to be running: arrive now, wait before the first remote store.
+  cs_cluster_arrive_relaxed();
+  const uint32_t r = cs_cluster_rank();
+  const int cg = local / kColsumCluster;
   const int j = cg * kColsumCols + lane * 4;
-  const int p0 = ch * kColsumChunkRows, p1 = min(job.P, p0 + kColsumChunkRows);
-  float4 acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (j < job.J) {
-    const float* col = job.part + j;
-    const size_t J = (size_t)job.J;
-    int p = p0 + warp;
-    for (; p + 24 < p1; p += 32) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] = add4(acc[k], *reinterpret_cast<const float4*>(col + (size_t)(p + 8 * k) * J));
-    }
-#pragma unroll
-    for (int k = 0; k < 3; ++k)
-      if (p + 8 * k < p1) acc[k] = add4(acc[k], *reinterpret_cast<const float4*>(col + (size_t)(p + 8 * k) * J));
-  }
-  part[warp][lane] = add4(add4(acc[0], acc[1]), add4(acc[2], acc[3]));
+  const int cr = (job.P + kColsumCluster - 1) / kColsumCluster;
+  const int p0 = (int)r * cr, p1 = min(job.P, p0 + cr);
+  part[warp][lane] = j < job.J ? colsum_rows(job.part + j, J, p0 + warp, p1) : make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
-  if (warp == 0 && j < job.J) {
+  cs_cluster_wait_acquire();
+  if (warp == 0) {
     float4 tot = part[0][lane];
 #pragma unroll
     for (int w = 1; w < 8; ++w) tot = add4(tot, part[w][lane]);
-    if (a.nchunks[jb] == 1)
-      store4<T>(job.out, j, tot);
-    else
-      *reinterpret_cast<float4*>(a.chunk_out[jb] + (size_t)ch * job.J + j) = tot;
+    cs_st_cluster_f4(smem_u32(&chunk[r][lane]), 0u, tot);
   }
-}
-
-// Adds the chunk sums of the jobs with more than one chunk, in chunk order.
-template <typename T>
-__global__ void __launch_bounds__(128) k_colsums_final(const ColsumArgs a) {
-  pdl_enter();
-  const int jb = colsum_job_of(a);
-  const ColsumJob& job = a.job[jb];
-  const int j = ((int)blockIdx.x - a.block_start[jb]) * 512 + threadIdx.x * 4;
-  if (j >= job.J) return;
-  float4 tot = *reinterpret_cast<const float4*>(a.chunk_out[jb] + j);
-  for (int ch = 1; ch < a.nchunks[jb]; ++ch)
-    tot = add4(tot, *reinterpret_cast<const float4*>(a.chunk_out[jb] + (size_t)ch * job.J + j));
-  store4<T>(job.out, j, tot);
+  cs_cluster_arrive_release();
+  cs_cluster_wait_acquire();
+  if (r == 0 && warp == 0 && j < job.J) {
+    float4 tot = chunk[0][lane];
+#pragma unroll
+    for (int k = 1; k < kColsumCluster; ++k) tot = add4(tot, chunk[k][lane]);
+    store4<T>(job.out, j, tot);
+  }
 }
 
 template <typename T>
@@ -708,74 +726,46 @@ cudaError_t launch_gate_fwd(const RowArgs& a, const void* Z, const float* zstats
   return err;
 }
 
-size_t colsums_scratch_floats(const ColsumJob* jobs, int njobs) {
-  size_t n = 0;
-  for (int i = 0; i < njobs; ++i) {
-    const int nch = (jobs[i].P + kColsumChunkRows - 1) / kColsumChunkRows;
-    if (nch > 1) n += (size_t)nch * jobs[i].J;
-  }
-  return n;
-}
-
 namespace {
 // Fills the launch arguments; returns false for the one-pass form.
-bool colsum_plan(const ColsumJob* jobs, int njobs, float* scratch, size_t scratch_floats, ColsumArgs& a) {
+bool colsum_plan(const ColsumJob* jobs, int njobs, ColsumArgs& a) {
   a.njobs = njobs;
-  bool chunked = scratch != nullptr && colsums_scratch_floats(jobs, njobs) <= scratch_floats;
-  for (int i = 0; i < njobs; ++i) chunked = chunked && jobs[i].J % 4 == 0 && jobs[i].P > 0;
+  bool cluster = true;
+  for (int i = 0; i < njobs; ++i) cluster = cluster && jobs[i].J % 4 == 0 && jobs[i].P > 0;
   int blocks = 0;
-  float* next = scratch;
   for (int i = 0; i < njobs; ++i) {
     a.job[i] = jobs[i];
     a.ncg[i] = (jobs[i].J + kColsumCols - 1) / kColsumCols;
-    a.nchunks[i] = chunked ? (jobs[i].P + kColsumChunkRows - 1) / kColsumChunkRows : 1;
-    a.wide[i] = chunked && jobs[i].P <= kColsumWideRows ? 1 : 0;
-    a.chunk_out[i] = nullptr;
-    if (a.nchunks[i] > 1) {
-      a.chunk_out[i] = next;
-      next += (size_t)a.nchunks[i] * jobs[i].J;
-    }
+    a.wide[i] = cluster && jobs[i].P <= kColsumWideRows ? 1 : 0;
     a.block_start[i] = blocks;
-    blocks += !chunked ? (jobs[i].J + 31) / 32 : a.wide[i] ? (a.ncg[i] + 7) / 8 : a.ncg[i] * a.nchunks[i];
+    if (!cluster) {
+      blocks += (jobs[i].J + 31) / 32;
+    } else if (a.wide[i]) {
+      const int nb = (a.ncg[i] + 7) / 8;  // eight warps of 128 columns per CTA
+      blocks += (nb + kColsumCluster - 1) / kColsumCluster * kColsumCluster;
+    } else {
+      blocks += a.ncg[i] * kColsumCluster;
+    }
   }
   a.block_start[njobs] = blocks;
-  return chunked;
+  return cluster;
 }
 }  // namespace
 
-cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
-                           cudaStream_t st, bool* needs_final) {
-  if (needs_final) *needs_final = false;
+cudaError_t launch_colsums(const ColsumJob* jobs, int njobs, int dtype, cudaStream_t st) {
   if (njobs <= 0 || njobs > kMaxColsumJobs) return cudaErrorInvalidValue;
   ColsumArgs a;
-  const bool chunked = colsum_plan(jobs, njobs, scratch, scratch_floats, a);
+  const bool cluster = colsum_plan(jobs, njobs, a);
   const int blocks = a.block_start[njobs];
   if (blocks == 0) return cudaSuccess;
   cudaError_t err = cudaSuccess;
-  if (!chunked) {
+  if (!cluster) {
     RMX_DISPATCH_T(dtype, { err = launch_k(k_colsums_onepass<T>, dim3(blocks), dim3(32, 16), 0, st, 1, a); });
     return err;
   }
-  RMX_DISPATCH_T(dtype, { err = launch_k(k_colsums_chunks<T>, dim3(blocks), dim3(256), 0, st, 1, a); });
-  if (needs_final)
-    for (int i = 0; i < njobs; ++i) *needs_final = *needs_final || a.nchunks[i] > 1;
-  return err;
-}
-
-cudaError_t launch_colsums_final(const ColsumJob* jobs, int njobs, int dtype, float* scratch, size_t scratch_floats,
-                                 cudaStream_t st) {
-  if (njobs <= 0 || njobs > kMaxColsumJobs) return cudaErrorInvalidValue;
-  ColsumArgs a;
-  if (!colsum_plan(jobs, njobs, scratch, scratch_floats, a)) return cudaErrorInvalidValue;
-  int fb = 0;
-  for (int i = 0; i < njobs; ++i) {
-    a.block_start[i] = fb;
-    if (a.nchunks[i] > 1) fb += (jobs[i].J + 511) / 512;
-  }
-  a.block_start[njobs] = fb;
-  if (fb == 0) return cudaErrorInvalidValue;
-  cudaError_t err = cudaSuccess;
-  RMX_DISPATCH_T(dtype, { err = launch_k(k_colsums_final<T>, dim3(fb), dim3(128), 0, st, 1, a); });
+  RMX_DISPATCH_T(dtype, {
+    err = launch_k(k_colsums_cluster<T>, dim3(blocks), dim3(256), 0, st, kColsumCluster, a);
+  });
   return err;
 }
 
