@@ -755,8 +755,9 @@ cudaError_t launch_typed(const GateBwdArgs& base, cudaStream_t st, dim3 grid) {
 // with T = 64, D = 1280, and at H = 1536, where it holds two CTAs per SM).
 // The runtime's occupancy query reports one CTA per SM for the TMEM form
 // although the SM holds two (the profiler's occupancy limits and its
-// achieved warps per SM both show two); the grid is sized from the query's
-// figure, which is the sizing measured.
+// achieved warps per SM both show two).  The grid is sized for the two that
+// run from 192 rows per SM up, for the query's one below (measured: two
+// faster at B = 512 and 1024 with T = 64, one faster at B = 256).
 struct GateForm {
   bool tm;
   int ctas;
@@ -787,7 +788,10 @@ GateForm gate_form(const RowArgs& ra) {
   }
   if (wide) return {true, n.first};
   const long long rows_per_sm = (long long)ra.B * ra.T / (sm_count() > 0 ? sm_count() : 1);
-  if (n.second < 2 && rows_per_sm >= 96) return {true, n.first};
+  if (n.second < 2 && rows_per_sm >= 96) {
+    const int resident = 512 / gate_tm_cols((ra.H / kGateE + 31) / 32 * 32);
+    return {true, rows_per_sm >= 192 && resident > n.first ? resident : n.first};
+  }
   return {false, n.second};
 }
 
