@@ -121,9 +121,11 @@ template <int MODE> struct LnRows {
 
 // Shared memory: stats [nb] float2 | red [2][4][32] float | stages x rows |
 // mbarriers.  Two rows are taken per barrier: their four row sums are reduced
-// together, which halves the per-row reduction and barrier work.
+// together, which halves the per-row reduction and barrier work.  At most 96
+// registers a thread (128 where the token-mixed copy is written too), so
+// that four CTAs of 160 threads share an SM.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(512) k_ln_bwd_ring(const LnBwdArgs a) {
+__global__ void __maxnreg__(MODE == LNB_MIXED_TOO ? 128 : 96) k_ln_bwd_ring(const LnBwdArgs a) {
   pdl_enter();
   constexpr int E = VecN<T>::value;
   constexpr int NR = LnRows<MODE>::value;
