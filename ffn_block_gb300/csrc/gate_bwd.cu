@@ -490,15 +490,20 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
     const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
                                       (volatile int*)&abort_flag);
     const float4 sr = st_row[i];
-    // Pass 1: du, dg and the normalised halves stay in registers for pass 2.
+    // Pass 1: du, dg and the normalised halves stay in registers for pass 2
+    // (zeros for a lane with no columns or a row that never landed, assigned
+    // on that path only, so that the common path carries no zeroing).
     float2 kdu[4], kUh[4], kdg[4], kGh[4];
-    float2 rs[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) kdu[q] = kUh[q] = kdg[q] = kGh[q] = f2(0.f);
+    float2 rs[4];
     float2 wa[8], wb[8];  // [wx | wg], [bx | bg]
     tm_ld16(tw, wa);
     tm_ld16(tw + 16, wb);
-    if (ok && active) {
+    if (!(ok && active)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) kdu[q] = kUh[q] = kdg[q] = kGh[q] = rs[q] = f2(0.f);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) rs[q] = f2(0.f);
       const T* st = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
       float2 dhv[4], zu[4], zg[4];
       ld8<T>(st + c0, dhv);
@@ -576,10 +581,11 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
       for (int k = 0; k < NS; ++k) m[k] = __shfl_sync(0xffffffffu, v, k * LPS) * invH;
     }
     float2 oU[4], oG[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) oU[q] = oG[q] = f2(0.f);
     tm_ld16(tw, wa);
-    if (active) {
+    if (!active) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) oU[q] = oG[q] = f2(0.f);
+    } else {
       const float sU = sr.x, sG = sr.z;
       const float2 pU = f2(-m[1]), qU = f2(-sU * m[0]);
       const float2 pG = f2(-m[3]), qG = f2(-sG * m[2]);
@@ -588,7 +594,10 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
         const float2 gU = mul2(wa[q], kdu[q]), gG = mul2(wa[4 + q], kdg[q]);
         oU[q] = fma2(f2(sU), fma2(pU, kUh[q], gU), qU);
         oG[q] = fma2(f2(sG), fma2(pG, kGh[q], gG), qG);
-        if (tail) {
+      }
+      if (tail) {  // padding columns are written as zeros
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
           const int c = c0 + 2 * q;
           if (c >= a.Hl) oU[q].x = oG[q].x = 0.f;
           if (c + 1 >= a.Hl) oU[q].y = oG[q].y = 0.f;
