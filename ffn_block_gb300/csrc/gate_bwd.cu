@@ -306,11 +306,17 @@ __global__ void __maxnreg__(WREG ? 168 : 128) k_gate_bwd(const GateBwdArgs a) {
           for (int q = 0; q < 4; ++q) {
             oU[q] = fma2(f2(sU), fma2(pU, kUh[r][q], kgU[r][q]), qU);
             oG[q] = fma2(f2(sG), fma2(pG, kGh[r][q], kgG[r][q]), qG);
-            if (tail) {
+          }
+          if (tail) {  // padding columns are written as zeros
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
               const int c = c0 + 2 * q;
               if (c >= a.Hl) oU[q].x = oG[q].x = 0.f;
               if (c + 1 >= a.Hl) oU[q].y = oG[q].y = 0.f;
             }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
             a1u[q] = add2(a1u[q], oU[q]);
             a1g[q] = add2(a1g[q], oG[q]);
           }

@@ -263,13 +263,17 @@ __global__ void __maxnreg__(MODE == LNB_MIXED_TOO ? 128 : 96) k_ln_bwd_ring(cons
           const float2 nmgx = f2(-m[2 * r + 1]), rs = f2(rstd[r]), q0 = f2(-rstd[r] * m[2 * r]);
           float2 o[P];
 #pragma unroll
-          for (int k = 0; k < P; ++k) {
-            o[k] = fma2(rs, fma2(nmgx, xh[r][k], g[r][k]), q0);
-            if (tail) {
+          for (int k = 0; k < P; ++k) o[k] = fma2(rs, fma2(nmgx, xh[r][k], g[r][k]), q0);
+          if (tail) {  // padding columns are written as zeros
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
               if (c0 + 2 * k >= a.Dl) o[k].x = 0.f;
               if (c0 + 2 * k + 1 >= a.Dl) o[k].y = 0.f;
             }
-            if (MODE == LNB_BIAS) ao[k] = add2(ao[k], o[k]);
+          }
+          if (MODE == LNB_BIAS) {
+#pragma unroll
+            for (int k = 0; k < P; ++k) ao[k] = add2(ao[k], o[k]);
           }
           if (MODE == LNB_MIXED_TOO)
             store_mixed_row<T, E>(reinterpret_cast<T*>(a.out_mixed) + (size_t)(b0 + i + r) * a.T * D,
