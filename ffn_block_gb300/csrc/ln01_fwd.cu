@@ -437,28 +437,26 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
   const int nv = D / V;
   float mean0 = 0.f, rstd0 = 0.f;
   if (ok) {
+    // One pass: sums and sums of squares shifted by the row's first element
+    // (a value of the row's scale, so that the difference of the two moments
+    // loses little).
     const int il = warp;
     const unsigned char* row = own + (size_t)il * geo.own_pitch;
-    float2 s2 = f2(0.f);
-    for (int vi = lane; vi < nv; vi += 32) {
-      float2 v[P];
-      ld16p<T>(row + (size_t)vi * 16, v);
-#pragma unroll
-      for (int k = 0; k < P; ++k) s2 = add2(s2, v[k]);
-    }
-    const float mean = warp_sum(s2.x + s2.y) * invD;
-    const float2 nm = f2(-mean);
-    float2 q2 = f2(0.f);
+    const float2 nk = f2(-to_f(*reinterpret_cast<const T*>(row)));
+    float2 s2 = f2(0.f), q2 = f2(0.f);
     for (int vi = lane; vi < nv; vi += 32) {
       float2 v[P];
       ld16p<T>(row + (size_t)vi * 16, v);
 #pragma unroll
       for (int k = 0; k < P; ++k) {
-        const float2 c = add2(v[k], nm);
+        const float2 c = add2(v[k], nk);
+        s2 = add2(s2, c);
         q2 = fma2(c, c, q2);
       }
     }
-    const float rstd = 1.0f / sqrtf(warp_sum(q2.x + q2.y) * invD + a.eps);
+    const float dm = warp_sum(s2.x + s2.y) * invD;
+    const float mean = dm - nk.x;
+    const float rstd = 1.0f / sqrtf(fmaxf(warp_sum(q2.x + q2.y) * invD - dm * dm, 0.f) + a.eps);
     if (lane < geo.cs) st_cluster_f2(smem_u32(&st0[i0 + il]), (uint32_t)lane, mean, rstd);
     mean0 = mean;
     rstd0 = rstd;
@@ -493,7 +491,11 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
     const int i = i0 + il;
     unsigned char* orow = own + (size_t)il * geo.own_pitch;
     const int nch = C / NE;
-    float2 sum2 = f2(0.f);
+    // norm1's statistics in the same pass: sums and sums of squares shifted
+    // by x[i, 0] (read before lane 0 overwrites it).
+    const float2 nk1 = f2(-to_f(*reinterpret_cast<const T*>(orow)));
+    __syncwarp();
+    float2 sum2 = f2(0.f), sq2 = f2(0.f);
     for (int j = lane; j < Tn; j += 32) {
       const float2 sj = st0[j];
       const unsigned char* sp = stripe + (size_t)j * geo.stripe_pitch + (size_t)il * C * e;
@@ -514,7 +516,11 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
           // Rounded to the storage type in place; xo then holds the rounded values.
           sts_pairs_round<T, NE>(op + ch * NE * e, xo);
 #pragma unroll
-          for (int k = 0; k < NE / 2; ++k) sum2 = add2(sum2, xo[k]);
+          for (int k = 0; k < NE / 2; ++k) {
+            const float2 c = add2(xo[k], nk1);
+            sum2 = add2(sum2, c);
+            sq2 = fma2(c, c, sq2);
+          }
         }
       } else {
         const float2* gb = gb0 + il * C;
@@ -527,26 +533,19 @@ __global__ void __launch_bounds__(32 * kLn01Rows)
             const float2 w = gb[ch * NE + q];
             const float a0 = fmaf((xs[q] - sj.x) * sj.y, w.x, w.y);
             sv[q] = to_f(from_f<T>(a0 + xo[q]));
-            sum2.x += sv[q];
+            const float c = sv[q] + nk1.x;
+            sum2.x += c;
+            sq2.x = fmaf(c, c, sq2.x);
           }
           sts_elems<T, NE>(op + ch * NE * e, sv);
         }
       }
     }
-    const float mean = warp_sum(sum2.x + sum2.y) * invD;
+    const float dm = warp_sum(sum2.x + sum2.y) * invD;
+    const float mean = dm - nk1.x;
     const float2 nm = f2(-mean);
     __syncwarp();
-    float2 q2 = f2(0.f);
-    for (int vi = lane; vi < nv; vi += 32) {
-      float2 v[P];
-      ld16p<T>(orow + (size_t)vi * 16, v);
-#pragma unroll
-      for (int k = 0; k < P; ++k) {
-        const float2 c = add2(v[k], nm);
-        q2 = fma2(c, c, q2);
-      }
-    }
-    const float rstd = 1.0f / sqrtf(warp_sum(q2.x + q2.y) * invD + a.eps);
+    const float rstd = 1.0f / sqrtf(fmaxf(warp_sum(sq2.x + sq2.y) * invD - dm * dm, 0.f) + a.eps);
     const float2 r2 = f2(rstd);
     const size_t r = (size_t)b * Tn + i;
     if (lane == 0) {

@@ -366,8 +366,9 @@ __global__ void __launch_bounds__(256, 5) k_gate_fwd(const T* __restrict__ Z, co
 // F3 with the statistics taken in-pass (16-bit rows of at most
 // kGateRowVecs 16-byte vectors per half and lane, H <= 2560): one warp per
 // row holds the row's U and G halves in registers as loaded (packed), takes
-// the mean and then the centred sum of squares of each half over the Hl real
-// columns (two passes over registers, exact), writes the statistics and
+// the statistics of each half in one pass over the registers (sums and sums
+// of squares shifted by the half's first element; padded rows: the mean, then
+// the centred sum of squares over the Hl real columns), writes them and
 // hidden = LN_x(U) * silu(LN_gate(G)).  The GEMM that produces Z then needs
 // no statistics epilogue.  Every lane's loads are issued before the first
 // use, so a warp has its whole row (10 KB at H = 2560) in flight.  The grid
@@ -409,48 +410,83 @@ __global__ void __launch_bounds__(256, 2) k_gate_fwd_rows(const T* __restrict__ 
     }
   }
   auto pairs = [](const uint4& w, float2 (&p)[4]) { ld8<T>(reinterpret_cast<const T*>(&w), p); };
-  // Pass 1: sums (the padding columns hold zeros).
-  float2 su = f2(0.f), sg = f2(0.f);
+  const float inv = 1.0f / (float)Hl;
+  float mU, mG, sU, sG;
+  if (!padded) {
+    // One pass over the registers: sums and sums of squares of each half
+    // shifted by its first element (lane 0's, a value of the row's scale,
+    // so that the difference of the two moments loses little).
+    float2 a0[4], b0[4];
+    pairs(u[0], a0);
+    pairs(g[0], b0);
+    const float2 nkU = f2(-__shfl_sync(0xffffffffu, a0[0].x, 0));
+    const float2 nkG = f2(-__shfl_sync(0xffffffffu, b0[0].x, 0));
+    float2 su = f2(0.f), sg = f2(0.f), qu = f2(0.f), qg = f2(0.f);
 #pragma unroll
-  for (int q = 0; q < kGateRowVecs; ++q) {
-    if (lane + 32 * q < nv) {
-      float2 a[4], b[4];
-      pairs(u[q], a);
-      pairs(g[q], b);
+    for (int q = 0; q < kGateRowVecs; ++q) {
+      if (lane + 32 * q < nv) {
+        float2 a[4], b[4];
+        pairs(u[q], a);
+        pairs(g[q], b);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        su = add2(su, a[k]);
-        sg = add2(sg, b[k]);
+        for (int k = 0; k < 4; ++k) {
+          const float2 du = add2(a[k], nkU), dg = add2(b[k], nkG);
+          su = add2(su, du);
+          qu = fma2(du, du, qu);
+          sg = add2(sg, dg);
+          qg = fma2(dg, dg, qg);
+        }
       }
     }
-  }
-  const float inv = 1.0f / (float)Hl;
-  const float mU = warp_sum(su.x + su.y) * inv, mG = warp_sum(sg.x + sg.y) * inv;
-  // Pass 2: centred sums of squares over the real columns.
-  float2 qu = f2(0.f), qg = f2(0.f);
-  const float2 nmU = f2(-mU), nmG = f2(-mG);
+    const float dmU = warp_sum(su.x + su.y) * inv, dmG = warp_sum(sg.x + sg.y) * inv;
+    const float vU = fmaxf(warp_sum(qu.x + qu.y) * inv - dmU * dmU, 0.f);
+    const float vG = fmaxf(warp_sum(qg.x + qg.y) * inv - dmG * dmG, 0.f);
+    mU = dmU - nkU.x;
+    mG = dmG - nkG.x;
+    sU = 1.0f / sqrtf(vU + eps);
+    sG = 1.0f / sqrtf(vG + eps);
+  } else {
+    // Padded rows: the mean, then the centred sum of squares over the real
+    // columns (the padding columns hold zeros).
+    float2 su = f2(0.f), sg = f2(0.f);
 #pragma unroll
-  for (int q = 0; q < kGateRowVecs; ++q) {
-    const int vi = lane + 32 * q;
-    if (vi < nv) {
-      float2 a[4], b[4];
-      pairs(u[q], a);
-      pairs(g[q], b);
+    for (int q = 0; q < kGateRowVecs; ++q) {
+      if (lane + 32 * q < nv) {
+        float2 a[4], b[4];
+        pairs(u[q], a);
+        pairs(g[q], b);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float2 du = add2(a[k], nmU), dg = add2(b[k], nmG);
-        if (padded) {
+        for (int k = 0; k < 4; ++k) {
+          su = add2(su, a[k]);
+          sg = add2(sg, b[k]);
+        }
+      }
+    }
+    mU = warp_sum(su.x + su.y) * inv;
+    mG = warp_sum(sg.x + sg.y) * inv;
+    float2 qu = f2(0.f), qg = f2(0.f);
+    const float2 nmU = f2(-mU), nmG = f2(-mG);
+#pragma unroll
+    for (int q = 0; q < kGateRowVecs; ++q) {
+      const int vi = lane + 32 * q;
+      if (vi < nv) {
+        float2 a[4], b[4];
+        pairs(u[q], a);
+        pairs(g[q], b);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float2 du = add2(a[k], nmU), dg = add2(b[k], nmG);
           const int c = vi * V + 2 * k;
           if (c >= Hl) du.x = dg.x = 0.f;
           if (c + 1 >= Hl) du.y = dg.y = 0.f;
+          qu = fma2(du, du, qu);
+          qg = fma2(dg, dg, qg);
         }
-        qu = fma2(du, du, qu);
-        qg = fma2(dg, dg, qg);
       }
     }
+    sU = 1.0f / sqrtf(warp_sum(qu.x + qu.y) * inv + eps);
+    sG = 1.0f / sqrtf(warp_sum(qg.x + qg.y) * inv + eps);
   }
-  const float sU = 1.0f / sqrtf(warp_sum(qu.x + qu.y) * inv + eps);
-  const float sG = 1.0f / sqrtf(warp_sum(qg.x + qg.y) * inv + eps);
   if (lane == 0) {
     muU[r] = mU;
     rU[r] = sU;
