@@ -523,7 +523,10 @@ def run_ours(args) -> dict | None:
         nbytes = hx.numel() * hx.element_size()
         e2e = {"value": aggregate(rows, e_ms, ws), "unit": "rows/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
-               "samples_ms": [round(v, 4) for v in e_samples]}
+               "samples_ms": [round(v, 4) for v in e_samples],
+               # value is the mean (whole-job throughput); the median shows
+               # a step's time without the host's occasional stalls
+               "median_ms": round(float(np.median(e_samples)), 4)}
 
     if rank != 0:
         return None
