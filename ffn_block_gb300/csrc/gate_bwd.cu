@@ -377,6 +377,26 @@ __device__ __forceinline__ void tm_ld16(uint32_t taddr, float2 (&v)[8]) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) v[k] = make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
 }
+// 32 consecutive columns in one load: the first 16 into a, the next 16 into b.
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float2 (&a)[8], float2 (&b)[8]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    a[k] = make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+    b[k] = make_float2(__uint_as_float(r[16 + 2 * k]), __uint_as_float(r[16 + 2 * k + 1]));
+  }
+}
 __device__ __forceinline__ void tm_st16(uint32_t taddr, const float2 (&v)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -502,8 +522,7 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
     float2 kdu[4], kUh[4], kdg[4], kGh[4];
     float2 rs[4];
     float2 wa[8], wb[8];  // [wx | wg], [bx | bg]
-    tm_ld16(tw, wa);
-    tm_ld16(tw + 16, wb);
+    tm_ld32(tw, wa, wb);
     if (!(ok && active)) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) kdu[q] = kUh[q] = kdg[q] = kGh[q] = rs[q] = f2(0.f);
@@ -540,6 +559,24 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
         kGh[q] = Gh;
       }
     }
+    // Row sums over the CTA: per warp, then over the warps in a fixed order.
+    float* rb = red + (i & 1) * kGateRedWarps * NS;
+    {
+      const float rsum[NS] = {rs[0].x + rs[0].y, rs[1].x + rs[1].y, rs[2].x + rs[2].y, rs[3].x + rs[3].y};
+      const float k = warp_sum_transposed<NS>(rsum);
+      if (lane % LPS == 0) rb[warp * NS + lane / LPS] = k;
+    }
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    if (tid == 0 && issued < nrows) issue(issued++, s);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+    // (After the barrier: the TMEM round trips of the partial updates then
+    // overlap the other warps' arrival instead of delaying it.)
     {
       // Column partials of dwx, dbx, then dwg, dbg (inactive lanes add zeros).
       float2 p[8];
@@ -557,22 +594,6 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
         p[4 + q] = add2(p[4 + q], kdg[q]);
       }
       tm_st16(tp + 16, p);
-    }
-    // Row sums over the CTA: per warp, then over the warps in a fixed order.
-    float* rb = red + (i & 1) * kGateRedWarps * NS;
-    {
-      const float rsum[NS] = {rs[0].x + rs[0].y, rs[1].x + rs[1].y, rs[2].x + rs[2].y, rs[3].x + rs[3].y};
-      const float k = warp_sum_transposed<NS>(rsum);
-      if (lane % LPS == 0) rb[warp * NS + lane / LPS] = k;
-    }
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    if (tid == 0 && issued < nrows) issue(issued++, s);
-    if (++s == S) {
-      s = 0;
-      ph ^= 1u;
     }
     float m[NS];
     {
