@@ -579,6 +579,9 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
     // overlap the other warps' arrival instead of delaying it.)
     {
       // Column partials of dwx, dbx, then dwg, dbg (inactive lanes add zeros).
+      // The previous row's store of the db1 partials has long been issued:
+      // waiting for it here rather than at the end of that row costs little.
+      tm_wait_st();
       float2 p[8];
       tm_ld16(tp, p);
 #pragma unroll
@@ -643,7 +646,6 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
         p[4 + q] = add2(p[4 + q], oG[q]);
       }
       tm_st16(tp + 32, p);
-      tm_wait_st();
     }
   }
 
@@ -660,6 +662,7 @@ __global__ void __maxnreg__(96) k_gate_bwd_tm(const GateBwdArgs a) {
     }
   } else {
     float2 p0[8], p1[8], p2[8];
+    tm_wait_st();
     tm_ld16(tp, p0);
     tm_ld16(tp + 16, p1);
     tm_ld16(tp + 32, p2);
