@@ -218,7 +218,9 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
                                 (volatile int*)&abort_flag);
     ok = ok && mbar_wait_bounded(smem_u32(&bar[1]), ph, kWaitLimitNs, a.err, ERRBIT_WAIT_ROWS,
                                  (volatile int*)&abort_flag);
-    // Pass 1: gather da0, g = gamma0 * da0, the row sums and column partials.
+    // Pass 1: gather da0, g = gamma0 * da0 and the row sums (the column
+    // partials wait for pass 2, after the barrier, which gathers da0 again:
+    // less work before the barrier every warp waits at).
     float sums[16];
 #pragma unroll
     for (int jl = 0; jl < kRowsPerCta; ++jl) {
@@ -236,8 +238,6 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
           const float2 gg = mul2(gam[k], da);
           s0 = add2(s0, gg);
           s1 = fma2(gg, xh, s1);
-          pg[k] = fma2(da, xh, pg[k]);
-          pb[k] = add2(pb[k], da);
         }
       }
       sums[2 * jl] = s0.x + s0.y;
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
         const float2 rc = rowst[(si & 1) * kRowsPerCta + jl];
         const float r = rc.x, cst = rc.y;
         const float mg = means[2 * jl], mgx = means[2 * jl + 1];
-        const float2 A = f2(-r * r * mgx), Bc = f2(-r * mg - r * mgx * cst), r2 = f2(r);
+        const float2 A = f2(-r * r * mgx), Bc = f2(-r * mg - r * mgx * cst), r2 = f2(r), c2 = f2(cst);
         float2 xv[P], dv[P], o[P];
         ld16p<T>(reinterpret_cast<const T*>(ownx + (size_t)jl * geo.row_bytes) + c0, xv);
         ld16p<T>(reinterpret_cast<const T*>(ownd + (size_t)jl * geo.row_bytes) + c0, dv);
@@ -275,6 +275,8 @@ __global__ void __launch_bounds__(kLn0MaxThreads, 3)
         for (int k = 0; k < P; ++k) {
           const float2 da = gather(sp, k);
           o[k] = add2(fma2(r2, mul2(gam[k], da), fma2(A, xv[k], Bc)), dv[k]);
+          pg[k] = fma2(da, fma2(xv[k], r2, c2), pg[k]);
+          pb[k] = add2(pb[k], da);
         }
         st16p<T>(reinterpret_cast<T*>(a.dx) + row * D + c0, o);
       }
